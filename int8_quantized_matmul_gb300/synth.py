@@ -1,0 +1,84 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module draws random numbers and nothing else: it holds none of the
+method's arithmetic (no packing, no quantization, no matmul). Both the GPU path
+and the CPU oracle receive the arrays it returns and each packs/quantizes them
+with its own code.
+
+Distributions follow the workloads of the I2_S / I8_S pages:
+  * ternary codes {0,1,2} i.i.d. with P = (0.3, 0.4, 0.3);
+  * F32 activations ~ N(0, 1), optionally with 1% outliers scaled by 20
+    (prefill shape);
+  * int8 weights ~ round(N(0, 40)) clamped to +-127 (I8_S encoder FC);
+  * per-tensor weight scales ~ U(0.01, 0.1) for the decoder projection set.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+CODE_P = (0.3, 0.4, 0.3)
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(int(seed)))
+
+
+def codes(N: int, K: int, seed: int, p=CODE_P) -> np.ndarray:
+    """N x K ternary codes in {0,1,2} (uint8), i.i.d. with probabilities p."""
+    u = rng(seed).random((N, K), dtype=np.float32)
+    c = np.zeros((N, K), dtype=np.uint8)
+    c[u >= p[0]] = 1
+    c[u >= p[0] + p[1]] = 2
+    return c
+
+
+def packed_code_bytes(nbytes: int, seed: int, p=CODE_P) -> np.ndarray:
+    """Raw bytes whose four 2-bit fields are i.i.d. codes with probabilities p.
+
+    Because the codes are i.i.d., the byte distribution does not depend on which
+    field holds which position, so large weight payloads for the benchmark are
+    drawn directly as bytes (one draw per byte from the 81 four-code patterns).
+    """
+    pats = np.arange(81)
+    c = np.stack([(pats // 27) % 3, (pats // 9) % 3, (pats // 3) % 3, pats % 3], axis=1)
+    pp = np.asarray(p, dtype=np.float64)
+    prob = pp[c[:, 0]] * pp[c[:, 1]] * pp[c[:, 2]] * pp[c[:, 3]]
+    byte_of = (c[:, 0] << 6) | (c[:, 1] << 4) | (c[:, 2] << 2) | c[:, 3]
+    idx = rng(seed).choice(81, size=int(nbytes), p=prob / prob.sum())
+    return byte_of.astype(np.uint8)[idx]
+
+
+def normal_f32(shape, seed: int, std: float = 1.0, outlier_p: float = 0.0,
+               outlier_scale: float = 20.0) -> np.ndarray:
+    g = rng(seed)
+    x = g.standard_normal(shape, dtype=np.float32) * np.float32(std)
+    if outlier_p > 0:
+        mask = g.random(shape, dtype=np.float32) < outlier_p
+        x[mask] *= np.float32(outlier_scale)
+    return x
+
+
+def uniform_f32(shape, seed: int, lo: float, hi: float) -> np.ndarray:
+    return rng(seed).uniform(lo, hi, size=shape).astype(np.float32)
+
+
+def int8_normal(shape, seed: int, std: float = 40.0) -> np.ndarray:
+    """int8 weights drawn as round(N(0, std)) clamped to +-127."""
+    x = rng(seed).standard_normal(shape) * std
+    return np.clip(np.rint(x), -127, 127).astype(np.int8)
+
+
+# Qwen2-1.5B decoder projection shapes (out N, in K): hidden 1536, intermediate
+# 8960, 12 heads of 128 over 2 KV heads (so k/v project to 256).
+QWEN2_1P5B_LAYER = (
+    ("q", 1536, 1536),
+    ("k", 256, 1536),
+    ("v", 256, 1536),
+    ("o", 1536, 1536),
+    ("gate", 8960, 1536),
+    ("up", 8960, 1536),
+    ("down", 1536, 8960),
+)
+QWEN2_1P5B_LAYERS = 28
+QWEN2_1P5B_LM_HEAD = ("lm_head", 151936, 1536)

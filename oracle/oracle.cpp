@@ -1,0 +1,390 @@
+// Plain CPU oracle for the I2_S ternary x INT8 matmul and the I8_S fused
+// mul_mat_add(_relu).
+//
+// TEST INFRASTRUCTURE ONLY. This file is the slow, obviously-correct statement
+// of what the GPU library computes. Only the test suite, the smoke check and
+// the benchmark's CPU-baseline leg load it. It shares no code, header, table or
+// helper with the CUDA library, and the library never calls it.
+//
+// Built with plain gcc/g++ at -O2 -ffp-contract=off and no fast-math, so every
+// float operation below is one IEEE-754 binary32 operation, rounded to nearest,
+// in the order written (no fused multiply-add).
+//
+// Sources (web pages; cited by title and section):
+//   [P1] "ggml: additive INT8/ternary types, fused CPU ops, and kernels for
+//        VibeASR (1/2)" (audio.cpp pull request 447)
+//   [P2] "ggml-cpu: ternary I2_S matmul kernel (VibeASR, 3/4)" (audio.cpp pull
+//        request 445)
+//   [P3] "VibeASR in audio.cpp" (docs/models/vibeasr.md)
+//   [P4] "Experiment - int8 W8A8 path" (ork-driver wiki)
+//
+// Readings where the pages are silent (each is also listed in the design notes):
+//   R1 rounding: round to nearest, halfway cases away from zero (C roundf).
+//   R2 quantizer arithmetic: amax floored at 1e-5; scale = amax/127 (stored,
+//      a multiplier); inv = 127/amax; v = x*inv; q = clamp(round(v), -127, 127).
+//   R3 "padded" F32 scale: the payload is padded with zero bytes to a multiple
+//      of 32, then the F32 scale, then 28 zero bytes (32-byte trailer).
+//   R4 I8_S mul_mat_add: y = (float)acc * (w_scale*x_scale), then + bias[n],
+//      then ReLU (y > 0 ? y : +0), then per-tensor requantization (R2).
+//
+// Parity pins: every function here is pinned by tests that do not re-use its
+// arithmetic (hand decode, closed forms, brute force, numpy integer matmul in
+// special cases); see tests/test_oracle_pins.py.
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <stdio.h>
+
+#include <thread>
+#include <vector>
+
+#define ORC_API extern "C" __attribute__((visibility("default")))
+
+// ORC_PLANT selects one deliberate mistake for the mutation test that proves
+// the pins can fail (tests/test_oracle_mutations.py builds one library per
+// value). The shipped oracle is built with ORC_PLANT == 0: no mistake.
+#ifndef ORC_PLANT
+#define ORC_PLANT 0
+#endif
+
+// ---------------------------------------------------------------------------
+// Byte layouts ([P1] "Two new types"; [P2] "Kernels"; [P3] "Decoder")
+// ---------------------------------------------------------------------------
+
+static int64_t round_up32(int64_t n) { return (n + 31) / 32 * 32; }
+
+// I2_S: 2 bits per value, so N*K/4 payload bytes (K % 128 == 0 makes this a
+// whole number of 32-byte groups), then the 32-byte scale trailer (R3).
+ORC_API int64_t orc_i2s_nbytes(int64_t N, int64_t K) { return N * K / 4 + 32; }
+ORC_API int64_t orc_i2s_scale_offset(int64_t N, int64_t K) { return N * K / 4; }
+
+// I8_S: nelements int8 bytes, zero padded to 32, then the 32-byte trailer (R3).
+ORC_API int64_t orc_i8s_nbytes(int64_t n) { return round_up32(n) + 32; }
+ORC_API int64_t orc_i8s_scale_offset(int64_t n) { return round_up32(n); }
+
+static void put_scale(uint8_t* dst, int64_t off, float s) {
+    memcpy(dst + off, &s, 4);
+    memset(dst + off + 4, 0, 28);
+}
+
+static float get_scale(const uint8_t* src, int64_t off) {
+    float s;
+    memcpy(&s, src + off, 4);
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// I2_S packing ([P1] "Kernels", [P2] "Kernels"):
+// the flat tensor is cut into groups of 128 values, each stored in 32 bytes.
+// Byte gp of a group holds the group-relative positions gp, 32+gp, 64+gp and
+// 96+gp in its bit pairs at shifts 6, 4, 2 and 0. Codes are {0,1,2} for the
+// ternary values {-1,0,+1}.
+// ---------------------------------------------------------------------------
+
+// Packer: walks the values in flat order and drops each code into its place.
+ORC_API void orc_i2s_pack(const uint8_t* codes, int64_t N, int64_t K, float absmax,
+                          uint8_t* dst) {
+    const int64_t n_values = N * K;
+    memset(dst, 0, (size_t)(n_values / 4));
+    for (int64_t f = 0; f < n_values; ++f) {
+        const int64_t group = f / 128;
+        const int64_t pos = f % 128;            // group-relative position
+        const int64_t byte = group * 32 + pos % 32;
+#if ORC_PLANT == 2
+        const int shift = 2 * (int)(pos / 32);
+#else
+        const int shift = 6 - 2 * (int)(pos / 32);
+#endif
+        dst[byte] |= (uint8_t)((codes[f] & 3u) << shift);
+    }
+    put_scale(dst, orc_i2s_scale_offset(N, K), absmax);
+}
+
+// Unpacker, written independently of the packer: walks the bytes of each group
+// and the four bit pairs of each byte.
+ORC_API void orc_i2s_unpack(const uint8_t* src, int64_t N, int64_t K, uint8_t* codes,
+                            float* absmax) {
+    const int64_t n_groups = N * K / 128;
+    for (int64_t g = 0; g < n_groups; ++g) {
+        const uint8_t* grp = src + g * 32;
+        uint8_t* out = codes + g * 128;
+        for (int gp = 0; gp < 32; ++gp) {
+            const uint8_t b = grp[gp];
+#if ORC_PLANT == 1
+            out[gp] = b & 3;
+            out[32 + gp] = (b >> 2) & 3;
+            out[64 + gp] = (b >> 4) & 3;
+            out[96 + gp] = (b >> 6) & 3;
+#else
+            out[gp] = (b >> 6) & 3;
+            out[32 + gp] = (b >> 4) & 3;
+            out[64 + gp] = (b >> 2) & 3;
+            out[96 + gp] = b & 3;
+#endif
+        }
+    }
+    if (absmax) *absmax = get_scale(src, orc_i2s_scale_offset(N, K));
+}
+
+// Dequantizer: w = (code - 1) * absmax ([P3] "Decoder": ternary {-1,0,+1}
+// stored as codes {0,1,2} with one F32 absmax after the payload).
+ORC_API void orc_i2s_dequantize(const uint8_t* src, int64_t N, int64_t K, float* w) {
+    std::vector<uint8_t> c((size_t)(N * K));
+    float a;
+    orc_i2s_unpack(src, N, K, c.data(), &a);
+    for (int64_t i = 0; i < N * K; ++i) w[i] = (float)((int)c[i] - 1) * a;
+}
+
+// ---------------------------------------------------------------------------
+// Quantization of an F32 block to int8 with one multiplier scale
+// ([P1] "Two new types": scale = amax/127, dequantize by multiplying;
+//  [P3] "Encoder": amax floored at 1e-5;
+//  [P4] "Implementation": scale = amax/127, inv = 127/amax, q = round(x*inv)
+//  clamped to +-127). Rounding is R1.
+// ---------------------------------------------------------------------------
+
+ORC_API float orc_round(float v) { return roundf(v); }
+
+ORC_API void orc_round_array(const float* v, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = roundf(v[i]);
+}
+
+// Quantizes x[0..n) to q with scale; returns the int8 sum in *sum (may be null).
+static void quantize_block(const float* x, int64_t n, int8_t* q, float* scale, int32_t* sum) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+#if ORC_PLANT != 6
+    if (amax < 1e-5f) amax = 1e-5f;
+#endif
+#if ORC_PLANT == 4
+    const float s = 127.0f / amax;
+#else
+    const float s = amax / 127.0f;
+#endif
+    const float inv = 127.0f / amax;
+    int64_t acc = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const float v = x[i] * inv;
+#if ORC_PLANT == 5
+        float r = rintf(v);
+#else
+        float r = roundf(v);
+#endif
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        q[i] = (int8_t)(int)r;
+        acc += q[i];
+    }
+    *scale = s;
+    if (sum) *sum = (int32_t)acc;
+}
+
+// Per-row activation quantization for the I2_S matmul ([P2] "Arithmetic" and
+// "Kernels" threading paragraph; [P1] "Arithmetic is exact where it can be":
+// quantized rows, then per-row scale and per-row int8 sum as a sidecar).
+ORC_API void orc_quantize_rows(const float* x, int64_t M, int64_t K, int8_t* q,
+                               float* act_scale, int32_t* row_sum) {
+    for (int64_t m = 0; m < M; ++m)
+        quantize_block(x + m * K, K, q + m * K, &act_scale[m], &row_sum[m]);
+}
+
+// ---------------------------------------------------------------------------
+// I2_S x F32 -> F32 matmul ([P2] "Interface", "Arithmetic", "Kernels").
+// W is N x K (K contiguous, row stride K/4 bytes), X is M x K, Y is M x N.
+// Phase 1 quantizes activation rows striped over threads; the join is the
+// barrier; phase 2 splits the output features in chunks of 64 over threads and
+// sweeps the whole batch for each weight row. The result does not depend on
+// the thread count.
+//
+// dot = sum_k code*q (int32), and by the code identity
+// sum(code*q) = sum(w*q) + sum(q), the epilogue is
+//   y = (float)(dot - row_sum) * (w_scale * act_scale).
+// The oracle also forms sum(w*q) directly and aborts if the identity fails.
+// ---------------------------------------------------------------------------
+
+struct I2SJob {
+    const uint8_t* codes;
+    const int8_t* q;
+    const float* act_scale;
+    const int32_t* row_sum;
+    float w_scale;
+    int64_t M, N, K;
+    float* y;
+    int32_t* dot_out;   // optional, M x N raw sum(code*q)
+};
+
+static void i2s_features(const I2SJob* j, int tid, int nth) {
+    const int64_t chunk = 64;
+    const int64_t n_chunks = (j->N + chunk - 1) / chunk;
+    for (int64_t c = tid; c < n_chunks; c += nth) {
+        const int64_t n_lo = c * chunk;
+        const int64_t n_hi = n_lo + chunk < j->N ? n_lo + chunk : j->N;
+        for (int64_t n = n_lo; n < n_hi; ++n) {
+            const uint8_t* wrow = j->codes + n * j->K;
+            for (int64_t m = 0; m < j->M; ++m) {
+                const int8_t* qrow = j->q + m * j->K;
+                int64_t dot = 0, wq = 0;
+                for (int64_t k = 0; k < j->K; ++k) {
+                    dot += (int64_t)wrow[k] * qrow[k];
+                    wq += (int64_t)((int)wrow[k] - 1) * qrow[k];
+                }
+                if (dot != wq + j->row_sum[m] || dot > INT32_MAX || dot < INT32_MIN) {
+                    fprintf(stderr, "oracle: code identity or int32 range violated\n");
+                    abort();
+                }
+#if ORC_PLANT == 9
+                const int32_t d = (int32_t)(int16_t)dot;
+#else
+                const int32_t d = (int32_t)dot;
+#endif
+                if (j->dot_out) j->dot_out[m * j->N + n] = d;
+#if ORC_PLANT == 3
+                const float r = (float)d * (j->w_scale * j->act_scale[m]);
+#elif ORC_PLANT == 10
+                const float r = (float)(d - j->row_sum[m]) * (j->w_scale * j->act_scale[0]);
+#else
+                const float r = (float)(d - j->row_sum[m]) * (j->w_scale * j->act_scale[m]);
+#endif
+#if ORC_PLANT == 7
+                j->y[n * j->M + m] = r;
+#else
+                j->y[m * j->N + n] = r;
+#endif
+            }
+        }
+    }
+}
+
+ORC_API void orc_i2s_mul_mat(const uint8_t* w_i2s, int64_t N, int64_t K, const float* x,
+                             int64_t M, float* y, int nth, int8_t* q_out, float* scale_out,
+                             int32_t* row_sum_out, int32_t* dot_out) {
+    if (nth < 1) nth = 1;
+    std::vector<uint8_t> codes((size_t)(N * K));
+    float w_scale;
+    orc_i2s_unpack(w_i2s, N, K, codes.data(), &w_scale);
+    std::vector<int8_t> q((size_t)(M * K));
+    std::vector<float> s((size_t)M);
+    std::vector<int32_t> rs((size_t)M);
+
+    // Phase 1: rows striped across threads (a row-wide absmax cannot be split).
+    {
+        std::vector<std::thread> ts;
+        for (int t = 0; t < nth; ++t)
+            ts.emplace_back([&, t] {
+                for (int64_t m = t; m < M; m += nth)
+                    quantize_block(x + m * K, K, q.data() + m * K, &s[m], &rs[m]);
+            });
+        for (auto& th : ts) th.join();   // the barrier
+    }
+    // Phase 2: output features split over threads.
+    I2SJob job{codes.data(), q.data(), s.data(), rs.data(), w_scale, M, N, K, y, dot_out};
+    {
+        std::vector<std::thread> ts;
+        for (int t = 0; t < nth; ++t) ts.emplace_back([&, t] { i2s_features(&job, t, nth); });
+        for (auto& th : ts) th.join();
+    }
+    if (q_out) memcpy(q_out, q.data(), (size_t)(M * K));
+    if (scale_out) memcpy(scale_out, s.data(), (size_t)M * 4);
+    if (row_sum_out) memcpy(row_sum_out, rs.data(), (size_t)M * 4);
+}
+
+// ---------------------------------------------------------------------------
+// I8_S: per-tensor int8 with an in-band multiplier scale ([P1] "Two new types").
+// ---------------------------------------------------------------------------
+
+ORC_API void orc_i8s_pack(const int8_t* q, int64_t n, float scale, uint8_t* dst) {
+    const int64_t off = orc_i8s_scale_offset(n);
+    memset(dst, 0, (size_t)off);
+    memcpy(dst, q, (size_t)n);
+    put_scale(dst, off, scale);
+}
+
+ORC_API float orc_i8s_unpack(const uint8_t* src, int64_t n, int8_t* q) {
+    if (q) memcpy(q, src, (size_t)n);
+    return get_scale(src, orc_i8s_scale_offset(n));
+}
+
+ORC_API void orc_i8s_dequantize(const uint8_t* src, int64_t n, float* out) {
+    const float s = get_scale(src, orc_i8s_scale_offset(n));
+    const int8_t* q = (const int8_t*)src;
+    for (int64_t i = 0; i < n; ++i) out[i] = (float)q[i] * s;
+}
+
+// F32 -> I8_S, one scale for the whole tensor ([P1] "Five fused INT8 ops":
+// every op requantizes its output; [P3] "Encoder": whole-waveform scale, amax
+// floored at 1e-5).
+ORC_API void orc_i8s_quantize(const float* y, int64_t n, uint8_t* dst) {
+    std::vector<int8_t> q((size_t)n);
+    float s;
+    quantize_block(y, n, q.data(), &s, nullptr);
+    orc_i8s_pack(q.data(), n, s, dst);
+}
+
+// ggml_mul_mat_add / ggml_mul_mat_add_relu ([P1] "Five fused INT8 ops"):
+// I8_S W (N x K) times I8_S X (M x K) -> I8_S Y (M x N); bias added, optional
+// ReLU, output requantized in the op. Formula and order are reading R4.
+// y_f32 (optional) receives the F32 values before requantization.
+ORC_API void orc_i8s_mul_mat_add(const uint8_t* w_i8s, int64_t N, int64_t K,
+                                 const uint8_t* x_i8s, int64_t M, const float* bias,
+                                 int relu, uint8_t* y_i8s, float* y_f32, int nth) {
+    if (nth < 1) nth = 1;
+    const int8_t* w = (const int8_t*)w_i8s;
+    const int8_t* xq = (const int8_t*)x_i8s;
+    const float ws = get_scale(w_i8s, orc_i8s_scale_offset(N * K));
+    const float xs = get_scale(x_i8s, orc_i8s_scale_offset(M * K));
+    const float sc = ws * xs;
+    std::vector<float> yv((size_t)(M * N));
+    std::vector<std::thread> ts;
+    for (int t = 0; t < nth; ++t)
+        ts.emplace_back([&, t] {
+            for (int64_t n = t; n < N; n += nth) {
+                for (int64_t m = 0; m < M; ++m) {
+                    int64_t acc = 0;
+                    for (int64_t k = 0; k < K; ++k) acc += (int64_t)w[n * K + k] * xq[m * K + k];
+                    if (acc > INT32_MAX || acc < INT32_MIN) {
+                        fprintf(stderr, "oracle: int32 accumulator range violated\n");
+                        abort();
+                    }
+#if ORC_PLANT == 11
+                    float v = (float)(int32_t)acc;
+                    if (bias) v = v + bias[n];
+                    v = v * sc;
+#elif ORC_PLANT == 13
+                    float v = (float)(int32_t)acc * ws;
+                    if (bias) v = v + bias[n];
+#else
+                    float v = (float)(int32_t)acc * sc;
+                    if (bias) v = v + bias[n];
+#endif
+#if ORC_PLANT != 12
+                    if (relu) v = v > 0.0f ? v : 0.0f;
+#endif
+                    yv[m * N + n] = v;
+                }
+            }
+        });
+    for (auto& th : ts) th.join();
+    if (y_f32) memcpy(y_f32, yv.data(), (size_t)(M * N) * 4);
+    orc_i8s_quantize(yv.data(), M * N, y_i8s);
+}
+
+// ggml_cont(ggml_permute(...)) of an I8_S tensor: the values move, and the
+// in-band scale must travel with them ([P1] "Two new types", dup/cont note).
+// src is a x b (row-major); dst is b x a.
+ORC_API void orc_i8s_permute_cont(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst) {
+    const int64_t n = a * b;
+    const int8_t* s = (const int8_t*)src;
+    std::vector<int8_t> t((size_t)n);
+    for (int64_t i = 0; i < a; ++i)
+        for (int64_t j = 0; j < b; ++j) t[j * a + i] = s[i * b + j];
+#if ORC_PLANT == 8
+    orc_i8s_pack(t.data(), n, 1.0f, dst);
+#else
+    orc_i8s_pack(t.data(), n, get_scale(src, orc_i8s_scale_offset(n)), dst);
+#endif
+}
