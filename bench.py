@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the I2_S ternary x INT8 matmul hot path on GB300.
+
+Headline workload: the Qwen2-1.5B-shaped decoder projection set (per layer
+q 1536->1536, k/v 1536->256, o 1536->1536, gate/up 1536->8960, down
+8960->1536) for all 28 layers, as I2_S weights (327,548,928 bytes of 2-bit
+codes per pass, more than the 129 MB L2), decoded for M = 1 and M = 8
+activation rows. One step is one pass of the whole path for each M:
+activation quantization (one launch over the 112 distinct activations) and
+the 196-projection GEMV with its fused epilogue (one launch). The metric is
+weight GB/s: code bytes streamed per second.
+
+Also reported (outside the headline timed region): the prefill shape (M = 512
+over the same set plus the lm_head) and the I8_S encoder FC pair.
+
+--impl reference times the CPU oracle (tests' reference implementation, as it
+stands) on the host cores on a bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no cross-GPU exchange); value = all ranks' bytes / max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int8_quantized_matmul_gb300 import synth  # noqa: E402
+
+LAYERS = synth.QWEN2_1P5B_LAYERS
+PROJ = synth.QWEN2_1P5B_LAYER
+WEIGHT_BYTES_PER_PASS = LAYERS * sum(N * K // 4 for _, N, K in PROJ)   # 327,548,928
+METRIC = "I2_S decode GEMV weight GB/s (% HBM peak); Qwen2-1.5B projection set x28 layers, M=1 and M=8"
+WORKLOAD = "qwen2-1.5b decode projection set x28 layers (I2_S weights), M=1 and M=8 activation rows"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def make_weights(torch, device, seed_base=0):
+    """28 layers x 7 projections of I2_S bytes, drawn on the device."""
+    ws = []
+    for layer in range(LAYERS):
+        row = []
+        for i, (name, N, K) in enumerate(PROJ):
+            payload = synth.packed_code_bytes_device(N * K // 4, seed_base + 1000 * layer + i, device)
+            scale = synth.uniform_f32(1, seed_base + 2000 * layer + i, 0.01, 0.1)[0]
+            trailer = np.zeros(32, np.uint8)
+            trailer[:4] = np.frombuffer(np.float32(scale).tobytes(), np.uint8)
+            row.append(torch.cat([payload, torch.from_numpy(trailer).to(device)]).contiguous())
+        ws.append(row)
+    return ws
+
+
+ACT_OF = {"q": 0, "k": 0, "v": 0, "o": 1, "gate": 2, "up": 2, "down": 3}   # shared layer inputs
+ACT_K = (1536, 1536, 1536, 8960)
+
+
+class DecodePass:
+    """Device buffers and the grouped call for one M. Activations and outputs are
+    slices of one contiguous buffer each, so the end-to-end variant moves them
+    with one host->device and one device->host copy per pass."""
+
+    def __init__(self, torch, i2s, weights, M, device, seed):
+        self.M = M
+        act_elems = LAYERS * M * sum(ACT_K)
+        out_elems = LAYERS * M * sum(N for _, N, _ in PROJ)
+        x = synth.normal_f32(act_elems, seed=seed)
+        self.x_host = torch.from_numpy(x).pin_memory()
+        self.x = self.x_host.to(device)
+        self.y = torch.empty(out_elems, dtype=torch.float32, device=device)
+        self.y_host = torch.empty(out_elems, dtype=torch.float32).pin_memory()
+        problems, xo, yo = [], 0, 0
+        for layer in range(LAYERS):
+            xs = []
+            for K in ACT_K:
+                xs.append(self.x[xo:xo + M * K].view(M, K))
+                xo += M * K
+            for i, (name, N, K) in enumerate(PROJ):
+                y = self.y[yo:yo + M * N].view(M, N)
+                yo += M * N
+                problems.append((weights[layer][i], N, K, xs[ACT_OF[name]], y))
+        self.group = i2s.Group(problems, M)
+        self.h2d_bytes = self.x.numel() * 4
+        self.d2h_bytes = self.y.numel() * 4
+        n_act = LAYERS * len(ACT_K)
+        kp = [((K + 255) // 256) * 256 for K in ACT_K]
+        # algorithmic bytes of one GEMV launch: codes + scale trailers, the quantized
+        # activation operand (2 bytes per padded position) with scale and row sum,
+        # and the F32 outputs
+        self.gemv_bytes = (WEIGHT_BYTES_PER_PASS + LAYERS * len(PROJ) * 32 +
+                           LAYERS * M * sum(2 * k + 8 for k in kp) + out_elems * 4)
+        self.quant_bytes = act_elems * 4 + LAYERS * M * sum(2 * k + 8 for k in kp)
+        del n_act
+
+
+def cpu_baseline_decode(seconds_target=12.0):
+    """Times the oracle (as it stands) on whole layers of the same workload, M = 1
+    and M = 8, on all host cores, until about seconds_target of work is done."""
+    import oracle
+    o = oracle.get()
+    nth = os.cpu_count() or 1
+    done_bytes, elapsed, layers = 0, 0.0, 0
+    for layer in range(LAYERS):
+        packed = []
+        for i, (name, N, K) in enumerate(PROJ):
+            payload = synth.packed_code_bytes(N * K // 4, seed=1000 * layer + i)
+            scale = synth.uniform_f32(1, 2000 * layer + i, 0.01, 0.1)[0]
+            trailer = np.zeros(32, np.uint8)
+            trailer[:4] = np.frombuffer(np.float32(scale).tobytes(), np.uint8)
+            packed.append(np.concatenate([payload, trailer]))
+        for M in (1, 8):
+            xs = [synth.normal_f32((M, K), seed=layer * 10 + j) for j, K in enumerate(ACT_K)]
+            t0 = time.perf_counter()
+            for i, (name, N, K) in enumerate(PROJ):
+                o.i2s_mul_mat(packed[i], N, K, xs[ACT_OF[name]], nth=nth)
+            elapsed += time.perf_counter() - t0
+            done_bytes += sum(N * K // 4 for _, N, K in PROJ)
+        layers += 1
+        if elapsed >= seconds_target:
+            break
+    return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+            "sample": f"first {layers} of 28 layers, all 7 projections, M=1 and M=8 "
+                      f"({done_bytes / 1e6:.1f} MB of codes, {elapsed:.1f} s)"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    o = oracle.get()
+    nth = os.cpu_count() or 1
+    # Each step: one layer (all 7 projections) at M = 1 and M = 8, layers taken in turn.
+    cache = {}
+
+    def layer_inputs(layer):
+        if layer not in cache:
+            packed = []
+            for i, (name, N, K) in enumerate(PROJ):
+                payload = synth.packed_code_bytes(N * K // 4, seed=1000 * layer + i)
+                scale = synth.uniform_f32(1, 2000 * layer + i, 0.01, 0.1)[0]
+                trailer = np.zeros(32, np.uint8)
+                trailer[:4] = np.frombuffer(np.float32(scale).tobytes(), np.uint8)
+                packed.append(np.concatenate([payload, trailer]))
+            xs = {M: [synth.normal_f32((M, K), seed=layer * 10 + j) for j, K in enumerate(ACT_K)] for M in (1, 8)}
+            cache.clear()
+            cache[layer] = (packed, xs)
+        return cache[layer]
+
+    def step(s):
+        layer = s % LAYERS
+        packed, xs = layer_inputs(layer)
+        for M in (1, 8):
+            for i, (name, N, K) in enumerate(PROJ):
+                o.i2s_mul_mat(packed[i], N, K, xs[M][ACT_OF[name]], nth=nth)
+
+    for s in range(args.warmup):
+        layer_inputs(s % LAYERS)
+        step(s)
+    t_total = 0.0
+    for s in range(args.steps):
+        layer_inputs((args.warmup + s) % LAYERS)
+        t0 = time.perf_counter()
+        step(args.warmup + s)
+        t_total += time.perf_counter() - t0
+    bytes_per_step = 2 * sum(N * K // 4 for _, N, K in PROJ)
+    value = args.steps * bytes_per_step / t_total / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_per_step": "one layer (7 projections) at M=1 and M=8",
+                       "layers": LAYERS, "M": [1, 8]},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nth, "kind": "oracle",
+                             "sample": "one decoder layer of the projection set per step, M=1 and M=8"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, torch, dist):
+    from int8_quantized_matmul_gb300 import build as libbuild
+    libbuild.build()
+    from int8_quantized_matmul_gb300 import i2s
+
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    weights = make_weights(torch, device)
+    passes = [DecodePass(torch, i2s, weights, M, device, seed=100 + M) for M in (1, 8)]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # Each phase (quantize, run) of each M is captured once as a CUDA graph, so
+    # a step replays 4 kernel launches with no host-side marshalling.
+    for p in passes:
+        p.group()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(device=device)
+    graphs = []
+    with torch.cuda.stream(cap):
+        for p in passes:
+            gq, gr = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gq, stream=cap):
+                p.group.quantize()
+            with torch.cuda.graph(gr, stream=cap):
+                p.group.run()
+            graphs.append((gq, gr))
+    torch.cuda.synchronize()
+
+    def one_step(ev=None):
+        for k, (gq, gr) in enumerate(graphs):
+            if ev is not None:
+                ev[k][0].record(stream)
+            gq.replay()
+            if ev is not None:
+                ev[k][1].record(stream)
+            gr.replay()
+            if ev is not None:
+                ev[k][2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    barrier()
+
+    # Clocks are sampled from a ~1.5 s soak of the same step right before the
+    # timed region through its end (the timed region alone is a few ms).
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        for _ in range(50):
+            one_step()
+        torch.cuda.synchronize()
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in passes] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start.record(stream)
+    for s in range(args.steps):
+        one_step(events[s])
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    per_m = {}
+    gemv_ms_all, gemv_bytes_all = [], []
+    for k, p in enumerate(passes):
+        q_ms = [events[s][k][0].elapsed_time(events[s][k][1]) for s in range(args.steps)]
+        g_ms = [events[s][k][1].elapsed_time(events[s][k][2]) for s in range(args.steps)]
+        gemv_ms_all += g_ms
+        gemv_bytes_all += [p.gemv_bytes] * len(g_ms)
+        per_m[str(p.M)] = {
+            "gemv_ms": statistics.median(g_ms), "quant_ms": statistics.median(q_ms),
+            "weight_gbs": WEIGHT_BYTES_PER_PASS / (statistics.median(g_ms) + statistics.median(q_ms)) / 1e6,
+            "gemv_only_weight_gbs": WEIGHT_BYTES_PER_PASS / statistics.median(g_ms) / 1e6,
+        }
+    bytes_per_step = WEIGHT_BYTES_PER_PASS * len(passes)
+    value = world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9
+    gemv_avg_ms = sum(gemv_ms_all) / len(gemv_ms_all)
+    gemv_avg_bytes = sum(gemv_bytes_all) / len(gemv_bytes_all)
+    achieved = gemv_avg_bytes / (gemv_avg_ms * 1e-3) / 1e9
+
+    # end to end through the public API: activations host->device, the pass,
+    # outputs device->host, every step (pinned buffers)
+    for _ in range(2):
+        for p in passes:
+            p.x.copy_(p.x_host, non_blocking=True)
+            p.group()
+            p.y_host.copy_(p.y, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for p in passes:
+            p.x.copy_(p.x_host, non_blocking=True)
+            p.group()
+            p.y_host.copy_(p.y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * args.steps * bytes_per_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": sum(p.h2d_bytes for p in passes),
+           "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": LAYERS, "M": [1, 8], "launch": "CUDA graph per phase",
+                   "weight_bytes_per_pass": WEIGHT_BYTES_PER_PASS, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 327.5 MB of codes per pass vs 129 MB L2, streamed once per pass"},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 2 * len(passes) * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "k_i2s_gemv", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     else "fallback 6800 GB/s"},
+        "per_m": per_m,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", init_method="env://")
+        dist = dist_mod
+    line = run_ours(args, rank, world, torch, dist)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_decode()
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

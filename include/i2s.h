@@ -1,0 +1,253 @@
+/*
+ * i2s.h - C ABI of libi2s.so: the I2_S ternary-weight x INT8-activation
+ * matmul and the I8_S x I8_S fused mul_mat_add(_relu), on NVIDIA GB300
+ * (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "ggml: additive INT8/ternary types, fused CPU ops, and kernels for
+ *        VibeASR (1/2)" (audio.cpp pull request 447)
+ *   [P2] "ggml-cpu: ternary I2_S matmul kernel (VibeASR, 3/4)" (audio.cpp
+ *        pull request 445)
+ *   [P3] "VibeASR in audio.cpp"
+ *   [P4] "Experiment - int8 W8A8 path" (ork-driver wiki)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Shapes follow ggml: a weight W is N x K (K contiguous), activations X are
+ * M x K (K contiguous), outputs Y are M x N (N contiguous). All sizes are
+ * element counts.
+ *
+ * Pointers documented as "device" must point to memory the current CUDA device
+ * can read or write (cudaMalloc, torch CUDA tensors, managed memory). Pointers
+ * documented as "host" are ordinary CPU memory. The library never allocates,
+ * frees or retains any caller buffer; the caller owns every buffer and must
+ * keep it alive until the work queued on `stream` has finished.
+ *
+ * Device entry points are asynchronous and stream-ordered: they validate their
+ * arguments on the host, enqueue kernels on `stream` (NULL = legacy default
+ * stream) and return without synchronizing. A non-zero return means nothing
+ * was enqueued (argument errors) or the launch failed (I2S_E_CUDA).
+ *
+ * Scales live in band, after the payload ([P1] "Two new types"), so a weight
+ * or I8_S activation is fully described by its bytes and its shape.
+ *
+ * Byte layouts
+ * ------------
+ * I2_S (N x K, K % 128 == 0): N*K/4 payload bytes. The flat tensor is cut
+ *   into groups of 128 values stored in 32 bytes; byte gp of a group holds the
+ *   group-relative positions gp, 32+gp, 64+gp, 96+gp in its bit pairs at
+ *   shifts 6, 4, 2, 0 ([P1] Kernels; [P2] Kernels). Codes {0,1,2} stand for
+ *   the ternary values {-1,0,+1}. Then the F32 absmax (a multiplier:
+ *   w = (code-1)*absmax) at byte offset N*K/4, then 28 zero bytes.
+ * I8_S (n elements): n int8 bytes, zero padded to a multiple of 32, then the
+ *   F32 scale (a multiplier: x = q*scale, scale = amax/127), then 28 zero
+ *   bytes ([P1] "Two new types"). The pages call the scale "padded" without
+ *   saying how; the 32-byte trailer is this library's reading.
+ *
+ * Arithmetic ([P2] Arithmetic; [P1] "Arithmetic is exact where it can be")
+ * ----------
+ * Every result is bit-identical to the plain definition:
+ *   row quantization: amax = max(max_k |x|, 1e-5); scale = amax/127;
+ *     inv = 127/amax; q = clamp(round(x*inv), -127, 127), halfway cases
+ *     rounded away from zero; row_sum = sum_k q.
+ *   I2_S: dot = sum_k code*q (int32, exact);
+ *     y = (float)(dot - row_sum) * (w_scale * act_scale).
+ *   I8_S: acc = sum_k w*x (int32, exact);
+ *     y = (float)acc * (w_scale * x_scale) + bias[n]; ReLU: y > 0 ? y : +0;
+ *     the output is requantized with one scale for the whole tensor.
+ * Every float step is one IEEE-754 binary32 operation rounded to nearest
+ * (no fused multiply-add).
+ */
+#ifndef I2S_H
+#define I2S_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* i2s_stream_t;
+
+/* Status codes (0 = success). */
+enum {
+    I2S_OK = 0,
+    I2S_E_BAD_SHAPE = -1,          /* non-positive size, K % 128 != 0, too large */
+    I2S_E_NULL_PTR = -2,           /* a required pointer is NULL */
+    I2S_E_MISALIGNED = -3,         /* a device pointer is not 16-byte aligned */
+    I2S_E_WORKSPACE_TOO_SMALL = -4,/* ws_bytes below the *_workspace() size */
+    I2S_E_CUDA = -5,               /* a CUDA runtime call or launch failed */
+    I2S_E_DEVICE_TIMEOUT = -6,     /* a kernel gave up a bounded wait (see i2s_read_status) */
+    I2S_E_UNSUPPORTED_DEVICE = -7, /* current device is not sm_103 */
+    I2S_E_BAD_ARG = -8             /* any other invalid argument */
+};
+
+/* Human-readable name of a status code. Never NULL; the string is static. */
+const char* i2s_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int i2s_version(void);
+
+/* 1 if the current CUDA device can run this library (compute capability
+ * 10.3), 0 if not, a negative status if the CUDA runtime fails. */
+int i2s_device_supported(void);
+
+/* ---------------------------------------------------------------------------
+ * Layout helpers (host only, no CUDA calls). Return 0 for invalid shapes.
+ * ------------------------------------------------------------------------- */
+size_t i2s_nbytes(int64_t N, int64_t K);        /* N*K/4 + 32 */
+size_t i2s_scale_offset(int64_t N, int64_t K);  /* N*K/4 */
+size_t i8s_nbytes(int64_t n);                   /* align32(n) + 32 */
+size_t i8s_scale_offset(int64_t n);             /* align32(n) */
+
+/* Packs N x K ternary codes (host, one code in {0,1,2} per byte, row-major)
+ * and the F32 absmax into I2_S bytes at dst (host, i2s_nbytes(N,K) bytes).
+ * Codes above 3 are masked to their low 2 bits. Errors: BAD_SHAPE, NULL_PTR. */
+int i2s_pack_host(const uint8_t* codes, int64_t N, int64_t K, float w_scale, void* dst);
+
+/* Packs n int8 values (host) and an F32 scale into I8_S bytes at dst (host,
+ * i8s_nbytes(n) bytes). Errors: BAD_SHAPE, NULL_PTR. */
+int i8s_pack_host(const int8_t* q, int64_t n, float scale, void* dst);
+
+/* ---------------------------------------------------------------------------
+ * Activation quantization, per row ([P2] Arithmetic and the threading
+ * paragraph of Kernels; [P3] Encoder for the 1e-5 floor; [P4] Implementation
+ * for scale = amax/127, inv = 127/amax, round, clamp +-127).
+ *
+ * x        device, M x K F32, 16-byte aligned.
+ * q        device, M x K int8 (row-major, same order as x).
+ * act_scale device, M F32: amax/127 of each row.
+ * row_sum  device, M int32: sum of each quantized row (the sidecar that the
+ *          I2_S epilogue subtracts, [P1] "Arithmetic is exact where it can be").
+ * K % 4 == 0 is required (K % 128 == 0 for use with I2_S weights).
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, CUDA.
+ * ------------------------------------------------------------------------- */
+int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act_scale,
+                     int32_t* row_sum, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * I2_S x F32 -> F32 matmul: ggml_mul_mat with an I2_S src0 and an F32 src1
+ * ([P2] Interface, Arithmetic; [P1] "Five fused INT8 ops", last paragraph).
+ *
+ * w_i2s  device, i2s_nbytes(N,K) bytes of I2_S weights (scale read in band).
+ * x      device, M x K F32 activations (a batched 3-D src1 is passed flattened
+ *        into M rows), 16-byte aligned.
+ * y      device, M x N F32 output, 16-byte aligned.
+ * ws     device workspace of at least i2s_mul_mat_workspace(M,N,K) bytes,
+ *        256-byte aligned; holds the quantized rows, per-row scale and sum
+ *        (the counterpart of the sidecar ggml keeps in params->wdata), the
+ *        integer partial sums of a K-split launch and a status word. Not
+ *        preserved between calls; calls sharing one ws must be ordered on one
+ *        stream.
+ * Requirements: K % 128 == 0, M >= 1, N >= 1, M*K < 2^31, N*K/4 < 2^31.
+ * M <= 16 runs the decode GEMV (weight-bandwidth bound); larger M runs the
+ * tensor-core GEMM. Both give identical bits.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
+ * ------------------------------------------------------------------------- */
+size_t i2s_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
+int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,
+                void* ws, size_t ws_bytes, i2s_stream_t stream);
+
+/* Launch-shape overrides for testing and tuning. Every setting gives the same
+ * bits; zero fields mean "choose automatically". */
+typedef struct i2s_config {
+    int path;        /* 0 auto, 1 decode GEMV (any M, in slices of 16 rows), 2 tensor-core GEMM */
+    int split_k;     /* GEMV: CTAs sharing one row block along K (1, 2, 4, 8) */
+    int rows_per_cta;/* GEMV: weight rows per CTA tile (multiple of 16) */
+    int grid_ctas;   /* GEMM: persistent CTA count (<= SM count) */
+} i2s_config;
+
+int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,
+                   void* ws, size_t ws_bytes, const i2s_config* config, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouped I2_S matmul: several independent projections with the same number of
+ * activation rows M, run as one quantization launch plus one GEMV/GEMM launch
+ * (the per-layer q/k/v/o/gate/up/down set of a decoder, or many layers).
+ * Projections whose x pointers (and K) are equal share one quantization.
+ *
+ * probs  host array of `count` problems; read during the call only.
+ * count  1 .. I2S_MAX_GROUP.
+ * ws     device workspace of at least i2s_mul_mat_grouped_workspace() bytes.
+ * Requirements per problem as for i2s_mul_mat.
+ * Errors: as i2s_mul_mat, plus BAD_ARG for count out of range.
+ * ------------------------------------------------------------------------- */
+#define I2S_MAX_GROUP 256
+
+typedef struct i2s_problem {
+    const void* w_i2s; /* device, I2_S N x K */
+    int64_t N;
+    int64_t K;
+    const float* x;    /* device, M x K F32 */
+    float* y;          /* device, M x N F32 */
+} i2s_problem;
+
+size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M);
+int i2s_mul_mat_grouped(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                        i2s_stream_t stream);
+
+/* The two phases of i2s_mul_mat_grouped as separate calls, as the pages'
+ * mul_mat runs them ([P2] Kernels, threading paragraph: quantize the rows,
+ * one barrier, then the output features). _quantize writes every distinct
+ * activation's quantized rows, scale and row sum into ws; _run computes all
+ * the projections from ws. A _run call must use the same problem list, M and
+ * workspace as the _quantize call before it on the stream. Splitting lets a
+ * caller quantize once and run the projections later or in several launches.
+ * Errors: as i2s_mul_mat_grouped. */
+int i2s_mul_mat_grouped_quantize(const i2s_problem* probs, int count, int64_t M, void* ws,
+                                 size_t ws_bytes, i2s_stream_t stream);
+int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void* ws,
+                            size_t ws_bytes, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * I8_S x I8_S -> I8_S fused matmul + bias (+ ReLU) with requantization in the
+ * op: ggml_mul_mat_add (relu = 0) and ggml_mul_mat_add_relu (relu != 0)
+ * ([P1] "Five fused INT8 ops").
+ *
+ * w_i8s  device, i8s_nbytes(N*K) bytes: N x K int8 weights + in-band scale.
+ * x_i8s  device, i8s_nbytes(M*K) bytes: M x K int8 activations + scale.
+ * bias   device, N F32, or NULL for no bias.
+ * y_i8s  device, i8s_nbytes(M*N) bytes: M x N int8 output + in-band scale.
+ * ws     device workspace of at least i8s_mul_mat_workspace(M,N,K) bytes,
+ *        256-byte aligned. After the call it holds the F32 output before
+ *        requantization (M x N, row-major) at offset 256 (i8s_ws_f32_offset).
+ * Requirements: K % 64 == 0, M*K, N*K, M*N < 2^31; all pointers 16-byte
+ * aligned.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
+ * ------------------------------------------------------------------------- */
+size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
+size_t i8s_ws_f32_offset(void);
+int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M,
+                         const float* bias, int relu, void* y_i8s, void* ws, size_t ws_bytes,
+                         i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * F32 -> I8_S requantization with one scale for the whole tensor ([P1] "Two
+ * new types", "Five fused INT8 ops"; [P3] Encoder): amax = max(max|y|, 1e-5),
+ * scale = amax/127, q = clamp(round(y*127/amax), -127, 127).
+ *
+ * y      device, n F32, 16-byte aligned.
+ * dst    device, i8s_nbytes(n) bytes.
+ * ws     device workspace of at least i8s_requant_workspace(n) bytes.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
+ * ------------------------------------------------------------------------- */
+size_t i8s_requant_workspace(int64_t n);
+int i8s_requant(const float* y, int64_t n, void* dst_i8s, void* ws, size_t ws_bytes,
+                i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Device status. Kernels with bounded waits (the tensor-core pipelines) never
+ * trap: when a wait runs out they record a code in the status word at the
+ * start of the workspace and exit. This call synchronizes `stream`, reads and
+ * clears that word, and returns I2S_OK or I2S_E_DEVICE_TIMEOUT (or
+ * I2S_E_CUDA if the stream reports an error).
+ * ------------------------------------------------------------------------- */
+int i2s_read_status(void* ws, i2s_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I2S_H */

@@ -1,0 +1,446 @@
+// The C ABI of libi2s.so (declared and documented in include/i2s.h): argument
+// validation, workspace layout, path choice and kernel launches. Every step of
+// the computation runs in the kernels of quant.cu, gemv.cu, gemm_tc.cu and
+// i8s.cu; this file only marshals.
+
+#include <atomic>
+#include <cstring>
+#include <vector>
+
+#include "../../include/i2s.h"
+#include "internal.h"
+
+namespace i2s {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeader = 256;             // status word at 0, amax word at 128
+constexpr size_t kStatusOff = 0;
+constexpr size_t kAmaxOff = 128;
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
+
+struct DevInfo {
+    std::atomic<int> state{0};   // 0 unknown, 1 supported, 2 unsupported
+    int sms = 0;
+};
+DevInfo g_dev[kMaxDevices];
+
+// Returns I2S_OK if the current device is sm_103, caching per device.
+int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return I2S_E_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return I2S_E_UNSUPPORTED_DEVICE;
+    DevInfo& d = g_dev[dev];
+    int st = d.state.load(std::memory_order_acquire);
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return I2S_E_CUDA;
+        d.sms = sms;
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        d.state.store(st, std::memory_order_release);
+    }
+    return st == 1 ? I2S_OK : I2S_E_UNSUPPORTED_DEVICE;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? I2S_OK : I2S_E_CUDA; }
+
+// ---------------------------------------------------------------------------
+// I2_S workspace: [header][act_scale M][row_sum M][operand][dot_acc M*N][tickets]
+// The operand is large enough for either matmul path: the GEMV's e4m3 records
+// (2*Kp bytes per row, Kp = K rounded up to 256) or the GEMM's f16 rows.
+// ---------------------------------------------------------------------------
+struct ActSlot {
+    size_t scale_off, sum_off, op_off;
+};
+
+size_t act_slot_bytes(int64_t M, int64_t K) {
+    const int64_t Kp = round_up(K, 256);
+    return align_up((size_t)M * 4) * 2 + align_up((size_t)M * (size_t)Kp * 2);
+}
+
+ActSlot act_slot_at(size_t base, int64_t M) {
+    ActSlot s;
+    s.scale_off = base;
+    s.sum_off = base + align_up((size_t)M * 4);
+    s.op_off = s.sum_off + align_up((size_t)M * 4);
+    return s;
+}
+
+bool i2s_shape_ok(int64_t N, int64_t K, int64_t M) {
+    if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return false;
+    if (M * K >= ((int64_t)1 << 31) || N * (K / 4) >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31)) return false;
+    if (K > 65536) return false;   // keeps |dot| = |sum code*q| <= 254*K below 2^24
+    return true;
+}
+
+int pick_split_k(int N, int K, int sms) {
+    const int tiles = (N + kGemvTileRows - 1) / kGemvTileRows;
+    const int KB = (K + 255) / 256;
+    int s = 1;
+    while (s < 8 && tiles * s < sms && s * 2 <= KB) s *= 2;
+    return s;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    if (g_dev[dev].state.load() == 0) check_device();
+    return g_dev[dev].sms > 0 ? g_dev[dev].sms : 152;
+}
+
+}  // namespace i2s
+
+using namespace i2s;
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+const char* i2s_status_string(int status) {
+    switch (status) {
+        case I2S_OK: return "ok";
+        case I2S_E_BAD_SHAPE: return "bad shape";
+        case I2S_E_NULL_PTR: return "null pointer";
+        case I2S_E_MISALIGNED: return "misaligned pointer";
+        case I2S_E_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case I2S_E_CUDA: return "CUDA error";
+        case I2S_E_DEVICE_TIMEOUT: return "device wait timed out";
+        case I2S_E_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+        case I2S_E_BAD_ARG: return "bad argument";
+        default: return "unknown status";
+    }
+}
+
+int i2s_version(void) { return 100; }
+
+int i2s_device_supported(void) {
+    const int r = check_device();
+    if (r == I2S_OK) return 1;
+    if (r == I2S_E_UNSUPPORTED_DEVICE) return 0;
+    return r;
+}
+
+size_t i2s_nbytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 128 || K % 128) return 0;
+    return (size_t)N * (size_t)K / 4 + 32;
+}
+size_t i2s_scale_offset(int64_t N, int64_t K) {
+    if (N < 1 || K < 128 || K % 128) return 0;
+    return (size_t)N * (size_t)K / 4;
+}
+size_t i8s_nbytes(int64_t n) { return n < 1 ? 0 : (size_t)round_up(n, 32) + 32; }
+size_t i8s_scale_offset(int64_t n) { return n < 1 ? 0 : (size_t)round_up(n, 32); }
+
+int i2s_pack_host(const uint8_t* codes, int64_t N, int64_t K, float w_scale, void* dst) {
+    if (!codes || !dst) return I2S_E_NULL_PTR;
+    if (N < 1 || K < 128 || K % 128) return I2S_E_BAD_SHAPE;
+    uint8_t* out = static_cast<uint8_t*>(dst);
+    const int64_t groups = N * K / 128;
+    for (int64_t g = 0; g < groups; ++g) {
+        const uint8_t* c = codes + g * 128;
+        uint8_t* o = out + g * 32;
+        for (int gp = 0; gp < 32; ++gp)
+            o[gp] = (uint8_t)(((c[gp] & 3) << 6) | ((c[32 + gp] & 3) << 4) | ((c[64 + gp] & 3) << 2) | (c[96 + gp] & 3));
+    }
+    uint8_t* trailer = out + N * K / 4;
+    std::memset(trailer, 0, 32);
+    std::memcpy(trailer, &w_scale, 4);
+    return I2S_OK;
+}
+
+int i8s_pack_host(const int8_t* q, int64_t n, float scale, void* dst) {
+    if (!q || !dst) return I2S_E_NULL_PTR;
+    if (n < 1) return I2S_E_BAD_SHAPE;
+    uint8_t* out = static_cast<uint8_t*>(dst);
+    const size_t off = i8s_scale_offset(n);
+    std::memcpy(out, q, (size_t)n);
+    std::memset(out + n, 0, off + 32 - (size_t)n);
+    std::memcpy(out + off, &scale, 4);
+    return I2S_OK;
+}
+
+int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act_scale, int32_t* row_sum,
+                     i2s_stream_t stream) {
+    if (!x || !q || !act_scale || !row_sum) return I2S_E_NULL_PTR;
+    if (M < 1 || K < 4 || K % 4 || M * K >= ((int64_t)1 << 31)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(x) || ((uintptr_t)q & 3u) || ((uintptr_t)act_scale & 3u) || ((uintptr_t)row_sum & 3u))
+        return I2S_E_MISALIGNED;
+    int r = check_device();
+    if (r) return r;
+    QuantArgs a;
+    a.count = 1;
+    a.M = (int)M;
+    a.layout = kQuantI8Rows;
+    a.j[0] = QuantJob{x, q, act_scale, row_sum, (int)K, (int)K};
+    return cuda_status(launch_quant(a, stream));
+}
+
+size_t i2s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
+    if (!i2s_shape_ok(N, K, M)) return 0;
+    const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
+    return kHeader + act_slot_bytes(M, K) + align_up((size_t)M * (size_t)N * 4) + align_up(tiles * 4);
+}
+
+int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
+                   size_t ws_bytes, const i2s_config* config, i2s_stream_t stream) {
+    if (!w_i2s || !x || !y || !ws) return I2S_E_NULL_PTR;
+    if (!i2s_shape_ok(N, K, M)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(w_i2s) || !aligned16(x) || !aligned16(y) || !aligned256(ws)) return I2S_E_MISALIGNED;
+    if (ws_bytes < i2s_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+
+    const int path = config ? config->path : 0;
+    const bool use_gemv = path == 1 || (path == 0 && M <= 16);
+    if (!use_gemv) return I2S_E_BAD_ARG;   // tensor-core GEMM: see gemm_tc.cu
+
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const ActSlot slot = act_slot_at(kHeader, M);
+    const size_t dot_off = kHeader + act_slot_bytes(M, K);
+    const size_t tick_off = dot_off + align_up((size_t)M * (size_t)N * 4);
+    const int Kp = (int)round_up(K, 256);
+
+    QuantArgs qa;
+    qa.count = 1;
+    qa.M = (int)M;
+    qa.layout = kQuantE4M3Frag;
+    qa.j[0] = QuantJob{x, base + slot.op_off, reinterpret_cast<float*>(base + slot.scale_off),
+                       reinterpret_cast<int32_t*>(base + slot.sum_off), (int)K, Kp};
+    r = cuda_status(launch_quant(qa, stream));
+    if (r) return r;
+
+    const int sms = device_sm_count();
+    int split = config && config->split_k > 0 ? config->split_k : pick_split_k((int)N, (int)K, sms);
+    if (split > 8) split = 8;
+    if (split > 1) {
+        const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
+        r = cuda_status(cudaMemsetAsync(base + dot_off, 0, tick_off - dot_off + tiles * 4, stream));
+        if (r) return r;
+    }
+    // Activation rows are processed in slices of at most 16 (one launch each).
+    static thread_local GemvArgs ga;
+    for (int64_t m0 = 0; m0 < M; m0 += 16) {
+        const int mm = (int)(M - m0 < 16 ? M - m0 : 16);
+        ga.count = 1;
+        ga.M = mm;
+        ga.split_k = split;
+        GemvProb& p = ga.p[0];
+        p.w = static_cast<const uint8_t*>(w_i2s);
+        p.act = reinterpret_cast<const uint32_t*>(base + slot.op_off) + (size_t)m0 * (Kp / 2);
+        p.act_scale = reinterpret_cast<const float*>(base + slot.scale_off) + m0;
+        p.row_sum = reinterpret_cast<const int32_t*>(base + slot.sum_off) + m0;
+        p.y = y + (size_t)m0 * N;
+        p.dot_acc = reinterpret_cast<int32_t*>(base + dot_off) + (size_t)m0 * N;
+        p.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
+        p.N = (int)N;
+        p.K = (int)K;
+        p.tile0 = 0;
+        if (split > 1 && m0 > 0) {
+            // each slice reuses the ticket counters: clear them between slices
+            const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
+            r = cuda_status(cudaMemsetAsync(base + tick_off, 0, tiles * 4, stream));
+            if (r) return r;
+        }
+        r = cuda_status(launch_gemv(ga, gemv_ctas_for((int)N, split), stream));
+        if (r) return r;
+    }
+    return I2S_OK;
+}
+
+int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
+                size_t ws_bytes, i2s_stream_t stream) {
+    return i2s_mul_mat_ex(w_i2s, N, K, x, M, y, ws, ws_bytes, nullptr, stream);
+}
+
+// Distinct activations of a group, in first-use order.
+static int group_acts(const i2s_problem* probs, int count, std::vector<int>& act_of,
+                      std::vector<int>& first) {
+    act_of.assign(count, -1);
+    first.clear();
+    for (int i = 0; i < count; ++i) {
+        for (size_t a = 0; a < first.size(); ++a) {
+            const i2s_problem& f = probs[first[a]];
+            if (f.x == probs[i].x && f.K == probs[i].K) { act_of[i] = (int)a; break; }
+        }
+        if (act_of[i] < 0) { act_of[i] = (int)first.size(); first.push_back(i); }
+    }
+    return (int)first.size();
+}
+
+size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M) {
+    if (!probs || count < 1 || count > I2S_MAX_GROUP) return 0;
+    std::vector<int> act_of, first;
+    group_acts(probs, count, act_of, first);
+    size_t total = kHeader;
+    for (int a : first) {
+        if (!i2s_shape_ok(probs[a].N, probs[a].K, M)) return 0;
+        total += act_slot_bytes(M, probs[a].K);
+    }
+    return total;
+}
+
+// Phase bits of a grouped call: 1 = quantize the distinct activations into
+// the workspace, 2 = run the matmuls from the workspace.
+static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                        i2s_stream_t stream, int phases) {
+    if (!probs || !ws) return I2S_E_NULL_PTR;
+    if (count < 1 || count > I2S_MAX_GROUP) return I2S_E_BAD_ARG;
+    for (int i = 0; i < count; ++i) {
+        const i2s_problem& p = probs[i];
+        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
+        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
+        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+    }
+    if (!aligned256(ws)) return I2S_E_MISALIGNED;
+    if (ws_bytes < i2s_mul_mat_grouped_workspace(probs, count, M)) return I2S_E_WORKSPACE_TOO_SMALL;
+    if (M > 16) return I2S_E_BAD_ARG;   // grouped tensor-core GEMM: see gemm_tc.cu
+    int r = check_device();
+    if (r) return r;
+
+    std::vector<int> act_of, first;
+    const int n_act = group_acts(probs, count, act_of, first);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    std::vector<ActSlot> slots(n_act);
+    size_t off = kHeader;
+    for (int a = 0; a < n_act; ++a) {
+        slots[a] = act_slot_at(off, M);
+        off += act_slot_bytes(M, probs[first[a]].K);
+    }
+    if (phases & 1) {
+        static thread_local QuantArgs qa;
+        qa.count = n_act;
+        qa.M = (int)M;
+        qa.layout = kQuantE4M3Frag;
+        for (int a = 0; a < n_act; ++a) {
+            const i2s_problem& p = probs[first[a]];
+            qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
+                               reinterpret_cast<int32_t*>(base + slots[a].sum_off), (int)p.K,
+                               (int)round_up(p.K, 256)};
+        }
+        r = cuda_status(launch_quant(qa, stream));
+        if (r) return r;
+    }
+    if (phases & 2) {
+        static thread_local GemvArgs ga;
+        ga.count = count;
+        ga.M = (int)M;
+        ga.split_k = 1;
+        int ctas = 0;
+        for (int i = 0; i < count; ++i) {
+            const i2s_problem& q = probs[i];
+            const ActSlot& s = slots[act_of[i]];
+            GemvProb& p = ga.p[i];
+            p.w = static_cast<const uint8_t*>(q.w_i2s);
+            p.act = reinterpret_cast<const uint32_t*>(base + s.op_off);
+            p.act_scale = reinterpret_cast<const float*>(base + s.scale_off);
+            p.row_sum = reinterpret_cast<const int32_t*>(base + s.sum_off);
+            p.y = q.y;
+            p.dot_acc = nullptr;
+            p.tickets = nullptr;
+            p.N = (int)q.N;
+            p.K = (int)q.K;
+            p.tile0 = ctas;
+            ctas += gemv_ctas_for((int)q.N, 1);
+        }
+        r = cuda_status(launch_gemv(ga, ctas, stream));
+        if (r) return r;
+    }
+    return I2S_OK;
+}
+
+int i2s_mul_mat_grouped(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                        i2s_stream_t stream) {
+    return grouped_impl(probs, count, M, ws, ws_bytes, stream, 3);
+}
+
+int i2s_mul_mat_grouped_quantize(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                                 i2s_stream_t stream) {
+    return grouped_impl(probs, count, M, ws, ws_bytes, stream, 1);
+}
+
+int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                            i2s_stream_t stream) {
+    return grouped_impl(probs, count, M, ws, ws_bytes, stream, 2);
+}
+
+size_t i8s_ws_f32_offset(void) { return kHeader; }
+
+size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 64 || K % 64) return 0;
+    return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)M * (size_t)K * 2);
+}
+
+int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
+                         int relu, void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!w_i8s || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
+    if (M < 1 || N < 1 || K < 64 || K % 64) return I2S_E_BAD_SHAPE;
+    if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
+        return I2S_E_BAD_SHAPE;
+    if (!aligned16(w_i8s) || !aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) ||
+        (bias && ((uintptr_t)bias & 3u)))
+        return I2S_E_MISALIGNED;
+    if (ws_bytes < i8s_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    float* yf = reinterpret_cast<float*>(base + kHeader);
+    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    if (r) return r;
+    I8sMatArgs a;
+    a.w = static_cast<const int8_t*>(w_i8s);
+    a.x = static_cast<const int8_t*>(x_i8s);
+    a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
+    a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
+    a.bias = bias;
+    a.y = yf;
+    a.amax_bits = amax;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.relu = relu ? 1 : 0;
+    r = cuda_status(launch_i8s_mat(a, stream));
+    if (r) return r;
+    return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
+}
+
+size_t i8s_requant_workspace(int64_t n) { return n < 1 ? 0 : kHeader; }
+
+int i8s_requant(const float* y, int64_t n, void* dst_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!y || !dst_i8s || !ws) return I2S_E_NULL_PTR;
+    if (n < 1 || n >= ((int64_t)1 << 40)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(y) || !aligned16(dst_i8s) || !aligned256(ws)) return I2S_E_MISALIGNED;
+    if (ws_bytes < i8s_requant_workspace(n)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    unsigned int* amax = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kAmaxOff);
+    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    if (r) return r;
+    r = cuda_status(launch_absmax(y, n, amax, stream));
+    if (r) return r;
+    return cuda_status(launch_requant(y, n, amax, static_cast<uint8_t*>(dst_i8s), stream));
+}
+
+int i2s_read_status(void* ws, i2s_stream_t stream) {
+    if (!ws) return I2S_E_NULL_PTR;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return I2S_E_CUDA;
+    uint32_t word = 0;
+    uint8_t* p = static_cast<uint8_t*>(ws) + kStatusOff;
+    if (cudaMemcpy(&word, p, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return I2S_E_CUDA;
+    if (word == 0) return I2S_OK;
+    if (cudaMemset(p, 0, 4) != cudaSuccess) return I2S_E_CUDA;
+    return I2S_E_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

@@ -1,0 +1,152 @@
+// I8_S x I8_S fused mul_mat_add(_relu) and the per-tensor requantization
+// ("ggml: additive INT8/ternary types, fused CPU ops, and kernels for VibeASR
+// (1/2)", sections "Two new types" and "Five fused INT8 ops").
+//
+// The matmul epilogue forms y = (float)acc * (w_scale * x_scale) + bias[n],
+// applies ReLU if asked, writes y (F32) to the workspace and folds max|y| into
+// one word with atomicMax on the float bits (valid because |y| >= 0, where the
+// IEEE order equals the unsigned order). The requant pass then turns the F32
+// tensor into I8_S with one scale, as the op's output must be self-describing.
+// Two passes are needed because the scale depends on the whole output.
+//
+// This file holds the dp4a tile kernel (exact int32 accumulation of int8
+// products); the tensor-core version lives in gemm_tc.cu.
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace i2s {
+
+namespace {
+
+constexpr int kT = 64;        // output tile 64 x 64
+constexpr int kKs = 64;       // K bytes per step
+constexpr int kPad = 16;      // row padding (bytes) against bank conflicts
+
+__global__ void __launch_bounds__(256) k_i8s_mat_dp4a(const I8sMatArgs a) {
+    __shared__ __align__(16) int8_t xs[kT][kKs + kPad];
+    __shared__ __align__(16) int8_t ws[kT][kKs + kPad];
+    __shared__ float s_max[8];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.y * kT, n0 = blockIdx.x * kT;
+    int acc[4][4] = {};
+
+    for (int k0 = 0; k0 < a.K; k0 += kKs) {
+        {   // one 16-byte chunk of each operand per thread
+            const int r = tid >> 2, c = (tid & 3) * 16;
+            const int m = m0 + r, n = n0 + r;
+            uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+            if (m < a.M) xv = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0 + c);
+            if (n < a.N) wv = *reinterpret_cast<const uint4*>(a.w + (size_t)n * a.K + k0 + c);
+            *reinterpret_cast<uint4*>(&xs[r][c]) = xv;
+            *reinterpret_cast<uint4*>(&ws[r][c]) = wv;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < kKs; kk += 4) {
+            int xw[4], ww[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xw[i] = *reinterpret_cast<const int*>(&xs[ty * 4 + i][kk]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ww[j] = *reinterpret_cast<const int*>(&ws[tx * 4 + j][kk]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = __dp4a(xw[i], ww[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+
+    const float sc = __fmul_rn(*a.w_scale_ptr, *a.x_scale_ptr);
+    float local_max = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx * 4 + j;
+            if (m < a.M && n < a.N) {
+                float v = __fmul_rn(__int2float_rn(acc[i][j]), sc);
+                if (a.bias) v = __fadd_rn(v, a.bias[n]);
+                if (a.relu) v = v > 0.0f ? v : 0.0f;
+                a.y[(size_t)m * a.N + n] = v;
+                local_max = fmaxf(local_max, fabsf(v));
+            }
+        }
+    }
+    local_max = warp_max(local_max);
+    if ((tid & 31) == 0) s_max[tid >> 5] = local_max;
+    __syncthreads();
+    if (tid == 0) {
+        float mx = 0.0f;
+        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, s_max[i]);
+        atomicMax(a.amax_bits, __float_as_uint(mx));
+    }
+}
+
+__global__ void __launch_bounds__(256) k_absmax(const float* __restrict__ y, int64_t n, unsigned int* amax_bits) {
+    __shared__ float s_max[8];
+    float mx = 0.0f;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) mx = fmaxf(mx, fabsf(y[i]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < 8; ++i) mx = fmaxf(mx, s_max[i]);
+        atomicMax(amax_bits, __float_as_uint(fmaxf(mx, s_max[0])));
+    }
+}
+
+// y (F32, n) -> I8_S bytes at dst: int8 payload, zero padding to 32 bytes, the
+// F32 scale and 28 zero bytes.
+__global__ void __launch_bounds__(256) k_requant(const float* __restrict__ y, int64_t n,
+                                                 const unsigned int* __restrict__ amax_bits, uint8_t* dst) {
+    float scale, inv;
+    quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t n4 = n / 4;
+    const float4* y4 = reinterpret_cast<const float4*>(y);
+    uint32_t* d4 = reinterpret_cast<uint32_t*>(dst);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 v = y4[i];
+        d4[i] = (uint32_t)(quantize_one(v.x, inv) & 0xff) | ((uint32_t)(quantize_one(v.y, inv) & 0xff) << 8) |
+                ((uint32_t)(quantize_one(v.z, inv) & 0xff) << 16) | ((uint32_t)(quantize_one(v.w, inv) & 0xff) << 24);
+    }
+    if (blockIdx.x == 0) {
+        const int64_t padded = (n + 31) / 32 * 32;
+        for (int64_t i = n4 * 4 + threadIdx.x; i < padded + 32; i += blockDim.x) {
+            uint8_t b = 0;
+            if (i < n) b = (uint8_t)(quantize_one(y[i], inv) & 0xff);
+            else if (i >= padded && i < padded + 4) b = (uint8_t)(__float_as_uint(scale) >> (8 * (i - padded)));
+            dst[i] = b;
+        }
+    }
+}
+
+int grid_for(int64_t n4) {
+    const int64_t want = (n4 + 255) / 256;
+    const int cap = device_sm_count() * 8;
+    return (int)(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_i8s_mat(const I8sMatArgs& a, cudaStream_t s) {
+    dim3 grid((a.N + kT - 1) / kT, (a.M + kT - 1) / kT);
+    k_i8s_mat_dp4a<<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s) {
+    k_absmax<<<grid_for(n), 256, 0, s>>>(y, n, amax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
+    k_requant<<<grid_for(n / 4), 256, 0, s>>>(y, n, amax_bits, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace i2s

@@ -1,0 +1,92 @@
+// Host-side declarations shared by the translation units of libi2s.so.
+// Not part of the public ABI (include/i2s.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace i2s {
+
+constexpr int kMaxGroup = 256;   // same value as I2S_MAX_GROUP
+
+// ---------------------------------------------------------------------------
+// Row quantizer. One warp quantizes one row of one activation matrix.
+// ---------------------------------------------------------------------------
+enum QuantLayout : int {
+    kQuantI8Rows = 0,    // plain int8, row-major M x K (the public sidecar)
+    kQuantE4M3Frag = 1,  // GEMV operand records (see gemv.cu), 2*Kp bytes per row
+    kQuantF16Perm = 2,   // tensor-core GEMM operand: f16, K permuted per 128-group
+};
+
+struct QuantJob {
+    const float* x;   // M x K F32
+    void* out;        // layout-dependent
+    float* scale;     // M
+    int32_t* sum;     // M
+    int K;
+    int Kp;           // K rounded up to the layout's padding (GEMV: 256)
+};
+
+struct QuantArgs {
+    int count;
+    int M;
+    int layout;
+    QuantJob j[kMaxGroup];
+};
+
+cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Decode GEMV (M <= 16) on the legacy e4m3 warp MMA.
+// ---------------------------------------------------------------------------
+constexpr int kGemvWarps = 8;
+constexpr int kGemvRowsPerWarp = 64;
+constexpr int kGemvTileRows = kGemvWarps * kGemvRowsPerWarp;   // 512 weight rows per CTA
+
+struct GemvProb {
+    const uint8_t* w;         // I2_S bytes, N x K/4 payload then the scale trailer
+    const uint32_t* act;      // e4m3 operand records, M rows x (2*Kp) bytes
+    const float* act_scale;   // M
+    const int32_t* row_sum;   // M
+    float* y;                 // M x N
+    int32_t* dot_acc;         // split-K only: M x N int32, zeroed before launch
+    uint32_t* tickets;        // split-K only: one counter per row tile, zeroed
+    int N;
+    int K;
+    int tile0;                // first linear CTA of this problem
+};
+
+struct GemvArgs {
+    int count;
+    int M;
+    int split_k;
+    GemvProb p[kMaxGroup];
+};
+
+int gemv_ctas_for(int N, int split_k);
+cudaError_t launch_gemv(const GemvArgs& a, int total_ctas, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// I8_S fused matmul (first version: dp4a tiles) and the per-tensor requant.
+// ---------------------------------------------------------------------------
+struct I8sMatArgs {
+    const int8_t* w;     // N x K
+    const int8_t* x;     // M x K
+    const float* w_scale_ptr;
+    const float* x_scale_ptr;
+    const float* bias;   // N or null
+    float* y;            // M x N F32
+    unsigned int* amax_bits;   // zeroed before launch
+    int M, N, K;
+    int relu;
+};
+cudaError_t launch_i8s_mat(const I8sMatArgs& a, cudaStream_t s);
+
+cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s);
+cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst,
+                           cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace i2s

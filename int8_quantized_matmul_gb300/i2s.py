@@ -1,0 +1,279 @@
+"""Python binding of libi2s.so (include/i2s.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels. Torch is used for device
+memory and streams: tensors are passed as raw device pointers, and calls are
+queued on torch's current CUDA stream. Importing this module fails loudly if
+the library has not been built (python -m int8_quantized_matmul_gb300.build).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libi2s.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libi2s.so is not built ({LIB_PATH} missing); run "
+                      "`python -m int8_quantized_matmul_gb300.build` first")
+_L = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+_f32 = ctypes.c_float
+
+MAX_GROUP = 256
+
+STATUS = {0: "I2S_OK", -1: "I2S_E_BAD_SHAPE", -2: "I2S_E_NULL_PTR", -3: "I2S_E_MISALIGNED",
+          -4: "I2S_E_WORKSPACE_TOO_SMALL", -5: "I2S_E_CUDA", -6: "I2S_E_DEVICE_TIMEOUT",
+          -7: "I2S_E_UNSUPPORTED_DEVICE", -8: "I2S_E_BAD_ARG"}
+
+
+class i2s_config(ctypes.Structure):
+    _fields_ = [("path", _int), ("split_k", _int), ("rows_per_cta", _int), ("grid_ctas", _int)]
+
+
+class i2s_problem(ctypes.Structure):
+    _fields_ = [("w_i2s", _p), ("N", _i64), ("K", _i64), ("x", _p), ("y", _p)]
+
+
+_SIGS = {
+    "i2s_status_string": (ctypes.c_char_p, [_int]),
+    "i2s_version": (_int, []),
+    "i2s_device_supported": (_int, []),
+    "i2s_nbytes": (_sz, [_i64, _i64]),
+    "i2s_scale_offset": (_sz, [_i64, _i64]),
+    "i8s_nbytes": (_sz, [_i64]),
+    "i8s_scale_offset": (_sz, [_i64]),
+    "i2s_pack_host": (_int, [_p, _i64, _i64, _f32, _p]),
+    "i8s_pack_host": (_int, [_p, _i64, _f32, _p]),
+    "i2s_quantize_act": (_int, [_p, _i64, _i64, _p, _p, _p, _p]),
+    "i2s_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
+    "i2s_mul_mat": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "i2s_mul_mat_ex": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, ctypes.POINTER(i2s_config), _p]),
+    "i2s_mul_mat_grouped_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
+    "i2s_mul_mat_grouped": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i2s_mul_mat_grouped_quantize": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i2s_mul_mat_grouped_run": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i8s_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
+    "i8s_ws_f32_offset": (_sz, []),
+    "i8s_mul_mat_add_relu": (_int, [_p, _i64, _i64, _p, _i64, _p, _int, _p, _p, _sz, _p]),
+    "i8s_requant_workspace": (_sz, [_i64]),
+    "i8s_requant": (_int, [_p, _i64, _p, _p, _sz, _p]),
+    "i2s_read_status": (_int, [_p, _p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_L, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+lib = _L
+
+
+class I2SError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} ({STATUS.get(status, status)})")
+
+
+def status_string(status: int) -> str:
+    return _L.i2s_status_string(int(status)).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise I2SError(fn, rc)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _dptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _ws(nbytes: int, device):
+    return _torch().empty(max(int(nbytes), 256), dtype=_torch().uint8, device=device)
+
+
+# -- layouts and host packers -------------------------------------------------
+
+def i2s_nbytes(N: int, K: int) -> int:
+    return int(_L.i2s_nbytes(N, K))
+
+
+def i2s_scale_offset(N: int, K: int) -> int:
+    return int(_L.i2s_scale_offset(N, K))
+
+
+def i8s_nbytes(n: int) -> int:
+    return int(_L.i8s_nbytes(n))
+
+
+def i8s_scale_offset(n: int) -> int:
+    return int(_L.i8s_scale_offset(n))
+
+
+def i2s_pack_host(codes: np.ndarray, w_scale: float) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    out = np.zeros(i2s_nbytes(N, K) or 1, dtype=np.uint8)
+    _check("i2s_pack_host", _L.i2s_pack_host(codes.ctypes.data, N, K, float(w_scale), out.ctypes.data))
+    return out
+
+
+def i8s_pack_host(q: np.ndarray, scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8).reshape(-1)
+    out = np.zeros(i8s_nbytes(q.size), dtype=np.uint8)
+    _check("i8s_pack_host", _L.i8s_pack_host(q.ctypes.data, q.size, float(scale), out.ctypes.data))
+    return out
+
+
+# -- device entry points --------------------------------------------------------
+
+def i2s_quantize_act(x):
+    """Per-row quantization of an M x K F32 CUDA tensor -> (q int8, scale, row_sum)."""
+    torch = _torch()
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    s = torch.empty(M, dtype=torch.float32, device=x.device)
+    rs = torch.empty(M, dtype=torch.int32, device=x.device)
+    _check("i2s_quantize_act", _L.i2s_quantize_act(_dptr(x), M, K, _dptr(q), _dptr(s), _dptr(rs), _stream()))
+    return q, s, rs
+
+
+def i2s_mul_mat_workspace(M: int, N: int, K: int) -> int:
+    return int(_L.i2s_mul_mat_workspace(M, N, K))
+
+
+def i2s_mul_mat(w, N: int, K: int, x, y=None, ws=None, path: int = 0, split_k: int = 0):
+    """y (M x N F32) = I2_S weights w (N x K, device bytes) times x (M x K F32)."""
+    torch = _torch()
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _ws(i2s_mul_mat_workspace(M, N, K), x.device)
+    if path or split_k:
+        cfg = i2s_config(path, split_k, 0, 0)
+        rc = _L.i2s_mul_mat_ex(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), ctypes.byref(cfg),
+                               _stream())
+    else:
+        rc = _L.i2s_mul_mat(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), _stream())
+    _check("i2s_mul_mat", rc)
+    return y
+
+
+def _problems(problems: Sequence):
+    arr = (i2s_problem * len(problems))()
+    for i, (w, N, K, x, y) in enumerate(problems):
+        arr[i] = i2s_problem(_dptr(w), N, K, _dptr(x), _dptr(y))
+    return arr
+
+
+def i2s_mul_mat_grouped_workspace(problems: Sequence, M: int) -> int:
+    arr = _problems(problems)
+    return int(_L.i2s_mul_mat_grouped_workspace(arr, len(problems), M))
+
+
+def i2s_mul_mat_grouped(problems: Sequence, M: int, ws=None):
+    """Runs [(w, N, K, x, y), ...] (all with M activation rows) as one group."""
+    arr = _problems(problems)
+    if ws is None:
+        ws = _ws(_L.i2s_mul_mat_grouped_workspace(arr, len(problems), M), problems[0][3].device)
+    _check("i2s_mul_mat_grouped", _L.i2s_mul_mat_grouped(arr, len(problems), M, _dptr(ws), ws.numel(), _stream()))
+    return ws
+
+
+class Group:
+    """A fixed list of projections [(w, N, K, x, y), ...] sharing M activation
+    rows, marshalled once; quantize()/run() are the two phases and __call__
+    runs both. The tensors must stay alive as long as the Group is used."""
+
+    def __init__(self, problems: Sequence, M: int, ws=None):
+        self.problems = list(problems)
+        self.M = int(M)
+        self.arr = _problems(self.problems)
+        need = int(_L.i2s_mul_mat_grouped_workspace(self.arr, len(self.problems), self.M))
+        if need == 0:
+            raise I2SError("i2s_mul_mat_grouped_workspace", -1)
+        self.ws = ws if ws is not None else _ws(need, self.problems[0][3].device)
+
+    def quantize(self):
+        _check("i2s_mul_mat_grouped_quantize",
+               _L.i2s_mul_mat_grouped_quantize(self.arr, len(self.problems), self.M, _dptr(self.ws),
+                                               self.ws.numel(), _stream()))
+
+    def run(self):
+        _check("i2s_mul_mat_grouped_run",
+               _L.i2s_mul_mat_grouped_run(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
+                                          _stream()))
+
+    def __call__(self):
+        _check("i2s_mul_mat_grouped",
+               _L.i2s_mul_mat_grouped(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
+                                      _stream()))
+
+
+def i8s_mul_mat_workspace(M: int, N: int, K: int) -> int:
+    return int(_L.i8s_mul_mat_workspace(M, N, K))
+
+
+def i8s_ws_f32_offset() -> int:
+    return int(_L.i8s_ws_f32_offset())
+
+
+def i8s_mul_mat_add_relu(w, N: int, K: int, x, M: int, bias=None, relu: bool = False, y=None, ws=None):
+    """I8_S y (M x N) = requant(W x^T + bias, ReLU optional); returns (y, ws)."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(i8s_nbytes(M * N), dtype=torch.uint8, device=x.device)
+    if ws is None:
+        ws = _ws(i8s_mul_mat_workspace(M, N, K), x.device)
+    _check("i8s_mul_mat_add_relu",
+           _L.i8s_mul_mat_add_relu(_dptr(w), N, K, _dptr(x), M, _dptr(bias), 1 if relu else 0, _dptr(y), _dptr(ws),
+                                   ws.numel(), _stream()))
+    return y, ws
+
+
+def i8s_ws_f32(ws, M: int, N: int):
+    """View of the F32 output (before requantization) kept in an I8_S workspace."""
+    off = i8s_ws_f32_offset()
+    return ws[off:off + M * N * 4].view(_torch().float32).view(M, N)
+
+
+def i8s_requant(y, dst=None, ws=None):
+    torch = _torch()
+    n = y.numel()
+    if dst is None:
+        dst = torch.empty(i8s_nbytes(n), dtype=torch.uint8, device=y.device)
+    if ws is None:
+        ws = _ws(_L.i8s_requant_workspace(n), y.device)
+    _check("i8s_requant", _L.i8s_requant(_dptr(y), n, _dptr(dst), _dptr(ws), ws.numel(), _stream()))
+    return dst
+
+
+def read_status(ws) -> int:
+    return int(_L.i2s_read_status(_dptr(ws), _stream()))
+
+
+def device_supported() -> int:
+    return int(_L.i2s_device_supported())

@@ -33,20 +33,34 @@ def codes(N: int, K: int, seed: int, p=CODE_P) -> np.ndarray:
     return c
 
 
-def packed_code_bytes(nbytes: int, seed: int, p=CODE_P) -> np.ndarray:
-    """Raw bytes whose four 2-bit fields are i.i.d. codes with probabilities p.
+def packed_code_bytes(nbytes: int, seed: int) -> np.ndarray:
+    """Raw bytes whose four 2-bit fields are i.i.d. codes with P = (0.3, 0.4, 0.3).
 
     Because the codes are i.i.d., the byte distribution does not depend on which
-    field holds which position, so large weight payloads for the benchmark are
-    drawn directly as bytes (one draw per byte from the 81 four-code patterns).
+    field holds which position, so large weight payloads are drawn directly as
+    bytes: each field is a uniform draw r in [0, 10) mapped to (r >= 3) + (r >= 7).
     """
-    pats = np.arange(81)
-    c = np.stack([(pats // 27) % 3, (pats // 9) % 3, (pats // 3) % 3, pats % 3], axis=1)
-    pp = np.asarray(p, dtype=np.float64)
-    prob = pp[c[:, 0]] * pp[c[:, 1]] * pp[c[:, 2]] * pp[c[:, 3]]
-    byte_of = (c[:, 0] << 6) | (c[:, 1] << 4) | (c[:, 2] << 2) | c[:, 3]
-    idx = rng(seed).choice(81, size=int(nbytes), p=prob / prob.sum())
-    return byte_of.astype(np.uint8)[idx]
+    g = rng(seed)
+    out = np.empty(int(nbytes), dtype=np.uint8)
+    chunk = 1 << 24
+    for lo in range(0, int(nbytes), chunk):
+        hi = min(int(nbytes), lo + chunk)
+        r = g.integers(0, 10, size=(hi - lo, 4), dtype=np.uint8)
+        c = (r >= 3).astype(np.uint8) + (r >= 7).astype(np.uint8)
+        out[lo:hi] = (c[:, 0] << 6) | (c[:, 1] << 4) | (c[:, 2] << 2) | c[:, 3]
+    return out
+
+
+def packed_code_bytes_device(nbytes: int, seed: int, device):
+    """The same law as packed_code_bytes, drawn on a CUDA device with torch's
+    generator (used for the benchmark's 327 MB weight set; the draws differ from
+    the numpy ones, the distribution does not)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    r = torch.randint(0, 10, (int(nbytes), 4), dtype=torch.uint8, device=device, generator=g)
+    c = (r >= 3).to(torch.uint8) + (r >= 7).to(torch.uint8)
+    return (c[:, 0] << 6) | (c[:, 1] << 4) | (c[:, 2] << 2) | c[:, 3]
 
 
 def normal_f32(shape, seed: int, std: float = 1.0, outlier_p: float = 0.0,

@@ -1,0 +1,325 @@
+"""GPU path (through the C ABI) against the CPU oracle, bit for bit.
+
+Every float output is compared as raw bits (uint32), every integer output
+exactly: the method is exact up to its final IEEE multiplies, and both sides
+perform those in binary32 round-to-nearest. Shapes span several tiles with
+ragged tails; the full-size workloads are checked on sampled output rows that
+the oracle computes one by one, plus properties that hold at any size.
+"""
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_matmul_gb300 import synth
+from tests import pins
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def i2s():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int8_quantized_matmul_gb300 import build as libbuild
+    libbuild.build()
+    from int8_quantized_matmul_gb300 import i2s as mod
+    assert mod.device_supported() == 1, "the library needs an sm_103 device"
+    return mod
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def same_bits(a, b):
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    if a.dtype == np.float32:
+        a, b = a.view(np.uint32), b.view(np.uint32)
+    bad = np.nonzero(a.reshape(-1) != b.reshape(-1))[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first at {bad[:5]}: {a.reshape(-1)[bad[:5]]} vs {b.reshape(-1)[bad[:5]]}"
+
+
+# ---------------------------------------------------------------------------
+# activation quantizer
+# ---------------------------------------------------------------------------
+
+def test_quantize_act_golden_rows(i2s, o):
+    cases = pins.load_cases("quant_rows.txt")
+    x = np.zeros((len(cases), 128), dtype=np.float32)
+    for i, c in enumerate(cases):
+        x[i, :len(c["x"])] = [float(Fraction(v)) for v in c["x"]]
+    q, s, rs = i2s.i2s_quantize_act(dev(x))
+    q, s, rs = host(q), host(s), host(rs)
+    for i, c in enumerate(cases):
+        n = len(c["q"])
+        assert np.array_equal(q[i, :n], np.array([int(v) for v in c["q"]], np.int8)), c["name"]
+        assert int(rs[i]) == int(c["sum"][0])
+        assert pins.f32_bits(s[i]) == pins.f32_bits(pins.nearest_f32(pins.parse_rational(c["scale"][0])))
+    oq, os_, ors = o.quantize_rows(x)
+    same_bits(q, oq), same_bits(s, os_), same_bits(rs, ors)
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 1152), (8, 8960), (513, 1536)])
+def test_quantize_act_random(i2s, o, M, K):
+    x = synth.normal_f32((M, K), seed=M * 7 + K, outlier_p=0.01)
+    x[M // 2] = 0.0
+    q, s, rs = i2s.i2s_quantize_act(dev(x))
+    oq, os_, ors = o.quantize_rows(x)
+    same_bits(host(q), oq)
+    same_bits(host(s), os_)
+    same_bits(host(rs), ors)
+
+
+# ---------------------------------------------------------------------------
+# I2_S matmul
+# ---------------------------------------------------------------------------
+
+def run_i2s(i2s, o, N, K, M, seed, w_scale=0.05, x=None, **kw):
+    c = synth.codes(N, K, seed=seed)
+    packed = o.i2s_pack(c, w_scale)
+    if x is None:
+        x = synth.normal_f32((M, K), seed=seed + 1, outlier_p=0.01)
+    y = i2s.i2s_mul_mat(dev(packed), N, K, dev(x), **kw)
+    return host(y), o.i2s_mul_mat(packed, N, K, x, nth=4)
+
+
+@pytest.mark.parametrize("K", [128, 1024, 1152])
+@pytest.mark.parametrize("N", [1, 2, 64, 70, 100])
+@pytest.mark.parametrize("M", [1, 3, 8, 16])
+def test_i2s_page_grid(i2s, o, K, N, M):
+    got, want = run_i2s(i2s, o, N, K, M, seed=K * 131 + N * 7 + M)
+    same_bits(got, want)
+
+
+def test_i2s_single_matmul_n256_k1024_m4(i2s, o):
+    # codes P = (.3,.4,.3), w_scale 0.05, x ~ N(0,1), seed 0
+    c = synth.codes(256, 1024, seed=0)
+    packed = o.i2s_pack(c, 0.05)
+    x = synth.normal_f32((4, 1024), seed=0)
+    y = host(i2s.i2s_mul_mat(dev(packed), 256, 1024, dev(x)))
+    same_bits(y, o.i2s_mul_mat(packed, 256, 1024, x))
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 8])
+def test_i2s_split_k_gives_identical_bits(i2s, o, split):
+    got, want = run_i2s(i2s, o, 1100, 1536, 8, seed=77, path=1, split_k=split)
+    same_bits(got, want)
+
+
+@pytest.mark.parametrize("M", [9, 17, 40])
+def test_i2s_gemv_row_slices(i2s, o, M):
+    got, want = run_i2s(i2s, o, 300, 1152, M, seed=M, path=1)
+    same_bits(got, want)
+
+
+def test_i2s_headroom_k8960(i2s, o):
+    # every code 2 and every activation quantizing to +127 (x = 1.0)
+    K, N, M = 8960, 1536, 64
+    packed = o.i2s_pack(np.full((N, K), 2, np.uint8), 0.05)
+    x = np.ones((M, K), np.float32)
+    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x), path=1))
+    small = o.i2s_mul_mat(o.i2s_pack(np.full((4, K), 2, np.uint8), 0.05), 4, K, x[:2])
+    assert (small == small[0, 0]).all()
+    assert (y.view(np.uint32) == small[0, 0].view(np.uint32)).all()
+    act_scale = np.float32(1.0) / np.float32(127.0)
+    assert small[0, 0] == np.float32(127 * K) * (np.float32(0.05) * act_scale)
+
+
+def test_i2s_degenerate(i2s, o):
+    K, N, M = 1024, 70, 4
+    x = synth.normal_f32((M, K), seed=3)
+    x[1] = 0.0
+    got, want = run_i2s(i2s, o, N, K, M, seed=5, x=x)
+    same_bits(got, want)
+    assert (got[1] == 0).all() and not np.isnan(got).any()
+    zero_w = o.i2s_pack(np.ones((N, K), np.uint8), 0.0)
+    y = host(i2s.i2s_mul_mat(dev(zero_w), N, K, dev(x)))
+    assert (y == 0).all() and not np.isnan(y).any()
+
+
+@pytest.mark.parametrize("N", [1, 2, 64, 70, 100])
+def test_i2s_single_group_k128(i2s, o, N):
+    got, want = run_i2s(i2s, o, N, 128, 3, seed=N)
+    same_bits(got, want)
+
+
+def test_i2s_code3_behaves_like_oracle(i2s, o):
+    c = synth.codes(70, 256, seed=9)
+    c[::7, ::5] = 3
+    packed = o.i2s_pack(c, 0.5)
+    x = synth.normal_f32((5, 256), seed=10)
+    same_bits(host(i2s.i2s_mul_mat(dev(packed), 70, 256, dev(x))), o.i2s_mul_mat(packed, 70, 256, x))
+
+
+def layer_problems(o, K_h=1536, K_i=8960, M=1, seed=0, scale_div=1):
+    """One decoder layer's projections with the activations a real layer shares."""
+    shapes = [(n, N // scale_div, K) for n, N, K in synth.QWEN2_1P5B_LAYER]
+    xs = {1536: None}
+    acts = {"attn": synth.normal_f32((M, K_h), seed=seed + 100),
+            "o": synth.normal_f32((M, K_h), seed=seed + 101),
+            "ffn": synth.normal_f32((M, K_h), seed=seed + 102),
+            "down": synth.normal_f32((M, K_i), seed=seed + 103)}
+    which = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "ffn", "up": "ffn", "down": "down"}
+    probs = []
+    for i, (name, N, K) in enumerate(shapes):
+        c = synth.codes(N, K, seed=seed + i)
+        ws = float(synth.uniform_f32(1, seed + 50 + i, 0.01, 0.1)[0])
+        probs.append((name, N, K, o.i2s_pack(c, ws), acts[which[name]], which[name]))
+    del xs
+    return probs, acts
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_i2s_grouped_decoder_layer(i2s, o, M):
+    probs, acts = layer_problems(o, M=M, seed=M)
+    dacts = {k: dev(v) for k, v in acts.items()}
+    dys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _, N, _, _, _, _ in probs]
+    group = [(dev(p[3]), p[1], p[2], dacts[p[5]], y) for p, y in zip(probs, dys)]
+    i2s.i2s_mul_mat_grouped(group, M)
+    for (name, N, K, packed, x, _), y in zip(probs, dys):
+        same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=4))
+
+
+def test_i2s_grouped_under_cuda_graph(i2s, o):
+    probs, acts = layer_problems(o, M=8, seed=3, scale_div=4)
+    dacts = {k: dev(v) for k, v in acts.items()}
+    dys = [torch.zeros((8, N), dtype=torch.float32, device="cuda") for _, N, _, _, _, _ in probs]
+    group = [(dev(p[3]), p[1], p[2], dacts[p[5]], y) for p, y in zip(probs, dys)]
+    ws = torch.empty(i2s.i2s_mul_mat_grouped_workspace(group, 8), dtype=torch.uint8, device="cuda")
+    i2s.i2s_mul_mat_grouped(group, 8, ws=ws)   # warm-up outside capture
+    torch.cuda.synchronize()
+    for y in dys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            i2s.i2s_mul_mat_grouped(group, 8, ws=ws)
+    g.replay()
+    for (name, N, K, packed, x, _), y in zip(probs, dys):
+        same_bits(host(y), o.i2s_mul_mat(packed, N, K, x))
+
+
+def _row_slice(packed, N, K, n0, n1):
+    """I2_S bytes of weight rows n0..n1 (rows are contiguous, K/4 bytes each)."""
+    rb = K // 4
+    return np.concatenate([packed[n0 * rb:n1 * rb], packed[N * rb:N * rb + 32]])
+
+
+def test_i2s_full_decode_set_sampled(i2s, o):
+    """The 28-layer Qwen2-1.5B projection set at M = 8, one grouped launch per
+    layer pair, checked on sampled weight rows of every projection."""
+    M = 8
+    rng = synth.rng(5)
+    for layer in (0, 27):
+        xs = {1536: synth.normal_f32((M, 1536), seed=layer), 8960: synth.normal_f32((M, 8960), seed=layer + 1)}
+        dx = {k: dev(v) for k, v in xs.items()}
+        group, keep = [], []
+        for i, (name, N, K) in enumerate(synth.QWEN2_1P5B_LAYER):
+            payload = synth.packed_code_bytes(N * K // 4, seed=layer * 10 + i)
+            ws = np.float32(synth.uniform_f32(1, layer * 10 + i, 0.01, 0.1)[0])
+            packed = np.concatenate([payload, np.frombuffer(ws.tobytes(), np.uint8), np.zeros(28, np.uint8)])
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            group.append((dev(packed), N, K, dx[K], y))
+            keep.append((name, N, K, packed, y))
+        i2s.i2s_mul_mat_grouped(group, M)
+        for name, N, K, packed, y in keep:
+            yh = host(y)
+            for n0 in sorted(set([0, N - 16] + list(rng.integers(0, N - 16, size=2)))):
+                sub = _row_slice(packed, N, K, n0, n0 + 16)
+                same_bits(yh[:, n0:n0 + 16], o.i2s_mul_mat(sub, 16, K, xs[K]))
+
+
+def test_i2s_lm_head_m1_sampled(i2s, o):
+    N, K, M = 151936, 1536, 1
+    payload = synth.packed_code_bytes(N * K // 4, seed=99)
+    packed = np.concatenate([payload, np.frombuffer(np.float32(0.03).tobytes(), np.uint8), np.zeros(28, np.uint8)])
+    x = synth.normal_f32((M, K), seed=98)
+    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x)))
+    for n0 in (0, 70000, N - 32):
+        same_bits(y[:, n0:n0 + 32], o.i2s_mul_mat(_row_slice(packed, N, K, n0, n0 + 32), 32, K, x))
+
+
+# ---------------------------------------------------------------------------
+# I8_S requant and fused mul_mat_add(_relu)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 31, 4096, 1000003])
+def test_i8s_requant(i2s, o, n):
+    y = synth.normal_f32(n, seed=n, outlier_p=0.01)
+    got = host(i2s.i8s_requant(dev(y)))
+    same_bits(got, o.i8s_quantize(y))
+    z = host(i2s.i8s_requant(dev(np.zeros(n, np.float32))))
+    same_bits(z, o.i8s_quantize(np.zeros(n, np.float32)))
+
+
+def i8s_inputs(o, M, N, K, seed):
+    W = synth.int8_normal((N, K), seed=seed)
+    wp = o.i8s_pack(W, 0.01)
+    xp = o.i8s_quantize(synth.normal_f32((M, K), seed=seed + 1))
+    bias = synth.normal_f32(N, seed=seed + 2, std=0.1)
+    return wp, xp, bias
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 64), (100, 300, 256), (130, 257, 1024), (64, 128, 2048)])
+@pytest.mark.parametrize("relu", [False, True])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_i8s_mul_mat_add(i2s, o, M, N, K, relu, with_bias):
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=M + N + K)
+    b = bias if with_bias else None
+    y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M, bias=dev(b) if b is not None else None, relu=relu)
+    yf = host(i2s.i8s_ws_f32(ws, M, N))
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=b, relu=relu, nth=4)
+    same_bits(yf, oyf)
+    same_bits(host(y8), oy8)
+
+
+def test_i8s_headroom(i2s, o):
+    # every weight and activation at +127: acc = 127*127*K = 132,120,576 (> 2^24)
+    M, N, K = 16, 64, 8192
+    wp = o.i8s_pack(np.full((N, K), 127, np.int8), 0.01)
+    xp = o.i8s_pack(np.full((M, K), 127, np.int8), 0.02)
+    y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M)
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M)
+    same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+    same_bits(host(y8), oy8)
+
+
+@pytest.mark.parametrize("N,K,relu", [(8192, 2048, True), (2048, 8192, False)])
+def test_i8s_encoder_fc_sampled(i2s, o, N, K, relu):
+    """Encoder FC1 (2048 -> 8192, ReLU) / FC2 (8192 -> 2048) at L = 900 frames:
+    sampled rows against the oracle, the requantization checked as a property
+    of the whole output."""
+    M = 900
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=N)
+    y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M, bias=dev(bias), relu=relu)
+    yf = host(i2s.i8s_ws_f32(ws, M, N))
+    q_all, x_scale = o.i8s_unpack(xp, M * K)
+    for m0 in (0, 451, M - 8):
+        sub = o.i8s_pack(q_all.reshape(M, K)[m0:m0 + 8], x_scale)
+        _, oyf = o.i8s_mul_mat_add(wp, N, K, sub, 8, bias=bias, relu=relu, nth=8)
+        same_bits(yf[m0:m0 + 8], oyf)
+    # requant property: one scale = max(max|y|, 1e-5)/127, every q = round(y*127/amax)
+    q, s = o.i8s_unpack(host(y8), M * N)
+    amax = np.float32(max(np.abs(yf).max(), np.float32(1e-5)))
+    assert pins.f32_bits(s) == pins.f32_bits(amax / np.float32(127.0))
+    inv = np.float32(127.0) / amax
+    v = (yf.reshape(-1) * inv).astype(np.float32).astype(np.float64)
+    ref = np.clip(np.floor(np.abs(v) + 0.5) * np.sign(v), -127, 127).astype(np.int8)
+    assert np.array_equal(q, ref)
