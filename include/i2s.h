@@ -240,9 +240,11 @@ int i8s_requant(const float* y, int64_t n, void* dst_i8s, void* ws, size_t ws_by
 /* ---------------------------------------------------------------------------
  * Device status. Kernels with bounded waits (the tensor-core pipelines) never
  * trap: when a wait runs out they record a code in the status word at the
- * start of the workspace and exit. This call synchronizes `stream`, reads and
- * clears that word, and returns I2S_OK or I2S_E_DEVICE_TIMEOUT (or
- * I2S_E_CUDA if the stream reports an error).
+ * start of the workspace and exit. Every i2s_mul_mat* call clears the word in
+ * its first (quantization) launch, so it reflects the latest call on that
+ * workspace. This call synchronizes `stream`, reads and clears that word, and
+ * returns I2S_OK or I2S_E_DEVICE_TIMEOUT (or I2S_E_CUDA if the stream reports
+ * an error).
  * ------------------------------------------------------------------------- */
 int i2s_read_status(void* ws, i2s_stream_t stream);
 

@@ -106,6 +106,9 @@ using namespace i2s;
 #pragma GCC visibility push(default)
 extern "C" {
 
+static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
+                       i2s_stream_t stream, int phases);
+
 const char* i2s_status_string(int status) {
     switch (status) {
         case I2S_OK: return "ok";
@@ -178,6 +181,7 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
     int r = check_device();
     if (r) return r;
     QuantArgs a;
+    a.status = nullptr;
     a.count = 1;
     a.M = (int)M;
     a.layout = kQuantI8Rows;
@@ -201,8 +205,12 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     if (r) return r;
 
     const int path = config ? config->path : 0;
+    if (path < 0 || path > 2) return I2S_E_BAD_ARG;
     const bool use_gemv = path == 1 || (path == 0 && M <= 16);
-    if (!use_gemv) return I2S_E_BAD_ARG;   // tensor-core GEMM: see gemm_tc.cu
+    if (!use_gemv) {
+        i2s_problem p{w_i2s, N, K, x, y};
+        return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
+    }
 
     uint8_t* base = static_cast<uint8_t*>(ws);
     const ActSlot slot = act_slot_at(kHeader, M);
@@ -211,6 +219,7 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     const int Kp = (int)round_up(K, 256);
 
     QuantArgs qa;
+    qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     qa.count = 1;
     qa.M = (int)M;
     qa.layout = kQuantE4M3Frag;
@@ -277,6 +286,75 @@ static int group_acts(const i2s_problem* probs, int count, std::vector<int>& act
     return (int)first.size();
 }
 
+// Tensor-core GEMM path (M > 16): phase 1 quantizes every distinct activation
+// into the f16 operand layout, phase 2 runs one persistent GEMM launch over
+// all problems. Arguments are validated by the callers.
+static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
+                       i2s_stream_t stream, int phases) {
+    std::vector<int> act_of, first;
+    const int n_act = group_acts(probs, count, act_of, first);
+    if (n_act > kTcMaxMaps) return I2S_E_BAD_ARG;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    std::vector<ActSlot> slots(n_act);
+    size_t off = kHeader;
+    for (int a = 0; a < n_act; ++a) {
+        slots[a] = act_slot_at(off, M);
+        off += act_slot_bytes(M, probs[first[a]].K);
+    }
+    int r;
+    if (phases & 1) {
+        static thread_local QuantArgs qa;
+        qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        qa.count = n_act;
+        qa.M = (int)M;
+        qa.layout = kQuantF16Perm;
+        for (int a = 0; a < n_act; ++a) {
+            const i2s_problem& p = probs[first[a]];
+            qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
+                               reinterpret_cast<int32_t*>(base + slots[a].sum_off), (int)p.K, (int)p.K};
+        }
+        r = cuda_status(launch_quant(qa, stream));
+        if (r) return r;
+    }
+    if (phases & 2) {
+        static thread_local TcArgs ta;
+        const int BN = M >= 256 ? 256 : (int)round_up(M, 32);
+        ta.n_maps = n_act;
+        ta.count = count;
+        ta.M = (int)M;
+        ta.BN = BN;
+        ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        for (int a = 0; a < n_act; ++a)
+            if (!make_f16_operand_map(&ta.maps[a], base + slots[a].op_off, (int)M, (int)probs[first[a]].K, BN))
+                return I2S_E_CUDA;
+        const int n_act_tiles = (int)((M + BN - 1) / BN);
+        int tiles = 0;
+        for (int i = 0; i < count; ++i) {
+            const i2s_problem& q = probs[i];
+            const ActSlot& s = slots[act_of[i]];
+            TcProb& p = ta.p[i];
+            p.w = static_cast<const uint8_t*>(q.w_i2s);
+            p.act_scale = reinterpret_cast<const float*>(base + s.scale_off);
+            p.row_sum = reinterpret_cast<const int32_t*>(base + s.sum_off);
+            p.y = q.y;
+            p.N = (int)q.N;
+            p.K = (int)q.K;
+            p.map = act_of[i];
+            p.tile0 = tiles;
+            p.n_act_tiles = n_act_tiles;
+            tiles += (int)((q.N + kTcTileW - 1) / kTcTileW) * n_act_tiles;
+        }
+        ta.total_tiles = tiles;
+        const int sms = device_sm_count();
+        int grid = grid_ctas > 0 ? grid_ctas : sms;
+        if (grid > sms) grid = sms;
+        if (grid > tiles) grid = tiles;
+        r = cuda_status(launch_gemm_tc(ta, grid, stream));
+        if (r) return r;
+    }
+    return I2S_OK;
+}
+
 size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M) {
     if (!probs || count < 1 || count > I2S_MAX_GROUP) return 0;
     std::vector<int> act_of, first;
@@ -303,9 +381,9 @@ static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws
     }
     if (!aligned256(ws)) return I2S_E_MISALIGNED;
     if (ws_bytes < i2s_mul_mat_grouped_workspace(probs, count, M)) return I2S_E_WORKSPACE_TOO_SMALL;
-    if (M > 16) return I2S_E_BAD_ARG;   // grouped tensor-core GEMM: see gemm_tc.cu
     int r = check_device();
     if (r) return r;
+    if (M > 16) return run_gemm_tc(probs, count, M, ws, 0, stream, phases);
 
     std::vector<int> act_of, first;
     const int n_act = group_acts(probs, count, act_of, first);
@@ -318,6 +396,7 @@ static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws
     }
     if (phases & 1) {
         static thread_local QuantArgs qa;
+        qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         qa.count = n_act;
         qa.M = (int)M;
         qa.layout = kQuantE4M3Frag;

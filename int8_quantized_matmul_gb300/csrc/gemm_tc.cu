@@ -1,0 +1,334 @@
+// Prefill GEMM for the I2_S ternary x INT8 matmul (M > 16 activation rows) on
+// the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA)
+// ("ggml-cpu: ternary I2_S matmul kernel", sections Arithmetic and Kernels;
+// "ggml: additive INT8/ternary types ...", "Arithmetic is exact where it can
+// be").
+//
+// sm_103a has no integer tcgen05 MMA, so the exact int32 dot sum_k code*q is
+// formed with kind::f16 and f32 accumulation, exactly:
+//   * a code c in {0,1,2} placed in the low bits of an f16 is the subnormal
+//     c*2^-24, so a shift and a mask turn two packed codes into an f16 pair;
+//   * q in [-127,127] is an exact f16 integer (the quantizer writes it so);
+//   * every product and partial sum is an integer multiple of 2^-24 of
+//     magnitude <= 254*K*2^-24 < 1 for K <= 66052, which binary32 holds
+//     exactly, so dot = D * 2^24 exactly.
+//
+// Roles (one CTA per SM, persistent over a static tile schedule):
+//   warps 0-3  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
+//              (w_scale * act_scale), coalesced F32 stores (warp w reads
+//              TMEM lanes 32w..32w+31 = weight rows of the tile);
+//   warps 4-7  converters: each thread owns one weight row of the 128-row
+//              tile, loads its 16 packed bytes per K block (64 positions),
+//              expands them to 64 f16 in the 128B-swizzled K-major layout and
+//              fences the writes into the async proxy;
+//   warp 8     TMA producer of the activation tile (f16, 128B swizzle);
+//   warp 9     TMEM allocation and the MMA issuer (one lane).
+// MMA: M = 128 weight rows (the "swapped" A operand), N = up to 256
+// activation rows, K = 16 per instruction, 4 instructions per K block. Two
+// TMEM accumulators of 256 columns let the epilogue of one tile overlap the
+// MMAs of the next.
+//
+// K order: the converters emit a K block's 64 positions in the order in which
+// the packed bytes yield them (per 32-bit word: for each bit-pair slice, bytes
+// (0,2) then (1,3)); the quantizer writes the activation operand in the same
+// order (quant.cu, perm_index_of), and a dot product does not depend on the
+// order of its terms.
+//
+// Every wait is bounded: after ~1 s without progress the kernel records a
+// timeout in the status word, lets its own TMA copies land (bounded), waits
+// for its issued MMAs (bounded), frees TMEM and returns.
+
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace i2s {
+
+namespace {
+
+constexpr int kEpiWarps = 4;
+constexpr int kCvtWarps = 4;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreadsTc = 320;
+constexpr int kStagesTc = 4;
+constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
+constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
+constexpr int kATileBytes = kTileW * 128;   // 16 KB
+constexpr int kBTileBytesMax = 256 * 128;   // 32 KB
+constexpr int kTmemCols = 512;
+constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
+
+struct SmemTc {
+    uint64_t full_a[kStagesTc];
+    uint64_t full_b[kStagesTc];
+    uint64_t empty[kStagesTc];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemTcBytes = 1024 + (size_t)kStagesTc * (kATileBytes + kBTileBytesMax) + sizeof(SmemTc);
+
+__device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
+    int lo = 0, hi = a.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.p[mid].tile0 <= tile) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Expands one 32-bit word of packed codes into 8 f16 pairs (two 16-byte
+// chunks): for slices s = 6, 4, 2, 0: (byte0, byte2) then (byte1, byte3).
+__device__ __forceinline__ void expand_word_f16(uint32_t w, uint4& c0, uint4& c1) {
+    constexpr uint32_t m = 0x00030003u;
+    c0.x = (w >> 6) & m;  c0.y = (w >> 14) & m;
+    c0.z = (w >> 4) & m;  c0.w = (w >> 12) & m;
+    c1.x = (w >> 2) & m;  c1.y = (w >> 10) & m;
+    c1.z = w & m;         c1.w = (w >> 8) & m;
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_constant__ TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + (size_t)kStagesTc * kATileBytes;
+    SmemTc& S = *reinterpret_cast<SmemTc*>(sB + (size_t)kStagesTc * kBTileBytesMax);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int BN = a.BN;
+    const uint32_t b_tile_bytes = (uint32_t)BN * 128u;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStagesTc; ++s) {
+            tc::mbar_init(&S.full_a[s], kCvtWarps * 32);
+            tc::mbar_init(&S.full_b[s], 1);
+            tc::mbar_init(&S.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&S.tmem_full[b], 1);
+            tc::mbar_init(&S.tmem_empty[b], kEpiWarps * 32);
+        }
+        tc::mbar_init(&S.mma_done, 1);
+        S.abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(&S.tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == kTmaWarp && lane == 0)
+        for (int i = 0; i < a.n_maps; ++i) tc::tma_prefetch_desc(&a.maps[i]);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = S.tmem_base;
+    volatile int* abort_flag = &S.abort;
+
+    auto fail = [&](uint32_t code) {
+        *abort_flag = 1;
+        atomicOr(a.status, code);
+    };
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool pending[kStagesTc] = {};
+            uint32_t pending_phase[kStagesTc] = {};
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+                const TcProb& P = a.p[find_problem(a, tile)];
+                const int at = (tile - P.tile0) % P.n_act_tiles;
+                const int KB = P.K / kBlockK;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(1); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&S.full_b[stage], b_tile_bytes);
+                    tc::tma_load_2d(sB + (size_t)stage * kBTileBytesMax, &a.maps[P.map], kb * kBlockK, at * BN,
+                                    &S.full_b[stage]);
+                    pending[stage] = true;
+                    pending_phase[stage] = phase;
+                    if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // let this thread's copies in flight land before the CTA exits
+                for (int s = 0; s < kStagesTc; ++s)
+                    if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimit / 8);
+            }
+        }
+    } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
+        // ---------------------------------------------------------- converters
+        const int r = tid - kEpiWarps * 32;   // weight row within the tile
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+            const TcProb& P = a.p[find_problem(a, tile)];
+            const int wt = (tile - P.tile0) / P.n_act_tiles;
+            const int n = wt * kTileW + r;
+            const int KB = P.K / kBlockK;
+            const uint8_t* src = P.w + (size_t)(n < P.N ? n : 0) * (P.K / 4);
+            const bool valid = n < P.N;
+            uint4 cur = valid ? ldg_stream(src) : make_uint4(0, 0, 0, 0);
+            for (int kb = 0; kb < KB; ++kb) {
+                uint4 nxt = make_uint4(0, 0, 0, 0);
+                if (valid && kb + 1 < KB) nxt = ldg_stream(src + (size_t)(kb + 1) * 16);
+                if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(2); ok = false; break; }
+                uint8_t* dst = sA + (size_t)stage * kATileBytes;
+                const uint32_t words[4] = {cur.x, cur.y, cur.z, cur.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint4 c0, c1;
+                    expand_word_f16(words[w], c0, c1);
+                    *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w)) = c0;
+                    *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w + 1)) = c1;
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&S.full_a[stage]);
+                cur = nxt;
+                if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16_f32(kTileW, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+                const TcProb& P = a.p[find_problem(a, tile)];
+                const int KB = P.K / kBlockK;
+                if (!tc::mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimit)) { fail(4); break; }
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit) ||
+                        !tc::mbar_wait(&S.full_b[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kATileBytes));
+                    const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBTileBytesMax));
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 16; ++k)   // +32 bytes per 16-element K step
+                        tc::umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    tc::umma_commit(&S.empty[stage]);
+                    if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::umma_commit(&S.tmem_full[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            tc::umma_commit(&S.mma_done);
+            tc::mbar_wait(&S.mma_done, 0, abort_flag, kWaitLimit / 8);
+        }
+    } else if (warp < kEpiWarps) {
+        // ------------------------------------------------------------ epilogue
+        const int r = warp * 32 + lane;   // TMEM lane = weight row within the tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
+            const TcProb& P = a.p[find_problem(a, tile)];
+            const int local = tile - P.tile0;
+            const int wt = local / P.n_act_tiles, at = local % P.n_act_tiles;
+            const int n = wt * kTileW + r;
+            if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimit)) { fail(16); break; }
+            tc::tc_fence_after();
+            const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
+            const int m_base = at * BN;
+            for (int c = 0; c < (BN + 31) / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256 + c * 32), v);
+                tc::tmem_ld_wait();
+                if (n < P.N) {
+#pragma unroll 8
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m_base + c * 32 + j;
+                        if (c * 32 + j < BN && m < a.M) {
+                            const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
+                            const float sc = __fmul_rn(w_scale, P.act_scale[m]);
+                            P.y[(size_t)m * P.N + n] = __fmul_rn(__int2float_rn(dot - P.row_sum[m]), sc);
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&S.tmem_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load();
+    if (f) return f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f);
+    return f;
+}
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return kSmemTcBytes; }
+
+// 2-D tensor map of an f16 operand of `rows` x `K` (K contiguous), box 64 x box_rows,
+// 128-byte swizzle, zero fill beyond the extents.
+bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    std::memset(map, 0, sizeof(*map));
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s) {
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(k_i2s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTcBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    k_i2s_gemm_tc<<<grid, kThreadsTc, kSmemTcBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace i2s

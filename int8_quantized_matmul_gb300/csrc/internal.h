@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace i2s {
@@ -29,6 +30,7 @@ struct QuantJob {
 };
 
 struct QuantArgs {
+    uint32_t* status;   // if set, cleared by the launch (the matmul that follows reports into it)
     int count;
     int M;
     int layout;
@@ -66,6 +68,43 @@ struct GemvArgs {
 
 int gemv_ctas_for(int N, int split_k);
 cudaError_t launch_gemv(const GemvArgs& a, int total_ctas, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Prefill GEMM (M > 16) on tcgen05 (gemm_tc.cu).
+// ---------------------------------------------------------------------------
+constexpr int kTcMaxMaps = 120;   // distinct activation operands per launch
+constexpr int kTcTileW = 128;     // weight rows per tile
+
+struct TcProb {
+    const uint8_t* w;         // I2_S bytes
+    const float* act_scale;   // M
+    const int32_t* row_sum;   // M
+    float* y;                 // M x N
+    int N;
+    int K;
+    int map;                  // index into TcArgs::maps (the activation operand)
+    int tile0;                // first linear tile of this problem
+    int n_act_tiles;          // ceil(M / BN)
+};
+
+struct TcArgs {
+    CUtensorMap maps[kTcMaxMaps];
+    uint32_t* status;         // workspace status word (timeouts)
+    int n_maps;
+    int count;
+    int M;
+    int BN;                   // activation rows per tile (MMA N), multiple of 32, <= 256
+    int total_tiles;
+    TcProb p[kMaxGroup];
+};
+
+// Kernel parameters are limited to 32764 bytes.
+static_assert(sizeof(TcArgs) <= 32764, "TcArgs exceeds the kernel parameter limit");
+static_assert(sizeof(GemvArgs) <= 32764, "GemvArgs exceeds the kernel parameter limit");
+static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
+
+bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
+cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // I8_S fused matmul (first version: dp4a tiles) and the per-tensor requant.

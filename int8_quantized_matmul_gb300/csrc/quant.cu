@@ -54,6 +54,7 @@ __device__ __forceinline__ int perm_index_of(int pos) {   // pos: group-relative
 __global__ void __launch_bounds__(256) k_quant_rows(const __grid_constant__ QuantArgs a) {
     const int gw = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
+    if (a.status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     if (gw >= a.count * a.M) return;
     const QuantJob& J = a.j[gw / a.M];
     const int m = gw % a.M;

@@ -63,6 +63,28 @@ def packed_code_bytes_device(nbytes: int, seed: int, device):
     return (c[:, 0] << 6) | (c[:, 1] << 4) | (c[:, 2] << 2) | c[:, 3]
 
 
+def normal_f32_device(n: int, seed: int, device, std: float = 1.0, outlier_p: float = 0.0,
+                      outlier_scale: float = 20.0):
+    """N(0, std) F32 drawn on a CUDA device (same law as normal_f32)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(int(n), generator=g, device=device, dtype=torch.float32) * std
+    if outlier_p > 0:
+        mask = torch.rand(int(n), generator=g, device=device) < outlier_p
+        x = torch.where(mask, x * outlier_scale, x)
+    return x
+
+
+def int8_normal_device(n: int, seed: int, device, std: float = 40.0):
+    """int8 drawn as round(N(0, std)) clamped to +-127, on a CUDA device."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn(int(n), generator=g, device=device, dtype=torch.float32) * std
+    return torch.clamp(torch.round(x), -127, 127).to(torch.int8)
+
+
 def normal_f32(shape, seed: int, std: float = 1.0, outlier_p: float = 0.0,
                outlier_scale: float = 20.0) -> np.ndarray:
     g = rng(seed)

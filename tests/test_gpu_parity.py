@@ -257,6 +257,88 @@ def test_i2s_lm_head_m1_sampled(i2s, o):
 
 
 # ---------------------------------------------------------------------------
+# I2_S prefill GEMM (tcgen05)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M", [17, 64, 130, 512])
+@pytest.mark.parametrize("N,K", [(100, 1152), (300, 1536), (257, 128), (128, 8960)])
+def test_i2s_gemm(i2s, o, M, N, K):
+    got, want = run_i2s(i2s, o, N, K, M, seed=M * 3 + N + K)
+    same_bits(got, want)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_i2s_gemm_small_m(i2s, o, M):
+    got, want = run_i2s(i2s, o, 300, 1152, M, seed=M + 11, path=2)
+    same_bits(got, want)
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7, 0])
+def test_i2s_gemm_grid_sizes_give_identical_bits(i2s, o, grid):
+    c = synth.codes(700, 1536, seed=4)
+    packed = o.i2s_pack(c, 0.07)
+    x = synth.normal_f32((300, 1536), seed=5, outlier_p=0.01)
+    y = torch.empty((300, 700), dtype=torch.float32, device="cuda")
+    ws = torch.empty(i2s.i2s_mul_mat_workspace(300, 700, 1536), dtype=torch.uint8, device="cuda")
+    cfg = i2s.i2s_config(2, 0, 0, grid)
+    import ctypes
+    rc = i2s.lib.i2s_mul_mat_ex(dev(packed).data_ptr(), 700, 1536, dev(x).data_ptr(), 300, y.data_ptr(), ws.data_ptr(),
+                                ws.numel(), ctypes.byref(cfg), i2s._stream())
+    assert rc == 0
+    same_bits(host(y), o.i2s_mul_mat(packed, 700, 1536, x, nth=8))
+    assert i2s.read_status(ws) == 0
+
+
+def test_i2s_gemm_headroom_k8960_m64(i2s, o):
+    K, N, M = 8960, 1536, 64
+    packed = o.i2s_pack(np.full((N, K), 2, np.uint8), 0.05)
+    x = np.ones((M, K), np.float32)
+    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x)))   # M = 64 -> tensor-core GEMM
+    small = o.i2s_mul_mat(o.i2s_pack(np.full((4, K), 2, np.uint8), 0.05), 4, K, x[:2])
+    assert (y.view(np.uint32) == small[0, 0].view(np.uint32)).all()
+
+
+def test_i2s_gemm_degenerate(i2s, o):
+    K, N, M = 1024, 70, 40
+    x = synth.normal_f32((M, K), seed=13)
+    x[7] = 0.0
+    got, want = run_i2s(i2s, o, N, K, M, seed=14, x=x)
+    same_bits(got, want)
+    assert (got[7] == 0).all()
+    zero_w = o.i2s_pack(np.ones((N, K), np.uint8), 0.0)
+    y = host(i2s.i2s_mul_mat(dev(zero_w), N, K, dev(x)))
+    assert (y == 0).all() and not np.isnan(y).any()
+
+
+def test_i2s_gemm_prefill_layer_and_lm_head_sampled(i2s, o):
+    """One decoder layer plus the lm_head at M = 512 (pp512 shape, 1% outliers),
+    grouped into one tensor-core launch; sampled weight rows of each projection
+    against the oracle."""
+    M = 512
+    rng = synth.rng(8)
+    xs = {k: synth.normal_f32((M, 1536), seed=20 + k, outlier_p=0.01) for k in range(3)}
+    xs[3] = synth.normal_f32((M, 8960), seed=23, outlier_p=0.01)
+    which = {"q": 0, "k": 0, "v": 0, "o": 1, "gate": 2, "up": 2, "down": 3}
+    dx = {k: dev(v) for k, v in xs.items()}
+    shapes = list(synth.QWEN2_1P5B_LAYER) + [synth.QWEN2_1P5B_LM_HEAD]
+    group, keep = [], []
+    for i, (name, N, K) in enumerate(shapes):
+        payload = synth.packed_code_bytes(N * K // 4, seed=300 + i)
+        ws_ = np.float32(synth.uniform_f32(1, 400 + i, 0.01, 0.1)[0])
+        packed = np.concatenate([payload, np.frombuffer(ws_.tobytes(), np.uint8), np.zeros(28, np.uint8)])
+        a = which.get(name, 2)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        group.append((dev(packed), N, K, dx[a], y))
+        keep.append((name, N, K, packed, y, xs[a]))
+    ws = i2s.i2s_mul_mat_grouped(group, M)
+    assert i2s.read_status(ws) == 0
+    for name, N, K, packed, y, x in keep:
+        yh = host(y)
+        for n0 in sorted(set([0, N - 16] + list(rng.integers(0, N - 16, size=2)))):
+            same_bits(yh[:, n0:n0 + 16], o.i2s_mul_mat(_row_slice(packed, N, K, n0, n0 + 16), 16, K, x, nth=8))
+
+
+# ---------------------------------------------------------------------------
 # I8_S requant and fused mul_mat_add(_relu)
 # ---------------------------------------------------------------------------
 
