@@ -143,7 +143,7 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
  *        stream.
  * Requirements: K % 128 == 0, M >= 1, N >= 1, M*K < 2^31, N*K/4 < 2^31.
  * M <= 16 runs the decode GEMV (weight-bandwidth bound); larger M runs the
- * tensor-core GEMM. Both give identical bits.
+ * GEMM. Both run on the tcgen05 tensor cores and give identical bits.
  * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
  * ------------------------------------------------------------------------- */
 size_t i2s_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
@@ -153,10 +153,11 @@ int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t
 /* Launch-shape overrides for testing and tuning. Every setting gives the same
  * bits; zero fields mean "choose automatically". */
 typedef struct i2s_config {
-    int path;        /* 0 auto, 1 decode GEMV (any M, in slices of 16 rows), 2 tensor-core GEMM */
+    int path;        /* 0 auto (M <= 16: 3, else 2); 1 warp-MMA GEMV (any M, in slices of 16
+                        rows); 2 tensor-core GEMM; 3 tensor-core GEMV (M <= 16) */
     int split_k;     /* GEMV: CTAs sharing one row block along K (1, 2, 4, 8) */
     int rows_per_cta;/* GEMV: weight rows per CTA tile (multiple of 16) */
-    int grid_ctas;   /* GEMM: persistent CTA count (<= SM count) */
+    int grid_ctas;   /* paths 2 and 3: persistent CTA count (<= SM count, 2x for path 3) */
 } i2s_config;
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,

@@ -62,9 +62,17 @@ struct ActSlot {
     size_t scale_off, sum_off, op_off;
 };
 
+// Operand rows of the tensor-core GEMV's e4m3 operand per half (hi / lo).
+int64_t gemv_tc_rows(int64_t M) { return M <= 8 ? 8 : 16; }
+
 size_t act_slot_bytes(int64_t M, int64_t K) {
     const int64_t Kp = round_up(K, 256);
-    return align_up((size_t)M * 4) * 2 + align_up((size_t)M * (size_t)Kp * 2);
+    size_t op = (size_t)M * (size_t)Kp * 2;                      // GEMV records / GEMM f16 rows
+    if (M <= 16) {
+        const size_t tc = (size_t)(2 * gemv_tc_rows(M)) * (size_t)K;   // GEMV tensor-core operand
+        if (tc > op) op = tc;
+    }
+    return align_up((size_t)M * 4) * 2 + align_up(op);
 }
 
 ActSlot act_slot_at(size_t base, int64_t M) {
@@ -107,6 +115,8 @@ using namespace i2s;
 extern "C" {
 
 static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
+                       i2s_stream_t stream, int phases);
+static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
                        i2s_stream_t stream, int phases);
 
 const char* i2s_status_string(int status) {
@@ -182,17 +192,27 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
     if (r) return r;
     QuantArgs a;
     a.status = nullptr;
+    a.zero = nullptr;
+    a.zero_16 = 0;
     a.count = 1;
     a.M = (int)M;
+    a.rows = (int)M;
     a.layout = kQuantI8Rows;
     a.j[0] = QuantJob{x, q, act_scale, row_sum, (int)K, (int)K};
     return cuda_status(launch_quant(a, stream));
 }
 
+// Split-K partial area of one problem: M x N int32 partial dots and one chunk
+// counter per 128-row tile (also large enough for the warp-MMA GEMV's
+// 512-row tiles).
+static size_t split_area_bytes(int64_t M, int64_t N) {
+    const size_t tiles = (size_t)((N + kTcTileW - 1) / kTcTileW);
+    return align_up((size_t)M * (size_t)N * 4) + align_up(tiles * 4);
+}
+
 size_t i2s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (!i2s_shape_ok(N, K, M)) return 0;
-    const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
-    return kHeader + act_slot_bytes(M, K) + align_up((size_t)M * (size_t)N * 4) + align_up(tiles * 4);
+    return kHeader + act_slot_bytes(M, K) + split_area_bytes(M, N);
 }
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
@@ -205,11 +225,15 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     if (r) return r;
 
     const int path = config ? config->path : 0;
-    if (path < 0 || path > 2) return I2S_E_BAD_ARG;
-    const bool use_gemv = path == 1 || (path == 0 && M <= 16);
-    if (!use_gemv) {
+    if (path < 0 || path > 3) return I2S_E_BAD_ARG;
+    if (path == 3 && M > 16) return I2S_E_BAD_ARG;
+    if (path == 2 || (path == 0 && M > 16)) {
         i2s_problem p{w_i2s, N, K, x, y};
         return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
+    }
+    if (path == 3 || path == 0) {
+        i2s_problem p{w_i2s, N, K, x, y};
+        return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
     }
 
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -220,8 +244,11 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
 
     QuantArgs qa;
     qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+    qa.zero = nullptr;
+    qa.zero_16 = 0;
     qa.count = 1;
     qa.M = (int)M;
+    qa.rows = (int)M;
     qa.layout = kQuantE4M3Frag;
     qa.j[0] = QuantJob{x, base + slot.op_off, reinterpret_cast<float*>(base + slot.scale_off),
                        reinterpret_cast<int32_t*>(base + slot.sum_off), (int)K, Kp};
@@ -305,8 +332,11 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     if (phases & 1) {
         static thread_local QuantArgs qa;
         qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        qa.zero = nullptr;
+        qa.zero_16 = 0;
         qa.count = n_act;
         qa.M = (int)M;
+        qa.rows = (int)M;
         qa.layout = kQuantF16Perm;
         for (int a = 0; a < n_act; ++a) {
             const i2s_problem& p = probs[first[a]];
@@ -355,6 +385,99 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     return I2S_OK;
 }
 
+// Tensor-core GEMV path (M <= 16): phase 1 quantizes every distinct activation
+// into the e4m3 hi/lo operand rows, phase 2 runs one persistent launch over all
+// problems (two CTAs per SM). Arguments are validated by the callers.
+static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
+                       i2s_stream_t stream, int phases) {
+    std::vector<int> act_of, first;
+    const int n_act = group_acts(probs, count, act_of, first);
+    if (n_act > kTcMaxMaps) return I2S_E_BAD_ARG;
+    const int Mp = (int)gemv_tc_rows(M);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    std::vector<ActSlot> slots(n_act);
+    size_t off = kHeader;
+    for (int a = 0; a < n_act; ++a) {
+        slots[a] = act_slot_at(off, M);
+        off += act_slot_bytes(M, probs[first[a]].K);
+    }
+    int r;
+    // split-K partial dots and chunk counters (problems with K above one chunk)
+    size_t dots = 0, tickets = 0;
+    for (int i = 0; i < count; ++i)
+        if (probs[i].K > kGemvChunkPositions) {
+            dots += (size_t)M * (size_t)probs[i].N;
+            tickets += (size_t)((probs[i].N + kTcTileW - 1) / kTcTileW);
+        }
+    const size_t dot_off_bytes = off;
+    const size_t ticket_off_bytes = off + align_up(dots * 4);
+    const size_t split_bytes = align_up(dots * 4) + align_up(tickets * 4);
+    if (phases & 1) {
+        static thread_local QuantArgs qa;
+        qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        qa.zero = split_bytes ? reinterpret_cast<uint4*>(base + dot_off_bytes) : nullptr;
+        qa.zero_16 = split_bytes / 16;
+        qa.count = n_act;
+        qa.M = (int)M;
+        qa.rows = Mp;
+        qa.layout = kQuantE4M3Tc;
+        for (int a = 0; a < n_act; ++a) {
+            const i2s_problem& p = probs[first[a]];
+            qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
+                               reinterpret_cast<int32_t*>(base + slots[a].sum_off), (int)p.K, (int)p.K};
+        }
+        r = cuda_status(launch_quant(qa, stream));
+        if (r) return r;
+    }
+    if (phases & 2) {
+        static thread_local TcArgs ta;
+        ta.n_maps = n_act;
+        ta.count = count;
+        ta.M = (int)M;
+        ta.BN = Mp;
+        ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        for (int a = 0; a < n_act; ++a)
+            if (!make_e4m3_operand_map(&ta.maps[a], base + slots[a].op_off, 2 * Mp, (int)probs[first[a]].K))
+                return I2S_E_CUDA;
+        ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off_bytes);
+        ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off_bytes);
+        int units = 0, dot_elems = 0, ticket_elems = 0;
+        for (int i = 0; i < count; ++i) {
+            const i2s_problem& q = probs[i];
+            const ActSlot& s = slots[act_of[i]];
+            TcProb& p = ta.p[i];
+            const int row_tiles = (int)((q.N + kTcTileW - 1) / kTcTileW);
+            const int chunks = (int)((q.K + kGemvChunkPositions - 1) / kGemvChunkPositions);
+            p.w = static_cast<const uint8_t*>(q.w_i2s);
+            p.act_scale = reinterpret_cast<const float*>(base + s.scale_off);
+            p.row_sum = reinterpret_cast<const int32_t*>(base + s.sum_off);
+            p.y = q.y;
+            p.N = (int)q.N;
+            p.K = (int)q.K;
+            p.map = act_of[i];
+            p.tile0 = units;
+            p.n_act_tiles = 1;
+            p.chunks = chunks;
+            p.dot_off = dot_elems;
+            p.ticket_off = ticket_elems;
+            if (chunks > 1) {
+                dot_elems += (int)(M * q.N);
+                ticket_elems += row_tiles;
+            }
+            units += row_tiles * chunks;
+        }
+        ta.total_tiles = units;
+        const int tiles = units;
+        const int cap = 2 * device_sm_count();
+        int grid = grid_ctas > 0 ? grid_ctas : cap;
+        if (grid > cap) grid = cap;
+        if (grid > tiles) grid = tiles;
+        r = cuda_status(launch_gemv_tc(ta, grid, stream));
+        if (r) return r;
+    }
+    return I2S_OK;
+}
+
 size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M) {
     if (!probs || count < 1 || count > I2S_MAX_GROUP) return 0;
     std::vector<int> act_of, first;
@@ -364,11 +487,23 @@ size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_
         if (!i2s_shape_ok(probs[a].N, probs[a].K, M)) return 0;
         total += act_slot_bytes(M, probs[a].K);
     }
+    if (M <= 16) {   // split-K partials of the tensor-core GEMV
+        size_t dots = 0, tickets = 0;
+        for (int i = 0; i < count; ++i) {
+            if (!i2s_shape_ok(probs[i].N, probs[i].K, M)) return 0;
+            if (probs[i].K > kGemvChunkPositions) {
+                dots += (size_t)M * (size_t)probs[i].N;
+                tickets += (size_t)((probs[i].N + kTcTileW - 1) / kTcTileW);
+            }
+        }
+        total += align_up(dots * 4) + align_up(tickets * 4);
+    }
     return total;
 }
 
 // Phase bits of a grouped call: 1 = quantize the distinct activations into
-// the workspace, 2 = run the matmuls from the workspace.
+// the workspace, 2 = run the matmuls from the workspace. M <= 16 runs the
+// tensor-core GEMV, larger M the tensor-core GEMM.
 static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
                         i2s_stream_t stream, int phases) {
     if (!probs || !ws) return I2S_E_NULL_PTR;
@@ -384,57 +519,7 @@ static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws
     int r = check_device();
     if (r) return r;
     if (M > 16) return run_gemm_tc(probs, count, M, ws, 0, stream, phases);
-
-    std::vector<int> act_of, first;
-    const int n_act = group_acts(probs, count, act_of, first);
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    std::vector<ActSlot> slots(n_act);
-    size_t off = kHeader;
-    for (int a = 0; a < n_act; ++a) {
-        slots[a] = act_slot_at(off, M);
-        off += act_slot_bytes(M, probs[first[a]].K);
-    }
-    if (phases & 1) {
-        static thread_local QuantArgs qa;
-        qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
-        qa.count = n_act;
-        qa.M = (int)M;
-        qa.layout = kQuantE4M3Frag;
-        for (int a = 0; a < n_act; ++a) {
-            const i2s_problem& p = probs[first[a]];
-            qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
-                               reinterpret_cast<int32_t*>(base + slots[a].sum_off), (int)p.K,
-                               (int)round_up(p.K, 256)};
-        }
-        r = cuda_status(launch_quant(qa, stream));
-        if (r) return r;
-    }
-    if (phases & 2) {
-        static thread_local GemvArgs ga;
-        ga.count = count;
-        ga.M = (int)M;
-        ga.split_k = 1;
-        int ctas = 0;
-        for (int i = 0; i < count; ++i) {
-            const i2s_problem& q = probs[i];
-            const ActSlot& s = slots[act_of[i]];
-            GemvProb& p = ga.p[i];
-            p.w = static_cast<const uint8_t*>(q.w_i2s);
-            p.act = reinterpret_cast<const uint32_t*>(base + s.op_off);
-            p.act_scale = reinterpret_cast<const float*>(base + s.scale_off);
-            p.row_sum = reinterpret_cast<const int32_t*>(base + s.sum_off);
-            p.y = q.y;
-            p.dot_acc = nullptr;
-            p.tickets = nullptr;
-            p.N = (int)q.N;
-            p.K = (int)q.K;
-            p.tile0 = ctas;
-            ctas += gemv_ctas_for((int)q.N, 1);
-        }
-        r = cuda_status(launch_gemv(ga, ctas, stream));
-        if (r) return r;
-    }
-    return I2S_OK;
+    return run_gemv_tc(probs, count, M, ws, 0, stream, phases);
 }
 
 int i2s_mul_mat_grouped(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,

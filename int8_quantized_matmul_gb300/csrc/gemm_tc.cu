@@ -316,6 +316,21 @@ bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D tensor map of the GEMV's e4m3 operand: `rows` x `K` bytes (K contiguous),
+// box 128 x rows (one K block of every operand row), 128-byte swizzle.
+bool make_e4m3_operand_map(CUtensorMap* map, const void* base, int rows, int K) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    std::memset(map, 0, sizeof(*map));
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {128u, (cuuint32_t)rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s) {
     static std::atomic<uint64_t> configured{0};
     int dev = 0;

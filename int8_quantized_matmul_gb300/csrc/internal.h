@@ -18,6 +18,7 @@ enum QuantLayout : int {
     kQuantI8Rows = 0,    // plain int8, row-major M x K (the public sidecar)
     kQuantE4M3Frag = 1,  // GEMV operand records (see gemv.cu), 2*Kp bytes per row
     kQuantF16Perm = 2,   // tensor-core GEMM operand: f16, K permuted per 128-group
+    kQuantE4M3Tc = 3,    // tensor-core GEMV operand: e4m3 hi rows then lo rows (2*M' x K)
 };
 
 struct QuantJob {
@@ -31,8 +32,11 @@ struct QuantJob {
 
 struct QuantArgs {
     uint32_t* status;   // if set, cleared by the launch (the matmul that follows reports into it)
+    uint4* zero;        // if set, zero_16 16-byte words zeroed by the launch (split-K partials)
+    unsigned long long zero_16;
     int count;
     int M;
+    int rows;           // rows written per job: M, or M' (8 or 16) for kQuantE4M3Tc
     int layout;
     QuantJob j[kMaxGroup];
 };
@@ -83,20 +87,29 @@ struct TcProb {
     int N;
     int K;
     int map;                  // index into TcArgs::maps (the activation operand)
-    int tile0;                // first linear tile of this problem
-    int n_act_tiles;          // ceil(M / BN)
+    int tile0;                // GEMM: first linear tile; GEMV: first linear work unit
+    int n_act_tiles;          // GEMM: ceil(M / BN)
+    int chunks;               // GEMV: K chunks per row tile (work units per tile)
+    int dot_off;              // GEMV, chunks > 1: offset (elements) of this problem's M x N partial dots
+    int ticket_off;           // GEMV, chunks > 1: offset of this problem's per-tile chunk counters
 };
 
 struct TcArgs {
     CUtensorMap maps[kTcMaxMaps];
     uint32_t* status;         // workspace status word (timeouts)
+    int32_t* dot_base;        // GEMV split-K partial dots (zeroed by the quantize launch)
+    uint32_t* ticket_base;    // GEMV split-K chunk counters (zeroed by the quantize launch)
     int n_maps;
     int count;
     int M;
-    int BN;                   // activation rows per tile (MMA N), multiple of 32, <= 256
-    int total_tiles;
+    int BN;                   // GEMM: activation rows per tile (MMA N, multiple of 32, <= 256);
+                              // GEMV: operand rows per half M' (8 or 16), MMA N = 2M'
+
+    int total_tiles;          // GEMM: tiles; GEMV: work units
     TcProb p[kMaxGroup];
 };
+
+constexpr int kGemvChunkPositions = 1536;   // K positions per GEMV work unit
 
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(TcArgs) <= 32764, "TcArgs exceeds the kernel parameter limit");
@@ -104,7 +117,9 @@ static_assert(sizeof(GemvArgs) <= 32764, "GemvArgs exceeds the kernel parameter 
 static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
 
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
+bool make_e4m3_operand_map(CUtensorMap* map, const void* base, int rows, int K);
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // I8_S fused matmul (first version: dp4a tiles) and the per-tensor requant.

@@ -3,9 +3,9 @@
 // the 1e-5 amax floor; "Experiment - int8 W8A8 path", section Implementation
 // for scale = amax/127, inv = 127/amax, round, clamp to +-127).
 //
-// One warp per row: a shuffle reduction finds the row's absmax, then the row
-// is read again (L1/L2 hit) and quantized. The int8 row sum is reduced the same
-// way. Besides the plain int8 layout of the public sidecar, the kernel can
+// One CTA per row: the row is read once into registers, a block reduction
+// finds its absmax, and the quantized values and their int8 sum (reduced the
+// same way) are written out. Besides the plain int8 layout of the public sidecar, the kernel can
 // write the operand layouts of the two matmul kernels directly, so no separate
 // repacking pass is needed:
 //   kQuantE4M3Frag  the decode GEMV's B operand: each q is split exactly into
@@ -51,82 +51,138 @@ __device__ __forceinline__ int perm_index_of(int pos) {   // pos: group-relative
     return 16 * w + 4 * s + j;
 }
 
-__global__ void __launch_bounds__(256) k_quant_rows(const __grid_constant__ QuantArgs a) {
-    const int gw = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (a.status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
-    if (gw >= a.count * a.M) return;
-    const QuantJob& J = a.j[gw / a.M];
-    const int m = gw % a.M;
+// Position (within its 128-group) of the e4m3 element at index e of the
+// tensor-core GEMV operand: TMEM column 4w + i of a K block holds the codes of
+// group bytes 4w..4w+3 at bit-pair slice i, i.e. positions 32i + 4w + 0..3.
+// Returns the element index of group-relative position p (p % 4 == 0 keeps
+// the four elements of a word together).
+__device__ __forceinline__ int e4m3_tc_index(int p) {
+    return 16 * ((p & 31) >> 2) + 4 * (p >> 5) + (p & 3);
+}
+
+// Writes the four quantized values of positions 4c..4c+3 of row m in the
+// requested operand layout.
+__device__ __forceinline__ void emit4(const QuantArgs& a, const QuantJob& J, int m, int c, const int (&q)[4]) {
     const int K = J.K;
+    if (a.layout == kQuantI8Rows) {
+        uint32_t* q4 = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(J.out) + (size_t)m * K);
+        q4[c] = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
+                ((uint32_t)(q[3] & 0xff) << 24);
+    } else if (a.layout == kQuantE4M3Frag) {
+        uint32_t* rec = static_cast<uint32_t*>(J.out) + (size_t)m * (J.Kp / 2);
+        uint32_t hi = 0, lo = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hi |= (uint32_t)e4m3_times16(q[e] >> 4) << (8 * e);
+            lo |= (uint32_t)e4m3_small_int(q[e] & 15) << (8 * e);
+        }
+        const int wi = frag_word(4 * c);
+        rec[wi] = hi;
+        rec[wi + 2] = lo;
+    } else if (a.layout == kQuantE4M3Tc) {
+        uint32_t* hi = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)m * K);
+        uint32_t* lo = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)(a.rows + m) * K);
+        uint32_t h = 0, l = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            h |= (uint32_t)e4m3_times16(q[e] >> 4) << (8 * e);
+            l |= (uint32_t)e4m3_small_int(q[e] & 15) << (8 * e);
+        }
+        const int p = 4 * c;
+        const int word = ((p & ~127) + e4m3_tc_index(p & 127)) >> 2;
+        hi[word] = h;
+        lo[word] = l;
+    } else {   // kQuantF16Perm
+        __half* out = static_cast<__half*>(J.out) + (size_t)m * K;
+        const int pos0 = 4 * c;
+        const int group_base = pos0 & ~127;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) out[group_base + perm_index_of((pos0 + e) & 127)] = __int2half_rn(q[e]);
+    }
+}
+
+constexpr int kQThreads = 256;
+constexpr int kQCache = 12;   // float4 per thread kept in registers (rows up to 12288 values)
+
+// One CTA per row: the row is loaded once (kept in registers), its absmax and
+// int8 sum are reduced across the block, and the quantized values are written
+// in the requested layout.
+__global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant__ QuantArgs a) {
+    __shared__ float s_red[kQThreads / 32];
+    __shared__ int s_sum[kQThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
+    for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
+         i += (unsigned long long)gridDim.x * kQThreads)
+        a.zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    const QuantJob& J = a.j[blockIdx.x / a.rows];
+    const int m = blockIdx.x % a.rows;
+    const int K = J.K, K4 = K / 4;
+    if (m >= a.M) {
+        // padding operand rows (kQuantE4M3Tc only): zero hi and lo rows
+        uint32_t* hi = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)m * K);
+        uint32_t* lo = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)(a.rows + m) * K);
+        for (int c = tid; c < K4; c += kQThreads) { hi[c] = 0u; lo[c] = 0u; }
+        return;
+    }
     const float4* x4 = reinterpret_cast<const float4*>(J.x + (size_t)m * K);
 
+    float4 cache[kQCache];
     float amax = 0.0f;
-    for (int c = lane; c < K / 4; c += 32) {
+#pragma unroll
+    for (int i = 0; i < kQCache; ++i) {
+        const int c = tid + i * kQThreads;
+        cache[i] = c < K4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(cache[i].x), fabsf(cache[i].y)), fmaxf(fabsf(cache[i].z), fabsf(cache[i].w))));
+    }
+    for (int c = tid + kQCache * kQThreads; c < K4; c += kQThreads) {   // rows longer than the cache
         const float4 v = x4[c];
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
     amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    amax = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
     float scale, inv;
     quant_params(amax, scale, inv);
 
     int sum = 0;
-    if (a.layout == kQuantI8Rows) {
-        uint32_t* q4 = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(J.out) + (size_t)m * K);
-        for (int c = lane; c < K / 4; c += 32) {
-            const float4 v = x4[c];
-            const int q0 = quantize_one(v.x, inv), q1 = quantize_one(v.y, inv);
-            const int q2 = quantize_one(v.z, inv), q3 = quantize_one(v.w, inv);
-            sum += q0 + q1 + q2 + q3;
-            q4[c] = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
-                    ((uint32_t)(q3 & 0xff) << 24);
-        }
-    } else if (a.layout == kQuantE4M3Frag) {
-        uint32_t* rec = static_cast<uint32_t*>(J.out) + (size_t)m * (J.Kp / 2);
-        for (int c = lane; c < J.Kp / 4; c += 32) {
-            int q[4] = {0, 0, 0, 0};
-            if (4 * c < K) {
-                const float4 v = x4[c];
-                q[0] = quantize_one(v.x, inv); q[1] = quantize_one(v.y, inv);
-                q[2] = quantize_one(v.z, inv); q[3] = quantize_one(v.w, inv);
-            }
-            uint32_t hi = 0, lo = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sum += q[e];
-                hi |= (uint32_t)e4m3_times16(q[e] >> 4) << (8 * e);
-                lo |= (uint32_t)e4m3_small_int(q[e] & 15) << (8 * e);
-            }
-            const int wi = frag_word(4 * c);
-            rec[wi] = hi;
-            rec[wi + 2] = lo;
-        }
-    } else {   // kQuantF16Perm
-        __half* out = static_cast<__half*>(J.out) + (size_t)m * K;
-        for (int c = lane; c < K / 4; c += 32) {
-            const float4 v = x4[c];
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-            const int pos0 = 4 * c;
-            const int group_base = pos0 & ~127;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = quantize_one(vv[e], inv);
-                sum += q;
-                out[group_base + perm_index_of((pos0 + e) & 127)] = __int2half_rn(q);
-            }
+    for (int i = 0; i < kQCache; ++i) {
+        const int c = tid + i * kQThreads;
+        if (c < K4) {
+            const int q[4] = {quantize_one(cache[i].x, inv), quantize_one(cache[i].y, inv),
+                              quantize_one(cache[i].z, inv), quantize_one(cache[i].w, inv)};
+            sum += q[0] + q[1] + q[2] + q[3];
+            emit4(a, J, m, c, q);
         }
     }
+    for (int c = tid + kQCache * kQThreads; c < K4; c += kQThreads) {
+        const float4 v = x4[c];
+        const int q[4] = {quantize_one(v.x, inv), quantize_one(v.y, inv), quantize_one(v.z, inv), quantize_one(v.w, inv)};
+        sum += q[0] + q[1] + q[2] + q[3];
+        emit4(a, J, m, c, q);
+    }
+    if (a.layout == kQuantE4M3Frag) {   // zero records of the padding positions K..Kp-1
+        const int zero[4] = {0, 0, 0, 0};
+        for (int c = K4 + tid; c < J.Kp / 4; c += kQThreads) emit4(a, J, m, c, zero);
+    }
     sum = warp_sum(sum);
-    if (lane == 0) {
+    if (lane == 0) s_sum[warp] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kQThreads / 32; ++w) total += s_sum[w];
         J.scale[m] = scale;
-        J.sum[m] = sum;
+        J.sum[m] = total;
     }
 }
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
-    const int warps = a.count * a.M;
-    const int blocks = (warps + 7) / 8;
-    k_quant_rows<<<blocks, 256, 0, s>>>(a);
+    k_quant_rows<<<a.count * a.rows, kQThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

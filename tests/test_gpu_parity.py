@@ -116,6 +116,40 @@ def test_i2s_single_matmul_n256_k1024_m4(i2s, o):
     same_bits(y, o.i2s_mul_mat(packed, 256, 1024, x))
 
 
+@pytest.mark.parametrize("M", [1, 2, 8, 9, 16])
+@pytest.mark.parametrize("grid", [1, 5, 7, 0])
+@pytest.mark.parametrize("K", [1152, 4608, 8960])
+def test_i2s_gemv_tc_grid_sizes(i2s, o, M, grid, K):
+    # CTA counts that cut row tiles into K-chunk segments at different places
+    # (split-K partials combined by integer atomics) give identical bits
+    import ctypes
+    N = 900
+    c = synth.codes(N, K, seed=M + K)
+    packed = o.i2s_pack(c, 0.07)
+    x = synth.normal_f32((M, K), seed=M + 1, outlier_p=0.01)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(i2s.i2s_mul_mat_workspace(M, N, K), dtype=torch.uint8, device="cuda")
+    cfg = i2s.i2s_config(3, 0, 0, grid)
+    wd, xd = dev(packed), dev(x)   # keep the device buffers alive across the call
+    for _ in range(2):   # twice: the partial buffers are re-zeroed by each call
+        rc = i2s.lib.i2s_mul_mat_ex(wd.data_ptr(), N, K, xd.data_ptr(), M, y.data_ptr(), ws.data_ptr(),
+                                    ws.numel(), ctypes.byref(cfg), i2s._stream())
+        assert rc == 0
+        same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=8))
+        assert i2s.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_i2s_gemv_paths_agree(i2s, o, M):
+    # the warp-MMA GEMV (path 1), the tensor-core GEMV (3) and GEMM (2) give the same bits
+    c = synth.codes(300, 1536, seed=60 + M)
+    packed = o.i2s_pack(c, 0.02)
+    x = synth.normal_f32((M, 1536), seed=61 + M)
+    want = o.i2s_mul_mat(packed, 300, 1536, x)
+    for path in (1, 2, 3):
+        same_bits(host(i2s.i2s_mul_mat(dev(packed), 300, 1536, dev(x), path=path)), want)
+
+
 @pytest.mark.parametrize("split", [1, 2, 3, 4, 8])
 def test_i2s_split_k_gives_identical_bits(i2s, o, split):
     got, want = run_i2s(i2s, o, 1100, 1536, 8, seed=77, path=1, split_k=split)
@@ -282,7 +316,8 @@ def test_i2s_gemm_grid_sizes_give_identical_bits(i2s, o, grid):
     ws = torch.empty(i2s.i2s_mul_mat_workspace(300, 700, 1536), dtype=torch.uint8, device="cuda")
     cfg = i2s.i2s_config(2, 0, 0, grid)
     import ctypes
-    rc = i2s.lib.i2s_mul_mat_ex(dev(packed).data_ptr(), 700, 1536, dev(x).data_ptr(), 300, y.data_ptr(), ws.data_ptr(),
+    wd, xd = dev(packed), dev(x)   # keep the device buffers alive across the call
+    rc = i2s.lib.i2s_mul_mat_ex(wd.data_ptr(), 700, 1536, xd.data_ptr(), 300, y.data_ptr(), ws.data_ptr(),
                                 ws.numel(), ctypes.byref(cfg), i2s._stream())
     assert rc == 0
     same_bits(host(y), o.i2s_mul_mat(packed, 700, 1536, x, nth=8))
