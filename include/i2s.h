@@ -164,6 +164,46 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
                    void* ws, size_t ws_bytes, const i2s_config* config, i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode I2_S matmul without a workspace. The pages have no counterpart of
+ * this call: ggml always hands its kernels a work buffer (params->wdata). It
+ * exists for callers that cannot provide device scratch memory: a plain C or
+ * ctypes host with no device allocator of its own, or a serving loop that
+ * must not allocate once it runs, because cudaMalloc and cudaFree can
+ * synchronize the device and a fixed memory budget leaves no room for
+ * per-call buffers. Such a caller passes only the weights, the activations
+ * and the output; the call itself allocates no memory.
+ *
+ * Same operation, arguments, requirements and bits as i2s_mul_mat on the
+ * tensor-core GEMV path, limited to 1 <= M <= 16 (BAD_SHAPE otherwise). The
+ * scratch is a fixed array of I2S_NOALLOC_SCRATCH_BYTES inside the library's
+ * device code, one per device. A problem needs 768 + up256(2*Mp*K) bytes of
+ * it (Mp = 8 for M <= 8, else 16) plus, when K > 1536, up256(4*M*N) +
+ * up256(4*ceil(N/128)), where up256 rounds up to a multiple of 256. A problem
+ * that needs more is rejected with WORKSPACE_TOO_SMALL before anything is
+ * enqueued. Every decode projection of a 1.5B-parameter decoder (K, N up to
+ * 8960, a 151936-row output head at K = 1536) fits.
+ *
+ * Set-up: the first call made with a device current loads the array on that
+ * device and looks up its address. Make that first call (for example one
+ * warm-up call) before capturing any stream, and before the point from which
+ * the caller cannot tolerate set-up work.
+ * Races: every call on a device uses the same array, so calls whose work can
+ * overlap on the GPU race and give wrong results. Order all calls on one
+ * device, for example on a single stream.
+ * Contents: the array keeps what the previous call left in it. Each call
+ * clears what must start at zero (the status word, the split-K partial sums
+ * and their counters) in its first launch, so callers never clear it.
+ * Device waits that run out are recorded in the array's status word, which
+ * this call cannot return; the return value reports validation and launch
+ * errors only.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL,
+ * UNSUPPORTED_DEVICE, CUDA.
+ * ------------------------------------------------------------------------- */
+#define I2S_NOALLOC_SCRATCH_BYTES 4194304
+int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,
+                        i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Grouped I2_S matmul: several independent projections with the same number of
  * activation rows M, run as one quantization launch plus one GEMV/GEMM launch
  * (the per-layer q/k/v/o/gate/up/down set of a decoder, or many layers).

@@ -57,6 +57,7 @@ _SIGS = {
     "i2s_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
     "i2s_mul_mat": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "i2s_mul_mat_ex": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, ctypes.POINTER(i2s_config), _p]),
+    "i2s_mul_mat_noalloc": (_int, [_p, _i64, _i64, _p, _i64, _p, _p]),
     "i2s_mul_mat_grouped_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
     "i2s_mul_mat_grouped": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_quantize": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
@@ -179,6 +180,18 @@ def i2s_mul_mat(w, N: int, K: int, x, y=None, ws=None, path: int = 0, split_k: i
     else:
         rc = _L.i2s_mul_mat(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), _stream())
     _check("i2s_mul_mat", rc)
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 4194304   # I2S_NOALLOC_SCRATCH_BYTES
+
+
+def i2s_mul_mat_noalloc(w, N: int, K: int, x, y):
+    """y (M x N F32, caller-provided) = I2_S w times x, M <= 16, with the
+    library's fixed per-device scratch instead of a workspace; nothing is
+    allocated. Calls on one device must not overlap on the GPU."""
+    M = x.shape[0]
+    _check("i2s_mul_mat_noalloc", _L.i2s_mul_mat_noalloc(_dptr(w), N, K, _dptr(x), M, _dptr(y), _stream()))
     return y
 
 
