@@ -62,14 +62,11 @@ struct ActSlot {
     size_t scale_off, sum_off, op_off;
 };
 
-// Operand rows of the tensor-core GEMV's e4m3 operand per half (hi / lo).
-int64_t gemv_tc_rows(int64_t M) { return M <= 8 ? 8 : 16; }
-
 size_t act_slot_bytes(int64_t M, int64_t K) {
     const int64_t Kp = round_up(K, 256);
     size_t op = (size_t)M * (size_t)Kp * 2;                      // GEMV records / GEMM f16 rows
     if (M <= 16) {
-        const size_t tc = (size_t)(2 * gemv_tc_rows(M)) * (size_t)K;   // GEMV tensor-core operand
+        const size_t tc = (size_t)gemv_tc_op_rows(gemv_tc_mp(M)) * (size_t)(K / 2);   // GEMV tensor-core operand
         if (tc > op) op = tc;
     }
     return align_up((size_t)M * 4) * 2 + align_up(op);
@@ -393,7 +390,7 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     std::vector<int> act_of, first;
     const int n_act = group_acts(probs, count, act_of, first);
     if (n_act > kTcMaxMaps) return I2S_E_BAD_ARG;
-    const int Mp = (int)gemv_tc_rows(M);
+    const int Mp = gemv_tc_mp(M);
     uint8_t* base = static_cast<uint8_t*>(ws);
     std::vector<ActSlot> slots(n_act);
     size_t off = kHeader;
@@ -420,7 +417,7 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         qa.count = n_act;
         qa.M = (int)M;
         qa.rows = Mp;
-        qa.layout = kQuantE4M3Tc;
+        qa.layout = kQuantE2M1Tc;
         for (int a = 0; a < n_act; ++a) {
             const i2s_problem& p = probs[first[a]];
             qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
@@ -437,7 +434,8 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         ta.BN = Mp;
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         for (int a = 0; a < n_act; ++a)
-            if (!make_e4m3_operand_map(&ta.maps[a], base + slots[a].op_off, 2 * Mp, (int)probs[first[a]].K))
+            if (!make_u8_operand_map(&ta.maps[a], base + slots[a].op_off, gemv_tc_op_rows(Mp),
+                                     (int)(probs[first[a]].K / 2)))
                 return I2S_E_CUDA;
         ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off_bytes);
         ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off_bytes);

@@ -318,12 +318,12 @@ bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, i
 
 // 2-D tensor map of the GEMV's e4m3 operand: `rows` x `K` bytes (K contiguous),
 // box 128 x rows (one K block of every operand row), 128-byte swizzle.
-bool make_e4m3_operand_map(CUtensorMap* map, const void* base, int rows, int K) {
+bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     std::memset(map, 0, sizeof(*map));
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
     cuuint32_t box[2] = {128u, (cuuint32_t)rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,

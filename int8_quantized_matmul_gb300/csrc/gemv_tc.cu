@@ -5,41 +5,42 @@
 //
 // The op is bound by weight bandwidth: each 2-bit weight is read from HBM
 // once and used for all M activation rows. What limits a tensor-core GEMV here
-// is the expansion of the codes into MMA operands, so it is kept off shared
-// memory: converter threads expand each weight row's codes in registers and
-// write them straight into tensor memory (tcgen05.st), and the MMA reads its A
-// operand from there.
+// is turning the codes into MMA operands and issuing the MMAs, so the codes
+// are expanded in registers and written straight into tensor memory
+// (tcgen05.st), where the MMA reads its A operand, and each MMA covers as many
+// codes as the hardware allows.
 //
-// Arithmetic (exact): tcgen05.mma kind::f8f6f4 with e4m3 operands and f32
-// accumulation.
-//   * A: a code c in {0,1,2} read as an e4m3 bit pattern is the subnormal
-//     c * 2^-9, so (packed >> s) & 0x03030303 yields four operands.
-//   * B: each quantized activation q in [-127,127] is split exactly into
-//     16*(q>>4) and (q&15), both exact e4m3 values, stored as two operand rows
-//     ("hi" rows 0..M'-1 and "lo" rows M'..2M'-1 with M' = 8 or 16), so
-//     MMA N = 2M'.
-//   * D columns m and M'+m hold sum_k c*16*(q>>4) * 2^-9 and sum_k c*(q&15) *
-//     2^-9: integer multiples of 2^-9 below 2^24 * 2^-9 in magnitude, held
-//     exactly in f32. dot = (D_hi + D_lo) * 2^9, as two exact conversions.
+// Arithmetic (exact): tcgen05.mma kind::mxf4 (packed e2m1 operands, K = 64 per
+// instruction) with every block scale equal to 1 and f32 accumulation.
+//   * A: a code c in {0,1,2} read as an e2m1 nibble is c/2, so
+//     packed & 0x33333333 and (packed >> 2) & 0x33333333 yield eight operands
+//     each.
+//   * B: each quantized activation q in [-127,127] is written as three digits
+//     q = d0 + 8*d1 + 64*d2 (d0, d1 in [-4,3], d2 in [-2,2]), each an exact
+//     e2m1 value, one operand row per digit: row j*M' + m (M' = 8 or 16), so
+//     MMA N = 32 (M' = 8, with 8 zero rows) or 48.
+//   * D column j*M' + m holds sum_k (c/2)*d_j: a multiple of 1/2 below 2^23,
+//     exact in f32. dot = 2*D_0 + 16*D_1 + 128*D_2, formed in integers.
 // The epilogue is the pages' y = (float)(dot - row_sum) * (w_scale*act_scale).
 //
-// K order: a K block is one 128-position group (32 packed bytes per weight
-// row). TMEM column 4w + i of the block holds the four codes of word w (group
-// bytes 4w..4w+3) at shift (6, 4, 2, 0)[i], i.e. positions 32i + 4w + 0..3;
-// the quantizer writes the B rows in the same order (quant.cu,
-// e4m3_tc_index), and the dot product does not depend on the order.
+// K order: TMEM column 16g + 2w + t of a stage holds, for 128-group g, the
+// eight codes of group word w (bytes 4w..4w+3) at shifts (0,4) (t = 0) or
+// (2,6) (t = 1), in that nibble order per byte; the quantizer writes the B
+// rows in the same order (quant.cu, k_quant_rows_tc4), and the dot product
+// does not depend on the order.
 //
-// Roles (persistent CTAs, static tile schedule, 128 weight rows per tile):
-//   warp 8     weight producer: per 4 K blocks, each row's contiguous 128
-//              packed bytes, copied with cp.async by 8 consecutive lanes (a warp
-//              instruction moves 4 whole rows) into a 4-stage shared ring (rows
-//              padded to 144 bytes so the 16-byte reads are free of bank
-//              conflicts), completion signalled on an mbarrier;
-//   warps 0-3  converters: thread = weight row = TMEM lane reads its row's 32
-//              bytes of a K block, expands them and tcgen05.st's them into a
-//              4-stage TMEM ring of A operands;
-//   warp 10    TMA producer of the B rows of each K block;
-//   warp 9     TMEM allocation and the MMA issuer;
+// Roles (persistent CTAs, contiguous ranges of work units, 128 weight rows per
+// tile, 512 K positions per pipeline stage):
+//   warp 8     weight producer: each row's 128 packed bytes of a stage, copied
+//              with cp.async by 8 consecutive lanes (a warp instruction moves 4
+//              whole rows) into a 3-stage shared ring (rows padded to 144 bytes
+//              so the 16-byte reads are free of bank conflicts), completion
+//              signalled on an mbarrier;
+//   warps 0-3  converters: thread = weight row = TMEM lane reads its row's 128
+//              bytes, expands them and tcgen05.st's them into a 2-stage TMEM
+//              ring of A operands (64 columns per stage);
+//   warp 10    TMA producer of the B rows of each stage;
+//   warp 9     TMEM allocation and the MMA issuer (8 MMAs per stage);
 //   warps 4-7  epilogue (TMEM lanes 32(w-4) .. +31 = weight rows).
 // Every wait is bounded (~1 s) and reports a timeout in the status word.
 
@@ -59,21 +60,25 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kWProdWarp = 8;
 constexpr int kMmaWarpGv = 9;
 constexpr int kBProdWarp = 10;
-constexpr int kKB = 256;               // K positions per pipeline stage (64 packed bytes per row)
-constexpr int kSbK = 2;                // stages per weight super-block (128 bytes per row)
-constexpr int kWStages = 3;            // weight ring depth (super-blocks)
+constexpr int kKB = 512;               // K positions per pipeline stage (128 packed bytes per row)
+constexpr int kStageBytes = kKB / 4;
+constexpr int kWStages = 3;            // weight ring depth
 constexpr int kWPitch = 144;           // padded bytes per row in the weight ring
-constexpr int kStagesGv = 3;           // TMEM A ring depth (stages of 64 columns)
-constexpr int kBRingBytes = 32 * 1024; // activation ring: 8 stages of 4 KB (M' = 8) or 4 of 8 KB (M' = 16)
-constexpr int kBStagesMax = 16;
+constexpr int kStagesGv = 2;           // TMEM A ring depth (stages of 64 columns)
+constexpr int kBRingBytes = 36 * 1024; // activation ring: 4 stages of 8 KB (M' = 8) or 3 of 12 KB (M' = 16)
+constexpr int kBStagesMax = 8;
 constexpr int kTileRows = 128;
 constexpr int kWStageBytes = kTileRows * kWPitch;
-constexpr uint32_t kTmemColsGv = 256;  // A ring 3 x 64 columns, D 2 x 32 columns
-constexpr uint32_t kDCol0 = 192;
+constexpr uint32_t kTmemColsGv = 256;
+// TMEM columns: A stages 0..127, accumulator 0 at 128 (up to 48 columns),
+// block scales 176..191, accumulator 1 at 192.
+constexpr uint32_t kDCol0 = 128, kDCol1 = 192;
+constexpr uint32_t kSfCol = 176;
+constexpr uint32_t kSfOnes = 0x7F7F7F7Fu;   // ue8m0 1.0 in every byte
 constexpr long long kWaitLimitGv = 2000000000LL;
 
 struct SmemGv {
-    uint64_t full_w[kWStages];          // a weight super-block stage is in shared memory
+    uint64_t full_w[kWStages];          // a weight stage is in shared memory
     uint64_t empty_w[kWStages];         // every converter is done with a stage
     uint64_t full_a[kStagesGv];
     uint64_t empty[kStagesGv];          // TMEM A stage free (MMA done)
@@ -121,7 +126,7 @@ struct SProb {
     int N, K, map, unit0, chunks, dot_off, ticket_off, pad;
 };
 
-constexpr int kChunkStages = kGemvChunkPositions / kKB;   // 6 stages per work unit
+constexpr int kChunkStages = kGemvChunkPositions / kKB;   // 3 stages per work unit
 
 // A segment: the consecutive K chunks of one row tile that fall inside this
 // CTA's contiguous range of work units [u, u_hi). Every role walks the same
@@ -170,7 +175,15 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     return g;
 }
 
+template <int Mp>
 __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_constant__ TcArgs a) {
+    constexpr int kN = gemv_tc_op_rows(Mp);                 // MMA N: three digit rows per activation row, padded
+    constexpr uint32_t kBSub = (uint32_t)kN * 128u;          // one 256-position operand sub-tile (1024-aligned)
+    constexpr uint32_t kBStageBytes = 2 * kBSub;             // a stage holds two sub-tiles
+    constexpr int kBStages = kBRingBytes / (int)kBStageBytes;
+    static_assert(kBStages >= 2 && kBStages <= kBStagesMax, "activation ring depth");
+    static_assert(kN % 16 == 0 && kN <= 48, "MMA N");
+
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sB = smem;
@@ -179,10 +192,6 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     SProb* sp = reinterpret_cast<SProb*>(reinterpret_cast<uint8_t*>(&S) + ((sizeof(SmemGv) + 15) & ~(size_t)15));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int Mp = a.BN;                                     // operand rows per half (8 or 16); MMA N = 2*Mp
-    const uint32_t b_sub = (uint32_t)(2 * Mp) * 128u;        // one 128-position operand sub-tile (1024-aligned)
-    const uint32_t b_stage_bytes = 2 * b_sub;                // a stage holds two sub-tiles
-    const int b_stages = kBRingBytes / (int)b_stage_bytes;
     // this CTA's contiguous share of the work units
     const int u_begin = (int)(((long long)blockIdx.x * a.total_tiles) / gridDim.x);
     const int u_end = (int)(((long long)(blockIdx.x + 1) * a.total_tiles) / gridDim.x);
@@ -251,22 +260,22 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
 
     if (warp == kWProdWarp) {
         // --------------------------------------------------- weight producer
-        // Per super-block (two stages, 512 positions), each row's contiguous
-        // packed bytes (up to 128) are copied with cp.async, 8 consecutive lanes
-        // per row (a warp instruction moves 4 whole rows), into a 3-stage ring;
-        // completion is signalled on the stage's mbarrier by every lane.
+        // Per stage, each row's contiguous packed bytes (up to 128) are copied
+        // with cp.async, 8 consecutive lanes per row (a warp instruction moves
+        // 4 whole rows), into a 3-stage ring; completion is signalled on the
+        // stage's mbarrier by every lane.
         int ws = 0;
         uint32_t wphase = 0;
         bool ok = true;
         for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
             const int row_bytes = g.K / 4;
-            const int end = min(g.st_hi * 64, row_bytes);
-            for (int off = g.st_lo * 64; off < end; off += 128) {
-                const int bytes = min(128, end - off);   // 32, 64, 96 or 128
+            const int end = min(g.st_hi * kStageBytes, row_bytes);
+            for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
+                const int bytes = min(kStageBytes, end - off);   // 32, 64, 96 or 128
                 if (!tc::mbar_wait_spin(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
                 const uint8_t* base = g.w + (size_t)g.n0 * row_bytes + off;
                 uint8_t* dst = sW + (size_t)ws * kWStageBytes;
-                if (bytes == 128) {
+                if (bytes == kStageBytes) {
                     const int col = lane & 7;
                     for (int row = lane >> 3; row < kTileRows; row += 4) {
                         const bool v = g.n0 + row < g.N;
@@ -287,66 +296,64 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         cp_async_wait<0>();
     } else if (warp < kCvtWarpsGv) {
         // ---------------------------------------------------------- converters
-        // thread = weight row = TMEM lane: per stage, read the row's 64 (or 32)
-        // bytes from the weight ring, expand, tcgen05.st into the TMEM ring;
-        // then wait for the stage's activation operand to land and publish the
-        // stage, so that one barrier tells the MMA thread both are ready.
+        // thread = weight row = TMEM lane. First the block scales (all 1.0),
+        // then per stage: read the row's 128 (or fewer) bytes from the weight
+        // ring, expand, tcgen05.st into the TMEM ring; wait for the stage's
+        // activation operand to land and publish the stage, so that one
+        // barrier tells the MMA thread both are ready.
         const int r = tid;
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        {
+            uint32_t ones[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ones[i] = kSfOnes;
+            tc::tmem_st_32x32b_x16(lane_base + kSfCol, ones);
+        }
         int ws = 0, stage = 0, bstage = 0;
         uint32_t wphase = 0, phase = 0, bphase = 0;
         bool ok = true;
         for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
             const bool valid = g.n0 + r < g.N;
             const int row_bytes = g.K / 4;
-            const int end = min(g.st_hi * 64, row_bytes);
-            for (int off = g.st_lo * 64; ok && off < end; off += 128) {
-                const int bytes = min(128, end - off);
+            const int end = min(g.st_hi * kStageBytes, row_bytes);
+            for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
+                const int bytes = min(kStageBytes, end - off);
                 if (!tc::mbar_wait_spin(&S.full_w[ws], wphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 const uint8_t* row = sW + (size_t)ws * kWStageBytes + r * kWPitch;
-                for (int so = 0; so < bytes; so += 64) {            // one pipeline stage: 64 (or 32) bytes
-                    const bool two = bytes - so >= 64;              // 256 positions, else 128
-                    uint4 c[4];
+                uint4 c[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) c[i] = make_uint4(0, 0, 0, 0);
-                    if (valid) {
-                        c[0] = *reinterpret_cast<const uint4*>(row + so);
-                        c[1] = *reinterpret_cast<const uint4*>(row + so + 16);
-                        if (two) {
-                            c[2] = *reinterpret_cast<const uint4*>(row + so + 32);
-                            c[3] = *reinterpret_cast<const uint4*>(row + so + 48);
-                        }
-                    }
-                    if (so + 64 >= bytes) tc::mbar_arrive(&S.empty_w[ws]);   // this row's bytes of the ring stage are read
-                    uint32_t v[64];
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = make_uint4(0, 0, 0, 0);
+                    if (valid && 16 * i < bytes) c[i] = *reinterpret_cast<const uint4*>(row + 16 * i);
+                }
+                tc::mbar_arrive(&S.empty_w[ws]);   // this row's bytes of the ring stage are read
+                if (++ws == kWStages) { ws = 0; wphase ^= 1; }
+                if (!tc::mbar_wait_spin(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t col0 = lane_base + (uint32_t)(stage * 64);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 1 && bytes <= 64) break;
+                    uint32_t v[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const uint32_t w4[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
+                        const uint4 q = c[4 * half + i];
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int w = 4 * i + j;   // word of the 64 bytes (group = w / 8)
-                            v[4 * w + 0] = (w4[j] >> 6) & 0x03030303u;
-                            v[4 * w + 1] = (w4[j] >> 4) & 0x03030303u;
-                            v[4 * w + 2] = (w4[j] >> 2) & 0x03030303u;
-                            v[4 * w + 3] = w4[j] & 0x03030303u;
+                            v[8 * i + 2 * j] = w4[j] & 0x33333333u;
+                            v[8 * i + 2 * j + 1] = (w4[j] >> 2) & 0x33333333u;
                         }
                     }
-                    if (!tc::mbar_wait_spin(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t col0 = lane_base + (uint32_t)(stage * 64);
-                    uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
-                    uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
-                    tc::tmem_st_32x32b_x32(col0, v0);
-                    if (two) tc::tmem_st_32x32b_x32(col0 + 32, v1);
-                    tc::tmem_st_wait();
-                    // the stage's activation operand must have landed before publishing
-                    if (!tc::mbar_wait_spin(&S.full_b[bstage], bphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&S.full_a[stage]);
-                    if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
-                    if (++bstage == b_stages) { bstage = 0; bphase ^= 1; }
+                    tc::tmem_st_32x32b_x32(col0 + 32u * half, v);
                 }
-                if (++ws == kWStages) { ws = 0; wphase ^= 1; }
+                tc::tmem_st_wait();
+                // the stage's activation operand must have landed before publishing
+                if (!tc::mbar_wait_spin(&S.full_b[bstage], bphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&S.full_a[stage]);
+                if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
+                if (++bstage == kBStages) { bstage = 0; bphase ^= 1; }
             }
         }
     } else if (warp == kBProdWarp) {
@@ -368,27 +375,29 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                     if (gn.live && gn.map != g.map) tc::tma_prefetch_desc(&a.maps[gn.map]);
                 }
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
-                    const bool two = (kb + 1) * kKB <= g.K;
+                    const bool two = kb * kKB + kKB / 2 < g.K;   // the stage reaches its second 256 positions
                     if (!tc::mbar_wait_spin(&S.empty_b[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(64); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&S.full_b[stage], two ? b_stage_bytes : b_sub);
-                    uint8_t* dst = sB + (size_t)stage * b_stage_bytes;
-                    tc::tma_load_2d(dst, map, kb * kKB, 0, &S.full_b[stage]);
-                    if (two) tc::tma_load_2d(dst + b_sub, map, kb * kKB + 128, 0, &S.full_b[stage]);
+                    tc::mbar_arrive_expect_tx(&S.full_b[stage], two ? kBStageBytes : kBSub);
+                    uint8_t* dst = sB + (size_t)stage * kBStageBytes;
+                    tc::tma_load_2d(dst, map, kb * (kKB / 2), 0, &S.full_b[stage]);
+                    if (two) tc::tma_load_2d(dst + kBSub, map, kb * (kKB / 2) + 128, 0, &S.full_b[stage]);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
-                    if (++stage == b_stages) { stage = 0; phase ^= 1; }
+                    if (++stage == kBStages) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok)
-                for (int s = 0; s < b_stages; ++s)
+                for (int s = 0; s < kBStages; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimitGv / 8);
         }
     } else if (warp == kMmaWarpGv) {
         // ---------------------------------------------------------------- MMA
         // One wait per stage: a complete full_a implies the activation operand
-        // has landed too (the converters waited for it before arriving).
+        // has landed too (the converters waited for it before arriving). The
+        // stage's MMAs (two per 128-position group) are unrolled.
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_e4m3_f32(kTileRows, 2 * Mp);
+            constexpr uint32_t idesc = tc::idesc_mxf4_f32(kTileRows, kN);
+            const uint32_t sfa = tmem_base + kSfCol, sfb = tmem_base + kSfCol + 4;
             int stage = 0, bstage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -397,21 +406,25 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 if (!tc::mbar_wait_spin(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimitGv)) { fail(128); break; }
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + kDCol0 + (uint32_t)(acc * 32);
+                const uint32_t d_tmem = tmem_base + (acc ? kDCol1 : kDCol0);
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
-                    const int steps = (kb + 1) * kKB <= g.K ? 8 : 4;   // 32 positions per MMA
+                    const int n_mma = 2 * min(4, (g.K - kb * kKB) / 128);   // 64 positions per MMA
                     if (!tc::mbar_wait_spin(&S.full_a[stage], phase, abort_flag, kWaitLimitGv)) { fail(256); ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t b0 = tc::smem_u32(sB + (size_t)bstage * b_stage_bytes);
+                    const uint32_t b0 = tc::smem_u32(sB + (size_t)bstage * kBStageBytes);
                     const uint64_t bd0 = tc::sdesc_sw128_kmajor(b0);
-                    const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + b_sub);
-                    for (int k = 0; k < steps; ++k)
-                        tc::umma_f8f6f4_tmem_a(d_tmem, tmem_base + (uint32_t)(stage * 64 + k * 8),
-                                               (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, (kb != g.st_lo) || k != 0);
+                    const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + kBSub);
+                    const uint32_t a0 = tmem_base + (uint32_t)(stage * 64);
+                    const uint32_t first = kb != g.st_lo;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (k < n_mma)
+                            tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa, sfb,
+                                                 k == 0 ? first : 1u);
                     tc::umma_commit(&S.empty[stage]);
                     tc::umma_commit(&S.empty_b[bstage]);
                     if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
-                    if (++bstage == b_stages) bstage = 0;
+                    if (++bstage == kBStages) bstage = 0;
                 }
                 if (!ok) break;
                 tc::umma_commit(&S.tmem_full[acc]);
@@ -434,26 +447,29 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             const int n = g.n0 + r;
             if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimitGv)) { fail(512); break; }
             tc::tc_fence_after();
-            uint32_t v[32];
-            tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + kDCol0 + (uint32_t)(acc * 32), v);
+            const uint32_t dcol = tmem_base + ((uint32_t)(q * 32) << 16) + (acc ? kDCol1 : kDCol0);
+            uint32_t v[48];
+            tc::tmem_ld_32x32b_x32(dcol, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
+            if (kN > 32) tc::tmem_ld_32x32b_x16(dcol + 32, *reinterpret_cast<uint32_t (*)[16]>(&v[32]));
             tc::tmem_ld_wait();
             tc::tc_fence_before();
             tc::mbar_arrive(&S.tmem_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-            int dot[16];
+            int dot[Mp];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                // "lo" operand rows start at column Mp (8 or 16); indices stay static
-                const float d_hi = __uint_as_float(v[m]);
-                const float d_lo = __uint_as_float(Mp == 8 ? v[(8 + m) & 31] : v[(16 + m) & 31]);
-                dot[m] = __float2int_rn(__fmul_rn(d_hi, 512.0f)) + __float2int_rn(__fmul_rn(d_lo, 512.0f));
+            for (int m = 0; m < Mp; ++m) {
+                // 2*D_j is an exact integer; dot = sum_j 8^j * 2*D_j
+                const int d0 = __float2int_rn(__fmul_rn(__uint_as_float(v[m]), 2.0f));
+                const int d1 = __float2int_rn(__fmul_rn(__uint_as_float(v[Mp + m]), 2.0f));
+                const int d2 = __float2int_rn(__fmul_rn(__uint_as_float(v[2 * Mp + m]), 2.0f));
+                dot[m] = d0 + 8 * d1 + 64 * d2;
             }
             bool write = g.c_lo == 0 && g.c_hi == g.chunks;
             if (!write) {
                 int32_t* part = a.dot_base + g.dot_off;
                 if (n < g.N) {
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
+                    for (int m = 0; m < Mp; ++m)
                         if (m < a.M) atomicAdd(&part[(size_t)m * g.N + n], dot[m]);
                 }
                 __threadfence();
@@ -472,7 +488,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                     __threadfence();
                     if (n < g.N) {
 #pragma unroll
-                        for (int m = 0; m < 16; ++m)
+                        for (int m = 0; m < Mp; ++m)
                             if (m < a.M) dot[m] = __ldcg(&part[(size_t)m * g.N + n]);
                     }
                 }
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             if (write && n < g.N) {
                 const float w_scale = *reinterpret_cast<const float*>(g.w + (size_t)g.N * (g.K / 4));
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
+                for (int m = 0; m < Mp; ++m) {
                     if (m < a.M) {
                         const float sc = __fmul_rn(w_scale, g.act_scale[m]);
                         g.y[(size_t)m * g.N + n] = __fmul_rn(__int2float_rn(dot[m] - g.row_sum[m]), sc);
@@ -507,11 +523,16 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(k_i2s_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemGvBytes);
+        e = cudaFuncSetAttribute(k_i2s_gemv_tc<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemGvBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_i2s_gemv_tc<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemGvBytes);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    k_i2s_gemv_tc<<<grid, kThreadsGv, kSmemGvBytes, s>>>(a);
+    if (a.BN == 8)
+        k_i2s_gemv_tc<8><<<grid, kThreadsGv, kSmemGvBytes, s>>>(a);
+    else
+        k_i2s_gemv_tc<16><<<grid, kThreadsGv, kSmemGvBytes, s>>>(a);
     return cudaGetLastError();
 }
 

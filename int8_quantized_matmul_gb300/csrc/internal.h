@@ -18,7 +18,7 @@ enum QuantLayout : int {
     kQuantI8Rows = 0,    // plain int8, row-major M x K (the public sidecar)
     kQuantE4M3Frag = 1,  // GEMV operand records (see gemv.cu), 2*Kp bytes per row
     kQuantF16Perm = 2,   // tensor-core GEMM operand: f16, K permuted per 128-group
-    kQuantE4M3Tc = 3,    // tensor-core GEMV operand: e4m3 hi rows then lo rows (2*M' x K)
+    kQuantE2M1Tc = 3,    // tensor-core GEMV operand: e2m1 digit rows (gemv_tc.cu), gemv_tc_op_rows(M') x K/2 bytes
 };
 
 struct QuantJob {
@@ -36,7 +36,7 @@ struct QuantArgs {
     unsigned long long zero_16;
     int count;
     int M;
-    int rows;           // rows written per job: M, or M' (8 or 16) for kQuantE4M3Tc
+    int rows;           // rows written per job: M, or M' (8 or 16) for kQuantE2M1Tc
     int layout;
     QuantJob j[kMaxGroup];
 };
@@ -103,7 +103,7 @@ struct TcArgs {
     int count;
     int M;
     int BN;                   // GEMM: activation rows per tile (MMA N, multiple of 32, <= 256);
-                              // GEMV: operand rows per half M' (8 or 16), MMA N = 2M'
+                              // GEMV: M' (8 or 16), MMA N = gemv_tc_op_rows(M')
 
     int total_tiles;          // GEMM: tiles; GEMV: work units
     TcProb p[kMaxGroup];
@@ -111,13 +111,20 @@ struct TcArgs {
 
 constexpr int kGemvChunkPositions = 1536;   // K positions per GEMV work unit
 
+// Tensor-core GEMV activation operand: M' = 8 (M <= 8) or 16 activation rows,
+// each split into three base-8 digit rows (digit j of row m at row j*M' + m),
+// padded to a multiple of 16 rows (the MMA N). Row-major, K/2 bytes per row.
+__host__ __device__ constexpr int gemv_tc_mp(int64_t M) { return M <= 8 ? 8 : 16; }
+__host__ __device__ constexpr int gemv_tc_op_rows(int Mp) { return Mp == 8 ? 32 : 48; }
+
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(TcArgs) <= 32764, "TcArgs exceeds the kernel parameter limit");
 static_assert(sizeof(GemvArgs) <= 32764, "GemvArgs exceeds the kernel parameter limit");
 static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
 
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
-bool make_e4m3_operand_map(CUtensorMap* map, const void* base, int rows, int K);
+// rows x row_bytes uint8 matrix, box {128 bytes, rows}, 128-byte swizzle
+bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes);
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 

@@ -3,13 +3,13 @@
 // library a workspace (declared and documented in include/i2s.h).
 //
 // It runs the same two launches as i2s_mul_mat's tensor-core GEMV path -- the
-// per-row quantization into the e4m3 hi/lo operand, then the tcgen05 GEMV --
+// per-row quantization into the e2m1 digit operand, then the tcgen05 GEMV --
 // for a single problem, with the workspace replaced by g_scratch below. The
 // scratch layout is the one the workspace path uses for one problem:
 //   [0, 256)          status word (cleared by the quantization launch)
 //   [256, 512)        act_scale, M F32
 //   [512, 768)        row_sum, M int32
-//   [768, op_end)     e4m3 operand: Mp hi rows then Mp lo rows of K bytes
+//   [768, op_end)     e2m1 operand: gemv_tc_op_rows(Mp) digit rows of K/2 bytes
 //   [op_end, ...)     K > 1536 only: M x N int32 split-K partials, then one
 //                     uint32 chunk counter per 128-row tile; both zeroed by
 //                     the quantization launch of every call.
@@ -86,12 +86,13 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     if (N * (K / 4) >= ((int64_t)1 << 31)) return I2S_E_BAD_SHAPE;
     if (((uintptr_t)w_i2s & 15u) || ((uintptr_t)x & 15u) || ((uintptr_t)y & 15u)) return I2S_E_MISALIGNED;
 
-    const int Mp = M <= 8 ? 8 : 16;
+    const int Mp = gemv_tc_mp(M);
+    const int op_rows = gemv_tc_op_rows(Mp);
     const bool split = K > kGemvChunkPositions;
     const size_t scale_off = kSlotAlign;
     const size_t sum_off = scale_off + up256((size_t)M * 4);
     const size_t op_off = sum_off + up256((size_t)M * 4);
-    const size_t dot_off = op_off + up256((size_t)(2 * Mp) * (size_t)K);
+    const size_t dot_off = op_off + up256((size_t)op_rows * (size_t)(K / 2));
     const int row_tiles = (int)((N + kTcTileW - 1) / kTcTileW);
     const size_t ticket_off = dot_off + (split ? up256((size_t)M * (size_t)N * 4) : 0);
     const size_t end = ticket_off + (split ? up256((size_t)row_tiles * 4) : 0);
@@ -114,7 +115,7 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     qa.count = 1;
     qa.M = (int)M;
     qa.rows = Mp;
-    qa.layout = kQuantE4M3Tc;
+    qa.layout = kQuantE2M1Tc;
     qa.j[0] = QuantJob{x, base + op_off, act_scale, row_sum, (int)K, (int)K};
     if (launch_quant(qa, stream) != cudaSuccess) return I2S_E_CUDA;
 
@@ -125,7 +126,7 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     ta.M = (int)M;
     ta.BN = Mp;
     ta.status = status;
-    if (!make_e4m3_operand_map(&ta.maps[0], base + op_off, 2 * Mp, (int)K)) return I2S_E_CUDA;
+    if (!make_u8_operand_map(&ta.maps[0], base + op_off, op_rows, (int)(K / 2))) return I2S_E_CUDA;
     ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off);
     ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off);
     const int chunks = (int)((K + kGemvChunkPositions - 1) / kGemvChunkPositions);

@@ -12,7 +12,9 @@
 //                   16*(q>>4) and (q&15), both exact in e4m3, stored in the
 //                   warp-MMA fragment order (see gemv.cu);
 //   kQuantF16Perm   the tensor-core GEMM's activation operand: q as f16 in the
-//                   K order in which the GEMM expands the packed codes.
+//                   K order in which the GEMM expands the packed codes;
+//   kQuantE2M1Tc    the tensor-core GEMV's operand: each q as three base-8
+//                   digits in e2m1, one operand row per digit (k_quant_rows_tc4).
 
 #include "common.cuh"
 #include "internal.h"
@@ -51,15 +53,6 @@ __device__ __forceinline__ int perm_index_of(int pos) {   // pos: group-relative
     return 16 * w + 4 * s + j;
 }
 
-// Position (within its 128-group) of the e4m3 element at index e of the
-// tensor-core GEMV operand: TMEM column 4w + i of a K block holds the codes of
-// group bytes 4w..4w+3 at bit-pair slice i, i.e. positions 32i + 4w + 0..3.
-// Returns the element index of group-relative position p (p % 4 == 0 keeps
-// the four elements of a word together).
-__device__ __forceinline__ int e4m3_tc_index(int p) {
-    return 16 * ((p & 31) >> 2) + 4 * (p >> 5) + (p & 3);
-}
-
 // Writes the four quantized values of positions 4c..4c+3 of row m in the
 // requested operand layout.
 __device__ __forceinline__ void emit4(const QuantArgs& a, const QuantJob& J, int m, int c, const int (&q)[4]) {
@@ -79,19 +72,6 @@ __device__ __forceinline__ void emit4(const QuantArgs& a, const QuantJob& J, int
         const int wi = frag_word(4 * c);
         rec[wi] = hi;
         rec[wi + 2] = lo;
-    } else if (a.layout == kQuantE4M3Tc) {
-        uint32_t* hi = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)m * K);
-        uint32_t* lo = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)(a.rows + m) * K);
-        uint32_t h = 0, l = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            h |= (uint32_t)e4m3_times16(q[e] >> 4) << (8 * e);
-            l |= (uint32_t)e4m3_small_int(q[e] & 15) << (8 * e);
-        }
-        const int p = 4 * c;
-        const int word = ((p & ~127) + e4m3_tc_index(p & 127)) >> 2;
-        hi[word] = h;
-        lo[word] = l;
     } else {   // kQuantF16Perm
         __half* out = static_cast<__half*>(J.out) + (size_t)m * K;
         const int pos0 = 4 * c;
@@ -118,13 +98,6 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
     const QuantJob& J = a.j[blockIdx.x / a.rows];
     const int m = blockIdx.x % a.rows;
     const int K = J.K, K4 = K / 4;
-    if (m >= a.M) {
-        // padding operand rows (kQuantE4M3Tc only): zero hi and lo rows
-        uint32_t* hi = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)m * K);
-        uint32_t* lo = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(J.out) + (size_t)(a.rows + m) * K);
-        for (int c = tid; c < K4; c += kQThreads) { hi[c] = 0u; lo[c] = 0u; }
-        return;
-    }
     const float4* x4 = reinterpret_cast<const float4*>(J.x + (size_t)m * K);
 
     float4 cache[kQCache];
@@ -181,8 +154,163 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core GEMV operand (kQuantE2M1Tc). Each q in [-127, 127] is written as
+// three digits q = d0 + 8*d1 + 64*d2 with d0, d1 in [-4, 3] and d2 in [-2, 2],
+// every one exact in e2m1; digit j of activation row m goes to operand row
+// j*M' + m (rows 3M'.. are zero padding up to the MMA N). Within a 128-position
+// group the K order is the one the GEMV's converters produce from the packed
+// weight bytes: element 16w + 8t + 2i + h holds position 32s + 4w + i, where
+// (t, h) = (0, 0), (0, 1), (1, 0), (1, 1) for bit-pair slices s = 3, 1, 2, 0.
+// Elements are packed two per byte, the even one in the low nibble.
+// ---------------------------------------------------------------------------
+
+// e2m1 code of an integer digit d in [-4, 3] (magnitudes 0, 1, 2, 3, 4 encode
+// as 0, 2, 4, 5, 6; bit 3 is the sign).
+__device__ __forceinline__ uint32_t e2m1_digit(int d) {
+    const int a = d < 0 ? -d : d;
+    const uint32_t mag = a <= 2 ? 2u * (uint32_t)a : (uint32_t)a + 2u;
+    return mag | (d < 0 ? 8u : 0u);
+}
+
+// Balanced base-8 digits: q = d[0] + 8*d[1] + 64*d[2].
+__device__ __forceinline__ void base8_digits(int q, int (&d)[3]) {
+    d[0] = ((q + 4) & 7) - 4;
+    const int q1 = (q - d[0]) >> 3;   // exact: q - d0 is a multiple of 8
+    d[1] = ((q1 + 4) & 7) - 4;
+    d[2] = (q1 - d[1]) >> 3;
+}
+
+constexpr int kQ4Cache = 3;   // 16-value units cached per thread (rows up to 12288 values)
+
+// A unit is (group g, word w): the 16 positions 32s + 4w + i (s, i in 0..3) of
+// 128-group g, read as four float4 and written as one 8-byte word per digit row.
+__device__ __forceinline__ void load_unit(const float4* x4, int u, float4 (&v)[4]) {
+    const int base = 32 * (u >> 3) + (u & 7);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) v[s] = x4[base + 8 * s];
+}
+
+__device__ __forceinline__ float unit_amax(const float4 (&v)[4]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) m = fmaxf(m, fmaxf(fmaxf(fabsf(v[s].x), fabsf(v[s].y)), fmaxf(fabsf(v[s].z), fabsf(v[s].w))));
+    return m;
+}
+
+// Quantizes a unit, writes its three digit words, returns the sum of its q.
+__device__ __forceinline__ int emit_unit(const float4 (&v)[4], float inv, int u, uint8_t* op, size_t row_bytes, int Mp,
+                                         int m) {
+    int q[4][4];
+    int sum = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        q[s][0] = quantize_one(v[s].x, inv);
+        q[s][1] = quantize_one(v[s].y, inv);
+        q[s][2] = quantize_one(v[s].z, inv);
+        q[s][3] = quantize_one(v[s].w, inv);
+        sum += q[s][0] + q[s][1] + q[s][2] + q[s][3];
+    }
+    uint32_t w0[3] = {0u, 0u, 0u}, w1[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int d0[3], d1[3], d2[3], d3[3];
+        base8_digits(q[0][i], d0);
+        base8_digits(q[1][i], d1);
+        base8_digits(q[2][i], d2);
+        base8_digits(q[3][i], d3);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            // word t = 0: low nibble slice 3, high nibble slice 1; t = 1: slices 2 and 0
+            w0[j] |= (e2m1_digit(d3[j]) | (e2m1_digit(d1[j]) << 4)) << (8 * i);
+            w1[j] |= (e2m1_digit(d2[j]) | (e2m1_digit(d0[j]) << 4)) << (8 * i);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        reinterpret_cast<uint2*>(op + (size_t)(j * Mp + m) * row_bytes)[u] = make_uint2(w0[j], w1[j]);
+    return sum;
+}
+
+__global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_constant__ QuantArgs a) {
+    __shared__ float s_red[kQThreads / 32];
+    __shared__ int s_sum[kQThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
+    for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
+         i += (unsigned long long)gridDim.x * kQThreads)
+        a.zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    const QuantJob& J = a.j[blockIdx.x / a.rows];
+    const int m = blockIdx.x % a.rows;
+    const int Mp = a.rows;
+    const int K = J.K, U = K / 16;
+    const size_t row_bytes = (size_t)K / 2;
+    uint8_t* op = static_cast<uint8_t*>(J.out);
+    if (3 * Mp + m < gemv_tc_op_rows(Mp)) {   // padding rows after the three digit blocks
+        uint2* z = reinterpret_cast<uint2*>(op + (size_t)(3 * Mp + m) * row_bytes);
+        for (int u = tid; u < U; u += kQThreads) z[u] = make_uint2(0u, 0u);
+    }
+    if (m >= a.M) {   // operand rows of absent activation rows are zero
+        for (int j = 0; j < 3; ++j) {
+            uint2* z = reinterpret_cast<uint2*>(op + (size_t)(j * Mp + m) * row_bytes);
+            for (int u = tid; u < U; u += kQThreads) z[u] = make_uint2(0u, 0u);
+        }
+        return;
+    }
+    const float4* x4 = reinterpret_cast<const float4*>(J.x + (size_t)m * K);
+
+    float4 cache[kQ4Cache][4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kQ4Cache; ++c) {
+        const int u = tid + c * kQThreads;
+        if (u < U) {
+            load_unit(x4, u, cache[c]);
+            amax = fmaxf(amax, unit_amax(cache[c]));
+        }
+    }
+    for (int u = tid + kQ4Cache * kQThreads; u < U; u += kQThreads) {   // rows longer than the cache
+        float4 v[4];
+        load_unit(x4, u, v);
+        amax = fmaxf(amax, unit_amax(v));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    amax = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
+    float scale, inv;
+    quant_params(amax, scale, inv);
+
+    int sum = 0;
+#pragma unroll
+    for (int c = 0; c < kQ4Cache; ++c) {
+        const int u = tid + c * kQThreads;
+        if (u < U) sum += emit_unit(cache[c], inv, u, op, row_bytes, Mp, m);
+    }
+    for (int u = tid + kQ4Cache * kQThreads; u < U; u += kQThreads) {
+        float4 v[4];
+        load_unit(x4, u, v);
+        sum += emit_unit(v, inv, u, op, row_bytes, Mp, m);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) s_sum[warp] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kQThreads / 32; ++w) total += s_sum[w];
+        J.scale[m] = scale;
+        J.sum[m] = total;
+    }
+}
+
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
-    k_quant_rows<<<a.count * a.rows, kQThreads, 0, s>>>(a);
+    if (a.layout == kQuantE2M1Tc)
+        k_quant_rows_tc4<<<a.count * a.rows, kQThreads, 0, s>>>(a);
+    else
+        k_quant_rows<<<a.count * a.rows, kQThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
