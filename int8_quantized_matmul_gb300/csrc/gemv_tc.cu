@@ -42,7 +42,9 @@
 //   warp 10    TMA producer of the B rows of each stage;
 //   warp 9     TMEM allocation and the MMA issuer (8 MMAs per stage);
 //   warps 4-7  epilogue (TMEM lanes 32(w-4) .. +31 = weight rows).
-// Every wait is bounded (~1 s) and reports a timeout in the status word.
+// Every wait is bounded (~1 s) and reports a timeout in the status word. The
+// MMA thread spins on its barriers; the other roles suspend while they wait,
+// leaving the issue slots to the converters and the MMA thread.
 
 #include <atomic>
 
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             const int end = min(g.st_hi * kStageBytes, row_bytes);
             for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
                 const int bytes = min(kStageBytes, end - off);   // 32, 64, 96 or 128
-                if (!tc::mbar_wait_spin(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
+                if (!tc::mbar_wait_idle(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
                 const uint8_t* base = g.w + (size_t)g.n0 * row_bytes + off;
                 uint8_t* dst = sW + (size_t)ws * kWStageBytes;
                 if (bytes == kStageBytes) {
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             const int end = min(g.st_hi * kStageBytes, row_bytes);
             for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
                 const int bytes = min(kStageBytes, end - off);
-                if (!tc::mbar_wait_spin(&S.full_w[ws], wphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
+                if (!tc::mbar_wait_idle(&S.full_w[ws], wphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 const uint8_t* row = sW + (size_t)ws * kWStageBytes + r * kWPitch;
                 uint4 c[8];
 #pragma unroll
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 }
                 tc::mbar_arrive(&S.empty_w[ws]);   // this row's bytes of the ring stage are read
                 if (++ws == kWStages) { ws = 0; wphase ^= 1; }
-                if (!tc::mbar_wait_spin(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
+                if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t col0 = lane_base + (uint32_t)(stage * 64);
 #pragma unroll
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 }
                 tc::tmem_st_wait();
                 // the stage's activation operand must have landed before publishing
-                if (!tc::mbar_wait_spin(&S.full_b[bstage], bphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
+                if (!tc::mbar_wait_idle(&S.full_b[bstage], bphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 tc::tc_fence_before();
                 tc::mbar_arrive(&S.full_a[stage]);
                 if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 }
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
                     const bool two = kb * kKB + kKB / 2 < g.K;   // the stage reaches its second 256 positions
-                    if (!tc::mbar_wait_spin(&S.empty_b[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(64); ok = false; break; }
+                    if (!tc::mbar_wait_idle(&S.empty_b[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(64); ok = false; break; }
                     tc::mbar_arrive_expect_tx(&S.full_b[stage], two ? kBStageBytes : kBSub);
                     uint8_t* dst = sB + (size_t)stage * kBStageBytes;
                     tc::tma_load_2d(dst, map, kb * (kKB / 2), 0, &S.full_b[stage]);
@@ -416,11 +418,18 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                     const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + kBSub);
                     const uint32_t a0 = tmem_base + (uint32_t)(stage * 64);
                     const uint32_t first = kb != g.st_lo;
+                    if (n_mma == 8) {   // full stage: straight-line issue
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        if (k < n_mma)
-                            tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa, sfb,
-                                                 k == 0 ? first : 1u);
+                        for (int k = 0; k < 8; ++k)
+                            tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa,
+                                                 sfb, k == 0 ? first : 1u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (k < n_mma)
+                                tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa,
+                                                     sfb, k == 0 ? first : 1u);
+                    }
                     tc::umma_commit(&S.empty[stage]);
                     tc::umma_commit(&S.empty_b[bstage]);
                     if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
@@ -474,14 +483,14 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 }
                 __threadfence();
                 tc::mbar_arrive(&S.epi_sync);
-                if (!tc::mbar_wait_spin(&S.epi_sync, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
+                if (!tc::mbar_wait_idle(&S.epi_sync, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
                 if (r == 0) {
                     __threadfence();
                     const unsigned prev = atomicAdd(&a.ticket_base[g.ticket_off + g.tile], (unsigned)g.units);
                     S.final_flag = prev + (unsigned)g.units == (unsigned)g.chunks;
                     tc::mbar_arrive(&S.epi_bcast);
                 }
-                if (!tc::mbar_wait_spin(&S.epi_bcast, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
+                if (!tc::mbar_wait_idle(&S.epi_bcast, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
                 sync_phase ^= 1;
                 write = S.final_flag != 0;
                 if (write) {

@@ -86,6 +86,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
+// Bounded wait for roles off the critical path: one non-blocking probe, then
+// suspending try_waits, so a waiting warp leaves the issue slots to the warps
+// that share its scheduler (it still wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                               long long limit_cycles) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+}
+
 // Bounded wait for the phase of `parity` to complete. Gives up (returns false)
 // after `limit_cycles` SM clocks or as soon as *abort is set by another warp.
 // Each try_wait sleeps up to 20 us, so the abort flag and the clock are
