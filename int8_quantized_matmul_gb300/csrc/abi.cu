@@ -537,9 +537,18 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
 
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
+// I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
+// rows_pad x K][split-tile int32 sums, tiles x 128 x 128][tile tickets]
+static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTile - 1) / kI8sTile * kI8sTile; }
+static int64_t i8s_tiles(int64_t M, int64_t N) {
+    return ((N + kI8sTile - 1) / kI8sTile) * ((M + kI8sTile - 1) / kI8sTile);
+}
+
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 64 || K % 64) return 0;
-    return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)M * (size_t)K * 2);
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
+           align_up(tiles * kI8sTile * kI8sTile * 4) + align_up(tiles * 4);
 }
 
 int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
@@ -556,22 +565,42 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     if (r) return r;
     uint8_t* base = static_cast<uint8_t*>(ws);
     unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     float* yf = reinterpret_cast<float*>(base + kHeader);
-    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    const int64_t rows_pad = i8s_rows_pad(M);
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    const size_t xf_off = kHeader + align_up((size_t)M * (size_t)N * 4);
+    const size_t part_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
+    const size_t tick_off = part_off + align_up(tiles * kI8sTile * kI8sTile * 4);
+    const size_t zero_bytes = tick_off + align_up(tiles * 4) - part_off;
+    __half* xf = reinterpret_cast<__half*>(base + xf_off);
+    // pre-pass: activations to f16 rows; clears the status and amax words and
+    // the split-tile sums and tickets
+    r = cuda_status(launch_i8s_x_to_f16(static_cast<const int8_t*>(x_i8s), (int)M, (int)K, (int)rows_pad, xf,
+                                        base + part_off, zero_bytes, status, amax, stream));
     if (r) return r;
-    I8sMatArgs a;
+    static thread_local I8sTcArgs a;
+    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTile)) return I2S_E_CUDA;
     a.w = static_cast<const int8_t*>(w_i8s);
-    a.x = static_cast<const int8_t*>(x_i8s);
     a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
     a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
     a.bias = bias;
     a.y = yf;
     a.amax_bits = amax;
+    a.part = reinterpret_cast<int32_t*>(base + part_off);
+    a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
+    a.status = status;
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
     a.relu = relu ? 1 : 0;
-    r = cuda_status(launch_i8s_mat(a, stream));
+    a.n_wt = (int)((N + kI8sTile - 1) / kI8sTile);
+    a.n_at = (int)(rows_pad / kI8sTile);
+    a.chunks = (int)((K + kI8sChunkK - 1) / kI8sChunkK);
+    a.total_units = (int)tiles * a.chunks;
+    int grid = device_sm_count();
+    if (grid > a.total_units) grid = a.total_units;
+    r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
 }

@@ -9,8 +9,8 @@
 // tensor into I8_S with one scale, as the op's output must be self-describing.
 // Two passes are needed because the scale depends on the whole output.
 //
-// This file holds the dp4a tile kernel (exact int32 accumulation of int8
-// products); the tensor-core version lives in gemm_tc.cu.
+// This file holds the requantization kernels; the matmul with its fused
+// epilogue is the tensor-core kernel in i8s_tc.cu.
 
 #include "common.cuh"
 #include "internal.h"
@@ -18,72 +18,6 @@
 namespace i2s {
 
 namespace {
-
-constexpr int kT = 64;        // output tile 64 x 64
-constexpr int kKs = 64;       // K bytes per step
-constexpr int kPad = 16;      // row padding (bytes) against bank conflicts
-
-__global__ void __launch_bounds__(256) k_i8s_mat_dp4a(const I8sMatArgs a) {
-    __shared__ __align__(16) int8_t xs[kT][kKs + kPad];
-    __shared__ __align__(16) int8_t ws[kT][kKs + kPad];
-    __shared__ float s_max[8];
-    const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;
-    const int m0 = blockIdx.y * kT, n0 = blockIdx.x * kT;
-    int acc[4][4] = {};
-
-    for (int k0 = 0; k0 < a.K; k0 += kKs) {
-        {   // one 16-byte chunk of each operand per thread
-            const int r = tid >> 2, c = (tid & 3) * 16;
-            const int m = m0 + r, n = n0 + r;
-            uint4 xv = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
-            if (m < a.M) xv = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0 + c);
-            if (n < a.N) wv = *reinterpret_cast<const uint4*>(a.w + (size_t)n * a.K + k0 + c);
-            *reinterpret_cast<uint4*>(&xs[r][c]) = xv;
-            *reinterpret_cast<uint4*>(&ws[r][c]) = wv;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int kk = 0; kk < kKs; kk += 4) {
-            int xw[4], ww[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) xw[i] = *reinterpret_cast<const int*>(&xs[ty * 4 + i][kk]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ww[j] = *reinterpret_cast<const int*>(&ws[tx * 4 + j][kk]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = __dp4a(xw[i], ww[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-
-    const float sc = __fmul_rn(*a.w_scale_ptr, *a.x_scale_ptr);
-    float local_max = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = m0 + ty * 4 + i;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx * 4 + j;
-            if (m < a.M && n < a.N) {
-                float v = __fmul_rn(__int2float_rn(acc[i][j]), sc);
-                if (a.bias) v = __fadd_rn(v, a.bias[n]);
-                if (a.relu) v = v > 0.0f ? v : 0.0f;
-                a.y[(size_t)m * a.N + n] = v;
-                local_max = fmaxf(local_max, fabsf(v));
-            }
-        }
-    }
-    local_max = warp_max(local_max);
-    if ((tid & 31) == 0) s_max[tid >> 5] = local_max;
-    __syncthreads();
-    if (tid == 0) {
-        float mx = 0.0f;
-        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, s_max[i]);
-        atomicMax(a.amax_bits, __float_as_uint(mx));
-    }
-}
 
 __global__ void __launch_bounds__(256) k_absmax(const float* __restrict__ y, int64_t n, unsigned int* amax_bits) {
     __shared__ float s_max[8];
@@ -133,11 +67,6 @@ int grid_for(int64_t n4) {
 
 }  // namespace
 
-cudaError_t launch_i8s_mat(const I8sMatArgs& a, cudaStream_t s) {
-    dim3 grid((a.N + kT - 1) / kT, (a.M + kT - 1) / kT);
-    k_i8s_mat_dp4a<<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s) {
     k_absmax<<<grid_for(n), 256, 0, s>>>(y, n, amax_bits);

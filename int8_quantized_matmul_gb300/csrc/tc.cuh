@@ -186,6 +186,21 @@ __device__ __forceinline__ void umma_f8f6f4_tmem_a(uint32_t d_tmem, uint32_t a_t
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (f16 inputs, f32
+// accumulate). A occupies 128 lanes; each 32-bit column holds two consecutive
+// K elements, the even one in the low half.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::mxf4 with block scaling: packed
 // e2m1 inputs (two per byte, K = 64 per instruction), ue8m0 scale factors
 // read from TMEM (one per 32 K elements), f32 accumulate. A occupies 128 lanes;
