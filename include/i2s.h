@@ -176,7 +176,7 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
  * Same operation, arguments, requirements and bits as i2s_mul_mat on the
  * tensor-core GEMV path, limited to 1 <= M <= 16 (BAD_SHAPE otherwise). The
  * scratch is a fixed array of I2S_NOALLOC_SCRATCH_BYTES inside the library's
- * device code, one per device. A problem needs 768 + up256(R*K/2) bytes of
+ * device code, one per device. A problem needs 1024 + up256(R*K/2) bytes of
  * it (R = 32 for M <= 8, else 48) plus, when K > 1536, up256(4*M*N) +
  * up256(4*ceil(N/128)), where up256 rounds up to a multiple of 256. A problem
  * that needs more is rejected with WORKSPACE_TOO_SMALL before anything is

@@ -188,6 +188,8 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
     int r = check_device();
     if (r) return r;
     QuantArgs a;
+    a.wmaps = nullptr;
+    a.n_wmaps = 0;
     a.status = nullptr;
     a.zero = nullptr;
     a.zero_16 = 0;
@@ -207,9 +209,12 @@ static size_t split_area_bytes(int64_t M, int64_t N) {
     return align_up((size_t)M * (size_t)N * 4) + align_up(tiles * 4);
 }
 
+// TMA tensor maps of the GEMV's weight matrices (one per problem), at the end.
+static size_t wmap_area(int count) { return align_up((size_t)count * sizeof(CUtensorMap)); }
+
 size_t i2s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (!i2s_shape_ok(N, K, M)) return 0;
-    return kHeader + act_slot_bytes(M, K) + split_area_bytes(M, N);
+    return kHeader + act_slot_bytes(M, K) + split_area_bytes(M, N) + wmap_area(1);
 }
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
@@ -240,6 +245,8 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     const int Kp = (int)round_up(K, 256);
 
     QuantArgs qa;
+    qa.wmaps = nullptr;
+    qa.n_wmaps = 0;
     qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     qa.zero = nullptr;
     qa.zero_16 = 0;
@@ -328,6 +335,8 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     int r;
     if (phases & 1) {
         static thread_local QuantArgs qa;
+        qa.wmaps = nullptr;
+        qa.n_wmaps = 0;
         qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         qa.zero = nullptr;
         qa.zero_16 = 0;
@@ -409,8 +418,14 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     const size_t dot_off_bytes = off;
     const size_t ticket_off_bytes = off + align_up(dots * 4);
     const size_t split_bytes = align_up(dots * 4) + align_up(tickets * 4);
+    // one TMA map per weight matrix, written by the quantization launch
+    CUtensorMap* wmaps = reinterpret_cast<CUtensorMap*>(base + dot_off_bytes + split_bytes);
     if (phases & 1) {
         static thread_local QuantArgs qa;
+        if (!make_u8_operand_map(&qa.wtmpl, wmaps, kTcTileW, 128, kTcTileW)) return I2S_E_CUDA;
+        qa.wmaps = wmaps;
+        qa.n_wmaps = count;
+        for (int i = 0; i < count; ++i) qa.wj[i] = WMapJob{probs[i].w_i2s, (int)probs[i].N, (int)probs[i].K};
         qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         qa.zero = split_bytes ? reinterpret_cast<uint4*>(base + dot_off_bytes) : nullptr;
         qa.zero_16 = split_bytes / 16;
@@ -435,10 +450,11 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         for (int a = 0; a < n_act; ++a)
             if (!make_u8_operand_map(&ta.maps[a], base + slots[a].op_off, gemv_tc_op_rows(Mp),
-                                     (int)(probs[first[a]].K / 2)))
+                                     (int)(probs[first[a]].K / 2), gemv_tc_op_rows(Mp)))
                 return I2S_E_CUDA;
         ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off_bytes);
         ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off_bytes);
+        ta.wmaps = wmaps;
         int units = 0, dot_elems = 0, ticket_elems = 0;
         for (int i = 0; i < count; ++i) {
             const i2s_problem& q = probs[i];
@@ -494,7 +510,7 @@ size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_
                 tickets += (size_t)((probs[i].N + kTcTileW - 1) / kTcTileW);
             }
         }
-        total += align_up(dots * 4) + align_up(tickets * 4);
+        total += align_up(dots * 4) + align_up(tickets * 4) + wmap_area(count);
     }
     return total;
 }

@@ -316,15 +316,16 @@ bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor map of the GEMV's e4m3 operand: `rows` x `K` bytes (K contiguous),
-// box 128 x rows (one K block of every operand row), 128-byte swizzle.
-bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes) {
+// 2-D tensor map of a uint8 matrix of `rows` x `row_bytes` (row-major), box
+// 128 bytes x box_rows, 128-byte swizzle, zero fill beyond the extents: the
+// GEMV's activation operand and the template of its weight maps.
+bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes, int box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     std::memset(map, 0, sizeof(*map));
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128u, (cuuint32_t)rows};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -31,11 +31,11 @@
 //
 // Roles (persistent CTAs, contiguous ranges of work units, 128 weight rows per
 // tile, 512 K positions per pipeline stage):
-//   warp 8     weight producer: each row's 128 packed bytes of a stage, copied
-//              with cp.async by 8 consecutive lanes (a warp instruction moves 4
-//              whole rows) into a 3-stage shared ring (rows padded to 144 bytes
-//              so the 16-byte reads are free of bank conflicts), completion
-//              signalled on an mbarrier;
+//   warp 8     weight producer: one TMA box per stage (128 rows x 128 packed
+//              bytes, 128-byte swizzle, so the converters' 16-byte row reads
+//              are free of bank conflicts) into a 3-stage shared ring. Each
+//              weight matrix has its own tensor map, written into the
+//              workspace by the quantization launch from a template;
 //   warps 0-3  converters: thread = weight row = TMEM lane reads its row's 128
 //              bytes, expands them and tcgen05.st's them into a 2-stage TMEM
 //              ring of A operands (64 columns per stage);
@@ -64,13 +64,12 @@ constexpr int kMmaWarpGv = 9;
 constexpr int kBProdWarp = 10;
 constexpr int kKB = 512;               // K positions per pipeline stage (128 packed bytes per row)
 constexpr int kStageBytes = kKB / 4;
-constexpr int kWStages = 3;            // weight ring depth
-constexpr int kWPitch = 144;           // padded bytes per row in the weight ring
+constexpr int kWStages = 3;            // weight ring depth (16 KB stages, 128-byte swizzle)
 constexpr int kStagesGv = 2;           // TMEM A ring depth (stages of 64 columns)
 constexpr int kBRingBytes = 36 * 1024; // activation ring: 4 stages of 8 KB (M' = 8) or 3 of 12 KB (M' = 16)
 constexpr int kBStagesMax = 8;
 constexpr int kTileRows = 128;
-constexpr int kWStageBytes = kTileRows * kWPitch;
+constexpr int kWStageBytes = kTileRows * kStageBytes;
 constexpr uint32_t kTmemColsGv = 256;
 // TMEM columns: A stages 0..127, accumulator 0 at 128 (up to 48 columns),
 // block scales 176..191, accumulator 1 at 192.
@@ -103,20 +102,6 @@ constexpr size_t kSmemGvUsed = 1024 + (size_t)kBRingBytes + (size_t)kWStages * k
 // 512 TMEM columns for its whole life.
 constexpr size_t kSmemGvBytes = kSmemGvUsed > 80 * 1024 ? kSmemGvUsed : 80 * 1024;
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    const int n = valid ? 16 : 0;   // 0 source bytes: the 16 bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Arrives on `bar` once every cp.async this thread issued so far has completed
-// (the arrival is counted in the barrier's expected count: .noinc).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Problem table copied into shared memory at kernel start (parameter-space
 // reads through a generic pointer are slow once the table misses the constant
 // cache, and every role resolves a problem at each segment).
@@ -125,7 +110,7 @@ struct SProb {
     const float* act_scale;
     const int32_t* row_sum;
     float* y;
-    int N, K, map, unit0, chunks, dot_off, ticket_off, pad;
+    int N, K, map, unit0, chunks, dot_off, ticket_off, pidx;
 };
 
 constexpr int kChunkStages = kGemvChunkPositions / kKB;   // 3 stages per work unit
@@ -138,7 +123,7 @@ struct Seg {
     const float* act_scale;
     const int32_t* row_sum;
     float* y;
-    int N, K, map, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units;
+    int N, K, map, pidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units;
     bool live;
 };
 
@@ -163,6 +148,7 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     g.N = P.N;
     g.K = P.K;
     g.map = P.map;
+    g.pidx = P.pidx;
     g.chunks = P.chunks;
     g.dot_off = P.dot_off;
     g.ticket_off = P.ticket_off;
@@ -217,11 +203,12 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     const int n_sp = s_prange[1] - p_first + 1;
     for (int i = tid; i < n_sp; i += kThreadsGv) {
         const TcProb& P = a.p[p_first + i];
-        sp[i] = SProb{P.w, P.act_scale, P.row_sum, P.y, P.N, P.K, P.map, P.tile0, P.chunks, P.dot_off, P.ticket_off, 0};
+        sp[i] = SProb{P.w, P.act_scale, P.row_sum, P.y, P.N, P.K, P.map, P.tile0, P.chunks, P.dot_off, P.ticket_off,
+                      p_first + i};
     }
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
-            tc::mbar_init(&S.full_w[s], 32);                  // one cp.async-completion arrival per producer lane
+            tc::mbar_init(&S.full_w[s], 1);                   // the producer's arrive.expect_tx (+ TMA bytes)
             tc::mbar_init(&S.empty_w[s], kCvtWarpsGv * 32);
         }
         for (int s = 0; s < kStagesGv; ++s) {
@@ -262,40 +249,37 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
 
     if (warp == kWProdWarp) {
         // --------------------------------------------------- weight producer
-        // Per stage, each row's contiguous packed bytes (up to 128) are copied
-        // with cp.async, 8 consecutive lanes per row (a warp instruction moves
-        // 4 whole rows), into a 3-stage ring; completion is signalled on the
-        // stage's mbarrier by every lane.
-        int ws = 0;
-        uint32_t wphase = 0;
-        bool ok = true;
-        for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
-            const int row_bytes = g.K / 4;
-            const int end = min(g.st_hi * kStageBytes, row_bytes);
-            for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
-                const int bytes = min(kStageBytes, end - off);   // 32, 64, 96 or 128
-                if (!tc::mbar_wait_idle(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
-                const uint8_t* base = g.w + (size_t)g.n0 * row_bytes + off;
-                uint8_t* dst = sW + (size_t)ws * kWStageBytes;
-                if (bytes == kStageBytes) {
-                    const int col = lane & 7;
-                    for (int row = lane >> 3; row < kTileRows; row += 4) {
-                        const bool v = g.n0 + row < g.N;
-                        cp_async16(dst + row * kWPitch + col * 16, v ? base + (size_t)row * row_bytes + col * 16 : g.w, v);
-                    }
-                } else {
-                    const int cpr = bytes / 16;   // 16-byte chunks per row
-                    for (int ch = lane; ch < kTileRows * cpr; ch += 32) {
-                        const int row = ch / cpr, col = ch - row * cpr;
-                        const bool v = g.n0 + row < g.N;
-                        cp_async16(dst + row * kWPitch + col * 16, v ? base + (size_t)row * row_bytes + col * 16 : g.w, v);
-                    }
+        // One TMA box per stage: 128 rows x 128 packed bytes of the tile, from
+        // the problem's weight map (written by the quantization launch; rows
+        // past N and bytes past K/4 are zero-filled), into a 3-stage ring.
+        if (lane == 0) {
+            int ws = 0;
+            uint32_t wphase = 0;
+            bool pending[kWStages] = {};
+            uint32_t pending_phase[kWStages] = {};
+            bool ok = true;
+            int cur_p = -1;
+            for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
+                const CUtensorMap* map = a.wmaps + g.pidx;
+                if (g.pidx != cur_p) {   // first use of this map: order it after the writer's release
+                    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                    cur_p = g.pidx;
                 }
-                cp_async_arrive(&S.full_w[ws]);
-                if (++ws == kWStages) { ws = 0; wphase ^= 1; }
+                const int row_bytes = g.K / 4;
+                const int end = min(g.st_hi * kStageBytes, row_bytes);
+                for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
+                    if (!tc::mbar_wait_idle(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&S.full_w[ws], kWStageBytes);
+                    tc::tma_load_2d(sW + (size_t)ws * kWStageBytes, map, off, g.n0, &S.full_w[ws]);
+                    pending[ws] = true;
+                    pending_phase[ws] = wphase;
+                    if (++ws == kWStages) { ws = 0; wphase ^= 1; }
+                }
             }
+            if (!ok)
+                for (int s2 = 0; s2 < kWStages; ++s2)
+                    if (pending[s2]) tc::mbar_wait(&S.full_w[s2], pending_phase[s2], abort_flag, kWaitLimitGv / 8);
         }
-        cp_async_wait<0>();
     } else if (warp < kCvtWarpsGv) {
         // ---------------------------------------------------------- converters
         // thread = weight row = TMEM lane. First the block scales (all 1.0),
@@ -315,18 +299,17 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         uint32_t wphase = 0, phase = 0, bphase = 0;
         bool ok = true;
         for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
-            const bool valid = g.n0 + r < g.N;
             const int row_bytes = g.K / 4;
             const int end = min(g.st_hi * kStageBytes, row_bytes);
             for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
                 const int bytes = min(kStageBytes, end - off);
                 if (!tc::mbar_wait_idle(&S.full_w[ws], wphase, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
-                const uint8_t* row = sW + (size_t)ws * kWStageBytes + r * kWPitch;
+                const uint8_t* wst = sW + (size_t)ws * kWStageBytes;
                 uint4 c[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 8; ++i) {   // rows past N and bytes past K/4 arrive as zeros
                     c[i] = make_uint4(0, 0, 0, 0);
-                    if (valid && 16 * i < bytes) c[i] = *reinterpret_cast<const uint4*>(row + 16 * i);
+                    if (16 * i < bytes) c[i] = *reinterpret_cast<const uint4*>(wst + tc::sw128_offset(r, i));
                 }
                 tc::mbar_arrive(&S.empty_w[ws]);   // this row's bytes of the ring stage are read
                 if (++ws == kWStages) { ws = 0; wphase ^= 1; }

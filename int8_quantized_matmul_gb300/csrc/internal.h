@@ -31,7 +31,17 @@ struct QuantJob {
     int Kp;           // K rounded up to the layout's padding (GEMV: 256)
 };
 
+// A weight matrix whose TMA tensor map the quantization launch writes for the
+// tensor-core GEMV (kQuantE2M1Tc only).
+struct WMapJob {
+    const void* w;   // I2_S bytes (payload N x K/4)
+    int N;
+    int K;
+};
+
 struct QuantArgs {
+    CUtensorMap wtmpl;  // template map: uint8 2-D, box 128 bytes x 128 rows, 128-byte swizzle
+    CUtensorMap* wmaps; // if set, n_wmaps maps written here, wj[i] -> wmaps[i]
     uint32_t* status;   // if set, cleared by the launch (the matmul that follows reports into it)
     uint4* zero;        // if set, zero_16 16-byte words zeroed by the launch (split-K partials)
     unsigned long long zero_16;
@@ -39,6 +49,8 @@ struct QuantArgs {
     int M;
     int rows;           // rows written per job: M, or M' (8 or 16) for kQuantE2M1Tc
     int layout;
+    int n_wmaps;
+    WMapJob wj[kMaxGroup];
     QuantJob j[kMaxGroup];
 };
 
@@ -97,6 +109,7 @@ struct TcProb {
 
 struct TcArgs {
     CUtensorMap maps[kTcMaxMaps];
+    const CUtensorMap* wmaps; // GEMV: per-problem weight maps in the workspace (written by the quantize launch)
     uint32_t* status;         // workspace status word (timeouts)
     int32_t* dot_base;        // GEMV split-K partial dots (zeroed by the quantize launch)
     uint32_t* ticket_base;    // GEMV split-K chunk counters (zeroed by the quantize launch)
@@ -124,8 +137,8 @@ static_assert(sizeof(GemvArgs) <= 32764, "GemvArgs exceeds the kernel parameter 
 static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
 
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
-// rows x row_bytes uint8 matrix, box {128 bytes, rows}, 128-byte swizzle
-bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes);
+// rows x row_bytes uint8 matrix, box {128 bytes, box_rows}, 128-byte swizzle
+bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes, int box_rows);
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 

@@ -5,11 +5,12 @@
 // It runs the same two launches as i2s_mul_mat's tensor-core GEMV path -- the
 // per-row quantization into the e2m1 digit operand, then the tcgen05 GEMV --
 // for a single problem, with the workspace replaced by g_scratch below. The
-// scratch layout is the one the workspace path uses for one problem:
+// scratch layout:
 //   [0, 256)          status word (cleared by the quantization launch)
-//   [256, 512)        act_scale, M F32
-//   [512, 768)        row_sum, M int32
-//   [768, op_end)     e2m1 operand: gemv_tc_op_rows(Mp) digit rows of K/2 bytes
+//   [256, 512)        the weight matrix's TMA map (written by the quantization launch)
+//   [512, 768)        act_scale, M F32
+//   [768, 1024)       row_sum, M int32
+//   [1024, op_end)    e2m1 operand: gemv_tc_op_rows(Mp) digit rows of K/2 bytes
 //   [op_end, ...)     K > 1536 only: M x N int32 split-K partials, then one
 //                     uint32 chunk counter per 128-row tile; both zeroed by
 //                     the quantization launch of every call.
@@ -89,7 +90,8 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     const int Mp = gemv_tc_mp(M);
     const int op_rows = gemv_tc_op_rows(Mp);
     const bool split = K > kGemvChunkPositions;
-    const size_t scale_off = kSlotAlign;
+    const size_t map_off = kSlotAlign;
+    const size_t scale_off = map_off + kSlotAlign;
     const size_t sum_off = scale_off + up256((size_t)M * 4);
     const size_t op_off = sum_off + up256((size_t)M * 4);
     const size_t dot_off = op_off + up256((size_t)op_rows * (size_t)(K / 2));
@@ -109,6 +111,11 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     // Phase 1: quantize x into the operand; the same launch clears the status
     // word and the split-K partials and counters left by the previous call.
     QuantArgs qa;
+    CUtensorMap* wmap = reinterpret_cast<CUtensorMap*>(base + map_off);
+    if (!make_u8_operand_map(&qa.wtmpl, wmap, kTcTileW, 128, kTcTileW)) return I2S_E_CUDA;
+    qa.wmaps = wmap;
+    qa.n_wmaps = 1;
+    qa.wj[0] = WMapJob{w_i2s, (int)N, (int)K};
     qa.status = status;
     qa.zero = split ? reinterpret_cast<uint4*>(base + dot_off) : nullptr;
     qa.zero_16 = split ? (end - dot_off) / 16 : 0;
@@ -126,7 +133,8 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     ta.M = (int)M;
     ta.BN = Mp;
     ta.status = status;
-    if (!make_u8_operand_map(&ta.maps[0], base + op_off, op_rows, (int)(K / 2))) return I2S_E_CUDA;
+    if (!make_u8_operand_map(&ta.maps[0], base + op_off, op_rows, (int)(K / 2), op_rows)) return I2S_E_CUDA;
+    ta.wmaps = wmap;
     ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off);
     ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off);
     const int chunks = (int)((K + kGemvChunkPositions - 1) / kGemvChunkPositions);

@@ -232,11 +232,32 @@ __device__ __forceinline__ int emit_unit(const float4 (&v)[4], float inv, int u,
     return sum;
 }
 
+// Writes the TMA tensor map of weight matrix i: the template (uint8 2-D, box
+// 128 bytes x 128 rows, 128-byte swizzle) with its address, extents (K/4 bytes
+// by N rows) and row stride replaced, then releases it to the tensor-map proxy
+// for the GEMV launch that follows.
+__device__ __forceinline__ void write_weight_map(const QuantArgs& a, int i) {
+    CUtensorMap* dst = a.wmaps + i;
+    const uint4* src = reinterpret_cast<const uint4*>(&a.wtmpl);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(CUtensorMap) / 16); ++k) d[k] = src[k];
+    const WMapJob& J = a.wj[i];
+    const uint32_t row_bytes = (uint32_t)(J.K / 4);
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(J.w) : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 0, %1;" ::"l"(dst), "r"(row_bytes) : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst), "r"((uint32_t)J.N) : "memory");
+    asm volatile("tensormap.replace.tile.global_stride.global.b1024.b64 [%0], 0, %1;" ::"l"(dst),
+                 "l"((uint64_t)row_bytes) : "memory");
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_constant__ QuantArgs a) {
     __shared__ float s_red[kQThreads / 32];
     __shared__ int s_sum[kQThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
+    for (int i = blockIdx.x * kQThreads + tid; i < a.n_wmaps; i += gridDim.x * kQThreads) write_weight_map(a, i);
     for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
          i += (unsigned long long)gridDim.x * kQThreads)
         a.zero[i] = make_uint4(0u, 0u, 0u, 0u);

@@ -43,7 +43,7 @@ def need_bytes(M, N, K):
     """Scratch the call needs, by the formula documented with the entry point."""
     up = lambda v: (v + 255) // 256 * 256
     rows = 32 if M <= 8 else 48
-    n = 768 + up(rows * K // 2)
+    n = 1024 + up(rows * K // 2)
     if K > 1536:
         n += up(4 * M * N) + up(4 * ((N + 127) // 128))
     return n
