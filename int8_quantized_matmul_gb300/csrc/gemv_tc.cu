@@ -123,7 +123,7 @@ struct Seg {
     const float* act_scale;
     const int32_t* row_sum;
     float* y;
-    int N, K, map, pidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units;
+    int N, K, map, pidx, sidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units;
     bool live;
 };
 
@@ -141,6 +141,7 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     }
     const SProb& P = sp[lo];
     const int local = u - P.unit0;
+    g.sidx = lo;
     g.w = P.w;
     g.act_scale = P.act_scale;
     g.row_sum = P.row_sum;
@@ -161,6 +162,41 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     g.st_lo = g.c_lo * kChunkStages;
     g.st_hi = min(KB, g.c_hi * kChunkStages);
     return g;
+}
+
+// The segment after g, starting at unit u (< u_hi when live). A segment that
+// does not reach u_hi ends at its tile's last chunk, so the next one starts at
+// chunk 0 of the following tile (or of the next problem's first tile): a step
+// with no search and no division, unlike seg_at.
+__device__ __forceinline__ Seg seg_next(const SProb* sp, const Seg& g, int u, int u_hi) {
+    Seg n;
+    n.live = u < u_hi;
+    if (!n.live) return n;
+    n.sidx = g.sidx;
+    n.tile = g.tile + 1;
+    if (n.tile >= (sp[n.sidx].N + kTileRows - 1) / kTileRows) {
+        ++n.sidx;
+        n.tile = 0;
+    }
+    const SProb& P = sp[n.sidx];
+    n.w = P.w;
+    n.act_scale = P.act_scale;
+    n.row_sum = P.row_sum;
+    n.y = P.y;
+    n.N = P.N;
+    n.K = P.K;
+    n.map = P.map;
+    n.pidx = P.pidx;
+    n.chunks = P.chunks;
+    n.dot_off = P.dot_off;
+    n.ticket_off = P.ticket_off;
+    n.c_lo = 0;
+    n.c_hi = min(P.chunks, u_hi - u);
+    n.units = n.c_hi;
+    n.n0 = n.tile * kTileRows;
+    n.st_lo = 0;
+    n.st_hi = min((P.K + kKB - 1) / kKB, n.c_hi * kChunkStages);
+    return n;
 }
 
 template <int Mp>
@@ -245,7 +281,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     };
 
     int ucur = u_begin;   // each role advances its own copy of the unit cursor
-    auto next_seg = [&](const Seg& g) { ucur += g.units; return seg_at(sp, n_sp, ucur, u_end); };
+    auto next_seg = [&](const Seg& g) { ucur += g.units; return seg_next(sp, g, ucur, u_end); };
 
     if (warp == kWProdWarp) {
         // --------------------------------------------------- weight producer
@@ -356,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 const CUtensorMap* map = &a.maps[g.map];
                 {   // fetch the next segment's descriptor while this one streams
-                    const Seg gn = seg_at(sp, n_sp, ucur + g.units, u_end);
+                    const Seg gn = seg_next(sp, g, ucur + g.units, u_end);
                     if (gn.live && gn.map != g.map) tc::tma_prefetch_desc(&a.maps[gn.map]);
                 }
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
