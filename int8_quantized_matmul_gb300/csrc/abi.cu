@@ -394,6 +394,9 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
 // Tensor-core GEMV path (M <= 16): phase 1 quantizes every distinct activation
 // into the e4m3 hi/lo operand rows, phase 2 runs one persistent launch over all
 // problems (two CTAs per SM). Arguments are validated by the callers.
+// Unit shares of the first and second CTA on an SM for a full GEMV grid.
+constexpr int kGemvShareFirst = 23, kGemvShareSecond = 17;
+
 static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
                        i2s_stream_t stream, int phases) {
     std::vector<int> act_of, first;
@@ -486,6 +489,10 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         int grid = grid_ctas > 0 ? grid_ctas : cap;
         if (grid > cap) grid = cap;
         if (grid > tiles) grid = tiles;
+        // With a full grid (two CTAs per SM) the first CTA on each SM gets the
+        // larger share measured to make both finish together.
+        ta.share_first = grid == cap ? kGemvShareFirst : 1;
+        ta.share_second = grid == cap ? kGemvShareSecond : 1;
         r = cuda_status(launch_gemv_tc(ta, grid, stream));
         if (r) return r;
     }

@@ -18,7 +18,8 @@
 //   * B: each quantized activation q in [-127,127] is written as three digits
 //     q = d0 + 8*d1 + 64*d2 (d0, d1 in [-4,3], d2 in [-2,2]), each an exact
 //     e2m1 value, one operand row per digit: row j*M' + m (M' = 8 or 16), so
-//     MMA N = 32 (M' = 8, with 8 zero rows) or 48.
+//     MMA N = 32 (M' = 8, with 8 unused rows) or 48. Rows of absent
+//     activation rows hold stale values; their D columns are never read.
 //   * D column j*M' + m holds sum_k (c/2)*d_j: a multiple of 1/2 below 2^23,
 //     exact in f32. dot = 2*D_0 + 16*D_1 + 128*D_2, formed in integers.
 // The epilogue is the pages' y = (float)(dot - row_sum) * (w_scale*act_scale).
@@ -217,8 +218,18 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // this CTA's contiguous share of the work units
-    const int u_begin = (int)(((long long)blockIdx.x * a.total_tiles) / gridDim.x);
-    const int u_end = (int)(((long long)(blockIdx.x + 1) * a.total_tiles) / gridDim.x);
+    // This CTA's contiguous share of the work units. With two CTAs per SM the
+    // first CTA placed on an SM (the first half of the grid) is issued ahead of
+    // the second and runs faster, so the host may give it a larger share.
+    const int h = (int)gridDim.x / 2;
+    const long long w1 = a.share_first, w2 = a.share_second;
+    const long long den = (long long)h * w1 + (long long)((int)gridDim.x - h) * w2;
+    auto bound = [&](int b) {
+        const long long num = b <= h ? (long long)b * w1 : (long long)h * w1 + (long long)(b - h) * w2;
+        return (int)(num * a.total_tiles / den);
+    };
+    const int u_begin = bound((int)blockIdx.x);
+    const int u_end = bound((int)blockIdx.x + 1);
 
     // Copy the (few) problem-table entries this CTA's unit range touches.
     __shared__ int s_prange[2];

@@ -120,6 +120,8 @@ struct TcArgs {
                               // GEMV: M' (8 or 16), MMA N = gemv_tc_op_rows(M')
 
     int total_tiles;          // GEMM: tiles; GEMV: work units
+    int share_first;          // GEMV: relative unit shares of the first and second half of the
+    int share_second;         //   grid (the first and second CTA placed on each SM)
     TcProb p[kMaxGroup];
 };
 

@@ -152,6 +152,8 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     p.dot_off = 0;
     p.ticket_off = 0;
     ta.total_tiles = row_tiles * chunks;
+    ta.share_first = 1;
+    ta.share_second = 1;
     int grid = 2 * (d->sms > 0 ? d->sms : 152);
     if (grid > ta.total_tiles) grid = ta.total_tiles;
     if (launch_gemv_tc(ta, grid, stream) != cudaSuccess) return I2S_E_CUDA;

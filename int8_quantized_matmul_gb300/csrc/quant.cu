@@ -158,7 +158,10 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
 // Tensor-core GEMV operand (kQuantE2M1Tc). Each q in [-127, 127] is written as
 // three digits q = d0 + 8*d1 + 64*d2 with d0, d1 in [-4, 3] and d2 in [-2, 2],
 // every one exact in e2m1; digit j of activation row m goes to operand row
-// j*M' + m (rows 3M'.. are zero padding up to the MMA N). Within a 128-position
+// j*M' + m. The operand rows of absent activation rows (m >= M) and the rows
+// after 3M' are never written: each MMA output column depends only on its own
+// operand row, every 4-bit pattern is a finite e2m1 value, and the GEMV reads
+// only the columns of present rows. Within a 128-position
 // group the K order is the one the GEMV's converters produce from the packed
 // weight bytes: element 16w + 8t + 2i + h holds position 32s + 4w + i, where
 // (t, h) = (0, 0), (0, 1), (1, 0), (1, 1) for bit-pair slices s = 3, 1, 2, 0.
@@ -198,9 +201,29 @@ __device__ __forceinline__ float unit_amax(const float4 (&v)[4]) {
     return m;
 }
 
+// The three e2m1 digit nibbles of q, at bits 0, 8 and 16 (shared-memory table
+// indexed by q + 127, filled at kernel start from base8_digits/e2m1_digit).
+__device__ __forceinline__ uint32_t digit_code(int q) {
+    int d[3];
+    base8_digits(q, d);
+    return e2m1_digit(d[0]) | (e2m1_digit(d[1]) << 8) | (e2m1_digit(d[2]) << 16);
+}
+
+// Four codes (byte j of c[i] = nibble pair of digit j for word byte i) ->
+// the word of digit rows 0, 1 and 2 (byte i of out[j] = byte j of c[i]).
+__device__ __forceinline__ void transpose_codes(const uint32_t (&c)[4], uint32_t (&out)[3]) {
+    const uint32_t lo01 = __byte_perm(c[0], c[1], 0x5140);   // c0.b0 c1.b0 c0.b1 c1.b1
+    const uint32_t lo23 = __byte_perm(c[2], c[3], 0x5140);
+    const uint32_t hi01 = __byte_perm(c[0], c[1], 0x0062);   // c0.b2 c1.b2
+    const uint32_t hi23 = __byte_perm(c[2], c[3], 0x0062);
+    out[0] = __byte_perm(lo01, lo23, 0x5410);
+    out[1] = __byte_perm(lo01, lo23, 0x7632);
+    out[2] = __byte_perm(hi01, hi23, 0x5410);
+}
+
 // Quantizes a unit, writes its three digit words, returns the sum of its q.
 __device__ __forceinline__ int emit_unit(const float4 (&v)[4], float inv, int u, uint8_t* op, size_t row_bytes, int Mp,
-                                         int m) {
+                                         int m, const uint32_t* code) {
     int q[4][4];
     int sum = 0;
 #pragma unroll
@@ -211,21 +234,16 @@ __device__ __forceinline__ int emit_unit(const float4 (&v)[4], float inv, int u,
         q[s][3] = quantize_one(v[s].w, inv);
         sum += q[s][0] + q[s][1] + q[s][2] + q[s][3];
     }
-    uint32_t w0[3] = {0u, 0u, 0u}, w1[3] = {0u, 0u, 0u};
+    // word t = 0: low nibble slice 3, high nibble slice 1; t = 1: slices 2 and 0
+    uint32_t c0[4], c1[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int d0[3], d1[3], d2[3], d3[3];
-        base8_digits(q[0][i], d0);
-        base8_digits(q[1][i], d1);
-        base8_digits(q[2][i], d2);
-        base8_digits(q[3][i], d3);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            // word t = 0: low nibble slice 3, high nibble slice 1; t = 1: slices 2 and 0
-            w0[j] |= (e2m1_digit(d3[j]) | (e2m1_digit(d1[j]) << 4)) << (8 * i);
-            w1[j] |= (e2m1_digit(d2[j]) | (e2m1_digit(d0[j]) << 4)) << (8 * i);
-        }
+        c0[i] = code[q[3][i] + 127] | (code[q[1][i] + 127] << 4);
+        c1[i] = code[q[2][i] + 127] | (code[q[0][i] + 127] << 4);
     }
+    uint32_t w0[3], w1[3];
+    transpose_codes(c0, w0);
+    transpose_codes(c1, w1);
 #pragma unroll
     for (int j = 0; j < 3; ++j)
         reinterpret_cast<uint2*>(op + (size_t)(j * Mp + m) * row_bytes)[u] = make_uint2(w0[j], w1[j]);
@@ -255,29 +273,20 @@ __device__ __forceinline__ void write_weight_map(const QuantArgs& a, int i) {
 __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_constant__ QuantArgs a) {
     __shared__ float s_red[kQThreads / 32];
     __shared__ int s_sum[kQThreads / 32];
+    __shared__ uint32_t s_code[255];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 255) s_code[tid] = digit_code(tid - 127);
     if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
     for (int i = blockIdx.x * kQThreads + tid; i < a.n_wmaps; i += gridDim.x * kQThreads) write_weight_map(a, i);
     for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
          i += (unsigned long long)gridDim.x * kQThreads)
         a.zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    const QuantJob& J = a.j[blockIdx.x / a.rows];
-    const int m = blockIdx.x % a.rows;
+    const QuantJob& J = a.j[blockIdx.x / a.M];   // one CTA per present activation row
+    const int m = blockIdx.x % a.M;
     const int Mp = a.rows;
     const int K = J.K, U = K / 16;
     const size_t row_bytes = (size_t)K / 2;
     uint8_t* op = static_cast<uint8_t*>(J.out);
-    if (3 * Mp + m < gemv_tc_op_rows(Mp)) {   // padding rows after the three digit blocks
-        uint2* z = reinterpret_cast<uint2*>(op + (size_t)(3 * Mp + m) * row_bytes);
-        for (int u = tid; u < U; u += kQThreads) z[u] = make_uint2(0u, 0u);
-    }
-    if (m >= a.M) {   // operand rows of absent activation rows are zero
-        for (int j = 0; j < 3; ++j) {
-            uint2* z = reinterpret_cast<uint2*>(op + (size_t)(j * Mp + m) * row_bytes);
-            for (int u = tid; u < U; u += kQThreads) z[u] = make_uint2(0u, 0u);
-        }
-        return;
-    }
     const float4* x4 = reinterpret_cast<const float4*>(J.x + (size_t)m * K);
 
     float4 cache[kQ4Cache][4];
@@ -308,12 +317,12 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
 #pragma unroll
     for (int c = 0; c < kQ4Cache; ++c) {
         const int u = tid + c * kQThreads;
-        if (u < U) sum += emit_unit(cache[c], inv, u, op, row_bytes, Mp, m);
+        if (u < U) sum += emit_unit(cache[c], inv, u, op, row_bytes, Mp, m, s_code);
     }
     for (int u = tid + kQ4Cache * kQThreads; u < U; u += kQThreads) {
         float4 v[4];
         load_unit(x4, u, v);
-        sum += emit_unit(v, inv, u, op, row_bytes, Mp, m);
+        sum += emit_unit(v, inv, u, op, row_bytes, Mp, m, s_code);
     }
     sum = warp_sum(sum);
     if (lane == 0) s_sum[warp] = sum;
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
     if (a.layout == kQuantE2M1Tc)
-        k_quant_rows_tc4<<<a.count * a.rows, kQThreads, 0, s>>>(a);
+        k_quant_rows_tc4<<<a.count * a.M, kQThreads, 0, s>>>(a);
     else
         k_quant_rows<<<a.count * a.rows, kQThreads, 0, s>>>(a);
     return cudaGetLastError();
