@@ -55,6 +55,7 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreadsTc = 320;
 constexpr int kStagesTc = 4;
+constexpr int kCvtPrefetch = 8;             // K blocks of packed codes each converter keeps in flight
 constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
 constexpr int kATileBytes = kTileW * 128;   // 16 KB
@@ -63,12 +64,15 @@ constexpr int kTmemCols = 512;
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
 
 struct SmemTc {
+    float sc_col[2][256];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
+    int rs_col[2][256];     // epilogue: row_sum[m] per tile column, by accumulator
     uint64_t full_a[kStagesTc];
     uint64_t full_b[kStagesTc];
     uint64_t empty[kStagesTc];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    uint64_t stage_bar;     // the epilogue threads have staged a tile's column factors
     uint32_t tmem_base;
     int abort;
 };
@@ -117,6 +121,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             tc::mbar_init(&S.tmem_empty[b], kEpiWarps * 32);
         }
         tc::mbar_init(&S.mma_done, 1);
+        tc::mbar_init(&S.stage_bar, kEpiWarps * 32);
         S.abort = 0;
         tc::fence_mbar_init();
     }
@@ -178,24 +183,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             const int KB = P.K / kBlockK;
             const uint8_t* src = P.w + (size_t)(n < P.N ? n : 0) * (P.K / 4);
             const bool valid = n < P.N;
-            uint4 cur = valid ? ldg_stream(src) : make_uint4(0, 0, 0, 0);
-            for (int kb = 0; kb < KB; ++kb) {
-                uint4 nxt = make_uint4(0, 0, 0, 0);
-                if (valid && kb + 1 < KB) nxt = ldg_stream(src + (size_t)(kb + 1) * 16);
-                if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(2); ok = false; break; }
-                uint8_t* dst = sA + (size_t)stage * kATileBytes;
-                const uint32_t words[4] = {cur.x, cur.y, cur.z, cur.w};
+            // the row's packed bytes, kCvtPrefetch K blocks ahead (16 bytes each)
+            uint4 buf[kCvtPrefetch];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    uint4 c0, c1;
-                    expand_word_f16(words[w], c0, c1);
-                    *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w)) = c0;
-                    *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w + 1)) = c1;
+            for (int j = 0; j < kCvtPrefetch; ++j)
+                buf[j] = (valid && j < KB) ? ldg_stream(src + (size_t)j * 16) : make_uint4(0, 0, 0, 0);
+            for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
+#pragma unroll
+                for (int j = 0; j < kCvtPrefetch; ++j) {
+                    const int kb = kb0 + j;
+                    if (kb >= KB) break;
+                    if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(2); ok = false; break; }
+                    uint8_t* dst = sA + (size_t)stage * kATileBytes;
+                    const uint32_t words[4] = {buf[j].x, buf[j].y, buf[j].z, buf[j].w};
+                    buf[j] = (valid && kb + kCvtPrefetch < KB) ? ldg_stream(src + (size_t)(kb + kCvtPrefetch) * 16)
+                                                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint4 c0, c1;
+                        expand_word_f16(words[w], c0, c1);
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w)) = c0;
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w + 1)) = c1;
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(&S.full_a[stage]);
+                    if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&S.full_a[stage]);
-                cur = nxt;
-                if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -237,28 +250,47 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
         // ------------------------------------------------------------ epilogue
         const int r = warp * 32 + lane;   // TMEM lane = weight row within the tile
         int acc = 0;
-        uint32_t acc_phase = 0;
+        uint32_t acc_phase = 0, stage_phase = 0;
         for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
             const TcProb& P = a.p[find_problem(a, tile)];
             const int local = tile - P.tile0;
             const int wt = local / P.n_act_tiles, at = local % P.n_act_tiles;
             const int n = wt * kTileW + r;
+            // stage the tile's per-column factors (w_scale * act_scale[m] and
+            // row_sum[m]) in shared memory while the accumulator fills
+            const int m_base = at * BN;
+            {
+                const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
+                float* sc_col = S.sc_col[acc];
+                int* rs_col = S.rs_col[acc];
+                for (int j = r; j < BN; j += kEpiWarps * 32) {
+                    const int m = m_base + j;
+                    sc_col[j] = m < a.M ? __fmul_rn(w_scale, P.act_scale[m]) : 0.0f;
+                    rs_col[j] = m < a.M ? P.row_sum[m] : 0;
+                }
+                // every epilogue thread has staged its columns (bounded wait)
+                tc::mbar_arrive(&S.stage_bar);
+                if (!tc::mbar_wait(&S.stage_bar, stage_phase, abort_flag, kWaitLimit)) { fail(16); break; }
+                stage_phase ^= 1;
+            }
             if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimit)) { fail(16); break; }
             tc::tc_fence_after();
-            const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
-            const int m_base = at * BN;
+            const float* sc_col = S.sc_col[acc];
+            const int* rs_col = S.rs_col[acc];
+            const int N = P.N, M = a.M;
+            float* y_col = P.y + n;   // this thread's output column
             for (int c = 0; c < (BN + 31) / 32; ++c) {
                 uint32_t v[32];
                 tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256 + c * 32), v);
                 tc::tmem_ld_wait();
-                if (n < P.N) {
-#pragma unroll 8
+                if (n < N) {
+#pragma unroll   // static indices keep v[] in registers
                     for (int j = 0; j < 32; ++j) {
-                        const int m = m_base + c * 32 + j;
-                        if (c * 32 + j < BN && m < a.M) {
+                        const int jj = c * 32 + j;
+                        const int m = m_base + jj;
+                        if (jj < BN && m < M) {
                             const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
-                            const float sc = __fmul_rn(w_scale, P.act_scale[m]);
-                            P.y[(size_t)m * P.N + n] = __fmul_rn(__int2float_rn(dot - P.row_sum[m]), sc);
+                            y_col[(size_t)m * N] = __fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]);
                         }
                     }
                 }
