@@ -17,12 +17,12 @@
 //   warps 0-3  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
 //              (w_scale * act_scale), coalesced F32 stores (warp w reads
 //              TMEM lanes 32w..32w+31 = weight rows of the tile);
-//   warps 4-7  converters: each thread owns one weight row of the 128-row
-//              tile, loads its 16 packed bytes per K block (64 positions),
-//              expands them to 64 f16 in the 128B-swizzled K-major layout and
-//              fences the writes into the async proxy;
-//   warp 8     TMA producer of the activation tile (f16, 128B swizzle);
-//   warp 9     TMEM allocation and the MMA issuer (one lane).
+//   warps 4-11 converters: two threads per weight row of the 128-row tile,
+//              each loading 8 of the row's 16 packed bytes per K block (64
+//              positions) and expanding them to 32 f16 in the 128B-swizzled
+//              K-major layout, then fencing the writes into the async proxy;
+//   warp 12    TMA producer of the activation tile (f16, 128B swizzle);
+//   warp 13    TMEM allocation and the MMA issuer (one lane).
 // MMA: M = 128 weight rows (the "swapped" A operand), N = up to 256
 // activation rows, K = 16 per instruction, 4 instructions per K block. Two
 // TMEM accumulators of 256 columns let the epilogue of one tile overlap the
@@ -50,10 +50,10 @@ namespace i2s {
 namespace {
 
 constexpr int kEpiWarps = 4;
-constexpr int kCvtWarps = 4;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreadsTc = 320;
+constexpr int kCvtWarps = 8;               // two threads per weight row, 8 packed bytes each
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreadsTc = 448;
 constexpr int kStagesTc = 4;
 constexpr int kCvtPrefetch = 8;             // K blocks of packed codes each converter keeps in flight
 constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
@@ -172,7 +172,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
         // ---------------------------------------------------------- converters
-        const int r = tid - kEpiWarps * 32;   // weight row within the tile
+        // two threads per weight row: thread half hf expands the row's packed
+        // bytes 8hf..8hf+7 of each K block (32 positions) into 4 f16 chunks
+        const int ct = tid - kEpiWarps * 32;
+        const int r = ct & (kTileW - 1);   // weight row within the tile
+        const int hf = ct >> 7;
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -181,13 +185,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             const int wt = (tile - P.tile0) / P.n_act_tiles;
             const int n = wt * kTileW + r;
             const int KB = P.K / kBlockK;
-            const uint8_t* src = P.w + (size_t)(n < P.N ? n : 0) * (P.K / 4);
             const bool valid = n < P.N;
-            // the row's packed bytes, kCvtPrefetch K blocks ahead (16 bytes each)
-            uint4 buf[kCvtPrefetch];
+            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4) + 8 * hf;
+            auto load = [&](int kb) {
+                return (valid && kb < KB) ? __ldg(reinterpret_cast<const uint2*>(src + (size_t)kb * 16))
+                                          : make_uint2(0u, 0u);
+            };
+            // the row's packed bytes, kCvtPrefetch K blocks ahead
+            uint2 buf[kCvtPrefetch];
 #pragma unroll
-            for (int j = 0; j < kCvtPrefetch; ++j)
-                buf[j] = (valid && j < KB) ? ldg_stream(src + (size_t)j * 16) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < kCvtPrefetch; ++j) buf[j] = load(j);
             for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
 #pragma unroll
                 for (int j = 0; j < kCvtPrefetch; ++j) {
@@ -195,15 +202,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                     if (kb >= KB) break;
                     if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(2); ok = false; break; }
                     uint8_t* dst = sA + (size_t)stage * kATileBytes;
-                    const uint32_t words[4] = {buf[j].x, buf[j].y, buf[j].z, buf[j].w};
-                    buf[j] = (valid && kb + kCvtPrefetch < KB) ? ldg_stream(src + (size_t)(kb + kCvtPrefetch) * 16)
-                                                               : make_uint4(0, 0, 0, 0);
+                    const uint32_t words[2] = {buf[j].x, buf[j].y};
+                    buf[j] = load(kb + kCvtPrefetch);
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
+                    for (int w = 0; w < 2; ++w) {
+                        const int word = 2 * hf + w;   // 32-bit word of the row's 16 bytes
                         uint4 c0, c1;
                         expand_word_f16(words[w], c0, c1);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w)) = c0;
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * w + 1)) = c1;
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word)) = c0;
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word + 1)) = c1;
                     }
                     tc::fence_proxy_async_smem();
                     tc::mbar_arrive(&S.full_a[stage]);
