@@ -286,24 +286,45 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             const int* rs_col = S.rs_col[acc];
             const int N = P.N, M = a.M;
             float* y_col = P.y + n;   // this thread's output column
-            for (int c = 0; c < (BN + 31) / 32; ++c) {
-                uint32_t v[32];
-                tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256 + c * 32), v);
-                tc::tmem_ld_wait();
-                if (n < N) {
+            // TMEM -> registers 32 columns at a time, the load of the next slice
+            // overlapping the stores of this one; the accumulator is released as
+            // soon as its last slice is in registers
+            const uint32_t d_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
+            const int C = (BN + 31) / 32;
+            auto store_slice = [&](int c, const uint32_t (&v)[32]) {
+                if (n >= N) return;
 #pragma unroll   // static indices keep v[] in registers
-                    for (int j = 0; j < 32; ++j) {
-                        const int jj = c * 32 + j;
-                        const int m = m_base + jj;
-                        if (jj < BN && m < M) {
-                            const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
-                            y_col[(size_t)m * N] = __fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]);
-                        }
+                for (int j = 0; j < 32; ++j) {
+                    const int jj = c * 32 + j;
+                    const int m = m_base + jj;
+                    if (jj < BN && m < M) {
+                        const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
+                        y_col[(size_t)m * N] = __fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]);
+                    }
+                }
+            };
+            auto release = [&]() {
+                tc::tc_fence_before();
+                tc::mbar_arrive(&S.tmem_empty[acc]);
+            };
+            uint32_t va[32], vb[32];
+            tc::tmem_ld_32x32b_x32(d_addr, va);
+            tc::tmem_ld_wait();
+            if (C == 1) release();
+            for (int c = 0; c < C; c += 2) {
+                if (c + 1 < C) tc::tmem_ld_32x32b_x32(d_addr + 32u * (c + 1), vb);
+                store_slice(c, va);
+                if (c + 1 < C) {
+                    tc::tmem_ld_wait();
+                    if (c + 2 == C) release();
+                    if (c + 2 < C) tc::tmem_ld_32x32b_x32(d_addr + 32u * (c + 2), va);
+                    store_slice(c + 1, vb);
+                    if (c + 2 < C) {
+                        tc::tmem_ld_wait();
+                        if (c + 3 == C) release();
                     }
                 }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(&S.tmem_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
