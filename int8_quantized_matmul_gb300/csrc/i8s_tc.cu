@@ -25,9 +25,10 @@
 // CTAs is completed through exact int32 atomics and a per-tile ticket; the CTA
 // that brings the ticket to the chunk count applies the epilogue.
 //
-// Roles (320 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
-// warps 4-7 converters, warp 8 TMA producer, warp 9 TMEM allocation and MMA
-// issue. Every wait is bounded (~1 s) and records a timeout in the status word.
+// Roles (448 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
+// warps 4-11 converters (two per TMEM lane quarter), warp 12 TMA producer,
+// warp 13 TMEM allocation and MMA issue. Every wait is bounded (~1 s) and
+// records a timeout in the status word.
 
 #include <atomic>
 
@@ -39,11 +40,12 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreads8 = 320;
+constexpr int kThreads8 = 448;
 constexpr int kEpiWarps8 = 4;
-constexpr int kCvtWarp0 = 4;
-constexpr int kTmaWarp8 = 8;
-constexpr int kMmaWarp8 = 9;
+constexpr int kCvtWarp0 = 4;                 // warps 4-11: two converter warps per TMEM lane quarter
+constexpr int kCvtWarps8 = 8;
+constexpr int kTmaWarp8 = 12;
+constexpr int kMmaWarp8 = 13;
 constexpr int kKB8 = 64;                     // K positions per stage
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
 constexpr int kAStages = 4;                  // TMEM A ring (32 columns per stage)
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
 
     if (tid == 0) {
         for (int s = 0; s < kAStages; ++s) {
-            tc::mbar_init(&S.full_a[s], 4 * 32);
+            tc::mbar_init(&S.full_a[s], kCvtWarps8 * 32);
             tc::mbar_init(&S.empty_a[s], 1);
         }
         for (int s = 0; s < kBStages8; ++s) {
@@ -179,25 +181,28 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 for (int s = 0; s < kBStages8; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
         }
-    } else if (warp >= kCvtWarp0 && warp < kCvtWarp0 + 4) {
+    } else if (warp >= kCvtWarp0 && warp < kCvtWarp0 + kCvtWarps8) {
         // ---------------------------------------------------------- converters
-        // thread = weight row = TMEM lane; three stages of row bytes in flight.
-        const int q = warp - kCvtWarp0;
+        // thread = weight row = TMEM lane, two threads per row: half hf turns
+        // the row's bytes 32hf..32hf+31 of each 64-position stage into TMEM
+        // columns 16hf..16hf+15; three stages of row bytes in flight.
+        const int q = (warp - kCvtWarp0) & 3;   // TMEM lane quarter (warp % 4)
+        const int hf = (warp - kCvtWarp0) >> 2;
         const int r = q * 32 + lane;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(16 * hf);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
             const int n = g.wt * kI8sTile + r;
             const bool valid = n < a.N;
-            const int8_t* row = a.w + (size_t)(valid ? n : 0) * a.K;
+            const int8_t* row = a.w + (size_t)(valid ? n : 0) * a.K + 32 * hf;
             const int kb_lo = g.c_lo * kStagesPerChunk;
             const int kb_hi = min(KB, g.c_hi * kStagesPerChunk);
-            uint4 buf[3][4];
-            auto load = [&](uint4 (&b)[4], int kb) {
+            uint4 buf[3][2];
+            auto load = [&](uint4 (&b)[2], int kb) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 2; ++i)
                     b[i] = valid ? ldg_stream(row + (size_t)kb * kKB8 + 16 * i) : make_uint4(0, 0, 0, 0);
             };
 #pragma unroll
@@ -208,9 +213,9 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 for (int j = 0; j < 3; ++j) {
                     const int kb = kb0 + j;
                     if (kb >= kb_hi) break;
-                    uint32_t v[32];
+                    uint32_t v[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 2; ++i) {
                         const uint32_t w4[4] = {buf[j][i].x, buf[j][i].y, buf[j][i].z, buf[j][i].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) i8x4_to_f16x4(w4[e], v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                     if (kb + 3 < kb_hi) load(buf[j], kb + 3);
                     if (!tc::mbar_wait_idle(&S.empty_a[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(2); ok = false; break; }
                     tc::tc_fence_after();
-                    tc::tmem_st_32x32b_x32(lane_base + (uint32_t)(stage * 32), v);
+                    tc::tmem_st_32x32b_x16(lane_base + (uint32_t)(stage * 32), v);
                     tc::tmem_st_wait();
                     tc::tc_fence_before();
                     tc::mbar_arrive(&S.full_a[stage]);
