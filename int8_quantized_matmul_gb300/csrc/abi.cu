@@ -561,17 +561,18 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
 // I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
-// rows_pad x K][split-tile int32 sums, tiles x 128 x 128][tile tickets]
-static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTile - 1) / kI8sTile * kI8sTile; }
+// rows_pad x K][weights f16, N x K][split-tile int32 sums, tiles x 160 x 128]
+// [tile tickets]
+static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTileM - 1) / kI8sTileM * kI8sTileM; }
 static int64_t i8s_tiles(int64_t M, int64_t N) {
-    return ((N + kI8sTile - 1) / kI8sTile) * ((M + kI8sTile - 1) / kI8sTile);
+    return ((N + kI8sTileN - 1) / kI8sTileN) * ((M + kI8sTileM - 1) / kI8sTileM);
 }
 
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 64 || K % 64) return 0;
     const size_t tiles = (size_t)i8s_tiles(M, N);
     return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
-           align_up(tiles * kI8sTile * kI8sTile * 4) + align_up(tiles * 4);
+           align_up((size_t)N * (size_t)K * 2) + align_up(tiles * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4);
 }
 
 int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
@@ -593,17 +594,21 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     const int64_t rows_pad = i8s_rows_pad(M);
     const size_t tiles = (size_t)i8s_tiles(M, N);
     const size_t xf_off = kHeader + align_up((size_t)M * (size_t)N * 4);
-    const size_t part_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
-    const size_t tick_off = part_off + align_up(tiles * kI8sTile * kI8sTile * 4);
+    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
+    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
+    const size_t tick_off = part_off + align_up(tiles * kI8sTileN * kI8sTileM * 4);
     const size_t zero_bytes = tick_off + align_up(tiles * 4) - part_off;
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
-    // pre-pass: activations to f16 rows; clears the status and amax words and
-    // the split-tile sums and tickets
-    r = cuda_status(launch_i8s_x_to_f16(static_cast<const int8_t*>(x_i8s), (int)M, (int)K, (int)rows_pad, xf,
-                                        base + part_off, zero_bytes, status, amax, stream));
+    __half* wf = reinterpret_cast<__half*>(base + wf_off);
+    // pre-pass: weights and activations to f16 rows, once per call; clears the
+    // status and amax words and the split-tile sums and tickets
+    r = cuda_status(launch_i8s_to_f16(static_cast<const int8_t*>(w_i8s), (int)N, wf, static_cast<const int8_t*>(x_i8s),
+                                      (int)M, (int)rows_pad, (int)K, xf, base + part_off, zero_bytes, status, amax,
+                                      stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
-    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTile)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
     a.w = static_cast<const int8_t*>(w_i8s);
     a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
     a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
@@ -617,8 +622,8 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.N = (int)N;
     a.K = (int)K;
     a.relu = relu ? 1 : 0;
-    a.n_wt = (int)((N + kI8sTile - 1) / kI8sTile);
-    a.n_at = (int)(rows_pad / kI8sTile);
+    a.n_wt = (int)((N + kI8sTileN - 1) / kI8sTileN);
+    a.n_at = (int)(rows_pad / kI8sTileM);
     a.chunks = (int)((K + kI8sChunkK - 1) / kI8sChunkK);
     a.total_units = (int)tiles * a.chunks;
     int grid = device_sm_count();

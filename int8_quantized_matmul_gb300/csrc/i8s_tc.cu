@@ -13,22 +13,21 @@
 // Every chunk gets a fresh accumulator, which the epilogue warps drain into an
 // int32 running sum kept in tensor memory.
 //
-// Operands: the weights are the A operand (128 output features per tile).
-// Converter threads (thread = weight row = TMEM lane) load each row's int8
-// bytes, turn them into f16 pairs and tcgen05.st them into a TMEM ring, where
-// the MMA reads them. The activations are the B operand: a pre-pass writes
-// them once as f16 rows (k_i8s_x_to_f16), and TMA streams 128-row x 64-position
-// tiles into a shared-memory ring.
+// Operands: a pre-pass (k_i8s_to_f16) converts the int8 weights and
+// activations to f16 rows once per call; every tile then streams both through
+// TMA into one shared-memory stage ring. The weights are the A operand (128
+// output features per tile), the activations the B operand (160 rows per
+// tile). One stage covers 128 K positions: two swizzle atoms of A and of B,
+// eight 128 x 160 x 16 MMAs.
 //
 // Work: units are (tile, K chunk) pairs, tile-major. Each CTA (one per SM)
 // takes a contiguous range of units. A tile whose chunks are split between
 // CTAs is completed through exact int32 atomics and a per-tile ticket; the CTA
 // that brings the ticket to the chunk count applies the epilogue.
 //
-// Roles (448 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
-// warps 4-11 converters (two per TMEM lane quarter), warp 12 TMA producer,
-// warp 13 TMEM allocation and MMA issue. Every wait is bounded (~1 s) and
-// records a timeout in the status word.
+// Roles (192 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
+// warp 4 TMA producer, warp 5 TMEM allocation and MMA issue. Every wait is
+// bounded (~1 s) and records a timeout in the status word.
 
 #include <atomic>
 
@@ -40,27 +39,28 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreads8 = 448;
+constexpr int kThreads8 = 192;
 constexpr int kEpiWarps8 = 4;
-constexpr int kCvtWarp0 = 4;                 // warps 4-11: two converter warps per TMEM lane quarter
-constexpr int kCvtWarps8 = 8;
-constexpr int kTmaWarp8 = 12;
-constexpr int kMmaWarp8 = 13;
-constexpr int kKB8 = 64;                     // K positions per stage
+constexpr int kTmaWarp8 = 4;
+constexpr int kMmaWarp8 = 5;
+constexpr int kKB8 = 128;                    // K positions per stage (two 64-position swizzle atoms)
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
-constexpr int kAStages = 4;                  // TMEM A ring (32 columns per stage)
-constexpr int kBStages8 = 6;                 // shared-memory B ring
-constexpr int kBStage8Bytes = kI8sTile * kKB8 * 2;   // 128 rows x 128 bytes
+constexpr int kStages8 = 3;
+constexpr int kAAtomBytes = kI8sTileN * 128;          // 128 rows x 64 f16
+constexpr int kBAtomBytes = kI8sTileM * 128;          // 160 rows x 64 f16
+constexpr int kAStage8 = 2 * kAAtomBytes;
+constexpr int kBStage8 = 2 * kBAtomBytes;
 constexpr uint32_t kTmemCols8 = 512;
-constexpr uint32_t kDCol8a = 128, kDCol8b = 256;   // the two f32 accumulators
-constexpr uint32_t kSCol8 = 384;             // int32 running sums
+constexpr uint32_t kDCol8a = 0, kDCol8b = kI8sTileM;   // the two f32 accumulators
+constexpr uint32_t kSCol8 = 2 * kI8sTileM;             // int32 running sums
+constexpr int kSlices8 = kI8sTileM / 32;               // 32-column TMEM slices of a tile
 constexpr long long kWaitLimit8 = 2000000000LL;
+static_assert(kSCol8 + kI8sTileM <= kTmemCols8, "TMEM budget");
+static_assert(kI8sTileM % 32 == 0 && kI8sTileM % 16 == 0 && kI8sTileM <= 256, "MMA N");
 
 struct Smem8 {
-    uint64_t full_a[kAStages];
-    uint64_t empty_a[kAStages];
-    uint64_t full_b[kBStages8];
-    uint64_t empty_b[kBStages8];
+    uint64_t full[kStages8];
+    uint64_t empty[kStages8];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
@@ -71,9 +71,7 @@ struct Smem8 {
     int final_flag;
 };
 
-constexpr size_t kSmem8Used = 1024 + (size_t)kBStages8 * kBStage8Bytes + sizeof(Smem8);
-// At least 120 KB so that one CTA runs per SM: it holds all 512 TMEM columns.
-constexpr size_t kSmem8Bytes = kSmem8Used > 120 * 1024 ? kSmem8Used : 120 * 1024;
+constexpr size_t kSmem8Bytes = 1024 + (size_t)kStages8 * (kAStage8 + kBStage8) + sizeof(Smem8);
 
 // The part of the unit range [u, u_hi) that lies in one tile.
 struct Seg8 {
@@ -111,22 +109,22 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_constant__ I8sTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* sB = smem;
-    Smem8& S = *reinterpret_cast<Smem8*>(sB + (size_t)kBStages8 * kBStage8Bytes);
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + (size_t)kStages8 * kAStage8;
+    Smem8& S = *reinterpret_cast<Smem8*>(sB + (size_t)kStages8 * kBStage8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int u_begin = (int)(((long long)blockIdx.x * a.total_units) / gridDim.x);
     const int u_end = (int)(((long long)(blockIdx.x + 1) * a.total_units) / gridDim.x);
-    const int KB = a.K / kKB8;
+    // stages of 128 positions; with K % 128 == 64 the last stage's second atom
+    // is zero (the converters write zeros, the TMA box lies past K and is
+    // zero-filled), which adds nothing to the dot products
+    const int KB = (a.K + kKB8 - 1) / kKB8;
 
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) {
-            tc::mbar_init(&S.full_a[s], kCvtWarps8 * 32);
-            tc::mbar_init(&S.empty_a[s], 1);
-        }
-        for (int s = 0; s < kBStages8; ++s) {
-            tc::mbar_init(&S.full_b[s], 1);
-            tc::mbar_init(&S.empty_b[s], 1);
+        for (int s = 0; s < kStages8; ++s) {
+            tc::mbar_init(&S.full[s], 1);
+            tc::mbar_init(&S.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&S.tmem_full[b], 1);
@@ -143,7 +141,10 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
         tc::tmem_alloc(&S.tmem_base, kTmemCols8);
         tc::tmem_relinquish();
     }
-    if (warp == kTmaWarp8 && lane == 0) tc::tma_prefetch_desc(&a.xmap);
+    if (warp == kTmaWarp8 && lane == 0) {
+        tc::tma_prefetch_desc(&a.xmap);
+        tc::tma_prefetch_desc(&a.wmap);
+    }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -158,85 +159,40 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
     auto next_seg = [&](const Seg8& g) { ucur += g.units; return seg8_at(a, ucur, u_end); };
 
     if (warp == kTmaWarp8) {
-        // ---------------------------------------------- activation producer
+        // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            bool pending[kBStages8] = {};
-            uint32_t pending_phase[kBStages8] = {};
+            bool pending[kStages8] = {};
+            uint32_t pending_phase[kStages8] = {};
             bool ok = true;
             for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 const int kb_hi = min(KB, g.c_hi * kStagesPerChunk);
                 for (int kb = g.c_lo * kStagesPerChunk; kb < kb_hi; ++kb) {
-                    if (!tc::mbar_wait_idle(&S.empty_b[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(1); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&S.full_b[stage], kBStage8Bytes);
-                    tc::tma_load_2d(sB + (size_t)stage * kBStage8Bytes, &a.xmap, kb * kKB8, g.at * kI8sTile,
-                                    &S.full_b[stage]);
+                    if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(1); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&S.full[stage], kAStage8 + kBStage8);
+                    uint8_t* da = sA + (size_t)stage * kAStage8;
+                    uint8_t* db = sB + (size_t)stage * kBStage8;
+                    const int x0 = kb * kKB8;
+                    tc::tma_load_2d(da, &a.wmap, x0, g.wt * kI8sTileN, &S.full[stage]);
+                    tc::tma_load_2d(da + kAAtomBytes, &a.wmap, x0 + 64, g.wt * kI8sTileN, &S.full[stage]);
+                    tc::tma_load_2d(db, &a.xmap, x0, g.at * kI8sTileM, &S.full[stage]);
+                    tc::tma_load_2d(db + kBAtomBytes, &a.xmap, x0 + 64, g.at * kI8sTileM, &S.full[stage]);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
-                    if (++stage == kBStages8) { stage = 0; phase ^= 1; }
+                    if (++stage == kStages8) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok)
-                for (int s = 0; s < kBStages8; ++s)
-                    if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
-        }
-    } else if (warp >= kCvtWarp0 && warp < kCvtWarp0 + kCvtWarps8) {
-        // ---------------------------------------------------------- converters
-        // thread = weight row = TMEM lane, two threads per row: half hf turns
-        // the row's bytes 32hf..32hf+31 of each 64-position stage into TMEM
-        // columns 16hf..16hf+15; three stages of row bytes in flight.
-        const int q = (warp - kCvtWarp0) & 3;   // TMEM lane quarter (warp % 4)
-        const int hf = (warp - kCvtWarp0) >> 2;
-        const int r = q * 32 + lane;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(16 * hf);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
-            const int n = g.wt * kI8sTile + r;
-            const bool valid = n < a.N;
-            const int8_t* row = a.w + (size_t)(valid ? n : 0) * a.K + 32 * hf;
-            const int kb_lo = g.c_lo * kStagesPerChunk;
-            const int kb_hi = min(KB, g.c_hi * kStagesPerChunk);
-            uint4 buf[3][2];
-            auto load = [&](uint4 (&b)[2], int kb) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    b[i] = valid ? ldg_stream(row + (size_t)kb * kKB8 + 16 * i) : make_uint4(0, 0, 0, 0);
-            };
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-                if (kb_lo + j < kb_hi) load(buf[j], kb_lo + j);
-            for (int kb0 = kb_lo; ok && kb0 < kb_hi; kb0 += 3) {
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int kb = kb0 + j;
-                    if (kb >= kb_hi) break;
-                    uint32_t v[16];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const uint32_t w4[4] = {buf[j][i].x, buf[j][i].y, buf[j][i].z, buf[j][i].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) i8x4_to_f16x4(w4[e], v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
-                    }
-                    if (kb + 3 < kb_hi) load(buf[j], kb + 3);
-                    if (!tc::mbar_wait_idle(&S.empty_a[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(2); ok = false; break; }
-                    tc::tc_fence_after();
-                    tc::tmem_st_32x32b_x16(lane_base + (uint32_t)(stage * 32), v);
-                    tc::tmem_st_wait();
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&S.full_a[stage]);
-                    if (++stage == kAStages) { stage = 0; phase ^= 1; }
-                }
-            }
+                for (int s = 0; s < kStages8; ++s)
+                    if (pending[s]) tc::mbar_wait(&S.full[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
         }
     } else if (warp == kMmaWarp8) {
         // ---------------------------------------------------------------- MMA
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16_f32(kI8sTile, kI8sTile);
-            int stage = 0, bstage = 0;
-            uint32_t phase = 0, bphase = 0;
+            constexpr uint32_t idesc = tc::idesc_f16_f32(kI8sTileN, kI8sTileM);
+            int stage = 0;
+            uint32_t phase = 0;
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
@@ -247,19 +203,19 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                     const uint32_t d_tmem = tmem_base + (buf ? kDCol8b : kDCol8a);
                     const int kb_lo = c * kStagesPerChunk, kb_hi = min(KB, (c + 1) * kStagesPerChunk);
                     for (int kb = kb_lo; kb < kb_hi; ++kb) {
-                        if (!tc::mbar_wait_spin(&S.full_a[stage], phase, abort_flag, kWaitLimit8) ||
-                            !tc::mbar_wait_spin(&S.full_b[bstage], bphase, abort_flag, kWaitLimit8)) { fail(8); ok = false; break; }
+                        if (!tc::mbar_wait_spin(&S.full[stage], phase, abort_flag, kWaitLimit8)) { fail(8); ok = false; break; }
                         tc::tc_fence_after();
-                        const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)bstage * kBStage8Bytes));
-                        const uint32_t a0 = tmem_base + (uint32_t)(stage * 32);
+                        const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kAStage8));
+                        const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBStage8));
                         const uint32_t first = kb != kb_lo;
 #pragma unroll
-                        for (int k = 0; k < kKB8 / 16; ++k)   // 16 positions = 8 A columns = 32 B bytes per MMA
-                            tc::umma_f16_tmem_a(d_tmem, a0 + 8u * k, bd + 2 * k, idesc, k == 0 ? first : 1u);
-                        tc::umma_commit(&S.empty_a[stage]);
-                        tc::umma_commit(&S.empty_b[bstage]);
-                        if (++stage == kAStages) { stage = 0; phase ^= 1; }
-                        if (++bstage == kBStages8) { bstage = 0; bphase ^= 1; }
+                        for (int k = 0; k < kKB8 / 16; ++k) {   // atom k/4, +32 bytes per 16 positions
+                            const uint64_t ak = ad + (uint64_t)((k >> 2) * (kAAtomBytes >> 4)) + 2 * (k & 3);
+                            const uint64_t bk = bd + (uint64_t)((k >> 2) * (kBAtomBytes >> 4)) + 2 * (k & 3);
+                            tc::umma_f16(d_tmem, ak, bk, idesc, k == 0 ? first : 1u);
+                        }
+                        tc::umma_commit(&S.empty[stage]);
+                        if (++stage == kStages8) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
                     tc::umma_commit(&S.tmem_full[buf]);
@@ -286,7 +242,7 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 const uint32_t dcol = tmem_base + lane_off + (buf ? kDCol8b : kDCol8a);
                 const uint32_t scol = tmem_base + lane_off + kSCol8;
 #pragma unroll 1
-                for (int h = 0; h < kI8sTile / 32; ++h) {
+                for (int h = 0; h < kSlices8; ++h) {
                     uint32_t d[32], s[32];
                     tc::tmem_ld_32x32b_x32(dcol + 32u * h, d);
                     if (c != g.c_lo) tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
@@ -304,21 +260,21 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
-            const int n = g.wt * kI8sTile + r;
-            const int m0 = g.at * kI8sTile;
+            const int n = g.wt * kI8sTileN + r;
+            const int m0 = g.at * kI8sTileM;
             const uint32_t scol = tmem_base + lane_off + kSCol8;
-            int32_t* part = a.part + (size_t)g.tile * kI8sTile * kI8sTile;
+            int32_t* part = a.part + (size_t)g.tile * kI8sTileM * kI8sTileN;
             bool write = g.c_lo == 0 && g.c_hi == a.chunks;
             if (!write) {
                 // this CTA holds only some chunks of the tile: add them to the
                 // tile's exact int32 sums; the CTA completing the count finishes
 #pragma unroll 1
-                for (int h = 0; h < kI8sTile / 32; ++h) {
+                for (int h = 0; h < kSlices8; ++h) {
                     uint32_t s[32];
                     tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) atomicAdd(&part[(size_t)(32 * h + j) * kI8sTile + r], (int)s[j]);
+                    for (int j = 0; j < 32; ++j) atomicAdd(&part[(size_t)(32 * h + j) * kI8sTileN + r], (int)s[j]);
                 }
                 __threadfence();
                 tc::mbar_arrive(&S.epi_sync);
@@ -338,14 +294,14 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 const bool full = g.c_lo == 0 && g.c_hi == a.chunks;
                 const float bn = (a.bias && n < a.N) ? a.bias[n] : 0.0f;
 #pragma unroll 1
-                for (int h = 0; h < kI8sTile / 32; ++h) {
+                for (int h = 0; h < kSlices8; ++h) {
                     uint32_t s[32];
                     if (full) {
                         tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
                         tc::tmem_ld_wait();
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) s[j] = (uint32_t)__ldcg(&part[(size_t)(32 * h + j) * kI8sTile + r]);
+                        for (int j = 0; j < 32; ++j) s[j] = (uint32_t)__ldcg(&part[(size_t)(32 * h + j) * kI8sTileN + r]);
                     }
                     if (n < a.N) {
 #pragma unroll
@@ -375,11 +331,14 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
     }
 }
 
-// int8 activations -> f16 rows (zero rows up to rows_pad); also clears the
-// status and amax words and the split-tile sums and tickets.
-__global__ void __launch_bounds__(256) k_i8s_x_to_f16(const int8_t* __restrict__ x, int M, int K, int rows_pad,
-                                                      __half* __restrict__ xf, uint4* zero, unsigned long long zero_16,
-                                                      uint32_t* status, unsigned int* amax_bits) {
+// int8 -> f16 rows of the weights (N x K) and activations (M x K, zero rows up
+// to rows_pad), 16 values per step; also clears the status and amax words and
+// the split-tile sums and tickets.
+__global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w, unsigned long long w16,
+                                                    __half* __restrict__ wf, const int8_t* __restrict__ x,
+                                                    unsigned long long x16, unsigned long long x16_pad,
+                                                    __half* __restrict__ xf, uint4* zero, unsigned long long zero_16,
+                                                    uint32_t* status, unsigned int* amax_bits) {
     const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
     const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
     if (t0 == 0) {
@@ -387,17 +346,21 @@ __global__ void __launch_bounds__(256) k_i8s_x_to_f16(const int8_t* __restrict__
         *amax_bits = 0u;
     }
     for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    const unsigned long long n16 = (unsigned long long)rows_pad * K / 16;   // 16 values per step
-    const unsigned long long valid16 = (unsigned long long)M * K / 16;
-    for (unsigned long long i = t0; i < n16; i += stride) {
+    auto convert = [](const uint4 v, uint4& o0, uint4& o1) {
+        i8x4_to_f16x4(v.x, o0.x, o0.y);
+        i8x4_to_f16x4(v.y, o0.z, o0.w);
+        i8x4_to_f16x4(v.z, o1.x, o1.y);
+        i8x4_to_f16x4(v.w, o1.z, o1.w);
+    };
+    for (unsigned long long i = t0; i < w16; i += stride) {
+        uint4 o0, o1;
+        convert(reinterpret_cast<const uint4*>(w)[i], o0, o1);
+        reinterpret_cast<uint4*>(wf)[2 * i] = o0;
+        reinterpret_cast<uint4*>(wf)[2 * i + 1] = o1;
+    }
+    for (unsigned long long i = t0; i < x16_pad; i += stride) {
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-        if (i < valid16) {
-            const uint4 v = reinterpret_cast<const uint4*>(x)[i];
-            i8x4_to_f16x4(v.x, o0.x, o0.y);
-            i8x4_to_f16x4(v.y, o0.z, o0.w);
-            i8x4_to_f16x4(v.z, o1.x, o1.y);
-            i8x4_to_f16x4(v.w, o1.z, o1.w);
-        }
+        if (i < x16) convert(reinterpret_cast<const uint4*>(x)[i], o0, o1);
         reinterpret_cast<uint4*>(xf)[2 * i] = o0;
         reinterpret_cast<uint4*>(xf)[2 * i + 1] = o1;
     }
@@ -405,14 +368,17 @@ __global__ void __launch_bounds__(256) k_i8s_x_to_f16(const int8_t* __restrict__
 
 }  // namespace
 
-cudaError_t launch_i8s_x_to_f16(const int8_t* x, int M, int K, int rows_pad, __half* xf, void* zero, size_t zero_bytes,
-                                uint32_t* status, unsigned int* amax_bits, cudaStream_t s) {
-    const unsigned long long n = (unsigned long long)rows_pad * K / 16;
+cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
+                              __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
+                              cudaStream_t s) {
+    const unsigned long long w16 = (unsigned long long)N * K / 16;
+    const unsigned long long x16 = (unsigned long long)M * K / 16, x16p = (unsigned long long)rows_pad * K / 16;
+    const unsigned long long n = w16 > x16p ? w16 : x16p;
     const unsigned long long want = (n + 255) / 256;
     const int cap = device_sm_count() * 8;
     const int grid = (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
-    k_i8s_x_to_f16<<<grid, 256, 0, s>>>(x, M, K, rows_pad, xf, static_cast<uint4*>(zero), zero_bytes / 16, status,
-                                        amax_bits);
+    k_i8s_to_f16<<<grid, 256, 0, s>>>(w, w16, wf, x, x16, x16p, xf, static_cast<uint4*>(zero), zero_bytes / 16, status,
+                                      amax_bits);
     return cudaGetLastError();
 }
 

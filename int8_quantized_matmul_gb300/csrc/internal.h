@@ -148,28 +148,31 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 // I8_S fused matmul on tcgen05 (i8s_tc.cu) and the per-tensor requant (i8s.cu).
 // ---------------------------------------------------------------------------
 
-// Tensor-core I8_S GEMM (i8s_tc.cu): 128 x 128 output tiles (output features x
+// Tensor-core I8_S GEMM (i8s_tc.cu): 128 x 160 output tiles (output features x
 // activation rows), K in chunks of kI8sChunkK positions whose f32 partial sums
 // are exact (1024 * 127^2 < 2^24).
-constexpr int kI8sTile = 128;
+constexpr int kI8sTileN = 128;   // output features (weight rows) per tile: the MMA M
+constexpr int kI8sTileM = 160;   // activation rows per tile: the MMA N
 constexpr int kI8sChunkK = 1024;
 
 struct I8sTcArgs {
-    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x 128, 128-byte swizzle
+    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM, 128-byte swizzle
+    CUtensorMap wmap;          // f16 weights, N x K, box 64 x kI8sTileN, 128-byte swizzle
     const int8_t* w;           // N x K
     const float* w_scale_ptr;
     const float* x_scale_ptr;
     const float* bias;         // N or null
     float* y;                  // M x N F32
     unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass)
-    int32_t* part;             // tiles x 128 x 128 int32 sums of split tiles (cleared by the pre-pass)
+    int32_t* part;             // tiles x kI8sTileM x kI8sTileN int32 sums of split tiles (cleared by the pre-pass)
     uint32_t* tickets;         // tiles chunk counters (cleared by the pre-pass)
     uint32_t* status;
     int M, N, K, relu;
     int n_wt, n_at, chunks, total_units;
 };
-cudaError_t launch_i8s_x_to_f16(const int8_t* x, int M, int K, int rows_pad, __half* xf, void* zero, size_t zero_bytes,
-                                uint32_t* status, unsigned int* amax_bits, cudaStream_t s);
+cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
+                              __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
+                              cudaStream_t s);
 cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s);
 
 cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s);
