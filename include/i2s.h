@@ -254,8 +254,8 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
  * ws     device workspace of at least i8s_mul_mat_workspace(M,N,K) bytes,
  *        256-byte aligned. After the call it holds the F32 output before
  *        requantization (M x N, row-major) at offset 256 (i8s_ws_f32_offset).
- * Requirements: K % 64 == 0, M*K, N*K, M*N < 2^31; all pointers 16-byte
- * aligned.
+ * Requirements: K % 64 == 0, K <= 65536 (at most 64 accumulation chunks of
+ * 1024 positions), M*K, N*K, M*N < 2^31; all pointers 16-byte aligned.
  * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
  * ------------------------------------------------------------------------- */
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K);

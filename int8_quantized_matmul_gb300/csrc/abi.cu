@@ -561,24 +561,28 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
 // I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
-// rows_pad x K][weights f16, N x K][split-tile int32 sums, tiles x 160 x 128]
-// [tile tickets]
+// rows_pad x K][weights f16, N x K][split-tile int32 sums, tiles x chunks
+// slots of 160 x 128][tile tickets][tile slot masks]
 static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTileM - 1) / kI8sTileM * kI8sTileM; }
 static int64_t i8s_tiles(int64_t M, int64_t N) {
     return ((N + kI8sTileN - 1) / kI8sTileN) * ((M + kI8sTileM - 1) / kI8sTileM);
 }
 
+static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
+
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
-    if (M < 1 || N < 1 || K < 64 || K % 64) return 0;
+    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return 0;
     const size_t tiles = (size_t)i8s_tiles(M, N);
     return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
-           align_up((size_t)N * (size_t)K * 2) + align_up(tiles * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4);
+           align_up((size_t)N * (size_t)K * 2) +
+           align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4) +
+           align_up(tiles * 8);
 }
 
 int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
                          int relu, void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
     if (!w_i8s || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
-    if (M < 1 || N < 1 || K < 64 || K % 64) return I2S_E_BAD_SHAPE;
+    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
     if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
         return I2S_E_BAD_SHAPE;
     if (!aligned16(w_i8s) || !aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) ||
@@ -596,14 +600,15 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     const size_t xf_off = kHeader + align_up((size_t)M * (size_t)N * 4);
     const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
     const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
-    const size_t tick_off = part_off + align_up(tiles * kI8sTileN * kI8sTileM * 4);
-    const size_t zero_bytes = tick_off + align_up(tiles * 4) - part_off;
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+    const size_t mask_off = tick_off + align_up(tiles * 4);
+    const size_t zero_bytes = mask_off + align_up(tiles * 8) - tick_off;   // tickets and masks (slots need no clearing)
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
     __half* wf = reinterpret_cast<__half*>(base + wf_off);
     // pre-pass: weights and activations to f16 rows, once per call; clears the
     // status and amax words and the split-tile sums and tickets
     r = cuda_status(launch_i8s_to_f16(static_cast<const int8_t*>(w_i8s), (int)N, wf, static_cast<const int8_t*>(x_i8s),
-                                      (int)M, (int)rows_pad, (int)K, xf, base + part_off, zero_bytes, status, amax,
+                                      (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes, status, amax,
                                       stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
@@ -617,6 +622,7 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.amax_bits = amax;
     a.part = reinterpret_cast<int32_t*>(base + part_off);
     a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
+    a.slot_masks = reinterpret_cast<unsigned long long*>(base + mask_off);
     a.status = status;
     a.M = (int)M;
     a.N = (int)N;
@@ -624,7 +630,7 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.relu = relu ? 1 : 0;
     a.n_wt = (int)((N + kI8sTileN - 1) / kI8sTileN);
     a.n_at = (int)(rows_pad / kI8sTileM);
-    a.chunks = (int)((K + kI8sChunkK - 1) / kI8sChunkK);
+    a.chunks = (int)i8s_chunks(K);
     a.total_units = (int)tiles * a.chunks;
     int grid = device_sm_count();
     if (grid > a.total_units) grid = a.total_units;

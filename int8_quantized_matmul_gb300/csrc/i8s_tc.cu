@@ -22,8 +22,10 @@
 //
 // Work: units are (tile, K chunk) pairs, tile-major. Each CTA (one per SM)
 // takes a contiguous range of units. A tile whose chunks are split between
-// CTAs is completed through exact int32 atomics and a per-tile ticket; the CTA
-// that brings the ticket to the chunk count applies the epilogue.
+// CTAs is completed exactly: every segment but the last stores its int32 sums
+// in a slot of its own and marks it in the tile's mask; the CTA that brings
+// the tile's ticket to the chunk count adds the marked slots to its sums and
+// applies the epilogue (plain stores instead of contended atomics).
 //
 // Roles (192 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
 // warp 4 TMA producer, warp 5 TMEM allocation and MMA issue. Every wait is
@@ -66,6 +68,7 @@ struct Smem8 {
     uint64_t mma_done;
     uint64_t epi_sync;
     uint64_t epi_bcast;
+    unsigned long long final_mask;
     uint32_t tmem_base;
     int abort;
     int final_flag;
@@ -263,45 +266,56 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
             const int n = g.wt * kI8sTileN + r;
             const int m0 = g.at * kI8sTileM;
             const uint32_t scol = tmem_base + lane_off + kSCol8;
-            int32_t* part = a.part + (size_t)g.tile * kI8sTileM * kI8sTileN;
+            constexpr size_t kSlot = (size_t)kI8sTileM * kI8sTileN;   // one segment's int32 sums
+            int32_t* slots = a.part + (size_t)g.tile * a.chunks * kSlot;
             bool write = g.c_lo == 0 && g.c_hi == a.chunks;
+            unsigned long long others = 0;   // slots of the tile's other segments (final CTA)
             if (!write) {
-                // this CTA holds only some chunks of the tile: add them to the
-                // tile's exact int32 sums; the CTA completing the count finishes
+                // this CTA holds only some chunks of the tile: store its exact
+                // int32 sums in the slot of its first chunk (plain coalesced
+                // stores), mark the slot, then count its chunks; the CTA that
+                // completes the count adds the marked slots to its own sums
+                int32_t* mine = slots + (size_t)g.c_lo * kSlot;
 #pragma unroll 1
                 for (int h = 0; h < kSlices8; ++h) {
                     uint32_t s[32];
                     tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) atomicAdd(&part[(size_t)(32 * h + j) * kI8sTileN + r], (int)s[j]);
+                    for (int j = 0; j < 32; ++j) __stcg(&mine[(size_t)(32 * h + j) * kI8sTileN + r], (int)s[j]);
                 }
                 __threadfence();
                 tc::mbar_arrive(&S.epi_sync);
                 if (!tc::mbar_wait_idle(&S.epi_sync, sync_phase, abort_flag, kWaitLimit8)) { fail(32); break; }
                 if (r == 0) {
+                    const unsigned long long bit = 1ull << g.c_lo;
+                    const unsigned long long seen = atomicOr(&a.slot_masks[g.tile], bit) | bit;
                     __threadfence();
                     const unsigned prev = atomicAdd(&a.tickets[g.tile], (unsigned)g.units);
-                    S.final_flag = prev + (unsigned)g.units == (unsigned)a.chunks;
+                    const bool last = prev + (unsigned)g.units == (unsigned)a.chunks;
+                    // every other segment set its bit before adding to the ticket
+                    S.final_mask = last ? (atomicOr(&a.slot_masks[g.tile], 0ull) | seen) & ~bit : 0ull;
+                    S.final_flag = last;
                     tc::mbar_arrive(&S.epi_bcast);
                 }
                 if (!tc::mbar_wait_idle(&S.epi_bcast, sync_phase, abort_flag, kWaitLimit8)) { fail(32); break; }
                 sync_phase ^= 1;
                 write = S.final_flag != 0;
+                others = S.final_mask;
                 if (write) __threadfence();
             }
             if (write) {
-                const bool full = g.c_lo == 0 && g.c_hi == a.chunks;
                 const float bn = (a.bias && n < a.N) ? a.bias[n] : 0.0f;
 #pragma unroll 1
                 for (int h = 0; h < kSlices8; ++h) {
                     uint32_t s[32];
-                    if (full) {
-                        tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
-                        tc::tmem_ld_wait();
-                    } else {
+                    tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
+                    tc::tmem_ld_wait();
+                    for (unsigned long long mk = others; mk; mk &= mk - 1) {
+                        const int32_t* src = slots + (size_t)__ffsll((long long)mk) * kSlot - kSlot;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) s[j] = (uint32_t)__ldcg(&part[(size_t)(32 * h + j) * kI8sTileN + r]);
+                        for (int j = 0; j < 32; ++j)
+                            s[j] = (uint32_t)((int)s[j] + __ldcg(&src[(size_t)(32 * h + j) * kI8sTileN + r]));
                     }
                     if (n < a.N) {
 #pragma unroll

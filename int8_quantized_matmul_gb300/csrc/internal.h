@@ -154,6 +154,7 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 constexpr int kI8sTileN = 128;   // output features (weight rows) per tile: the MMA M
 constexpr int kI8sTileM = 160;   // activation rows per tile: the MMA N
 constexpr int kI8sChunkK = 1024;
+constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask of a split tile)
 
 struct I8sTcArgs {
     CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM, 128-byte swizzle
@@ -164,8 +165,9 @@ struct I8sTcArgs {
     const float* bias;         // N or null
     float* y;                  // M x N F32
     unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass)
-    int32_t* part;             // tiles x kI8sTileM x kI8sTileN int32 sums of split tiles (cleared by the pre-pass)
+    int32_t* part;             // split tiles: tiles x chunks slots of kI8sTileM x kI8sTileN int32 sums
     uint32_t* tickets;         // tiles chunk counters (cleared by the pre-pass)
+    unsigned long long* slot_masks;   // tiles masks of the slots written (cleared by the pre-pass)
     uint32_t* status;
     int M, N, K, relu;
     int n_wt, n_at, chunks, total_units;
