@@ -291,15 +291,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             // soon as its last slice is in registers
             const uint32_t d_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
             const int C = (BN + 31) / 32;
-            auto store_slice = [&](int c, const uint32_t (&v)[32]) {
+            auto store_slice = [&](int c, uint32_t (&v)[32]) {
                 if (n >= N) return;
-#pragma unroll   // static indices keep v[] in registers
-                for (int j = 0; j < 32; ++j) {
-                    const int jj = c * 32 + j;
-                    const int m = m_base + jj;
-                    if (jj < BN && m < M) {
+                // 16 outputs at a time, computed in place with no per-element
+                // branch so that the conversions overlap, then stored (static
+                // indices keep v[] in registers; jj < C * 32 <= 256 stays
+                // inside the per-column tables)
+                const int rows = min(BN - c * 32, M - (m_base + c * 32));
+                float* yp = y_col + (size_t)(m_base + c * 32) * N;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int j = 16 * hh; j < 16 * hh + 16; ++j) {
+                        const int jj = c * 32 + j;
                         const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
-                        y_col[(size_t)m * N] = __fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]);
+                        v[j] = __float_as_uint(__fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]));
+                    }
+                    if (rows >= 32) {
+#pragma unroll
+                        for (int j = 16 * hh; j < 16 * hh + 16; ++j) yp[(size_t)j * N] = __uint_as_float(v[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 16 * hh; j < 16 * hh + 16; ++j)
+                            if (j < rows) yp[(size_t)j * N] = __uint_as_float(v[j]);
                     }
                 }
             };

@@ -235,6 +235,9 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
         int buf = 0;
         uint32_t buf_phase = 0, sync_phase = 0;
         const float sc = __fmul_rn(*a.w_scale_ptr, *a.x_scale_ptr);
+        float* const yb = a.y;
+        const int M = a.M, N = a.N;
+        const bool has_bias = a.bias != nullptr, relu = a.relu != 0;
         float local_max = 0.0f;
         bool ok = true;
         for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 if (write) __threadfence();
             }
             if (write) {
-                const float bn = (a.bias && n < a.N) ? a.bias[n] : 0.0f;
+                const float bn = (has_bias && n < N) ? a.bias[n] : 0.0f;
 #pragma unroll 1
                 for (int h = 0; h < kSlices8; ++h) {
                     uint32_t s[32];
@@ -317,17 +320,36 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                         for (int j = 0; j < 32; ++j)
                             s[j] = (uint32_t)((int)s[j] + __ldcg(&src[(size_t)(32 * h + j) * kI8sTileN + r]));
                     }
-                    if (n < a.N) {
+                    // all 32 values first (no per-element branch, so the
+                    // conversions and products overlap), then the stores
+                    float v[32];
+                    if (has_bias) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int m = m0 + 32 * h + j;
-                            if (m < a.M) {
-                                float v = __fmul_rn(__int2float_rn((int)s[j]), sc);
-                                if (a.bias) v = __fadd_rn(v, bn);
-                                if (a.relu) v = v > 0.0f ? v : 0.0f;
-                                a.y[(size_t)m * a.N + n] = v;
-                                local_max = fmaxf(local_max, fabsf(v));
+                        for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(__fmul_rn(__int2float_rn((int)s[j]), sc), bn);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__int2float_rn((int)s[j]), sc);
+                    }
+                    if (relu) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
+                    }
+                    if (n < N) {
+                        float* yp = yb + (size_t)(m0 + 32 * h) * N + n;
+                        const int rows = M - (m0 + 32 * h);
+                        if (rows >= 32) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                yp[(size_t)j * N] = v[j];
+                                local_max = fmaxf(local_max, fabsf(v[j]));
                             }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < rows) {
+                                    yp[(size_t)j * N] = v[j];
+                                    local_max = fmaxf(local_max, fabsf(v[j]));
+                                }
                         }
                     }
                 }
