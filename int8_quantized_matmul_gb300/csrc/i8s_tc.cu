@@ -27,9 +27,16 @@
 // the tile's ticket to the chunk count adds the marked slots to its sums and
 // applies the epilogue (plain stores instead of contended atomics).
 //
-// Roles (192 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
-// warp 4 TMA producer, warp 5 TMEM allocation and MMA issue. Every wait is
-// bounded (~1 s) and records a timeout in the status word.
+// MMA issue: one thread needs well over 100 SM cycles to issue a tcgen05.mma,
+// more than the tensor time of a 128 x 160 x 16 MMA, so three warps issue,
+// taking the stages of the stream in turn, all into the same accumulator.
+// Every MMA accumulates (the drain zeroes the accumulator after reading it);
+// the partial sums are exact integers, so the order in which the three
+// streams land does not matter.
+//
+// Roles (256 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
+// warp 4 TMA producer, warps 5-7 MMA issue (warp 5 also allocates TMEM). Every
+// wait is bounded (~1 s) and records a timeout in the status word.
 
 #include <atomic>
 
@@ -41,10 +48,11 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreads8 = 192;
+constexpr int kThreads8 = 256;
 constexpr int kEpiWarps8 = 4;
 constexpr int kTmaWarp8 = 4;
-constexpr int kMmaWarp8 = 5;
+constexpr int kMmaWarp8 = 5;                // warps 5-7
+constexpr int kIssuers8 = 3;
 constexpr int kKB8 = 128;                    // K positions per stage (two 64-position swizzle atoms)
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
 constexpr int kStages8 = 3;
@@ -65,7 +73,7 @@ struct Smem8 {
     uint64_t empty[kStages8];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t mma_done;
+    uint64_t mma_done[kIssuers8];
     uint64_t epi_sync;
     uint64_t epi_bcast;
     unsigned long long final_mask;
@@ -130,10 +138,10 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
             tc::mbar_init(&S.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&S.tmem_full[b], 1);
+            tc::mbar_init(&S.tmem_full[b], kIssuers8);
             tc::mbar_init(&S.tmem_empty[b], kEpiWarps8 * 32);
         }
-        tc::mbar_init(&S.mma_done, 1);
+        for (int i = 0; i < kIssuers8; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.epi_sync, kEpiWarps8 * 32);
         tc::mbar_init(&S.epi_bcast, 1);
         S.abort = 0;
@@ -152,6 +160,19 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem_base = S.tmem_base;
+    if (warp < kEpiWarps8) {
+        // both accumulators start at zero (every MMA accumulates)
+        uint32_t z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+        for (int col = 0; col < 2 * kI8sTileM; col += 32)
+            tc::tmem_st_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)col, z);
+        tc::tmem_st_wait();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
     volatile int* abort_flag = &S.abort;
     auto fail = [&](uint32_t code) {
         *abort_flag = 1;
@@ -190,14 +211,18 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 for (int s = 0; s < kStages8; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
         }
-    } else if (warp == kMmaWarp8) {
-        // ---------------------------------------------------------------- MMA
+    } else if (warp >= kMmaWarp8 && warp < kMmaWarp8 + kIssuers8) {
+        // ---------------------------------------------------------- MMA issue
+        // issuer `me` takes the stages whose position in this CTA's stage
+        // stream is me modulo kIssuers8; the ring index advances over all
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(kI8sTileN, kI8sTileM);
+            const int me = warp - kMmaWarp8;
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
             uint32_t buf_phase = 0;
+            int seq = 0;
             bool ok = true;
             for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 for (int c = g.c_lo; ok && c < g.c_hi; ++c) {
@@ -205,28 +230,30 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                     tc::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (buf ? kDCol8b : kDCol8a);
                     const int kb_lo = c * kStagesPerChunk, kb_hi = min(KB, (c + 1) * kStagesPerChunk);
-                    for (int kb = kb_lo; kb < kb_hi; ++kb) {
-                        if (!tc::mbar_wait_spin(&S.full[stage], phase, abort_flag, kWaitLimit8)) { fail(8); ok = false; break; }
-                        tc::tc_fence_after();
-                        const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kAStage8));
-                        const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBStage8));
-                        const uint32_t first = kb != kb_lo;
+                    for (int kb = kb_lo; kb < kb_hi; ++kb, ++seq) {
+                        if (seq % kIssuers8 == me) {
+                            if (!tc::mbar_wait_spin(&S.full[stage], phase, abort_flag, kWaitLimit8)) { fail(8); ok = false; break; }
+                            tc::tc_fence_after();
+                            const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kAStage8));
+                            const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBStage8));
 #pragma unroll
-                        for (int k = 0; k < kKB8 / 16; ++k) {   // atom k/4, +32 bytes per 16 positions
-                            const uint64_t ak = ad + (uint64_t)((k >> 2) * (kAAtomBytes >> 4)) + 2 * (k & 3);
-                            const uint64_t bk = bd + (uint64_t)((k >> 2) * (kBAtomBytes >> 4)) + 2 * (k & 3);
-                            tc::umma_f16(d_tmem, ak, bk, idesc, k == 0 ? first : 1u);
+                            for (int k = 0; k < kKB8 / 16; ++k) {   // atom k/4, +32 bytes per 16 positions
+                                const uint64_t ak = ad + (uint64_t)((k >> 2) * (kAAtomBytes >> 4)) + 2 * (k & 3);
+                                const uint64_t bk = bd + (uint64_t)((k >> 2) * (kBAtomBytes >> 4)) + 2 * (k & 3);
+                                tc::umma_f16(d_tmem, ak, bk, idesc, 1u);
+                            }
+                            tc::umma_commit(&S.empty[stage]);
                         }
-                        tc::umma_commit(&S.empty[stage]);
                         if (++stage == kStages8) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
+                    // the chunk is complete once every issuer's MMAs are
                     tc::umma_commit(&S.tmem_full[buf]);
                     if (++buf == 2) { buf = 0; buf_phase ^= 1; }
                 }
             }
-            tc::umma_commit(&S.mma_done);
-            tc::mbar_wait(&S.mma_done, 0, abort_flag, kWaitLimit8 / 8);
+            tc::umma_commit(&S.mma_done[me]);
+            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit8 / 8);
         }
     } else if (warp < kEpiWarps8) {
         // ------------------------------------------------- drain and epilogue
@@ -257,8 +284,10 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                     for (int j = 0; j < 32; ++j) {
                         const int x = __float2int_rn(__uint_as_float(d[j]));
                         s[j] = (uint32_t)((c != g.c_lo ? (int)s[j] : 0) + x);
+                        d[j] = 0u;
                     }
                     tc::tmem_st_32x32b_x32(scol + 32u * h, s);
+                    tc::tmem_st_32x32b_x32(dcol + 32u * h, d);   // the next chunk accumulates from zero
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
