@@ -43,10 +43,22 @@ __global__ void __launch_bounds__(256) k_requant(const float* __restrict__ y, in
     const int64_t n4 = n / 4;
     const float4* y4 = reinterpret_cast<const float4*>(y);
     uint32_t* d4 = reinterpret_cast<uint32_t*>(dst);
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
-        const float4 v = y4[i];
-        d4[i] = (uint32_t)(quantize_one(v.x, inv) & 0xff) | ((uint32_t)(quantize_one(v.y, inv) & 0xff) << 8) |
-                ((uint32_t)(quantize_one(v.z, inv) & 0xff) << 16) | ((uint32_t)(quantize_one(v.w, inv) & 0xff) << 24);
+    // four float4 loads in flight per thread
+    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < n4; i0 += 4 * stride) {
+        float4 v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = i0 + e * stride;
+            v[e] = i < n4 ? y4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = i0 + e * stride;
+            if (i < n4)
+                d4[i] = (uint32_t)(quantize_one(v[e].x, inv) & 0xff) | ((uint32_t)(quantize_one(v[e].y, inv) & 0xff) << 8) |
+                        ((uint32_t)(quantize_one(v[e].z, inv) & 0xff) << 16) |
+                        ((uint32_t)(quantize_one(v[e].w, inv) & 0xff) << 24);
+        }
     }
     if (blockIdx.x == 0) {
         const int64_t padded = (n + 31) / 32 * 32;
@@ -74,7 +86,7 @@ cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cu
 }
 
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
-    k_requant<<<grid_for(n / 4), 256, 0, s>>>(y, n, amax_bits, dst);
+    k_requant<<<grid_for(n / 16), 256, 0, s>>>(y, n, amax_bits, dst);   // four float4 per thread and step
     return cudaGetLastError();
 }
 

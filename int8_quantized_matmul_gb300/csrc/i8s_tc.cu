@@ -397,8 +397,38 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
 }
 
 // int8 -> f16 rows of the weights (N x K) and activations (M x K, zero rows up
-// to rows_pad), 16 values per step; also clears the status and amax words and
-// the split-tile sums and tickets.
+// to rows_pad), four 16-value loads in flight per thread; also clears the
+// status and amax words and the split-tile tickets and masks.
+__device__ __forceinline__ void i8x16_to_f16(const uint4 v, uint4& o0, uint4& o1) {
+    i8x4_to_f16x4(v.x, o0.x, o0.y);
+    i8x4_to_f16x4(v.y, o0.z, o0.w);
+    i8x4_to_f16x4(v.z, o1.x, o1.y);
+    i8x4_to_f16x4(v.w, o1.z, o1.w);
+}
+
+// dst[0 .. n_pad) (in units of 16 values) from src[0 .. n): values past n are zeros
+__device__ __forceinline__ void convert_rows(const uint4* __restrict__ src, unsigned long long n,
+                                             unsigned long long n_pad, uint4* __restrict__ dst, unsigned long long t0,
+                                             unsigned long long stride) {
+    for (unsigned long long i0 = t0; i0 < n_pad; i0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const unsigned long long i = i0 + e * stride;
+            v[e] = i < n ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const unsigned long long i = i0 + e * stride;
+            if (i >= n_pad) break;
+            uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+            if (i < n) i8x16_to_f16(v[e], o0, o1);
+            dst[2 * i] = o0;
+            dst[2 * i + 1] = o1;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w, unsigned long long w16,
                                                     __half* __restrict__ wf, const int8_t* __restrict__ x,
                                                     unsigned long long x16, unsigned long long x16_pad,
@@ -411,24 +441,8 @@ __global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w
         *amax_bits = 0u;
     }
     for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    auto convert = [](const uint4 v, uint4& o0, uint4& o1) {
-        i8x4_to_f16x4(v.x, o0.x, o0.y);
-        i8x4_to_f16x4(v.y, o0.z, o0.w);
-        i8x4_to_f16x4(v.z, o1.x, o1.y);
-        i8x4_to_f16x4(v.w, o1.z, o1.w);
-    };
-    for (unsigned long long i = t0; i < w16; i += stride) {
-        uint4 o0, o1;
-        convert(reinterpret_cast<const uint4*>(w)[i], o0, o1);
-        reinterpret_cast<uint4*>(wf)[2 * i] = o0;
-        reinterpret_cast<uint4*>(wf)[2 * i + 1] = o1;
-    }
-    for (unsigned long long i = t0; i < x16_pad; i += stride) {
-        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-        if (i < x16) convert(reinterpret_cast<const uint4*>(x)[i], o0, o1);
-        reinterpret_cast<uint4*>(xf)[2 * i] = o0;
-        reinterpret_cast<uint4*>(xf)[2 * i + 1] = o1;
-    }
+    convert_rows(reinterpret_cast<const uint4*>(w), w16, w16, reinterpret_cast<uint4*>(wf), t0, stride);
+    convert_rows(reinterpret_cast<const uint4*>(x), x16, x16_pad, reinterpret_cast<uint4*>(xf), t0, stride);
 }
 
 }  // namespace
@@ -439,7 +453,7 @@ cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* 
     const unsigned long long w16 = (unsigned long long)N * K / 16;
     const unsigned long long x16 = (unsigned long long)M * K / 16, x16p = (unsigned long long)rows_pad * K / 16;
     const unsigned long long n = w16 > x16p ? w16 : x16p;
-    const unsigned long long want = (n + 255) / 256;
+    const unsigned long long want = (n + 1023) / 1024;
     const int cap = device_sm_count() * 8;
     const int grid = (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
     k_i8s_to_f16<<<grid, 256, 0, s>>>(w, w16, wf, x, x16, x16p, xf, static_cast<uint4*>(zero), zero_bytes / 16, status,
