@@ -22,11 +22,15 @@
 //              positions) and expanding them to 32 f16 in the 128B-swizzled
 //              K-major layout, then fencing the writes into the async proxy;
 //   warp 12    TMA producer of the activation tile (f16, 128B swizzle);
-//   warp 13    TMEM allocation and the MMA issuer (one lane).
+//   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM).
 // MMA: M = 128 weight rows (the "swapped" A operand), N = up to 256
 // activation rows, K = 16 per instruction, 4 instructions per K block. Two
 // TMEM accumulators of 256 columns let the epilogue of one tile overlap the
-// MMAs of the next.
+// MMAs of the next. One thread needs well over 100 SM cycles to issue a
+// tcgen05.mma, so two warps issue, taking the K blocks of the stream in turn,
+// both into the tile's accumulator: every MMA accumulates, the epilogue zeroes
+// an accumulator after reading it, and since every partial sum is exact the
+// order in which the two streams land does not matter.
 //
 // K order: the converters emit a K block's 64 positions in the order in which
 // the packed bytes yield them (per 32-bit word: for each bit-pair slice, bytes
@@ -52,8 +56,9 @@ namespace {
 constexpr int kEpiWarps = 4;
 constexpr int kCvtWarps = 8;               // two threads per weight row, 8 packed bytes each
 constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kThreadsTc = 448;
+constexpr int kMmaWarp = 13;                // warps 13-14
+constexpr int kIssuersTc = 2;
+constexpr int kThreadsTc = 480;
 constexpr int kStagesTc = 4;
 constexpr int kCvtPrefetch = 8;             // K blocks of packed codes each converter keeps in flight
 constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
@@ -71,7 +76,7 @@ struct SmemTc {
     uint64_t empty[kStagesTc];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t mma_done;
+    uint64_t mma_done[kIssuersTc];
     uint64_t stage_bar;     // the epilogue threads have staged a tile's column factors
     uint32_t tmem_base;
     int abort;
@@ -117,10 +122,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             tc::mbar_init(&S.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&S.tmem_full[b], 1);
+            tc::mbar_init(&S.tmem_full[b], kIssuersTc);
             tc::mbar_init(&S.tmem_empty[b], kEpiWarps * 32);
         }
-        tc::mbar_init(&S.mma_done, 1);
+        for (int i = 0; i < kIssuersTc; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.stage_bar, kEpiWarps * 32);
         S.abort = 0;
         tc::fence_mbar_init();
@@ -136,6 +141,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
     tc::tc_fence_after();
     const uint32_t tmem_base = S.tmem_base;
     volatile int* abort_flag = &S.abort;
+    if (warp < kEpiWarps) {
+        // both accumulators start at zero (every MMA accumulates)
+        for (uint32_t col = 0; col < (uint32_t)kTmemCols; col += 32)
+            tc::tmem_st_zero_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + col);
+        tc::tmem_st_wait();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
 
     auto fail = [&](uint32_t code) {
         *abort_flag = 1;
@@ -218,14 +232,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                 }
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA
+    } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc) {
+        // ---------------------------------------------------------- MMA issue
+        // issuer `me` takes the K blocks whose position in this CTA's stream
+        // is me modulo kIssuersTc; the ring index advances over all of them
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16_f32(kTileW, BN);
+            const int me = warp - kMmaWarp;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int seq = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
                 const TcProb& P = a.p[find_problem(a, tile)];
@@ -233,25 +251,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                 if (!tc::mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimit)) { fail(4); break; }
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit) ||
-                        !tc::mbar_wait(&S.full_b[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kATileBytes));
-                    const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBTileBytesMax));
+                for (int kb = 0; kb < KB; ++kb, ++seq) {
+                    if (seq % kIssuersTc == me) {
+                        if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit) ||
+                            !tc::mbar_wait(&S.full_b[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kATileBytes));
+                        const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBTileBytesMax));
 #pragma unroll
-                    for (int k = 0; k < kBlockK / 16; ++k)   // +32 bytes per 16-element K step
-                        tc::umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-                    tc::umma_commit(&S.empty[stage]);
+                        for (int k = 0; k < kBlockK / 16; ++k)   // +32 bytes per 16-element K step
+                            tc::umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
+                        tc::umma_commit(&S.empty[stage]);
+                    }
                     if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
+                // the tile is complete once every issuer's MMAs are
                 tc::umma_commit(&S.tmem_full[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
             // every MMA this thread issued has completed before TMEM is freed
-            tc::umma_commit(&S.mma_done);
-            tc::mbar_wait(&S.mma_done, 0, abort_flag, kWaitLimit / 8);
+            tc::umma_commit(&S.mma_done[me]);
+            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit / 8);
         }
     } else if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
@@ -318,6 +339,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                 }
             };
             auto release = [&]() {
+                // every slice is in registers: zero the accumulator for the
+                // tile after next, then hand it back
+                for (int c2 = 0; c2 < C; ++c2) tc::tmem_st_zero_32x32b_x32(d_addr + 32u * c2);
+                tc::tmem_st_wait();
                 tc::tc_fence_before();
                 tc::mbar_arrive(&S.tmem_empty[acc]);
             };
