@@ -57,12 +57,14 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreadsGv = 352;
+constexpr int kThreadsGv = 384;
 constexpr int kCvtWarpsGv = 4;
 constexpr int kEpiWarp0 = 4;
 constexpr int kWProdWarp = 8;
 constexpr int kMmaWarpGv = 9;
 constexpr int kBProdWarp = 10;
+constexpr int kMmaWarpGv2 = 11;        // the second MMA issuer
+constexpr int kIssuersGv = 2;
 constexpr int kKB = 512;               // K positions per pipeline stage (128 packed bytes per row)
 constexpr int kStageBytes = kKB / 4;
 constexpr int kWStages = 3;            // weight ring depth (16 KB stages, 128-byte swizzle)
@@ -88,7 +90,7 @@ struct SmemGv {
     uint64_t empty_b[kBStagesMax];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t mma_done;
+    uint64_t mma_done[kIssuersGv];
     uint64_t epi_sync;                  // the 4 epilogue warps finished their partial-dot atomics
     uint64_t epi_bcast;                 // the split-K finalize decision is published
     uint32_t tmem_base;
@@ -260,17 +262,17 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         }
         for (int s = 0; s < kStagesGv; ++s) {
             tc::mbar_init(&S.full_a[s], kCvtWarpsGv * 32);
-            tc::mbar_init(&S.empty[s], 1);
+            tc::mbar_init(&S.empty[s], kIssuersGv);
         }
         for (int s = 0; s < kBStagesMax; ++s) {
             tc::mbar_init(&S.full_b[s], 1);
-            tc::mbar_init(&S.empty_b[s], 1);
+            tc::mbar_init(&S.empty_b[s], kIssuersGv);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&S.tmem_full[b], 1);
+            tc::mbar_init(&S.tmem_full[b], kIssuersGv);
             tc::mbar_init(&S.tmem_empty[b], 4 * 32);
         }
-        tc::mbar_init(&S.mma_done, 1);
+        for (int i = 0; i < kIssuersGv; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.epi_sync, 4 * 32);
         tc::mbar_init(&S.epi_bcast, 1);
         S.abort = 0;
@@ -290,6 +292,20 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         *abort_flag = 1;
         atomicOr(a.status, code);
     };
+    if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+        // both accumulators start at zero (every MMA accumulates)
+        const uint32_t lane_off = (uint32_t)((warp - kEpiWarp0) * 32) << 16;
+        tc::tmem_st_zero_32x32b_x32(tmem_base + lane_off + kDCol0);
+        tc::tmem_st_zero_32x32b_x32(tmem_base + lane_off + kDCol1);
+        if (kN > 32) {
+            tc::tmem_st_zero_32x32b_x16(tmem_base + lane_off + kDCol0 + 32);
+            tc::tmem_st_zero_32x32b_x16(tmem_base + lane_off + kDCol1 + 32);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
 
     int ucur = u_begin;   // each role advances its own copy of the unit cursor
     auto next_seg = [&](const Seg& g) { ucur += g.units; return seg_next(sp, g, ucur, u_end); };
@@ -358,9 +374,10 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                     c[i] = make_uint4(0, 0, 0, 0);
                     if (16 * i < bytes) c[i] = *reinterpret_cast<const uint4*>(wst + tc::sw128_offset(r, i));
                 }
+                // the loads complete while this thread waits for its TMEM stage
+                if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 tc::mbar_arrive(&S.empty_w[ws]);   // this row's bytes of the ring stage are read
                 if (++ws == kWStages) { ws = 0; wphase ^= 1; }
-                if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(32); ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t col0 = lane_base + (uint32_t)(stage * 64);
 #pragma unroll
@@ -422,12 +439,19 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 for (int s = 0; s < kBStages; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimitGv / 8);
         }
-    } else if (warp == kMmaWarpGv) {
-        // ---------------------------------------------------------------- MMA
+    } else if (warp == kMmaWarpGv || warp == kMmaWarpGv2) {
+        // ---------------------------------------------------------- MMA issue
+        // One thread needs well over 100 SM cycles to issue a tcgen05.mma, so
+        // two warps issue every stage, each the MMAs of one 256-position half,
+        // both into the segment's accumulator. Every MMA accumulates; the
+        // epilogue zeroes an accumulator after reading it, and the sums are
+        // exact integers, so the order in which the two streams land does not
+        // matter. A stage is free again once both issuers have committed.
         // One wait per stage: a complete full_a implies the activation operand
         // has landed too (the converters waited for it before arriving). The
         // stage's MMAs (two per 128-position group) are unrolled.
         if (lane == 0) {
+            const int me = warp == kMmaWarpGv ? 0 : 1;
             constexpr uint32_t idesc = tc::idesc_mxf4_f32(kTileRows, kN);
             const uint32_t sfa = tmem_base + kSfCol, sfb = tmem_base + kSfCol + 4;
             int stage = 0, bstage = 0;
@@ -436,31 +460,27 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             uint32_t acc_phase = 0;
             bool ok = true;
             for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
-                if (!tc::mbar_wait_spin(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimitGv)) { fail(128); break; }
+                if (!tc::mbar_wait_idle(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimitGv)) { fail(128); break; }
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (acc ? kDCol1 : kDCol0);
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
                     const int n_mma = 2 * min(4, (g.K - kb * kKB) / 128);   // 64 positions per MMA
-                    if (!tc::mbar_wait_spin(&S.full_a[stage], phase, abort_flag, kWaitLimitGv)) { fail(256); ok = false; break; }
+                    if (!tc::mbar_wait_idle(&S.full_a[stage], phase, abort_flag, kWaitLimitGv)) { fail(256); ok = false; break; }
                     tc::tc_fence_after();
+                    // issuer `me` takes the stage's 256-position half `me`: MMAs 4me..4me+3
                     const uint32_t b0 = tc::smem_u32(sB + (size_t)bstage * kBStageBytes);
-                    const uint64_t bd0 = tc::sdesc_sw128_kmajor(b0);
-                    const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + kBSub);
-                    const uint32_t a0 = tmem_base + (uint32_t)(stage * 64);
-                    const uint32_t first = kb != g.st_lo;
+                    const uint64_t bd = tc::sdesc_sw128_kmajor(b0 + (me ? kBSub : 0u));
+                    const uint32_t a0 = tmem_base + (uint32_t)(stage * 64) + 32u * (uint32_t)me;
                     if (n_mma == 8) {   // full stage: straight-line issue
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa,
-                                                 sfb, k == 0 ? first : 1u);
+                        for (int k = 0; k < 4; ++k)
+                            tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, bd + 2 * k, idesc, sfa, sfb, 1u);
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            if (k < n_mma)
-                                tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, (k < 4 ? bd0 : bd1) + 2 * (k & 3), idesc, sfa,
-                                                     sfb, k == 0 ? first : 1u);
+                        for (int k = 0; k < 4; ++k)
+                            if (4 * me + k < n_mma) tc::umma_mxf4_tmem_a(d_tmem, a0 + 8u * k, bd + 2 * k, idesc, sfa, sfb, 1u);
                     }
-                    tc::umma_commit(&S.empty[stage]);
+                    tc::umma_commit(&S.empty[stage]);      // one arrival from each issuer
                     tc::umma_commit(&S.empty_b[bstage]);
                     if (++stage == kStagesGv) { stage = 0; phase ^= 1; }
                     if (++bstage == kBStages) bstage = 0;
@@ -469,8 +489,8 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 tc::umma_commit(&S.tmem_full[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
-            tc::umma_commit(&S.mma_done);
-            tc::mbar_wait(&S.mma_done, 0, abort_flag, kWaitLimitGv / 8);
+            tc::umma_commit(&S.mma_done[me]);
+            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimitGv / 8);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue
@@ -491,6 +511,10 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             tc::tmem_ld_32x32b_x32(dcol, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
             if (kN > 32) tc::tmem_ld_32x32b_x16(dcol + 32, *reinterpret_cast<uint32_t (*)[16]>(&v[32]));
             tc::tmem_ld_wait();
+            // zero the accumulator for the segment after next, then hand it back
+            tc::tmem_st_zero_32x32b_x32(dcol);
+            if (kN > 32) tc::tmem_st_zero_32x32b_x16(dcol + 32);
+            tc::tmem_st_wait();
             tc::tc_fence_before();
             tc::mbar_arrive(&S.tmem_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
