@@ -277,7 +277,10 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 255) s_code[tid] = digit_code(tid - 127);
     if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
-    for (int i = blockIdx.x * kQThreads + tid; i < a.n_wmaps; i += gridDim.x * kQThreads) write_weight_map(a, i);
+    // map i is written by thread i / gridDim.x of CTA i % gridDim.x: one or two
+    // maps per CTA instead of all of them in the first CTA, whose row work
+    // would otherwise wait behind them
+    for (int i = blockIdx.x + (int)gridDim.x * tid; i < a.n_wmaps; i += (int)gridDim.x * kQThreads) write_weight_map(a, i);
     for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
          i += (unsigned long long)gridDim.x * kQThreads)
         a.zero[i] = make_uint4(0u, 0u, 0u, 0u);
