@@ -561,11 +561,13 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
 // I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
-// rows_pad x K][weights f16, N x K][split-tile int32 sums, tiles x chunks
-// slots of 160 x 128][tile tickets][tile slot masks]
+// rows_pad x K][weights f16, N x K][split-tile int32 sums, half-tiles x chunks
+// slots of 160 x 128][half-tile tickets][half-tile slot masks]. A tile is 256
+// output features x 160 activation rows, computed by a CTA pair; each CTA owns
+// one 128-feature half.
 static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTileM - 1) / kI8sTileM * kI8sTileM; }
-static int64_t i8s_tiles(int64_t M, int64_t N) {
-    return ((N + kI8sTileN - 1) / kI8sTileN) * ((M + kI8sTileM - 1) / kI8sTileM);
+static int64_t i8s_tiles(int64_t M, int64_t N) {   // half-tiles: 128 features x 160 rows
+    return 2 * ((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN)) * ((M + kI8sTileM - 1) / kI8sTileM);
 }
 
 static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
@@ -612,7 +614,7 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
                                       stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
-    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
     a.w = static_cast<const int8_t*>(w_i8s);
     a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
@@ -628,12 +630,13 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.N = (int)N;
     a.K = (int)K;
     a.relu = relu ? 1 : 0;
-    a.n_wt = (int)((N + kI8sTileN - 1) / kI8sTileN);
+    a.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));   // 256-feature tiles
     a.n_at = (int)(rows_pad / kI8sTileM);
     a.chunks = (int)i8s_chunks(K);
-    a.total_units = (int)tiles * a.chunks;
-    int grid = device_sm_count();
-    if (grid > a.total_units) grid = a.total_units;
+    a.total_units = (int)(tiles / 2) * a.chunks;   // units of whole (256-feature) tiles
+    int pairs = device_sm_count() / 2;
+    if (pairs > a.total_units) pairs = a.total_units;
+    const int grid = 2 * pairs;   // clusters of two CTAs
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));

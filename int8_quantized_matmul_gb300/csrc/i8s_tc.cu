@@ -14,29 +14,41 @@
 // int32 running sum kept in tensor memory.
 //
 // Operands: a pre-pass (k_i8s_to_f16) converts the int8 weights and
-// activations to f16 rows once per call; every tile then streams both through
-// TMA into one shared-memory stage ring. The weights are the A operand (128
-// output features per tile), the activations the B operand (160 rows per
-// tile). One stage covers 128 K positions: two swizzle atoms of A and of B,
-// eight 128 x 160 x 16 MMAs.
+// activations to f16 rows once per call. The kernel runs on CTA pairs (clusters
+// of two CTAs on two SMs) driving cta_group::2 MMAs: a tile is 256 output
+// features (the A operand; 128 rows in each CTA's shared memory and TMEM) x 160
+// activation rows (the B operand; 80 rows in each CTA's shared memory). Each
+// CTA streams its halves through TMA into its own 4-stage ring, every load
+// counted on the leader's (rank 0) barrier. One stage covers 128 K positions:
+// two swizzle atoms of A and of B, eight 256 x 160 x 16 MMAs issued by the
+// leader. Splitting B halves each CTA's shared-memory stage (52 KB instead of
+// 72 KB for a 128 x 160 tile), so one more stage is in flight, and one MMA
+// instruction does the work of two SMs.
 //
-// Work: units are (tile, K chunk) pairs, tile-major. Each CTA (one per SM)
-// takes a contiguous range of units. A tile whose chunks are split between
+// Work: units are (tile, K chunk) pairs, tile-major. Each CTA pair takes a
+// contiguous range of units; each CTA owns its 128 rows of every tile. A tile whose chunks are split between
 // CTAs is completed exactly: every segment but the last stores its int32 sums
 // in a slot of its own and marks it in the tile's mask; the CTA that brings
 // the tile's ticket to the chunk count adds the marked slots to its sums and
 // applies the epilogue (plain stores instead of contended atomics).
 //
 // MMA issue: one thread needs well over 100 SM cycles to issue a tcgen05.mma,
-// more than the tensor time of a 128 x 160 x 16 MMA, so three warps issue,
-// taking the stages of the stream in turn, all into the same accumulator.
+// more than the tensor time of a 128 x 160 x 16 MMA per SM, so three warps of
+// the leader issue, taking the stages of the stream in turn, all into the same
+// accumulator.
 // Every MMA accumulates (the drain zeroes the accumulator after reading it);
 // the partial sums are exact integers, so the order in which the three
 // streams land does not matter.
 //
-// Roles (256 threads): warps 0-3 drain and epilogue (TMEM lanes 32w..32w+31),
-// warp 4 TMA producer, warps 5-7 MMA issue (warp 5 also allocates TMEM). Every
-// wait is bounded (~1 s) and records a timeout in the status word.
+// Roles (384 threads per CTA): warps 0-7 drain and epilogue (warp w: TMEM
+// lanes 32(w%4)..+31 of the CTA's own TMEM, accumulator columns 80(w/4)..+79),
+// warp 8 TMA producer, warps 9-11 MMA issue (the leader's; warp 9 of each CTA
+// also allocates TMEM, collectively for the pair). Every wait is bounded (~1 s) and records a timeout in the status word.
+//
+// Barriers: full[s] (leader) counts the leader's expect_tx and both CTAs'
+// bytes of stage s; empty[s] (both CTAs) and tmem_full[b] (both) get the
+// leader's multicast commits; tmem_empty[b] (leader) counts both CTAs' 256
+// epilogue threads, the peer's by remote arrive.
 
 #include <atomic>
 
@@ -48,24 +60,28 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreads8 = 256;
-constexpr int kEpiWarps8 = 4;
-constexpr int kTmaWarp8 = 4;
-constexpr int kMmaWarp8 = 5;                // warps 5-7
+constexpr int kThreads8 = 384;
+constexpr int kEpiWarps8 = 8;                // two per TMEM lane quarter, one per half of the columns
+constexpr int kTmaWarp8 = 8;
+constexpr int kMmaWarp8 = 9;                // warps 9-11
 constexpr int kIssuers8 = 3;
 constexpr int kKB8 = 128;                    // K positions per stage (two 64-position swizzle atoms)
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
-constexpr int kStages8 = 3;
+constexpr int kStages8 = 4;
 constexpr int kAAtomBytes = kI8sTileN * 128;          // 128 rows x 64 f16
-constexpr int kBAtomBytes = kI8sTileM * 128;          // 160 rows x 64 f16
+constexpr int kBRows8 = kI8sTileM / 2;               // activation rows of a tile in each CTA
+constexpr int kBAtomBytes = kBRows8 * 128;            // 80 rows x 64 f16 (a multiple of 1024)
 constexpr int kAStage8 = 2 * kAAtomBytes;
 constexpr int kBStage8 = 2 * kBAtomBytes;
 constexpr uint32_t kTmemCols8 = 512;
 constexpr uint32_t kDCol8a = 0, kDCol8b = kI8sTileM;   // the two f32 accumulators
 constexpr uint32_t kSCol8 = 2 * kI8sTileM;             // int32 running sums
-constexpr int kSlices8 = kI8sTileM / 32;               // 32-column TMEM slices of a tile
+constexpr int kEpiCols8 = kI8sTileM / 2;               // accumulator columns each epilogue warp owns
+constexpr int kESlices8 = kEpiCols8 / 16;              // 16-column TMEM slices of them
+static_assert(kEpiCols8 % 16 == 0, "epilogue slices");
 constexpr long long kWaitLimit8 = 2000000000LL;
 static_assert(kSCol8 + kI8sTileM <= kTmemCols8, "TMEM budget");
+static_assert(kBAtomBytes % 1024 == 0 && kI8sTileM % 32 == 0, "swizzle atoms of the B half");
 static_assert(kI8sTileM % 32 == 0 && kI8sTileM % 16 == 0 && kI8sTileM <= 256, "MMA N");
 
 struct Smem8 {
@@ -117,7 +133,7 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&h1);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_constant__ I8sTcArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_constant__ I8sTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
@@ -125,8 +141,10 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
     Smem8& S = *reinterpret_cast<Smem8*>(sB + (size_t)kStages8 * kBStage8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int u_begin = (int)(((long long)blockIdx.x * a.total_units) / gridDim.x);
-    const int u_end = (int)(((long long)(blockIdx.x + 1) * a.total_units) / gridDim.x);
+    const uint32_t rank = tc::cluster_rank();   // 0: the leader, which issues the MMAs
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int u_begin = (int)(((long long)pair * a.total_units) / n_pairs);
+    const int u_end = (int)(((long long)(pair + 1) * a.total_units) / n_pairs);
     // stages of 128 positions; with K % 128 == 64 the last stage's second atom
     // is zero (the converters write zeros, the TMA box lies past K and is
     // zero-filled), which adds nothing to the dot products
@@ -139,7 +157,7 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&S.tmem_full[b], kIssuers8);
-            tc::mbar_init(&S.tmem_empty[b], kEpiWarps8 * 32);
+            tc::mbar_init(&S.tmem_empty[b], 2 * kEpiWarps8 * 32);   // both CTAs' epilogue threads
         }
         for (int i = 0; i < kIssuers8; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.epi_sync, kEpiWarps8 * 32);
@@ -148,9 +166,9 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
         S.final_flag = 0;
         tc::fence_mbar_init();
     }
-    if (warp == kMmaWarp8) {
-        tc::tmem_alloc(&S.tmem_base, kTmemCols8);
-        tc::tmem_relinquish();
+    if (warp == kMmaWarp8) {   // one warp of each CTA, collectively for the pair
+        tc::pair_tmem_alloc(&S.tmem_base, kTmemCols8);
+        tc::pair_tmem_relinquish();
     }
     if (warp == kTmaWarp8 && lane == 0) {
         tc::tma_prefetch_desc(&a.xmap);
@@ -161,17 +179,20 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
     tc::tc_fence_after();
     const uint32_t tmem_base = S.tmem_base;
     if (warp < kEpiWarps8) {
-        // both accumulators start at zero (every MMA accumulates)
-        uint32_t z[32];
+        // both accumulators start at zero (every MMA accumulates): each warp
+        // its lane quarter and its half of the columns
+        const uint32_t base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * kEpiCols8);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0u;
-#pragma unroll
-        for (int col = 0; col < 2 * kI8sTileM; col += 32)
-            tc::tmem_st_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)col, z);
+        for (int h = 0; h < kESlices8; ++h) {
+            tc::tmem_st_zero_32x32b_x16(base + kDCol8a + 16u * h);
+            tc::tmem_st_zero_32x32b_x16(base + kDCol8b + 16u * h);
+        }
         tc::tmem_st_wait();
     }
+    // both CTAs' barriers initialised and accumulators zeroed before any
+    // remote arrive, multicast commit or MMA
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     tc::tc_fence_after();
     volatile int* abort_flag = &S.abort;
     auto fail = [&](uint32_t code) {
@@ -192,31 +213,38 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
             bool ok = true;
             for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 const int kb_hi = min(KB, g.c_hi * kStagesPerChunk);
+                const int wrow = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN;   // this CTA's weight rows
+                const int xrow = g.at * kI8sTileM + (int)rank * kBRows8;           // this CTA's activation rows
                 for (int kb = g.c_lo * kStagesPerChunk; kb < kb_hi; ++kb) {
                     if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(1); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&S.full[stage], kAStage8 + kBStage8);
+                    // the leader expects both CTAs' bytes; a peer's bytes may land first
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&S.full[stage], 2 * (kAStage8 + kBStage8));
+                    const uint32_t full_bar = tc::smem_in_rank(&S.full[stage], 0);
                     uint8_t* da = sA + (size_t)stage * kAStage8;
                     uint8_t* db = sB + (size_t)stage * kBStage8;
                     const int x0 = kb * kKB8;
-                    tc::tma_load_2d(da, &a.wmap, x0, g.wt * kI8sTileN, &S.full[stage]);
-                    tc::tma_load_2d(da + kAAtomBytes, &a.wmap, x0 + 64, g.wt * kI8sTileN, &S.full[stage]);
-                    tc::tma_load_2d(db, &a.xmap, x0, g.at * kI8sTileM, &S.full[stage]);
-                    tc::tma_load_2d(db + kBAtomBytes, &a.xmap, x0 + 64, g.at * kI8sTileM, &S.full[stage]);
+                    tc::pair_tma_load_2d(da, &a.wmap, x0, wrow, full_bar);
+                    tc::pair_tma_load_2d(da + kAAtomBytes, &a.wmap, x0 + 64, wrow, full_bar);
+                    tc::pair_tma_load_2d(db, &a.xmap, x0, xrow, full_bar);
+                    tc::pair_tma_load_2d(db + kBAtomBytes, &a.xmap, x0 + 64, xrow, full_bar);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
                     if (++stage == kStages8) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok)
+            // on a failure, let this CTA's copies in flight land before it exits
+            // (the leader's own full barriers count them; the peer's copies land
+            // within the bounded waits of the final cluster barrier's wait)
+            if (!ok && rank == 0)
                 for (int s = 0; s < kStages8; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
         }
-    } else if (warp >= kMmaWarp8 && warp < kMmaWarp8 + kIssuers8) {
+    } else if (warp >= kMmaWarp8 && warp < kMmaWarp8 + kIssuers8 && rank == 0) {
         // ---------------------------------------------------------- MMA issue
         // issuer `me` takes the stages whose position in this CTA's stage
         // stream is me modulo kIssuers8; the ring index advances over all
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16_f32(kI8sTileN, kI8sTileM);
+            constexpr uint32_t idesc = tc::idesc_f16_f32(2 * kI8sTileN, kI8sTileM);   // 256 x 160 over the pair
             const int me = warp - kMmaWarp8;
             int stage = 0;
             uint32_t phase = 0;
@@ -240,25 +268,27 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                             for (int k = 0; k < kKB8 / 16; ++k) {   // atom k/4, +32 bytes per 16 positions
                                 const uint64_t ak = ad + (uint64_t)((k >> 2) * (kAAtomBytes >> 4)) + 2 * (k & 3);
                                 const uint64_t bk = bd + (uint64_t)((k >> 2) * (kBAtomBytes >> 4)) + 2 * (k & 3);
-                                tc::umma_f16(d_tmem, ak, bk, idesc, 1u);
+                                tc::pair_umma_f16(d_tmem, ak, bk, idesc, 1u);
                             }
-                            tc::umma_commit(&S.empty[stage]);
+                            tc::pair_commit(&S.empty[stage], 0x3);   // both CTAs' stage slots are free
                         }
                         if (++stage == kStages8) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
-                    // the chunk is complete once every issuer's MMAs are
-                    tc::umma_commit(&S.tmem_full[buf]);
+                    // the chunk is complete (in both CTAs' TMEM) once every issuer's MMAs are
+                    tc::pair_commit(&S.tmem_full[buf], 0x3);
                     if (++buf == 2) { buf = 0; buf_phase ^= 1; }
                 }
             }
-            tc::umma_commit(&S.mma_done[me]);
+            tc::pair_commit(&S.mma_done[me], 0x1);
             tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit8 / 8);
         }
     } else if (warp < kEpiWarps8) {
         // ------------------------------------------------- drain and epilogue
-        const int r = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int q = warp & 3;                        // TMEM lane quarter
+        const int c0 = (warp >> 2) * kEpiCols8;        // first accumulator column (activation row) of this warp
+        const int r = q * 32 + lane;                   // TMEM lane = weight row of this CTA's half
+        const uint32_t lane_off = ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
         int buf = 0;
         uint32_t buf_phase = 0, sync_phase = 0;
         const float sc = __fmul_rn(*a.w_scale_ptr, *a.x_scale_ptr);
@@ -275,31 +305,31 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 const uint32_t dcol = tmem_base + lane_off + (buf ? kDCol8b : kDCol8a);
                 const uint32_t scol = tmem_base + lane_off + kSCol8;
 #pragma unroll 1
-                for (int h = 0; h < kSlices8; ++h) {
-                    uint32_t d[32], s[32];
-                    tc::tmem_ld_32x32b_x32(dcol + 32u * h, d);
-                    if (c != g.c_lo) tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
+                for (int h = 0; h < kESlices8; ++h) {
+                    uint32_t d[16], s[16];
+                    tc::tmem_ld_32x32b_x16(dcol + 16u * h, d);
+                    if (c != g.c_lo) tc::tmem_ld_32x32b_x16(scol + 16u * h, s);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         const int x = __float2int_rn(__uint_as_float(d[j]));
                         s[j] = (uint32_t)((c != g.c_lo ? (int)s[j] : 0) + x);
-                        d[j] = 0u;
                     }
-                    tc::tmem_st_32x32b_x32(scol + 32u * h, s);
-                    tc::tmem_st_32x32b_x32(dcol + 32u * h, d);   // the next chunk accumulates from zero
+                    tc::tmem_st_32x32b_x16(scol + 16u * h, s);
+                    tc::tmem_st_zero_32x32b_x16(dcol + 16u * h);   // the next chunk accumulates from zero
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
-                tc::mbar_arrive(&S.tmem_empty[buf]);
+                tc::mbar_arrive_cluster(tc::smem_in_rank(&S.tmem_empty[buf], 0));   // the leader's barrier
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
-            const int n = g.wt * kI8sTileN + r;
-            const int m0 = g.at * kI8sTileM;
+            const int n = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN + r;
+            const int ht = 2 * g.tile + (int)rank;   // this CTA's half of the tile: its slots, ticket and mask
+            const int m0 = g.at * kI8sTileM + c0;     // first activation row of this warp's columns
             const uint32_t scol = tmem_base + lane_off + kSCol8;
             constexpr size_t kSlot = (size_t)kI8sTileM * kI8sTileN;   // one segment's int32 sums
-            int32_t* slots = a.part + (size_t)g.tile * a.chunks * kSlot;
+            int32_t* slots = a.part + (size_t)ht * a.chunks * kSlot + (size_t)c0 * kI8sTileN;
             bool write = g.c_lo == 0 && g.c_hi == a.chunks;
             unsigned long long others = 0;   // slots of the tile's other segments (final CTA)
             if (!write) {
@@ -309,24 +339,24 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
                 // completes the count adds the marked slots to its own sums
                 int32_t* mine = slots + (size_t)g.c_lo * kSlot;
 #pragma unroll 1
-                for (int h = 0; h < kSlices8; ++h) {
-                    uint32_t s[32];
-                    tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
+                for (int h = 0; h < kESlices8; ++h) {
+                    uint32_t s[16];
+                    tc::tmem_ld_32x32b_x16(scol + 16u * h, s);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) __stcg(&mine[(size_t)(32 * h + j) * kI8sTileN + r], (int)s[j]);
+                    for (int j = 0; j < 16; ++j) __stcg(&mine[(size_t)(16 * h + j) * kI8sTileN + r], (int)s[j]);
                 }
                 __threadfence();
                 tc::mbar_arrive(&S.epi_sync);
                 if (!tc::mbar_wait_idle(&S.epi_sync, sync_phase, abort_flag, kWaitLimit8)) { fail(32); break; }
-                if (r == 0) {
+                if (warp == 0 && lane == 0) {
                     const unsigned long long bit = 1ull << g.c_lo;
-                    const unsigned long long seen = atomicOr(&a.slot_masks[g.tile], bit) | bit;
+                    const unsigned long long seen = atomicOr(&a.slot_masks[ht], bit) | bit;
                     __threadfence();
-                    const unsigned prev = atomicAdd(&a.tickets[g.tile], (unsigned)g.units);
+                    const unsigned prev = atomicAdd(&a.tickets[ht], (unsigned)g.units);
                     const bool last = prev + (unsigned)g.units == (unsigned)a.chunks;
                     // every other segment set its bit before adding to the ticket
-                    S.final_mask = last ? (atomicOr(&a.slot_masks[g.tile], 0ull) | seen) & ~bit : 0ull;
+                    S.final_mask = last ? (atomicOr(&a.slot_masks[ht], 0ull) | seen) & ~bit : 0ull;
                     S.final_flag = last;
                     tc::mbar_arrive(&S.epi_bcast);
                 }
@@ -339,42 +369,42 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
             if (write) {
                 const float bn = (has_bias && n < N) ? a.bias[n] : 0.0f;
 #pragma unroll 1
-                for (int h = 0; h < kSlices8; ++h) {
-                    uint32_t s[32];
-                    tc::tmem_ld_32x32b_x32(scol + 32u * h, s);
+                for (int h = 0; h < kESlices8; ++h) {
+                    uint32_t s[16];
+                    tc::tmem_ld_32x32b_x16(scol + 16u * h, s);
                     tc::tmem_ld_wait();
                     for (unsigned long long mk = others; mk; mk &= mk - 1) {
                         const int32_t* src = slots + (size_t)__ffsll((long long)mk) * kSlot - kSlot;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            s[j] = (uint32_t)((int)s[j] + __ldcg(&src[(size_t)(32 * h + j) * kI8sTileN + r]));
+                        for (int j = 0; j < 16; ++j)
+                            s[j] = (uint32_t)((int)s[j] + __ldcg(&src[(size_t)(16 * h + j) * kI8sTileN + r]));
                     }
-                    // all 32 values first (no per-element branch, so the
+                    // all 16 values first (no per-element branch, so the
                     // conversions and products overlap), then the stores
-                    float v[32];
+                    float v[16];
                     if (has_bias) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(__fmul_rn(__int2float_rn((int)s[j]), sc), bn);
+                        for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(__fmul_rn(__int2float_rn((int)s[j]), sc), bn);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__int2float_rn((int)s[j]), sc);
+                        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(__int2float_rn((int)s[j]), sc);
                     }
                     if (relu) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
+                        for (int j = 0; j < 16; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
                     }
                     if (n < N) {
-                        float* yp = yb + (size_t)(m0 + 32 * h) * N + n;
-                        const int rows = M - (m0 + 32 * h);
-                        if (rows >= 32) {
+                        float* yp = yb + (size_t)(m0 + 16 * h) * N + n;
+                        const int rows = M - (m0 + 16 * h);
+                        if (rows >= 16) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
+                            for (int j = 0; j < 16; ++j) {
                                 yp[(size_t)j * N] = v[j];
                                 local_max = fmaxf(local_max, fabsf(v[j]));
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
+                            for (int j = 0; j < 16; ++j)
                                 if (j < rows) {
                                     yp[(size_t)j * N] = v[j];
                                     local_max = fmaxf(local_max, fabsf(v[j]));
@@ -388,11 +418,14 @@ __global__ void __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_const
         if (lane == 0) atomicMax(a.amax_bits, __float_as_uint(local_max));
     }
 
+    // every MMA of the pair has completed (the epilogues waited for the last
+    // tmem_full) and neither CTA's shared memory is read any more
+    __syncwarp();
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     if (warp == kMmaWarp8) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, kTmemCols8);
+        tc::pair_tmem_dealloc(tmem_base, kTmemCols8);
     }
 }
 

@@ -157,7 +157,7 @@ constexpr int kI8sChunkK = 1024;
 constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask of a split tile)
 
 struct I8sTcArgs {
-    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM, 128-byte swizzle
+    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM / 2, 128-byte swizzle
     CUtensorMap wmap;          // f16 weights, N x K, box 64 x kI8sTileN, 128-byte swizzle
     const int8_t* w;           // N x K
     const float* w_scale_ptr;
@@ -165,12 +165,12 @@ struct I8sTcArgs {
     const float* bias;         // N or null
     float* y;                  // M x N F32
     unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass)
-    int32_t* part;             // split tiles: tiles x chunks slots of kI8sTileM x kI8sTileN int32 sums
-    uint32_t* tickets;         // tiles chunk counters (cleared by the pre-pass)
-    unsigned long long* slot_masks;   // tiles masks of the slots written (cleared by the pre-pass)
+    int32_t* part;             // split tiles: half-tiles x chunks slots of kI8sTileM x kI8sTileN int32 sums
+    uint32_t* tickets;         // half-tile chunk counters (cleared by the pre-pass)
+    unsigned long long* slot_masks;   // half-tile masks of the slots written (cleared by the pre-pass)
     uint32_t* status;
     int M, N, K, relu;
-    int n_wt, n_at, chunks, total_units;
+    int n_wt, n_at, chunks, total_units;   // n_wt: 256-feature tiles (a CTA pair each)
 };
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
                               __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
