@@ -33,16 +33,16 @@
 // applies the epilogue (plain stores instead of contended atomics).
 //
 // MMA issue: one thread needs well over 100 SM cycles to issue a tcgen05.mma,
-// more than the tensor time of a 128 x 160 x 16 MMA per SM, so three warps of
-// the leader issue, taking the stages of the stream in turn, all into the same
-// accumulator.
+// more than the tensor time of a 128 x 160 x 16 MMA per SM, so four warps of
+// the leader issue, taking the stages of the stream in turn (each always the
+// same ring slot), all into the same accumulator.
 // Every MMA accumulates (the drain zeroes the accumulator after reading it);
-// the partial sums are exact integers, so the order in which the three
+// the partial sums are exact integers, so the order in which the four
 // streams land does not matter.
 //
-// Roles (384 threads per CTA): warps 0-7 drain and epilogue (warp w: TMEM
+// Roles (416 threads per CTA): warps 0-7 drain and epilogue (warp w: TMEM
 // lanes 32(w%4)..+31 of the CTA's own TMEM, accumulator columns 80(w/4)..+79),
-// warp 8 TMA producer, warps 9-11 MMA issue (the leader's; warp 9 of each CTA
+// warp 8 TMA producer, warps 9-12 MMA issue (the leader's; warp 9 of each CTA
 // also allocates TMEM, collectively for the pair). Every wait is bounded (~1 s) and records a timeout in the status word.
 //
 // Barriers: full[s] (leader) counts the leader's expect_tx and both CTAs'
@@ -60,11 +60,11 @@ namespace i2s {
 
 namespace {
 
-constexpr int kThreads8 = 384;
+constexpr int kThreads8 = 416;
 constexpr int kEpiWarps8 = 8;                // two per TMEM lane quarter, one per half of the columns
 constexpr int kTmaWarp8 = 8;
-constexpr int kMmaWarp8 = 9;                // warps 9-11
-constexpr int kIssuers8 = 3;
+constexpr int kMmaWarp8 = 9;                // warps 9-12
+constexpr int kIssuers8 = 4;
 constexpr int kKB8 = 128;                    // K positions per stage (two 64-position swizzle atoms)
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
 constexpr int kStages8 = 4;
@@ -83,6 +83,11 @@ constexpr long long kWaitLimit8 = 2000000000LL;
 static_assert(kSCol8 + kI8sTileM <= kTmemCols8, "TMEM budget");
 static_assert(kBAtomBytes % 1024 == 0 && kI8sTileM % 32 == 0, "swizzle atoms of the B half");
 static_assert(kI8sTileM % 32 == 0 && kI8sTileM % 16 == 0 && kI8sTileM <= 256, "MMA N");
+// Issuer i takes the stages s with s % kIssuers8 == i. Each ring slot must
+// always be served by the same issuer: a parity wait cannot tell the phase it
+// wants from the one two phases later, so an issuer must never wait on a slot
+// whose previous phase another issuer has not consumed yet.
+static_assert(kStages8 % kIssuers8 == 0, "ring slots per issuer");
 
 struct Smem8 {
     uint64_t full[kStages8];
