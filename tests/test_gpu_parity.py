@@ -407,6 +407,35 @@ def test_i8s_mul_mat_add(i2s, o, M, N, K, relu, with_bias):
     same_bits(host(y8), oy8)
 
 
+@pytest.mark.parametrize("K", [384, 640, 1088, 3072])
+def test_i8s_stage_ring_wraps(i2s, o, K):
+    # 3, 5, 9 and 24 stages of 128 positions: every stage slot of the
+    # operand ring is reused, with a ragged N that leaves part of the second
+    # CTA of a pair without weight rows
+    M, N = 64, 300
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=K)
+    y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M, bias=dev(bias), relu=True)
+    assert i2s.read_status(ws) == 0
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, relu=True, nth=4)
+    same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+    same_bits(host(y8), oy8)
+
+
+def test_i8s_repeated_calls_identical(i2s, o):
+    # the same call twenty times: every run's bits equal the oracle's (the MMA
+    # issuers, producers and split-tile completion race differently each time)
+    M, N, K = 300, 640, 4096
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=5)
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, nth=8)
+    dw, dx, db = dev(wp), dev(xp), dev(bias)
+    y8, ws = i2s.i8s_mul_mat_add_relu(dw, N, K, dx, M, bias=db)
+    for _ in range(20):
+        i2s.i8s_mul_mat_add_relu(dw, N, K, dx, M, bias=db, y=y8, ws=ws)
+        assert i2s.read_status(ws) == 0
+        same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+        same_bits(host(y8), oy8)
+
+
 def test_i8s_headroom(i2s, o):
     # every weight and activation at +127: acc = 127*127*K = 132,120,576 (> 2^24)
     M, N, K = 16, 64, 8192
