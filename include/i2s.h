@@ -157,7 +157,7 @@ typedef struct i2s_config {
                         rows); 2 tensor-core GEMM; 3 tensor-core GEMV (M <= 16) */
     int split_k;     /* GEMV: CTAs sharing one row block along K (1, 2, 4, 8) */
     int rows_per_cta;/* GEMV: weight rows per CTA tile (multiple of 16) */
-    int grid_ctas;   /* paths 2 and 3: persistent CTA count (<= SM count, 2x for path 3) */
+    int grid_ctas;   /* paths 2 and 3: persistent CTA count (<= SM count, 2x for path 3; path 2 runs CTA pairs: rounded down to an even count, at least 2) */
 } i2s_config;
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,

@@ -361,8 +361,8 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         ta.BN = BN;
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         for (int a = 0; a < n_act; ++a)
-            if (!make_f16_operand_map(&ta.maps[a], base + slots[a].op_off, (int)M, (int)probs[first[a]].K, BN))
-                return I2S_E_CUDA;
+            if (!make_f16_operand_map(&ta.maps[a], base + slots[a].op_off, (int)M, (int)probs[first[a]].K, BN / 2))
+                return I2S_E_CUDA;   // each CTA of a pair loads half of a tile's activation rows
         const int n_act_tiles = (int)((M + BN - 1) / BN);
         int tiles = 0;
         for (int i = 0; i < count; ++i) {
@@ -378,14 +378,16 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
             p.map = act_of[i];
             p.tile0 = tiles;
             p.n_act_tiles = n_act_tiles;
-            tiles += (int)((q.N + kTcTileW - 1) / kTcTileW) * n_act_tiles;
+            tiles += (int)((q.N + 2 * kTcTileW - 1) / (2 * kTcTileW)) * n_act_tiles;   // 256-row tiles, one CTA pair each
         }
         ta.total_tiles = tiles;
         const int sms = device_sm_count();
-        int grid = grid_ctas > 0 ? grid_ctas : sms;
-        if (grid > sms) grid = sms;
-        if (grid > tiles) grid = tiles;
-        r = cuda_status(launch_gemm_tc(ta, grid, stream));
+        int pairs = (grid_ctas > 0 ? grid_ctas : sms) / 2;   // clusters of two CTAs
+        const int resident = gemm_tc_max_pairs();   // a persistent grid: no second wave
+        if (pairs > resident) pairs = resident;
+        if (pairs > tiles) pairs = tiles;
+        if (pairs < 1) pairs = 1;
+        r = cuda_status(launch_gemm_tc(ta, 2 * pairs, stream));
         if (r) return r;
     }
     return I2S_OK;
@@ -634,7 +636,7 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.n_at = (int)(rows_pad / kI8sTileM);
     a.chunks = (int)i8s_chunks(K);
     a.total_units = (int)(tiles / 2) * a.chunks;   // units of whole (256-feature) tiles
-    int pairs = device_sm_count() / 2;
+    int pairs = i8s_gemm_tc_max_pairs();   // resident pairs: a persistent grid, no second wave
     if (pairs > a.total_units) pairs = a.total_units;
     const int grid = 2 * pairs;   // clusters of two CTAs
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));

@@ -23,8 +23,14 @@
 //              K-major layout, then fencing the writes into the async proxy;
 //   warp 12    TMA producer of the activation tile (f16, 128B swizzle);
 //   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM).
-// MMA: M = 128 weight rows (the "swapped" A operand), N = up to 256
-// activation rows, K = 16 per instruction, 4 instructions per K block. Two
+// CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
+// cta_group::2 MMAs. A tile is 256 weight rows (the "swapped" A operand; 128
+// converted in each CTA's shared memory, 128 accumulator rows in each CTA's
+// TMEM) x up to 256 activation rows (the B operand; half of them TMA'd into
+// each CTA's shared memory). The leader (rank 0) issues M = 256 x N x K = 16
+// MMAs, 4 per K block; both CTAs' converters and TMA loads report to the
+// leader's stage barriers, its commits multicast to both CTAs, and each CTA's
+// epilogue releases the leader's accumulator barrier by a remote arrive. Two
 // TMEM accumulators of 256 columns let the epilogue of one tile overlap the
 // MMAs of the next. One thread needs well over 100 SM cycles to issue a
 // tcgen05.mma, so two warps issue, taking the K blocks of the stream in turn,
@@ -59,14 +65,19 @@ constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;                // warps 13-14
 constexpr int kIssuersTc = 2;
 constexpr int kThreadsTc = 480;
-constexpr int kStagesTc = 4;
+constexpr int kStagesTc = 6;
 constexpr int kCvtPrefetch = 8;             // K blocks of packed codes each converter keeps in flight
 constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
 constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
 constexpr int kATileBytes = kTileW * 128;   // 16 KB
-constexpr int kBTileBytesMax = 256 * 128;   // 32 KB
+constexpr int kBTileBytesMax = 128 * 128;   // 16 KB: this CTA's half of up to 256 activation rows
 constexpr int kTmemCols = 512;
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
+// Issuer i takes the K blocks s with s % kIssuersTc == i; each stage slot must
+// always be served by the same issuer (a parity wait cannot tell the phase it
+// wants from the one two phases later).
+static_assert(kStagesTc % kIssuersTc == 0, "ring slots per issuer");
+static_assert(kCvtPrefetch % 2 == 0, "converters take K blocks in pairs");
 
 struct SmemTc {
     float sc_col[2][256];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
@@ -78,6 +89,7 @@ struct SmemTc {
     uint64_t tmem_empty[2];
     uint64_t mma_done[kIssuersTc];
     uint64_t stage_bar;     // the epilogue threads have staged a tile's column factors
+    alignas(16) uint8_t signal[16];   // source (peer) and destination (leader) of the stage-ready copies
     uint32_t tmem_base;
     int abort;
 };
@@ -103,7 +115,7 @@ __device__ __forceinline__ void expand_word_f16(uint32_t w, uint4& c0, uint4& c1
     c1.z = w & m;         c1.w = (w >> 8) & m;
 }
 
-__global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_constant__ TcArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
@@ -113,26 +125,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int BN = a.BN;
-    const uint32_t b_tile_bytes = (uint32_t)BN * 128u;
+    const int BH = BN / 2;                                  // activation rows of a tile in each CTA
+    const uint32_t b_half_bytes = (uint32_t)BH * 128u;
+    const uint32_t rank = tc::cluster_rank();               // 0: the leader, which issues the MMAs
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
     if (tid == 0) {
         for (int s = 0; s < kStagesTc; ++s) {
-            tc::mbar_init(&S.full_a[s], kCvtWarps * 32);
+            // one arrive per converter warp; the leader's also counts the
+            // 16 bytes of the peer's stage-ready copy
+            tc::mbar_init(&S.full_a[s], kCvtWarps);
             tc::mbar_init(&S.full_b[s], 1);
             tc::mbar_init(&S.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&S.tmem_full[b], kIssuersTc);
-            tc::mbar_init(&S.tmem_empty[b], kEpiWarps * 32);
+            tc::mbar_init(&S.tmem_empty[b], 2 * kEpiWarps);   // one arrive per epilogue warp of both CTAs
         }
         for (int i = 0; i < kIssuersTc; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.stage_bar, kEpiWarps * 32);
         S.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
-        tc::tmem_alloc(&S.tmem_base, kTmemCols);
-        tc::tmem_relinquish();
+    if (warp == kMmaWarp) {   // one warp of each CTA, collectively for the pair
+        tc::pair_tmem_alloc(&S.tmem_base, kTmemCols);
+        tc::pair_tmem_relinquish();
     }
     if (warp == kTmaWarp && lane == 0)
         for (int i = 0; i < a.n_maps; ++i) tc::tma_prefetch_desc(&a.maps[i]);
@@ -147,8 +164,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             tc::tmem_st_zero_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + col);
         tc::tmem_st_wait();
     }
+    // both CTAs' barriers initialised and accumulators zeroed before any
+    // remote arrive, multicast commit or MMA
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     tc::tc_fence_after();
 
     auto fail = [&](uint32_t code) {
@@ -164,22 +183,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             bool pending[kStagesTc] = {};
             uint32_t pending_phase[kStagesTc] = {};
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+            for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
                 const TcProb& P = a.p[find_problem(a, tile)];
                 const int at = (tile - P.tile0) % P.n_act_tiles;
                 const int KB = P.K / kBlockK;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(1); ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&S.full_b[stage], b_tile_bytes);
-                    tc::tma_load_2d(sB + (size_t)stage * kBTileBytesMax, &a.maps[P.map], kb * kBlockK, at * BN,
-                                    &S.full_b[stage]);
+                    // the leader expects both CTAs' halves; a peer's bytes may land first
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&S.full_b[stage], 2 * b_half_bytes);
+                    tc::pair_tma_load_2d(sB + (size_t)stage * kBTileBytesMax, &a.maps[P.map], kb * kBlockK,
+                                         at * BN + (int)rank * BH, tc::smem_in_rank(&S.full_b[stage], 0));
                     pending[stage] = true;
                     pending_phase[stage] = phase;
                     if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // let this thread's copies in flight land before the CTA exits
+            if (!ok && rank == 0) {
+                // let the copies in flight land before the CTA exits (they are
+                // counted on the leader's barriers)
                 for (int s = 0; s < kStagesTc; ++s)
                     if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimit / 8);
             }
@@ -194,10 +215,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+        for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
             const TcProb& P = a.p[find_problem(a, tile)];
             const int wt = (tile - P.tile0) / P.n_act_tiles;
-            const int n = wt * kTileW + r;
+            const int n = wt * (2 * kTileW) + (int)rank * kTileW + r;   // this CTA's half of the 256 rows
             const int KB = P.K / kBlockK;
             const bool valid = n < P.N;
             const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4) + 8 * hf;
@@ -210,34 +231,59 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
 #pragma unroll
             for (int j = 0; j < kCvtPrefetch; ++j) buf[j] = load(j);
             for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
+                // two K blocks (stage slots) per pass: one proxy fence and one
+                // warp sync for both halve the per-stage latency of the loop
 #pragma unroll
-                for (int j = 0; j < kCvtPrefetch; ++j) {
+                for (int j = 0; j < kCvtPrefetch; j += 2) {
                     const int kb = kb0 + j;
                     if (kb >= KB) break;
-                    if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(2); ok = false; break; }
-                    uint8_t* dst = sA + (size_t)stage * kATileBytes;
-                    const uint32_t words[2] = {buf[j].x, buf[j].y};
-                    buf[j] = load(kb + kCvtPrefetch);
+                    const bool two = kb + 1 < KB;
+                    const int stage1 = stage + 1 == kStagesTc ? 0 : stage + 1;
+                    const uint32_t phase1 = stage + 1 == kStagesTc ? phase ^ 1 : phase;
+                    // warp-uniform outcome: the warp arrives as one
+                    bool got = tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit);
+                    if (got && two) got = tc::mbar_wait(&S.empty[stage1], phase1 ^ 1, abort_flag, kWaitLimit);
+                    if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
 #pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int word = 2 * hf + w;   // 32-bit word of the row's 16 bytes
-                        uint4 c0, c1;
-                        expand_word_f16(words[w], c0, c1);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word)) = c0;
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word + 1)) = c1;
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two) break;
+                        uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
+                        const uint32_t words[2] = {buf[j + h].x, buf[j + h].y};
+                        buf[j + h] = load(kb + h + kCvtPrefetch);
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) {
+                            const int word = 2 * hf + w;   // 32-bit word of the row's 16 bytes
+                            uint4 c0, c1;
+                            expand_word_f16(words[w], c0, c1);
+                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word)) = c0;
+                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word + 1)) = c1;
+                        }
                     }
                     tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(&S.full_a[stage]);
-                    if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
+                    __syncwarp();
+                    // CTA-scope arrives: a cluster-scope release here would
+                    // also wait for this thread's prefetched loads to land
+                    if (lane == 0) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (h == 1 && !two) break;
+                            uint64_t* bar = &S.full_a[h ? stage1 : stage];
+                            if (rank == 0 && warp == kEpiWarps) tc::mbar_arrive_expect_tx(bar, 16);
+                            else tc::mbar_arrive(bar);
+                        }
+                    }
+                    stage = stage1;
+                    phase = phase1;
+                    if (two && ++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
             }
         }
-    } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc) {
+    } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc && rank == 0) {
         // ---------------------------------------------------------- MMA issue
         // issuer `me` takes the K blocks whose position in this CTA's stream
         // is me modulo kIssuersTc; the ring index advances over all of them
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16_f32(kTileW, BN);
+            const uint32_t idesc = tc::idesc_f16_f32(2 * kTileW, BN);   // 256 x BN over the pair
             const int me = warp - kMmaWarp;
             int stage = 0;
             uint32_t phase = 0;
@@ -245,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
             uint32_t acc_phase = 0;
             int seq = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+            for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
                 const TcProb& P = a.p[find_problem(a, tile)];
                 const int KB = P.K / kBlockK;
                 if (!tc::mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimit)) { fail(4); break; }
@@ -260,30 +306,49 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                         const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBTileBytesMax));
 #pragma unroll
                         for (int k = 0; k < kBlockK / 16; ++k)   // +32 bytes per 16-element K step
-                            tc::umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
-                        tc::umma_commit(&S.empty[stage]);
+                            tc::pair_umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
+                        tc::pair_commit(&S.empty[stage], 0x3);   // both CTAs' stage slots are free
                     }
                     if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                // the tile is complete once every issuer's MMAs are
-                tc::umma_commit(&S.tmem_full[acc]);
+                // the tile is complete (in both CTAs' TMEM) once every issuer's MMAs are
+                tc::pair_commit(&S.tmem_full[acc], 0x3);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
             // every MMA this thread issued has completed before TMEM is freed
-            tc::umma_commit(&S.mma_done[me]);
+            tc::pair_commit(&S.mma_done[me], 0x1);
             tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit / 8);
+        }
+    } else if (warp == kMmaWarp && rank == 1) {
+        // ---------------------------------------------------------- forwarder
+        // the peer's converted stages, each signalled to the leader's barrier
+        // by a 16-byte copy, in the order the MMAs consume them (a remote
+        // release arrive costs over a thousand cycles, serialising the ring)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
+                const int KB = a.p[find_problem(a, tile)].K / kBlockK;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
+                    tc::dsmem_copy_signal(tc::smem_in_rank(S.signal, 0), S.signal, 16,
+                                          tc::smem_in_rank(&S.full_a[stage], 0));
+                    if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
+                }
+            }
         }
     } else if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
         const int r = warp * 32 + lane;   // TMEM lane = weight row within the tile
         int acc = 0;
         uint32_t acc_phase = 0, stage_phase = 0;
-        for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
+        for (int tile = pair; tile < a.total_tiles; tile += n_pairs) {
             const TcProb& P = a.p[find_problem(a, tile)];
             const int local = tile - P.tile0;
             const int wt = local / P.n_act_tiles, at = local % P.n_act_tiles;
-            const int n = wt * kTileW + r;
+            const int n = wt * (2 * kTileW) + (int)rank * kTileW + r;
             // stage the tile's per-column factors (w_scale * act_scale[m] and
             // row_sum[m]) in shared memory while the accumulator fills
             const int m_base = at * BN;
@@ -298,10 +363,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                 }
                 // every epilogue thread has staged its columns (bounded wait)
                 tc::mbar_arrive(&S.stage_bar);
-                if (!tc::mbar_wait(&S.stage_bar, stage_phase, abort_flag, kWaitLimit)) { fail(16); break; }
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.stage_bar, stage_phase, abort_flag, kWaitLimit))) {
+                    fail(16);
+                    break;
+                }
                 stage_phase ^= 1;
             }
-            if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimit)) { fail(16); break; }
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimit))) {
+                fail(16);
+                break;
+            }
             tc::tc_fence_after();
             const float* sc_col = S.sc_col[acc];
             const int* rs_col = S.rs_col[acc];
@@ -344,7 +415,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
                 for (int c2 = 0; c2 < C; ++c2) tc::tmem_st_zero_32x32b_x32(d_addr + 32u * c2);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
-                tc::mbar_arrive(&S.tmem_empty[acc]);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_cluster(tc::smem_in_rank(&S.tmem_empty[acc], 0));   // the leader's barrier
             };
             uint32_t va[32], vb[32];
             tc::tmem_ld_32x32b_x32(d_addr, va);
@@ -368,11 +440,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_cons
         }
     }
 
+    // every MMA of the pair has completed (the epilogues waited for the last
+    // tmem_full) and neither CTA's shared memory is read any more
+    __syncwarp();
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     if (warp == kMmaWarp) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        tc::pair_tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -431,17 +506,46 @@ bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s) {
-    static std::atomic<uint64_t> configured{0};
+// Per device: 1 + the number of CTA pairs that can be resident at once (0:
+// not yet configured). Clusters must fit inside a GPC, so on a part whose
+// GPCs have odd SM counts this is below half the SM count, and a persistent
+// grid of more pairs would run its surplus as a second wave.
+static std::atomic<int> g_pairs[64];
+
+static cudaError_t configure(int* dev_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(k_i2s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTcBytes);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
-    }
+    *dev_out = dev;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_pairs[dev].load() > 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_i2s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTcBytes);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(kThreadsTc, 1, 1);
+    cfg.dynamicSmemBytes = kSmemTcBytes;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, (void*)k_i2s_gemm_tc, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    g_pairs[dev].store(1 + clusters);
+    return cudaSuccess;
+}
+
+int gemm_tc_max_pairs() {
+    int dev = 0;
+    if (configure(&dev) != cudaSuccess) return 1;
+    return g_pairs[dev].load() - 1;
+}
+
+cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = configure(&dev);
+    if (e != cudaSuccess) return e;
     k_i2s_gemm_tc<<<grid, kThreadsTc, kSmemTcBytes, s>>>(a);
     return cudaGetLastError();
 }

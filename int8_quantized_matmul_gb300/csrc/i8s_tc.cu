@@ -499,17 +499,46 @@ cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s) {
-    static std::atomic<uint64_t> configured{0};
+// Per device: 1 + the number of CTA pairs that can be resident at once (0:
+// not yet configured). Clusters must fit inside a GPC, so on a part whose
+// GPCs have odd SM counts this is below half the SM count, and a persistent
+// grid of more pairs would run its surplus as a second wave.
+static std::atomic<int> g_pairs[64];
+
+static cudaError_t configure(int* dev_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(k_i8s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem8Bytes);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
-    }
+    *dev_out = dev;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_pairs[dev].load() > 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_i8s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem8Bytes);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(kThreads8, 1, 1);
+    cfg.dynamicSmemBytes = kSmem8Bytes;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, (void*)k_i8s_gemm_tc, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    g_pairs[dev].store(1 + clusters);
+    return cudaSuccess;
+}
+
+int i8s_gemm_tc_max_pairs() {
+    int dev = 0;
+    if (configure(&dev) != cudaSuccess) return 1;
+    return g_pairs[dev].load() - 1;
+}
+
+cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = configure(&dev);
+    if (e != cudaSuccess) return e;
     k_i8s_gemm_tc<<<grid, kThreads8, kSmem8Bytes, s>>>(a);
     return cudaGetLastError();
 }

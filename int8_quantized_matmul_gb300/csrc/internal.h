@@ -142,6 +142,7 @@ bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, i
 // rows x row_bytes uint8 matrix, box {128 bytes, box_rows}, 128-byte swizzle
 bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes, int box_rows);
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
+int gemm_tc_max_pairs();   // CTA pairs of the GEMM that fit on the device at once
 cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -176,6 +177,7 @@ cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* 
                               __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
                               cudaStream_t s);
 cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s);
+int i8s_gemm_tc_max_pairs();   // CTA pairs of the I8_S GEMM that fit on the device at once
 
 cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s);
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst,

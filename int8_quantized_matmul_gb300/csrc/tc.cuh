@@ -163,6 +163,19 @@ __device__ __forceinline__ uint32_t smem_in_rank(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's of the cluster, completing that
+// many transaction bytes on a barrier of the destination CTA (dst and bar are
+// shared::cluster addresses of the same CTA). An async-proxy signal: unlike a
+// cluster-scope release arrive, issuing it does not wait for the thread's
+// earlier memory operations.
+__device__ __forceinline__ void dsmem_copy_signal(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
 // One warp in each CTA of the pair, collectively; both get the same address.
 __device__ __forceinline__ void pair_tmem_alloc(uint32_t* holder, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)), "r"(ncols)
