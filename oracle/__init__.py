@@ -21,6 +21,16 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   i8s_mul_mat_add         numpy int64 matmul in the power-of-two special case,
                           with and without ReLU and bias
   i8s_permute_cont        numpy transpose plus the carried scale bytes
+  i8s_add_scaled          power-of-two scales (exact): numpy sum; swap symmetry
+  i8s_rms_norm_scaled     constant-row closed form, power-of-two scale
+                          invariance, unit RMS of the rows, zero rows, gamma
+                          scaling
+  i8s_im2col_asym         numpy pad + strided windows, causal geometry, the
+                          carried scale bytes
+  i8s_depthwise_mul_mat_add  numpy per-channel correlation in the power-of-two
+                          special case
+  w8a8_quantize_weights   hand-made ties (ties to even), amax floor
+  w8a8_mul_mat            numpy int64 matmul with power-of-two scales
 """
 
 from __future__ import annotations
@@ -88,6 +98,15 @@ class Oracle:
             "orc_i8s_quantize": (None, [_p, _i64, _p]),
             "orc_i8s_mul_mat_add": (None, [_p, _i64, _i64, _p, _i64, _p, _int, _p, _p, _int]),
             "orc_i8s_permute_cont": (None, [_p, _i64, _i64, _p]),
+            "orc_i8s_add_scaled": (None, [_p, _p, _i64, _p, _p]),
+            "orc_i8s_rms_norm_scaled": (None, [_p, _i64, _i64, _f32, _p, _p, _p]),
+            "orc_im2col_out_len": (_i64, [_i64, _i64, _i64, _i64, _i64]),
+            "orc_i8s_im2col_asym": (None, [_p, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+            "orc_i8s_depthwise_mul_mat_add": (None, [_p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _p, _int,
+                                                     _p, _p]),
+            "orc_w8a8_quantize_weights": (None, [_p, _i64, _i64, _p, _p]),
+            "orc_w8a8_quantize_rows": (None, [_p, _i64, _i64, _p, _p]),
+            "orc_w8a8_mul_mat": (None, [_p, _p, _i64, _i64, _p, _i64, _p, _int, _p, _p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -205,6 +224,78 @@ class Oracle:
         dst = np.zeros(self.i8s_nbytes(a * b), dtype=np.uint8)
         self._L.orc_i8s_permute_cont(_ptr(packed), a, b, _ptr(dst))
         return dst
+
+    # -- I8_S element-wise and conv pieces ---------------------------------
+    def i8s_add_scaled(self, a_packed, b_packed, n):
+        a_packed = np.ascontiguousarray(a_packed, dtype=np.uint8)
+        b_packed = np.ascontiguousarray(b_packed, dtype=np.uint8)
+        y8 = np.zeros(self.i8s_nbytes(n), dtype=np.uint8)
+        yf = np.zeros(n, dtype=np.float32)
+        self._L.orc_i8s_add_scaled(_ptr(a_packed), _ptr(b_packed), n, _ptr(y8), _ptr(yf))
+        return y8, yf
+
+    def i8s_rms_norm_scaled(self, x_packed, rows, ne0, eps=1e-5, gamma=None):
+        x_packed = np.ascontiguousarray(x_packed, dtype=np.uint8)
+        if gamma is not None:
+            gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+        y8 = np.zeros(self.i8s_nbytes(rows * ne0), dtype=np.uint8)
+        yf = np.zeros((rows, ne0), dtype=np.float32)
+        self._L.orc_i8s_rms_norm_scaled(_ptr(x_packed), rows, ne0, float(eps), _ptr(gamma), _ptr(y8), _ptr(yf))
+        return y8, yf
+
+    def im2col_out_len(self, L, KW, stride, pad_l, pad_r):
+        return int(self._L.orc_im2col_out_len(L, KW, stride, pad_l, pad_r))
+
+    def i8s_im2col_asym(self, x_packed, C, L, KW, stride, pad_l, pad_r):
+        x_packed = np.ascontiguousarray(x_packed, dtype=np.uint8)
+        OL = self.im2col_out_len(L, KW, stride, pad_l, pad_r)
+        dst = np.zeros(self.i8s_nbytes(OL * C * KW), dtype=np.uint8)
+        self._L.orc_i8s_im2col_asym(_ptr(x_packed), C, L, KW, stride, pad_l, pad_r, _ptr(dst))
+        return dst, OL
+
+    def i8s_depthwise_mul_mat_add(self, w_packed, KW, x_packed, C, L, stride, pad_l, pad_r, bias=None,
+                                  relu=False):
+        w_packed = np.ascontiguousarray(w_packed, dtype=np.uint8)
+        x_packed = np.ascontiguousarray(x_packed, dtype=np.uint8)
+        if bias is not None:
+            bias = np.ascontiguousarray(bias, dtype=np.float32)
+        OL = self.im2col_out_len(L, KW, stride, pad_l, pad_r)
+        y8 = np.zeros(self.i8s_nbytes(C * OL), dtype=np.uint8)
+        yf = np.zeros((C, OL), dtype=np.float32)
+        self._L.orc_i8s_depthwise_mul_mat_add(_ptr(w_packed), KW, _ptr(x_packed), C, L, stride, pad_l, pad_r,
+                                              _ptr(bias), 1 if relu else 0, _ptr(y8), _ptr(yf))
+        return y8, yf
+
+    # -- W8A8 per-channel ---------------------------------------------------
+    def w8a8_quantize_weights(self, w):
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        N, K = w.shape
+        wq = np.zeros((N, K), dtype=np.int8)
+        bs = np.zeros(N, dtype=np.float32)
+        self._L.orc_w8a8_quantize_weights(_ptr(w), N, K, _ptr(wq), _ptr(bs))
+        return wq, bs
+
+    def w8a8_quantize_rows(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        M, K = x.shape
+        q = np.zeros((M, K), dtype=np.int8)
+        s = np.zeros(M, dtype=np.float32)
+        self._L.orc_w8a8_quantize_rows(_ptr(x), M, K, _ptr(q), _ptr(s))
+        return q, s
+
+    def w8a8_mul_mat(self, wq, bscale, x, nth=1, want_sidecar=False):
+        wq = np.ascontiguousarray(wq, dtype=np.int8)
+        bscale = np.ascontiguousarray(bscale, dtype=np.float32)
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        N, K = wq.shape
+        M = x.shape[0]
+        d = np.zeros((M, N), dtype=np.float32)
+        q = np.zeros((M, K), dtype=np.int8) if want_sidecar else None
+        s = np.zeros(M, dtype=np.float32) if want_sidecar else None
+        self._L.orc_w8a8_mul_mat(_ptr(wq), _ptr(bscale), N, K, _ptr(x), M, _ptr(d), int(nth), _ptr(q), _ptr(s))
+        if want_sidecar:
+            return d, q, s
+        return d
 
 
 _default: Oracle | None = None

@@ -26,6 +26,23 @@
 //      of 32, then the F32 scale, then 28 zero bytes (32-byte trailer).
 //   R4 I8_S mul_mat_add: y = (float)acc * (w_scale*x_scale), then + bias[n],
 //      then ReLU (y > 0 ? y : +0), then per-tensor requantization (R2).
+//   R5 add_scaled: y = (float)qa*sa + (float)qb*sb (two products, one sum),
+//      then per-tensor requantization (R2).
+//   R6 rms_norm_scaled: rows of ne0 contiguous values x = q*s; mean square
+//      (double)sum(q^2) * ((double)s*(double)s) / ne0 in double; row factor
+//      r = (float)(1/sqrt(mean + eps)) in double; y = (x*r) (*gamma[i]) in
+//      float; then per-tensor requantization (R2). No weight when gamma is null.
+//   R7 im2col_asym: input C x L (L contiguous), output OL x (C*KW) with
+//      dst[t][c*KW + k] = src[c][t*stride + k - pad_l] (0 outside [0, L)),
+//      OL = (L + pad_l + pad_r - KW) / stride + 1; the scale is carried.
+//   R8 depthwise mul_mat_add: per channel, the im2col_asym geometry of R7 on
+//      that channel alone, acc in int32, then R4's epilogue with bias[c];
+//      output C x OL.
+//   R9 W8A8 ([P4]): per-channel weights: amax floored at 1e-9, bscale =
+//      amax/127, q = rint(w / bscale) (ties to even, as the page's lrintf)
+//      clamped to +-127; per-row activations: amax floored at 1e-9, ascale =
+//      amax/127, inv = 127/amax, q = round(x*inv) (R1) clamped; then
+//      d = ascale[m] * bscale[n] * (float)C, left to right.
 //
 // Parity pins: every function here is pinned by tests that do not re-use its
 // arithmetic (hand decode, closed forms, brute force, numpy integer matmul in
@@ -387,4 +404,215 @@ ORC_API void orc_i8s_permute_cont(const uint8_t* src, int64_t a, int64_t b, uint
 #else
     orc_i8s_pack(t.data(), n, get_scale(src, orc_i8s_scale_offset(n)), dst);
 #endif
+}
+
+// ---------------------------------------------------------------------------
+// ggml_add_scaled ([P1] "Five fused INT8 ops": I8_S + I8_S -> I8_S with the
+// two input scales reconciled). Reading R5: both inputs are dequantized (one
+// IEEE product each), added (one IEEE sum) and the sum is requantized with one
+// scale for the whole tensor. y_f32 (optional) receives the sums.
+// ---------------------------------------------------------------------------
+ORC_API void orc_i8s_add_scaled(const uint8_t* a_i8s, const uint8_t* b_i8s, int64_t n, uint8_t* y_i8s,
+                                float* y_f32) {
+    const int8_t* qa = (const int8_t*)a_i8s;
+    const int8_t* qb = (const int8_t*)b_i8s;
+    const float sa = get_scale(a_i8s, orc_i8s_scale_offset(n));
+#if ORC_PLANT == 14
+    const float sb = sa;
+#else
+    const float sb = get_scale(b_i8s, orc_i8s_scale_offset(n));
+#endif
+    std::vector<float> y((size_t)n);
+    for (int64_t i = 0; i < n; ++i) {
+        const float va = (float)qa[i] * sa;
+        const float vb = (float)qb[i] * sb;
+        y[i] = va + vb;
+    }
+    if (y_f32) memcpy(y_f32, y.data(), (size_t)n * 4);
+    orc_i8s_quantize(y.data(), n, y_i8s);
+}
+
+// ---------------------------------------------------------------------------
+// ggml_rms_norm_scaled ([P1] "Five fused INT8 ops": RMSNorm straight from I8_S
+// to I8_S; [P3] "Encoder": RMSNorm epsilon 1e-5 everywhere). Reading R6. The
+// mean square of a row of dequantized values q*s is s^2 * sum(q^2) / ne0; the
+// integer sum is exact, and the rest is a fixed sequence of double operations,
+// so the row factor does not depend on a summation order.
+// ---------------------------------------------------------------------------
+ORC_API void orc_i8s_rms_norm_scaled(const uint8_t* x_i8s, int64_t rows, int64_t ne0, float eps,
+                                     const float* gamma, uint8_t* y_i8s, float* y_f32) {
+    const int64_t n = rows * ne0;
+    const int8_t* q = (const int8_t*)x_i8s;
+    const float s = get_scale(x_i8s, orc_i8s_scale_offset(n));
+    std::vector<float> y((size_t)n);
+    for (int64_t r = 0; r < rows; ++r) {
+        const int8_t* qr = q + r * ne0;
+        int64_t ssq = 0;
+        for (int64_t i = 0; i < ne0; ++i) ssq += (int64_t)qr[i] * qr[i];
+#if ORC_PLANT == 15
+        const double mean = (double)ssq / (double)ne0;
+#elif ORC_PLANT == 16
+        const double mean = (double)ssq * ((double)s * (double)s) / (double)(ne0 > 1 ? ne0 - 1 : 1);
+#else
+        const double mean = (double)ssq * ((double)s * (double)s) / (double)ne0;
+#endif
+        const float rf = (float)(1.0 / sqrt(mean + (double)eps));
+        for (int64_t i = 0; i < ne0; ++i) {
+            const float x = (float)qr[i] * s;
+            float v = x * rf;
+            if (gamma) v = v * gamma[i];
+            y[r * ne0 + i] = v;
+        }
+    }
+    if (y_f32) memcpy(y_f32, y.data(), (size_t)n * 4);
+    orc_i8s_quantize(y.data(), n, y_i8s);
+}
+
+// ---------------------------------------------------------------------------
+// ggml_im2col_asym ([P1] "Five fused INT8 ops": im2col with independent
+// left/right padding, so a causal conv needs no separate pad node; [P3]
+// "Encoder": each stage starts with a strided causal conv, left pad
+// K - stride, right pad 0). Reading R7. The padding is the value 0, exact in
+// any scale, so the I8_S scale is carried unchanged.
+// ---------------------------------------------------------------------------
+ORC_API int64_t orc_im2col_out_len(int64_t L, int64_t KW, int64_t stride, int64_t pad_l, int64_t pad_r) {
+    const int64_t span = L + pad_l + pad_r - KW;
+    return span < 0 ? 0 : span / stride + 1;
+}
+
+ORC_API void orc_i8s_im2col_asym(const uint8_t* src_i8s, int64_t C, int64_t L, int64_t KW, int64_t stride,
+                                 int64_t pad_l, int64_t pad_r, uint8_t* dst_i8s) {
+    const int64_t OL = orc_im2col_out_len(L, KW, stride, pad_l, pad_r);
+    const int8_t* src = (const int8_t*)src_i8s;
+    std::vector<int8_t> out((size_t)(OL * C * KW));
+    for (int64_t t = 0; t < OL; ++t)
+        for (int64_t c = 0; c < C; ++c)
+            for (int64_t k = 0; k < KW; ++k) {
+#if ORC_PLANT == 17
+                const int64_t pos = t * stride + k - pad_r;
+#else
+                const int64_t pos = t * stride + k - pad_l;
+#endif
+                out[(t * C + c) * KW + k] = (pos >= 0 && pos < L) ? src[c * L + pos] : (int8_t)0;
+            }
+    orc_i8s_pack(out.data(), OL * C * KW, get_scale(src_i8s, orc_i8s_scale_offset(C * L)), dst_i8s);
+}
+
+// ---------------------------------------------------------------------------
+// Depthwise mul_mat_add ([P1] "Tests": depthwise mul_mat_add among the fused
+// ops' cases; [P3] "Encoder": RMSNorm -> depthwise conv -> ... in every
+// block, causal). Reading R8: channel c of the I8_S input (C x L) is
+// convolved with row c of the I8_S kernel (C x KW) over the R7 geometry,
+// accumulated exactly, then y = (float)acc * (w_scale*x_scale) + bias[c]
+// (ReLU optional) and one scale for the whole C x OL output.
+// ---------------------------------------------------------------------------
+ORC_API void orc_i8s_depthwise_mul_mat_add(const uint8_t* w_i8s, int64_t KW, const uint8_t* x_i8s, int64_t C,
+                                           int64_t L, int64_t stride, int64_t pad_l, int64_t pad_r,
+                                           const float* bias, int relu, uint8_t* y_i8s, float* y_f32) {
+    const int64_t OL = orc_im2col_out_len(L, KW, stride, pad_l, pad_r);
+    const int8_t* w = (const int8_t*)w_i8s;
+    const int8_t* x = (const int8_t*)x_i8s;
+    const float ws = get_scale(w_i8s, orc_i8s_scale_offset(C * KW));
+    const float xs = get_scale(x_i8s, orc_i8s_scale_offset(C * L));
+    const float sc = ws * xs;
+    std::vector<float> y((size_t)(C * OL));
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t t = 0; t < OL; ++t) {
+            int64_t acc = 0;
+            for (int64_t k = 0; k < KW; ++k) {
+                const int64_t pos = t * stride + k - pad_l;
+#if ORC_PLANT == 18
+                const int64_t kk = KW - 1 - k;
+#else
+                const int64_t kk = k;
+#endif
+                if (pos >= 0 && pos < L) acc += (int64_t)w[c * KW + kk] * x[c * L + pos];
+            }
+            float v = (float)(int32_t)acc * sc;
+            if (bias) v = v + bias[c];
+            if (relu) v = v > 0.0f ? v : 0.0f;
+            y[c * OL + t] = v;
+        }
+    if (y_f32) memcpy(y_f32, y.data(), (size_t)(C * OL) * 4);
+    orc_i8s_quantize(y.data(), C * OL, y_i8s);
+}
+
+// ---------------------------------------------------------------------------
+// W8A8 per-channel matmul ([P4] "Hypothesis" and "Implementation"): int8
+// weights with one scale per output channel, int8 activations with one scale
+// per row, int32 accumulation, then d[m][n] = aScale[m] * bScale[n] * C[m][n].
+// Reading R9 for the two quantizers.
+// ---------------------------------------------------------------------------
+
+// Per-channel weight quantization, done once per weight on the page's
+// cache-miss path: w is N x K F32; wq is N x K int8 (row n = channel n).
+ORC_API void orc_w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale) {
+    for (int64_t n = 0; n < N; ++n) {
+        float mx = 1e-9f;
+        for (int64_t k = 0; k < K; ++k) {
+            const float v = fabsf(w[n * K + k]);
+            if (v > mx) mx = v;
+        }
+        const float s = mx / 127.0f;
+        bscale[n] = s;
+        for (int64_t k = 0; k < K; ++k) {
+#if ORC_PLANT == 20
+            float r = roundf(w[n * K + k] / s);
+#else
+            float r = rintf(w[n * K + k] / s);   // ties to even under the default rounding mode
+#endif
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            wq[n * K + k] = (int8_t)(int)r;
+        }
+    }
+}
+
+// Per-row activation quantization with the page's 1e-9 floor.
+ORC_API void orc_w8a8_quantize_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale) {
+    for (int64_t m = 0; m < M; ++m) {
+        const float* xr = x + m * K;
+        float mx = 1e-9f;
+        for (int64_t k = 0; k < K; ++k) {
+            const float v = fabsf(xr[k]);
+            if (v > mx) mx = v;
+        }
+        ascale[m] = mx / 127.0f;
+        const float inv = 127.0f / mx;
+        for (int64_t k = 0; k < K; ++k) {
+            float r = roundf(xr[k] * inv);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            q[m * K + k] = (int8_t)(int)r;
+        }
+    }
+}
+
+ORC_API void orc_w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x,
+                              int64_t M, float* d, int nth, int8_t* q_out, float* ascale_out) {
+    if (nth < 1) nth = 1;
+    std::vector<int8_t> q((size_t)(M * K));
+    std::vector<float> as((size_t)M);
+    orc_w8a8_quantize_rows(x, M, K, q.data(), as.data());
+    std::vector<std::thread> ts;
+    for (int t = 0; t < nth; ++t)
+        ts.emplace_back([&, t] {
+            for (int64_t n = t; n < N; n += nth)
+                for (int64_t m = 0; m < M; ++m) {
+                    int64_t acc = 0;
+                    for (int64_t k = 0; k < K; ++k) acc += (int64_t)wq[n * K + k] * q[m * K + k];
+                    if (acc > INT32_MAX || acc < INT32_MIN) {
+                        fprintf(stderr, "oracle: int32 accumulator range violated\n");
+                        abort();
+                    }
+#if ORC_PLANT == 19
+                    d[m * N + n] = bscale[n] * (float)(int32_t)acc;
+#else
+                    d[m * N + n] = as[m] * bscale[n] * (float)(int32_t)acc;
+#endif
+                }
+        });
+    for (auto& th : ts) th.join();
+    if (q_out) memcpy(q_out, q.data(), (size_t)(M * K));
+    if (ascale_out) memcpy(ascale_out, as.data(), (size_t)M * 4);
 }

@@ -363,4 +363,142 @@ def pin_i8s_permute_cont(o):
     assert np.array_equal(o.i8s_dequantize(t, a * b).reshape(b, a), deq.T)
 
 
+def pin_i8s_add_scaled_pow2(o):
+    # scales 2^-1 and 2^-3: qa/2 + qb/8 is exact in float, so numpy's float64
+    # sum rounded to float32 is the exact result; the op then requantizes it
+    for n in (1, 33, 4096, 100003):
+        qa = synth.int8_normal(n, seed=71)
+        qb = synth.int8_normal(n, seed=72)
+        a, b = o.i8s_pack(qa, 0.5), o.i8s_pack(qb, 0.125)
+        y8, yf = o.i8s_add_scaled(a, b, n)
+        ref = qa.astype(np.float64) / 2.0 + qb.astype(np.float64) / 8.0
+        assert np.array_equal(yf, ref.astype(np.float32)), n
+        assert np.array_equal(y8, o.i8s_quantize(yf)), n
+        # addition is commutative, scales included
+        assert np.array_equal(o.i8s_add_scaled(b, a, n)[0], y8), n
+
+
+def pin_i8s_rms_norm_closed_forms(o):
+    # (1) constant rows, eps = 0, power-of-two scale and |c|: x = c*s, the mean
+    #     square is (c*s)^2 exactly, so every output is sign(c) * 1 exactly
+    cs = np.array([1, -1, 2, -4, 64, -64, 8, 16], dtype=np.int8)
+    ne0 = 48
+    q = np.repeat(cs[:, None], ne0, axis=1)
+    y8, yf = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.125), len(cs), ne0, eps=0.0)
+    assert np.array_equal(yf, np.sign(q).astype(np.float32))
+    # ... and the requantized tensor is +-127 with scale 1/127
+    qq, sc = o.i8s_unpack(y8, q.size)
+    assert np.array_equal(qq.reshape(q.shape), (127 * np.sign(q)).astype(np.int8))
+    assert sc == np.float32(1.0) / np.float32(127.0)
+    # (2) with eps = 0 the result does not depend on a power-of-two input scale
+    g = synth.rng(73)
+    q = g.integers(-127, 128, size=(9, 70)).astype(np.int8)
+    q[:, 0] = 5   # no all-zero row
+    ya = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.5), 9, 70, eps=0.0)[1]
+    yb = o.i8s_rms_norm_scaled(o.i8s_pack(q, 4.0), 9, 70, eps=0.0)[1]
+    assert np.array_equal(ya, yb)
+    # (3) rows come out with unit RMS (eps far below the mean square)
+    q = synth.int8_normal((16, 64), seed=74)
+    q[:, 0] = 100
+    yf = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.05), 16, 64, eps=1e-5)[1].astype(np.float64)
+    rms = np.sqrt((yf * yf).mean(axis=1))
+    assert np.all(np.abs(rms - 1.0) < 1e-5), rms
+    # (4) an all-zero row stays zero (eps keeps the factor finite)
+    q = np.zeros((3, 32), dtype=np.int8)
+    q[1] = 9
+    yf = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.3), 3, 32, eps=1e-5)[1]
+    assert np.all(yf[0] == 0) and np.all(yf[2] == 0) and np.all(yf[1] > 0)
+    # (5) a power-of-two weight per feature scales the outputs exactly
+    q = synth.int8_normal((5, 40), seed=75)
+    q[:, 0] = 50
+    gamma = (2.0 ** synth.rng(76).integers(-3, 4, size=40)).astype(np.float32)
+    y0 = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.07), 5, 40)[1]
+    yg = o.i8s_rms_norm_scaled(o.i8s_pack(q, 0.07), 5, 40, gamma=gamma)[1]
+    assert np.array_equal(yg, y0 * gamma[None, :])
+
+
+def pin_i8s_im2col_asym(o):
+    g = synth.rng(77)
+    for (C, L, KW, stride, pad_l, pad_r) in ((3, 20, 4, 1, 3, 0), (5, 37, 7, 2, 5, 0), (2, 16, 8, 4, 4, 0),
+                                             (4, 29, 3, 3, 0, 2), (1, 5, 7, 1, 6, 1), (6, 64, 5, 5, 0, 0)):
+        X = g.integers(-127, 128, size=(C, L)).astype(np.int8)
+        packed = o.i8s_pack(X, 0.0625)
+        dst, OL = o.i8s_im2col_asym(packed, C, L, KW, stride, pad_l, pad_r)
+        xp = np.pad(X, ((0, 0), (pad_l, pad_r)))
+        starts = list(range(0, xp.shape[1] - KW + 1, stride))
+        assert OL == len(starts), (OL, len(starts))
+        ref = np.stack([xp[:, t:t + KW].reshape(-1) for t in starts]) if starts else np.zeros((0, C * KW), np.int8)
+        n = OL * C * KW
+        assert np.array_equal(dst[:n].view(np.int8), ref.reshape(-1))
+        off_s, off_d = o.i8s_scale_offset(C * L), o.i8s_scale_offset(n)
+        assert np.array_equal(dst[off_d:off_d + 32], packed[off_s:off_s + 32])
+    # causal geometry (left pad KW - stride, right pad 0): one output per
+    # stride step, and output t sees no input past t*stride + stride - 1
+    C, L, KW, stride = 2, 40, 8, 4
+    X = np.zeros((C, L), dtype=np.int8)
+    X[:, 21] = 7
+    dst, OL = o.i8s_im2col_asym(o.i8s_pack(X, 1.0), C, L, KW, stride, KW - stride, 0)
+    assert OL == L // stride
+    cols = dst[:OL * C * KW].view(np.int8).reshape(OL, C, KW)
+    first = min(t for t in range(OL) if cols[t].any())
+    assert first * stride + stride - 1 >= 21 and (first - 1) * stride + stride - 1 < 21
+
+
+def pin_i8s_depthwise_pow2(o):
+    # w_scale 2^-1, x_scale 2^-2, bias on the 2^-3 grid: y = acc/8 + bias
+    # exactly; acc is numpy's per-channel correlation of the padded input
+    g = synth.rng(78)
+    for (C, L, KW, stride, pad_l, pad_r) in ((4, 30, 7, 1, 6, 0), (3, 41, 7, 2, 5, 0), (8, 64, 3, 1, 1, 1)):
+        W = g.integers(-20, 21, size=(C, KW)).astype(np.int8)
+        X = g.integers(-127, 128, size=(C, L)).astype(np.int8)
+        bias = (g.integers(-64, 65, size=C) / 8.0).astype(np.float32)
+        wp, xp8 = o.i8s_pack(W, 0.5), o.i8s_pack(X, 0.25)
+        xp = np.pad(X.astype(np.int64), ((0, 0), (pad_l, pad_r)))
+        acc = np.stack([np.correlate(xp[c], W[c].astype(np.int64), mode="valid")[::stride] for c in range(C)])
+        for relu in (False, True):
+            y8, yf = o.i8s_depthwise_mul_mat_add(wp, KW, xp8, C, L, stride, pad_l, pad_r, bias=bias, relu=relu)
+            ref = acc.astype(np.float64) / 8.0 + bias.astype(np.float64)[:, None]
+            if relu:
+                ref = np.maximum(ref, 0.0)
+            assert yf.shape == ref.shape
+            assert np.array_equal(yf, ref.astype(np.float32)), (C, L, relu)
+            assert np.array_equal(y8, o.i8s_quantize(yf))
+
+
+def pin_w8a8_weight_quant(o):
+    # amax 127 gives scale exactly 1: the page divides by the scale and rounds
+    # with lrintf, so halfway values go to the even neighbour
+    w = np.array([[127.0, 2.5, -2.5, 3.5, 0.5, -0.5, 1.5, 126.5, -127.0, 4.4]], dtype=np.float32)
+    wq, bs = o.w8a8_quantize_weights(w)
+    assert bs[0] == np.float32(1.0)
+    assert wq[0].tolist() == [127, 2, -2, 4, 0, 0, 2, 126, -127, 4]
+    # an all-zero channel: the 1e-9 floor keeps the scale finite, codes 0
+    wq, bs = o.w8a8_quantize_weights(np.zeros((2, 8), dtype=np.float32))
+    assert np.all(wq == 0) and np.all(bs == np.float32(1e-9) / np.float32(127.0))
+
+
+def pin_w8a8_mul_mat_pow2(o):
+    # activations q/16 with max |q| = 127 per row: amax = 127/16, so the row
+    # scale is exactly 1/16 and the codes are exactly q; weight scales 2^-3:
+    # d = C / 128 exactly (|C| < 2^24)
+    g = synth.rng(79)
+    for (M, N, K) in ((3, 5, 64), (17, 70, 256), (9, 33, 2048)):
+        Q = g.integers(-127, 128, size=(M, K)).astype(np.int64)
+        Q[:, 0] = 127
+        x = (Q / 16.0).astype(np.float32)
+        wq = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+        bs = np.full(N, 0.125, dtype=np.float32)
+        d, q, s = o.w8a8_mul_mat(wq, bs, x, nth=2, want_sidecar=True)
+        assert np.array_equal(q.astype(np.int64), Q)
+        assert np.all(s == np.float32(1.0 / 16.0))
+        ref = (Q @ wq.astype(np.int64).T).astype(np.float64) / 128.0
+        assert np.array_equal(d, ref.astype(np.float32)), (M, N, K)
+    # the page's 1e-9 floor (not the 1e-5 of the I2_S quantizer): a row with
+    # amax 1e-7 still uses the full code range
+    x = np.zeros((1, 8), dtype=np.float32)
+    x[0, 3] = 1e-7
+    q, s = o.w8a8_quantize_rows(x)
+    assert q[0, 3] == 127 and s[0] == np.float32(1e-7) / np.float32(127.0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -30,6 +30,13 @@ PLANTS = {
     11: ["pin_i8s_mul_mat_add_special_case"],  # bias added before scaling
     12: ["pin_i8s_mul_mat_add_special_case"],  # ReLU dropped
     13: ["pin_i8s_mul_mat_add_special_case"],  # activation scale dropped
+    14: ["pin_i8s_add_scaled_pow2"],       # second input read with the first's scale
+    15: ["pin_i8s_rms_norm_closed_forms"],  # mean square without the scale
+    16: ["pin_i8s_rms_norm_closed_forms"],  # mean over ne0 - 1
+    17: ["pin_i8s_im2col_asym"],           # right pad used as the left pad
+    18: ["pin_i8s_depthwise_pow2"],        # kernel taps reversed (convolution)
+    19: ["pin_w8a8_mul_mat_pow2"],         # row scale dropped
+    20: ["pin_w8a8_weight_quant"],         # weight ties rounded away from zero
 }
 
 
