@@ -29,9 +29,10 @@
 //   R5 add_scaled: y = (float)qa*sa + (float)qb*sb (two products, one sum),
 //      then per-tensor requantization (R2).
 //   R6 rms_norm_scaled: rows of ne0 contiguous values x = q*s; mean square
-//      (double)sum(q^2) * ((double)s*(double)s) / ne0 in double; row factor
-//      r = (float)(1/sqrt(mean + eps)) in double; y = (x*r) (*gamma[i]) in
-//      float; then per-tensor requantization (R2). No weight when gamma is null.
+//      ((float)sum(q^2) * (s*s)) / ne0 and row factor r = 1 / sqrt(mean + eps),
+//      each an IEEE binary32 operation (the integer sum is exact); y = (x*r)
+//      (*gamma[i]); then per-tensor requantization (R2). No weight when gamma
+//      is null.
 //   R7 im2col_asym: input C x L (L contiguous), output OL x (C*KW) with
 //      dst[t][c*KW + k] = src[c][t*stride + k - pad_l] (0 outside [0, L)),
 //      OL = (L + pad_l + pad_r - KW) / stride + 1; the scale is carried.
@@ -436,8 +437,8 @@ ORC_API void orc_i8s_add_scaled(const uint8_t* a_i8s, const uint8_t* b_i8s, int6
 // ggml_rms_norm_scaled ([P1] "Five fused INT8 ops": RMSNorm straight from I8_S
 // to I8_S; [P3] "Encoder": RMSNorm epsilon 1e-5 everywhere). Reading R6. The
 // mean square of a row of dequantized values q*s is s^2 * sum(q^2) / ne0; the
-// integer sum is exact, and the rest is a fixed sequence of double operations,
-// so the row factor does not depend on a summation order.
+// integer sum is exact, and the rest is a fixed sequence of correctly rounded
+// binary32 operations, so the row factor does not depend on a summation order.
 // ---------------------------------------------------------------------------
 ORC_API void orc_i8s_rms_norm_scaled(const uint8_t* x_i8s, int64_t rows, int64_t ne0, float eps,
                                      const float* gamma, uint8_t* y_i8s, float* y_f32) {
@@ -449,14 +450,15 @@ ORC_API void orc_i8s_rms_norm_scaled(const uint8_t* x_i8s, int64_t rows, int64_t
         const int8_t* qr = q + r * ne0;
         int64_t ssq = 0;
         for (int64_t i = 0; i < ne0; ++i) ssq += (int64_t)qr[i] * qr[i];
+        const float ss = s * s;
 #if ORC_PLANT == 15
-        const double mean = (double)ssq / (double)ne0;
+        const float mean = (float)ssq / (float)ne0;
 #elif ORC_PLANT == 16
-        const double mean = (double)ssq * ((double)s * (double)s) / (double)(ne0 > 1 ? ne0 - 1 : 1);
+        const float mean = ((float)ssq * ss) / (float)(ne0 > 1 ? ne0 - 1 : 1);
 #else
-        const double mean = (double)ssq * ((double)s * (double)s) / (double)ne0;
+        const float mean = ((float)ssq * ss) / (float)ne0;
 #endif
-        const float rf = (float)(1.0 / sqrt(mean + (double)eps));
+        const float rf = 1.0f / sqrtf(mean + eps);
         for (int64_t i = 0; i < ne0; ++i) {
             const float x = (float)qr[i] * s;
             float v = x * rf;
