@@ -279,6 +279,98 @@ int i8s_requant(const float* y, int64_t n, void* dst_i8s, void* ws, size_t ws_by
                 i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * I8_S element-wise ops ([P1] "Five fused INT8 ops": ggml_add_scaled and
+ * ggml_rms_norm_scaled; "Two new types", the dup/cont note: a permuted copy
+ * carries the in-band scale). Each output is a self-describing I8_S tensor:
+ * where its scale depends on the values, the op requantizes per tensor as
+ * i8s_requant does (amax floored at 1e-5, scale = amax/127, round half away
+ * from zero, clamp to +-127). Two passes over the inputs: the first folds
+ * max|y|, the second recomputes y and quantizes it.
+ *
+ * i8s_add_scaled:      y = (float)a*a_scale + (float)b*b_scale (two IEEE
+ *                      products, one IEEE sum), n elements.
+ * i8s_rms_norm_scaled: rows x ne0 (ne0 contiguous), each row normalised:
+ *                      x = q*scale; mean = ((float)sum(q^2) * (scale*scale))
+ *                      / ne0; r = 1/sqrt(mean + eps), each a correctly
+ *                      rounded binary32 operation; y = (x*r) (* gamma[i]).
+ *                      eps >= 0: 1e-5 in the encoder ([P3] "Encoder"); with
+ *                      eps = 0 an all-zero row is undefined (0 * inf). gamma:
+ *                      device F32 [ne0] or NULL for none. ne0 <= 131072.
+ * i8s_transpose:       src a x b (row-major) -> dst b x a, scale copied
+ *                      (ggml_cont(ggml_permute(...))). No workspace.
+ *
+ * Inputs and outputs are device I8_S buffers of i8s_nbytes(n) bytes; an
+ * output must not overlap an input. add_scaled and rms_norm_scaled need
+ * 16-byte aligned buffers and a 256-byte aligned workspace of at least
+ * i8s_eltwise_workspace(rows) bytes (rows = 1 for add_scaled).
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, BAD_ARG (an
+ * output overlapping an input), CUDA.
+ * ------------------------------------------------------------------------- */
+size_t i8s_eltwise_workspace(int64_t rows);
+int i8s_add_scaled(const void* a_i8s, const void* b_i8s, int64_t n, void* y_i8s, void* ws,
+                   size_t ws_bytes, i2s_stream_t stream);
+int i8s_rms_norm_scaled(const void* x_i8s, int64_t rows, int64_t ne0, float eps, const float* gamma,
+                        void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream);
+int i8s_transpose(const void* src_i8s, int64_t a, int64_t b, void* dst_i8s, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Encoder convolution pieces on I8_S ([P1] "Five fused INT8 ops":
+ * ggml_im2col_asym, im2col with independent left/right padding so that a
+ * causal conv needs no pad node; "Tests": depthwise mul_mat_add; [P3]
+ * "Encoder": strided causal convs with left pad K - stride, right pad 0, and
+ * a depthwise conv in every block).
+ *
+ * Geometry: input C x L (L contiguous, one channel per row); kernel width KW,
+ * stride, left pad pad_l, right pad pad_r (zeros); output length
+ * OL = (L + pad_l + pad_r - KW) / stride + 1 (i8s_im2col_out_len; 0 if the
+ * padded input is shorter than KW).
+ *
+ * i8s_im2col_asym:  dst is OL x (C*KW), dst[t][c*KW + k] =
+ *                   src[c][t*stride + k - pad_l] (0 outside the input), with
+ *                   the input's scale. No workspace.
+ * i8s_depthwise_mul_mat_add: w_i8s is C x KW (one kernel row per channel);
+ *                   y[c][t] = (float)acc * (w_scale*x_scale) + bias[c], ReLU
+ *                   if relu != 0, acc = sum_k w[c][k] * x[c][t*stride + k -
+ *                   pad_l] in int32; y is C x OL, requantized per tensor.
+ *                   bias: device F32 [C] or NULL. Workspace as
+ *                   i8s_eltwise_workspace(1).
+ * Requirements: C, L, KW, stride >= 1; pad_l, pad_r >= 0; C*L, OL*C*KW and
+ * C*OL < 2^31; dst/y 16-byte aligned; no overlap of output and inputs.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, BAD_ARG (an
+ * output overlapping an input), CUDA.
+ * ------------------------------------------------------------------------- */
+int64_t i8s_im2col_out_len(int64_t L, int64_t KW, int64_t stride, int64_t pad_l, int64_t pad_r);
+int i8s_im2col_asym(const void* src_i8s, int64_t C, int64_t L, int64_t KW, int64_t stride, int64_t pad_l,
+                    int64_t pad_r, void* dst_i8s, i2s_stream_t stream);
+int i8s_depthwise_mul_mat_add(const void* w_i8s, int64_t KW, const void* x_i8s, int64_t C, int64_t L,
+                              int64_t stride, int64_t pad_l, int64_t pad_r, const float* bias, int relu,
+                              void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * W8A8 per-channel matmul ([P4] "Experiment - int8 W8A8 path", sections
+ * "Hypothesis" and "Implementation"): int8 weights with one scale per output
+ * channel, int8 activations with one scale per row, int32 accumulation, then
+ * d[m][n] = aScale[m] * bScale[n] * (float)C[m][n] (left to right).
+ *
+ * w8a8_quantize_weights: w is N x K F32 (device); per channel n: amax =
+ *   max(max_k |w|, 1e-9), bscale[n] = amax/127, wq = clamp(rint(w /
+ *   bscale[n]), -127, 127) (an IEEE division, ties to even), N x K int8.
+ * w8a8_mul_mat: x is M x K F32 (device); per row: amax = max(max_k |x|,
+ *   1e-9), aScale[m] = amax/127, q = clamp(round(x * (127/amax))) (half away
+ *   from zero); d is M x N F32. The exact int32 dot runs on the I8_S
+ *   tensor-core path (f16 operands, f32 chunk sums of at most 1024
+ *   positions, drained into int32).
+ * Requirements: K % 64 == 0, K <= 65536; M*K, N*K, M*N < 2^31; 16-byte
+ * aligned pointers; ws 256-byte aligned, at least w8a8_mul_mat_workspace.
+ * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
+ * ------------------------------------------------------------------------- */
+int w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale,
+                          i2s_stream_t stream);
+size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
+int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M,
+                 float* d, void* ws, size_t ws_bytes, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Device status. Kernels with bounded waits (the tensor-core pipelines) never
  * trap: when a wait runs out they record a code in the status word at the
  * start of the workspace and exit. Every i2s_mul_mat* call clears the word in

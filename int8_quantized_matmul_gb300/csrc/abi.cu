@@ -622,6 +622,8 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
     a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
     a.bias = bias;
+    a.row_scale = nullptr;
+    a.col_scale = nullptr;
     a.y = yf;
     a.amax_bits = amax;
     a.part = reinterpret_cast<int32_t*>(base + part_off);
@@ -659,6 +661,200 @@ int i8s_requant(const float* y, int64_t n, void* dst_i8s, void* ws, size_t ws_by
     r = cuda_status(launch_absmax(y, n, amax, stream));
     if (r) return r;
     return cuda_status(launch_requant(y, n, amax, static_cast<uint8_t*>(dst_i8s), stream));
+}
+
+// ---------------------------------------------------------------------------
+// I8_S element-wise ops, convolution pieces and W8A8. Workspace of the
+// element-wise ops: [header: status, amax][row factors, rows F32].
+// ---------------------------------------------------------------------------
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+size_t i8s_eltwise_workspace(int64_t rows) {
+    return rows < 1 ? 0 : kHeader + align_up((size_t)rows * 4);
+}
+
+int i8s_add_scaled(const void* a_i8s, const void* b_i8s, int64_t n, void* y_i8s, void* ws, size_t ws_bytes,
+                   i2s_stream_t stream) {
+    if (!a_i8s || !b_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
+    if (n < 1 || n >= ((int64_t)1 << 40)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(a_i8s) || !aligned16(b_i8s) || !aligned16(y_i8s) || !aligned256(ws)) return I2S_E_MISALIGNED;
+    const size_t nb = i8s_nbytes(n);
+    if (overlaps(y_i8s, nb, a_i8s, nb) || overlaps(y_i8s, nb, b_i8s, nb)) return I2S_E_BAD_ARG;
+    if (ws_bytes < i8s_eltwise_workspace(1)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    unsigned int* amax = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kAmaxOff);
+    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    if (r) return r;
+    return cuda_status(launch_add_scaled(static_cast<const uint8_t*>(a_i8s), static_cast<const uint8_t*>(b_i8s), n,
+                                         amax, static_cast<uint8_t*>(y_i8s), stream));
+}
+
+int i8s_rms_norm_scaled(const void* x_i8s, int64_t rows, int64_t ne0, float eps, const float* gamma, void* y_i8s,
+                        void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
+    if (rows < 1 || ne0 < 1 || ne0 > 131072 || rows * ne0 >= ((int64_t)1 << 40) || !(eps >= 0.0f))
+        return I2S_E_BAD_SHAPE;
+    if (!aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) || (gamma && ((uintptr_t)gamma & 3u)))
+        return I2S_E_MISALIGNED;
+    const size_t nb = i8s_nbytes(rows * ne0);
+    if (overlaps(y_i8s, nb, x_i8s, nb)) return I2S_E_BAD_ARG;
+    if (ws_bytes < i8s_eltwise_workspace(rows)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    if (r) return r;
+    return cuda_status(launch_rms_norm_scaled(static_cast<const uint8_t*>(x_i8s), rows, ne0, eps, gamma,
+                                              reinterpret_cast<float*>(base + kHeader), amax,
+                                              static_cast<uint8_t*>(y_i8s), stream));
+}
+
+int i8s_transpose(const void* src_i8s, int64_t a, int64_t b, void* dst_i8s, i2s_stream_t stream) {
+    if (!src_i8s || !dst_i8s) return I2S_E_NULL_PTR;
+    if (a < 1 || b < 1 || a * b >= ((int64_t)1 << 40) || ((a + 63) / 64) * ((b + 63) / 64) >= ((int64_t)1 << 31))
+        return I2S_E_BAD_SHAPE;
+    const size_t nb = i8s_nbytes(a * b);
+    if (overlaps(dst_i8s, nb, src_i8s, nb)) return I2S_E_BAD_ARG;
+    int r = check_device();
+    if (r) return r;
+    return cuda_status(launch_i8s_transpose(static_cast<const uint8_t*>(src_i8s), a, b,
+                                            static_cast<uint8_t*>(dst_i8s), stream));
+}
+
+int64_t i8s_im2col_out_len(int64_t L, int64_t KW, int64_t stride, int64_t pad_l, int64_t pad_r) {
+    if (L < 1 || KW < 1 || stride < 1 || pad_l < 0 || pad_r < 0) return 0;
+    const int64_t span = L + pad_l + pad_r - KW;
+    return span < 0 ? 0 : span / stride + 1;
+}
+
+static bool conv_shape_ok(int64_t C, int64_t L, int64_t KW, int64_t stride, int64_t pad_l, int64_t pad_r) {
+    if (C < 1 || L < 1 || KW < 1 || stride < 1 || pad_l < 0 || pad_r < 0) return false;
+    if (KW > 65536 || stride > 65536 || pad_l > 65536 || pad_r > 65536) return false;
+    const int64_t OL = i8s_im2col_out_len(L, KW, stride, pad_l, pad_r);
+    const int64_t lim = (int64_t)1 << 31;
+    return OL >= 1 && C * L < lim && OL * C * KW < lim && C * OL < lim && L + pad_l + pad_r < lim;
+}
+
+int i8s_im2col_asym(const void* src_i8s, int64_t C, int64_t L, int64_t KW, int64_t stride, int64_t pad_l,
+                    int64_t pad_r, void* dst_i8s, i2s_stream_t stream) {
+    if (!src_i8s || !dst_i8s) return I2S_E_NULL_PTR;
+    if (!conv_shape_ok(C, L, KW, stride, pad_l, pad_r)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(dst_i8s)) return I2S_E_MISALIGNED;
+    const int64_t OL = i8s_im2col_out_len(L, KW, stride, pad_l, pad_r);
+    if (overlaps(dst_i8s, i8s_nbytes(OL * C * KW), src_i8s, i8s_nbytes(C * L))) return I2S_E_BAD_ARG;
+    int r = check_device();
+    if (r) return r;
+    return cuda_status(launch_im2col_asym(static_cast<const uint8_t*>(src_i8s), C, L, (int)KW, (int)stride,
+                                          (int)pad_l, OL, static_cast<uint8_t*>(dst_i8s), stream));
+}
+
+int i8s_depthwise_mul_mat_add(const void* w_i8s, int64_t KW, const void* x_i8s, int64_t C, int64_t L,
+                              int64_t stride, int64_t pad_l, int64_t pad_r, const float* bias, int relu,
+                              void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!w_i8s || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
+    if (!conv_shape_ok(C, L, KW, stride, pad_l, pad_r)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(y_i8s) || !aligned256(ws) || (bias && ((uintptr_t)bias & 3u))) return I2S_E_MISALIGNED;
+    const int64_t OL = i8s_im2col_out_len(L, KW, stride, pad_l, pad_r);
+    const size_t ny = i8s_nbytes(C * OL);
+    if (overlaps(y_i8s, ny, x_i8s, i8s_nbytes(C * L)) || overlaps(y_i8s, ny, w_i8s, i8s_nbytes(C * KW)))
+        return I2S_E_BAD_ARG;
+    if (ws_bytes < i8s_eltwise_workspace(1)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    unsigned int* amax = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kAmaxOff);
+    r = cuda_status(cudaMemsetAsync(amax, 0, 4, stream));
+    if (r) return r;
+    return cuda_status(launch_depthwise(static_cast<const uint8_t*>(w_i8s), static_cast<const uint8_t*>(x_i8s), bias,
+                                        C, L, (int)KW, (int)stride, (int)pad_l, OL, relu ? 1 : 0, amax,
+                                        static_cast<uint8_t*>(y_i8s), stream));
+}
+
+int w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale, i2s_stream_t stream) {
+    if (!w || !wq || !bscale) return I2S_E_NULL_PTR;
+    if (N < 1 || K < 1 || N * K >= ((int64_t)1 << 40) || N >= ((int64_t)1 << 31)) return I2S_E_BAD_SHAPE;
+    if (((uintptr_t)w & 3u) || ((uintptr_t)bscale & 3u)) return I2S_E_MISALIGNED;
+    int r = check_device();
+    if (r) return r;
+    return cuda_status(launch_w8a8_weights(w, N, K, wq, bscale, stream));
+}
+
+// W8A8 workspace: [header: status, amax][activations int8, M x K][row scales,
+// M F32][then the I8_S GEMM's operands and split-tile areas: activations f16,
+// rows_pad x K; weights f16, N x K; slots; tickets; masks].
+static size_t w8a8_front(int64_t M, int64_t K) { return kHeader + align_up((size_t)M * K) + align_up((size_t)M * 4); }
+
+size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
+    const size_t i8 = i8s_mul_mat_workspace(M, N, K);
+    if (i8 == 0) return 0;
+    return w8a8_front(M, K) + (i8 - kHeader - align_up((size_t)M * (size_t)N * 4));
+}
+
+int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M, float* d,
+                 void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!wq || !bscale || !x || !d || !ws) return I2S_E_NULL_PTR;
+    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
+    if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
+        return I2S_E_BAD_SHAPE;
+    if (!aligned16(wq) || !aligned16(x) || !aligned16(d) || !aligned256(ws) || ((uintptr_t)bscale & 3u))
+        return I2S_E_MISALIGNED;
+    if (ws_bytes < w8a8_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+    int8_t* xq = reinterpret_cast<int8_t*>(base + kHeader);
+    float* ascale = reinterpret_cast<float*>(base + kHeader + align_up((size_t)M * K));
+    const int64_t rows_pad = i8s_rows_pad(M);
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    const size_t xf_off = w8a8_front(M, K);
+    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
+    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+    const size_t mask_off = tick_off + align_up(tiles * 4);
+    const size_t zero_bytes = mask_off + align_up(tiles * 8) - tick_off;
+    __half* xf = reinterpret_cast<__half*>(base + xf_off);
+    __half* wf = reinterpret_cast<__half*>(base + wf_off);
+    // per-row activation quantization (1e-9 floor), then the int8 rows and
+    // weights to f16 (the pre-pass also clears the status word and the
+    // split-tile tickets), then the tensor-core GEMM with the W8A8 epilogue
+    r = cuda_status(launch_w8a8_rows(x, M, K, xq, ascale, stream));
+    if (r) return r;
+    r = cuda_status(launch_i8s_to_f16(wq, (int)N, wf, xq, (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes,
+                                      status, amax, stream));
+    if (r) return r;
+    static thread_local I8sTcArgs a;
+    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
+    a.w = wq;
+    a.w_scale_ptr = bscale;   // read by the kernel's I8_S prologue; the W8A8 epilogue uses the arrays
+    a.x_scale_ptr = ascale;
+    a.bias = nullptr;
+    a.row_scale = ascale;
+    a.col_scale = bscale;
+    a.y = d;
+    a.amax_bits = amax;
+    a.part = reinterpret_cast<int32_t*>(base + part_off);
+    a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
+    a.slot_masks = reinterpret_cast<unsigned long long*>(base + mask_off);
+    a.status = status;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.relu = 0;
+    a.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
+    a.n_at = (int)(rows_pad / kI8sTileM);
+    a.chunks = (int)i8s_chunks(K);
+    a.total_units = (int)(tiles / 2) * a.chunks;
+    int pairs = i8s_gemm_tc_max_pairs();
+    if (pairs > a.total_units) pairs = a.total_units;
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
 }
 
 int i2s_read_status(void* ws, i2s_stream_t stream) {

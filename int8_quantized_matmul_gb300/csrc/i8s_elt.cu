@@ -1,0 +1,422 @@
+// I8_S element-wise and convolution pieces, and the W8A8 row quantizer
+// ("ggml: additive INT8/ternary types, fused CPU ops, and kernels for VibeASR
+// (1/2)", sections "Two new types", "Five fused INT8 ops" and "Tests";
+// "VibeASR in audio.cpp", section "Encoder"; "Experiment - int8 W8A8 path",
+// section "Implementation").
+//
+//   add_scaled       y = (float)qa*sa + (float)qb*sb, requantized per tensor
+//   rms_norm_scaled  per row of ne0 values x = q*s: r = 1/sqrt(mean(x^2) + eps)
+//                    with mean(x^2) = ((float)sum(q^2) * (s*s)) / ne0, each a
+//                    correctly rounded binary32 operation; y = x*r (*gamma[i]),
+//                    requantized per tensor
+//   transpose        a x b -> b x a; the in-band scale travels with the values
+//   im2col_asym      C x L -> OL x (C*KW), independent left/right padding
+//   depthwise        per-channel causal conv, R4's epilogue with bias[c],
+//                    requantized per tensor
+//   w8a8 rows        per-row int8 activations, amax floored at 1e-9
+//   w8a8 weights     per-channel int8 weights: rint(w / (amax/127)), amax
+//                    floored at 1e-9
+//
+// Every op here moves bytes: each is bound by HBM bandwidth. An op whose output
+// scale depends on the whole output runs two passes over its inputs: the first
+// folds max|y| into one word (atomicMax on the float bits, valid because
+// |y| >= 0), the second recomputes y and quantizes it. Recomputing costs fewer
+// bytes than writing and re-reading an F32 intermediate.
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace i2s {
+
+namespace {
+
+constexpr int kEltThreads = 256;
+
+__device__ __forceinline__ int64_t pad32(int64_t n) { return (n + 31) / 32 * 32; }
+
+__device__ __forceinline__ float i8s_scale_of(const uint8_t* t, int64_t n) {
+    return *reinterpret_cast<const float*>(t + pad32(n));
+}
+
+// Block-wide max folded into *amax_bits.
+__device__ __forceinline__ void fold_max(float mx, unsigned int* amax_bits) {
+    __shared__ float s_max[kEltThreads / 32];
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < kEltThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+        atomicMax(amax_bits, __float_as_uint(fmaxf(mx, s_max[0])));
+    }
+}
+
+// The I8_S trailer of an n-element output: zero padding up to the next
+// multiple of 32, the F32 scale, 28 zero bytes. Called by one block.
+__device__ __forceinline__ void write_trailer(uint8_t* dst, int64_t n, float scale) {
+    const int64_t padded = pad32(n);
+    for (int64_t i = n + threadIdx.x; i < padded + 32; i += blockDim.x) {
+        uint8_t b = 0;
+        if (i >= padded && i < padded + 4) b = (uint8_t)(__float_as_uint(scale) >> (8 * (i - padded)));
+        dst[i] = b;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
+           ((uint32_t)(d & 0xff) << 24);
+}
+
+__device__ __forceinline__ int8_t byte_of(uint32_t w, int i) { return (int8_t)(w >> (8 * i)); }
+
+// ---------------------------------------------------------------- add_scaled
+
+__device__ __forceinline__ float add_one(int8_t qa, int8_t qb, float sa, float sb) {
+    return __fadd_rn(__fmul_rn((float)qa, sa), __fmul_rn((float)qb, sb));
+}
+
+// Pass 1: max |y| over the tensor. 16 bytes of each input per thread and step.
+__global__ void __launch_bounds__(kEltThreads) k_add_amax(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b,
+                                                          int64_t n, unsigned int* amax_bits) {
+    const float sa = i8s_scale_of(a, n), sb = i8s_scale_of(b, n);
+    const int64_t n16 = n / 16, stride = (int64_t)gridDim.x * blockDim.x;
+    float mx = 0.0f;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 va = ldg_stream(a + 16 * i), vb = ldg_stream(b + 16 * i);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb)));
+    }
+    if (blockIdx.x == 0)
+        for (int64_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x)
+            mx = fmaxf(mx, fabsf(add_one((int8_t)a[i], (int8_t)b[i], sa, sb)));
+    fold_max(mx, amax_bits);
+}
+
+// Pass 2: recompute y and quantize it with the folded amax.
+__global__ void __launch_bounds__(kEltThreads) k_add_quant(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b,
+                                                           int64_t n, const unsigned int* __restrict__ amax_bits,
+                                                           uint8_t* __restrict__ dst) {
+    const float sa = i8s_scale_of(a, n), sb = i8s_scale_of(b, n);
+    float scale, inv;
+    quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int64_t n16 = n / 16, stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 va = ldg_stream(a + 16 * i), vb = ldg_stream(b + 16 * i);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            int q[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) q[e] = quantize_one(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb), inv);
+            o[w] = pack4(q[0], q[1], q[2], q[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x)
+            dst[i] = (uint8_t)(quantize_one(add_one((int8_t)a[i], (int8_t)b[i], sa, sb), inv) & 0xff);
+        write_trailer(dst, n, scale);
+    }
+}
+
+// ------------------------------------------------------------ rms_norm_scaled
+// One warp per row (grid-stride over rows), lanes striding over the row.
+
+__device__ __forceinline__ float rms_factor(int ssq, int64_t ne0, float s, float eps) {
+    const float mean = __fdiv_rn(__fmul_rn((float)ssq, __fmul_rn(s, s)), (float)ne0);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+__device__ __forceinline__ float rms_one(int8_t q, float s, float r, const float* gamma, int64_t i) {
+    float v = __fmul_rn(__fmul_rn((float)q, s), r);
+    if (gamma) v = __fmul_rn(v, gamma[i]);
+    return v;
+}
+
+// Pass 1: the row factors (kept in the workspace) and max |y|.
+__global__ void __launch_bounds__(kEltThreads) k_rms_rows(const uint8_t* __restrict__ x, int64_t rows, int64_t ne0,
+                                                          float eps, const float* __restrict__ gamma,
+                                                          float* __restrict__ rfac, unsigned int* amax_bits) {
+    const int64_t n = rows * ne0;
+    const float s = i8s_scale_of(x, n);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int8_t* q = reinterpret_cast<const int8_t*>(x);
+    float mx = 0.0f;
+    for (int64_t row = warp0; row < rows; row += warps) {
+        const int8_t* qr = q + row * ne0;
+        int ssq = 0, qmax = 0;   // ne0 * 127^2 < 2^31 for ne0 < 133,000 (checked by the host)
+        if ((ne0 & 3) == 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(qr);
+            for (int64_t w = lane; w < ne0 / 4; w += 32) {
+                const uint32_t v = src[w];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int b = byte_of(v, e);
+                    ssq += b * b;
+                    qmax = max(qmax, abs(b));
+                }
+            }
+        } else {
+            for (int64_t i = lane; i < ne0; i += 32) {
+                const int v = qr[i];
+                ssq += v * v;
+                qmax = max(qmax, abs(v));
+            }
+        }
+        ssq = warp_sum(ssq);
+        const float r = rms_factor(ssq, ne0, s, eps);
+        if (lane == 0) rfac[row] = r;
+        if (gamma) {   // the weight varies along the row: every element
+            for (int64_t i = lane; i < ne0; i += 32) mx = fmaxf(mx, fabsf(rms_one(qr[i], s, r, gamma, i)));
+        } else {       // x*r is monotonic in |q|: the row's largest |q| gives its max
+            qmax = (int)warp_max((float)qmax);
+            mx = fmaxf(mx, fabsf(rms_one((int8_t)qmax, s, r, nullptr, 0)));
+        }
+    }
+    fold_max(mx, amax_bits);
+}
+
+// Pass 2: y = x*r (*gamma), quantized with the folded amax; one warp per row
+// again, four values per lane and step when rows are whole 32-bit words.
+__global__ void __launch_bounds__(kEltThreads) k_rms_quant(const uint8_t* __restrict__ x, int64_t rows, int64_t ne0,
+                                                           const float* __restrict__ gamma,
+                                                           const float* __restrict__ rfac,
+                                                           const unsigned int* __restrict__ amax_bits,
+                                                           uint8_t* __restrict__ dst) {
+    const int64_t n = rows * ne0;
+    const float s = i8s_scale_of(x, n);
+    float scale, inv;
+    quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int8_t* q = reinterpret_cast<const int8_t*>(x);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const bool words = (ne0 & 3) == 0;
+    for (int64_t row = warp0; row < rows; row += warps) {
+        const float r = rfac[row];
+        if (words) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(q + row * ne0);
+            uint32_t* out = reinterpret_cast<uint32_t*>(dst + row * ne0);
+            for (int64_t w = lane; w < ne0 / 4; w += 32) {
+                const uint32_t v = src[w];
+                int o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = quantize_one(rms_one(byte_of(v, e), s, r, gamma, 4 * w + e), inv);
+                out[w] = pack4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            for (int64_t i = lane; i < ne0; i += 32)
+                dst[row * ne0 + i] = (uint8_t)(quantize_one(rms_one(q[row * ne0 + i], s, r, gamma, i), inv) & 0xff);
+        }
+    }
+    if (blockIdx.x == 0) write_trailer(dst, n, scale);
+}
+
+// ------------------------------------------------------------------ transpose
+// 64 x 64-byte tiles through shared memory: a warp reads 64 contiguous bytes
+// of each of eight source rows and writes 64 contiguous bytes of each of eight
+// destination rows.
+
+constexpr int kTT = 64;
+
+__global__ void __launch_bounds__(kEltThreads) k_transpose(const uint8_t* __restrict__ src, int64_t a, int64_t b,
+                                                           uint8_t* __restrict__ dst, int64_t tiles_b) {
+    __shared__ uint8_t tile[kTT][kTT + 4];
+    const int64_t ti = blockIdx.x / tiles_b, tj = blockIdx.x - ti * tiles_b;
+    const int64_t i0 = ti * kTT, j0 = tj * kTT;
+    const int c = threadIdx.x & 63, r0 = threadIdx.x >> 6;   // 4 rows per pass
+    for (int r = r0; r < kTT; r += kEltThreads / kTT) {
+        const int64_t i = i0 + r, j = j0 + c;
+        tile[r][c] = (i < a && j < b) ? src[i * b + j] : (uint8_t)0;
+    }
+    __syncthreads();
+    for (int r = r0; r < kTT; r += kEltThreads / kTT) {
+        const int64_t j = j0 + r, i = i0 + c;   // destination row j, column i
+        if (j < b && i < a) dst[j * a + i] = tile[c][r];
+    }
+    if (blockIdx.x == 0) {
+        __syncthreads();
+        write_trailer(dst, a * b, i8s_scale_of(src, a * b));
+    }
+}
+
+// ---------------------------------------------------------------- im2col_asym
+
+// Output and input sizes below 2^31 (checked by the host): 32-bit index math.
+__global__ void __launch_bounds__(kEltThreads) k_im2col(const uint8_t* __restrict__ src, int C, int L, int KW,
+                                                        int stride, int pad_l, int OL, uint8_t* __restrict__ dst) {
+    const int n = OL * C * KW;
+    const int8_t* x = reinterpret_cast<const int8_t*>(src);
+    auto value = [&](int f) -> int {
+        const int row = f / KW, k = f - row * KW;   // row = t*C + c
+        const int t = row / C, c = row - t * C;
+        const int pos = t * stride + k - pad_l;
+        return (pos >= 0 && pos < L) ? (int)x[c * L + pos] : 0;
+    };
+    const int n4 = n / 4, step = gridDim.x * blockDim.x;
+    for (int i4 = blockIdx.x * blockDim.x + threadIdx.x; i4 < n4; i4 += step)
+        *reinterpret_cast<uint32_t*>(dst + 4 * i4) =
+            pack4(value(4 * i4), value(4 * i4 + 1), value(4 * i4 + 2), value(4 * i4 + 3));
+    if (blockIdx.x == 0) {
+        for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(value(i) & 0xff);
+        write_trailer(dst, n, i8s_scale_of(src, (int64_t)C * L));
+    }
+}
+
+// ------------------------------------------------------------------ depthwise
+
+// Sizes below 2^31 (checked by the host): 32-bit index math.
+struct DwArgs {
+    const uint8_t* w;   // I8_S C x KW
+    const uint8_t* x;   // I8_S C x L
+    const float* bias;  // C or null
+    int C, L, OL, KW, stride, pad_l, relu;
+};
+
+__device__ __forceinline__ float dw_one(const DwArgs& d, float sc, int f) {
+    const int c = f / d.OL, t = f - c * d.OL;
+    const int8_t* w = reinterpret_cast<const int8_t*>(d.w) + (int64_t)c * d.KW;
+    const int8_t* x = reinterpret_cast<const int8_t*>(d.x) + (int64_t)c * d.L;
+    int acc = 0;
+    const int p0 = t * d.stride - d.pad_l;
+    for (int k = 0; k < d.KW; ++k) {
+        const int pos = p0 + k;
+        if (pos >= 0 && pos < d.L) acc += (int)w[k] * (int)x[pos];
+    }
+    float v = __fmul_rn(__int2float_rn(acc), sc);
+    if (d.bias) v = __fadd_rn(v, d.bias[c]);
+    if (d.relu) v = v > 0.0f ? v : 0.0f;
+    return v;
+}
+
+__global__ void __launch_bounds__(kEltThreads) k_dw_amax(const DwArgs d, unsigned int* amax_bits) {
+    const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
+    const int n = d.C * d.OL, step = gridDim.x * blockDim.x;
+    float mx = 0.0f;
+    for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < n; f += step) mx = fmaxf(mx, fabsf(dw_one(d, sc, f)));
+    fold_max(mx, amax_bits);
+}
+
+__global__ void __launch_bounds__(kEltThreads) k_dw_quant(const DwArgs d, const unsigned int* __restrict__ amax_bits,
+                                                          uint8_t* __restrict__ dst) {
+    const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
+    float scale, inv;
+    quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int n = d.C * d.OL, n4 = n / 4, step = gridDim.x * blockDim.x;
+    for (int i4 = blockIdx.x * blockDim.x + threadIdx.x; i4 < n4; i4 += step)
+        *reinterpret_cast<uint32_t*>(dst + 4 * i4) =
+            pack4(quantize_one(dw_one(d, sc, 4 * i4), inv), quantize_one(dw_one(d, sc, 4 * i4 + 1), inv),
+                  quantize_one(dw_one(d, sc, 4 * i4 + 2), inv), quantize_one(dw_one(d, sc, 4 * i4 + 3), inv));
+    if (blockIdx.x == 0) {
+        for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(quantize_one(dw_one(d, sc, i), inv) & 0xff);
+        write_trailer(dst, n, scale);
+    }
+}
+
+// ------------------------------------------------------------ W8A8 row quant
+// One CTA per activation row: the row's absmax (floored at 1e-9), then
+// q = clamp(round(x * inv)) with inv = 127/amax and the stored scale amax/127.
+
+__global__ void __launch_bounds__(kEltThreads) k_w8a8_rows(const float* __restrict__ x, int64_t K,
+                                                           int8_t* __restrict__ q, float* __restrict__ ascale) {
+    __shared__ float s_max[kEltThreads / 32];
+    const int64_t m = blockIdx.x;
+    const float* xr = x + m * K;
+    float mx = 0.0f;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = s_max[0];
+    for (int i = 1; i < kEltThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+    mx = fmaxf(mx, 1e-9f);
+    const float inv = __fdiv_rn(127.0f, mx);
+    if (threadIdx.x == 0) ascale[m] = __fdiv_rn(mx, 127.0f);
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) q[m * K + k] = (int8_t)quantize_one(xr[k], inv);
+}
+
+// W8A8 per-channel weights, one CTA per output channel: amax floored at 1e-9,
+// bscale = amax/127, q = clamp(rint(w / bscale)) (division, ties to even).
+__global__ void __launch_bounds__(kEltThreads) k_w8a8_weights(const float* __restrict__ w, int64_t K,
+                                                              int8_t* __restrict__ wq, float* __restrict__ bscale) {
+    __shared__ float s_max[kEltThreads / 32];
+    const int64_t n = blockIdx.x;
+    const float* wr = w + n * K;
+    float mx = 0.0f;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(wr[k]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = s_max[0];
+    for (int i = 1; i < kEltThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+    mx = fmaxf(mx, 1e-9f);
+    const float sc = __fdiv_rn(mx, 127.0f);
+    if (threadIdx.x == 0) bscale[n] = sc;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
+        const float r = fminf(fmaxf(rintf(__fdiv_rn(wr[k], sc)), -127.0f), 127.0f);
+        wq[n * K + k] = (int8_t)(int)r;
+    }
+}
+
+int elt_grid(int64_t work) {
+    const int64_t want = (work + kEltThreads - 1) / kEltThreads;
+    const int cap = device_sm_count() * 8;
+    return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_add_scaled(const uint8_t* a, const uint8_t* b, int64_t n, unsigned int* amax_bits, uint8_t* dst,
+                              cudaStream_t s) {
+    const int grid = elt_grid(n / 16 + 1);
+    k_add_amax<<<grid, kEltThreads, 0, s>>>(a, b, n, amax_bits);
+    k_add_quant<<<grid, kEltThreads, 0, s>>>(a, b, n, amax_bits, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, float eps, const float* gamma,
+                                   float* rfac, unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
+    k_rms_rows<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, eps, gamma, rfac, amax_bits);
+    k_rms_quant<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, gamma, rfac, amax_bits, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s) {
+    const int64_t ta = (a + kTT - 1) / kTT, tb = (b + kTT - 1) / kTT;
+    k_transpose<<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW, int stride, int pad_l, int64_t OL,
+                               uint8_t* dst, cudaStream_t s) {
+    k_im2col<<<elt_grid(OL * C * KW / 4 + 1), kEltThreads, 0, s>>>(src, (int)C, (int)L, KW, stride, pad_l, (int)OL,
+                                                                   dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bias, int64_t C, int64_t L, int KW,
+                             int stride, int pad_l, int64_t OL, int relu, unsigned int* amax_bits, uint8_t* dst,
+                             cudaStream_t s) {
+    const DwArgs d{w, x, bias, (int)C, (int)L, (int)OL, KW, stride, pad_l, relu};
+    const int grid = elt_grid(C * OL / 4 + 1);
+    k_dw_amax<<<grid, kEltThreads, 0, s>>>(d, amax_bits);
+    k_dw_quant<<<grid, kEltThreads, 0, s>>>(d, amax_bits, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale, cudaStream_t s) {
+    k_w8a8_rows<<<(unsigned)M, kEltThreads, 0, s>>>(x, K, q, ascale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w8a8_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale, cudaStream_t s) {
+    k_w8a8_weights<<<(unsigned)N, kEltThreads, 0, s>>>(w, K, wq, bscale);
+    return cudaGetLastError();
+}
+
+}  // namespace i2s

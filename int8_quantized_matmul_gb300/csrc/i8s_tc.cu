@@ -300,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
         float* const yb = a.y;
         const int M = a.M, N = a.N;
         const bool has_bias = a.bias != nullptr, relu = a.relu != 0;
+        const bool w8a8 = a.col_scale != nullptr;   // per-row / per-channel scales, no bias or ReLU
         float local_max = 0.0f;
         bool ok = true;
         for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
@@ -373,6 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             }
             if (write) {
                 const float bn = (has_bias && n < N) ? a.bias[n] : 0.0f;
+                const float bs_n = (w8a8 && n < N) ? a.col_scale[n] : 0.0f;
 #pragma unroll 1
                 for (int h = 0; h < kESlices8; ++h) {
                     uint32_t s[16];
@@ -387,7 +389,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                     // all 16 values first (no per-element branch, so the
                     // conversions and products overlap), then the stores
                     float v[16];
-                    if (has_bias) {
+                    if (w8a8) {
+                        // per-row activation and per-channel weight scales:
+                        // d = (as[m] * bs[n]) * (float)acc
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float as = a.row_scale[min(m0 + 16 * h + j, M - 1)];
+                            v[j] = __fmul_rn(__fmul_rn(as, bs_n), __int2float_rn((int)s[j]));
+                        }
+                    } else if (has_bias) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(__fmul_rn(__int2float_rn((int)s[j]), sc), bn);
                     } else {

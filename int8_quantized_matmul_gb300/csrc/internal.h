@@ -166,6 +166,8 @@ struct I8sTcArgs {
     const float* bias;         // N or null
     float* y;                  // M x N F32
     unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass)
+    const float* row_scale;    // W8A8 only (col_scale set): per-row activation scales, M
+    const float* col_scale;    // W8A8 only: per-channel weight scales, N; null for I8_S
     int32_t* part;             // split tiles: half-tiles x chunks slots of kI8sTileM x kI8sTileN int32 sums
     uint32_t* tickets;         // half-tile chunk counters (cleared by the pre-pass)
     unsigned long long* slot_masks;   // half-tile masks of the slots written (cleared by the pre-pass)
@@ -180,6 +182,20 @@ cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s);
 int i8s_gemm_tc_max_pairs();   // CTA pairs of the I8_S GEMM that fit on the device at once
 
 cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cudaStream_t s);
+
+// I8_S element-wise ops, convolution pieces and the W8A8 quantizers (i8s_elt.cu).
+cudaError_t launch_add_scaled(const uint8_t* a, const uint8_t* b, int64_t n, unsigned int* amax_bits, uint8_t* dst,
+                              cudaStream_t s);
+cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, float eps, const float* gamma,
+                                   float* rfac, unsigned int* amax_bits, uint8_t* dst, cudaStream_t s);
+cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s);
+cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW, int stride, int pad_l, int64_t OL,
+                               uint8_t* dst, cudaStream_t s);
+cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bias, int64_t C, int64_t L, int KW,
+                             int stride, int pad_l, int64_t OL, int relu, unsigned int* amax_bits, uint8_t* dst,
+                             cudaStream_t s);
+cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale, cudaStream_t s);
+cudaError_t launch_w8a8_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale, cudaStream_t s);
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst,
                            cudaStream_t s);
 

@@ -68,6 +68,16 @@ _SIGS = {
     "i8s_requant_workspace": (_sz, [_i64]),
     "i8s_requant": (_int, [_p, _i64, _p, _p, _sz, _p]),
     "i2s_read_status": (_int, [_p, _p]),
+    "i8s_eltwise_workspace": (_sz, [_i64]),
+    "i8s_add_scaled": (_int, [_p, _p, _i64, _p, _p, _sz, _p]),
+    "i8s_rms_norm_scaled": (_int, [_p, _i64, _i64, _f32, _p, _p, _p, _sz, _p]),
+    "i8s_transpose": (_int, [_p, _i64, _i64, _p, _p]),
+    "i8s_im2col_out_len": (_i64, [_i64, _i64, _i64, _i64, _i64]),
+    "i8s_im2col_asym": (_int, [_p, _i64, _i64, _i64, _i64, _i64, _i64, _p, _p]),
+    "i8s_depthwise_mul_mat_add": (_int, [_p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _p, _int, _p, _p, _sz, _p]),
+    "w8a8_quantize_weights": (_int, [_p, _i64, _i64, _p, _p, _p]),
+    "w8a8_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
+    "w8a8_mul_mat": (_int, [_p, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_L, _name)
@@ -282,6 +292,100 @@ def i8s_requant(y, dst=None, ws=None):
         ws = _ws(_L.i8s_requant_workspace(n), y.device)
     _check("i8s_requant", _L.i8s_requant(_dptr(y), n, _dptr(dst), _dptr(ws), ws.numel(), _stream()))
     return dst
+
+
+def i8s_eltwise_workspace(rows: int = 1) -> int:
+    return int(_L.i8s_eltwise_workspace(rows))
+
+
+def _u8(n: int, device):
+    return _torch().empty(n, dtype=_torch().uint8, device=device)
+
+
+def i8s_add_scaled(a, b, n: int, y=None, ws=None):
+    """I8_S y = requant(a*a_scale + b*b_scale) over n elements."""
+    if y is None:
+        y = _u8(i8s_nbytes(n), a.device)
+    if ws is None:
+        ws = _ws(i8s_eltwise_workspace(1), a.device)
+    _check("i8s_add_scaled", _L.i8s_add_scaled(_dptr(a), _dptr(b), n, _dptr(y), _dptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def i8s_rms_norm_scaled(x, rows: int, ne0: int, eps: float = 1e-5, gamma=None, y=None, ws=None):
+    """I8_S y = requant(RMSNorm of each of `rows` rows of ne0 values (* gamma))."""
+    if y is None:
+        y = _u8(i8s_nbytes(rows * ne0), x.device)
+    if ws is None:
+        ws = _ws(i8s_eltwise_workspace(rows), x.device)
+    _check("i8s_rms_norm_scaled", _L.i8s_rms_norm_scaled(_dptr(x), rows, ne0, float(eps), _dptr(gamma), _dptr(y),
+                                                         _dptr(ws), ws.numel(), _stream()))
+    return y
+
+
+def i8s_transpose(src, a: int, b: int, dst=None):
+    """I8_S a x b -> b x a, the scale carried."""
+    if dst is None:
+        dst = _u8(i8s_nbytes(a * b), src.device)
+    _check("i8s_transpose", _L.i8s_transpose(_dptr(src), a, b, _dptr(dst), _stream()))
+    return dst
+
+
+def i8s_im2col_out_len(L: int, KW: int, stride: int, pad_l: int, pad_r: int) -> int:
+    return int(_L.i8s_im2col_out_len(L, KW, stride, pad_l, pad_r))
+
+
+def i8s_im2col_asym(src, C: int, L: int, KW: int, stride: int, pad_l: int, pad_r: int, dst=None):
+    """I8_S C x L -> OL x (C*KW) windows with independent left/right zero padding."""
+    OL = i8s_im2col_out_len(L, KW, stride, pad_l, pad_r)
+    if dst is None:
+        dst = _u8(i8s_nbytes(OL * C * KW), src.device)
+    _check("i8s_im2col_asym", _L.i8s_im2col_asym(_dptr(src), C, L, KW, stride, pad_l, pad_r, _dptr(dst), _stream()))
+    return dst, OL
+
+
+def i8s_depthwise_mul_mat_add(w, KW: int, x, C: int, L: int, stride: int, pad_l: int, pad_r: int, bias=None,
+                              relu: bool = False, y=None, ws=None):
+    """I8_S per-channel conv: y (C x OL) = requant(conv(x, w) * (w_scale*x_scale) + bias, ReLU optional)."""
+    OL = i8s_im2col_out_len(L, KW, stride, pad_l, pad_r)
+    if y is None:
+        y = _u8(i8s_nbytes(C * OL), x.device)
+    if ws is None:
+        ws = _ws(i8s_eltwise_workspace(1), x.device)
+    _check("i8s_depthwise_mul_mat_add",
+           _L.i8s_depthwise_mul_mat_add(_dptr(w), KW, _dptr(x), C, L, stride, pad_l, pad_r, _dptr(bias),
+                                        1 if relu else 0, _dptr(y), _dptr(ws), ws.numel(), _stream()))
+    return y, OL
+
+
+def w8a8_quantize_weights(w, wq=None, bscale=None):
+    """Per-channel int8 weights of an N x K F32 tensor: (wq N x K int8, bscale N F32)."""
+    torch = _torch()
+    N, K = w.shape
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    if bscale is None:
+        bscale = torch.empty(N, dtype=torch.float32, device=w.device)
+    _check("w8a8_quantize_weights", _L.w8a8_quantize_weights(_dptr(w), N, K, _dptr(wq), _dptr(bscale), _stream()))
+    return wq, bscale
+
+
+def w8a8_mul_mat_workspace(M: int, N: int, K: int) -> int:
+    return int(_L.w8a8_mul_mat_workspace(M, N, K))
+
+
+def w8a8_mul_mat(wq, bscale, x, d=None, ws=None):
+    """d (M x N F32) = aScale[m] * bScale[n] * (int32 dot of the per-row int8 activations and wq)."""
+    torch = _torch()
+    N, K = wq.shape
+    M = x.shape[0]
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _ws(w8a8_mul_mat_workspace(M, N, K), x.device)
+    _check("w8a8_mul_mat", _L.w8a8_mul_mat(_dptr(wq), _dptr(bscale), N, K, _dptr(x), M, _dptr(d), _dptr(ws),
+                                           ws.numel(), _stream()))
+    return d, ws
 
 
 def read_status(ws) -> int:
