@@ -308,6 +308,105 @@ def run_encoder_fc(torch, i2s, device, peaks, steps=10):
                          "frac": tops / peaks["bf16_tflops"]}}
 
 
+def _timed_median(torch, fn, steps, flush):
+    """Median CUDA-event time (ms) of fn() over `steps` calls, each after an L2
+    flush (a write larger than L2) outside the timed region."""
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_encoder_eltwise(torch, i2s, device, peaks, steps=10):
+    """The I8_S element-wise ops and conv pieces on the encoder's stage-0
+    activations for two minutes of 24 kHz audio (32 channels x 2.88 M samples,
+    92 MB of int8 per tensor). Bytes are what each op's launches must move: a
+    per-tensor requantization needs two passes over its inputs (max|y| first),
+    so add_scaled moves 5n, rms_norm 3n, depthwise 2 reads and 1 write, im2col
+    and transpose one read and one write."""
+    C, L = 32, 2_880_000
+    n = C * L
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def i8s(seed):
+        q = synth.int8_normal_device(n, seed, device)
+        buf = torch.zeros(i2s.i8s_nbytes(n), dtype=torch.uint8, device=device)
+        buf[:n] = q.view(torch.uint8)
+        buf[i2s.i8s_scale_offset(n):i2s.i8s_scale_offset(n) + 4] = torch.tensor(
+            list(np.frombuffer(np.float32(0.02).tobytes(), np.uint8)), dtype=torch.uint8, device=device)
+        return buf
+    a, b = i8s(41), i8s(42)
+    y = torch.empty(i2s.i8s_nbytes(n), dtype=torch.uint8, device=device)
+    ws = torch.empty(i2s.i8s_eltwise_workspace(L), dtype=torch.uint8, device=device)
+    KWd = 7
+    wd = torch.zeros(i2s.i8s_nbytes(C * KWd), dtype=torch.uint8, device=device)
+    wd[:C * KWd] = synth.int8_normal_device(C * KWd, 43, device).view(torch.uint8)
+    wd[i2s.i8s_scale_offset(C * KWd):i2s.i8s_scale_offset(C * KWd) + 4] = torch.tensor(
+        list(np.frombuffer(np.float32(0.01).tobytes(), np.uint8)), dtype=torch.uint8, device=device)
+    bias = synth.normal_f32_device(C, 44, device, std=0.1)
+    KWc, sc = 4, 2
+    OLc = i2s.i8s_im2col_out_len(L, KWc, sc, KWc - sc, 0)
+    cols = torch.empty(i2s.i8s_nbytes(OLc * C * KWc), dtype=torch.uint8, device=device)
+    ops = {
+        "add_scaled": (lambda: i2s.i8s_add_scaled(a, b, n, y=y, ws=ws), 5 * n),
+        "rms_norm_scaled (32 channels per row)": (lambda: i2s.i8s_rms_norm_scaled(a, L, C, 1e-5, y=y, ws=ws),
+                                                  3 * n + 8 * L),
+        "transpose 32 x 2.88M": (lambda: i2s.i8s_transpose(a, C, L, dst=y), 2 * n),
+        "im2col_asym K=4 stride 2 causal": (lambda: i2s.i8s_im2col_asym(a, C, L, KWc, sc, KWc - sc, 0, dst=cols),
+                                            n + OLc * C * KWc),
+        "depthwise K=7 causal (+bias)": (lambda: i2s.i8s_depthwise_mul_mat_add(wd, KWd, a, C, L, 1, KWd - 1, 0,
+                                                                               bias=bias, y=y, ws=ws), 3 * n),
+    }
+    out = {}
+    for name, (fn, nbytes) in ops.items():
+        ms = _timed_median(torch, fn, steps, flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": ms * 1e3, "bytes": nbytes, "GB/s": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+    return {"workload": "I8_S encoder stage-0 activations, 32 channels x 2.88M samples (2 min of 24 kHz audio)",
+            "metric": "HBM GB/s per op (bytes each op's launches must move / CUDA-event time, L2 flushed)",
+            "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s"}, "ops": out}
+
+
+def run_w8a8_prefill(torch, i2s, device, peaks, steps=10):
+    """W8A8 per-channel matmul (the experiment page's scheme) over one
+    Qwen3-1.7B decoder layer's projections at M = 512 (pp512): per call the
+    per-row activation quantization, the f16 operand pre-pass and the
+    tensor-core GEMM with the aScale*bScale epilogue."""
+    M = 512
+    shapes = [("q", 2048, 2048), ("k", 1024, 2048), ("v", 1024, 2048), ("o", 2048, 2048),
+              ("gate", 6144, 2048), ("up", 6144, 2048), ("down", 2048, 6144)]
+    calls = []
+    for i, (name, N, K) in enumerate(shapes):
+        w = synth.normal_f32_device(N * K, 50 + i, device, std=0.02).view(N, K)
+        wq, bs = i2s.w8a8_quantize_weights(w)
+        x = synth.normal_f32_device(M * K, 60 + i, device, outlier_p=0.01).view(M, K)
+        d = torch.empty((M, N), dtype=torch.float32, device=device)
+        ws = torch.empty(i2s.w8a8_mul_mat_workspace(M, N, K), dtype=torch.uint8, device=device)
+        calls.append((wq, bs, x, d, ws, 2 * M * N * K))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        for wq, bs, x, d, ws, _ in calls:
+            i2s.w8a8_mul_mat(wq, bs, x, d=d, ws=ws)
+    ms = _timed_median(torch, step, steps, flush)
+    ops = sum(c[5] for c in calls)
+    tops = ops / (ms * 1e-3) / 1e12
+    return {"workload": "W8A8 per-channel, Qwen3-1.7B layer projections q,k,v,o,gate,up,down at M=512 (pp512 shape)",
+            "metric": "W8A8 int8 TOPS per whole call (row quantization + f16 pre-pass + GEMM)", "ms_per_layer": ms,
+            "value": tops, "unit": "TOPS",
+            "roofline": {"bound": "tensor", "achieved": tops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tops / peaks["bf16_tflops"]}}
+
+
 def cpu_baseline_decode(seconds_target=12.0):
     """Times the oracle (as it stands) on whole layers of the same workload, M = 1
     and M = 8, on all host cores, until about seconds_target of work is done."""
@@ -525,6 +624,8 @@ def run_ours(args, rank, world, torch, dist):
 
     prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None
     encoder = run_encoder_fc(torch, i2s, device, peaks) if not args.no_prefill else None
+    eltwise = run_encoder_eltwise(torch, i2s, device, peaks) if not args.no_prefill else None
+    w8a8 = run_w8a8_prefill(torch, i2s, device, peaks) if not args.no_prefill else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -546,6 +647,8 @@ def run_ours(args, rank, world, torch, dist):
     if prefill is not None:
         line["prefill"] = prefill
         line["encoder_fc"] = encoder
+        line["encoder_eltwise"] = eltwise
+        line["w8a8_prefill"] = w8a8
     return line
 
 
@@ -556,7 +659,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill and encoder-FC legs")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, encoder and W8A8 legs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
