@@ -217,27 +217,135 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant(const uint8_t* __rest
     if (blockIdx.x == 0) write_trailer(dst, n, scale);
 }
 
-// ------------------------------------------------------------------ transpose
-// 64 x 64-byte tiles through shared memory: a warp reads 64 contiguous bytes
-// of each of eight source rows and writes 64 contiguous bytes of each of eight
-// destination rows.
+// Short rows (ne0 = 16*V bytes, V <= 4): one thread per row, V 16-byte loads.
+// Pass 2 recomputes the row factor from the same bytes (cheaper than storing
+// and re-reading it).
+template <int V>
+__device__ __forceinline__ void load_row16(const uint8_t* p, uint32_t (&w)[4 * V]) {
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * v);
+        w[4 * v] = u.x;
+        w[4 * v + 1] = u.y;
+        w[4 * v + 2] = u.z;
+        w[4 * v + 3] = u.w;
+    }
+}
 
-constexpr int kTT = 64;
+template <int V>
+__device__ __forceinline__ float row_factor16(const uint32_t (&w)[4 * V], float s, float eps, int& qmax) {
+    int ssq = 0;
+    qmax = 0;
+#pragma unroll
+    for (int i = 0; i < 4 * V; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int b = byte_of(w[i], e);
+            ssq += b * b;
+            qmax = max(qmax, abs(b));
+        }
+    return rms_factor(ssq, 16 * V, s, eps);
+}
+
+template <int V>
+__global__ void __launch_bounds__(kEltThreads) k_rms_rows_t(const uint8_t* __restrict__ x, int64_t rows, float eps,
+                                                            const float* __restrict__ gamma,
+                                                            unsigned int* amax_bits) {
+    const float s = i8s_scale_of(x, rows * 16 * V);
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    float mx = 0.0f;
+    for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < rows; row += step) {
+        uint32_t w[4 * V];
+        load_row16<V>(x + row * 16 * V, w);
+        int qmax;
+        const float r = row_factor16<V>(w, s, eps, qmax);
+        if (gamma) {
+#pragma unroll
+            for (int i = 0; i < 4 * V; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(rms_one(byte_of(w[i], e), s, r, gamma, 4 * i + e)));
+        } else {
+            mx = fmaxf(mx, fabsf(rms_one((int8_t)qmax, s, r, nullptr, 0)));
+        }
+    }
+    fold_max(mx, amax_bits);
+}
+
+template <int V>
+__global__ void __launch_bounds__(kEltThreads) k_rms_quant_t(const uint8_t* __restrict__ x, int64_t rows, float eps,
+                                                             const float* __restrict__ gamma,
+                                                             const unsigned int* __restrict__ amax_bits,
+                                                             uint8_t* __restrict__ dst) {
+    const float s = i8s_scale_of(x, rows * 16 * V);
+    float scale, inv;
+    quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < rows; row += step) {
+        uint32_t w[4 * V];
+        load_row16<V>(x + row * 16 * V, w);
+        int qmax;
+        const float r = row_factor16<V>(w, s, eps, qmax);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wi = 4 * v + i;
+                o[i] = pack4(quantize_one(rms_one(byte_of(w[wi], 0), s, r, gamma, 4 * wi), inv),
+                             quantize_one(rms_one(byte_of(w[wi], 1), s, r, gamma, 4 * wi + 1), inv),
+                             quantize_one(rms_one(byte_of(w[wi], 2), s, r, gamma, 4 * wi + 2), inv),
+                             quantize_one(rms_one(byte_of(w[wi], 3), s, r, gamma, 4 * wi + 3), inv));
+            }
+            *reinterpret_cast<uint4*>(dst + row * 16 * V + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (blockIdx.x == 0) write_trailer(dst, rows * 16 * V, scale);
+}
+
+// ------------------------------------------------------------------ transpose
+// Tiles of 32 source rows x 128 source columns through shared memory. Loads:
+// one warp per source row segment, 4 bytes per lane (128 contiguous bytes per
+// warp instruction). Stores: 32-bit words of destination rows, eight threads
+// per 32-byte destination segment (for a = 32 the 128 destination rows of a
+// tile are one contiguous 4 KB block). Edge tiles and rows that are not whole
+// words take byte accesses.
+
+constexpr int kTR = 32, kTC = 128;
 
 __global__ void __launch_bounds__(kEltThreads) k_transpose(const uint8_t* __restrict__ src, int64_t a, int64_t b,
                                                            uint8_t* __restrict__ dst, int64_t tiles_b) {
-    __shared__ uint8_t tile[kTT][kTT + 4];
+    __shared__ __align__(16) uint8_t tile[kTR][kTC + 4];
     const int64_t ti = blockIdx.x / tiles_b, tj = blockIdx.x - ti * tiles_b;
-    const int64_t i0 = ti * kTT, j0 = tj * kTT;
-    const int c = threadIdx.x & 63, r0 = threadIdx.x >> 6;   // 4 rows per pass
-    for (int r = r0; r < kTT; r += kEltThreads / kTT) {
-        const int64_t i = i0 + r, j = j0 + c;
-        tile[r][c] = (i < a && j < b) ? src[i * b + j] : (uint8_t)0;
+    const int64_t i0 = ti * kTR, j0 = tj * kTC;
+    const bool full = i0 + kTR <= a && j0 + kTC <= b;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (full && (b & 3) == 0) {
+#pragma unroll
+        for (int r = warp; r < kTR; r += kEltThreads / 32)
+            *reinterpret_cast<uint32_t*>(&tile[r][4 * lane]) =
+                *reinterpret_cast<const uint32_t*>(src + (i0 + r) * b + j0 + 4 * lane);
+    } else {
+        for (int r = warp; r < kTR; r += kEltThreads / 32)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int64_t i = i0 + r, j = j0 + 4 * lane + e;
+                tile[r][4 * lane + e] = (i < a && j < b) ? src[i * b + j] : (uint8_t)0;
+            }
     }
     __syncthreads();
-    for (int r = r0; r < kTT; r += kEltThreads / kTT) {
-        const int64_t j = j0 + r, i = i0 + c;   // destination row j, column i
-        if (j < b && i < a) dst[j * a + i] = tile[c][r];
+    // destination row j0 + jr holds source rows i0..i0+31 at column jr
+    for (int w = threadIdx.x; w < kTC * (kTR / 4); w += kEltThreads) {
+        const int jr = w >> 3, k = w & 7;   // 8 words per destination segment
+        const uint32_t v = (uint32_t)tile[4 * k][jr] | ((uint32_t)tile[4 * k + 1][jr] << 8) |
+                           ((uint32_t)tile[4 * k + 2][jr] << 16) | ((uint32_t)tile[4 * k + 3][jr] << 24);
+        const int64_t j = j0 + jr, i = i0 + 4 * k;
+        if (full && (a & 3) == 0) {
+            *reinterpret_cast<uint32_t*>(dst + j * a + i) = v;
+        } else if (j < b) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i + e < a) dst[j * a + i + e] = (uint8_t)(v >> (8 * e));
+        }
     }
     if (blockIdx.x == 0) {
         __syncthreads();
@@ -266,6 +374,54 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col(const uint8_t* __restric
         for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(value(i) & 0xff);
         write_trailer(dst, n, i8s_scale_of(src, (int64_t)C * L));
     }
+}
+
+// Windowed im2col: a block covers T output positions (t0 .. t0+T-1) of every
+// channel. It stages each channel's input window (W = (T-1)*stride + KW bytes
+// from position t0*stride - pad_l, zeros outside [0, L)) in shared memory with
+// coalesced loads, then writes its T*C*KW contiguous output bytes as 32-bit
+// words, one per thread and step, reading the window. T is a multiple of 4, so
+// every block's output starts on a word. Sizes below 2^31 (checked by the host).
+__global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __restrict__ src, int C, int L, int KW,
+                                                            int stride, int pad_l, int OL, int T, int W,
+                                                            uint8_t* __restrict__ dst) {
+    extern __shared__ uint8_t win[];   // C x W
+    const int t0 = blockIdx.x * T;
+    const int p0 = t0 * stride - pad_l;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int c = warp; c < C; c += kEltThreads / 32) {
+        const uint8_t* row = src + (int64_t)c * L;
+        for (int xo = lane; xo < W; xo += 32) {
+            const int pos = p0 + xo;
+            win[c * W + xo] = (pos >= 0 && pos < L) ? row[pos] : (uint8_t)0;
+        }
+    }
+    __syncthreads();
+    const int Tn = min(T, OL - t0);
+    const int nloc = Tn * C * KW;
+    uint8_t* out = dst + (int64_t)t0 * C * KW;
+    for (int w = threadIdx.x; 4 * w < nloc; w += kEltThreads) {
+        const int f = 4 * w;
+        const int g = f / KW;
+        int k = f - g * KW, tl = g / C, c = g - tl * C;
+        uint32_t v = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (f + e < nloc) v |= (uint32_t)win[c * W + tl * stride + k] << (8 * e);
+            if (++k == KW) {
+                k = 0;
+                if (++c == C) { c = 0; ++tl; }
+            }
+        }
+        if (f + 3 < nloc) {
+            *reinterpret_cast<uint32_t*>(out + f) = v;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (f + e < nloc) out[f + e] = (uint8_t)(v >> (8 * e));
+        }
+    }
+    if (blockIdx.x == 0) write_trailer(dst, (int64_t)OL * C * KW, i8s_scale_of(src, (int64_t)C * L));
 }
 
 // ------------------------------------------------------------------ depthwise
@@ -315,6 +471,57 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_quant(const DwArgs d, const 
     if (blockIdx.x == 0) {
         for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(quantize_one(dw_one(d, sc, i), inv) & 0xff);
         write_trailer(dst, n, scale);
+    }
+}
+
+// Windowed depthwise: block (x, c) covers outputs t0 .. t0+1023 of channel c.
+// It stages the channel's input window (1023*stride + KW bytes) and the KW
+// taps in shared memory, then each thread forms four consecutive outputs.
+// kQuant = false folds max|y|; kQuant = true quantizes and stores. Needs
+// C <= 65535 (grid y), KW <= 64 and a window within 48 KB (host-checked).
+constexpr int kDwT = 4 * kEltThreads;
+
+template <bool kQuant>
+__global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, unsigned int* amax_bits,
+                                                        uint8_t* __restrict__ dst) {
+    extern __shared__ uint8_t dsm[];   // window (W bytes) then the taps
+    int8_t* win = reinterpret_cast<int8_t*>(dsm);
+    int8_t* taps = reinterpret_cast<int8_t*>(dsm + W);
+    const int c = blockIdx.y;
+    const int t0 = blockIdx.x * kDwT;
+    const int p0 = t0 * d.stride - d.pad_l;
+    const int8_t* row = reinterpret_cast<const int8_t*>(d.x) + (int64_t)c * d.L;
+    for (int xo = threadIdx.x; xo < W; xo += kEltThreads) {
+        const int pos = p0 + xo;
+        win[xo] = (pos >= 0 && pos < d.L) ? row[pos] : (int8_t)0;
+    }
+    if (threadIdx.x < d.KW) taps[threadIdx.x] = reinterpret_cast<const int8_t*>(d.w)[(int64_t)c * d.KW + threadIdx.x];
+    __syncthreads();
+    const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
+    const float bc = d.bias ? d.bias[c] : 0.0f;
+    float scale = 0.0f, inv = 0.0f;
+    if (kQuant) quant_params(__uint_as_float(*amax_bits), scale, inv);
+    float mx = 0.0f;
+    const int tl0 = 4 * threadIdx.x;
+    uint8_t* out = dst + (int64_t)c * d.OL + t0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int t = t0 + tl0 + e;
+        if (t < d.OL) {
+            const int8_t* xw = win + (tl0 + e) * d.stride;
+            int acc = 0;
+            for (int k = 0; k < d.KW; ++k) acc += (int)taps[k] * (int)xw[k];
+            float v = __fmul_rn(__int2float_rn(acc), sc);
+            if (d.bias) v = __fadd_rn(v, bc);
+            if (d.relu) v = v > 0.0f ? v : 0.0f;
+            if (kQuant) out[tl0 + e] = (uint8_t)(quantize_one(v, inv) & 0xff);
+            else mx = fmaxf(mx, fabsf(v));
+        }
+    }
+    if (kQuant) {
+        if (blockIdx.x == 0 && blockIdx.y == 0) write_trailer(dst, (int64_t)d.C * d.OL, scale);
+    } else {
+        fold_max(mx, amax_bits);
     }
 }
 
@@ -381,19 +588,46 @@ cudaError_t launch_add_scaled(const uint8_t* a, const uint8_t* b, int64_t n, uns
 
 cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, float eps, const float* gamma,
                                    float* rfac, unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
+    if (ne0 % 16 == 0 && ne0 <= 64) {   // short rows: one thread per row
+        const int grid = elt_grid(rows);
+        switch (ne0 / 16) {
+            case 1: k_rms_rows_t<1><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
+                    k_rms_quant_t<1><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+            case 2: k_rms_rows_t<2><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
+                    k_rms_quant_t<2><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+            case 3: k_rms_rows_t<3><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
+                    k_rms_quant_t<3><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+            default: k_rms_rows_t<4><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
+                     k_rms_quant_t<4><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+        }
+        return cudaGetLastError();
+    }
     k_rms_rows<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, eps, gamma, rfac, amax_bits);
     k_rms_quant<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, gamma, rfac, amax_bits, dst);
     return cudaGetLastError();
 }
 
 cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s) {
-    const int64_t ta = (a + kTT - 1) / kTT, tb = (b + kTT - 1) / kTT;
+    const int64_t ta = (a + kTR - 1) / kTR, tb = (b + kTC - 1) / kTC;
     k_transpose<<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
     return cudaGetLastError();
 }
 
 cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW, int stride, int pad_l, int64_t OL,
                                uint8_t* dst, cudaStream_t s) {
+    // windowed kernel: T output positions per block (a multiple of 4, at most
+    // 512) whose C windows fit in 48 KB of shared memory
+    constexpr int64_t kWinBytes = 48 * 1024;
+    int64_t T = 0;
+    if (C * KW <= kWinBytes) T = ((kWinBytes / C - KW) / stride + 1) & ~(int64_t)3;
+    if (T > 512) T = 512;
+    if (T >= 4) {
+        const int64_t W = (T - 1) * stride + KW;
+        const int64_t blocks = (OL + T - 1) / T;
+        k_im2col_win<<<(unsigned)blocks, kEltThreads, (size_t)(C * W), s>>>(src, (int)C, (int)L, KW, stride, pad_l,
+                                                                            (int)OL, (int)T, (int)W, dst);
+        return cudaGetLastError();
+    }
     k_im2col<<<elt_grid(OL * C * KW / 4 + 1), kEltThreads, 0, s>>>(src, (int)C, (int)L, KW, stride, pad_l, (int)OL,
                                                                    dst);
     return cudaGetLastError();
@@ -403,6 +637,14 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
                              int stride, int pad_l, int64_t OL, int relu, unsigned int* amax_bits, uint8_t* dst,
                              cudaStream_t s) {
     const DwArgs d{w, x, bias, (int)C, (int)L, (int)OL, KW, stride, pad_l, relu};
+    const int64_t W = (int64_t)(kDwT - 1) * stride + KW;
+    if (C <= 65535 && KW <= 64 && W + KW <= 48 * 1024) {   // windowed kernel
+        const dim3 g((unsigned)((OL + kDwT - 1) / kDwT), (unsigned)C);
+        const size_t sm = (size_t)(W + KW);
+        k_dw_win<false><<<g, kEltThreads, sm, s>>>(d, (int)W, amax_bits, dst);
+        k_dw_win<true><<<g, kEltThreads, sm, s>>>(d, (int)W, amax_bits, dst);
+        return cudaGetLastError();
+    }
     const int grid = elt_grid(C * OL / 4 + 1);
     k_dw_amax<<<grid, kEltThreads, 0, s>>>(d, amax_bits);
     k_dw_quant<<<grid, kEltThreads, 0, s>>>(d, amax_bits, dst);
