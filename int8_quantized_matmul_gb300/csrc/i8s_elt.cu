@@ -400,6 +400,21 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __res
     const int Tn = min(T, OL - t0);
     const int nloc = Tn * C * KW;
     uint8_t* out = dst + (int64_t)t0 * C * KW;
+    if ((KW & 3) == 0) {
+        // every output word lies inside one (t, c) group: two aligned window
+        // words and a funnel shift (the window buffer has 4 spare bytes)
+        const int wpg = KW >> 2;   // words per group
+        const uint32_t* win32 = reinterpret_cast<const uint32_t*>(win);
+        for (int w = threadIdx.x; 4 * w < nloc; w += kEltThreads) {
+            const int g = w / wpg, j = w - g * wpg;
+            const int tl = g / C, c = g - tl * C;
+            const int off = c * W + tl * stride + 4 * j;
+            const uint32_t lo = win32[off >> 2], hi = win32[(off >> 2) + 1];
+            *reinterpret_cast<uint32_t*>(out + 4 * w) = __funnelshift_r(lo, hi, 8 * (off & 3));
+        }
+        if (blockIdx.x == 0) write_trailer(dst, (int64_t)OL * C * KW, i8s_scale_of(src, (int64_t)C * L));
+        return;
+    }
     for (int w = threadIdx.x; 4 * w < nloc; w += kEltThreads) {
         const int f = 4 * w;
         const int g = f / KW;
@@ -525,6 +540,70 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, u
     }
 }
 
+// Stride-1 depthwise with at most 8 taps (the encoder blocks' 7-tap causal
+// conv): eight consecutive outputs per thread from four window words; each
+// output is two 4-way int8 dot products (__dp4a) of funnel-shifted window
+// words with the taps packed into two words (zero past KW).
+constexpr int kDw1Out = 8;
+constexpr int kDw1T = kDw1Out * kEltThreads;   // outputs per block
+
+template <bool kQuant>
+__global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned int* amax_bits,
+                                                       uint8_t* __restrict__ dst) {
+    __shared__ __align__(16) int8_t win[kDw1T + 16];
+    const int c = blockIdx.y;
+    const int t0 = blockIdx.x * kDw1T;
+    const int p0 = t0 - d.pad_l;
+    const int8_t* row = reinterpret_cast<const int8_t*>(d.x) + (int64_t)c * d.L;
+    for (int xo = threadIdx.x; xo < kDw1T + 16; xo += kEltThreads) {
+        const int pos = p0 + xo;
+        win[xo] = (pos >= 0 && pos < d.L) ? row[pos] : (int8_t)0;
+    }
+    const int8_t* wt = reinterpret_cast<const int8_t*>(d.w) + (int64_t)c * d.KW;
+    uint32_t tw[2] = {0u, 0u};
+    for (int k = 0; k < d.KW; ++k) tw[k >> 2] |= (uint32_t)(uint8_t)wt[k] << (8 * (k & 3));
+    __syncthreads();
+    const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
+    const float bc = d.bias ? d.bias[c] : 0.0f;
+    float scale = 0.0f, inv = 0.0f;
+    if (kQuant) quant_params(__uint_as_float(*amax_bits), scale, inv);
+    const int tl0 = kDw1Out * threadIdx.x;
+    // window bytes tl0 .. tl0+15 (tl0 is a multiple of 8: two 8-byte loads)
+    const uint2 wa = *reinterpret_cast<const uint2*>(win + tl0);
+    const uint2 wb = *reinterpret_cast<const uint2*>(win + tl0 + 8);
+    const uint32_t xw[4] = {wa.x, wa.y, wb.x, wb.y};
+    float mx = 0.0f;
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < kDw1Out; ++e) {
+        const int q = e >> 2, r = e & 3;
+        const int x0 = (int)__funnelshift_r(xw[q], xw[q + 1], 8 * r);
+        const int x1 = (int)__funnelshift_r(xw[q + 1], xw[q + 2], 8 * r);
+        const int acc = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
+        float v = __fmul_rn(__int2float_rn(acc), sc);
+        if (d.bias) v = __fadd_rn(v, bc);
+        if (d.relu) v = v > 0.0f ? v : 0.0f;
+        const bool live = t0 + tl0 + e < d.OL;
+        if (kQuant) packed[q] |= (uint32_t)(quantize_one(v, inv) & 0xff) << (8 * r);
+        else if (live) mx = fmaxf(mx, fabsf(v));
+    }
+    if (kQuant) {
+        uint8_t* out = dst + (int64_t)c * d.OL + t0 + tl0;
+        const bool aligned = ((((int64_t)c * d.OL) & 3) == 0);
+        if (aligned && t0 + tl0 + kDw1Out <= d.OL) {
+            reinterpret_cast<uint32_t*>(out)[0] = packed[0];
+            reinterpret_cast<uint32_t*>(out)[1] = packed[1];
+        } else {
+#pragma unroll
+            for (int e = 0; e < kDw1Out; ++e)
+                if (t0 + tl0 + e < d.OL) out[e] = (uint8_t)(packed[e >> 2] >> (8 * (e & 3)));
+        }
+        if (blockIdx.x == 0 && blockIdx.y == 0) write_trailer(dst, (int64_t)d.C * d.OL, scale);
+    } else {
+        fold_max(mx, amax_bits);
+    }
+}
+
 // ------------------------------------------------------------ W8A8 row quant
 // One CTA per activation row: the row's absmax (floored at 1e-9), then
 // q = clamp(round(x * inv)) with inv = 127/amax and the stored scale amax/127.
@@ -619,13 +698,13 @@ cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW,
     // 512) whose C windows fit in 48 KB of shared memory
     constexpr int64_t kWinBytes = 48 * 1024;
     int64_t T = 0;
-    if (C * KW <= kWinBytes) T = ((kWinBytes / C - KW) / stride + 1) & ~(int64_t)3;
+    if (C * KW <= kWinBytes - 4) T = (((kWinBytes - 4) / C - KW) / stride + 1) & ~(int64_t)3;
     if (T > 512) T = 512;
     if (T >= 4) {
         const int64_t W = (T - 1) * stride + KW;
         const int64_t blocks = (OL + T - 1) / T;
-        k_im2col_win<<<(unsigned)blocks, kEltThreads, (size_t)(C * W), s>>>(src, (int)C, (int)L, KW, stride, pad_l,
-                                                                            (int)OL, (int)T, (int)W, dst);
+        k_im2col_win<<<(unsigned)blocks, kEltThreads, (size_t)(C * W + 4), s>>>(src, (int)C, (int)L, KW, stride,
+                                                                                pad_l, (int)OL, (int)T, (int)W, dst);
         return cudaGetLastError();
     }
     k_im2col<<<elt_grid(OL * C * KW / 4 + 1), kEltThreads, 0, s>>>(src, (int)C, (int)L, KW, stride, pad_l, (int)OL,
@@ -637,6 +716,12 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
                              int stride, int pad_l, int64_t OL, int relu, unsigned int* amax_bits, uint8_t* dst,
                              cudaStream_t s) {
     const DwArgs d{w, x, bias, (int)C, (int)L, (int)OL, KW, stride, pad_l, relu};
+    if (stride == 1 && KW <= 8 && C <= 65535) {   // the 7-tap causal blocks: dp4a
+        const dim3 g((unsigned)((OL + kDw1T - 1) / kDw1T), (unsigned)C);
+        k_dw_s1<false><<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
+        k_dw_s1<true><<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
+        return cudaGetLastError();
+    }
     const int64_t W = (int64_t)(kDwT - 1) * stride + KW;
     if (C <= 65535 && KW <= 64 && W + KW <= 48 * 1024) {   // windowed kernel
         const dim3 g((unsigned)((OL + kDwT - 1) / kDwT), (unsigned)C);
