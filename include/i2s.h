@@ -370,6 +370,20 @@ size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
 int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M,
                  float* d, void* ws, size_t ws_bytes, i2s_stream_t stream);
 
+/* Packed weights ([P4] Implementation: the weights are quantized and packed
+ * for the matrix unit once, on the cache-miss path, and reused by every call).
+ * w8a8_pack_weights writes the f16 operand rows of wq (exact integers, N x K,
+ * w8a8_packed_bytes(N,K) bytes, 16-byte aligned, caller-owned) once;
+ * w8a8_mul_mat_packed then runs each call as two launches (rows quantized
+ * straight into f16 operand rows, then the GEMM) with no per-call weight
+ * conversion. Same requirements and results as w8a8_mul_mat; workspace at least
+ * w8a8_mul_mat_packed_workspace(M,N,K) bytes. */
+size_t w8a8_packed_bytes(int64_t N, int64_t K);
+int w8a8_pack_weights(const int8_t* wq, int64_t N, int64_t K, void* packed, i2s_stream_t stream);
+size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K);
+int w8a8_mul_mat_packed(const void* packed, const float* bscale, int64_t N, int64_t K, const float* x,
+                        int64_t M, float* d, void* ws, size_t ws_bytes, i2s_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Device status. Kernels with bounded waits (the tensor-core pipelines) never
  * trap: when a wait runs out they record a code in the status word at the

@@ -784,66 +784,30 @@ int w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, floa
     return cuda_status(launch_w8a8_weights(w, N, K, wq, bscale, stream));
 }
 
-// W8A8 workspace: [header: status, amax][activations int8, M x K][row scales,
-// M F32][then the I8_S GEMM's operands and split-tile areas: activations f16,
-// rows_pad x K; weights f16, N x K; slots; tickets; masks].
-static size_t w8a8_front(int64_t M, int64_t K) { return kHeader + align_up((size_t)M * K) + align_up((size_t)M * 4); }
-
-size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
-    const size_t i8 = i8s_mul_mat_workspace(M, N, K);
-    if (i8 == 0) return 0;
-    return w8a8_front(M, K) + (i8 - kHeader - align_up((size_t)M * (size_t)N * 4));
-}
-
-int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M, float* d,
-                 void* ws, size_t ws_bytes, i2s_stream_t stream) {
-    if (!wq || !bscale || !x || !d || !ws) return I2S_E_NULL_PTR;
-    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
-    if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
-        return I2S_E_BAD_SHAPE;
-    if (!aligned16(wq) || !aligned16(x) || !aligned16(d) || !aligned256(ws) || ((uintptr_t)bscale & 3u))
-        return I2S_E_MISALIGNED;
-    if (ws_bytes < w8a8_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
-    int r = check_device();
-    if (r) return r;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
-    uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
-    int8_t* xq = reinterpret_cast<int8_t*>(base + kHeader);
-    float* ascale = reinterpret_cast<float*>(base + kHeader + align_up((size_t)M * K));
+// The I8_S tensor-core GEMM with the W8A8 epilogue over f16 operands already
+// in place (xf: rows_pad x K, wf: N x K); the split-tile areas of the
+// workspace start at part_off and were cleared by the launch before.
+static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* ascale, const __half* xf, int64_t N,
+                            int64_t K, int64_t M, float* d, uint8_t* base, size_t part_off, i2s_stream_t stream) {
     const int64_t rows_pad = i8s_rows_pad(M);
     const size_t tiles = (size_t)i8s_tiles(M, N);
-    const size_t xf_off = w8a8_front(M, K);
-    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
-    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
     const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
     const size_t mask_off = tick_off + align_up(tiles * 4);
-    const size_t zero_bytes = mask_off + align_up(tiles * 8) - tick_off;
-    __half* xf = reinterpret_cast<__half*>(base + xf_off);
-    __half* wf = reinterpret_cast<__half*>(base + wf_off);
-    // per-row activation quantization (1e-9 floor), then the int8 rows and
-    // weights to f16 (the pre-pass also clears the status word and the
-    // split-tile tickets), then the tensor-core GEMM with the W8A8 epilogue
-    r = cuda_status(launch_w8a8_rows(x, M, K, xq, ascale, stream));
-    if (r) return r;
-    r = cuda_status(launch_i8s_to_f16(wq, (int)N, wf, xq, (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes,
-                                      status, amax, stream));
-    if (r) return r;
     static thread_local I8sTcArgs a;
     if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
-    a.w = wq;
+    a.w = nullptr;
     a.w_scale_ptr = bscale;   // read by the kernel's I8_S prologue; the W8A8 epilogue uses the arrays
     a.x_scale_ptr = ascale;
     a.bias = nullptr;
     a.row_scale = ascale;
     a.col_scale = bscale;
     a.y = d;
-    a.amax_bits = amax;
+    a.amax_bits = reinterpret_cast<unsigned int*>(base + kAmaxOff);
     a.part = reinterpret_cast<int32_t*>(base + part_off);
     a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
     a.slot_masks = reinterpret_cast<unsigned long long*>(base + mask_off);
-    a.status = status;
+    a.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
@@ -855,6 +819,113 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
     int pairs = i8s_gemm_tc_max_pairs();
     if (pairs > a.total_units) pairs = a.total_units;
     return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
+}
+
+// bytes of the GEMM's split-tile areas (slots, tickets, masks)
+static size_t w8a8_split_bytes(int64_t M, int64_t N, int64_t K) {
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    return align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4) +
+           align_up(tiles * 8);
+}
+
+static bool w8a8_shape_ok(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return false;
+    return M * K < ((int64_t)1 << 31) && N * K < ((int64_t)1 << 31) && M * N < ((int64_t)1 << 31);
+}
+
+// W8A8 workspace (int8 weights): [header: status, amax][activations int8,
+// M x K][row scales, M F32][activations f16, rows_pad x K][weights f16, N x K]
+// [split-tile slots, tickets, masks].
+static size_t w8a8_front(int64_t M, int64_t K) { return kHeader + align_up((size_t)M * K) + align_up((size_t)M * 4); }
+
+size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
+    if (!w8a8_shape_ok(M, N, K)) return 0;
+    return w8a8_front(M, K) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) + align_up((size_t)N * (size_t)K * 2) +
+           w8a8_split_bytes(M, N, K);
+}
+
+int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M, float* d,
+                 void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!wq || !bscale || !x || !d || !ws) return I2S_E_NULL_PTR;
+    if (!w8a8_shape_ok(M, N, K)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(wq) || !aligned16(x) || !aligned16(d) || !aligned256(ws) || ((uintptr_t)bscale & 3u))
+        return I2S_E_MISALIGNED;
+    if (ws_bytes < w8a8_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+    int8_t* xq = reinterpret_cast<int8_t*>(base + kHeader);
+    float* ascale = reinterpret_cast<float*>(base + kHeader + align_up((size_t)M * K));
+    const int64_t rows_pad = i8s_rows_pad(M);
+    const size_t xf_off = w8a8_front(M, K);
+    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
+    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+    const size_t zero_bytes = w8a8_split_bytes(M, N, K) - (tick_off - part_off);   // tickets and masks
+    __half* xf = reinterpret_cast<__half*>(base + xf_off);
+    __half* wf = reinterpret_cast<__half*>(base + wf_off);
+    // per-row activation quantization (1e-9 floor), then the int8 rows and
+    // weights to f16 (the pre-pass also clears the status word and the
+    // split-tile tickets), then the tensor-core GEMM with the W8A8 epilogue
+    r = cuda_status(launch_w8a8_rows(x, M, K, xq, ascale, stream));
+    if (r) return r;
+    r = cuda_status(launch_i8s_to_f16(wq, (int)N, wf, xq, (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes,
+                                      status, amax, stream));
+    if (r) return r;
+    return launch_w8a8_gemm(wf, bscale, ascale, xf, N, K, M, d, base, part_off, stream);
+}
+
+size_t w8a8_packed_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 64 || K % 64 || N * K >= ((int64_t)1 << 31)) return 0;
+    return (size_t)N * (size_t)K * 2;
+}
+
+int w8a8_pack_weights(const int8_t* wq, int64_t N, int64_t K, void* packed, i2s_stream_t stream) {
+    if (!wq || !packed) return I2S_E_NULL_PTR;
+    if (w8a8_packed_bytes(N, K) == 0) return I2S_E_BAD_SHAPE;
+    if (!aligned16(wq) || !aligned16(packed)) return I2S_E_MISALIGNED;
+    if (overlaps(wq, (size_t)N * K, packed, w8a8_packed_bytes(N, K))) return I2S_E_BAD_ARG;
+    int r = check_device();
+    if (r) return r;
+    return cuda_status(launch_i8_to_f16(wq, N * K, static_cast<__half*>(packed), stream));
+}
+
+// Packed W8A8 workspace: [header: status, amax][row scales, M F32]
+// [activations f16, rows_pad x K][split-tile slots, tickets, masks].
+size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
+    if (!w8a8_shape_ok(M, N, K)) return 0;
+    return kHeader + align_up((size_t)M * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
+           w8a8_split_bytes(M, N, K);
+}
+
+int w8a8_mul_mat_packed(const void* packed, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M,
+                        float* d, void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!packed || !bscale || !x || !d || !ws) return I2S_E_NULL_PTR;
+    if (!w8a8_shape_ok(M, N, K)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(d) || !aligned256(ws) || ((uintptr_t)bscale & 3u))
+        return I2S_E_MISALIGNED;
+    if (ws_bytes < w8a8_mul_mat_packed_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    float* ascale = reinterpret_cast<float*>(base + kHeader);
+    const int64_t rows_pad = i8s_rows_pad(M);
+    const size_t xf_off = kHeader + align_up((size_t)M * 4);
+    const size_t part_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
+    const size_t tiles = (size_t)i8s_tiles(M, N);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+    const size_t zero_bytes = w8a8_split_bytes(M, N, K) - (tick_off - part_off);
+    __half* xf = reinterpret_cast<__half*>(base + xf_off);
+    // rows straight into f16 operand rows (the launch also clears the status,
+    // amax and split-tile counters), then the GEMM
+    r = cuda_status(launch_w8a8_rows_f16(x, M, rows_pad, K, xf, ascale, base + tick_off, zero_bytes,
+                                         reinterpret_cast<uint32_t*>(base + kStatusOff),
+                                         reinterpret_cast<unsigned int*>(base + kAmaxOff), stream));
+    if (r) return r;
+    return launch_w8a8_gemm(static_cast<const __half*>(packed), bscale, ascale, xf, N, K, M, d, base, part_off, stream);
 }
 
 int i2s_read_status(void* ws, i2s_stream_t stream) {

@@ -15,7 +15,9 @@
 //                    requantized per tensor
 //   w8a8 rows        per-row int8 activations, amax floored at 1e-9
 //   w8a8 weights     per-channel int8 weights: rint(w / (amax/127)), amax
-//                    floored at 1e-9
+//                    floored at 1e-9; packed once into f16 operand rows
+//   w8a8 rows (f16)  the packed call's row quantizer, straight into the GEMM's
+//                    f16 operand rows
 //
 // Every op here moves bytes: each is bound by HBM bandwidth. An op whose output
 // scale depends on the whole output runs two passes over its inputs: the first
@@ -649,6 +651,58 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_weights(const float* __res
     }
 }
 
+// The packed W8A8 call: rows_pad blocks; block m < M quantizes row m (1e-9
+// floor) straight into the GEMM's f16 operand row (exact integers) and its
+// scale, blocks m >= M write zero rows. The same launch clears the status word,
+// the amax word and the GEMM's split-tile counters.
+__global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const float* __restrict__ x, int64_t M, int64_t K,
+                                                               __half* __restrict__ xf, float* __restrict__ ascale,
+                                                               uint4* zero, unsigned long long zero_16,
+                                                               uint32_t* status, unsigned int* amax_bits) {
+    __shared__ float s_max[kEltThreads / 32];
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *status = 0u;
+        *amax_bits = 0u;
+    }
+    for (unsigned long long i = blockIdx.x * (unsigned long long)kEltThreads + threadIdx.x; i < zero_16;
+         i += (unsigned long long)gridDim.x * kEltThreads)
+        zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t m = blockIdx.x;
+    __half* out = xf + m * K;
+    if (m >= M) {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __float2half_rn(0.0f);
+        return;
+    }
+    const float* xr = x + m * K;
+    float mx = 0.0f;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = s_max[0];
+    for (int i = 1; i < kEltThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
+    mx = fmaxf(mx, 1e-9f);
+    const float inv = __fdiv_rn(127.0f, mx);
+    if (threadIdx.x == 0) ascale[m] = __fdiv_rn(mx, 127.0f);
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_one(xr[k], inv));
+}
+
+// int8 -> f16 (exact), 16 values per thread and step.
+__global__ void __launch_bounds__(kEltThreads) k_i8_to_f16(const int8_t* __restrict__ src, int64_t n16,
+                                                           __half* __restrict__ dst) {
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += step) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        __align__(16) __half h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = __int2half_rn(byte_of(w[j >> 2], j & 3));
+        uint4* o = reinterpret_cast<uint4*>(dst + 16 * i);
+        o[0] = *reinterpret_cast<const uint4*>(&h[0]);
+        o[1] = *reinterpret_cast<const uint4*>(&h[8]);
+    }
+}
+
 int elt_grid(int64_t work) {
     const int64_t want = (work + kEltThreads - 1) / kEltThreads;
     const int cap = device_sm_count() * 8;
@@ -738,6 +792,19 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
 
 cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale, cudaStream_t s) {
     k_w8a8_rows<<<(unsigned)M, kEltThreads, 0, s>>>(x, K, q, ascale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_w8a8_rows_f16(const float* x, int64_t M, int64_t rows_pad, int64_t K, __half* xf, float* ascale,
+                                 void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
+                                 cudaStream_t s) {
+    k_w8a8_rows_f16<<<(unsigned)rows_pad, kEltThreads, 0, s>>>(x, M, K, xf, ascale, static_cast<uint4*>(zero),
+                                                                zero_bytes / 16, status, amax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_i8_to_f16(const int8_t* src, int64_t n, __half* dst, cudaStream_t s) {
+    k_i8_to_f16<<<elt_grid(n / 16), kEltThreads, 0, s>>>(src, n / 16, dst);
     return cudaGetLastError();
 }
 

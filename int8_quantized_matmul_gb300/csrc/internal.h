@@ -196,6 +196,10 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
                              cudaStream_t s);
 cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale, cudaStream_t s);
 cudaError_t launch_w8a8_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale, cudaStream_t s);
+cudaError_t launch_w8a8_rows_f16(const float* x, int64_t M, int64_t rows_pad, int64_t K, __half* xf, float* ascale,
+                                 void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
+                                 cudaStream_t s);
+cudaError_t launch_i8_to_f16(const int8_t* src, int64_t n, __half* dst, cudaStream_t s);
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst,
                            cudaStream_t s);
 

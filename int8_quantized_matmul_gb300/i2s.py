@@ -78,6 +78,10 @@ _SIGS = {
     "w8a8_quantize_weights": (_int, [_p, _i64, _i64, _p, _p, _p]),
     "w8a8_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
     "w8a8_mul_mat": (_int, [_p, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "w8a8_packed_bytes": (_sz, [_i64, _i64]),
+    "w8a8_pack_weights": (_int, [_p, _i64, _i64, _p, _p]),
+    "w8a8_mul_mat_packed_workspace": (_sz, [_i64, _i64, _i64]),
+    "w8a8_mul_mat_packed": (_int, [_p, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_L, _name)
@@ -385,6 +389,32 @@ def w8a8_mul_mat(wq, bscale, x, d=None, ws=None):
         ws = _ws(w8a8_mul_mat_workspace(M, N, K), x.device)
     _check("w8a8_mul_mat", _L.w8a8_mul_mat(_dptr(wq), _dptr(bscale), N, K, _dptr(x), M, _dptr(d), _dptr(ws),
                                            ws.numel(), _stream()))
+    return d, ws
+
+
+def w8a8_pack_weights(wq, packed=None):
+    """The f16 operand rows of per-channel int8 weights (N x K), written once."""
+    N, K = wq.shape
+    if packed is None:
+        packed = _u8(int(_L.w8a8_packed_bytes(N, K)), wq.device)
+    _check("w8a8_pack_weights", _L.w8a8_pack_weights(_dptr(wq), N, K, _dptr(packed), _stream()))
+    return packed
+
+
+def w8a8_mul_mat_packed_workspace(M: int, N: int, K: int) -> int:
+    return int(_L.w8a8_mul_mat_packed_workspace(M, N, K))
+
+
+def w8a8_mul_mat_packed(packed, bscale, N: int, K: int, x, d=None, ws=None):
+    """w8a8_mul_mat over weights packed once by w8a8_pack_weights."""
+    torch = _torch()
+    M = x.shape[0]
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _ws(w8a8_mul_mat_packed_workspace(M, N, K), x.device)
+    _check("w8a8_mul_mat_packed", _L.w8a8_mul_mat_packed(_dptr(packed), _dptr(bscale), N, K, _dptr(x), M, _dptr(d),
+                                                         _dptr(ws), ws.numel(), _stream()))
     return d, ws
 
 

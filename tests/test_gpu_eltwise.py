@@ -272,3 +272,27 @@ def test_w8a8_prefill_projection_sampled(i2s, o, N, K):
     got = host(d)
     for m0 in (0, 251, M - 8):
         same_bytes(got[m0:m0 + 8], o.w8a8_mul_mat(wq, bs, x[m0:m0 + 8], nth=8))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (17, 70, 256), (300, 640, 2048), (161, 257, 1088)])
+def test_w8a8_packed(i2s, o, M, N, K):
+    # weights packed once, then two calls on the same packed weights
+    wq, bs, x = w8a8_inputs(o, M, N, K, seed=M * 3 + N + K)
+    packed = i2s.w8a8_pack_weights(dev(wq))
+    ref = o.w8a8_mul_mat(wq, bs, x, nth=4)
+    d, ws = i2s.w8a8_mul_mat_packed(packed, dev(bs), N, K, dev(x))
+    assert i2s.read_status(ws) == 0
+    same_bytes(host(d), ref)
+    x2 = synth.normal_f32((M, K), seed=M + 99)
+    d2, _ = i2s.w8a8_mul_mat_packed(packed, dev(bs), N, K, dev(x2), ws=ws)
+    same_bytes(host(d2), o.w8a8_mul_mat(wq, bs, x2, nth=4))
+
+
+def test_w8a8_packed_prefill_projection_sampled(i2s, o):
+    M, N, K = 512, 6144, 2048
+    wq, bs, x = w8a8_inputs(o, M, N, K, seed=7)
+    packed = i2s.w8a8_pack_weights(dev(wq))
+    d, ws = i2s.w8a8_mul_mat_packed(packed, dev(bs), N, K, dev(x))
+    got = host(d)
+    for m0 in (0, 333, M - 8):
+        same_bytes(got[m0:m0 + 8], o.w8a8_mul_mat(wq, bs, x[m0:m0 + 8], nth=8))
