@@ -717,7 +717,7 @@ int i8s_rms_norm_scaled(const void* x_i8s, int64_t rows, int64_t ne0, float eps,
 
 int i8s_transpose(const void* src_i8s, int64_t a, int64_t b, void* dst_i8s, i2s_stream_t stream) {
     if (!src_i8s || !dst_i8s) return I2S_E_NULL_PTR;
-    if (a < 1 || b < 1 || a * b >= ((int64_t)1 << 40) || ((a + 63) / 64) * ((b + 63) / 64) >= ((int64_t)1 << 31))
+    if (a < 1 || b < 1 || a * b >= ((int64_t)1 << 40) || ((a + 31) / 32) * ((b + 31) / 32) >= ((int64_t)1 << 31))
         return I2S_E_BAD_SHAPE;
     const size_t nb = i8s_nbytes(a * b);
     if (overlaps(dst_i8s, nb, src_i8s, nb)) return I2S_E_BAD_ARG;

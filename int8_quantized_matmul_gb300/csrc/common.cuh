@@ -7,21 +7,29 @@
 
 namespace i2s {
 
-// Round to nearest, halfway cases away from zero, computed exactly:
-// v - trunc(v) is exact for every binary32 v, and t +- 1 is exact for
-// |t| < 2^24 (larger v are already integers).
-__device__ __forceinline__ float round_half_away(float v) {
-    const float t = truncf(v);
-    const float frac = fabsf(__fsub_rn(v, t));
-    return frac >= 0.5f ? __fadd_rn(t, copysignf(1.0f, v)) : t;
+// The quantizer step shared by the row quantizer and the per-tensor
+// requantizer: q = clamp(round(x * inv), -127, 127), rounding halfway cases
+// away from zero, in full-rate operations (the conversion instructions run at
+// an eighth of the FP32 rate). Clamping first gives the same result. Then
+// round(|v|) = floor(a) with a = |v| + h, h = 0.5 - 2^-25 (the largest float
+// below one half), the sum rounded to nearest: for |v| just below k + 1/2 the
+// sum stays below k + 1, at exactly k + 1/2 it is the midpoint k + 1 - 2^-25,
+// which rounds (ties to even) to k + 1, and for |v| >= 2^22 it cannot reach
+// the next integer. floor(a) (a < 128) is read from the low bits of
+// a + 1.5*2^23 added with rounding toward zero, and the sign is put back on
+// the integer. Checked on the GPU around every half integer against the CPU
+// reference (C roundf).
+__device__ __forceinline__ int quantize_one(float x, float inv) {
+    const float v = fminf(fmaxf(__fmul_rn(x, inv), -127.0f), 127.0f);
+    const float a = __fadd_rn(fabsf(v), 0x1.fffffep-2f);
+    const int m = (int)(__float_as_uint(__fadd_rz(a, 12582912.0f)) - 0x4B400000u);
+    return v < 0.0f ? -m : m;
 }
 
-// The quantizer step shared by the row quantizer and the per-tensor
-// requantizer: q = clamp(round(x * inv), -127, 127).
-__device__ __forceinline__ int quantize_one(float x, float inv) {
-    float r = round_half_away(__fmul_rn(x, inv));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return (int)r;
+// int8 -> float exactly in two full-rate operations: the byte b + 128 placed
+// in the mantissa of 2^23 (XOR with 0x4B000080), minus 2^23 + 128.
+__device__ __forceinline__ float i8_to_float(int8_t b) {
+    return __fsub_rn(__uint_as_float((uint32_t)(uint8_t)b ^ 0x4B000080u), 8388736.0f);
 }
 
 // amax floor and the two divisions of the quantizer: scale = amax/127 is

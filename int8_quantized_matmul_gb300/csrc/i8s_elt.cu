@@ -70,10 +70,34 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
 
 __device__ __forceinline__ int8_t byte_of(uint32_t w, int i) { return (int8_t)(w >> (8 * i)); }
 
+// Stages bytes [pos0, pos0 + nbytes) of a row of L bytes (zeros outside
+// [0, L)) in shared memory as 32-bit words read at aligned addresses: word i
+// holds the row bytes from pos0 - sh + 4i, where sh = the misalignment of
+// row + pos0. Words that reach outside the row take byte loads. Returns sh.
+__device__ __forceinline__ int stage_window(const uint8_t* row, int64_t L, int64_t pos0, int nbytes, uint32_t* win32,
+                                            int tid, int nthreads) {
+    const int sh = (int)(((uintptr_t)row + (uintptr_t)pos0) & 3u);
+    const int nw = (sh + nbytes + 3) >> 2;
+    for (int i = tid; i < nw; i += nthreads) {
+        const int64_t g = pos0 - sh + 4 * (int64_t)i;   // row position of the word's first byte
+        uint32_t w;
+        if (g >= 0 && g + 4 <= L) {
+            w = *reinterpret_cast<const uint32_t*>(row + g);
+        } else {
+            w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (g + e >= 0 && g + e < L) w |= (uint32_t)row[g + e] << (8 * e);
+        }
+        win32[i] = w;
+    }
+    return sh;
+}
+
 // ---------------------------------------------------------------- add_scaled
 
 __device__ __forceinline__ float add_one(int8_t qa, int8_t qb, float sa, float sb) {
-    return __fadd_rn(__fmul_rn((float)qa, sa), __fmul_rn((float)qb, sb));
+    return __fadd_rn(__fmul_rn(i8_to_float(qa), sa), __fmul_rn(i8_to_float(qb), sb));
 }
 
 // Pass 1: max |y| over the tensor. 16 bytes of each input per thread and step.
@@ -133,7 +157,7 @@ __device__ __forceinline__ float rms_factor(int ssq, int64_t ne0, float s, float
 }
 
 __device__ __forceinline__ float rms_one(int8_t q, float s, float r, const float* gamma, int64_t i) {
-    float v = __fmul_rn(__fmul_rn((float)q, s), r);
+    float v = __fmul_rn(__fmul_rn(i8_to_float(q), s), r);
     if (gamma) v = __fmul_rn(v, gamma[i]);
     return v;
 }
@@ -305,39 +329,42 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant_t(const uint8_t* __re
 }
 
 // ------------------------------------------------------------------ transpose
-// Tiles of 32 source rows x 128 source columns through shared memory. Loads:
-// one warp per source row segment, 4 bytes per lane (128 contiguous bytes per
-// warp instruction). Stores: 32-bit words of destination rows, eight threads
-// per 32-byte destination segment (for a = 32 the 128 destination rows of a
-// tile are one contiguous 4 KB block). Edge tiles and rows that are not whole
-// words take byte accesses.
+// Tiles of TR source rows x TC source columns through shared memory: 32 x 128
+// for wide source rows, 128 x 32 for narrow ones (b < 128), so that loads and
+// stores both move whole 128-byte segments per warp instruction. Loads: 32-bit
+// words of source rows; stores: 32-bit words of destination rows (TR/4 words
+// per destination segment). Edge tiles and rows that are not whole words take
+// byte accesses.
 
-constexpr int kTR = 32, kTC = 128;
-
+template <int TR, int TC>
 __global__ void __launch_bounds__(kEltThreads) k_transpose(const uint8_t* __restrict__ src, int64_t a, int64_t b,
                                                            uint8_t* __restrict__ dst, int64_t tiles_b) {
-    __shared__ __align__(16) uint8_t tile[kTR][kTC + 4];
+    __shared__ __align__(16) uint8_t tile[TR][TC + 4];
+    constexpr int kRowWords = TC / 4, kColWords = TR / 4;
     const int64_t ti = blockIdx.x / tiles_b, tj = blockIdx.x - ti * tiles_b;
-    const int64_t i0 = ti * kTR, j0 = tj * kTC;
-    const bool full = i0 + kTR <= a && j0 + kTC <= b;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t i0 = ti * TR, j0 = tj * TC;
+    const bool full = i0 + TR <= a && j0 + TC <= b;
     if (full && (b & 3) == 0) {
 #pragma unroll
-        for (int r = warp; r < kTR; r += kEltThreads / 32)
-            *reinterpret_cast<uint32_t*>(&tile[r][4 * lane]) =
-                *reinterpret_cast<const uint32_t*>(src + (i0 + r) * b + j0 + 4 * lane);
+        for (int w = threadIdx.x; w < TR * kRowWords; w += kEltThreads) {
+            const int r = w / kRowWords, cw = w - r * kRowWords;
+            *reinterpret_cast<uint32_t*>(&tile[r][4 * cw]) =
+                *reinterpret_cast<const uint32_t*>(src + (i0 + r) * b + j0 + 4 * cw);
+        }
     } else {
-        for (int r = warp; r < kTR; r += kEltThreads / 32)
+        for (int w = threadIdx.x; w < TR * kRowWords; w += kEltThreads) {
+            const int r = w / kRowWords, cw = w - r * kRowWords;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int64_t i = i0 + r, j = j0 + 4 * lane + e;
-                tile[r][4 * lane + e] = (i < a && j < b) ? src[i * b + j] : (uint8_t)0;
+                const int64_t i = i0 + r, j = j0 + 4 * cw + e;
+                tile[r][4 * cw + e] = (i < a && j < b) ? src[i * b + j] : (uint8_t)0;
             }
+        }
     }
     __syncthreads();
-    // destination row j0 + jr holds source rows i0..i0+31 at column jr
-    for (int w = threadIdx.x; w < kTC * (kTR / 4); w += kEltThreads) {
-        const int jr = w >> 3, k = w & 7;   // 8 words per destination segment
+    // destination row j0 + jr holds source rows i0 .. i0+TR-1 at column jr
+    for (int w = threadIdx.x; w < TC * kColWords; w += kEltThreads) {
+        const int jr = w / kColWords, k = w - jr * kColWords;
         const uint32_t v = (uint32_t)tile[4 * k][jr] | ((uint32_t)tile[4 * k + 1][jr] << 8) |
                            ((uint32_t)tile[4 * k + 2][jr] << 16) | ((uint32_t)tile[4 * k + 3][jr] << 24);
         const int64_t j = j0 + jr, i = i0 + 4 * k;
@@ -387,18 +414,19 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col(const uint8_t* __restric
 __global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __restrict__ src, int C, int L, int KW,
                                                             int stride, int pad_l, int OL, int T, int W,
                                                             uint8_t* __restrict__ dst) {
-    extern __shared__ uint8_t win[];   // C x W
+    // per channel: Wc words of staged window (the row bytes from p0 - sh[c])
+    extern __shared__ uint32_t wsm[];
+    const int Wc = (W + 3 + 3) / 4 + 1;
+    int* shs = reinterpret_cast<int*>(wsm + (size_t)C * Wc);
     const int t0 = blockIdx.x * T;
     const int p0 = t0 * stride - pad_l;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int c = warp; c < C; c += kEltThreads / 32) {
-        const uint8_t* row = src + (int64_t)c * L;
-        for (int xo = lane; xo < W; xo += 32) {
-            const int pos = p0 + xo;
-            win[c * W + xo] = (pos >= 0 && pos < L) ? row[pos] : (uint8_t)0;
-        }
+        const int sh = stage_window(src + (int64_t)c * L, L, p0, W, wsm + (size_t)c * Wc, lane, 32);
+        if (lane == 0) shs[c] = sh;
     }
     __syncthreads();
+    const uint8_t* win = reinterpret_cast<const uint8_t*>(wsm);
     const int Tn = min(T, OL - t0);
     const int nloc = Tn * C * KW;
     uint8_t* out = dst + (int64_t)t0 * C * KW;
@@ -406,13 +434,26 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __res
         // every output word lies inside one (t, c) group: two aligned window
         // words and a funnel shift (the window buffer has 4 spare bytes)
         const int wpg = KW >> 2;   // words per group
-        const uint32_t* win32 = reinterpret_cast<const uint32_t*>(win);
+        // word w = (tl*C + c)*wpg + j; each step advances w by the block size,
+        // so (tl, c, j) advance by fixed amounts with carries (no division)
+        const int dg = kEltThreads / wpg, dj = kEltThreads - dg * wpg;
+        const int dtl = dg / C, dc = dg - dtl * C;
+        int j, c, tl;
+        {
+            const int g0 = threadIdx.x / wpg;
+            j = threadIdx.x - g0 * wpg;
+            tl = g0 / C;
+            c = g0 - tl * C;
+        }
         for (int w = threadIdx.x; 4 * w < nloc; w += kEltThreads) {
-            const int g = w / wpg, j = w - g * wpg;
-            const int tl = g / C, c = g - tl * C;
-            const int off = c * W + tl * stride + 4 * j;
-            const uint32_t lo = win32[off >> 2], hi = win32[(off >> 2) + 1];
+            const int off = c * 4 * Wc + shs[c] + tl * stride + 4 * j;   // byte offset in the staged words
+            const uint32_t lo = wsm[off >> 2], hi = wsm[(off >> 2) + 1];
             *reinterpret_cast<uint32_t*>(out + 4 * w) = __funnelshift_r(lo, hi, 8 * (off & 3));
+            j += dj;
+            if (j >= wpg) { j -= wpg; ++c; }
+            c += dc;
+            if (c >= C) { c -= C; ++tl; }
+            tl += dtl;
         }
         if (blockIdx.x == 0) write_trailer(dst, (int64_t)OL * C * KW, i8s_scale_of(src, (int64_t)C * L));
         return;
@@ -424,7 +465,7 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __res
         uint32_t v = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            if (f + e < nloc) v |= (uint32_t)win[c * W + tl * stride + k] << (8 * e);
+            if (f + e < nloc) v |= (uint32_t)win[c * 4 * Wc + shs[c] + tl * stride + k] << (8 * e);
             if (++k == KW) {
                 k = 0;
                 if (++c == C) { c = 0; ++tl; }
@@ -547,20 +588,19 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, u
 // output is two 4-way int8 dot products (__dp4a) of funnel-shifted window
 // words with the taps packed into two words (zero past KW).
 constexpr int kDw1Out = 8;
-constexpr int kDw1T = kDw1Out * kEltThreads;   // outputs per block
+constexpr int kDw1Chunks = 4;                               // chunks of 2048 outputs per block
+constexpr int kDw1T = kDw1Out * kEltThreads * kDw1Chunks;   // outputs per block
 
 template <bool kQuant>
 __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned int* amax_bits,
                                                        uint8_t* __restrict__ dst) {
-    __shared__ __align__(16) int8_t win[kDw1T + 16];
+    constexpr int kWinBytes = kDw1T + 16;   // the block's outputs plus up to 8 taps, rounded
+    __shared__ uint32_t win32[(kWinBytes + 3) / 4 + 2];
     const int c = blockIdx.y;
     const int t0 = blockIdx.x * kDw1T;
     const int p0 = t0 - d.pad_l;
-    const int8_t* row = reinterpret_cast<const int8_t*>(d.x) + (int64_t)c * d.L;
-    for (int xo = threadIdx.x; xo < kDw1T + 16; xo += kEltThreads) {
-        const int pos = p0 + xo;
-        win[xo] = (pos >= 0 && pos < d.L) ? row[pos] : (int8_t)0;
-    }
+    const uint8_t* row = d.x + (int64_t)c * d.L;
+    const int sh = stage_window(row, d.L, p0, kWinBytes, win32, threadIdx.x, kEltThreads);
     const int8_t* wt = reinterpret_cast<const int8_t*>(d.w) + (int64_t)c * d.KW;
     uint32_t tw[2] = {0u, 0u};
     for (int k = 0; k < d.KW; ++k) tw[k >> 2] |= (uint32_t)(uint8_t)wt[k] << (8 * (k & 3));
@@ -569,37 +609,43 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     const float bc = d.bias ? d.bias[c] : 0.0f;
     float scale = 0.0f, inv = 0.0f;
     if (kQuant) quant_params(__uint_as_float(*amax_bits), scale, inv);
-    const int tl0 = kDw1Out * threadIdx.x;
-    // window bytes tl0 .. tl0+15 (tl0 is a multiple of 8: two 8-byte loads)
-    const uint2 wa = *reinterpret_cast<const uint2*>(win + tl0);
-    const uint2 wb = *reinterpret_cast<const uint2*>(win + tl0 + 8);
-    const uint32_t xw[4] = {wa.x, wa.y, wb.x, wb.y};
     float mx = 0.0f;
-    uint32_t packed[2] = {0u, 0u};
+    const bool aligned = ((((int64_t)c * d.OL) & 3) == 0);
+#pragma unroll 1
+    for (int chunk = 0; chunk < kDw1Chunks; ++chunk) {
+        const int tl0 = kDw1Out * (threadIdx.x + chunk * kEltThreads);
+        // window bytes tl0 .. tl0+15: five staged words shifted by sh
+        const int q0 = tl0 >> 2;
+        uint32_t xw[4];
 #pragma unroll
-    for (int e = 0; e < kDw1Out; ++e) {
-        const int q = e >> 2, r = e & 3;
-        const int x0 = (int)__funnelshift_r(xw[q], xw[q + 1], 8 * r);
-        const int x1 = (int)__funnelshift_r(xw[q + 1], xw[q + 2], 8 * r);
-        const int acc = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
-        float v = __fmul_rn(__int2float_rn(acc), sc);
-        if (d.bias) v = __fadd_rn(v, bc);
-        if (d.relu) v = v > 0.0f ? v : 0.0f;
-        const bool live = t0 + tl0 + e < d.OL;
-        if (kQuant) packed[q] |= (uint32_t)(quantize_one(v, inv) & 0xff) << (8 * r);
-        else if (live) mx = fmaxf(mx, fabsf(v));
+        for (int i = 0; i < 4; ++i) xw[i] = __funnelshift_r(win32[q0 + i], win32[q0 + i + 1], 8 * sh);
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < kDw1Out; ++e) {
+            const int q = e >> 2, r = e & 3;
+            const int x0 = (int)__funnelshift_r(xw[q], xw[q + 1], 8 * r);
+            const int x1 = (int)__funnelshift_r(xw[q + 1], xw[q + 2], 8 * r);
+            const int acc = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
+            float v = __fmul_rn(__int2float_rn(acc), sc);
+            if (d.bias) v = __fadd_rn(v, bc);
+            if (d.relu) v = v > 0.0f ? v : 0.0f;
+            const bool live = t0 + tl0 + e < d.OL;
+            if (kQuant) packed[q] |= (uint32_t)(quantize_one(v, inv) & 0xff) << (8 * r);
+            else if (live) mx = fmaxf(mx, fabsf(v));
+        }
+        if (kQuant) {
+            uint8_t* out = dst + (int64_t)c * d.OL + t0 + tl0;
+            if (aligned && t0 + tl0 + kDw1Out <= d.OL) {
+                reinterpret_cast<uint32_t*>(out)[0] = packed[0];
+                reinterpret_cast<uint32_t*>(out)[1] = packed[1];
+            } else {
+#pragma unroll
+                for (int e = 0; e < kDw1Out; ++e)
+                    if (t0 + tl0 + e < d.OL) out[e] = (uint8_t)(packed[e >> 2] >> (8 * (e & 3)));
+            }
+        }
     }
     if (kQuant) {
-        uint8_t* out = dst + (int64_t)c * d.OL + t0 + tl0;
-        const bool aligned = ((((int64_t)c * d.OL) & 3) == 0);
-        if (aligned && t0 + tl0 + kDw1Out <= d.OL) {
-            reinterpret_cast<uint32_t*>(out)[0] = packed[0];
-            reinterpret_cast<uint32_t*>(out)[1] = packed[1];
-        } else {
-#pragma unroll
-            for (int e = 0; e < kDw1Out; ++e)
-                if (t0 + tl0 + e < d.OL) out[e] = (uint8_t)(packed[e >> 2] >> (8 * (e & 3)));
-        }
         if (blockIdx.x == 0 && blockIdx.y == 0) write_trailer(dst, (int64_t)d.C * d.OL, scale);
     } else {
         fold_max(mx, amax_bits);
@@ -741,8 +787,13 @@ cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, 
 }
 
 cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s) {
-    const int64_t ta = (a + kTR - 1) / kTR, tb = (b + kTC - 1) / kTC;
-    k_transpose<<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    if (b >= 128) {
+        const int64_t ta = (a + 31) / 32, tb = (b + 127) / 128;
+        k_transpose<32, 128><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    } else {
+        const int64_t ta = (a + 127) / 128, tb = (b + 31) / 32;
+        k_transpose<128, 32><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    }
     return cudaGetLastError();
 }
 
@@ -750,14 +801,19 @@ cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW,
                                uint8_t* dst, cudaStream_t s) {
     // windowed kernel: T output positions per block (a multiple of 4, at most
     // 512) whose C windows fit in 48 KB of shared memory
+    // per channel 4*Wc bytes of staged words (W window bytes, up to 3 bytes of
+    // alignment shift, one spare word) and one shift word
     constexpr int64_t kWinBytes = 48 * 1024;
-    int64_t T = 0;
-    if (C * KW <= kWinBytes - 4) T = (((kWinBytes - 4) / C - KW) / stride + 1) & ~(int64_t)3;
-    if (T > 512) T = 512;
+    auto smem_for = [&](int64_t T_) {
+        const int64_t W_ = (T_ - 1) * stride + KW;
+        return C * (4 * ((W_ + 6) / 4 + 1) + 4);
+    };
+    int64_t T = 512;
+    while (T >= 4 && smem_for(T) > kWinBytes) T -= 4;
     if (T >= 4) {
         const int64_t W = (T - 1) * stride + KW;
         const int64_t blocks = (OL + T - 1) / T;
-        k_im2col_win<<<(unsigned)blocks, kEltThreads, (size_t)(C * W + 4), s>>>(src, (int)C, (int)L, KW, stride,
+        k_im2col_win<<<(unsigned)blocks, kEltThreads, (size_t)smem_for(T), s>>>(src, (int)C, (int)L, KW, stride,
                                                                                 pad_l, (int)OL, (int)T, (int)W, dst);
         return cudaGetLastError();
     }

@@ -296,3 +296,25 @@ def test_w8a8_packed_prefill_projection_sampled(i2s, o):
     got = host(d)
     for m0 in (0, 333, M - 8):
         same_bytes(got[m0:m0 + 8], o.w8a8_mul_mat(wq, bs, x[m0:m0 + 8], nth=8))
+
+
+def test_device_rounding_around_every_half_integer(i2s, o):
+    # amax = 127 makes inv = 127/127 = 1 exactly, so each code is round(y)
+    # itself: every float within 2000 ulps of k + 1/2 (k = 0..126), of the
+    # integers, and their negatives, against the CPU reference (C roundf)
+    pts = []
+    for k in range(128):
+        for centre in (k + 0.5, float(k)):
+            c = np.float32(centre)
+            lo, hi = c, c
+            for _ in range(2000):
+                lo = np.nextafter(lo, np.float32(-np.inf), dtype=np.float32)
+                hi = np.nextafter(hi, np.float32(np.inf), dtype=np.float32)
+                pts += [lo, hi]
+            pts.append(c)
+    y = np.array(pts, dtype=np.float32)
+    y = y[np.abs(y) <= 127.0]
+    y = np.concatenate([y, -y, np.array([127.0, -127.0], np.float32)])
+    got = host(i2s.i8s_requant(dev(y)))
+    ref = o.i8s_quantize(y)
+    same_bytes(got, ref)
