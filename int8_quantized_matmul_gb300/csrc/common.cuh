@@ -26,6 +26,12 @@ __device__ __forceinline__ int quantize_one(float x, float inv) {
     return v < 0.0f ? -m : m;
 }
 
+// int -> float exactly for |v| < 2^22 in two full-rate operations: v added to
+// the bit pattern of 1.5*2^23 (where the float step is 1), minus 1.5*2^23.
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f);
+}
+
 // int8 -> float exactly in two full-rate operations: the byte b + 128 placed
 // in the mantissa of 2^23 (XOR with 0x4B000080), minus 2^23 + 128.
 __device__ __forceinline__ float i8_to_float(int8_t b) {

@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, u
             const int8_t* xw = win + (tl0 + e) * d.stride;
             int acc = 0;
             for (int k = 0; k < d.KW; ++k) acc += (int)taps[k] * (int)xw[k];
-            float v = __fmul_rn(__int2float_rn(acc), sc);
+            float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
             if (d.bias) v = __fadd_rn(v, bc);
             if (d.relu) v = v > 0.0f ? v : 0.0f;
             if (kQuant) out[tl0 + e] = (uint8_t)(quantize_one(v, inv) & 0xff);
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
             const int x0 = (int)__funnelshift_r(xw[q], xw[q + 1], 8 * r);
             const int x1 = (int)__funnelshift_r(xw[q + 1], xw[q + 2], 8 * r);
             const int acc = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
-            float v = __fmul_rn(__int2float_rn(acc), sc);
+            float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
             if (d.bias) v = __fadd_rn(v, bc);
             if (d.relu) v = v > 0.0f ? v : 0.0f;
             const bool live = t0 + tl0 + e < d.OL;
@@ -800,7 +800,7 @@ cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8
 cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW, int stride, int pad_l, int64_t OL,
                                uint8_t* dst, cudaStream_t s) {
     // windowed kernel: T output positions per block (a multiple of 4, at most
-    // 512) whose C windows fit in 48 KB of shared memory
+    // 256) whose C windows fit in 48 KB of shared memory
     // per channel 4*Wc bytes of staged words (W window bytes, up to 3 bytes of
     // alignment shift, one spare word) and one shift word
     constexpr int64_t kWinBytes = 48 * 1024;
@@ -808,7 +808,7 @@ cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW,
         const int64_t W_ = (T_ - 1) * stride + KW;
         return C * (4 * ((W_ + 6) / 4 + 1) + 4);
     };
-    int64_t T = 512;
+    int64_t T = 256;   // more blocks per SM overlap one block's staging with another's stores
     while (T >= 4 && smem_for(T) > kWinBytes) T -= 4;
     if (T >= 4) {
         const int64_t W = (T - 1) * stride + KW;
