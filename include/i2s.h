@@ -264,6 +264,22 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
                          const float* bias, int relu, void* y_i8s, void* ws, size_t ws_bytes,
                          i2s_stream_t stream);
 
+/* Weights packed once (a load-time repack, as ggml's CPU backends repack weights
+ * for their kernels): i8s_pack_weights writes the f16 operand rows of an I8_S
+ * weight tensor (exact integers, N x K) followed by a 16-byte trailer holding
+ * its F32 scale: i8s_packed_bytes(N,K) bytes, 16-byte aligned, caller-owned.
+ * i8s_mul_mat_add_relu_packed then computes the same result as
+ * i8s_mul_mat_add_relu without converting the weights on every call; its
+ * workspace is i8s_mul_mat_packed_workspace(M,N,K) bytes (the F32 output
+ * before requantization is at the same offset). Requirements and errors as
+ * i8s_mul_mat_add_relu (BAD_ARG: the packed buffer overlaps the weights). */
+size_t i8s_packed_bytes(int64_t N, int64_t K);
+int i8s_pack_weights(const void* w_i8s, int64_t N, int64_t K, void* packed, i2s_stream_t stream);
+size_t i8s_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K);
+int i8s_mul_mat_add_relu_packed(const void* packed, int64_t N, int64_t K, const void* x_i8s, int64_t M,
+                                const float* bias, int relu, void* y_i8s, void* ws, size_t ws_bytes,
+                                i2s_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * F32 -> I8_S requantization with one scale for the whole tensor ([P1] "Two
  * new types", "Five fused INT8 ops"; [P3] Encoder): amax = max(max|y|, 1e-5),

@@ -562,6 +562,8 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
 
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+
 // I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
 // rows_pad x K][weights f16, N x K][split-tile int32 sums, half-tiles x chunks
 // slots of 160 x 128][half-tile tickets][half-tile slot masks]. A tile is 256
@@ -583,18 +585,12 @@ size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
            align_up(tiles * 8);
 }
 
-int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
-                         int relu, void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
-    if (!w_i8s || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
-    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
-    if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
-        return I2S_E_BAD_SHAPE;
-    if (!aligned16(w_i8s) || !aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) ||
-        (bias && ((uintptr_t)bias & 3u)))
-        return I2S_E_MISALIGNED;
-    if (ws_bytes < i8s_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
-    int r = check_device();
-    if (r) return r;
+// The I8_S call over f16 weight rows wf: either converted from w_i8s into the
+// workspace by this call's pre-pass (w_i8s set), or packed earlier (w_i8s
+// null, wf the caller's packed rows). w_scale points at the weight scale.
+static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_scale, int64_t N, int64_t K,
+                   const void* x_i8s, int64_t M, const float* bias, int relu, void* y_i8s, void* ws,
+                   i2s_stream_t stream) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
     uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
@@ -603,23 +599,23 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     const size_t tiles = (size_t)i8s_tiles(M, N);
     const size_t xf_off = kHeader + align_up((size_t)M * (size_t)N * 4);
     const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
-    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
+    const size_t part_off = wf_off + (w_i8s ? align_up((size_t)N * (size_t)K * 2) : 0);
     const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
     const size_t mask_off = tick_off + align_up(tiles * 4);
     const size_t zero_bytes = mask_off + align_up(tiles * 8) - tick_off;   // tickets and masks (slots need no clearing)
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
-    __half* wf = reinterpret_cast<__half*>(base + wf_off);
-    // pre-pass: weights and activations to f16 rows, once per call; clears the
-    // status and amax words and the split-tile sums and tickets
-    r = cuda_status(launch_i8s_to_f16(static_cast<const int8_t*>(w_i8s), (int)N, wf, static_cast<const int8_t*>(x_i8s),
-                                      (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes, status, amax,
-                                      stream));
+    const __half* wf = w_i8s ? reinterpret_cast<__half*>(base + wf_off) : wf_packed;
+    // pre-pass: weights (unless packed) and activations to f16 rows, once per
+    // call; clears the status and amax words and the split-tile tickets
+    int r = cuda_status(launch_i8s_to_f16(w_i8s, w_i8s ? (int)N : 0, reinterpret_cast<__half*>(base + wf_off),
+                                          static_cast<const int8_t*>(x_i8s), (int)M, (int)rows_pad, (int)K, xf,
+                                          base + tick_off, zero_bytes, status, amax, stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
     if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
-    a.w = static_cast<const int8_t*>(w_i8s);
-    a.w_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
+    a.w = w_i8s;
+    a.w_scale_ptr = w_scale;
     a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
     a.bias = bias;
     a.row_scale = nullptr;
@@ -644,6 +640,69 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
+}
+
+static int i8s_check(const void* w, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
+                     const void* y_i8s, const void* ws) {
+    if (!w || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
+    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
+    if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
+        return I2S_E_BAD_SHAPE;
+    if (!aligned16(w) || !aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) || (bias && ((uintptr_t)bias & 3u)))
+        return I2S_E_MISALIGNED;
+    return I2S_OK;
+}
+
+int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
+                         int relu, void* y_i8s, void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    int r = i8s_check(w_i8s, N, K, x_i8s, M, bias, y_i8s, ws);
+    if (r) return r;
+    if (ws_bytes < i8s_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    r = check_device();
+    if (r) return r;
+    const float* w_scale =
+        reinterpret_cast<const float*>(static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K));
+    return i8s_run(static_cast<const int8_t*>(w_i8s), nullptr, w_scale, N, K, x_i8s, M, bias, relu, y_i8s, ws, stream);
+}
+
+size_t i8s_packed_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 64 || K % 64 || K > kI8sMaxK || N * K >= ((int64_t)1 << 31)) return 0;
+    return (size_t)N * (size_t)K * 2 + 16;
+}
+
+int i8s_pack_weights(const void* w_i8s, int64_t N, int64_t K, void* packed, i2s_stream_t stream) {
+    if (!w_i8s || !packed) return I2S_E_NULL_PTR;
+    if (i8s_packed_bytes(N, K) == 0) return I2S_E_BAD_SHAPE;
+    if (!aligned16(w_i8s) || !aligned16(packed)) return I2S_E_MISALIGNED;
+    if (overlaps(w_i8s, i8s_nbytes(N * K), packed, i8s_packed_bytes(N, K))) return I2S_E_BAD_ARG;
+    int r = check_device();
+    if (r) return r;
+    uint8_t* dst = static_cast<uint8_t*>(packed);
+    r = cuda_status(launch_i8_to_f16(static_cast<const int8_t*>(w_i8s), N * K, reinterpret_cast<__half*>(dst), stream));
+    if (r) return r;
+    // the 16-byte trailer: the weight scale, then zeros
+    r = cuda_status(cudaMemsetAsync(dst + (size_t)N * K * 2, 0, 16, stream));
+    if (r) return r;
+    return cuda_status(cudaMemcpyAsync(dst + (size_t)N * K * 2, static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K),
+                                       4, cudaMemcpyDeviceToDevice, stream));
+}
+
+size_t i8s_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
+    const size_t full = i8s_mul_mat_workspace(M, N, K);
+    return full == 0 ? 0 : full - align_up((size_t)N * (size_t)K * 2);
+}
+
+int i8s_mul_mat_add_relu_packed(const void* packed, int64_t N, int64_t K, const void* x_i8s, int64_t M,
+                                const float* bias, int relu, void* y_i8s, void* ws, size_t ws_bytes,
+                                i2s_stream_t stream) {
+    int r = i8s_check(packed, N, K, x_i8s, M, bias, y_i8s, ws);
+    if (r) return r;
+    if (ws_bytes < i8s_mul_mat_packed_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
+    r = check_device();
+    if (r) return r;
+    const uint8_t* p = static_cast<const uint8_t*>(packed);
+    return i8s_run(nullptr, reinterpret_cast<const __half*>(p), reinterpret_cast<const float*>(p + (size_t)N * K * 2),
+                   N, K, x_i8s, M, bias, relu, y_i8s, ws, stream);
 }
 
 size_t i8s_requant_workspace(int64_t n) { return n < 1 ? 0 : kHeader; }

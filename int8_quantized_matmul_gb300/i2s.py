@@ -68,6 +68,10 @@ _SIGS = {
     "i8s_requant_workspace": (_sz, [_i64]),
     "i8s_requant": (_int, [_p, _i64, _p, _p, _sz, _p]),
     "i2s_read_status": (_int, [_p, _p]),
+    "i8s_packed_bytes": (_sz, [_i64, _i64]),
+    "i8s_pack_weights": (_int, [_p, _i64, _i64, _p, _p]),
+    "i8s_mul_mat_packed_workspace": (_sz, [_i64, _i64, _i64]),
+    "i8s_mul_mat_add_relu_packed": (_int, [_p, _i64, _i64, _p, _i64, _p, _int, _p, _p, _sz, _p]),
     "i8s_eltwise_workspace": (_sz, [_i64]),
     "i8s_add_scaled": (_int, [_p, _p, _i64, _p, _p, _sz, _p]),
     "i8s_rms_norm_scaled": (_int, [_p, _i64, _i64, _f32, _p, _p, _p, _sz, _p]),
@@ -278,6 +282,27 @@ def i8s_mul_mat_add_relu(w, N: int, K: int, x, M: int, bias=None, relu: bool = F
     _check("i8s_mul_mat_add_relu",
            _L.i8s_mul_mat_add_relu(_dptr(w), N, K, _dptr(x), M, _dptr(bias), 1 if relu else 0, _dptr(y), _dptr(ws),
                                    ws.numel(), _stream()))
+    return y, ws
+
+
+def i8s_pack_weights(w, N: int, K: int, packed=None):
+    """f16 operand rows of an I8_S weight tensor plus its scale, written once."""
+    if packed is None:
+        packed = _torch().empty(int(_L.i8s_packed_bytes(N, K)), dtype=_torch().uint8, device=w.device)
+    _check("i8s_pack_weights", _L.i8s_pack_weights(_dptr(w), N, K, _dptr(packed), _stream()))
+    return packed
+
+
+def i8s_mul_mat_add_relu_packed(packed, N: int, K: int, x, M: int, bias=None, relu: bool = False, y=None, ws=None):
+    """i8s_mul_mat_add_relu over weights packed once by i8s_pack_weights; returns (y, ws)."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(i8s_nbytes(M * N), dtype=torch.uint8, device=x.device)
+    if ws is None:
+        ws = _ws(int(_L.i8s_mul_mat_packed_workspace(M, N, K)), x.device)
+    _check("i8s_mul_mat_add_relu_packed",
+           _L.i8s_mul_mat_add_relu_packed(_dptr(packed), N, K, _dptr(x), M, _dptr(bias), 1 if relu else 0, _dptr(y),
+                                          _dptr(ws), ws.numel(), _stream()))
     return y, ws
 
 

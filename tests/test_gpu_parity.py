@@ -469,3 +469,34 @@ def test_i8s_encoder_fc_sampled(i2s, o, N, K, relu):
     v = (yf.reshape(-1) * inv).astype(np.float32).astype(np.float64)
     ref = np.clip(np.floor(np.abs(v) + 0.5) * np.sign(v), -127, 127).astype(np.int8)
     assert np.array_equal(q, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 64), (100, 300, 256), (130, 257, 1024), (300, 640, 4096)])
+@pytest.mark.parametrize("relu", [False, True])
+def test_i8s_packed_weights(i2s, o, M, N, K, relu):
+    # weights packed once (f16 rows + scale trailer), two calls on them
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=M + 2 * N + K)
+    packed = i2s.i8s_pack_weights(dev(wp), N, K)
+    ph = host(packed)
+    assert np.array_equal(ph[2 * N * K:2 * N * K + 16], wp[o.i8s_scale_offset(N * K):o.i8s_scale_offset(N * K) + 16])
+    y8, ws = i2s.i8s_mul_mat_add_relu_packed(packed, N, K, dev(xp), M, bias=dev(bias), relu=relu)
+    assert i2s.read_status(ws) == 0
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, relu=relu, nth=4)
+    same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+    same_bits(host(y8), oy8)
+    xp2 = o.i8s_quantize(synth.normal_f32((M, K), seed=M + 5))
+    y8b, _ = i2s.i8s_mul_mat_add_relu_packed(packed, N, K, dev(xp2), M, bias=dev(bias), relu=relu, ws=ws)
+    same_bits(host(y8b), o.i8s_mul_mat_add(wp, N, K, xp2, M, bias=bias, relu=relu, nth=4)[0])
+
+
+def test_i8s_packed_encoder_fc1_sampled(i2s, o):
+    M, N, K = 900, 8192, 2048
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=N + 1)
+    packed = i2s.i8s_pack_weights(dev(wp), N, K)
+    y8, ws = i2s.i8s_mul_mat_add_relu_packed(packed, N, K, dev(xp), M, bias=dev(bias), relu=True)
+    yf = host(i2s.i8s_ws_f32(ws, M, N))
+    q_all, x_scale = o.i8s_unpack(xp, M * K)
+    for m0 in (0, 449, M - 8):
+        sub = o.i8s_pack(q_all.reshape(M, K)[m0:m0 + 8], x_scale)
+        _, oyf = o.i8s_mul_mat_add(wp, N, K, sub, 8, bias=bias, relu=True, nth=8)
+        same_bits(yf[m0:m0 + 8], oyf)
