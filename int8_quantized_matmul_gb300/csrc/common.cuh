@@ -65,6 +65,16 @@ __host__ __device__ constexpr uint8_t e4m3_times16(int v) {
 static_assert(e4m3_small_int(1) == 0x38 && e4m3_small_int(3) == 0x44 && e4m3_small_int(15) == 0x57, "e4m3");
 static_assert(e4m3_times16(-8) == 0xF0 && e4m3_times16(7) == 0x6E, "e4m3 x16");
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization is scheduled as the CTAs of the kernel before it on the
+// stream retire, instead of after that kernel's completion is processed;
+// pdl_wait blocks until the previous kernel has completed and its memory is
+// visible. A no-op in a kernel launched without the attribute. (An explicit
+// early trigger, griddepcontrol.launch_dependents, made the decode step
+// slower: the GEMV's CTAs then took SM resources while the quantization
+// kernel was still running.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

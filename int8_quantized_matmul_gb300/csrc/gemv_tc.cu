@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    // everything above touched only parameters, shared memory and TMEM; the
+    // workspace (operands, weight maps, partial sums) is read from here on,
+    // after the quantization launch before this one has completed
+    pdl_wait();
 
     int ucur = u_begin;   // each role advances its own copy of the unit cursor
     auto next_seg = [&](const Seg& g) { ucur += g.units; return seg_next(sp, g, ucur, u_end); };
@@ -592,11 +596,19 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    if (a.BN == 8)
-        k_i2s_gemv_tc<8><<<grid, kThreadsGv, kSmemGvBytes, s>>>(a);
-    else
-        k_i2s_gemv_tc<16><<<grid, kThreadsGv, kSmemGvBytes, s>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the quantization launch before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreadsGv, 1, 1);
+    cfg.dynamicSmemBytes = kSmemGvBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.BN == 8) return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<8>, a);
+    return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<16>, a);
 }
 
 }  // namespace i2s

@@ -275,7 +275,11 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
     __shared__ int s_sum[kQThreads / 32];
     __shared__ uint32_t s_code[255];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // launched as a programmatic dependent of the kernel before it: wait for
+    // that kernel (which may use the same workspace, or produce x) before
+    // reading or writing global memory
     if (tid < 255) s_code[tid] = digit_code(tid - 127);
+    pdl_wait();
     if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
     // map i is written by thread i / gridDim.x of CTA i % gridDim.x: one or two
     // maps per CTA instead of all of them in the first CTA, whose row work
@@ -340,9 +344,19 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
 }
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
-    if (a.layout == kQuantE2M1Tc)
-        k_quant_rows_tc4<<<a.count * a.M, kQThreads, 0, s>>>(a);
-    else
+    if (a.layout == kQuantE2M1Tc) {
+        // the decode path: a programmatic dependent of the kernel before it
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(a.count * a.M), 1, 1);
+        cfg.blockDim = dim3(kQThreads, 1, 1);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_quant_rows_tc4, a);
+    } else
         k_quant_rows<<<a.count * a.rows, kQThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
