@@ -400,6 +400,31 @@ size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K);
 int w8a8_mul_mat_packed(const void* packed, const float* bscale, int64_t N, int64_t K, const float* x,
                         int64_t M, float* d, void* ws, size_t ws_bytes, i2s_stream_t stream);
 
+/* Several packed W8A8 matmuls with the same M in two launches: one quantizes
+ * every distinct activation (problems whose x pointer and K are equal share
+ * it, as q, k and v do), one tensor-core GEMM covers every matmul, so small
+ * projections share the GPU instead of each leaving most SMs idle. Results are
+ * those of w8a8_mul_mat_packed for each problem, bit for bit.
+ * probs  host array of `count` problems (1 .. W8A8_MAX_GROUP); read during the
+ *        call only. Per problem as w8a8_mul_mat_packed.
+ * ws     device workspace of at least w8a8_mul_mat_grouped_workspace() bytes,
+ *        256-byte aligned.
+ * Errors: as w8a8_mul_mat_packed, plus BAD_ARG for count out of range. */
+#define W8A8_MAX_GROUP 8
+
+typedef struct w8a8_problem {
+    const void* packed;   /* device, w8a8_pack_weights output (N x K) */
+    const float* bscale;  /* device, N per-channel weight scales */
+    int64_t N;
+    int64_t K;
+    const float* x;       /* device, M x K F32 activations */
+    float* d;             /* device, M x N F32 output */
+} w8a8_problem;
+
+size_t w8a8_mul_mat_grouped_workspace(const w8a8_problem* probs, int count, int64_t M);
+int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                         i2s_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Device status. Kernels with bounded waits (the tensor-core pipelines) never
  * trap: when a wait runs out they record a code in the status word at the

@@ -612,28 +612,32 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
                                           base + tick_off, zero_bytes, status, amax, stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
-    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
-    if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
-    a.w = w_i8s;
-    a.w_scale_ptr = w_scale;
-    a.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
-    a.bias = bias;
-    a.row_scale = nullptr;
-    a.col_scale = nullptr;
-    a.y = yf;
+    I8sProb& P = a.p[0];
+    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&P.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
+    P.w_scale_ptr = w_scale;
+    P.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
+    P.bias = bias;
+    P.row_scale = nullptr;
+    P.col_scale = nullptr;
+    P.y = yf;
+    P.slot0 = 0;
+    P.N = (int)N;
+    P.K = (int)K;
+    P.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));   // 256-feature tiles
+    P.chunks = (int)i8s_chunks(K);
+    P.unit0 = 0;
+    P.ht0 = 0;
+    a.count = 1;
     a.amax_bits = amax;
     a.part = reinterpret_cast<int32_t*>(base + part_off);
     a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
     a.slot_masks = reinterpret_cast<unsigned long long*>(base + mask_off);
     a.status = status;
     a.M = (int)M;
-    a.N = (int)N;
-    a.K = (int)K;
     a.relu = relu ? 1 : 0;
-    a.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));   // 256-feature tiles
     a.n_at = (int)(rows_pad / kI8sTileM);
-    a.chunks = (int)i8s_chunks(K);
-    a.total_units = (int)(tiles / 2) * a.chunks;   // units of whole (256-feature) tiles
+    a.total_units = (int)(tiles / 2) * P.chunks;   // units of whole (256-feature) tiles
     int pairs = i8s_gemm_tc_max_pairs();   // resident pairs: a persistent grid, no second wave
     if (pairs > a.total_units) pairs = a.total_units;
     const int grid = 2 * pairs;   // clusters of two CTAs
@@ -853,28 +857,32 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
     const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
     const size_t mask_off = tick_off + align_up(tiles * 4);
     static thread_local I8sTcArgs a;
-    if (!make_f16_operand_map(&a.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
-    if (!make_f16_operand_map(&a.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
-    a.w = nullptr;
-    a.w_scale_ptr = bscale;   // read by the kernel's I8_S prologue; the W8A8 epilogue uses the arrays
-    a.x_scale_ptr = ascale;
-    a.bias = nullptr;
-    a.row_scale = ascale;
-    a.col_scale = bscale;
-    a.y = d;
+    I8sProb& P = a.p[0];
+    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&P.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
+    P.w_scale_ptr = bscale;   // read by the kernel's I8_S path; the W8A8 epilogue uses the arrays
+    P.x_scale_ptr = ascale;
+    P.bias = nullptr;
+    P.row_scale = ascale;
+    P.col_scale = bscale;
+    P.y = d;
+    P.slot0 = 0;
+    P.N = (int)N;
+    P.K = (int)K;
+    P.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
+    P.chunks = (int)i8s_chunks(K);
+    P.unit0 = 0;
+    P.ht0 = 0;
+    a.count = 1;
     a.amax_bits = reinterpret_cast<unsigned int*>(base + kAmaxOff);
     a.part = reinterpret_cast<int32_t*>(base + part_off);
     a.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
     a.slot_masks = reinterpret_cast<unsigned long long*>(base + mask_off);
     a.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     a.M = (int)M;
-    a.N = (int)N;
-    a.K = (int)K;
     a.relu = 0;
-    a.n_wt = (int)((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
     a.n_at = (int)(rows_pad / kI8sTileM);
-    a.chunks = (int)i8s_chunks(K);
-    a.total_units = (int)(tiles / 2) * a.chunks;
+    a.total_units = (int)(tiles / 2) * P.chunks;
     int pairs = i8s_gemm_tc_max_pairs();
     if (pairs > a.total_units) pairs = a.total_units;
     return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
@@ -952,39 +960,153 @@ int w8a8_pack_weights(const int8_t* wq, int64_t N, int64_t K, void* packed, i2s_
     return cuda_status(launch_i8_to_f16(wq, N * K, static_cast<__half*>(packed), stream));
 }
 
-// Packed W8A8 workspace: [header: status, amax][row scales, M F32]
-// [activations f16, rows_pad x K][split-tile slots, tickets, masks].
+// Packed W8A8 calls, one matmul or a group of them with the same M. Workspace:
+// [header: status, amax][per distinct activation (x, K): row scales, M F32;
+// f16 operand rows, rows_pad x K][split-tile slots of every matmul][half-tile
+// tickets][half-tile slot masks]. Matmuls whose x pointer and K are equal
+// share one quantized activation.
+namespace {
+struct W8a8Plan {
+    int n_act = 0;
+    int act_of[kI8sMaxGroup];
+    size_t act_off[kI8sMaxGroup];   // row scales; the f16 rows follow at align_up(M * 4)
+    size_t slots = 0, tiles = 0;    // slots (kI8sTileM x kI8sTileN int32 each), half-tiles
+    size_t part_off = 0, tick_off = 0, mask_off = 0, end = 0;
+};
+}  // namespace
+
+static_assert(kI8sMaxGroup == W8A8_MAX_GROUP, "one GEMM launch holds every matmul of a group");
+
+static W8a8Plan w8a8_plan(const w8a8_problem* probs, int count, int64_t M) {
+    W8a8Plan pl;
+    const int64_t rows_pad = i8s_rows_pad(M);
+    size_t off = kHeader;
+    for (int i = 0; i < count; ++i) {
+        int a = -1;
+        for (int j = 0; j < i; ++j)
+            if (probs[j].x == probs[i].x && probs[j].K == probs[i].K) { a = pl.act_of[j]; break; }
+        if (a < 0) {
+            a = pl.n_act++;
+            pl.act_off[a] = off;
+            off += align_up((size_t)M * 4) + align_up((size_t)rows_pad * (size_t)probs[i].K * 2);
+        }
+        pl.act_of[i] = a;
+        const size_t ht = (size_t)i8s_tiles(M, probs[i].N);
+        pl.tiles += ht;
+        pl.slots += ht * (size_t)i8s_chunks(probs[i].K);
+    }
+    pl.part_off = off;
+    pl.tick_off = pl.part_off + align_up(pl.slots * kI8sTileN * kI8sTileM * 4);
+    pl.mask_off = pl.tick_off + align_up(pl.tiles * 4);
+    pl.end = pl.mask_off + align_up(pl.tiles * 8);
+    return pl;
+}
+
+static int w8a8_group_ok(const w8a8_problem* probs, int count, int64_t M) {
+    if (!probs) return I2S_E_NULL_PTR;
+    if (count < 1 || count > W8A8_MAX_GROUP) return I2S_E_BAD_ARG;
+    int64_t units = 0;
+    for (int i = 0; i < count; ++i) {
+        const w8a8_problem& q = probs[i];
+        if (!q.packed || !q.bscale || !q.x || !q.d) return I2S_E_NULL_PTR;
+        if (!w8a8_shape_ok(M, q.N, q.K)) return I2S_E_BAD_SHAPE;
+        if (!aligned16(q.packed) || !aligned16(q.x) || !aligned16(q.d) || ((uintptr_t)q.bscale & 3u))
+            return I2S_E_MISALIGNED;
+        units += (int64_t)i8s_tiles(M, q.N) / 2 * i8s_chunks(q.K);
+    }
+    return units < ((int64_t)1 << 30) ? I2S_OK : I2S_E_BAD_SHAPE;
+}
+
+size_t w8a8_mul_mat_grouped_workspace(const w8a8_problem* probs, int count, int64_t M) {
+    if (w8a8_group_ok(probs, count, M) != I2S_OK) return 0;
+    return w8a8_plan(probs, count, M).end;
+}
+
+int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                         i2s_stream_t stream) {
+    int r = w8a8_group_ok(probs, count, M);
+    if (r) return r;
+    if (!ws) return I2S_E_NULL_PTR;
+    if (!aligned256(ws)) return I2S_E_MISALIGNED;
+    const W8a8Plan pl = w8a8_plan(probs, count, M);
+    if (ws_bytes < pl.end) return I2S_E_WORKSPACE_TOO_SMALL;
+    r = check_device();
+    if (r) return r;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const int64_t rows_pad = i8s_rows_pad(M);
+    // one launch quantizes every distinct activation into its f16 operand
+    // rows (and clears the status, amax and split-tile counters)
+    static thread_local W8a8RowJobs J;
+    J.count = pl.n_act;
+    J.M = (int)M;
+    J.rows_pad = (int)rows_pad;
+    for (int i = 0; i < count; ++i) {
+        const int a = pl.act_of[i];
+        J.x[a] = probs[i].x;
+        J.K[a] = (int)probs[i].K;
+        J.ascale[a] = reinterpret_cast<float*>(base + pl.act_off[a]);
+        J.xf[a] = reinterpret_cast<__half*>(base + pl.act_off[a] + align_up((size_t)M * 4));
+    }
+    J.zero = reinterpret_cast<uint4*>(base + pl.tick_off);
+    J.zero_16 = (pl.end - pl.tick_off) / 16;
+    J.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+    J.amax_bits = reinterpret_cast<unsigned int*>(base + kAmaxOff);
+    r = cuda_status(launch_w8a8_rows_f16(J, stream));
+    if (r) return r;
+    // one tensor-core GEMM over every matmul, units numbered matmul by matmul
+    static thread_local I8sTcArgs a;
+    int units = 0, ht = 0;
+    long long slot = 0;
+    for (int i = 0; i < count; ++i) {
+        const w8a8_problem& q = probs[i];
+        I8sProb& P = a.p[i];
+        const int act = pl.act_of[i];
+        if (!make_f16_operand_map(&P.xmap, J.xf[act], (int)rows_pad, (int)q.K, kI8sTileM / 2)) return I2S_E_CUDA;
+        if (!make_f16_operand_map(&P.wmap, q.packed, (int)q.N, (int)q.K, kI8sTileN)) return I2S_E_CUDA;
+        P.w_scale_ptr = q.bscale;   // read by the kernel's I8_S path; the W8A8 epilogue uses the arrays
+        P.x_scale_ptr = J.ascale[act];
+        P.bias = nullptr;
+        P.row_scale = J.ascale[act];
+        P.col_scale = q.bscale;
+        P.y = q.d;
+        P.N = (int)q.N;
+        P.K = (int)q.K;
+        P.n_wt = (int)((q.N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
+        P.chunks = (int)i8s_chunks(q.K);
+        P.unit0 = units;
+        P.ht0 = ht;
+        P.slot0 = slot;
+        const int tiles_i = (int)i8s_tiles(M, q.N);   // half-tiles
+        units += tiles_i / 2 * P.chunks;
+        ht += tiles_i;
+        slot += (long long)tiles_i * P.chunks;
+    }
+    a.count = count;
+    a.amax_bits = J.amax_bits;
+    a.part = reinterpret_cast<int32_t*>(base + pl.part_off);
+    a.tickets = reinterpret_cast<uint32_t*>(base + pl.tick_off);
+    a.slot_masks = reinterpret_cast<unsigned long long*>(base + pl.mask_off);
+    a.status = J.status;
+    a.M = (int)M;
+    a.relu = 0;
+    a.n_at = (int)(rows_pad / kI8sTileM);
+    a.total_units = units;
+    int pairs = i8s_gemm_tc_max_pairs();
+    if (pairs > units) pairs = units;
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
+}
+
 size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
     if (!w8a8_shape_ok(M, N, K)) return 0;
-    return kHeader + align_up((size_t)M * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
-           w8a8_split_bytes(M, N, K);
+    const w8a8_problem q{reinterpret_cast<const void*>(16), reinterpret_cast<const float*>(16), N, K,
+                         reinterpret_cast<const float*>(16), reinterpret_cast<float*>(16)};
+    return w8a8_plan(&q, 1, M).end;
 }
 
 int w8a8_mul_mat_packed(const void* packed, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M,
                         float* d, void* ws, size_t ws_bytes, i2s_stream_t stream) {
-    if (!packed || !bscale || !x || !d || !ws) return I2S_E_NULL_PTR;
-    if (!w8a8_shape_ok(M, N, K)) return I2S_E_BAD_SHAPE;
-    if (!aligned16(packed) || !aligned16(x) || !aligned16(d) || !aligned256(ws) || ((uintptr_t)bscale & 3u))
-        return I2S_E_MISALIGNED;
-    if (ws_bytes < w8a8_mul_mat_packed_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
-    int r = check_device();
-    if (r) return r;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    float* ascale = reinterpret_cast<float*>(base + kHeader);
-    const int64_t rows_pad = i8s_rows_pad(M);
-    const size_t xf_off = kHeader + align_up((size_t)M * 4);
-    const size_t part_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
-    const size_t tiles = (size_t)i8s_tiles(M, N);
-    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
-    const size_t zero_bytes = w8a8_split_bytes(M, N, K) - (tick_off - part_off);
-    __half* xf = reinterpret_cast<__half*>(base + xf_off);
-    // rows straight into f16 operand rows (the launch also clears the status,
-    // amax and split-tile counters), then the GEMM
-    r = cuda_status(launch_w8a8_rows_f16(x, M, rows_pad, K, xf, ascale, base + tick_off, zero_bytes,
-                                         reinterpret_cast<uint32_t*>(base + kStatusOff),
-                                         reinterpret_cast<unsigned int*>(base + kAmaxOff), stream));
-    if (r) return r;
-    return launch_w8a8_gemm(static_cast<const __half*>(packed), bscale, ascale, xf, N, K, M, d, base, part_off, stream);
+    const w8a8_problem q{packed, bscale, N, K, x, d};
+    return w8a8_mul_mat_grouped(&q, 1, M, ws, ws_bytes, stream);
 }
 
 int i2s_read_status(void* ws, i2s_stream_t stream) {

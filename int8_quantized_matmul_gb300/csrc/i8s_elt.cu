@@ -697,29 +697,30 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_weights(const float* __res
     }
 }
 
-// The packed W8A8 call: rows_pad blocks; block m < M quantizes row m (1e-9
-// floor) straight into the GEMM's f16 operand row (exact integers) and its
-// scale, blocks m >= M write zero rows. The same launch clears the status word,
-// the amax word and the GEMM's split-tile counters.
-__global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const float* __restrict__ x, int64_t M, int64_t K,
-                                                               __half* __restrict__ xf, float* __restrict__ ascale,
-                                                               uint4* zero, unsigned long long zero_16,
-                                                               uint32_t* status, unsigned int* amax_bits) {
+// The packed W8A8 calls' row quantizer: one block per operand row of each
+// distinct activation (rows_pad rows each); a block with m < M quantizes row m
+// (1e-9 floor) straight into the GEMM's f16 operand row (exact integers) and
+// its scale, a block with m >= M writes a zero row. The same launch clears the
+// status word, the amax word and the GEMM's split-tile counters.
+__global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_constant__ W8a8RowJobs J) {
     __shared__ float s_max[kEltThreads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *status = 0u;
-        *amax_bits = 0u;
+        *J.status = 0u;
+        *J.amax_bits = 0u;
     }
-    for (unsigned long long i = blockIdx.x * (unsigned long long)kEltThreads + threadIdx.x; i < zero_16;
+    for (unsigned long long i = blockIdx.x * (unsigned long long)kEltThreads + threadIdx.x; i < J.zero_16;
          i += (unsigned long long)gridDim.x * kEltThreads)
-        zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    const int64_t m = blockIdx.x;
-    __half* out = xf + m * K;
-    if (m >= M) {
+        J.zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    int j = 0;
+    while (j + 1 < J.count && (int)blockIdx.x >= (j + 1) * J.rows_pad) ++j;
+    const int64_t m = (int64_t)blockIdx.x - (int64_t)j * J.rows_pad;
+    const int64_t K = J.K[j];
+    __half* out = J.xf[j] + m * K;
+    if (m >= J.M) {
         for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __float2half_rn(0.0f);
         return;
     }
-    const float* xr = x + m * K;
+    const float* xr = J.x[j] + m * K;
     float mx = 0.0f;
     for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
     mx = warp_max(mx);
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const float* __re
     for (int i = 1; i < kEltThreads / 32; ++i) mx = fmaxf(mx, s_max[i]);
     mx = fmaxf(mx, 1e-9f);
     const float inv = __fdiv_rn(127.0f, mx);
-    if (threadIdx.x == 0) ascale[m] = __fdiv_rn(mx, 127.0f);
+    if (threadIdx.x == 0) J.ascale[j][m] = __fdiv_rn(mx, 127.0f);
     for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_one(xr[k], inv));
 }
 
@@ -851,11 +852,8 @@ cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, fl
     return cudaGetLastError();
 }
 
-cudaError_t launch_w8a8_rows_f16(const float* x, int64_t M, int64_t rows_pad, int64_t K, __half* xf, float* ascale,
-                                 void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
-                                 cudaStream_t s) {
-    k_w8a8_rows_f16<<<(unsigned)rows_pad, kEltThreads, 0, s>>>(x, M, K, xf, ascale, static_cast<uint4*>(zero),
-                                                                zero_bytes / 16, status, amax_bits);
+cudaError_t launch_w8a8_rows_f16(const W8a8RowJobs& J, cudaStream_t s) {
+    k_w8a8_rows_f16<<<(unsigned)(J.count * J.rows_pad), kEltThreads, 0, s>>>(J);
     return cudaGetLastError();
 }
 

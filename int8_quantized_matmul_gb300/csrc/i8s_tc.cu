@@ -105,9 +105,10 @@ struct Smem8 {
 
 constexpr size_t kSmem8Bytes = 1024 + (size_t)kStages8 * (kAStage8 + kBStage8) + sizeof(Smem8);
 
-// The part of the unit range [u, u_hi) that lies in one tile.
+// The part of the unit range [u, u_hi) that lies in one tile of matmul p.
+// Units are numbered matmul by matmul, tile-major within each.
 struct Seg8 {
-    int tile, wt, at, c_lo, c_hi, units;
+    int p, tile, wt, at, c_lo, c_hi, units;
     bool live;
 };
 
@@ -115,9 +116,13 @@ __device__ __forceinline__ Seg8 seg8_at(const I8sTcArgs& a, int u, int u_hi) {
     Seg8 g;
     g.live = u < u_hi;
     if (!g.live) return g;
-    g.tile = u / a.chunks;
-    g.c_lo = u - g.tile * a.chunks;
-    g.c_hi = min(a.chunks, g.c_lo + (u_hi - u));
+    g.p = 0;
+    while (g.p + 1 < a.count && a.p[g.p + 1].unit0 <= u) ++g.p;
+    const int chunks = a.p[g.p].chunks;
+    const int local = u - a.p[g.p].unit0;
+    g.tile = local / chunks;
+    g.c_lo = local - g.tile * chunks;
+    g.c_hi = min(chunks, g.c_lo + (u_hi - u));
     g.units = g.c_hi - g.c_lo;
     g.wt = g.tile / a.n_at;
     g.at = g.tile - g.wt * a.n_at;
@@ -151,9 +156,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
     const int u_begin = (int)(((long long)pair * a.total_units) / n_pairs);
     const int u_end = (int)(((long long)(pair + 1) * a.total_units) / n_pairs);
     // stages of 128 positions; with K % 128 == 64 the last stage's second atom
-    // is zero (the converters write zeros, the TMA box lies past K and is
-    // zero-filled), which adds nothing to the dot products
-    const int KB = (a.K + kKB8 - 1) / kKB8;
+    // lies past K, where the TMA box is zero-filled, which adds nothing to the
+    // dot products
+    auto stages_of = [&](int p) { return (a.p[p].K + kKB8 - 1) / kKB8; };
 
     if (tid == 0) {
         for (int s = 0; s < kStages8; ++s) {
@@ -176,8 +181,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
         tc::pair_tmem_relinquish();
     }
     if (warp == kTmaWarp8 && lane == 0) {
-        tc::tma_prefetch_desc(&a.xmap);
-        tc::tma_prefetch_desc(&a.wmap);
+        for (int i = 0; i < a.count; ++i) {
+            tc::tma_prefetch_desc(&a.p[i].xmap);
+            tc::tma_prefetch_desc(&a.p[i].wmap);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -217,7 +224,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             uint32_t pending_phase[kStages8] = {};
             bool ok = true;
             for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
-                const int kb_hi = min(KB, g.c_hi * kStagesPerChunk);
+                const CUtensorMap* wmap = &a.p[g.p].wmap;
+                const CUtensorMap* xmap = &a.p[g.p].xmap;
+                const int kb_hi = min(stages_of(g.p), g.c_hi * kStagesPerChunk);
                 const int wrow = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN;   // this CTA's weight rows
                 const int xrow = g.at * kI8sTileM + (int)rank * kBRows8;           // this CTA's activation rows
                 for (int kb = g.c_lo * kStagesPerChunk; kb < kb_hi; ++kb) {
@@ -228,10 +237,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                     uint8_t* da = sA + (size_t)stage * kAStage8;
                     uint8_t* db = sB + (size_t)stage * kBStage8;
                     const int x0 = kb * kKB8;
-                    tc::pair_tma_load_2d(da, &a.wmap, x0, wrow, full_bar);
-                    tc::pair_tma_load_2d(da + kAAtomBytes, &a.wmap, x0 + 64, wrow, full_bar);
-                    tc::pair_tma_load_2d(db, &a.xmap, x0, xrow, full_bar);
-                    tc::pair_tma_load_2d(db + kBAtomBytes, &a.xmap, x0 + 64, xrow, full_bar);
+                    tc::pair_tma_load_2d(da, wmap, x0, wrow, full_bar);
+                    tc::pair_tma_load_2d(da + kAAtomBytes, wmap, x0 + 64, wrow, full_bar);
+                    tc::pair_tma_load_2d(db, xmap, x0, xrow, full_bar);
+                    tc::pair_tma_load_2d(db + kBAtomBytes, xmap, x0 + 64, xrow, full_bar);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
                     if (++stage == kStages8) { stage = 0; phase ^= 1; }
@@ -258,6 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             int seq = 0;
             bool ok = true;
             for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
+                const int KB = stages_of(g.p);
                 for (int c = g.c_lo; ok && c < g.c_hi; ++c) {
                     if (!tc::mbar_wait_spin(&S.tmem_empty[buf], buf_phase ^ 1, abort_flag, kWaitLimit8)) { fail(4); ok = false; break; }
                     tc::tc_fence_after();
@@ -296,14 +306,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
         const uint32_t lane_off = ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
         int buf = 0;
         uint32_t buf_phase = 0, sync_phase = 0;
-        const float sc = __fmul_rn(*a.w_scale_ptr, *a.x_scale_ptr);
-        float* const yb = a.y;
-        const int M = a.M, N = a.N;
-        const bool has_bias = a.bias != nullptr, relu = a.relu != 0;
-        const bool w8a8 = a.col_scale != nullptr;   // per-row / per-channel scales, no bias or ReLU
+        const int M = a.M;
+        const bool relu = a.relu != 0;
         float local_max = 0.0f;
         bool ok = true;
         for (Seg8 g = seg8_at(a, ucur, u_end); ok && g.live; g = next_seg(g)) {
+            const I8sProb& P = a.p[g.p];
+            const float sc = __fmul_rn(*P.w_scale_ptr, *P.x_scale_ptr);
+            float* const yb = P.y;
+            const int N = P.N, chunks = P.chunks;
+            const bool has_bias = P.bias != nullptr;
+            const bool w8a8 = P.col_scale != nullptr;   // per-row / per-channel scales, no bias or ReLU
             // drain each chunk's f32 accumulator (exact integers) into the int32 sums
             for (int c = g.c_lo; c < g.c_hi; ++c) {
                 if (!tc::mbar_wait_idle(&S.tmem_full[buf], buf_phase, abort_flag, kWaitLimit8)) { fail(16); ok = false; break; }
@@ -331,12 +344,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             }
             if (!ok) break;
             const int n = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN + r;
-            const int ht = 2 * g.tile + (int)rank;   // this CTA's half of the tile: its slots, ticket and mask
+            const int ht = P.ht0 + 2 * g.tile + (int)rank;   // this CTA's half of the tile: its ticket and mask
             const int m0 = g.at * kI8sTileM + c0;     // first activation row of this warp's columns
             const uint32_t scol = tmem_base + lane_off + kSCol8;
             constexpr size_t kSlot = (size_t)kI8sTileM * kI8sTileN;   // one segment's int32 sums
-            int32_t* slots = a.part + (size_t)ht * a.chunks * kSlot + (size_t)c0 * kI8sTileN;
-            bool write = g.c_lo == 0 && g.c_hi == a.chunks;
+            int32_t* slots = a.part + ((size_t)P.slot0 + (size_t)(2 * g.tile + (int)rank) * chunks) * kSlot +
+                             (size_t)c0 * kI8sTileN;
+            bool write = g.c_lo == 0 && g.c_hi == chunks;
             unsigned long long others = 0;   // slots of the tile's other segments (final CTA)
             if (!write) {
                 // this CTA holds only some chunks of the tile: store its exact
@@ -360,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                     const unsigned long long seen = atomicOr(&a.slot_masks[ht], bit) | bit;
                     __threadfence();
                     const unsigned prev = atomicAdd(&a.tickets[ht], (unsigned)g.units);
-                    const bool last = prev + (unsigned)g.units == (unsigned)a.chunks;
+                    const bool last = prev + (unsigned)g.units == (unsigned)chunks;
                     // every other segment set its bit before adding to the ticket
                     S.final_mask = last ? (atomicOr(&a.slot_masks[ht], 0ull) | seen) & ~bit : 0ull;
                     S.final_flag = last;
@@ -373,8 +387,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                 if (write) __threadfence();
             }
             if (write) {
-                const float bn = (has_bias && n < N) ? a.bias[n] : 0.0f;
-                const float bs_n = (w8a8 && n < N) ? a.col_scale[n] : 0.0f;
+                const float bn = (has_bias && n < N) ? P.bias[n] : 0.0f;
+                const float bs_n = (w8a8 && n < N) ? P.col_scale[n] : 0.0f;
 #pragma unroll 1
                 for (int h = 0; h < kESlices8; ++h) {
                     uint32_t s[16];
@@ -394,7 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                         // d = (as[m] * bs[n]) * (float)acc
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float as = a.row_scale[min(m0 + 16 * h + j, M - 1)];
+                            const float as = P.row_scale[min(m0 + 16 * h + j, M - 1)];
                             v[j] = __fmul_rn(__fmul_rn(as, bs_n), __int2float_rn((int)s[j]));
                         }
                     } else if (has_bias) {

@@ -157,24 +157,36 @@ constexpr int kI8sTileM = 160;   // activation rows per tile: the MMA N
 constexpr int kI8sChunkK = 1024;
 constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask of a split tile)
 
-struct I8sTcArgs {
+// One matmul of a launch: its operand maps, scales, output and offsets into
+// the launch's split-tile areas.
+constexpr int kI8sMaxGroup = 8;
+struct I8sProb {
     CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM / 2, 128-byte swizzle
     CUtensorMap wmap;          // f16 weights, N x K, box 64 x kI8sTileN, 128-byte swizzle
-    const int8_t* w;           // N x K
-    const float* w_scale_ptr;
+    const float* w_scale_ptr;  // I8_S: the weight and activation scales (W8A8: any valid floats)
     const float* x_scale_ptr;
     const float* bias;         // N or null
     float* y;                  // M x N F32
-    unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass)
     const float* row_scale;    // W8A8 only (col_scale set): per-row activation scales, M
     const float* col_scale;    // W8A8 only: per-channel weight scales, N; null for I8_S
-    int32_t* part;             // split tiles: half-tiles x chunks slots of kI8sTileM x kI8sTileN int32 sums
+    long long slot0;           // first split-tile slot (kI8sTileM x kI8sTileN int32 sums) of this matmul
+    int N, K;
+    int n_wt, chunks;          // n_wt: 256-feature tiles (a CTA pair each); chunks: ceil(K / kI8sChunkK)
+    int unit0;                 // first work unit
+    int ht0;                   // first half-tile (ticket and mask index)
+};
+
+struct I8sTcArgs {
+    I8sProb p[kI8sMaxGroup];
+    unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass); one word per launch
+    int32_t* part;             // split tiles: slots of kI8sTileM x kI8sTileN int32 sums
     uint32_t* tickets;         // half-tile chunk counters (cleared by the pre-pass)
     unsigned long long* slot_masks;   // half-tile masks of the slots written (cleared by the pre-pass)
     uint32_t* status;
-    int M, N, K, relu;
-    int n_wt, n_at, chunks, total_units;   // n_wt: 256-feature tiles (a CTA pair each)
+    int count;                 // matmuls in the launch (1 .. kI8sMaxGroup), all with the same M
+    int M, n_at, relu, total_units;
 };
+static_assert(sizeof(I8sTcArgs) <= 32764, "I8sTcArgs exceeds the kernel parameter limit");
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
                               __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
                               cudaStream_t s);
@@ -196,9 +208,19 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
                              cudaStream_t s);
 cudaError_t launch_w8a8_rows(const float* x, int64_t M, int64_t K, int8_t* q, float* ascale, cudaStream_t s);
 cudaError_t launch_w8a8_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale, cudaStream_t s);
-cudaError_t launch_w8a8_rows_f16(const float* x, int64_t M, int64_t rows_pad, int64_t K, __half* xf, float* ascale,
-                                 void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
-                                 cudaStream_t s);
+// Row quantization of the packed W8A8 calls: one job per distinct activation.
+struct W8a8RowJobs {
+    const float* x[kI8sMaxGroup];   // M x K F32
+    __half* xf[kI8sMaxGroup];       // rows_pad x K f16 operand rows
+    float* ascale[kI8sMaxGroup];    // M row scales
+    int K[kI8sMaxGroup];
+    int count, M, rows_pad;
+    uint4* zero;                    // cleared by the launch (the GEMM's tickets and masks)
+    unsigned long long zero_16;
+    uint32_t* status;
+    unsigned int* amax_bits;
+};
+cudaError_t launch_w8a8_rows_f16(const W8a8RowJobs& J, cudaStream_t s);
 cudaError_t launch_i8_to_f16(const int8_t* src, int64_t n, __half* dst, cudaStream_t s);
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst,
                            cudaStream_t s);

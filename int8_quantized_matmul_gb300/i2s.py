@@ -43,6 +43,10 @@ class i2s_problem(ctypes.Structure):
     _fields_ = [("w_i2s", _p), ("N", _i64), ("K", _i64), ("x", _p), ("y", _p)]
 
 
+class w8a8_problem(ctypes.Structure):
+    _fields_ = [("packed", _p), ("bscale", _p), ("N", _i64), ("K", _i64), ("x", _p), ("d", _p)]
+
+
 _SIGS = {
     "i2s_status_string": (ctypes.c_char_p, [_int]),
     "i2s_version": (_int, []),
@@ -86,6 +90,8 @@ _SIGS = {
     "w8a8_pack_weights": (_int, [_p, _i64, _i64, _p, _p]),
     "w8a8_mul_mat_packed_workspace": (_sz, [_i64, _i64, _i64]),
     "w8a8_mul_mat_packed": (_int, [_p, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "w8a8_mul_mat_grouped_workspace": (_sz, [ctypes.POINTER(w8a8_problem), _int, _i64]),
+    "w8a8_mul_mat_grouped": (_int, [ctypes.POINTER(w8a8_problem), _int, _i64, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_L, _name)
@@ -441,6 +447,41 @@ def w8a8_mul_mat_packed(packed, bscale, N: int, K: int, x, d=None, ws=None):
     _check("w8a8_mul_mat_packed", _L.w8a8_mul_mat_packed(_dptr(packed), _dptr(bscale), N, K, _dptr(x), M, _dptr(d),
                                                          _dptr(ws), ws.numel(), _stream()))
     return d, ws
+
+
+def _w8a8_problems(problems):
+    arr = (w8a8_problem * len(problems))()
+    for i, (packed, bscale, N, K, x, d) in enumerate(problems):
+        arr[i] = w8a8_problem(_dptr(packed), _dptr(bscale), N, K, _dptr(x), _dptr(d))
+    return arr
+
+
+def w8a8_mul_mat_grouped(problems, M: int, ws=None):
+    """problems: (packed, bscale, N, K, x, d) tuples with the same M; one
+    quantization launch and one GEMM launch for all. Returns ws."""
+    arr = _w8a8_problems(problems)
+    if ws is None:
+        ws = _ws(int(_L.w8a8_mul_mat_grouped_workspace(arr, len(problems), M)), problems[0][4].device)
+    _check("w8a8_mul_mat_grouped", _L.w8a8_mul_mat_grouped(arr, len(problems), M, _dptr(ws), ws.numel(), _stream()))
+    return ws
+
+
+class W8A8Group:
+    """A fixed list of packed W8A8 matmuls (same M) with its workspace, for
+    repeated calls (and CUDA graph capture)."""
+
+    def __init__(self, problems, M: int, ws=None):
+        self.problems = list(problems)
+        self.M = M
+        self._arr = _w8a8_problems(self.problems)
+        need = int(_L.w8a8_mul_mat_grouped_workspace(self._arr, len(self.problems), M))
+        if need == 0:
+            raise I2SError("w8a8_mul_mat_grouped_workspace", -1)
+        self.ws = ws if ws is not None else _ws(need, self.problems[0][4].device)
+
+    def __call__(self):
+        _check("w8a8_mul_mat_grouped", _L.w8a8_mul_mat_grouped(self._arr, len(self.problems), self.M,
+                                                               _dptr(self.ws), self.ws.numel(), _stream()))
 
 
 def read_status(ws) -> int:

@@ -318,3 +318,29 @@ def test_device_rounding_around_every_half_integer(i2s, o):
     got = host(i2s.i8s_requant(dev(y)))
     ref = o.i8s_quantize(y)
     same_bytes(got, ref)
+
+
+def test_w8a8_grouped_layer(i2s, o):
+    # a Qwen3-1.7B-shaped layer at a ragged M: q, k, v share one activation,
+    # gate and up another; every output equals the oracle's, bit for bit
+    M = 77
+    specs = [("q", 2048, 2048, 0), ("k", 1024, 2048, 0), ("v", 1024, 2048, 0), ("o", 2048, 2048, 1),
+             ("gate", 640, 2048, 2), ("up", 640, 2048, 2), ("down", 2048, 1088, 3)]
+    xs = {a: synth.normal_f32((M, K), seed=200 + a, outlier_p=0.01) for (_, _, K, a) in specs}
+    dxs = {a: dev(x) for a, x in xs.items()}
+    problems, refs = [], []
+    for i, (name, N, K, a) in enumerate(specs):
+        wq, bs = o.w8a8_quantize_weights(synth.normal_f32((N, K), seed=300 + i, std=0.02))
+        d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        problems.append((i2s.w8a8_pack_weights(dev(wq)), dev(bs), N, K, dxs[a], d))
+        refs.append(o.w8a8_mul_mat(wq, bs, xs[a], nth=8))
+    ws = i2s.w8a8_mul_mat_grouped(problems, M)
+    assert i2s.read_status(ws) == 0
+    for p, ref in zip(problems, refs):
+        same_bytes(host(p[5]), ref)
+    # a second call on the same workspace (counters cleared by the call)
+    for p in problems:
+        p[5].zero_()
+    i2s.w8a8_mul_mat_grouped(problems, M, ws=ws)
+    for p, ref in zip(problems, refs):
+        same_bytes(host(p[5]), ref)
