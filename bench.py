@@ -630,20 +630,44 @@ def run_ours(args, rank, world, torch, dist):
     achieved = gemv_avg_bytes / (gemv_avg_ms * 1e-3) / 1e9
 
     # end to end through the public API: activations host->device, the pass,
-    # outputs device->host, every step (pinned buffers)
+    # outputs device->host, every step (pinned buffers). The two passes are
+    # independent batches, so each one's copies run on a second stream beside
+    # the other's kernels: the M = 8 inputs go up first, the M = 1 inputs go up
+    # while the M = 8 pass computes, the M = 8 outputs come back while the M = 1
+    # pass computes. Steps do not overlap: a step's first copy waits for the
+    # previous step's last.
+    side = torch.cuda.Stream(device=device)
+    p_big, p_small = sorted(passes, key=lambda q: -q.M)
+
+    def e2e_step():
+        done_prev = torch.cuda.Event()
+        done_prev.record(stream)
+        side.wait_event(done_prev)
+        p_big.x.copy_(p_big.x_host, non_blocking=True)
+        with torch.cuda.stream(side):
+            p_small.x.copy_(p_small.x_host, non_blocking=True)
+            small_in = torch.cuda.Event()
+            small_in.record(side)
+        p_big.group()
+        big_done = torch.cuda.Event()
+        big_done.record(stream)
+        stream.wait_event(small_in)
+        p_small.group()
+        with torch.cuda.stream(side):
+            side.wait_event(big_done)
+            p_big.y_host.copy_(p_big.y, non_blocking=True)
+            big_out = torch.cuda.Event()
+            big_out.record(side)
+        p_small.y_host.copy_(p_small.y, non_blocking=True)
+        stream.wait_event(big_out)
+
     for _ in range(2):
-        for p in passes:
-            p.x.copy_(p.x_host, non_blocking=True)
-            p.group()
-            p.y_host.copy_(p.y, non_blocking=True)
+        e2e_step()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        for p in passes:
-            p.x.copy_(p.x_host, non_blocking=True)
-            p.group()
-            p.y_host.copy_(p.y, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
@@ -653,7 +677,8 @@ def run_ours(args, rank, world, torch, dist):
         e2e_ms = float(t.item())
     e2e = {"value": world * args.steps * bytes_per_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes for p in passes),
-           "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes)}
+           "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes),
+           "note": "each pass's pinned copies overlap the other pass's kernels on a second stream; steps are serial"}
 
     prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None
     encoder = run_encoder_fc(torch, i2s, device, peaks) if not args.no_prefill else None
