@@ -81,7 +81,7 @@ static_assert(kCvtPrefetch % 2 == 0, "converters take K blocks in pairs");
 
 struct SmemTc {
     float sc_col[2][256];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
-    int rs_col[2][256];     // epilogue: row_sum[m] per tile column, by accumulator
+    float rs_col[2][256];   // epilogue: row_sum[m] per tile column (exact as a float), by accumulator
     uint64_t full_a[kStagesTc];
     uint64_t full_b[kStagesTc];
     uint64_t empty[kStagesTc];
@@ -355,11 +355,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             {
                 const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
                 float* sc_col = S.sc_col[acc];
-                int* rs_col = S.rs_col[acc];
+                float* rs_col = S.rs_col[acc];
                 for (int j = r; j < BN; j += kEpiWarps * 32) {
                     const int m = m_base + j;
                     sc_col[j] = m < a.M ? __fmul_rn(w_scale, P.act_scale[m]) : 0.0f;
-                    rs_col[j] = m < a.M ? P.row_sum[m] : 0;
+                    rs_col[j] = m < a.M ? (float)P.row_sum[m] : 0.0f;   // |row_sum| <= 127 K < 2^24
                 }
                 // every epilogue thread has staged its columns (bounded wait)
                 tc::mbar_arrive(&S.stage_bar);
@@ -375,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             }
             tc::tc_fence_after();
             const float* sc_col = S.sc_col[acc];
-            const int* rs_col = S.rs_col[acc];
+            const float* rs_col = S.rs_col[acc];
             const int N = P.N, M = a.M;
             float* y_col = P.y + n;   // this thread's output column
             // TMEM -> registers 32 columns at a time, the load of the next slice
@@ -396,8 +396,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
 #pragma unroll
                     for (int j = 16 * hh; j < 16 * hh + 16; ++j) {
                         const int jj = c * 32 + j;
-                        const int dot = __float2int_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f));
-                        v[j] = __float_as_uint(__fmul_rn(__int2float_rn(dot - rs_col[jj]), sc_col[jj]));
+                        // D * 2^24 is the integer dot, exact; so is dot - row_sum
+                        // (|.| < 2^24): the float of (dot - row_sum) without any
+                        // conversion instruction
+                        const float dr = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f), rs_col[jj]);
+                        v[j] = __float_as_uint(__fmul_rn(dr, sc_col[jj]));
                     }
                     if (rows >= 32) {
 #pragma unroll

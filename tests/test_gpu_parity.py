@@ -250,6 +250,29 @@ def test_i2s_grouped_under_cuda_graph(i2s, o):
         same_bits(host(y), o.i2s_mul_mat(packed, N, K, x))
 
 
+def test_i2s_grouped_back_to_back_on_one_workspace(i2s, o):
+    # The quantization and GEMV launches are programmatic dependents of the
+    # launch before them: each waits for it before touching the workspace.
+    # Twelve calls alternate two input sets and two output sets on one
+    # workspace with no synchronisation; a launch that wrote the workspace
+    # while the previous GEMV still read it would corrupt an output.
+    M = 8
+    probs, acts_a = layer_problems(o, M=M, seed=21)
+    _, acts_b = layer_problems(o, M=M, seed=22)
+    dA = {k: dev(v) for k, v in acts_a.items()}
+    dB = {k: dev(v) for k, v in acts_b.items()}
+    ys = [[torch.zeros((M, N), dtype=torch.float32, device="cuda") for _, N, _, _, _, _ in probs] for _ in range(2)]
+    dw = [dev(p[3]) for p in probs]
+    groups = [[(w, p[1], p[2], acts[p[5]], y) for w, p, y in zip(dw, probs, ys[i])] for i, acts in enumerate((dA, dB))]
+    ws = torch.empty(i2s.i2s_mul_mat_grouped_workspace(groups[0], M), dtype=torch.uint8, device="cuda")
+    for it in range(12):
+        i2s.i2s_mul_mat_grouped(groups[it % 2], M, ws=ws)
+    assert i2s.read_status(ws) == 0
+    for acts, yset in ((acts_a, ys[0]), (acts_b, ys[1])):
+        for (name, N, K, packed, _, act), y in zip(probs, yset):
+            same_bits(host(y), o.i2s_mul_mat(packed, N, K, acts[act], nth=4))
+
+
 def _row_slice(packed, N, K, n0, n1):
     """I2_S bytes of weight rows n0..n1 (rows are contiguous, K/4 bytes each)."""
     rb = K // 4
