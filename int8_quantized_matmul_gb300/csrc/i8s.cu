@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) k_absmax(const float* __restrict__ y, int
 // F32 scale and 28 zero bytes.
 __global__ void __launch_bounds__(256) k_requant(const float* __restrict__ y, int64_t n,
                                                  const unsigned int* __restrict__ amax_bits, uint8_t* dst) {
+    pdl_wait();   // y and the folded amax come from the launch before
     float scale, inv;
     quant_params(__uint_as_float(*amax_bits), scale, inv);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -86,8 +87,8 @@ cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cu
 }
 
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
-    k_requant<<<grid_for(n / 16), 256, 0, s>>>(y, n, amax_bits, dst);   // four float4 per thread and step
-    return cudaGetLastError();
+    // four float4 per thread and step; a programmatic dependent of the launch before
+    return launch_pdl(k_requant, dim3(grid_for(n / 16)), dim3(256), 0, s, y, n, amax_bits, dst);
 }
 
 }  // namespace i2s

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kEltThreads) k_add_amax(const uint8_t* __restr
 __global__ void __launch_bounds__(kEltThreads) k_add_quant(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b,
                                                            int64_t n, const unsigned int* __restrict__ amax_bits,
                                                            uint8_t* __restrict__ dst) {
+    pdl_wait();   // the first pass's amax
     const float sa = i8s_scale_of(a, n), sb = i8s_scale_of(b, n);
     float scale, inv;
     quant_params(__uint_as_float(*amax_bits), scale, inv);
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant(const uint8_t* __rest
                                                            const float* __restrict__ rfac,
                                                            const unsigned int* __restrict__ amax_bits,
                                                            uint8_t* __restrict__ dst) {
+    pdl_wait();   // the first pass's row factors and amax
     const int64_t n = rows * ne0;
     const float s = i8s_scale_of(x, n);
     float scale, inv;
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant_t(const uint8_t* __re
                                                              const float* __restrict__ gamma,
                                                              const unsigned int* __restrict__ amax_bits,
                                                              uint8_t* __restrict__ dst) {
+    pdl_wait();   // the first pass's amax
     const float s = i8s_scale_of(x, rows * 16 * V);
     float scale, inv;
     quant_params(__uint_as_float(*amax_bits), scale, inv);
@@ -558,7 +561,10 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, u
     const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
     const float bc = d.bias ? d.bias[c] : 0.0f;
     float scale = 0.0f, inv = 0.0f;
-    if (kQuant) quant_params(__uint_as_float(*amax_bits), scale, inv);
+    if (kQuant) {
+        pdl_wait();   // the first pass's amax
+        quant_params(__uint_as_float(*amax_bits), scale, inv);
+    }
     float mx = 0.0f;
     const int tl0 = 4 * threadIdx.x;
     uint8_t* out = dst + (int64_t)c * d.OL + t0;
@@ -608,7 +614,10 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
     const float bc = d.bias ? d.bias[c] : 0.0f;
     float scale = 0.0f, inv = 0.0f;
-    if (kQuant) quant_params(__uint_as_float(*amax_bits), scale, inv);
+    if (kQuant) {
+        pdl_wait();   // the first pass's amax
+        quant_params(__uint_as_float(*amax_bits), scale, inv);
+    }
     float mx = 0.0f;
     const bool aligned = ((((int64_t)c * d.OL) & 3) == 0);
 #pragma unroll 1
@@ -762,29 +771,33 @@ cudaError_t launch_add_scaled(const uint8_t* a, const uint8_t* b, int64_t n, uns
                               cudaStream_t s) {
     const int grid = elt_grid(n / 16 + 1);
     k_add_amax<<<grid, kEltThreads, 0, s>>>(a, b, n, amax_bits);
-    k_add_quant<<<grid, kEltThreads, 0, s>>>(a, b, n, amax_bits, dst);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_add_quant, dim3(grid), dim3(kEltThreads), 0, s, a, b, n, (const unsigned int*)amax_bits, dst);
 }
 
 cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, float eps, const float* gamma,
                                    float* rfac, unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
     if (ne0 % 16 == 0 && ne0 <= 64) {   // short rows: one thread per row
         const int grid = elt_grid(rows);
+        cudaError_t e = cudaSuccess;
         switch (ne0 / 16) {
             case 1: k_rms_rows_t<1><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    k_rms_quant_t<1><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+                    e = launch_pdl(k_rms_quant_t<1>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
             case 2: k_rms_rows_t<2><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    k_rms_quant_t<2><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+                    e = launch_pdl(k_rms_quant_t<2>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
             case 3: k_rms_rows_t<3><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    k_rms_quant_t<3><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+                    e = launch_pdl(k_rms_quant_t<3>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
             default: k_rms_rows_t<4><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                     k_rms_quant_t<4><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits, dst); break;
+                     e = launch_pdl(k_rms_quant_t<4>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
         }
-        return cudaGetLastError();
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     k_rms_rows<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, eps, gamma, rfac, amax_bits);
-    k_rms_quant<<<elt_grid(rows * 32), kEltThreads, 0, s>>>(x, rows, ne0, gamma, rfac, amax_bits, dst);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_rms_quant, dim3(elt_grid(rows * 32)), dim3(kEltThreads), 0, s, x, rows, ne0, gamma,
+                      (const float*)rfac, (const unsigned int*)amax_bits, dst);
 }
 
 cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s) {
@@ -830,16 +843,18 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
     if (stride == 1 && KW <= 8 && C <= 65535) {   // the 7-tap causal blocks: dp4a
         const dim3 g((unsigned)((OL + kDw1T - 1) / kDw1T), (unsigned)C);
         k_dw_s1<false><<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
-        k_dw_s1<true><<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
-        return cudaGetLastError();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_pdl(k_dw_s1<true>, g, dim3(kEltThreads), 0, s, d, amax_bits, dst);
     }
     const int64_t W = (int64_t)(kDwT - 1) * stride + KW;
     if (C <= 65535 && KW <= 64 && W + KW <= 48 * 1024) {   // windowed kernel
         const dim3 g((unsigned)((OL + kDwT - 1) / kDwT), (unsigned)C);
         const size_t sm = (size_t)(W + KW);
         k_dw_win<false><<<g, kEltThreads, sm, s>>>(d, (int)W, amax_bits, dst);
-        k_dw_win<true><<<g, kEltThreads, sm, s>>>(d, (int)W, amax_bits, dst);
-        return cudaGetLastError();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_pdl(k_dw_win<true>, g, dim3(kEltThreads), sm, s, d, (int)W, amax_bits, dst);
     }
     const int grid = elt_grid(C * OL / 4 + 1);
     k_dw_amax<<<grid, kEltThreads, 0, s>>>(d, amax_bits);

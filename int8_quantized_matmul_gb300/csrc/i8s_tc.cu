@@ -206,6 +206,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
     tc::tc_fence_before();
     tc::cluster_sync();
     tc::tc_fence_after();
+    // everything above touched only parameters, shared memory and TMEM; the
+    // operands, counters and outputs are used from here on, after the launch
+    // before this one (the pre-pass or the row quantizer) has completed
+    pdl_wait();
     volatile int* abort_flag = &S.abort;
     auto fail = [&](uint32_t code) {
         *abort_flag = 1;
@@ -498,6 +502,7 @@ __global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w
                                                     uint32_t* status, unsigned int* amax_bits) {
     const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
     const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+    pdl_wait();   // the launch before may still use this workspace (or produce x)
     if (t0 == 0) {
         *status = 0u;
         *amax_bits = 0u;
@@ -518,9 +523,8 @@ cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* 
     const unsigned long long want = (n + 1023) / 1024;
     const int cap = device_sm_count() * 8;
     const int grid = (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
-    k_i8s_to_f16<<<grid, 256, 0, s>>>(w, w16, wf, x, x16, x16p, xf, static_cast<uint4*>(zero), zero_bytes / 16, status,
-                                      amax_bits);
-    return cudaGetLastError();
+    return launch_pdl(k_i8s_to_f16, dim3(grid), dim3(256), 0, s, w, w16, wf, x, x16, x16p, xf, static_cast<uint4*>(zero),
+                      (unsigned long long)(zero_bytes / 16), status, amax_bits);
 }
 
 // Per device: 1 + the number of CTA pairs that can be resident at once (0:
@@ -563,8 +567,8 @@ cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = configure(&dev);
     if (e != cudaSuccess) return e;
-    k_i8s_gemm_tc<<<grid, kThreads8, kSmem8Bytes, s>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the launch before it
+    return launch_pdl(k_i8s_gemm_tc, dim3(grid), dim3(kThreads8), kSmem8Bytes, s, a);
 }
 
 }  // namespace i2s
