@@ -29,7 +29,7 @@ def i2s():
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*\b((?:i2s|i8s)_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*\b((?:i2s|i8s|w8a8)_[a-z0-9_]+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -37,6 +37,12 @@ def test_header_declares_the_north_star_calls():
     names = header_functions()
     for must in ("i2s_quantize_act", "i2s_mul_mat", "i8s_mul_mat_add_relu", "i8s_requant"):
         assert must in names
+    # the rows past the core: element-wise and conv ops, packed and grouped calls, W8A8
+    for must in ("i8s_add_scaled", "i8s_rms_norm_scaled", "i8s_transpose", "i8s_im2col_asym",
+                 "i8s_depthwise_mul_mat_add", "i8s_pack_weights", "i8s_mul_mat_add_relu_packed",
+                 "w8a8_quantize_weights", "w8a8_mul_mat", "w8a8_pack_weights", "w8a8_mul_mat_packed",
+                 "w8a8_mul_mat_grouped"):
+        assert must in names, must
 
 
 def test_library_exports_every_declared_symbol(i2s):
@@ -115,3 +121,54 @@ def test_workspace_sizes_monotone(i2s):
     c = i2s.i2s_mul_mat_workspace(512, 1536, 8960)
     assert 0 < a < b < c
     assert i2s.i2s_mul_mat_workspace(4, 10, 100) == 0
+
+
+def test_eltwise_and_w8a8_validation_needs_no_device(i2s):
+    L = i2s.lib
+    A = 1 << 20
+    vp = ctypes.c_void_p
+    E = {v: k for k, v in i2s.STATUS.items()}
+    # element-wise: null, shape, alignment and overlap checks
+    assert L.i8s_add_scaled(None, vp(A), 100, vp(2 * A), vp(3 * A), 256, None) == E["I2S_E_NULL_PTR"]
+    assert L.i8s_add_scaled(vp(A), vp(2 * A), 0, vp(3 * A), vp(4 * A), 256, None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_add_scaled(vp(A + 4), vp(2 * A), 100, vp(3 * A), vp(4 * A), 256, None) == E["I2S_E_MISALIGNED"]
+    assert L.i8s_add_scaled(vp(A), vp(2 * A), 100, vp(A + 16), vp(4 * A), 256, None) == E["I2S_E_BAD_ARG"]
+    assert L.i8s_add_scaled(vp(A), vp(2 * A), 100, vp(3 * A), vp(4 * A), 16, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    assert L.i8s_rms_norm_scaled(vp(A), 4, 0, 1e-5, None, vp(2 * A), vp(3 * A), 4096, None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_rms_norm_scaled(vp(A), 4, 200000, 1e-5, None, vp(2 * A), vp(3 * A), 4096, None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_rms_norm_scaled(vp(A), 4, 32, -1.0, None, vp(2 * A), vp(3 * A), 4096, None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_rms_norm_scaled(vp(A), 4, 32, 1e-5, vp(5), vp(2 * A), vp(3 * A), 4096, None) == E["I2S_E_MISALIGNED"]
+    assert L.i8s_rms_norm_scaled(vp(A), 1000, 32, 1e-5, None, vp(2 * A), vp(3 * A), 256, None) == \
+        E["I2S_E_WORKSPACE_TOO_SMALL"]
+    assert L.i8s_transpose(vp(A), 0, 5, vp(2 * A), None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_transpose(vp(A), 64, 64, vp(A + 64), None) == E["I2S_E_BAD_ARG"]
+    # conv geometry
+    assert i2s.i8s_im2col_out_len(20, 4, 1, 3, 0) == 20
+    assert i2s.i8s_im2col_out_len(5, 7, 1, 0, 0) == 0
+    assert i2s.i8s_im2col_out_len(40, 8, 4, 4, 0) == 10
+    assert L.i8s_im2col_asym(vp(A), 2, 5, 7, 1, 0, 0, vp(2 * A), None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_im2col_asym(vp(A), 2, 40, 8, 0, 4, 0, vp(2 * A), None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i8s_im2col_asym(vp(A), 2, 40, 8, 4, 4, 0, vp(2 * A + 3), None) == E["I2S_E_MISALIGNED"]
+    assert L.i8s_depthwise_mul_mat_add(vp(A), 7, vp(2 * A), 4, 100, 1, 6, 0, None, 0, vp(2 * A + 16), vp(4 * A), 256,
+                                       None) == E["I2S_E_BAD_ARG"]
+    # W8A8: shapes (K % 64), alignment, group size
+    assert L.w8a8_mul_mat(vp(A), vp(2 * A), 64, 100, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
+        E["I2S_E_BAD_SHAPE"]
+    assert L.w8a8_mul_mat(vp(A + 8), vp(2 * A), 64, 128, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
+        E["I2S_E_MISALIGNED"]
+    assert L.w8a8_packed_bytes(64, 128) == 64 * 128 * 2 and L.w8a8_packed_bytes(64, 100) == 0
+    assert L.i8s_packed_bytes(64, 128) == 64 * 128 * 2 + 16
+    probs = (i2s.w8a8_problem * 9)()
+    for i in range(9):
+        probs[i] = i2s.w8a8_problem(A, A, 64, 128, A, A)
+    assert L.w8a8_mul_mat_grouped(probs, 9, 8, vp(2 * A), 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.w8a8_mul_mat_grouped(probs, 0, 8, vp(2 * A), 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.w8a8_mul_mat_grouped_workspace(probs, 9, 8) == 0
+    # a group's workspace: q, k, v share one activation (quantized once)
+    shared = (i2s.w8a8_problem * 3)()
+    for i in range(3):
+        shared[i] = i2s.w8a8_problem(A, A, 64, 128, A, A)
+    distinct = (i2s.w8a8_problem * 3)()
+    for i in range(3):
+        distinct[i] = i2s.w8a8_problem(A, A, 64, 128, A + 4096 * i, A)
+    assert L.w8a8_mul_mat_grouped_workspace(distinct, 3, 8) > L.w8a8_mul_mat_grouped_workspace(shared, 3, 8) > 0
