@@ -618,7 +618,18 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
         pdl_wait();   // the first pass's amax
         quant_params(__uint_as_float(*amax_bits), scale, inv);
     }
-    float mx = 0.0f;
+    // y of one accumulator, the same arithmetic in both passes
+    auto y_of = [&](int acc) {
+        float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
+        if (d.bias) v = __fadd_rn(v, bc);
+        if (d.relu) v = v > 0.0f ? v : 0.0f;
+        return v;
+    };
+    // Pass 1 keeps the extremes of the live accumulators only. y_of is monotone in acc (an exact
+    // int-to-float, then a multiply by one factor, an add and a ReLU, each rounded to nearest, and
+    // rounding to nearest is monotone), so over any set of accumulators max |y| is reached at the
+    // smallest or the largest one: the folded amax is the one every |y| would give.
+    int lo = INT_MAX, hi = INT_MIN;
     const bool aligned = ((((int64_t)c * d.OL) & 3) == 0);
 #pragma unroll 1
     for (int chunk = 0; chunk < kDw1Chunks; ++chunk) {
@@ -628,21 +639,31 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
         uint32_t xw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) xw[i] = __funnelshift_r(win32[q0 + i], win32[q0 + i + 1], 8 * sh);
-        uint32_t packed[2] = {0u, 0u};
+        int acc[kDw1Out];
 #pragma unroll
         for (int e = 0; e < kDw1Out; ++e) {
             const int q = e >> 2, r = e & 3;
             const int x0 = (int)__funnelshift_r(xw[q], xw[q + 1], 8 * r);
             const int x1 = (int)__funnelshift_r(xw[q + 1], xw[q + 2], 8 * r);
-            const int acc = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
-            float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
-            if (d.bias) v = __fadd_rn(v, bc);
-            if (d.relu) v = v > 0.0f ? v : 0.0f;
-            const bool live = t0 + tl0 + e < d.OL;
-            if (kQuant) packed[q] |= (uint32_t)(quantize_one(v, inv) & 0xff) << (8 * r);
-            else if (live) mx = fmaxf(mx, fabsf(v));
+            acc[e] = __dp4a(x1, (int)tw[1], __dp4a(x0, (int)tw[0], 0));
         }
-        if (kQuant) {
+        if (!kQuant) {
+            const int nlive = d.OL - t0 - tl0;   // outputs of this group inside the row
+            if (nlive >= kDw1Out) {
+#pragma unroll
+                for (int e = 0; e < kDw1Out; ++e) lo = min(lo, acc[e]), hi = max(hi, acc[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kDw1Out; ++e)
+                    if (e < nlive) lo = min(lo, acc[e]), hi = max(hi, acc[e]);
+            }
+            continue;
+        }
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int e = 0; e < kDw1Out; ++e)
+            packed[e >> 2] |= (uint32_t)(quantize_one(y_of(acc[e]), inv) & 0xff) << (8 * (e & 3));
+        {
             uint8_t* out = dst + (int64_t)c * d.OL + t0 + tl0;
             if (aligned && t0 + tl0 + kDw1Out <= d.OL) {
                 reinterpret_cast<uint32_t*>(out)[0] = packed[0];
@@ -657,6 +678,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     if (kQuant) {
         if (blockIdx.x == 0 && blockIdx.y == 0) write_trailer(dst, (int64_t)d.C * d.OL, scale);
     } else {
+        const float mx = lo <= hi ? fmaxf(fabsf(y_of(lo)), fabsf(y_of(hi))) : 0.0f;
         fold_max(mx, amax_bits);
     }
 }

@@ -201,6 +201,23 @@ def test_depthwise_no_bias_and_headroom(i2s, o):
     same_bytes(host(got), ref)
 
 
+def test_depthwise_positions_past_the_end_stay_out_of_the_amax(i2s, o):
+    # Every real output has a full window (no padding): acc = 7 * 100 and the bias cancels
+    # s * 700 exactly, so y = 0 everywhere and the amax is its floor. Positions past the last
+    # output (OL = 994 is not a multiple of the kernel's 8-output groups) see zero-filled
+    # windows, smaller acc and y != 0: folding any of them would change the scale and every byte.
+    C, L, KW = 4, 1000, 7
+    w = o.i8s_pack(np.full((C, KW), 1, np.int8), 0.5)
+    x = o.i8s_pack(np.full((C, L), 100, np.int8), 0.01)
+    s = np.float32(0.5) * np.float32(0.01)
+    bias = np.full(C, -(np.float32(700.0) * s), np.float32)
+    got, OL = i2s.i8s_depthwise_mul_mat_add(dev(w), KW, dev(x), C, L, 1, 0, 0, bias=dev(bias))
+    ref, y_ref = o.i8s_depthwise_mul_mat_add(w, KW, x, C, L, 1, 0, 0, bias=bias)
+    assert OL == y_ref.shape[1] == L - KW + 1
+    assert not y_ref.any() and not ref[: C * OL].any()
+    same_bytes(host(got), ref)
+
+
 def test_depthwise_encoder_size(i2s, o):
     # the 7-tap causal depthwise conv of a stage-0 block
     C, L, KW = ENC_C, ENC_L, 7
