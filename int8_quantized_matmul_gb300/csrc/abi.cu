@@ -3,6 +3,7 @@
 // the computation runs in the kernels of quant.cu, gemv.cu, gemm_tc.cu and
 // i8s.cu; this file only marshals.
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <vector>
@@ -566,23 +567,32 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb);
 
 // I8_S workspace: [header: status, amax][y F32 M x N][activations f16,
 // rows_pad x K][weights f16, N x K][split-tile int32 sums, half-tiles x chunks
-// slots of 160 x 128][half-tile tickets][half-tile slot masks]. A tile is 256
-// output features x 160 activation rows, computed by a CTA pair; each CTA owns
-// one 128-feature half.
-static int64_t i8s_rows_pad(int64_t M) { return (M + kI8sTileM - 1) / kI8sTileM * kI8sTileM; }
-static int64_t i8s_tiles(int64_t M, int64_t N) {   // half-tiles: 128 features x 160 rows
-    return 2 * ((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN)) * ((M + kI8sTileM - 1) / kI8sTileM);
+// slots of tm x 128][half-tile tickets][half-tile slot masks]. A tile is 256
+// output features x tm activation rows (tm = 160 or 128, chosen per call),
+// computed by a CTA pair; each CTA owns one 128-feature half. The workspace
+// sizes are the larger of the two layouts, so they need no device.
+static int64_t i8s_rows_pad(int64_t M, int tm) { return (M + tm - 1) / tm * tm; }
+static int64_t i8s_tiles(int64_t M, int64_t N, int tm) {   // half-tiles: 128 features x tm rows
+    return 2 * ((N + 2 * kI8sTileN - 1) / (2 * kI8sTileN)) * ((M + tm - 1) / tm);
 }
 
 static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
 
+// the tile height of a launch over these matmuls (the resident pairs decide)
+static int i8s_pick_tile(int64_t M, const int64_t* N, const int64_t* K, int count) {
+    return i8s_tile_m(M, N, K, count, i8s_gemm_tc_max_pairs());
+}
+
+static size_t i8s_ws_for(int64_t M, int64_t N, int64_t K, int tm) {
+    const size_t tiles = (size_t)i8s_tiles(M, N, tm);
+    return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M, tm) * (size_t)K * 2) +
+           align_up((size_t)N * (size_t)K * 2) + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4) +
+           align_up(tiles * 4) + align_up(tiles * 8);
+}
+
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return 0;
-    const size_t tiles = (size_t)i8s_tiles(M, N);
-    return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) +
-           align_up((size_t)N * (size_t)K * 2) +
-           align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4) +
-           align_up(tiles * 8);
+    return std::max(i8s_ws_for(M, N, K, kI8sTileM), i8s_ws_for(M, N, K, kI8sTileMSmall));
 }
 
 // The I8_S call over f16 weight rows wf: either converted from w_i8s into the
@@ -595,12 +605,13 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
     uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     float* yf = reinterpret_cast<float*>(base + kHeader);
-    const int64_t rows_pad = i8s_rows_pad(M);
-    const size_t tiles = (size_t)i8s_tiles(M, N);
+    const int tm = i8s_pick_tile(M, &N, &K, 1);
+    const int64_t rows_pad = i8s_rows_pad(M, tm);
+    const size_t tiles = (size_t)i8s_tiles(M, N, tm);
     const size_t xf_off = kHeader + align_up((size_t)M * (size_t)N * 4);
     const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
     const size_t part_off = wf_off + (w_i8s ? align_up((size_t)N * (size_t)K * 2) : 0);
-    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4);
     const size_t mask_off = tick_off + align_up(tiles * 4);
     const size_t zero_bytes = mask_off + align_up(tiles * 8) - tick_off;   // tickets and masks (slots need no clearing)
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
@@ -613,7 +624,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     if (r) return r;
     static thread_local I8sTcArgs a;
     I8sProb& P = a.p[0];
-    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, tm / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&P.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
     P.w_scale_ptr = w_scale;
     P.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
@@ -636,7 +647,8 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     a.status = status;
     a.M = (int)M;
     a.relu = relu ? 1 : 0;
-    a.n_at = (int)(rows_pad / kI8sTileM);
+    a.tile_m = tm;
+    a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;   // units of whole (256-feature) tiles
     int pairs = i8s_gemm_tc_max_pairs();   // resident pairs: a persistent grid, no second wave
     if (pairs > a.total_units) pairs = a.total_units;
@@ -851,14 +863,15 @@ int w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, floa
 // in place (xf: rows_pad x K, wf: N x K); the split-tile areas of the
 // workspace start at part_off and were cleared by the launch before.
 static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* ascale, const __half* xf, int64_t N,
-                            int64_t K, int64_t M, float* d, uint8_t* base, size_t part_off, i2s_stream_t stream) {
-    const int64_t rows_pad = i8s_rows_pad(M);
-    const size_t tiles = (size_t)i8s_tiles(M, N);
-    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
+                            int64_t K, int64_t M, int tm, float* d, uint8_t* base, size_t part_off,
+                            i2s_stream_t stream) {
+    const int64_t rows_pad = i8s_rows_pad(M, tm);
+    const size_t tiles = (size_t)i8s_tiles(M, N, tm);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4);
     const size_t mask_off = tick_off + align_up(tiles * 4);
     static thread_local I8sTcArgs a;
     I8sProb& P = a.p[0];
-    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, kI8sTileM / 2)) return I2S_E_CUDA;
+    if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, tm / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&P.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
     P.w_scale_ptr = bscale;   // read by the kernel's I8_S path; the W8A8 epilogue uses the arrays
     P.x_scale_ptr = ascale;
@@ -881,7 +894,8 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
     a.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     a.M = (int)M;
     a.relu = 0;
-    a.n_at = (int)(rows_pad / kI8sTileM);
+    a.tile_m = tm;
+    a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;
     int pairs = i8s_gemm_tc_max_pairs();
     if (pairs > a.total_units) pairs = a.total_units;
@@ -889,10 +903,9 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
 }
 
 // bytes of the GEMM's split-tile areas (slots, tickets, masks)
-static size_t w8a8_split_bytes(int64_t M, int64_t N, int64_t K) {
-    const size_t tiles = (size_t)i8s_tiles(M, N);
-    return align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4) + align_up(tiles * 4) +
-           align_up(tiles * 8);
+static size_t w8a8_split_bytes(int64_t M, int64_t N, int64_t K, int tm) {
+    const size_t tiles = (size_t)i8s_tiles(M, N, tm);
+    return align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4) + align_up(tiles * 4) + align_up(tiles * 8);
 }
 
 static bool w8a8_shape_ok(int64_t M, int64_t N, int64_t K) {
@@ -905,10 +918,14 @@ static bool w8a8_shape_ok(int64_t M, int64_t N, int64_t K) {
 // [split-tile slots, tickets, masks].
 static size_t w8a8_front(int64_t M, int64_t K) { return kHeader + align_up((size_t)M * K) + align_up((size_t)M * 4); }
 
+static size_t w8a8_ws_for(int64_t M, int64_t N, int64_t K, int tm) {
+    return w8a8_front(M, K) + align_up((size_t)i8s_rows_pad(M, tm) * (size_t)K * 2) +
+           align_up((size_t)N * (size_t)K * 2) + w8a8_split_bytes(M, N, K, tm);
+}
+
 size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
     if (!w8a8_shape_ok(M, N, K)) return 0;
-    return w8a8_front(M, K) + align_up((size_t)i8s_rows_pad(M) * (size_t)K * 2) + align_up((size_t)N * (size_t)K * 2) +
-           w8a8_split_bytes(M, N, K);
+    return std::max(w8a8_ws_for(M, N, K, kI8sTileM), w8a8_ws_for(M, N, K, kI8sTileMSmall));
 }
 
 int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M, float* d,
@@ -925,13 +942,14 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
     uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     int8_t* xq = reinterpret_cast<int8_t*>(base + kHeader);
     float* ascale = reinterpret_cast<float*>(base + kHeader + align_up((size_t)M * K));
-    const int64_t rows_pad = i8s_rows_pad(M);
+    const int tm = i8s_pick_tile(M, &N, &K, 1);
+    const int64_t rows_pad = i8s_rows_pad(M, tm);
     const size_t xf_off = w8a8_front(M, K);
     const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
     const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
-    const size_t tiles = (size_t)i8s_tiles(M, N);
-    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * kI8sTileM * 4);
-    const size_t zero_bytes = w8a8_split_bytes(M, N, K) - (tick_off - part_off);   // tickets and masks
+    const size_t tiles = (size_t)i8s_tiles(M, N, tm);
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4);
+    const size_t zero_bytes = w8a8_split_bytes(M, N, K, tm) - (tick_off - part_off);   // tickets and masks
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
     __half* wf = reinterpret_cast<__half*>(base + wf_off);
     // per-row activation quantization (1e-9 floor), then the int8 rows and
@@ -942,7 +960,7 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
     r = cuda_status(launch_i8s_to_f16(wq, (int)N, wf, xq, (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes,
                                       status, amax, stream));
     if (r) return r;
-    return launch_w8a8_gemm(wf, bscale, ascale, xf, N, K, M, d, base, part_off, stream);
+    return launch_w8a8_gemm(wf, bscale, ascale, xf, N, K, M, tm, d, base, part_off, stream);
 }
 
 size_t w8a8_packed_bytes(int64_t N, int64_t K) {
@@ -970,16 +988,16 @@ struct W8a8Plan {
     int n_act = 0;
     int act_of[kI8sMaxGroup];
     size_t act_off[kI8sMaxGroup];   // row scales; the f16 rows follow at align_up(M * 4)
-    size_t slots = 0, tiles = 0;    // slots (kI8sTileM x kI8sTileN int32 each), half-tiles
+    size_t slots = 0, tiles = 0;    // slots (tm x kI8sTileN int32 each), half-tiles
     size_t part_off = 0, tick_off = 0, mask_off = 0, end = 0;
 };
 }  // namespace
 
 static_assert(kI8sMaxGroup == W8A8_MAX_GROUP, "one GEMM launch holds every matmul of a group");
 
-static W8a8Plan w8a8_plan(const w8a8_problem* probs, int count, int64_t M) {
+static W8a8Plan w8a8_plan(const w8a8_problem* probs, int count, int64_t M, int tm) {
     W8a8Plan pl;
-    const int64_t rows_pad = i8s_rows_pad(M);
+    const int64_t rows_pad = i8s_rows_pad(M, tm);
     size_t off = kHeader;
     for (int i = 0; i < count; ++i) {
         int a = -1;
@@ -991,12 +1009,12 @@ static W8a8Plan w8a8_plan(const w8a8_problem* probs, int count, int64_t M) {
             off += align_up((size_t)M * 4) + align_up((size_t)rows_pad * (size_t)probs[i].K * 2);
         }
         pl.act_of[i] = a;
-        const size_t ht = (size_t)i8s_tiles(M, probs[i].N);
+        const size_t ht = (size_t)i8s_tiles(M, probs[i].N, tm);
         pl.tiles += ht;
         pl.slots += ht * (size_t)i8s_chunks(probs[i].K);
     }
     pl.part_off = off;
-    pl.tick_off = pl.part_off + align_up(pl.slots * kI8sTileN * kI8sTileM * 4);
+    pl.tick_off = pl.part_off + align_up(pl.slots * kI8sTileN * tm * 4);
     pl.mask_off = pl.tick_off + align_up(pl.tiles * 4);
     pl.end = pl.mask_off + align_up(pl.tiles * 8);
     return pl;
@@ -1012,14 +1030,14 @@ static int w8a8_group_ok(const w8a8_problem* probs, int count, int64_t M) {
         if (!w8a8_shape_ok(M, q.N, q.K)) return I2S_E_BAD_SHAPE;
         if (!aligned16(q.packed) || !aligned16(q.x) || !aligned16(q.d) || ((uintptr_t)q.bscale & 3u))
             return I2S_E_MISALIGNED;
-        units += (int64_t)i8s_tiles(M, q.N) / 2 * i8s_chunks(q.K);
+        units += (int64_t)i8s_tiles(M, q.N, kI8sTileMSmall) / 2 * i8s_chunks(q.K);   // the more numerous
     }
     return units < ((int64_t)1 << 30) ? I2S_OK : I2S_E_BAD_SHAPE;
 }
 
 size_t w8a8_mul_mat_grouped_workspace(const w8a8_problem* probs, int count, int64_t M) {
     if (w8a8_group_ok(probs, count, M) != I2S_OK) return 0;
-    return w8a8_plan(probs, count, M).end;
+    return std::max(w8a8_plan(probs, count, M, kI8sTileM).end, w8a8_plan(probs, count, M, kI8sTileMSmall).end);
 }
 
 int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
@@ -1028,12 +1046,15 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
     if (r) return r;
     if (!ws) return I2S_E_NULL_PTR;
     if (!aligned256(ws)) return I2S_E_MISALIGNED;
-    const W8a8Plan pl = w8a8_plan(probs, count, M);
-    if (ws_bytes < pl.end) return I2S_E_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < w8a8_mul_mat_grouped_workspace(probs, count, M)) return I2S_E_WORKSPACE_TOO_SMALL;
     r = check_device();
     if (r) return r;
+    int64_t Ns[kI8sMaxGroup], Ks[kI8sMaxGroup];
+    for (int i = 0; i < count; ++i) Ns[i] = probs[i].N, Ks[i] = probs[i].K;
+    const int tm = i8s_pick_tile(M, Ns, Ks, count);
+    const W8a8Plan pl = w8a8_plan(probs, count, M, tm);
     uint8_t* base = static_cast<uint8_t*>(ws);
-    const int64_t rows_pad = i8s_rows_pad(M);
+    const int64_t rows_pad = i8s_rows_pad(M, tm);
     // one launch quantizes every distinct activation into its f16 operand
     // rows (and clears the status, amax and split-tile counters)
     static thread_local W8a8RowJobs J;
@@ -1061,7 +1082,7 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
         const w8a8_problem& q = probs[i];
         I8sProb& P = a.p[i];
         const int act = pl.act_of[i];
-        if (!make_f16_operand_map(&P.xmap, J.xf[act], (int)rows_pad, (int)q.K, kI8sTileM / 2)) return I2S_E_CUDA;
+        if (!make_f16_operand_map(&P.xmap, J.xf[act], (int)rows_pad, (int)q.K, tm / 2)) return I2S_E_CUDA;
         if (!make_f16_operand_map(&P.wmap, q.packed, (int)q.N, (int)q.K, kI8sTileN)) return I2S_E_CUDA;
         P.w_scale_ptr = q.bscale;   // read by the kernel's I8_S path; the W8A8 epilogue uses the arrays
         P.x_scale_ptr = J.ascale[act];
@@ -1076,7 +1097,7 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
         P.unit0 = units;
         P.ht0 = ht;
         P.slot0 = slot;
-        const int tiles_i = (int)i8s_tiles(M, q.N);   // half-tiles
+        const int tiles_i = (int)i8s_tiles(M, q.N, tm);   // half-tiles
         units += tiles_i / 2 * P.chunks;
         ht += tiles_i;
         slot += (long long)tiles_i * P.chunks;
@@ -1089,7 +1110,8 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
     a.status = J.status;
     a.M = (int)M;
     a.relu = 0;
-    a.n_at = (int)(rows_pad / kI8sTileM);
+    a.tile_m = tm;
+    a.n_at = (int)(rows_pad / tm);
     a.total_units = units;
     int pairs = i8s_gemm_tc_max_pairs();
     if (pairs > units) pairs = units;
@@ -1100,7 +1122,7 @@ size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
     if (!w8a8_shape_ok(M, N, K)) return 0;
     const w8a8_problem q{reinterpret_cast<const void*>(16), reinterpret_cast<const float*>(16), N, K,
                          reinterpret_cast<const float*>(16), reinterpret_cast<float*>(16)};
-    return w8a8_plan(&q, 1, M).end;
+    return w8a8_mul_mat_grouped_workspace(&q, 1, M);
 }
 
 int w8a8_mul_mat_packed(const void* packed, const float* bscale, int64_t N, int64_t K, const float* x, int64_t M,

@@ -69,20 +69,26 @@ constexpr int kKB8 = 128;                    // K positions per stage (two 64-po
 constexpr int kStagesPerChunk = kI8sChunkK / kKB8;
 constexpr int kStages8 = 4;
 constexpr int kAAtomBytes = kI8sTileN * 128;          // 128 rows x 64 f16
-constexpr int kBRows8 = kI8sTileM / 2;               // activation rows of a tile in each CTA
-constexpr int kBAtomBytes = kBRows8 * 128;            // 80 rows x 64 f16 (a multiple of 1024)
 constexpr int kAStage8 = 2 * kAAtomBytes;
-constexpr int kBStage8 = 2 * kBAtomBytes;
 constexpr uint32_t kTmemCols8 = 512;
-constexpr uint32_t kDCol8a = 0, kDCol8b = kI8sTileM;   // the two f32 accumulators
-constexpr uint32_t kSCol8 = 2 * kI8sTileM;             // int32 running sums
-constexpr int kEpiCols8 = kI8sTileM / 2;               // accumulator columns each epilogue warp owns
-constexpr int kESlices8 = kEpiCols8 / 16;              // 16-column TMEM slices of them
-static_assert(kEpiCols8 % 16 == 0, "epilogue slices");
 constexpr long long kWaitLimit8 = 2000000000LL;
-static_assert(kSCol8 + kI8sTileM <= kTmemCols8, "TMEM budget");
-static_assert(kBAtomBytes % 1024 == 0 && kI8sTileM % 32 == 0, "swizzle atoms of the B half");
-static_assert(kI8sTileM % 32 == 0 && kI8sTileM % 16 == 0 && kI8sTileM <= 256, "MMA N");
+
+// What depends on BM, the activation rows of a tile (the MMA N): kI8sTileM
+// (160) or kI8sTileMSmall (128).
+template <int BM>
+struct Tile8 {
+    static constexpr int kBRows = BM / 2;                  // activation rows of a tile in each CTA
+    static constexpr int kBAtomBytes = kBRows * 128;       // BM/2 rows x 64 f16 (a multiple of 1024)
+    static constexpr int kBStage = 2 * kBAtomBytes;
+    static constexpr uint32_t kDColA = 0, kDColB = BM;     // the two f32 accumulators
+    static constexpr uint32_t kSCol = 2 * BM;              // int32 running sums
+    static constexpr int kEpiCols = BM / 2;                // accumulator columns each epilogue warp owns
+    static constexpr int kESlices = kEpiCols / 16;         // 16-column TMEM slices of them
+    static_assert(kEpiCols % 16 == 0, "epilogue slices");
+    static_assert(kSCol + BM <= kTmemCols8, "TMEM budget");
+    static_assert(kBAtomBytes % 1024 == 0 && BM % 32 == 0, "swizzle atoms of the B half");
+    static_assert(BM % 16 == 0 && BM <= 256, "MMA N");
+};
 // Issuer i takes the stages s with s % kIssuers8 == i. Each ring slot must
 // always be served by the same issuer: a parity wait cannot tell the phase it
 // wants from the one two phases later, so an issuer must never wait on a slot
@@ -103,7 +109,10 @@ struct Smem8 {
     int final_flag;
 };
 
-constexpr size_t kSmem8Bytes = 1024 + (size_t)kStages8 * (kAStage8 + kBStage8) + sizeof(Smem8);
+template <int BM>
+constexpr size_t smem8_bytes() {
+    return 1024 + (size_t)kStages8 * (kAStage8 + Tile8<BM>::kBStage) + sizeof(Smem8);
+}
 
 // The part of the unit range [u, u_hi) that lies in one tile of matmul p.
 // Units are numbered matmul by matmul, tile-major within each.
@@ -143,7 +152,16 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&h1);
 }
 
+template <int BM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_constant__ I8sTcArgs a) {
+    using T = Tile8<BM>;
+    constexpr int kBRows8 = T::kBRows;
+    constexpr int kBAtomBytes = T::kBAtomBytes;
+    constexpr int kBStage8 = T::kBStage;
+    constexpr uint32_t kDCol8a = T::kDColA, kDCol8b = T::kDColB;
+    constexpr uint32_t kSCol8 = T::kSCol;
+    constexpr int kEpiCols8 = T::kEpiCols;
+    constexpr int kESlices8 = T::kESlices;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
@@ -232,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                 const CUtensorMap* xmap = &a.p[g.p].xmap;
                 const int kb_hi = min(stages_of(g.p), g.c_hi * kStagesPerChunk);
                 const int wrow = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN;   // this CTA's weight rows
-                const int xrow = g.at * kI8sTileM + (int)rank * kBRows8;           // this CTA's activation rows
+                const int xrow = g.at * BM + (int)rank * kBRows8;           // this CTA's activation rows
                 for (int kb = g.c_lo * kStagesPerChunk; kb < kb_hi; ++kb) {
                     if (!tc::mbar_wait_idle(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit8)) { fail(1); ok = false; break; }
                     // the leader expects both CTAs' bytes; a peer's bytes may land first
@@ -262,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
         // issuer `me` takes the stages whose position in this CTA's stage
         // stream is me modulo kIssuers8; the ring index advances over all
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16_f32(2 * kI8sTileN, kI8sTileM);   // 256 x 160 over the pair
+            constexpr uint32_t idesc = tc::idesc_f16_f32(2 * kI8sTileN, BM);   // 256 x 160 over the pair
             const int me = warp - kMmaWarp8;
             int stage = 0;
             uint32_t phase = 0;
@@ -349,9 +367,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             if (!ok) break;
             const int n = g.wt * (2 * kI8sTileN) + (int)rank * kI8sTileN + r;
             const int ht = P.ht0 + 2 * g.tile + (int)rank;   // this CTA's half of the tile: its ticket and mask
-            const int m0 = g.at * kI8sTileM + c0;     // first activation row of this warp's columns
+            const int m0 = g.at * BM + c0;     // first activation row of this warp's columns
             const uint32_t scol = tmem_base + lane_off + kSCol8;
-            constexpr size_t kSlot = (size_t)kI8sTileM * kI8sTileN;   // one segment's int32 sums
+            constexpr size_t kSlot = (size_t)BM * kI8sTileN;   // one segment's int32 sums
             int32_t* slots = a.part + ((size_t)P.slot0 + (size_t)(2 * g.tile + (int)rank) * chunks) * kSlot +
                              (size_t)c0 * kI8sTileN;
             bool write = g.c_lo == 0 && g.c_hi == chunks;
@@ -540,7 +558,11 @@ static cudaError_t configure(int* dev_out) {
     *dev_out = dev;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (g_pairs[dev].load() > 0) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_i8s_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem8Bytes);
+    e = cudaFuncSetAttribute(k_i8s_gemm_tc<kI8sTileM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem8_bytes<kI8sTileM>());
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_i8s_gemm_tc<kI8sTileMSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem8_bytes<kI8sTileMSmall>());
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -548,9 +570,9 @@ static cudaError_t configure(int* dev_out) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
     cfg.blockDim = dim3(kThreads8, 1, 1);
-    cfg.dynamicSmemBytes = kSmem8Bytes;
+    cfg.dynamicSmemBytes = smem8_bytes<kI8sTileM>();   // the larger of the two: pairs that fit either
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, (void*)k_i8s_gemm_tc, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, (void*)k_i8s_gemm_tc<kI8sTileM>, &cfg);
     if (e != cudaSuccess) return e;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     g_pairs[dev].store(1 + clusters);
@@ -568,7 +590,10 @@ cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s) {
     cudaError_t e = configure(&dev);
     if (e != cudaSuccess) return e;
     // a programmatic dependent of the launch before it
-    return launch_pdl(k_i8s_gemm_tc, dim3(grid), dim3(kThreads8), kSmem8Bytes, s, a);
+    if (a.tile_m == kI8sTileMSmall)
+        return launch_pdl(k_i8s_gemm_tc<kI8sTileMSmall>, dim3(grid), dim3(kThreads8), smem8_bytes<kI8sTileMSmall>(), s, a);
+    if (a.tile_m != kI8sTileM) return cudaErrorInvalidValue;
+    return launch_pdl(k_i8s_gemm_tc<kI8sTileM>, dim3(grid), dim3(kThreads8), smem8_bytes<kI8sTileM>(), s, a);
 }
 
 }  // namespace i2s

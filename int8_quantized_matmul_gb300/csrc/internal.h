@@ -149,19 +149,44 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
 // I8_S fused matmul on tcgen05 (i8s_tc.cu) and the per-tensor requant (i8s.cu).
 // ---------------------------------------------------------------------------
 
-// Tensor-core I8_S GEMM (i8s_tc.cu): 128 x 160 output tiles (output features x
-// activation rows), K in chunks of kI8sChunkK positions whose f32 partial sums
-// are exact (1024 * 127^2 < 2^24).
-constexpr int kI8sTileN = 128;   // output features (weight rows) per tile: the MMA M
-constexpr int kI8sTileM = 160;   // activation rows per tile: the MMA N
+// Tensor-core I8_S GEMM (i8s_tc.cu): 128 x 160 or 128 x 128 output tiles
+// (output features x activation rows), K in chunks of kI8sChunkK positions
+// whose f32 partial sums are exact (1024 * 127^2 < 2^24).
+constexpr int kI8sTileN = 128;        // output features (weight rows) per tile: the MMA M
+constexpr int kI8sTileM = 160;        // activation rows per tile: the MMA N
+constexpr int kI8sTileMSmall = 128;   // the other tile height
 constexpr int kI8sChunkK = 1024;
 constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask of a split tile)
+
+// The tile height of a launch whose matmuls have M rows, N[i] features and
+// K[i] positions, run by `pairs` CTA pairs. The busiest pair takes
+// ceil(units / pairs) work units (a 256-feature x tm-row tile over one K
+// chunk) and each unit moves 256 weight rows and tm activation rows of
+// operands through shared memory, the kernel's bound. The height with the
+// smaller product wins, 160 on a tie (fewer, larger units): 128 when 160 would
+// pad M with more zero rows (512 rows: 640 against 512), 160 when the extra
+// units of 128 would lengthen the busiest pair (900 rows: 6 x 416 against
+// 7 x 384 over 76 pairs).
+inline int i8s_tile_m(int64_t M, const int64_t* N, const int64_t* K, int count, int pairs) {
+    int64_t best_cost = -1;
+    int best = kI8sTileM;
+    for (int tm : {kI8sTileM, kI8sTileMSmall}) {
+        int64_t units = 0;
+        for (int i = 0; i < count; ++i)
+            units += (N[i] + 2 * kI8sTileN - 1) / (2 * kI8sTileN) * ((M + tm - 1) / tm) *
+                     ((K[i] + kI8sChunkK - 1) / kI8sChunkK);
+        const int64_t p = pairs > 0 ? pairs : 1;
+        const int64_t cost = (units + p - 1) / p * (2 * kI8sTileN + tm);
+        if (best_cost < 0 || cost < best_cost) best_cost = cost, best = tm;
+    }
+    return best;
+}
 
 // One matmul of a launch: its operand maps, scales, output and offsets into
 // the launch's split-tile areas.
 constexpr int kI8sMaxGroup = 8;
 struct I8sProb {
-    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x kI8sTileM / 2, 128-byte swizzle
+    CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x tile_m / 2, 128-byte swizzle
     CUtensorMap wmap;          // f16 weights, N x K, box 64 x kI8sTileN, 128-byte swizzle
     const float* w_scale_ptr;  // I8_S: the weight and activation scales (W8A8: any valid floats)
     const float* x_scale_ptr;
@@ -169,7 +194,7 @@ struct I8sProb {
     float* y;                  // M x N F32
     const float* row_scale;    // W8A8 only (col_scale set): per-row activation scales, M
     const float* col_scale;    // W8A8 only: per-channel weight scales, N; null for I8_S
-    long long slot0;           // first split-tile slot (kI8sTileM x kI8sTileN int32 sums) of this matmul
+    long long slot0;           // first split-tile slot (tile_m x kI8sTileN int32 sums) of this matmul
     int N, K;
     int n_wt, chunks;          // n_wt: 256-feature tiles (a CTA pair each); chunks: ceil(K / kI8sChunkK)
     int unit0;                 // first work unit
@@ -179,12 +204,13 @@ struct I8sProb {
 struct I8sTcArgs {
     I8sProb p[kI8sMaxGroup];
     unsigned int* amax_bits;   // max |y| as float bits (cleared by the pre-pass); one word per launch
-    int32_t* part;             // split tiles: slots of kI8sTileM x kI8sTileN int32 sums
+    int32_t* part;             // split tiles: slots of tile_m x kI8sTileN int32 sums
     uint32_t* tickets;         // half-tile chunk counters (cleared by the pre-pass)
     unsigned long long* slot_masks;   // half-tile masks of the slots written (cleared by the pre-pass)
     uint32_t* status;
     int count;                 // matmuls in the launch (1 .. kI8sMaxGroup), all with the same M
     int M, n_at, relu, total_units;
+    int tile_m;                // activation rows per tile: kI8sTileM or kI8sTileMSmall
 };
 static_assert(sizeof(I8sTcArgs) <= 32764, "I8sTcArgs exceeds the kernel parameter limit");
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,

@@ -261,6 +261,18 @@ def test_w8a8_mul_mat(i2s, o, M, N, K):
     same_bytes(host(d), o.w8a8_mul_mat(wq, bs, x, nth=4))
 
 
+def test_w8a8_160_row_tiles(i2s, o):
+    # The GEMM takes 128- or 160-row activation tiles, whichever leaves less work on its busiest
+    # CTA pair. The small shapes above take 128-row tiles; here 150 rows are one 160-row tile
+    # against two 128-row ones, and with 76 weight tiles that is one unit per pair against two,
+    # so the call runs on 160-row tiles with ten zero rows at the tail. Every output is compared.
+    M, N, K = 150, 19456, 1024
+    wq, bs, x = w8a8_inputs(o, M, N, K, seed=7)
+    d, ws = i2s.w8a8_mul_mat(dev(wq), dev(bs), dev(x))
+    assert i2s.read_status(ws) == 0
+    same_bytes(host(d), o.w8a8_mul_mat(wq, bs, x, nth=8))
+
+
 def test_w8a8_headroom_and_zero_rows(i2s, o):
     # codes at +-127 over K = 8192 (|acc| = 127^2 * 8192 > 2^24) and an
     # all-zero activation row (scale 1e-9/127, outputs 0)
