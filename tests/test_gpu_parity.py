@@ -430,6 +430,22 @@ def test_i8s_mul_mat_add(i2s, o, M, N, K, relu, with_bias):
     same_bits(host(y8), oy8)
 
 
+@pytest.mark.parametrize("relu", [False, True])
+def test_i8s_split_tiles_ragged_chunk(i2s, o, relu):
+    # 10 weight tiles x 9 K chunks (K % 1024 = 704 and K % 128 = 64: the last chunk is short
+    # and its last stage half past K) over 74 or 76 CTA pairs: ranges of one or two chunks cut
+    # most tiles between pairs, and the pair that completes a tile adds the others' slots.
+    # Every output is compared.
+    M, N, K = 40, 2560, 8896
+    wp, xp, bias = i8s_inputs(o, M, N, K, seed=11 + relu)
+    y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M, bias=dev(bias), relu=relu)
+    assert i2s.read_status(ws) == 0
+    yf = host(i2s.i8s_ws_f32(ws, M, N))
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, relu=relu, nth=8)
+    same_bits(yf, oyf)
+    same_bits(host(y8), oy8)
+
+
 @pytest.mark.parametrize("K", [384, 640, 1088, 3072])
 def test_i8s_stage_ring_wraps(i2s, o, K):
     # 3, 5, 9 and 24 stages of 128 positions: every stage slot of the
