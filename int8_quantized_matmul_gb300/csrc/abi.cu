@@ -578,6 +578,18 @@ static int64_t i8s_tiles(int64_t M, int64_t N, int tm) {   // half-tiles: 128 fe
 
 static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
 
+// CTA pairs of a launch over `units` work units: the fewest that keep the
+// busiest pair's share of the resident pairs' split (ceil(units / resident)).
+// The pairs share L2 bandwidth, so the ones left idle cost little, and fewer
+// range boundaries cut fewer tiles into segments that go through slots (the
+// encoder's FC1, 384 units over 76 pairs, runs as 64 pairs of 6 whole tiles).
+static int i8s_grid_pairs(int64_t units) {
+    const int64_t resident = i8s_gemm_tc_max_pairs();
+    const int64_t per_pair = (units + resident - 1) / resident;
+    const int64_t pairs = (units + per_pair - 1) / per_pair;
+    return pairs < 1 ? 1 : (int)pairs;
+}
+
 // the tile height of a launch over these matmuls (the resident pairs decide)
 static int i8s_pick_tile(int64_t M, const int64_t* N, const int64_t* K, int count) {
     return i8s_tile_m(M, N, K, count, i8s_gemm_tc_max_pairs());
@@ -650,9 +662,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;   // units of whole (256-feature) tiles
-    int pairs = i8s_gemm_tc_max_pairs();   // resident pairs: a persistent grid, no second wave
-    if (pairs > a.total_units) pairs = a.total_units;
-    const int grid = 2 * pairs;   // clusters of two CTAs
+    const int grid = 2 * i8s_grid_pairs(a.total_units);   // at most the resident pairs, clusters of two CTAs
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
@@ -897,9 +907,7 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;
-    int pairs = i8s_gemm_tc_max_pairs();
-    if (pairs > a.total_units) pairs = a.total_units;
-    return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(a.total_units), stream));
 }
 
 // bytes of the GEMM's split-tile areas (slots, tickets, masks)
@@ -1113,9 +1121,7 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = units;
-    int pairs = i8s_gemm_tc_max_pairs();
-    if (pairs > units) pairs = units;
-    return cuda_status(launch_i8s_gemm_tc(a, 2 * pairs, stream));
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(units), stream));
 }
 
 size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
