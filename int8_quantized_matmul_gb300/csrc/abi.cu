@@ -579,13 +579,18 @@ static int64_t i8s_tiles(int64_t M, int64_t N, int tm) {   // half-tiles: 128 fe
 static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
 
 // CTA pairs of a launch over `units` work units: the fewest that keep the
-// busiest pair's share of the resident pairs' split (ceil(units / resident)).
-// The pairs share L2 bandwidth, so the ones left idle cost little, and fewer
-// range boundaries cut fewer tiles into segments that go through slots (the
-// encoder's FC1, 384 units over 76 pairs, runs as 64 pairs of 6 whole tiles).
-static int i8s_grid_pairs(int64_t units) {
+// busiest pair's share of the resident pairs' split (ceil(units / resident)),
+// that share rounded up to whole tiles of `tile_units` units (a single
+// matmul's K chunks) when this adds at most a third. The pairs share L2
+// bandwidth, so the ones left idle cost little, while a tile cut between
+// pairs stores and reloads an 80 KB slot of sums per CTA: the encoder's FC1
+// (384 units, 2 per tile) runs as 64 pairs of 6 units, FC2 (8 per tile) as
+// 48 pairs of one whole tile each rather than 64 pairs of 6 units.
+static int i8s_grid_pairs(int64_t units, int64_t tile_units = 1) {
     const int64_t resident = i8s_gemm_tc_max_pairs();
-    const int64_t per_pair = (units + resident - 1) / resident;
+    int64_t per_pair = (units + resident - 1) / resident;
+    const int64_t whole = (per_pair + tile_units - 1) / tile_units * tile_units;
+    if (3 * whole <= 4 * per_pair) per_pair = whole;
     const int64_t pairs = (units + per_pair - 1) / per_pair;
     return pairs < 1 ? 1 : (int)pairs;
 }
@@ -662,7 +667,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;   // units of whole (256-feature) tiles
-    const int grid = 2 * i8s_grid_pairs(a.total_units);   // at most the resident pairs, clusters of two CTAs
+    const int grid = 2 * i8s_grid_pairs(a.total_units, P.chunks);   // at most the resident pairs, clusters of two CTAs
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
@@ -907,7 +912,7 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;
-    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(a.total_units), stream));
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(a.total_units, P.chunks), stream));
 }
 
 // bytes of the GEMM's split-tile areas (slots, tickets, masks)
