@@ -33,7 +33,7 @@ def header_functions():
     return sorted(set(names))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_core_calls():
     names = header_functions()
     for must in ("i2s_quantize_act", "i2s_mul_mat", "i8s_mul_mat_add_relu", "i8s_requant"):
         assert must in names
