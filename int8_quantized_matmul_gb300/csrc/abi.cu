@@ -578,21 +578,55 @@ static int64_t i8s_tiles(int64_t M, int64_t N, int tm) {   // half-tiles: 128 fe
 
 static int64_t i8s_chunks(int64_t K) { return (K + kI8sChunkK - 1) / kI8sChunkK; }
 
-// CTA pairs of a launch over `units` work units: the fewest that keep the
-// busiest pair's share of the resident pairs' split (ceil(units / resident)),
-// that share rounded up to whole tiles of `tile_units` units (a single
-// matmul's K chunks) when this adds at most a third. The pairs share L2
-// bandwidth, so the ones left idle cost little, while a tile cut between
-// pairs stores and reloads an 80 KB slot of sums per CTA: the encoder's FC1
-// (384 units, 2 per tile) runs as 64 pairs of 6 units, FC2 (8 per tile) as
-// 48 pairs of one whole tile each rather than 64 pairs of 6 units.
-static int i8s_grid_pairs(int64_t units, int64_t tile_units = 1) {
-    const int64_t resident = i8s_gemm_tc_max_pairs();
-    int64_t per_pair = (units + resident - 1) / resident;
-    const int64_t whole = (per_pair + tile_units - 1) / tile_units * tile_units;
-    if (3 * whole <= 4 * per_pair) per_pair = whole;
-    const int64_t pairs = (units + per_pair - 1) / per_pair;
-    return pairs < 1 ? 1 : (int)pairs;
+// Ranges of whole tiles, in order, of at most L units each (a tile of matmul
+// i is chunks_i units): the number of ranges, their bounds in `bounds`, or -1
+// when a tile is larger than L or more than `max_ranges` ranges are needed.
+static int pack_whole_tiles(const I8sTcArgs& a, int64_t L, int64_t max_ranges, int* bounds) {
+    int ranges = 0;
+    int64_t cur = 0, u = 0;
+    bounds[0] = 0;
+    for (int i = 0; i < a.count; ++i) {
+        const int64_t c = a.p[i].chunks, n = (int64_t)a.p[i].n_wt * a.n_at;
+        if (c > L) return -1;
+        for (int64_t t = 0; t < n; ++t) {
+            if (cur + c > L) {   // close the range before this tile
+                if (++ranges >= max_ranges) return -1;
+                bounds[ranges] = (int)u;
+                cur = 0;
+            }
+            cur += c;
+            u += c;
+        }
+    }
+    bounds[++ranges] = (int)u;
+    return ranges;
+}
+
+// The CTA pairs of a launch and their unit ranges (a.bounds; a.total_units
+// and the matmuls' tiles set). An even split over the resident pairs gives the
+// busiest pair L0 = ceil(units / resident) units. Whole tiles are packed into
+// ranges of at most L units for the smallest L in [L0, 4 L0 / 3] that needs
+// no more than the resident pairs, so that no tile is cut between pairs: a
+// cut tile stores and reloads an 80 KB slot of int32 sums per CTA, while the
+// pairs share L2 bandwidth and the ones left idle cost little. The encoder's
+// FC1 (tiles of 2 units) runs as 64 pairs of 3 tiles, FC2 (8 units) as 48
+// pairs of one tile. Without such an L, the units are split evenly over the
+// fewest pairs that keep L0.
+static int i8s_plan_pairs(I8sTcArgs& a) {
+    const int64_t units = a.total_units;
+    int64_t resident = i8s_gemm_tc_max_pairs();
+    resident = std::max<int64_t>(1, std::min<int64_t>(resident, kI8sMaxPairs));
+    const int64_t L0 = (units + resident - 1) / resident;
+    int64_t tiles = 0;
+    for (int i = 0; i < a.count; ++i) tiles += (int64_t)a.p[i].n_wt * a.n_at;
+    if (tiles <= 65536)   // bounds the host work of the search
+        for (int64_t L = L0; 3 * L <= 4 * L0; ++L) {
+            const int pairs = pack_whole_tiles(a, L, resident, a.bounds);
+            if (pairs > 0) return pairs;
+        }
+    const int pairs = (int)((units + L0 - 1) / L0);
+    for (int q = 0; q <= pairs; ++q) a.bounds[q] = (int)(((int64_t)q * units) / pairs);
+    return pairs;
 }
 
 // the tile height of a launch over these matmuls (the resident pairs decide)
@@ -667,7 +701,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;   // units of whole (256-feature) tiles
-    const int grid = 2 * i8s_grid_pairs(a.total_units, P.chunks);   // at most the resident pairs, clusters of two CTAs
+    const int grid = 2 * i8s_plan_pairs(a);   // at most the resident pairs, clusters of two CTAs
     r = cuda_status(launch_i8s_gemm_tc(a, grid, stream));
     if (r) return r;
     return cuda_status(launch_requant(yf, M * N, amax, static_cast<uint8_t*>(y_i8s), stream));
@@ -912,7 +946,7 @@ static int launch_w8a8_gemm(const __half* wf, const float* bscale, const float* 
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = (int)(tiles / 2) * P.chunks;
-    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(a.total_units, P.chunks), stream));
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_plan_pairs(a), stream));
 }
 
 // bytes of the GEMM's split-tile areas (slots, tickets, masks)
@@ -1126,7 +1160,7 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
     a.tile_m = tm;
     a.n_at = (int)(rows_pad / tm);
     a.total_units = units;
-    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_grid_pairs(units), stream));
+    return cuda_status(launch_i8s_gemm_tc(a, 2 * i8s_plan_pairs(a), stream));
 }
 
 size_t w8a8_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {

@@ -170,9 +170,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = tc::cluster_rank();   // 0: the leader, which issues the MMAs
-    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-    const int u_begin = (int)(((long long)pair * a.total_units) / n_pairs);
-    const int u_end = (int)(((long long)(pair + 1) * a.total_units) / n_pairs);
+    const int pair = blockIdx.x >> 1;
+    const int u_begin = a.bounds[pair];   // this pair's units, planned on the host
+    const int u_end = a.bounds[pair + 1];
     // stages of 128 positions; with K % 128 == 64 the last stage's second atom
     // lies past K, where the TMA box is zero-filled, which adds nothing to the
     // dot products

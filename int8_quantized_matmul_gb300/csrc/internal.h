@@ -185,6 +185,7 @@ inline int i8s_tile_m(int64_t M, const int64_t* N, const int64_t* K, int count, 
 // One matmul of a launch: its operand maps, scales, output and offsets into
 // the launch's split-tile areas.
 constexpr int kI8sMaxGroup = 8;
+constexpr int kI8sMaxPairs = 128;   // CTA pairs of one launch (a GB300 holds 76 at once)
 struct I8sProb {
     CUtensorMap xmap;          // f16 activations, rows_pad x K, box 64 x tile_m / 2, 128-byte swizzle
     CUtensorMap wmap;          // f16 weights, N x K, box 64 x kI8sTileN, 128-byte swizzle
@@ -211,6 +212,7 @@ struct I8sTcArgs {
     int count;                 // matmuls in the launch (1 .. kI8sMaxGroup), all with the same M
     int M, n_at, relu, total_units;
     int tile_m;                // activation rows per tile: kI8sTileM or kI8sTileMSmall
+    int bounds[kI8sMaxPairs + 1];   // CTA pair q runs units [bounds[q], bounds[q + 1])
 };
 static_assert(sizeof(I8sTcArgs) <= 32764, "I8sTcArgs exceeds the kernel parameter limit");
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
