@@ -78,18 +78,24 @@ __device__ __forceinline__ int stage_window(const uint8_t* row, int64_t L, int64
                                             int tid, int nthreads) {
     const int sh = (int)(((uintptr_t)row + (uintptr_t)pos0) & 3u);
     const int nw = (sh + nbytes + 3) >> 2;
-    for (int i = tid; i < nw; i += nthreads) {
+    auto word = [&](int i) {
         const int64_t g = pos0 - sh + 4 * (int64_t)i;   // row position of the word's first byte
-        uint32_t w;
-        if (g >= 0 && g + 4 <= L) {
-            w = *reinterpret_cast<const uint32_t*>(row + g);
-        } else {
-            w = 0;
+        if (g >= 0 && g + 4 <= L) return *reinterpret_cast<const uint32_t*>(row + g);
+        uint32_t w = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (g + e >= 0 && g + e < L) w |= (uint32_t)row[g + e] << (8 * e);
-        }
-        win32[i] = w;
+        for (int e = 0; e < 4; ++e)
+            if (g + e >= 0 && g + e < L) w |= (uint32_t)row[g + e] << (8 * e);
+        return w;
+    };
+    // four independent loads in flight per thread before any store: one load
+    // at a time left the staging latency-bound
+    for (int i0 = tid; i0 < nw; i0 += 4 * nthreads) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = i0 + e * nthreads < nw ? word(i0 + e * nthreads) : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i0 + e * nthreads < nw) win32[i0 + e * nthreads] = w[e];
     }
     return sh;
 }
