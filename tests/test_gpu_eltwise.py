@@ -129,7 +129,7 @@ def test_rms_norm_encoder_size(i2s, o):
 # transpose (cont of a permute): the scale travels with the values
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("a,b", [(1, 1), (1, 100), (5, 7), (64, 64), (65, 129), (300, 17), (1000, 2048)])
+@pytest.mark.parametrize("a,b", [(1, 1), (1, 100), (5, 7), (64, 64), (65, 129), (300, 17), (1000, 2048), (77, 1000), (600, 40)])
 def test_transpose(i2s, o, a, b):
     _, src = i8s_tensor(o, (a, b), seed=a * 7 + b)
     got = host(i2s.i8s_transpose(dev(src), a, b))
