@@ -371,18 +371,31 @@ __global__ void __launch_bounds__(kEltThreads) k_transpose(const uint8_t* __rest
         }
     }
     __syncthreads();
-    // destination row j0 + jr holds source rows i0 .. i0+TR-1 at column jr
-    for (int w = threadIdx.x; w < TC * kColWords; w += kEltThreads) {
-        const int jr = w / kColWords, k = w - jr * kColWords;
-        const uint32_t v = (uint32_t)tile[4 * k][jr] | ((uint32_t)tile[4 * k + 1][jr] << 8) |
-                           ((uint32_t)tile[4 * k + 2][jr] << 16) | ((uint32_t)tile[4 * k + 3][jr] << 24);
-        const int64_t j = j0 + jr, i = i0 + 4 * k;
-        if (full && (a & 3) == 0) {
-            *reinterpret_cast<uint32_t*>(dst + j * a + i) = v;
-        } else if (j < b) {
+    // destination row j0 + jr holds source rows i0 .. i0+TR-1 at column jr. A
+    // thread reads one word from each of source rows 4k .. 4k+3 (columns
+    // 4jq .. 4jq+3) and transposes the 4 x 4 bytes in registers: four output
+    // words, one in each of destination rows 4jq .. 4jq+3
+    for (int w = threadIdx.x; w < (TC / 4) * kColWords; w += kEltThreads) {
+        const int jq = w / kColWords, k = w - jq * kColWords;
+        const uint32_t r0 = *reinterpret_cast<const uint32_t*>(&tile[4 * k][4 * jq]);
+        const uint32_t r1 = *reinterpret_cast<const uint32_t*>(&tile[4 * k + 1][4 * jq]);
+        const uint32_t r2 = *reinterpret_cast<const uint32_t*>(&tile[4 * k + 2][4 * jq]);
+        const uint32_t r3 = *reinterpret_cast<const uint32_t*>(&tile[4 * k + 3][4 * jq]);
+        const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r0, r1, 0x7362);   // bytes 0,1 / 2,3
+        const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
+        const uint32_t v[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                               __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+        const int64_t i = i0 + 4 * k;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i + e < a) dst[j * a + i + e] = (uint8_t)(v >> (8 * e));
+        for (int c = 0; c < 4; ++c) {
+            const int64_t j = j0 + 4 * jq + c;
+            if (full && (a & 3) == 0) {
+                *reinterpret_cast<uint32_t*>(dst + j * a + i) = v[c];
+            } else if (j < b) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (i + e < a) dst[j * a + i + e] = (uint8_t)(v[c] >> (8 * e));
+            }
         }
     }
     if (blockIdx.x == 0) {
