@@ -265,6 +265,8 @@ static void i2s_features(const I2SJob* j, int tid, int nth) {
                 const float r = (float)d * (j->w_scale * j->act_scale[m]);
 #elif ORC_PLANT == 10
                 const float r = (float)(d - j->row_sum[m]) * (j->w_scale * j->act_scale[0]);
+#elif ORC_PLANT == 21
+                const float r = (float)(d - j->row_sum[m]) * j->w_scale * j->act_scale[m];
 #else
                 const float r = (float)(d - j->row_sum[m]) * (j->w_scale * j->act_scale[m]);
 #endif
@@ -374,6 +376,9 @@ ORC_API void orc_i8s_mul_mat_add(const uint8_t* w_i8s, int64_t N, int64_t K,
                     v = v * sc;
 #elif ORC_PLANT == 13
                     float v = (float)(int32_t)acc * ws;
+                    if (bias) v = v + bias[n];
+#elif ORC_PLANT == 22
+                    float v = (float)(int32_t)acc * ws * xs;
                     if (bias) v = v + bias[n];
 #else
                     float v = (float)(int32_t)acc * sc;
@@ -609,6 +614,8 @@ ORC_API void orc_w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, 
                     }
 #if ORC_PLANT == 19
                     d[m * N + n] = bscale[n] * (float)(int32_t)acc;
+#elif ORC_PLANT == 23
+                    d[m * N + n] = as[m] * (bscale[n] * (float)(int32_t)acc);
 #else
                     d[m * N + n] = as[m] * bscale[n] * (float)(int32_t)acc;
 #endif

@@ -501,4 +501,83 @@ def pin_w8a8_mul_mat_pow2(o):
     assert q[0, 3] == 127 and s[0] == np.float32(1e-7) / np.float32(127.0)
 
 
+# ---------------------------------------------------------------------------
+# epilogue association (non-power-of-two scales)
+# ---------------------------------------------------------------------------
+
+def _rle(tokens, conv=float):
+    out = []
+    for t in tokens:
+        v, _, n = t.partition("*")
+        out.extend([conv(v)] * (int(n) if n else 1))
+    return out
+
+
+def _hex_f32(tok: str) -> np.float32:
+    return np.array([int(tok, 16)], dtype=np.uint32).view(np.float32)[0]
+
+
+def epilogue_cases():
+    return {c["name"]: c for c in load_cases("epilogue_association.txt")}
+
+
+def pin_i2s_epilogue_association(o):
+    # tests/golden/epilogue_association.txt, case i2s_epilogue: the page's
+    # (float)(dot - row_sum) * (w_scale * act_scale) worked out by hand for
+    # scales where the product order decides the last bit.
+    c = epilogue_cases()["i2s_epilogue"]
+    K = int(c["K"][0])
+    codes = np.array([_rle(c[f"codes{i}"], int) for i in range(3)], dtype=np.uint8)
+    x = np.array(_rle(c["x"]), dtype=np.float32)[None, :]
+    assert codes.shape == (3, K) and x.shape == (1, K)
+    w_scale = _hex_f32(c["w_scale"][0])
+    want = np.array([int(v, 16) for v in c["y"]], dtype=np.uint32)
+    # the fixture discriminates: the left-to-right order gives other bits
+    D = np.array([int(v) for v in c["dot_minus_row_sum"]], dtype=np.float32)
+    act_scale = _hex_f32("0x3C010204")
+    wrong = ((D * w_scale).astype(np.float32) * act_scale).astype(np.float32)
+    assert not np.any(wrong.view(np.uint32) == want)
+    packed = o.i2s_pack(codes, float(w_scale))
+    y, q, s, rs, dot = o.i2s_mul_mat(packed, 3, K, x, want_sidecar=True)
+    assert f32_bits(s[0]) == 0x3C010204 and int(rs[0]) == 8255
+    assert np.array_equal(dot[0].astype(np.int64) - int(rs[0]), D.astype(np.int64))
+    assert np.array_equal(y[0].view(np.uint32), want), [hex(v) for v in y[0].view(np.uint32)]
+
+
+def pin_i8s_epilogue_association(o):
+    # case i8s_epilogue: (float)acc * (w_scale * x_scale) + bias, by hand
+    c = epilogue_cases()["i8s_epilogue"]
+    K = int(c["K"][0])
+    X = np.array([int(v) for v in c["x"]], dtype=np.int8)[None, :]
+    W = np.array([[int(v) for v in c[f"w{i}"]] for i in range(2)], dtype=np.int8)
+    bias = np.array([_hex_f32(v) for v in c["bias"]], dtype=np.float32)
+    ws, xs = _hex_f32(c["w_scale"][0]), _hex_f32(c["x_scale"][0])
+    want = np.array([int(v, 16) for v in c["y"]], dtype=np.uint32)
+    acc = (X.astype(np.int64) @ W.astype(np.int64).T)[0]
+    assert acc.tolist() == [int(v) for v in c["acc"]]
+    wrong = (((acc.astype(np.float32) * ws).astype(np.float32) * xs).astype(np.float32) + bias).astype(np.float32)
+    assert not np.any(wrong.view(np.uint32) == want)
+    for relu in (False, True):
+        _, yf = o.i8s_mul_mat_add(o.i8s_pack(W, float(ws)), 2, K, o.i8s_pack(X, float(xs)), 1, bias=bias,
+                                  relu=relu)
+        assert np.array_equal(yf[0].view(np.uint32), want), (relu, [hex(v) for v in yf[0].view(np.uint32)])
+
+
+def pin_w8a8_epilogue_association(o):
+    # case w8a8_epilogue: (aScale * bScale) * (float)C, by hand
+    c = epilogue_cases()["w8a8_epilogue"]
+    K = int(c["K"][0])
+    x = np.array([float(v) for v in c["x"]], dtype=np.float32)[None, :]
+    wq = np.array([[int(v) for v in c[f"wq{i}"]] for i in range(2)], dtype=np.int8)
+    bs = np.array([_hex_f32(v) for v in c["b_scale"]], dtype=np.float32)
+    want = np.array([int(v, 16) for v in c["d"]], dtype=np.uint32)
+    d, q, s = o.w8a8_mul_mat(wq, bs, x, want_sidecar=True)
+    assert q[0].tolist() == [int(v) for v in c["q"]] and f32_bits(s[0]) == 0x3C010204
+    acc = (q.astype(np.int64) @ wq.astype(np.int64).T)[0]
+    assert acc.tolist() == [int(v) for v in c["acc"]]
+    wrong = (s[0] * (bs * acc.astype(np.float32)).astype(np.float32)).astype(np.float32)
+    assert not np.any(wrong.view(np.uint32) == want)
+    assert np.array_equal(d[0].view(np.uint32), want), [hex(v) for v in d[0].view(np.uint32)]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

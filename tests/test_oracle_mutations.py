@@ -3,8 +3,9 @@
 Each ORC_PLANT value compiles oracle.cpp with one plausible mistake (a wrong
 shift order, a dropped term, a reciprocal scale, ties-to-even rounding, a
 missing floor, a transposed output, a lost scale, int16 overflow, a wrong row
-scale, a wrong epilogue order, a missing ReLU, a dropped input scale). The test
-proves the pins are strong enough to notice each one.
+scale, a wrong epilogue order, a missing ReLU, a dropped input scale, a scale
+product associated the other way). The test proves the pins are strong enough
+to notice each one.
 """
 
 import os
@@ -37,6 +38,9 @@ PLANTS = {
     18: ["pin_i8s_depthwise_pow2"],        # kernel taps reversed (convolution)
     19: ["pin_w8a8_mul_mat_pow2"],         # row scale dropped
     20: ["pin_w8a8_weight_quant"],         # weight ties rounded away from zero
+    21: ["pin_i2s_epilogue_association"],  # (dot - row_sum) * w_scale * act_scale, left to right
+    22: ["pin_i8s_epilogue_association"],  # acc * w_scale * x_scale, left to right
+    23: ["pin_w8a8_epilogue_association"],  # aScale * (bScale * C)
 }
 
 
