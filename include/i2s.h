@@ -152,12 +152,16 @@ int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t
 
 /* Launch-shape overrides for testing and tuning. Every setting gives the same
  * bits; zero fields mean "choose automatically". */
+enum {
+    I2S_PATH_AUTO = 0,   /* M <= 16: the GEMV, else the GEMM */
+    I2S_PATH_GEMM = 2,   /* tensor-core GEMM, any M */
+    I2S_PATH_GEMV = 3    /* tensor-core GEMV, M <= 16 (BAD_ARG above) */
+};
 typedef struct i2s_config {
-    int path;        /* 0 auto (M <= 16: 3, else 2); 1 warp-MMA GEMV (any M, in slices of 16
-                        rows); 2 tensor-core GEMM; 3 tensor-core GEMV (M <= 16) */
-    int split_k;     /* GEMV: CTAs sharing one row block along K (1, 2, 4, 8) */
-    int rows_per_cta;/* GEMV: weight rows per CTA tile (multiple of 16) */
-    int grid_ctas;   /* paths 2 and 3: persistent CTA count (<= SM count, 2x for path 3; path 2 runs CTA pairs: rounded down to an even count, at least 2) */
+    int path;        /* I2S_PATH_*; any other value is BAD_ARG */
+    int grid_ctas;   /* persistent CTA count: GEMV at most 2 per SM; GEMM runs CTA pairs
+                        (rounded down to an even count, at least 2, at most the pairs that
+                        fit at once) */
 } i2s_config;
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,
@@ -165,8 +169,7 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
 
 /* ---------------------------------------------------------------------------
  * Decode I2_S matmul without a workspace. The pages have no counterpart of
- * this call: ggml always hands its kernels a work buffer (params->wdata). It
- * exists for callers that cannot provide device scratch memory: a plain C or
+ * this call. It exists for callers that cannot provide device scratch memory: a plain C or
  * ctypes host with no device allocator of its own, or a serving loop that
  * must not allocate once it runs, because cudaMalloc and cudaFree can
  * synchronize the device and a fixed memory budget leaves no room for
@@ -184,9 +187,12 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
  * 8960, a 151936-row output head at K = 1536) fits.
  *
  * Set-up: the first call made with a device current loads the array on that
- * device and looks up its address. Make that first call (for example one
- * warm-up call) before capturing any stream, and before the point from which
- * the caller cannot tolerate set-up work.
+ * device and looks up its address, which later calls on that device reuse.
+ * Make that first call (for example one warm-up call) before capturing any
+ * stream, and before the point from which the caller cannot tolerate set-up
+ * work. A device reset (cudaDeviceReset) unloads the array and invalidates
+ * that address: a process that resets a device must not call this entry
+ * point on that device again.
  * Races: every call on a device uses the same array, so calls whose work can
  * overlap on the GPU race and give wrong results. Order all calls on one
  * device, for example on a single stream.

@@ -19,7 +19,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libi2s.so")
 BUILD = os.path.join(HERE, "_build")
 
-SOURCES = ["abi.cu", "quant.cu", "gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "i8s.cu", "i8s_tc.cu", "i8s_elt.cu",
+SOURCES = ["abi.cu", "quant.cu", "gemv_tc.cu", "gemm_tc.cu", "i8s.cu", "i8s_tc.cu", "i8s_elt.cu",
            "noalloc.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

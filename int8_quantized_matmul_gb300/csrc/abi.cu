@@ -56,8 +56,8 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? I2S_OK : I2S_E_CUDA; 
 
 // ---------------------------------------------------------------------------
 // I2_S workspace: [header][act_scale M][row_sum M][operand][dot_acc M*N][tickets]
-// The operand is large enough for either matmul path: the GEMV's e4m3 records
-// (2*Kp bytes per row, Kp = K rounded up to 256) or the GEMM's f16 rows.
+// The operand is large enough for either matmul path: the GEMV's e2m1 digit
+// rows or the GEMM's f16 rows (2 bytes per position, K rounded up to 256).
 // ---------------------------------------------------------------------------
 struct ActSlot {
     size_t scale_off, sum_off, op_off;
@@ -65,7 +65,7 @@ struct ActSlot {
 
 size_t act_slot_bytes(int64_t M, int64_t K) {
     const int64_t Kp = round_up(K, 256);
-    size_t op = (size_t)M * (size_t)Kp * 2;                      // GEMV records / GEMM f16 rows
+    size_t op = (size_t)M * (size_t)Kp * 2;                      // GEMM f16 rows
     if (M <= 16) {
         const size_t tc = (size_t)gemv_tc_op_rows(gemv_tc_mp(M)) * (size_t)(K / 2);   // GEMV tensor-core operand
         if (tc > op) op = tc;
@@ -88,13 +88,6 @@ bool i2s_shape_ok(int64_t N, int64_t K, int64_t M) {
     return true;
 }
 
-int pick_split_k(int N, int K, int sms) {
-    const int tiles = (N + kGemvTileRows - 1) / kGemvTileRows;
-    const int KB = (K + 255) / 256;
-    int s = 1;
-    while (s < 8 && tiles * s < sms && s * 2 <= KB) s *= 2;
-    return s;
-}
 
 }  // namespace
 
@@ -203,8 +196,7 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
 }
 
 // Split-K partial area of one problem: M x N int32 partial dots and one chunk
-// counter per 128-row tile (also large enough for the warp-MMA GEMV's
-// 512-row tiles).
+// counter per 128-row tile.
 static size_t split_area_bytes(int64_t M, int64_t N) {
     const size_t tiles = (size_t)((N + kTcTileW - 1) / kTcTileW);
     return align_up((size_t)M * (size_t)N * 4) + align_up(tiles * 4);
@@ -228,74 +220,11 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     if (r) return r;
 
     const int path = config ? config->path : 0;
-    if (path < 0 || path > 3) return I2S_E_BAD_ARG;
+    if (path != 0 && path != 2 && path != 3) return I2S_E_BAD_ARG;
     if (path == 3 && M > 16) return I2S_E_BAD_ARG;
-    if (path == 2 || (path == 0 && M > 16)) {
-        i2s_problem p{w_i2s, N, K, x, y};
-        return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
-    }
-    if (path == 3 || path == 0) {
-        i2s_problem p{w_i2s, N, K, x, y};
-        return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
-    }
-
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    const ActSlot slot = act_slot_at(kHeader, M);
-    const size_t dot_off = kHeader + act_slot_bytes(M, K);
-    const size_t tick_off = dot_off + align_up((size_t)M * (size_t)N * 4);
-    const int Kp = (int)round_up(K, 256);
-
-    QuantArgs qa;
-    qa.wmaps = nullptr;
-    qa.n_wmaps = 0;
-    qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
-    qa.zero = nullptr;
-    qa.zero_16 = 0;
-    qa.count = 1;
-    qa.M = (int)M;
-    qa.rows = (int)M;
-    qa.layout = kQuantE4M3Frag;
-    qa.j[0] = QuantJob{x, base + slot.op_off, reinterpret_cast<float*>(base + slot.scale_off),
-                       reinterpret_cast<int32_t*>(base + slot.sum_off), (int)K, Kp};
-    r = cuda_status(launch_quant(qa, stream));
-    if (r) return r;
-
-    const int sms = device_sm_count();
-    int split = config && config->split_k > 0 ? config->split_k : pick_split_k((int)N, (int)K, sms);
-    if (split > 8) split = 8;
-    if (split > 1) {
-        const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
-        r = cuda_status(cudaMemsetAsync(base + dot_off, 0, tick_off - dot_off + tiles * 4, stream));
-        if (r) return r;
-    }
-    // Activation rows are processed in slices of at most 16 (one launch each).
-    static thread_local GemvArgs ga;
-    for (int64_t m0 = 0; m0 < M; m0 += 16) {
-        const int mm = (int)(M - m0 < 16 ? M - m0 : 16);
-        ga.count = 1;
-        ga.M = mm;
-        ga.split_k = split;
-        GemvProb& p = ga.p[0];
-        p.w = static_cast<const uint8_t*>(w_i2s);
-        p.act = reinterpret_cast<const uint32_t*>(base + slot.op_off) + (size_t)m0 * (Kp / 2);
-        p.act_scale = reinterpret_cast<const float*>(base + slot.scale_off) + m0;
-        p.row_sum = reinterpret_cast<const int32_t*>(base + slot.sum_off) + m0;
-        p.y = y + (size_t)m0 * N;
-        p.dot_acc = reinterpret_cast<int32_t*>(base + dot_off) + (size_t)m0 * N;
-        p.tickets = reinterpret_cast<uint32_t*>(base + tick_off);
-        p.N = (int)N;
-        p.K = (int)K;
-        p.tile0 = 0;
-        if (split > 1 && m0 > 0) {
-            // each slice reuses the ticket counters: clear them between slices
-            const size_t tiles = (size_t)((N + kGemvTileRows - 1) / kGemvTileRows);
-            r = cuda_status(cudaMemsetAsync(base + tick_off, 0, tiles * 4, stream));
-            if (r) return r;
-        }
-        r = cuda_status(launch_gemv(ga, gemv_ctas_for((int)N, split), stream));
-        if (r) return r;
-    }
-    return I2S_OK;
+    i2s_problem p{w_i2s, N, K, x, y};
+    if (path == 2 || (path == 0 && M > 16)) return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
+    return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
 }
 
 int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
@@ -395,10 +324,8 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
 }
 
 // Tensor-core GEMV path (M <= 16): phase 1 quantizes every distinct activation
-// into the e4m3 hi/lo operand rows, phase 2 runs one persistent launch over all
+// into the e2m1 digit operand rows, phase 2 runs one persistent launch over all
 // problems (two CTAs per SM). Arguments are validated by the callers.
-// Unit shares of the first and second CTA on an SM for a full GEMV grid.
-constexpr int kGemvShareFirst = 23, kGemvShareSecond = 17;
 
 static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
                        i2s_stream_t stream, int phases) {

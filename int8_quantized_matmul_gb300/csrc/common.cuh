@@ -46,25 +46,6 @@ __device__ __forceinline__ void quant_params(float amax, float& scale, float& in
     inv = __fdiv_rn(127.0f, amax);
 }
 
-// e4m3 bit pattern of a small integer v, |v| <= 15. Every such v is exact in
-// e4m3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits).
-__host__ __device__ constexpr int ilog2_upto15(int a) { return a >= 8 ? 3 : a >= 4 ? 2 : a >= 2 ? 1 : 0; }
-
-__host__ __device__ constexpr uint8_t e4m3_small_int(int v) {
-    const int a = v < 0 ? -v : v;
-    if (a == 0) return 0;
-    const int e = ilog2_upto15(a);
-    return (uint8_t)((v < 0 ? 0x80 : 0) | ((e + 7) << 3) | (((a << 3) >> e) & 7));
-}
-
-// e4m3 pattern of 16*v for v in [-8, 7]: the exponent of v raised by 4.
-__host__ __device__ constexpr uint8_t e4m3_times16(int v) {
-    return v == 0 ? 0 : (uint8_t)(e4m3_small_int(v) + (4 << 3));
-}
-
-static_assert(e4m3_small_int(1) == 0x38 && e4m3_small_int(3) == 0x44 && e4m3_small_int(15) == 0x57, "e4m3");
-static_assert(e4m3_times16(-8) == 0xF0 && e4m3_times16(7) == 0x6E, "e4m3 x16");
-
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialization is scheduled as the CTAs of the kernel before it on the
 // stream retire, instead of after that kernel's completion is processed;
@@ -104,16 +85,6 @@ __device__ __forceinline__ int warp_sum(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// Legacy warp-level e4m3 MMA with fp32 accumulation: 16x8x32 per warp.
-__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {

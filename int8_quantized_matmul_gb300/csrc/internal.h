@@ -17,7 +17,6 @@ constexpr int kMaxGroup = 256;   // same value as I2S_MAX_GROUP
 // ---------------------------------------------------------------------------
 enum QuantLayout : int {
     kQuantI8Rows = 0,    // plain int8, row-major M x K (the public sidecar)
-    kQuantE4M3Frag = 1,  // GEMV operand records (see gemv.cu), 2*Kp bytes per row
     kQuantF16Perm = 2,   // tensor-core GEMM operand: f16, K permuted per 128-group
     kQuantE2M1Tc = 3,    // tensor-core GEMV operand: e2m1 digit rows (gemv_tc.cu), gemv_tc_op_rows(M') x K/2 bytes
 };
@@ -28,7 +27,7 @@ struct QuantJob {
     float* scale;     // M
     int32_t* sum;     // M
     int K;
-    int Kp;           // K rounded up to the layout's padding (GEMV: 256)
+    int Kp;           // row stride of the operand in elements (K for every layout in use)
 };
 
 // A weight matrix whose TMA tensor map the quantization launch writes for the
@@ -55,36 +54,6 @@ struct QuantArgs {
 };
 
 cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
-
-// ---------------------------------------------------------------------------
-// Decode GEMV (M <= 16) on the legacy e4m3 warp MMA.
-// ---------------------------------------------------------------------------
-constexpr int kGemvWarps = 8;
-constexpr int kGemvRowsPerWarp = 64;
-constexpr int kGemvTileRows = kGemvWarps * kGemvRowsPerWarp;   // 512 weight rows per CTA
-
-struct GemvProb {
-    const uint8_t* w;         // I2_S bytes, N x K/4 payload then the scale trailer
-    const uint32_t* act;      // e4m3 operand records, M rows x (2*Kp) bytes
-    const float* act_scale;   // M
-    const int32_t* row_sum;   // M
-    float* y;                 // M x N
-    int32_t* dot_acc;         // split-K only: M x N int32, zeroed before launch
-    uint32_t* tickets;        // split-K only: one counter per row tile, zeroed
-    int N;
-    int K;
-    int tile0;                // first linear CTA of this problem
-};
-
-struct GemvArgs {
-    int count;
-    int M;
-    int split_k;
-    GemvProb p[kMaxGroup];
-};
-
-int gemv_ctas_for(int N, int split_k);
-cudaError_t launch_gemv(const GemvArgs& a, int total_ctas, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Prefill GEMM (M > 16) on tcgen05 (gemm_tc.cu).
@@ -126,6 +95,10 @@ struct TcArgs {
 };
 
 constexpr int kGemvChunkPositions = 1536;   // K positions per GEMV work unit
+// Relative unit shares of the first and second CTA placed on each SM when the
+// GEMV grid is full (two CTAs per SM): the first is issued ahead of the second,
+// and this split was measured to let both finish together.
+constexpr int kGemvShareFirst = 23, kGemvShareSecond = 17;
 
 // Tensor-core GEMV activation operand: M' = 8 (M <= 8) or 16 activation rows,
 // each split into three base-8 digit rows (digit j of row m at row j*M' + m),
@@ -135,7 +108,6 @@ __host__ __device__ constexpr int gemv_tc_op_rows(int Mp) { return Mp == 8 ? 32 
 
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(TcArgs) <= 32764, "TcArgs exceeds the kernel parameter limit");
-static_assert(sizeof(GemvArgs) <= 32764, "GemvArgs exceeds the kernel parameter limit");
 static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
 
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);

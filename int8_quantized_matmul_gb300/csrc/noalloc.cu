@@ -152,10 +152,11 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     p.dot_off = 0;
     p.ticket_off = 0;
     ta.total_tiles = row_tiles * chunks;
-    ta.share_first = 1;
-    ta.share_second = 1;
-    int grid = 2 * (d->sms > 0 ? d->sms : 152);
-    if (grid > ta.total_tiles) grid = ta.total_tiles;
+    const int cap = 2 * (d->sms > 0 ? d->sms : 152);
+    const int grid = ta.total_tiles < cap ? ta.total_tiles : cap;
+    // the same split of units between the two CTAs of an SM as the workspace path
+    ta.share_first = grid == cap ? kGemvShareFirst : 1;
+    ta.share_second = grid == cap ? kGemvShareSecond : 1;
     if (launch_gemv_tc(ta, grid, stream) != cudaSuccess) return I2S_E_CUDA;
     return I2S_OK;
 }

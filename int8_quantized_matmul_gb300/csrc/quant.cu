@@ -8,9 +8,6 @@
 // same way) are written out. Besides the plain int8 layout of the public sidecar, the kernel can
 // write the operand layouts of the two matmul kernels directly, so no separate
 // repacking pass is needed:
-//   kQuantE4M3Frag  the decode GEMV's B operand: each q is split exactly into
-//                   16*(q>>4) and (q&15), both exact in e4m3, stored in the
-//                   warp-MMA fragment order (see gemv.cu);
 //   kQuantF16Perm   the tensor-core GEMM's activation operand: q as f16 in the
 //                   K order in which the GEMM expands the packed codes;
 //   kQuantE2M1Tc    the tensor-core GEMV's operand: each q as three base-8
@@ -20,24 +17,6 @@
 #include "internal.h"
 
 namespace i2s {
-
-// Word index, inside one row's GEMV operand records, of the e4m3 byte quad that
-// holds positions p..p+3 (p % 4 == 0). A record covers 256 positions (64 bytes
-// of codes per weight row) for one lane quad t; see gemv.cu for the matching
-// fragment layout. Returns the index of the "high" word; the "low" word is +2.
-__device__ __forceinline__ int frag_word(int p) {
-    const int kb = p >> 8;          // 256-position block
-    const int r = p & 255;
-    const int half = r >> 7;        // which 32-byte group of the block
-    const int p2 = r & 127;         // group-relative position
-    const int slice = p2 >> 5;      // bit-pair slice: shift 6, 4, 2, 0
-    const int gp = p2 & 31;         // byte within the group
-    const int t = 2 * half + (gp >> 4);
-    const int i = (gp >> 2) & 3;    // 32-bit word within the lane's 16 bytes
-    const int h = slice >> 1;       // MMA pair: shifts (6,4) or (2,0)
-    const int b = slice & 1;        // first or second k-half of the MMA
-    return (kb * 4 + t) * 32 + 4 * (2 * i + h) + b;
-}
 
 // K position of the f16 element at index e of a 128-group in the tensor-core
 // operand order. The GEMM expands one 32-bit word of packed codes (bytes
@@ -61,17 +40,6 @@ __device__ __forceinline__ void emit4(const QuantArgs& a, const QuantJob& J, int
         uint32_t* q4 = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(J.out) + (size_t)m * K);
         q4[c] = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
                 ((uint32_t)(q[3] & 0xff) << 24);
-    } else if (a.layout == kQuantE4M3Frag) {
-        uint32_t* rec = static_cast<uint32_t*>(J.out) + (size_t)m * (J.Kp / 2);
-        uint32_t hi = 0, lo = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            hi |= (uint32_t)e4m3_times16(q[e] >> 4) << (8 * e);
-            lo |= (uint32_t)e4m3_small_int(q[e] & 15) << (8 * e);
-        }
-        const int wi = frag_word(4 * c);
-        rec[wi] = hi;
-        rec[wi + 2] = lo;
     } else {   // kQuantF16Perm
         __half* out = static_cast<__half*>(J.out) + (size_t)m * K;
         const int pos0 = 4 * c;
@@ -137,10 +105,6 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
         const int q[4] = {quantize_one(v.x, inv), quantize_one(v.y, inv), quantize_one(v.z, inv), quantize_one(v.w, inv)};
         sum += q[0] + q[1] + q[2] + q[3];
         emit4(a, J, m, c, q);
-    }
-    if (a.layout == kQuantE4M3Frag) {   // zero records of the padding positions K..Kp-1
-        const int zero[4] = {0, 0, 0, 0};
-        for (int c = K4 + tid; c < J.Kp / 4; c += kQThreads) emit4(a, J, m, c, zero);
     }
     sum = warp_sum(sum);
     if (lane == 0) s_sum[warp] = sum;

@@ -36,7 +36,7 @@ STATUS = {0: "I2S_OK", -1: "I2S_E_BAD_SHAPE", -2: "I2S_E_NULL_PTR", -3: "I2S_E_M
 
 
 class i2s_config(ctypes.Structure):
-    _fields_ = [("path", _int), ("split_k", _int), ("rows_per_cta", _int), ("grid_ctas", _int)]
+    _fields_ = [("path", _int), ("grid_ctas", _int)]
 
 
 class i2s_problem(ctypes.Structure):
@@ -189,16 +189,17 @@ def i2s_mul_mat_workspace(M: int, N: int, K: int) -> int:
     return int(_L.i2s_mul_mat_workspace(M, N, K))
 
 
-def i2s_mul_mat(w, N: int, K: int, x, y=None, ws=None, path: int = 0, split_k: int = 0):
-    """y (M x N F32) = I2_S weights w (N x K, device bytes) times x (M x K F32)."""
+def i2s_mul_mat(w, N: int, K: int, x, y=None, ws=None, path: int = 0, grid_ctas: int = 0):
+    """y (M x N F32) = I2_S weights w (N x K, device bytes) times x (M x K F32).
+    path / grid_ctas: the i2s_config overrides (0 = automatic)."""
     torch = _torch()
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     if ws is None:
         ws = _ws(i2s_mul_mat_workspace(M, N, K), x.device)
-    if path or split_k:
-        cfg = i2s_config(path, split_k, 0, 0)
+    if path or grid_ctas:
+        cfg = i2s_config(path, grid_ctas)
         rc = _L.i2s_mul_mat_ex(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), ctypes.byref(cfg),
                                _stream())
     else:

@@ -129,7 +129,7 @@ def test_i2s_gemv_tc_grid_sizes(i2s, o, M, grid, K):
     x = synth.normal_f32((M, K), seed=M + 1, outlier_p=0.01)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     ws = torch.empty(i2s.i2s_mul_mat_workspace(M, N, K), dtype=torch.uint8, device="cuda")
-    cfg = i2s.i2s_config(3, 0, 0, grid)
+    cfg = i2s.i2s_config(3, grid)
     wd, xd = dev(packed), dev(x)   # keep the device buffers alive across the call
     for _ in range(2):   # twice: the partial buffers are re-zeroed by each call
         rc = i2s.lib.i2s_mul_mat_ex(wd.data_ptr(), N, K, xd.data_ptr(), M, y.data_ptr(), ws.data_ptr(),
@@ -141,38 +141,62 @@ def test_i2s_gemv_tc_grid_sizes(i2s, o, M, grid, K):
 
 @pytest.mark.parametrize("M", [1, 8, 16])
 def test_i2s_gemv_paths_agree(i2s, o, M):
-    # the warp-MMA GEMV (path 1), the tensor-core GEMV (3) and GEMM (2) give the same bits
+    # the tensor-core GEMV (path 3) and GEMM (path 2) give the same bits
     c = synth.codes(300, 1536, seed=60 + M)
     packed = o.i2s_pack(c, 0.02)
     x = synth.normal_f32((M, 1536), seed=61 + M)
     want = o.i2s_mul_mat(packed, 300, 1536, x)
-    for path in (1, 2, 3):
+    for path in (2, 3):
         same_bits(host(i2s.i2s_mul_mat(dev(packed), 300, 1536, dev(x), path=path)), want)
 
 
-@pytest.mark.parametrize("split", [1, 2, 3, 4, 8])
-def test_i2s_split_k_gives_identical_bits(i2s, o, split):
-    got, want = run_i2s(i2s, o, 1100, 1536, 8, seed=77, path=1, split_k=split)
+@pytest.mark.parametrize("grid", [1, 2, 3, 4, 8, 0])
+def test_i2s_split_k_gives_identical_bits(i2s, o, grid):
+    # the shipped GEMV splits each 128-row tile into 1536-position K chunks;
+    # small grids give each CTA a range that starts or ends inside a tile, so
+    # partial dots from several CTAs meet in the integer split-K buffer
+    got, want = run_i2s(i2s, o, 1100, 8960, 8, seed=77, path=3, grid_ctas=grid)
     same_bits(got, want)
 
 
 @pytest.mark.parametrize("M", [9, 17, 40])
-def test_i2s_gemv_row_slices(i2s, o, M):
-    got, want = run_i2s(i2s, o, 300, 1152, M, seed=M, path=1)
+def test_i2s_row_counts_around_the_gemv_limit(i2s, o, M):
+    # 9 rows: the GEMV's 16-row operand; 17 and 40: the GEMM's ragged tiles
+    got, want = run_i2s(i2s, o, 300, 1152, M, seed=M)
     same_bits(got, want)
 
 
-def test_i2s_headroom_k8960(i2s, o):
-    # every code 2 and every activation quantizing to +127 (x = 1.0)
-    K, N, M = 8960, 1536, 64
+@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_i2s_headroom_k8960(i2s, o, M, grid):
+    # every code 2 and every activation quantizing to +127 (x = 1.0) on the
+    # shipped decode path: q = 127 becomes the digits (-1, 0, 2) of the GEMV's
+    # operand, and dot = 254 K = 2,275,840 comes from six K chunks per tile;
+    # grid 7 cuts tiles between CTAs, so the split-K sums meet at the extreme
+    K, N = 8960, 1536
     packed = o.i2s_pack(np.full((N, K), 2, np.uint8), 0.05)
     x = np.ones((M, K), np.float32)
-    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x), path=1))
+    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x), path=3, grid_ctas=grid))
     small = o.i2s_mul_mat(o.i2s_pack(np.full((4, K), 2, np.uint8), 0.05), 4, K, x[:2])
     assert (small == small[0, 0]).all()
     assert (y.view(np.uint32) == small[0, 0].view(np.uint32)).all()
     act_scale = np.float32(1.0) / np.float32(127.0)
     assert small[0, 0] == np.float32(127 * K) * (np.float32(0.05) * act_scale)
+
+
+@pytest.mark.parametrize("M", [1, 64])
+def test_i2s_epilogue_association_golden(i2s, o, M):
+    # the hand-derived epilogue case (scales that are not powers of two, so the
+    # order of the scale product decides the last bit) on the GPU, compared
+    # with the fixture's bits directly: M = 1 runs the GEMV, M = 64 the GEMM
+    c = pins.epilogue_cases()["i2s_epilogue"]
+    K = int(c["K"][0])
+    codes = np.array([pins._rle(c[f"codes{i}"], int) for i in range(3)], dtype=np.uint8)
+    x = np.repeat(np.array(pins._rle(c["x"]), dtype=np.float32)[None, :], M, axis=0)
+    packed = o.i2s_pack(codes, float(pins._hex_f32(c["w_scale"][0])))
+    y = host(i2s.i2s_mul_mat(dev(packed), 3, K, dev(x)))
+    want = np.array([int(v, 16) for v in c["y"]], dtype=np.uint32)
+    assert (y.view(np.uint32) == want[None, :]).all(), [hex(v) for v in y[0].view(np.uint32)]
 
 
 def test_i2s_degenerate(i2s, o):
@@ -337,7 +361,7 @@ def test_i2s_gemm_grid_sizes_give_identical_bits(i2s, o, grid):
     x = synth.normal_f32((300, 1536), seed=5, outlier_p=0.01)
     y = torch.empty((300, 700), dtype=torch.float32, device="cuda")
     ws = torch.empty(i2s.i2s_mul_mat_workspace(300, 700, 1536), dtype=torch.uint8, device="cuda")
-    cfg = i2s.i2s_config(2, 0, 0, grid)
+    cfg = i2s.i2s_config(2, grid)
     import ctypes
     wd, xd = dev(packed), dev(x)   # keep the device buffers alive across the call
     rc = i2s.lib.i2s_mul_mat_ex(wd.data_ptr(), 700, 1536, xd.data_ptr(), 300, y.data_ptr(), ws.data_ptr(),
@@ -487,27 +511,17 @@ def test_i8s_headroom(i2s, o):
 
 
 @pytest.mark.parametrize("N,K,relu", [(8192, 2048, True), (2048, 8192, False)])
-def test_i8s_encoder_fc_sampled(i2s, o, N, K, relu):
-    """Encoder FC1 (2048 -> 8192, ReLU) / FC2 (8192 -> 2048) at L = 900 frames:
-    sampled rows against the oracle, the requantization checked as a property
-    of the whole output."""
+def test_i8s_encoder_fc_full(i2s, o, N, K, relu):
+    """Encoder FC1 (2048 -> 8192, ReLU) / FC2 (8192 -> 2048) at L = 900 frames,
+    every F32 output and every I8_S byte (values, padding and the in-band
+    scale) against the oracle."""
     M = 900
     wp, xp, bias = i8s_inputs(o, M, N, K, seed=N)
     y8, ws = i2s.i8s_mul_mat_add_relu(dev(wp), N, K, dev(xp), M, bias=dev(bias), relu=relu)
-    yf = host(i2s.i8s_ws_f32(ws, M, N))
-    q_all, x_scale = o.i8s_unpack(xp, M * K)
-    for m0 in (0, 451, M - 8):
-        sub = o.i8s_pack(q_all.reshape(M, K)[m0:m0 + 8], x_scale)
-        _, oyf = o.i8s_mul_mat_add(wp, N, K, sub, 8, bias=bias, relu=relu, nth=8)
-        same_bits(yf[m0:m0 + 8], oyf)
-    # requant property: one scale = max(max|y|, 1e-5)/127, every q = round(y*127/amax)
-    q, s = o.i8s_unpack(host(y8), M * N)
-    amax = np.float32(max(np.abs(yf).max(), np.float32(1e-5)))
-    assert pins.f32_bits(s) == pins.f32_bits(amax / np.float32(127.0))
-    inv = np.float32(127.0) / amax
-    v = (yf.reshape(-1) * inv).astype(np.float32).astype(np.float64)
-    ref = np.clip(np.floor(np.abs(v) + 0.5) * np.sign(v), -127, 127).astype(np.int8)
-    assert np.array_equal(q, ref)
+    assert i2s.read_status(ws) == 0
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, relu=relu, nth=16)
+    same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+    same_bits(host(y8), oy8)
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 5, 64), (100, 300, 256), (130, 257, 1024), (300, 640, 4096)])
@@ -528,14 +542,12 @@ def test_i8s_packed_weights(i2s, o, M, N, K, relu):
     same_bits(host(y8b), o.i8s_mul_mat_add(wp, N, K, xp2, M, bias=bias, relu=relu, nth=4)[0])
 
 
-def test_i8s_packed_encoder_fc1_sampled(i2s, o):
+def test_i8s_packed_encoder_fc1_full(i2s, o):
     M, N, K = 900, 8192, 2048
     wp, xp, bias = i8s_inputs(o, M, N, K, seed=N + 1)
     packed = i2s.i8s_pack_weights(dev(wp), N, K)
     y8, ws = i2s.i8s_mul_mat_add_relu_packed(packed, N, K, dev(xp), M, bias=dev(bias), relu=True)
-    yf = host(i2s.i8s_ws_f32(ws, M, N))
-    q_all, x_scale = o.i8s_unpack(xp, M * K)
-    for m0 in (0, 449, M - 8):
-        sub = o.i8s_pack(q_all.reshape(M, K)[m0:m0 + 8], x_scale)
-        _, oyf = o.i8s_mul_mat_add(wp, N, K, sub, 8, bias=bias, relu=True, nth=8)
-        same_bits(yf[m0:m0 + 8], oyf)
+    assert i2s.read_status(ws) == 0
+    oy8, oyf = o.i8s_mul_mat_add(wp, N, K, xp, M, bias=bias, relu=True, nth=16)
+    same_bits(host(i2s.i8s_ws_f32(ws, M, N)), oyf)
+    same_bits(host(y8), oy8)

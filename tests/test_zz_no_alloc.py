@@ -1,15 +1,18 @@
 """i2s_mul_mat_noalloc (fixed library scratch, no workspace) against
-i2s_mul_mat (caller workspace) on the same device buffers.
+i2s_mul_mat (caller workspace) on the same device buffers, and against the CPU
+oracle on sampled weight rows of the large decode shapes.
 
-Both run the same arithmetic, so the outputs must agree bit for bit (the
-tolerance every I2_S parity test uses). Each case calls the no-alloc entry
-point twice in a row, and one test alternates shapes, so every call after the
-first starts from the scratch contents the previous call left behind.
+Both GPU entry points run the same arithmetic, so the outputs must agree bit
+for bit (the tolerance every I2_S parity test uses). Each case calls the
+no-alloc entry point twice in a row, and one test alternates shapes, so every
+call after the first starts from the scratch contents the previous call left
+behind.
 """
 
 import numpy as np
 import pytest
 
+import oracle
 from int8_quantized_matmul_gb300 import synth
 
 torch = pytest.importorskip("torch")
@@ -105,3 +108,20 @@ def test_noalloc_rejects_what_does_not_fit(i2s):
     rc = i2s.lib.i2s_mul_mat_noalloc(w.data_ptr(), N, K, x17.data_ptr(), 17, y.data_ptr(), i2s._stream())
     assert rc == -1   # I2S_E_BAD_SHAPE: the no-alloc call covers M <= 16 only
     assert bool((y == 3.0).all())
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8960, 1536), (8, 1536, 8960), (16, 151936 // 8, 1536)])
+def test_noalloc_against_the_oracle_sampled(i2s, M, N, K):
+    # the gate/up, down and (an eighth of) the output-head shapes: 32-row
+    # slices of the weights, first, last and two inside, computed by the oracle
+    o = oracle.get()
+    w, x = make_problem(i2s, M, N, K, seed=M + N + K)
+    wh = w.cpu().numpy()
+    xh = x.cpu().numpy()
+    rb = K // 4
+    for _ in range(2):
+        y = bits(noalloc(i2s, w, N, K, x)).view(np.float32)
+        for n0 in (0, N // 3, (2 * N) // 3, N - 32):
+            sub = np.concatenate([wh[n0 * rb:(n0 + 32) * rb], wh[N * rb:N * rb + 32]])
+            want = o.i2s_mul_mat(sub, 32, K, xh, nth=8)
+            np.testing.assert_array_equal(y[:, n0:n0 + 32].view(np.uint32), want.view(np.uint32))
