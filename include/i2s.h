@@ -260,8 +260,12 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
  * ws     device workspace of at least i8s_mul_mat_workspace(M,N,K) bytes,
  *        256-byte aligned. After the call it holds the F32 output before
  *        requantization (M x N, row-major) at offset 256 (i8s_ws_f32_offset).
- * Requirements: K % 64 == 0, K <= 65536 (at most 64 accumulation chunks of
- * 1024 positions), M*K, N*K, M*N < 2^31; all pointers 16-byte aligned.
+ * Requirements: K >= 1 with Kp <= 65536, Kp = K rounded up to a multiple of
+ * 64 (at most 64 accumulation chunks of 1024 positions); M*Kp, N*Kp, M*N <
+ * 2^31; all pointers 16-byte aligned. Any K is allowed: a conv run as
+ * im2col_asym then mul_mat_add has K = C*KW ([P3] Encoder), for example 7
+ * for a mono waveform stem. The operand rows hold Kp positions, the tail
+ * zero, which adds nothing to the integer dot.
  * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
  * ------------------------------------------------------------------------- */
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K);
@@ -272,8 +276,9 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
 
 /* Weights packed once (a load-time repack, as ggml's CPU backends repack weights
  * for their kernels): i8s_pack_weights writes the f16 operand rows of an I8_S
- * weight tensor (exact integers, N x K) followed by a 16-byte trailer holding
- * its F32 scale: i8s_packed_bytes(N,K) bytes, 16-byte aligned, caller-owned.
+ * weight tensor (exact integers, N x Kp, Kp = K rounded up to 64, the tail
+ * zero) followed by a 16-byte trailer holding its F32 scale:
+ * i8s_packed_bytes(N,K) bytes, 16-byte aligned, caller-owned.
  * i8s_mul_mat_add_relu_packed then computes the same result as
  * i8s_mul_mat_add_relu without converting the weights on every call; its
  * workspace is i8s_mul_mat_packed_workspace(M,N,K) bytes (the F32 output
@@ -382,8 +387,10 @@ int i8s_depthwise_mul_mat_add(const void* w_i8s, int64_t KW, const void* x_i8s, 
  *   from zero); d is M x N F32. The exact int32 dot runs on the I8_S
  *   tensor-core path (f16 operands, f32 chunk sums of at most 1024
  *   positions, drained into int32).
- * Requirements: K % 64 == 0, K <= 65536; M*K, N*K, M*N < 2^31; 16-byte
- * aligned pointers; ws 256-byte aligned, at least w8a8_mul_mat_workspace.
+ * Requirements: K >= 1 with Kp <= 65536 (Kp = K rounded up to a multiple of
+ * 64; the operand rows hold Kp positions, the tail zero); M*Kp, N*Kp, M*N <
+ * 2^31; 16-byte aligned pointers; ws 256-byte aligned, at least
+ * w8a8_mul_mat_workspace.
  * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
  * ------------------------------------------------------------------------- */
 int w8a8_quantize_weights(const float* w, int64_t N, int64_t K, int8_t* wq, float* bscale,
@@ -394,8 +401,9 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
 
 /* Packed weights ([P4] Implementation: the weights are quantized and packed
  * for the matrix unit once, on the cache-miss path, and reused by every call).
- * w8a8_pack_weights writes the f16 operand rows of wq (exact integers, N x K,
- * w8a8_packed_bytes(N,K) bytes, 16-byte aligned, caller-owned) once;
+ * w8a8_pack_weights writes the f16 operand rows of wq (exact integers, N x Kp,
+ * Kp = K rounded up to 64, the tail zero; w8a8_packed_bytes(N,K) bytes,
+ * 16-byte aligned, caller-owned) once;
  * w8a8_mul_mat_packed then runs each call as two launches (rows quantized
  * straight into f16 operand rows, then the GEMM) with no per-call weight
  * conversion. Same requirements and results as w8a8_mul_mat; workspace at least

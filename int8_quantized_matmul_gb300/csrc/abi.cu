@@ -561,7 +561,9 @@ static int i8s_pick_tile(int64_t M, const int64_t* N, const int64_t* K, int coun
     return i8s_tile_m(M, N, K, count, i8s_gemm_tc_max_pairs());
 }
 
+// K is the operand row length i8s_kpad(K) wherever f16 rows are sized.
 static size_t i8s_ws_for(int64_t M, int64_t N, int64_t K, int tm) {
+    K = i8s_kpad(K);
     const size_t tiles = (size_t)i8s_tiles(M, N, tm);
     return kHeader + align_up((size_t)M * (size_t)N * 4) + align_up((size_t)i8s_rows_pad(M, tm) * (size_t)K * 2) +
            align_up((size_t)N * (size_t)K * 2) + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4) +
@@ -569,7 +571,7 @@ static size_t i8s_ws_for(int64_t M, int64_t N, int64_t K, int tm) {
 }
 
 size_t i8s_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
-    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return 0;
+    if (M < 1 || N < 1 || K < 1 || i8s_kpad(K) > kI8sMaxK) return 0;
     return std::max(i8s_ws_for(M, N, K, kI8sTileM), i8s_ws_for(M, N, K, kI8sTileMSmall));
 }
 
@@ -583,6 +585,8 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     unsigned int* amax = reinterpret_cast<unsigned int*>(base + kAmaxOff);
     uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     float* yf = reinterpret_cast<float*>(base + kHeader);
+    const int64_t Kx = K;         // the activation's own K (its scale trailer follows M*Kx bytes)
+    K = i8s_kpad(K);              // operand row length from here on
     const int tm = i8s_pick_tile(M, &N, &K, 1);
     const int64_t rows_pad = i8s_rows_pad(M, tm);
     const size_t tiles = (size_t)i8s_tiles(M, N, tm);
@@ -597,7 +601,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     // pre-pass: weights (unless packed) and activations to f16 rows, once per
     // call; clears the status and amax words and the split-tile tickets
     int r = cuda_status(launch_i8s_to_f16(w_i8s, w_i8s ? (int)N : 0, reinterpret_cast<__half*>(base + wf_off),
-                                          static_cast<const int8_t*>(x_i8s), (int)M, (int)rows_pad, (int)K, xf,
+                                          static_cast<const int8_t*>(x_i8s), (int)M, (int)rows_pad, (int)Kx, xf,
                                           base + tick_off, zero_bytes, status, amax, stream));
     if (r) return r;
     static thread_local I8sTcArgs a;
@@ -605,7 +609,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
     if (!make_f16_operand_map(&P.xmap, xf, (int)rows_pad, (int)K, tm / 2)) return I2S_E_CUDA;
     if (!make_f16_operand_map(&P.wmap, wf, (int)N, (int)K, kI8sTileN)) return I2S_E_CUDA;
     P.w_scale_ptr = w_scale;
-    P.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * K));
+    P.x_scale_ptr = reinterpret_cast<const float*>(static_cast<const uint8_t*>(x_i8s) + i8s_scale_offset(M * Kx));
     P.bias = bias;
     P.row_scale = nullptr;
     P.col_scale = nullptr;
@@ -637,7 +641,7 @@ static int i8s_run(const int8_t* w_i8s, const __half* wf_packed, const float* w_
 static int i8s_check(const void* w, int64_t N, int64_t K, const void* x_i8s, int64_t M, const float* bias,
                      const void* y_i8s, const void* ws) {
     if (!w || !x_i8s || !y_i8s || !ws) return I2S_E_NULL_PTR;
-    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return I2S_E_BAD_SHAPE;
+    if (M < 1 || N < 1 || K < 1 || i8s_kpad(K) > kI8sMaxK) return I2S_E_BAD_SHAPE;
     if (M * K >= ((int64_t)1 << 31) || N * K >= ((int64_t)1 << 31) || M * N >= ((int64_t)1 << 31))
         return I2S_E_BAD_SHAPE;
     if (!aligned16(w) || !aligned16(x_i8s) || !aligned16(y_i8s) || !aligned256(ws) || (bias && ((uintptr_t)bias & 3u)))
@@ -658,8 +662,8 @@ int i8s_mul_mat_add_relu(const void* w_i8s, int64_t N, int64_t K, const void* x_
 }
 
 size_t i8s_packed_bytes(int64_t N, int64_t K) {
-    if (N < 1 || K < 64 || K % 64 || K > kI8sMaxK || N * K >= ((int64_t)1 << 31)) return 0;
-    return (size_t)N * (size_t)K * 2 + 16;
+    if (N < 1 || K < 1 || i8s_kpad(K) > kI8sMaxK || N * i8s_kpad(K) >= ((int64_t)1 << 31)) return 0;
+    return (size_t)N * (size_t)i8s_kpad(K) * 2 + 16;
 }
 
 int i8s_pack_weights(const void* w_i8s, int64_t N, int64_t K, void* packed, i2s_stream_t stream) {
@@ -670,18 +674,21 @@ int i8s_pack_weights(const void* w_i8s, int64_t N, int64_t K, void* packed, i2s_
     int r = check_device();
     if (r) return r;
     uint8_t* dst = static_cast<uint8_t*>(packed);
-    r = cuda_status(launch_i8_to_f16(static_cast<const int8_t*>(w_i8s), N * K, reinterpret_cast<__half*>(dst), stream));
+    const int64_t Kp = i8s_kpad(K);
+    r = cuda_status(K == Kp ? launch_i8_to_f16(static_cast<const int8_t*>(w_i8s), N * K, reinterpret_cast<__half*>(dst), stream)
+                            : launch_i8_to_f16_rows(static_cast<const int8_t*>(w_i8s), N, K, reinterpret_cast<__half*>(dst),
+                                                    stream));
     if (r) return r;
     // the 16-byte trailer: the weight scale, then zeros
-    r = cuda_status(cudaMemsetAsync(dst + (size_t)N * K * 2, 0, 16, stream));
+    r = cuda_status(cudaMemsetAsync(dst + (size_t)N * Kp * 2, 0, 16, stream));
     if (r) return r;
-    return cuda_status(cudaMemcpyAsync(dst + (size_t)N * K * 2, static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K),
+    return cuda_status(cudaMemcpyAsync(dst + (size_t)N * Kp * 2, static_cast<const uint8_t*>(w_i8s) + i8s_scale_offset(N * K),
                                        4, cudaMemcpyDeviceToDevice, stream));
 }
 
 size_t i8s_mul_mat_packed_workspace(int64_t M, int64_t N, int64_t K) {
     const size_t full = i8s_mul_mat_workspace(M, N, K);
-    return full == 0 ? 0 : full - align_up((size_t)N * (size_t)K * 2);
+    return full == 0 ? 0 : full - align_up((size_t)N * (size_t)i8s_kpad(K) * 2);
 }
 
 int i8s_mul_mat_add_relu_packed(const void* packed, int64_t N, int64_t K, const void* x_i8s, int64_t M,
@@ -693,8 +700,9 @@ int i8s_mul_mat_add_relu_packed(const void* packed, int64_t N, int64_t K, const 
     r = check_device();
     if (r) return r;
     const uint8_t* p = static_cast<const uint8_t*>(packed);
-    return i8s_run(nullptr, reinterpret_cast<const __half*>(p), reinterpret_cast<const float*>(p + (size_t)N * K * 2),
-                   N, K, x_i8s, M, bias, relu, y_i8s, ws, stream);
+    return i8s_run(nullptr, reinterpret_cast<const __half*>(p),
+                   reinterpret_cast<const float*>(p + (size_t)N * i8s_kpad(K) * 2), N, K, x_i8s, M, bias, relu, y_i8s, ws,
+                   stream);
 }
 
 size_t i8s_requant_workspace(int64_t n) { return n < 1 ? 0 : kHeader; }
@@ -883,18 +891,20 @@ static size_t w8a8_split_bytes(int64_t M, int64_t N, int64_t K, int tm) {
 }
 
 static bool w8a8_shape_ok(int64_t M, int64_t N, int64_t K) {
-    if (M < 1 || N < 1 || K < 64 || K % 64 || K > kI8sMaxK) return false;
-    return M * K < ((int64_t)1 << 31) && N * K < ((int64_t)1 << 31) && M * N < ((int64_t)1 << 31);
+    if (M < 1 || N < 1 || K < 1 || i8s_kpad(K) > kI8sMaxK) return false;
+    const int64_t Kp = i8s_kpad(K);
+    return M * Kp < ((int64_t)1 << 31) && N * Kp < ((int64_t)1 << 31) && M * N < ((int64_t)1 << 31);
 }
 
 // W8A8 workspace (int8 weights): [header: status, amax][activations int8,
-// M x K][row scales, M F32][activations f16, rows_pad x K][weights f16, N x K]
-// [split-tile slots, tickets, masks].
+// M x K][row scales, M F32][activations f16, rows_pad x Kp][weights f16,
+// N x Kp][split-tile slots, tickets, masks], Kp = i8s_kpad(K).
 static size_t w8a8_front(int64_t M, int64_t K) { return kHeader + align_up((size_t)M * K) + align_up((size_t)M * 4); }
 
 static size_t w8a8_ws_for(int64_t M, int64_t N, int64_t K, int tm) {
-    return w8a8_front(M, K) + align_up((size_t)i8s_rows_pad(M, tm) * (size_t)K * 2) +
-           align_up((size_t)N * (size_t)K * 2) + w8a8_split_bytes(M, N, K, tm);
+    const int64_t Kp = i8s_kpad(K);
+    return w8a8_front(M, K) + align_up((size_t)i8s_rows_pad(M, tm) * (size_t)Kp * 2) +
+           align_up((size_t)N * (size_t)Kp * 2) + w8a8_split_bytes(M, N, Kp, tm);
 }
 
 size_t w8a8_mul_mat_workspace(int64_t M, int64_t N, int64_t K) {
@@ -916,14 +926,15 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
     uint32_t* status = reinterpret_cast<uint32_t*>(base + kStatusOff);
     int8_t* xq = reinterpret_cast<int8_t*>(base + kHeader);
     float* ascale = reinterpret_cast<float*>(base + kHeader + align_up((size_t)M * K));
-    const int tm = i8s_pick_tile(M, &N, &K, 1);
+    int64_t Kp = i8s_kpad(K);   // operand row length (the tail zero-filled by the pre-pass)
+    const int tm = i8s_pick_tile(M, &N, &Kp, 1);
     const int64_t rows_pad = i8s_rows_pad(M, tm);
     const size_t xf_off = w8a8_front(M, K);
-    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)K * 2);
-    const size_t part_off = wf_off + align_up((size_t)N * (size_t)K * 2);
+    const size_t wf_off = xf_off + align_up((size_t)rows_pad * (size_t)Kp * 2);
+    const size_t part_off = wf_off + align_up((size_t)N * (size_t)Kp * 2);
     const size_t tiles = (size_t)i8s_tiles(M, N, tm);
-    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(K) * kI8sTileN * tm * 4);
-    const size_t zero_bytes = w8a8_split_bytes(M, N, K, tm) - (tick_off - part_off);   // tickets and masks
+    const size_t tick_off = part_off + align_up(tiles * (size_t)i8s_chunks(Kp) * kI8sTileN * tm * 4);
+    const size_t zero_bytes = w8a8_split_bytes(M, N, Kp, tm) - (tick_off - part_off);   // tickets and masks
     __half* xf = reinterpret_cast<__half*>(base + xf_off);
     __half* wf = reinterpret_cast<__half*>(base + wf_off);
     // per-row activation quantization (1e-9 floor), then the int8 rows and
@@ -934,12 +945,12 @@ int w8a8_mul_mat(const int8_t* wq, const float* bscale, int64_t N, int64_t K, co
     r = cuda_status(launch_i8s_to_f16(wq, (int)N, wf, xq, (int)M, (int)rows_pad, (int)K, xf, base + tick_off, zero_bytes,
                                       status, amax, stream));
     if (r) return r;
-    return launch_w8a8_gemm(wf, bscale, ascale, xf, N, K, M, tm, d, base, part_off, stream);
+    return launch_w8a8_gemm(wf, bscale, ascale, xf, N, Kp, M, tm, d, base, part_off, stream);
 }
 
 size_t w8a8_packed_bytes(int64_t N, int64_t K) {
-    if (N < 1 || K < 64 || K % 64 || N * K >= ((int64_t)1 << 31)) return 0;
-    return (size_t)N * (size_t)K * 2;
+    if (N < 1 || K < 1 || i8s_kpad(K) > kI8sMaxK || N * i8s_kpad(K) >= ((int64_t)1 << 31)) return 0;
+    return (size_t)N * (size_t)i8s_kpad(K) * 2;
 }
 
 int w8a8_pack_weights(const int8_t* wq, int64_t N, int64_t K, void* packed, i2s_stream_t stream) {
@@ -949,7 +960,8 @@ int w8a8_pack_weights(const int8_t* wq, int64_t N, int64_t K, void* packed, i2s_
     if (overlaps(wq, (size_t)N * K, packed, w8a8_packed_bytes(N, K))) return I2S_E_BAD_ARG;
     int r = check_device();
     if (r) return r;
-    return cuda_status(launch_i8_to_f16(wq, N * K, static_cast<__half*>(packed), stream));
+    if (K % 64 == 0) return cuda_status(launch_i8_to_f16(wq, N * K, static_cast<__half*>(packed), stream));
+    return cuda_status(launch_i8_to_f16_rows(wq, N, K, static_cast<__half*>(packed), stream));
 }
 
 // Packed W8A8 calls, one matmul or a group of them with the same M. Workspace:
@@ -980,12 +992,12 @@ static W8a8Plan w8a8_plan(const w8a8_problem* probs, int count, int64_t M, int t
         if (a < 0) {
             a = pl.n_act++;
             pl.act_off[a] = off;
-            off += align_up((size_t)M * 4) + align_up((size_t)rows_pad * (size_t)probs[i].K * 2);
+            off += align_up((size_t)M * 4) + align_up((size_t)rows_pad * (size_t)i8s_kpad(probs[i].K) * 2);
         }
         pl.act_of[i] = a;
         const size_t ht = (size_t)i8s_tiles(M, probs[i].N, tm);
         pl.tiles += ht;
-        pl.slots += ht * (size_t)i8s_chunks(probs[i].K);
+        pl.slots += ht * (size_t)i8s_chunks(i8s_kpad(probs[i].K));
     }
     pl.part_off = off;
     pl.tick_off = pl.part_off + align_up(pl.slots * kI8sTileN * tm * 4);
@@ -1004,7 +1016,7 @@ static int w8a8_group_ok(const w8a8_problem* probs, int count, int64_t M) {
         if (!w8a8_shape_ok(M, q.N, q.K)) return I2S_E_BAD_SHAPE;
         if (!aligned16(q.packed) || !aligned16(q.x) || !aligned16(q.d) || ((uintptr_t)q.bscale & 3u))
             return I2S_E_MISALIGNED;
-        units += (int64_t)i8s_tiles(M, q.N, kI8sTileMSmall) / 2 * i8s_chunks(q.K);   // the more numerous
+        units += (int64_t)i8s_tiles(M, q.N, kI8sTileMSmall) / 2 * i8s_chunks(i8s_kpad(q.K));   // the more numerous
     }
     return units < ((int64_t)1 << 30) ? I2S_OK : I2S_E_BAD_SHAPE;
 }
@@ -1024,7 +1036,7 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
     r = check_device();
     if (r) return r;
     int64_t Ns[kI8sMaxGroup], Ks[kI8sMaxGroup];
-    for (int i = 0; i < count; ++i) Ns[i] = probs[i].N, Ks[i] = probs[i].K;
+    for (int i = 0; i < count; ++i) Ns[i] = probs[i].N, Ks[i] = i8s_kpad(probs[i].K);
     const int tm = i8s_pick_tile(M, Ns, Ks, count);
     const W8a8Plan pl = w8a8_plan(probs, count, M, tm);
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -1056,8 +1068,9 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
         const w8a8_problem& q = probs[i];
         I8sProb& P = a.p[i];
         const int act = pl.act_of[i];
-        if (!make_f16_operand_map(&P.xmap, J.xf[act], (int)rows_pad, (int)q.K, tm / 2)) return I2S_E_CUDA;
-        if (!make_f16_operand_map(&P.wmap, q.packed, (int)q.N, (int)q.K, kI8sTileN)) return I2S_E_CUDA;
+        const int Kp = (int)i8s_kpad(q.K);   // operand row length
+        if (!make_f16_operand_map(&P.xmap, J.xf[act], (int)rows_pad, Kp, tm / 2)) return I2S_E_CUDA;
+        if (!make_f16_operand_map(&P.wmap, q.packed, (int)q.N, Kp, kI8sTileN)) return I2S_E_CUDA;
         P.w_scale_ptr = q.bscale;   // read by the kernel's I8_S path; the W8A8 epilogue uses the arrays
         P.x_scale_ptr = J.ascale[act];
         P.bias = nullptr;
@@ -1065,9 +1078,9 @@ int w8a8_mul_mat_grouped(const w8a8_problem* probs, int count, int64_t M, void* 
         P.col_scale = q.bscale;
         P.y = q.d;
         P.N = (int)q.N;
-        P.K = (int)q.K;
+        P.K = Kp;
         P.n_wt = (int)((q.N + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
-        P.chunks = (int)i8s_chunks(q.K);
+        P.chunks = (int)i8s_chunks(Kp);
         P.unit0 = units;
         P.ht0 = ht;
         P.slot0 = slot;

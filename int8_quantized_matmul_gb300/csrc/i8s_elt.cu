@@ -749,8 +749,9 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_weights(const float* __res
 
 // The packed W8A8 calls' row quantizer: one block per operand row of each
 // distinct activation (rows_pad rows each); a block with m < M quantizes row m
-// (1e-9 floor) straight into the GEMM's f16 operand row (exact integers) and
-// its scale, a block with m >= M writes a zero row. The same launch clears the
+// (1e-9 floor) straight into the GEMM's f16 operand row (exact integers; the
+// row holds K rounded up to 64 positions, the tail zero) and its scale, a
+// block with m >= M writes a zero row. The same launch clears the
 // status word, the amax word and the GEMM's split-tile counters.
 __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_constant__ W8a8RowJobs J) {
     __shared__ float s_max[kEltThreads / 32];
@@ -765,11 +766,13 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_cons
     while (j + 1 < J.count && (int)blockIdx.x >= (j + 1) * J.rows_pad) ++j;
     const int64_t m = (int64_t)blockIdx.x - (int64_t)j * J.rows_pad;
     const int64_t K = J.K[j];
-    __half* out = J.xf[j] + m * K;
+    const int64_t Kp = (K + 63) / 64 * 64;   // operand row length, the tail zero
+    __half* out = J.xf[j] + m * Kp;
     if (m >= J.M) {
-        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __float2half_rn(0.0f);
+        for (int64_t k = threadIdx.x; k < Kp; k += blockDim.x) out[k] = __float2half_rn(0.0f);
         return;
     }
+    for (int64_t k = K + threadIdx.x; k < Kp; k += blockDim.x) out[k] = __float2half_rn(0.0f);
     const float* xr = J.x[j] + m * K;
     float mx = 0.0f;
     for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));

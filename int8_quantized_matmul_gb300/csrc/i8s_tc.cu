@@ -530,19 +530,83 @@ __global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w
     convert_rows(reinterpret_cast<const uint4*>(x), x16, x16_pad, reinterpret_cast<uint4*>(xf), t0, stride);
 }
 
+// K that is not a multiple of 64: src rows of K int8 (not 16-byte aligned)
+// -> dst rows of Kp f16, positions K..Kp-1 and rows rows_in..rows_out-1 zero.
+// Zero products add nothing, so the padded contraction is the same integer
+// sum. One 16-byte output word (8 values) per thread and step, byte loads.
+__device__ __forceinline__ void convert_rows_ragged(const int8_t* __restrict__ src, int rows_in, int rows_out, int K,
+                                                    int Kp, uint4* __restrict__ dst, unsigned long long t0,
+                                                    unsigned long long stride) {
+    const unsigned long long words_per_row = (unsigned long long)(Kp / 8);
+    const unsigned long long n = (unsigned long long)rows_out * words_per_row;
+    for (unsigned long long i = t0; i < n; i += stride) {
+        const int r = (int)(i / words_per_row);
+        const int k0 = (int)(i - (unsigned long long)r * words_per_row) * 8;
+        __align__(16) __half h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = k0 + j;
+            const int v = (r < rows_in && k < K) ? (int)src[(size_t)r * K + k] : 0;
+            h[j] = __int2half_rn(v);
+        }
+        dst[i] = *reinterpret_cast<const uint4*>(h);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_i8s_to_f16_ragged(const int8_t* __restrict__ w, int N, __half* __restrict__ wf,
+                                                           const int8_t* __restrict__ x, int M, int rows_pad,
+                                                           __half* __restrict__ xf, int K, int Kp, uint4* zero,
+                                                           unsigned long long zero_16, uint32_t* status,
+                                                           unsigned int* amax_bits) {
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+    pdl_wait();   // the launch before may still use this workspace (or produce x)
+    if (t0 == 0) {
+        *status = 0u;
+        *amax_bits = 0u;
+    }
+    for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (w) convert_rows_ragged(w, N, N, K, Kp, reinterpret_cast<uint4*>(wf), t0, stride);
+    convert_rows_ragged(x, M, rows_pad, K, Kp, reinterpret_cast<uint4*>(xf), t0, stride);
+}
+
+__global__ void __launch_bounds__(256) k_i8_to_f16_rows(const int8_t* __restrict__ src, int rows, int K, int Kp,
+                                                        __half* __restrict__ dst) {
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    convert_rows_ragged(src, rows, rows, K, Kp, reinterpret_cast<uint4*>(dst),
+                        blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x, stride);
+}
+
+int prepass_grid(unsigned long long n16) {
+    const unsigned long long want = (n16 + 1023) / 1024;
+    const int cap = device_sm_count() * 8;
+    return (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
+}
+
 }  // namespace
 
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
                               __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
                               cudaStream_t s) {
+    const int Kp = (int)i8s_kpad(K);
+    if (Kp != K) {
+        const unsigned long long n8 = (unsigned long long)(N > rows_pad ? N : rows_pad) * (unsigned long long)(Kp / 8);
+        return launch_pdl(k_i8s_to_f16_ragged, dim3(prepass_grid(n8 / 4)), dim3(256), 0, s, w, N, wf, x, M, rows_pad,
+                          xf, K, Kp, static_cast<uint4*>(zero), (unsigned long long)(zero_bytes / 16), status,
+                          amax_bits);
+    }
     const unsigned long long w16 = (unsigned long long)N * K / 16;
     const unsigned long long x16 = (unsigned long long)M * K / 16, x16p = (unsigned long long)rows_pad * K / 16;
     const unsigned long long n = w16 > x16p ? w16 : x16p;
-    const unsigned long long want = (n + 1023) / 1024;
-    const int cap = device_sm_count() * 8;
-    const int grid = (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
-    return launch_pdl(k_i8s_to_f16, dim3(grid), dim3(256), 0, s, w, w16, wf, x, x16, x16p, xf, static_cast<uint4*>(zero),
-                      (unsigned long long)(zero_bytes / 16), status, amax_bits);
+    return launch_pdl(k_i8s_to_f16, dim3(prepass_grid(n)), dim3(256), 0, s, w, w16, wf, x, x16, x16p, xf,
+                      static_cast<uint4*>(zero), (unsigned long long)(zero_bytes / 16), status, amax_bits);
+}
+
+cudaError_t launch_i8_to_f16_rows(const int8_t* src, int64_t rows, int64_t K, __half* dst, cudaStream_t s) {
+    const int Kp = (int)i8s_kpad(K);
+    k_i8_to_f16_rows<<<prepass_grid((unsigned long long)rows * (Kp / 8) / 4), 256, 0, s>>>(src, (int)rows, (int)K, Kp,
+                                                                                          dst);
+    return cudaGetLastError();
 }
 
 // Per device: 1 + the number of CTA pairs that can be resident at once (0:

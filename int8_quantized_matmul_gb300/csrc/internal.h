@@ -130,6 +130,11 @@ constexpr int kI8sTileMSmall = 128;   // the other tile height
 constexpr int kI8sChunkK = 1024;
 constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask of a split tile)
 
+// The f16 operand rows of the I8_S / W8A8 GEMM hold K rounded up to a
+// multiple of 64 positions (one 128-byte swizzle atom), the tail zero-filled:
+// a zero product adds nothing, so any K gives the exact integer dot.
+inline int64_t i8s_kpad(int64_t K) { return (K + 63) / 64 * 64; }
+
 // The tile height of a launch whose matmuls have M rows, N[i] features and
 // K[i] positions, run by `pairs` CTA pairs. The busiest pair takes
 // ceil(units / pairs) work units (a 256-feature x tm-row tile over one K
@@ -190,6 +195,8 @@ static_assert(sizeof(I8sTcArgs) <= 32764, "I8sTcArgs exceeds the kernel paramete
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
                               __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
                               cudaStream_t s);
+// N x K int8 rows (any K) -> N x i8s_kpad(K) f16 rows, the tail zero.
+cudaError_t launch_i8_to_f16_rows(const int8_t* src, int64_t rows, int64_t K, __half* dst, cudaStream_t s);
 cudaError_t launch_i8s_gemm_tc(const I8sTcArgs& a, int grid, cudaStream_t s);
 int i8s_gemm_tc_max_pairs();   // CTA pairs of the I8_S GEMM that fit on the device at once
 
@@ -211,7 +218,7 @@ cudaError_t launch_w8a8_weights(const float* w, int64_t N, int64_t K, int8_t* wq
 // Row quantization of the packed W8A8 calls: one job per distinct activation.
 struct W8a8RowJobs {
     const float* x[kI8sMaxGroup];   // M x K F32
-    __half* xf[kI8sMaxGroup];       // rows_pad x K f16 operand rows
+    __half* xf[kI8sMaxGroup];       // rows_pad x i8s_kpad(K) f16 operand rows (tail zero)
     float* ascale[kI8sMaxGroup];    // M row scales
     int K[kI8sMaxGroup];
     int count, M, rows_pad;

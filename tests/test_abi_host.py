@@ -102,7 +102,10 @@ def test_validation_errors_need_no_device(i2s):
     assert need > 0
     assert L.i2s_mul_mat(FAKE, 64, 128, FAKE, 4, FAKE, FAKE, need - 1, None) == -4
     # I8_S
-    assert L.i8s_mul_mat_add_relu(FAKE, 64, 100, FAKE, 4, None, 0, FAKE, FAKE, ws_big, None) == -1
+    assert L.i8s_mul_mat_add_relu(FAKE, 64, 0, FAKE, 4, None, 0, FAKE, FAKE, ws_big, None) == -1
+    assert L.i8s_mul_mat_add_relu(FAKE, 64, 65537, FAKE, 4, None, 0, FAKE, FAKE, ws_big, None) == -1
+    # any K >= 1 is a valid shape (rows padded to 64 positions inside)
+    assert i2s.i8s_mul_mat_workspace(4, 64, 7) == i2s.i8s_mul_mat_workspace(4, 64, 64)
     assert L.i8s_mul_mat_add_relu(FAKE, 64, 128, FAKE, 4, None, 0, None, FAKE, ws_big, None) == -2
     need = i2s.i8s_mul_mat_workspace(4, 64, 128)
     assert L.i8s_mul_mat_add_relu(FAKE, 64, 128, FAKE, 4, None, 0, FAKE, FAKE, need - 1, None) == -4
@@ -151,13 +154,16 @@ def test_eltwise_and_w8a8_validation_needs_no_device(i2s):
     assert L.i8s_im2col_asym(vp(A), 2, 40, 8, 4, 4, 0, vp(2 * A + 3), None) == E["I2S_E_MISALIGNED"]
     assert L.i8s_depthwise_mul_mat_add(vp(A), 7, vp(2 * A), 4, 100, 1, 6, 0, None, 0, vp(2 * A + 16), vp(4 * A), 256,
                                        None) == E["I2S_E_BAD_ARG"]
-    # W8A8: shapes (K % 64), alignment, group size
-    assert L.w8a8_mul_mat(vp(A), vp(2 * A), 64, 100, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
+    # W8A8: shapes (any K from 1 to 65536), alignment, group size
+    assert L.w8a8_mul_mat(vp(A), vp(2 * A), 64, 0, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
+        E["I2S_E_BAD_SHAPE"]
+    assert L.w8a8_mul_mat(vp(A), vp(2 * A), 64, 65537, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
         E["I2S_E_BAD_SHAPE"]
     assert L.w8a8_mul_mat(vp(A + 8), vp(2 * A), 64, 128, vp(3 * A), 8, vp(4 * A), vp(5 * A), 1 << 30, None) == \
         E["I2S_E_MISALIGNED"]
-    assert L.w8a8_packed_bytes(64, 128) == 64 * 128 * 2 and L.w8a8_packed_bytes(64, 100) == 0
-    assert L.i8s_packed_bytes(64, 128) == 64 * 128 * 2 + 16
+    assert L.w8a8_packed_bytes(64, 128) == 64 * 128 * 2 and L.w8a8_packed_bytes(64, 100) == 64 * 128 * 2
+    assert L.w8a8_packed_bytes(64, 0) == 0
+    assert L.i8s_packed_bytes(64, 128) == 64 * 128 * 2 + 16 and L.i8s_packed_bytes(64, 7) == 64 * 64 * 2 + 16
     probs = (i2s.w8a8_problem * 9)()
     for i in range(9):
         probs[i] = i2s.w8a8_problem(A, A, 64, 128, A, A)
