@@ -249,6 +249,33 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
                             size_t ws_bytes, i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Fused decode step: the grouped I2_S matmul for M <= 16 as ONE launch whose
+ * prologue quantizes the activations, as the pages' mul_mat quantizes its
+ * src1 rows before the dot products in the same op ([P2] Kernels, threading
+ * paragraph; [P1] "Five fused INT8 ops", last paragraph). The rows of every
+ * distinct activation are spread over the launch's CTAs by cost; each row's
+ * e2m1 digit operand, scale and sum are published through a per-activation
+ * ready counter, and the weight stream starts before the activations are
+ * ready. Same results, bit for bit, as i2s_mul_mat_grouped.
+ *
+ * The workspace (i2s_mul_mat_grouped_fused_workspace bytes, 256-byte aligned)
+ * carries state between calls: a fixed area of flags at its start that every
+ * launch leaves cleared for the next one. Zero that area once with
+ * i2s_mul_mat_grouped_fused_init before the first fused call on a workspace
+ * (and again if the workspace was used for anything else in between). Calls
+ * sharing a workspace must be ordered on one stream. A device wait that runs
+ * out is recorded in the status word (i2s_read_status), which these calls do
+ * not clear.
+ * Requirements: 1 <= M <= 16; per problem as i2s_mul_mat; at most
+ * 8 distinct K among the problems and 120 distinct activations (BAD_ARG).
+ * Errors: as i2s_mul_mat_grouped.
+ * ------------------------------------------------------------------------- */
+size_t i2s_mul_mat_grouped_fused_workspace(const i2s_problem* probs, int count, int64_t M);
+int i2s_mul_mat_grouped_fused_init(void* ws, size_t ws_bytes, i2s_stream_t stream);
+int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                              i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * I8_S x I8_S -> I8_S fused matmul + bias (+ ReLU) with requantization in the
  * op: ggml_mul_mat_add (relu = 0) and ggml_mul_mat_add_relu (relu != 0)
  * ([P1] "Five fused INT8 ops").

@@ -429,6 +429,178 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     return I2S_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode launch: one GEMV launch whose prologue quantizes the
+// activations. Workspace: [header: status][flags, a fixed area cleared by
+// i2s_mul_mat_grouped_fused_init and left clear by every launch][row scales
+// and sums, 16 per activation][per distinct K: the digit operands of its
+// activations, stacked][split-K partial dots][chunk counters][weight maps].
+// ---------------------------------------------------------------------------
+static constexpr size_t kFusedFlagBytes = 2048;   // >= 4 * (I2S_MAX_GROUP + kTcMaxMaps + 1)
+static_assert(kFusedFlagBytes >= 4 * (kMaxGroup + kTcMaxMaps + 1), "fused flag area");
+
+struct FusedPlan {
+    int n_act = 0, n_class = 0;
+    std::vector<int> act_of, first, class_of_act, idx_in_class;
+    int class_K[kGvMaxKClasses] = {};
+    int class_n[kGvMaxKClasses] = {};
+    size_t scale_off = 0, sum_off = 0, class_off[kGvMaxKClasses] = {}, dot_off = 0, ticket_off = 0, map_off = 0,
+           end = 0;
+};
+
+// returns I2S_OK or BAD_ARG (too many activations or distinct K)
+static int fused_plan(const i2s_problem* probs, int count, int64_t M, FusedPlan& pl) {
+    pl.n_act = group_acts(probs, count, pl.act_of, pl.first);
+    if (pl.n_act > kTcMaxMaps) return I2S_E_BAD_ARG;
+    const int op_rows = gemv_tc_op_rows(gemv_tc_mp(M));
+    pl.class_of_act.assign(pl.n_act, -1);
+    pl.idx_in_class.assign(pl.n_act, 0);
+    for (int a = 0; a < pl.n_act; ++a) {
+        const int K = (int)probs[pl.first[a]].K;
+        int c = 0;
+        while (c < pl.n_class && pl.class_K[c] != K) ++c;
+        if (c == pl.n_class) {
+            if (pl.n_class == kGvMaxKClasses) return I2S_E_BAD_ARG;
+            pl.class_K[pl.n_class++] = K;
+        }
+        pl.class_of_act[a] = c;
+        pl.idx_in_class[a] = pl.class_n[c]++;
+    }
+    size_t off = kHeader + kFusedFlagBytes;
+    pl.scale_off = off;
+    off += align_up((size_t)pl.n_act * 16 * 4);
+    pl.sum_off = off;
+    off += align_up((size_t)pl.n_act * 16 * 4);
+    for (int c = 0; c < pl.n_class; ++c) {
+        pl.class_off[c] = off;
+        off += align_up((size_t)pl.class_n[c] * op_rows * (size_t)(pl.class_K[c] / 2));
+    }
+    size_t dots = 0, tickets = 0;
+    for (int i = 0; i < count; ++i)
+        if (probs[i].K > kGemvChunkPositions) {
+            dots += (size_t)M * (size_t)probs[i].N;
+            tickets += (size_t)((probs[i].N + kTcTileW - 1) / kTcTileW);
+        }
+    pl.dot_off = off;
+    off += align_up(dots * 4);
+    pl.ticket_off = off;
+    off += align_up(tickets * 4);
+    pl.map_off = off;
+    off += wmap_area(count);
+    pl.end = off;
+    return I2S_OK;
+}
+
+static int fused_check(const i2s_problem* probs, int count, int64_t M) {
+    if (!probs) return I2S_E_NULL_PTR;
+    if (count < 1 || count > I2S_MAX_GROUP) return I2S_E_BAD_ARG;
+    if (M < 1 || M > 16) return I2S_E_BAD_SHAPE;
+    for (int i = 0; i < count; ++i) {
+        const i2s_problem& p = probs[i];
+        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
+        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
+        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+    }
+    return I2S_OK;
+}
+
+size_t i2s_mul_mat_grouped_fused_workspace(const i2s_problem* probs, int count, int64_t M) {
+    if (fused_check(probs, count, M) != I2S_OK) return 0;
+    FusedPlan pl;
+    if (fused_plan(probs, count, M, pl) != I2S_OK) return 0;
+    return pl.end;
+}
+
+int i2s_mul_mat_grouped_fused_init(void* ws, size_t ws_bytes, i2s_stream_t stream) {
+    if (!ws) return I2S_E_NULL_PTR;
+    if (!aligned256(ws)) return I2S_E_MISALIGNED;
+    if (ws_bytes < kHeader + kFusedFlagBytes) return I2S_E_WORKSPACE_TOO_SMALL;
+    int r = check_device();
+    if (r) return r;
+    return cuda_status(cudaMemsetAsync(ws, 0, kHeader + kFusedFlagBytes, stream));
+}
+
+int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                              i2s_stream_t stream) {
+    int r = fused_check(probs, count, M);
+    if (r) return r;
+    if (!ws) return I2S_E_NULL_PTR;
+    if (!aligned256(ws)) return I2S_E_MISALIGNED;
+    FusedPlan pl;
+    r = fused_plan(probs, count, M, pl);
+    if (r) return r;
+    if (ws_bytes < pl.end) return I2S_E_WORKSPACE_TOO_SMALL;
+    r = check_device();
+    if (r) return r;
+    const int Mp = gemv_tc_mp(M);
+    const int op_rows = gemv_tc_op_rows(Mp);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    static thread_local GvFusedArgs fa;
+    for (int c = 0; c < pl.n_class; ++c)
+        if (!make_u8_operand_map(&fa.kmaps[c], base + pl.class_off[c], pl.class_n[c] * op_rows, pl.class_K[c] / 2,
+                                 op_rows))
+            return I2S_E_CUDA;
+    CUtensorMap* wmaps = reinterpret_cast<CUtensorMap*>(base + pl.map_off);
+    if (!make_u8_operand_map(&fa.wtmpl, wmaps, kTcTileW, 128, kTcTileW)) return I2S_E_CUDA;
+    long long cost = 0;
+    for (int a = 0; a < pl.n_act; ++a) {
+        const i2s_problem& p = probs[pl.first[a]];
+        GvAct& A = fa.acts[a];
+        const int c = pl.class_of_act[a];
+        A.x = p.x;
+        A.scale = reinterpret_cast<float*>(base + pl.scale_off) + 16 * a;
+        A.sum = reinterpret_cast<int32_t*>(base + pl.sum_off) + 16 * a;
+        A.row0 = pl.idx_in_class[a] * op_rows;
+        A.op = base + pl.class_off[c] + (size_t)A.row0 * (size_t)(p.K / 2);
+        A.cost0 = cost;
+        A.K = (int)p.K;
+        A.kclass = c;
+        A.pad_ = 0;
+        cost += M * p.K;
+    }
+    fa.cost_total = cost;
+    fa.wmaps = wmaps;
+    fa.flags = reinterpret_cast<uint32_t*>(base + kHeader);
+    fa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+    fa.dot_base = reinterpret_cast<int32_t*>(base + pl.dot_off);
+    fa.ticket_base = reinterpret_cast<uint32_t*>(base + pl.ticket_off);
+    fa.n_acts = pl.n_act;
+    fa.count = count;
+    fa.M = (int)M;
+    fa.BN = Mp;
+    int units = 0, dot_elems = 0, ticket_elems = 0;
+    for (int i = 0; i < count; ++i) {
+        const i2s_problem& q = probs[i];
+        const int act = pl.act_of[i];
+        TcProb& P = fa.p[i];
+        const int row_tiles = (int)((q.N + kTcTileW - 1) / kTcTileW);
+        const int chunks = (int)((q.K + kGemvChunkPositions - 1) / kGemvChunkPositions);
+        P.w = static_cast<const uint8_t*>(q.w_i2s);
+        P.act_scale = fa.acts[act].scale;
+        P.row_sum = fa.acts[act].sum;
+        P.y = q.y;
+        P.N = (int)q.N;
+        P.K = (int)q.K;
+        P.map = act;
+        P.tile0 = units;
+        P.n_act_tiles = 1;
+        P.chunks = chunks;
+        P.dot_off = dot_elems;
+        P.ticket_off = ticket_elems;
+        if (chunks > 1) {
+            dot_elems += (int)(M * q.N);
+            ticket_elems += row_tiles;
+        }
+        units += row_tiles * chunks;
+    }
+    fa.total_tiles = units;
+    const int cap = 2 * device_sm_count();
+    const int grid = units < cap ? units : cap;
+    fa.share_first = grid == cap ? kGemvShareFirst : 1;
+    fa.share_second = grid == cap ? kGemvShareSecond : 1;
+    return cuda_status(launch_gemv_fused(fa, grid, stream));
+}
+
 size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M) {
     if (!probs || count < 1 || count > I2S_MAX_GROUP) return 0;
     std::vector<int> act_of, first;

@@ -51,6 +51,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "quant_tc.cuh"
 #include "tc.cuh"
 
 namespace i2s {
@@ -98,7 +99,7 @@ struct SmemGv {
     int final_flag;
 };
 
-constexpr size_t kSProbBytes = 64;      // shared copy of one problem-table entry (SProb)
+constexpr size_t kSProbBytes = 72;      // shared copy of one problem-table entry (SProb)
 constexpr size_t kSmemGvUsed = 1024 + (size_t)kBRingBytes + (size_t)kWStages * kWStageBytes + sizeof(SmemGv) + 16 +
                                (size_t)kMaxGroup * kSProbBytes;
 // At least 80 KB so that at most two CTAs share an SM: each holds 256 of the
@@ -114,6 +115,8 @@ struct SProb {
     const int32_t* row_sum;
     float* y;
     int N, K, map, unit0, chunks, dot_off, ticket_off, pidx;
+    int row0;   // first row of the activation operand in its map (fused launch: stacked operands)
+    int act;    // activation index (fused launch: its ready counter)
 };
 
 constexpr int kChunkStages = kGemvChunkPositions / kKB;   // 3 stages per work unit
@@ -126,7 +129,7 @@ struct Seg {
     const float* act_scale;
     const int32_t* row_sum;
     float* y;
-    int N, K, map, pidx, sidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units;
+    int N, K, map, pidx, sidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units, row0, act;
     bool live;
 };
 
@@ -153,6 +156,8 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     g.K = P.K;
     g.map = P.map;
     g.pidx = P.pidx;
+    g.row0 = P.row0;
+    g.act = P.act;
     g.chunks = P.chunks;
     g.dot_off = P.dot_off;
     g.ticket_off = P.ticket_off;
@@ -190,6 +195,8 @@ __device__ __forceinline__ Seg seg_next(const SProb* sp, const Seg& g, int u, in
     n.K = P.K;
     n.map = P.map;
     n.pidx = P.pidx;
+    n.row0 = P.row0;
+    n.act = P.act;
     n.chunks = P.chunks;
     n.dot_off = P.dot_off;
     n.ticket_off = P.ticket_off;
@@ -202,8 +209,123 @@ __device__ __forceinline__ Seg seg_next(const SProb* sp, const Seg& g, int u, in
     return n;
 }
 
+// --------------------------------------------------------------------------
+// Fused launch: helpers of the prologue and of the waits on it.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (bounded, suspending between polls) until *p reaches want.
+__device__ __forceinline__ bool wait_flag(const uint32_t* p, uint32_t want, volatile int* abort_flag, long long limit) {
+    const long long t0 = clock64();
+    while (ld_acquire_u32(p) < want) {
+        if (*abort_flag || clock64() - t0 > limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+__device__ __forceinline__ void team_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // epilogue warps 4-7
+
+constexpr int kTeamCache = 2;   // 16-value units per thread kept in registers while the amax is reduced
+
+// The prologue's share of the row quantization, done by the 128 threads of
+// the epilogue warps (team thread t). The rows of all activations are laid
+// end to end, each costing K positions; this CTA takes the rows whose first
+// position falls in its equal share [lo, hi) of the total. A row is written
+// as the activation's e2m1 digit operand rows plus its scale and int8 sum,
+// exactly as the quantization kernel writes them, then counted in the
+// activation's ready counter (a release). The CTA that owns row 0 of an
+// activation first zeroes the split-K partial dots and chunk counters of the
+// problems that read it, so every add to them comes after the zeroing.
 template <int Mp>
-__global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_constant__ TcArgs a) {
+__device__ void fused_quantize(const GvFusedArgs& a, int t, const uint32_t* code, float* s_red, int* s_sum) {
+    const int lane = t & 31, w = t >> 5;
+    const long long C = a.cost_total, G = gridDim.x, b = blockIdx.x;
+    const long long lo = (b * C + G - 1) / G, hi = ((b + 1) * C + G - 1) / G;
+    for (int ai = 0; ai < a.n_acts; ++ai) {
+        const GvAct& A = a.acts[ai];
+        const long long K = A.K;
+        const long long s0 = A.cost0;
+        if (s0 + (long long)a.M * K <= lo || s0 >= hi) continue;
+        const int m_lo = lo <= s0 ? 0 : (int)((lo - s0 + K - 1) / K);
+        const int m_hi = (int)min((long long)a.M, (hi - s0 + K - 1) / K);
+        for (int m = m_lo; m < m_hi; ++m) {
+            if (m == 0) {
+                for (int i = 0; i < a.count; ++i) {
+                    const TcProb& P = a.p[i];
+                    if (P.map != ai || P.chunks <= 1) continue;
+                    int32_t* part = a.dot_base + P.dot_off;
+                    for (int e = t; e < a.M * P.N; e += 128) part[e] = 0;
+                    uint32_t* tk = a.ticket_base + P.ticket_off;
+                    for (int e = t; e < (P.N + kTileRows - 1) / kTileRows; e += 128) tk[e] = 0u;
+                }
+            }
+            const int Ki = A.K, U = Ki / 16;
+            const float4* x4 = reinterpret_cast<const float4*>(A.x + (size_t)m * Ki);
+            float4 cache[kTeamCache][4];
+            float amax = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kTeamCache; ++c) {
+                const int u = t + c * 128;
+                if (u < U) {
+                    load_unit(x4, u, cache[c]);
+                    amax = fmaxf(amax, unit_amax(cache[c]));
+                }
+            }
+            for (int u = t + kTeamCache * 128; u < U; u += 128) {
+                float4 v[4];
+                load_unit(x4, u, v);
+                amax = fmaxf(amax, unit_amax(v));
+            }
+            amax = warp_max(amax);
+            if (lane == 0) s_red[w] = amax;
+            team_sync();
+            amax = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+            float scale, inv;
+            quant_params(amax, scale, inv);
+            int sum = 0;
+#pragma unroll
+            for (int c = 0; c < kTeamCache; ++c) {
+                const int u = t + c * 128;
+                if (u < U) sum += emit_unit(cache[c], inv, u, A.op, (size_t)Ki / 2, Mp, m, code);
+            }
+            for (int u = t + kTeamCache * 128; u < U; u += 128) {
+                float4 v[4];
+                load_unit(x4, u, v);
+                sum += emit_unit(v, inv, u, A.op, (size_t)Ki / 2, Mp, m, code);
+            }
+            sum = warp_sum(sum);
+            if (lane == 0) s_sum[w] = sum;
+            // the digit rows are read by other CTAs' TMA loads (the async proxy)
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            team_sync();
+            if (t == 0) {
+                A.scale[m] = scale;
+                A.sum[m] = s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
+                __threadfence();
+                atomicAdd(&a.flags[a.count + ai], 1u);
+            }
+        }
+    }
+}
+
+template <bool kFused, typename Args>
+__device__ __forceinline__ const CUtensorMap* act_map(const Args& a, int i) {
+    if constexpr (kFused) return &a.kmaps[i];
+    else return &a.maps[i];
+}
+
+template <int Mp, bool kFused, typename Args>
+__global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_constant__ Args a) {
     constexpr int kN = gemv_tc_op_rows(Mp);                 // MMA N: three digit rows per activation row, padded
     constexpr uint32_t kBSub = (uint32_t)kN * 128u;          // one 256-position operand sub-tile (1024-aligned)
     constexpr uint32_t kBStageBytes = 2 * kBSub;             // a stage holds two sub-tiles
@@ -252,8 +374,25 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     const int n_sp = s_prange[1] - p_first + 1;
     for (int i = tid; i < n_sp; i += kThreadsGv) {
         const TcProb& P = a.p[p_first + i];
-        sp[i] = SProb{P.w, P.act_scale, P.row_sum, P.y, P.N, P.K, P.map, P.tile0, P.chunks, P.dot_off, P.ticket_off,
-                      p_first + i};
+        int map = P.map, row0 = 0;
+        if constexpr (kFused) {   // stacked operands: the activation's class map and first row
+            map = a.acts[P.map].kclass;
+            row0 = a.acts[P.map].row0;
+        }
+        sp[i] = SProb{P.w, P.act_scale, P.row_sum, P.y, P.N, P.K, map, P.tile0, P.chunks, P.dot_off, P.ticket_off,
+                      p_first + i, row0, P.map};
+    }
+    uint32_t* s_code = nullptr;
+    float* s_red = nullptr;
+    int* s_sum = nullptr;
+    if constexpr (kFused) {   // the digit table of the prologue's quantizer
+        __shared__ uint32_t s_code_tab[255];
+        __shared__ float s_red_team[4];
+        __shared__ int s_sum_team[4];
+        if (tid < 255) s_code_tab[tid] = digit_code(tid - 127);
+        s_code = s_code_tab;
+        s_red = s_red_team;
+        s_sum = s_sum_team;
     }
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
@@ -310,6 +449,23 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     // workspace (operands, weight maps, partial sums) is read from here on,
     // after the quantization launch before this one has completed
     pdl_wait();
+    if constexpr (kFused) {
+        // Prologue of the fused launch: the activation producer's lanes write
+        // the weight maps (map i by CTA i mod grid) and flag each; the
+        // epilogue warps quantize this CTA's share of the activation rows.
+        // The other roles start at once: the weight producer waits only for
+        // the flag of the map it needs, the activation producer and the
+        // epilogue for the ready counter of their activation.
+        if (warp == kBProdWarp) {
+            for (int i = (int)blockIdx.x + (int)gridDim.x * lane; i < a.count; i += (int)gridDim.x * 32) {
+                const TcProb& P = a.p[i];
+                write_weight_map(a.wtmpl, a.wmaps + i, P.w, P.N, P.K);
+                st_release_u32(a.flags + i, 1u);
+            }
+        } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+            fused_quantize<Mp>(a, tid - kEpiWarp0 * 32, s_code, s_red, s_sum);
+        }
+    }
 
     int ucur = u_begin;   // each role advances its own copy of the unit cursor
     auto next_seg = [&](const Seg& g) { ucur += g.units; return seg_next(sp, g, ucur, u_end); };
@@ -329,6 +485,9 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
                 const CUtensorMap* map = a.wmaps + g.pidx;
                 if (g.pidx != cur_p) {   // first use of this map: order it after the writer's release
+                    if constexpr (kFused) {
+                        if (!wait_flag(a.flags + g.pidx, 1u, abort_flag, kWaitLimitGv)) { fail(4096); ok = false; break; }
+                    }
                     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
                     cur_p = g.pidx;
                 }
@@ -419,21 +578,33 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             bool ok = true;
             {
                 const Seg g0 = seg_at(sp, n_sp, ucur, u_end);
-                if (g0.live) tc::tma_prefetch_desc(&a.maps[g0.map]);
+                if (g0.live) tc::tma_prefetch_desc(act_map<kFused>(a, g0.map));
             }
+            int cur_act = -1;
             for (Seg g = seg_at(sp, n_sp, ucur, u_end); ok && g.live; g = next_seg(g)) {
-                const CUtensorMap* map = &a.maps[g.map];
+                const CUtensorMap* map = act_map<kFused>(a, g.map);
                 {   // fetch the next segment's descriptor while this one streams
                     const Seg gn = seg_next(sp, g, ucur + g.units, u_end);
-                    if (gn.live && gn.map != g.map) tc::tma_prefetch_desc(&a.maps[gn.map]);
+                    if (gn.live && gn.map != g.map) tc::tma_prefetch_desc(act_map<kFused>(a, gn.map));
+                }
+                if constexpr (kFused) {   // the activation's rows are quantized by the prologue
+                    if (g.act != cur_act) {
+                        if (!wait_flag(a.flags + a.count + g.act, (uint32_t)a.M, abort_flag, kWaitLimitGv)) {
+                            fail(8192);
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        cur_act = g.act;
+                    }
                 }
                 for (int kb = g.st_lo; kb < g.st_hi; ++kb) {
                     const bool two = kb * kKB + kKB / 2 < g.K;   // the stage reaches its second 256 positions
                     if (!tc::mbar_wait_idle(&S.empty_b[stage], phase ^ 1, abort_flag, kWaitLimitGv)) { fail(64); ok = false; break; }
                     tc::mbar_arrive_expect_tx(&S.full_b[stage], two ? kBStageBytes : kBSub);
                     uint8_t* dst = sB + (size_t)stage * kBStageBytes;
-                    tc::tma_load_2d(dst, map, kb * (kKB / 2), 0, &S.full_b[stage]);
-                    if (two) tc::tma_load_2d(dst + kBSub, map, kb * (kKB / 2) + 128, 0, &S.full_b[stage]);
+                    tc::tma_load_2d(dst, map, kb * (kKB / 2), g.row0, &S.full_b[stage]);
+                    if (two) tc::tma_load_2d(dst + kBSub, map, kb * (kKB / 2) + 128, g.row0, &S.full_b[stage]);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
                     if (++stage == kBStages) { stage = 0; phase ^= 1; }
@@ -506,8 +677,15 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         const int r = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0, sync_phase = 0;
+        int cur_act = -1;
         for (Seg g = seg_at(sp, n_sp, ucur, u_end); g.live; g = next_seg(g)) {
             const int n = g.n0 + r;
+            if constexpr (kFused) {   // row scales and sums, and the zeroed partials, come from the prologue
+                if (g.act != cur_act) {
+                    if (!wait_flag(a.flags + a.count + g.act, (uint32_t)a.M, abort_flag, kWaitLimitGv)) { fail(8192); break; }
+                    cur_act = g.act;
+                }
+            }
             if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimitGv)) { fail(512); break; }
             tc::tc_fence_after();
             const uint32_t dcol = tmem_base + ((uint32_t)(q * 32) << 16) + (acc ? kDCol1 : kDCol0);
@@ -579,6 +757,20 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem_base, kTmemColsGv);
     }
+    if constexpr (kFused) {
+        // The last CTA to finish clears the flags and counters for the next
+        // launch on this workspace (every CTA has read its last flag by now).
+        if (tid == 0) {
+            __threadfence();
+            uint32_t* done = a.flags + a.count + a.n_acts;
+            if (atomicAdd(done, 1u) == gridDim.x - 1) {
+                __threadfence();
+                for (int i = 0; i < a.count + a.n_acts; ++i) a.flags[i] = 0u;
+                __threadfence();
+                *done = 0u;
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -590,9 +782,11 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(k_i2s_gemv_tc<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemGvBytes);
+        e = cudaFuncSetAttribute(k_i2s_gemv_tc<8, false, TcArgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemGvBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_i2s_gemv_tc<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemGvBytes);
+            e = cudaFuncSetAttribute(k_i2s_gemv_tc<16, false, TcArgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemGvBytes);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
@@ -607,8 +801,39 @@ cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.BN == 8) return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<8>, a);
-    return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<16>, a);
+    if (a.BN == 8) return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<8, false, TcArgs>, a);
+    return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<16, false, TcArgs>, a);
+}
+
+cudaError_t launch_gemv_fused(const GvFusedArgs& a, int grid, cudaStream_t s) {
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(k_i2s_gemv_tc<8, true, GvFusedArgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemGvBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_i2s_gemv_tc<16, true, GvFusedArgs>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemGvBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    // a programmatic dependent of the launch before it (which may produce x
+    // or use this workspace): the prologue starts after pdl_wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreadsGv, 1, 1);
+    cfg.dynamicSmemBytes = kSmemGvBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.BN == 8) return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<8, true, GvFusedArgs>, a);
+    return cudaLaunchKernelEx(&cfg, k_i2s_gemv_tc<16, true, GvFusedArgs>, a);
 }
 
 }  // namespace i2s

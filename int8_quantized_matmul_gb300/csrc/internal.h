@@ -106,8 +106,40 @@ constexpr int kGemvShareFirst = 23, kGemvShareSecond = 17;
 __host__ __device__ constexpr int gemv_tc_mp(int64_t M) { return M <= 8 ? 8 : 16; }
 __host__ __device__ constexpr int gemv_tc_op_rows(int Mp) { return Mp == 8 ? 32 : 48; }
 
+// Fused decode launch (i2s_mul_mat_grouped_fused): the GEMV whose prologue
+// quantizes the activations and writes the weight maps itself. The digit
+// operands of all activations with the same K are stacked in one buffer (one
+// tensor map per distinct K); activation a's rows start at row0.
+constexpr int kGvMaxKClasses = 8;
+struct GvAct {
+    const float* x;      // M x K F32 (the caller's)
+    float* scale;        // M row scales (workspace)
+    int32_t* sum;        // M row sums (workspace)
+    uint8_t* op;         // its gemv_tc_op_rows(M') digit rows of K/2 bytes (workspace)
+    long long cost0;     // position of its first row in the launch's quantization order (K per row)
+    int K;
+    int kclass;          // index into kmaps
+    int row0;            // first operand row in its class's stacked buffer
+    int pad_;
+};
+struct GvFusedArgs {
+    CUtensorMap kmaps[kGvMaxKClasses];
+    CUtensorMap wtmpl;          // uint8 2-D template, box 128 bytes x 128 rows, 128-byte swizzle
+    GvAct acts[kTcMaxMaps];
+    CUtensorMap* wmaps;         // one map per problem (workspace), written by the prologue
+    uint32_t* flags;            // [count] map written, [n_acts] rows quantized, [1] CTAs done
+    uint32_t* status;
+    int32_t* dot_base;          // split-K partial dots, zeroed by the prologue
+    uint32_t* ticket_base;      // split-K chunk counters, zeroed by the prologue
+    long long cost_total;       // sum over activations of M * K
+    int n_acts, count, M, BN, total_tiles, share_first, share_second;
+    TcProb p[kMaxGroup];        // TcProb::map = activation index (its class and row0 in acts[])
+};
+cudaError_t launch_gemv_fused(const GvFusedArgs& a, int grid, cudaStream_t s);
+
 // Kernel parameters are limited to 32764 bytes.
 static_assert(sizeof(TcArgs) <= 32764, "TcArgs exceeds the kernel parameter limit");
+static_assert(sizeof(GvFusedArgs) <= 32764, "GvFusedArgs exceeds the kernel parameter limit");
 static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel parameter limit");
 
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);

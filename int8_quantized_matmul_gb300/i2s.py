@@ -66,6 +66,9 @@ _SIGS = {
     "i2s_mul_mat_grouped": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_quantize": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_run": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i2s_mul_mat_grouped_fused_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
+    "i2s_mul_mat_grouped_fused_init": (_int, [_p, _sz, _p]),
+    "i2s_mul_mat_grouped_fused": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i8s_mul_mat_workspace": (_sz, [_i64, _i64, _i64]),
     "i8s_ws_f32_offset": (_sz, []),
     "i8s_mul_mat_add_relu": (_int, [_p, _i64, _i64, _p, _i64, _p, _int, _p, _p, _sz, _p]),
@@ -232,6 +235,29 @@ def i2s_mul_mat_grouped_workspace(problems: Sequence, M: int) -> int:
     return int(_L.i2s_mul_mat_grouped_workspace(arr, len(problems), M))
 
 
+def i2s_mul_mat_grouped_fused_workspace(problems: Sequence, M: int) -> int:
+    arr = _problems(problems)
+    return int(_L.i2s_mul_mat_grouped_fused_workspace(arr, len(problems), M))
+
+
+def i2s_mul_mat_grouped_fused_init(ws):
+    """Zeroes the flag area of a workspace before its first fused call."""
+    _check("i2s_mul_mat_grouped_fused_init", _L.i2s_mul_mat_grouped_fused_init(_dptr(ws), ws.numel(), _stream()))
+    return ws
+
+
+def i2s_mul_mat_grouped_fused(problems: Sequence, M: int, ws=None):
+    """The grouped decode matmul (M <= 16) as one launch that quantizes its own
+    activations; ws must have been initialised (a new ws is)."""
+    arr = _problems(problems)
+    if ws is None:
+        ws = _ws(_L.i2s_mul_mat_grouped_fused_workspace(arr, len(problems), M), problems[0][3].device)
+        i2s_mul_mat_grouped_fused_init(ws)
+    _check("i2s_mul_mat_grouped_fused",
+           _L.i2s_mul_mat_grouped_fused(arr, len(problems), M, _dptr(ws), ws.numel(), _stream()))
+    return ws
+
+
 def i2s_mul_mat_grouped(problems: Sequence, M: int, ws=None):
     """Runs [(w, N, K, x, y), ...] (all with M activation rows) as one group."""
     arr = _problems(problems)
@@ -269,6 +295,27 @@ class Group:
         _check("i2s_mul_mat_grouped",
                _L.i2s_mul_mat_grouped(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
                                       _stream()))
+
+
+class FusedGroup:
+    """A fixed list of decode projections [(w, N, K, x, y), ...] with M <= 16
+    rows, run as one fused launch (the GEMV quantizes its own activations);
+    marshalled once, the workspace initialised once."""
+
+    def __init__(self, problems: Sequence, M: int, ws=None):
+        self.problems = list(problems)
+        self.M = int(M)
+        self.arr = _problems(self.problems)
+        need = int(_L.i2s_mul_mat_grouped_fused_workspace(self.arr, len(self.problems), self.M))
+        if need == 0:
+            raise I2SError("i2s_mul_mat_grouped_fused_workspace", -1)
+        self.ws = ws if ws is not None else _ws(need, self.problems[0][3].device)
+        i2s_mul_mat_grouped_fused_init(self.ws)
+
+    def __call__(self):
+        _check("i2s_mul_mat_grouped_fused",
+               _L.i2s_mul_mat_grouped_fused(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
+                                            _stream()))
 
 
 def i8s_mul_mat_workspace(M: int, N: int, K: int) -> int:

@@ -178,3 +178,31 @@ def test_eltwise_and_w8a8_validation_needs_no_device(i2s):
     for i in range(3):
         distinct[i] = i2s.w8a8_problem(A, A, 64, 128, A + 4096 * i, A)
     assert L.w8a8_mul_mat_grouped_workspace(distinct, 3, 8) > L.w8a8_mul_mat_grouped_workspace(shared, 3, 8) > 0
+
+
+def test_fused_decode_validation_needs_no_device(i2s):
+    L = i2s.lib
+    A = 1 << 20
+    vp = ctypes.c_void_p
+    E = {v: k for k, v in i2s.STATUS.items()}
+    probs = (i2s.i2s_problem * 2)()
+    probs[0] = i2s.i2s_problem(A, 64, 1536, 2 * A, 3 * A)
+    probs[1] = i2s.i2s_problem(A, 300, 1536, 2 * A, 4 * A)   # shares the activation
+    ws1 = L.i2s_mul_mat_grouped_fused_workspace(probs, 2, 1)
+    ws16 = L.i2s_mul_mat_grouped_fused_workspace(probs, 2, 16)
+    assert 0 < ws1 < ws16
+    assert L.i2s_mul_mat_grouped_fused_workspace(probs, 2, 17) == 0      # M <= 16 only
+    assert L.i2s_mul_mat_grouped_fused(probs, 2, 17, vp(8 * A), 1 << 30, None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i2s_mul_mat_grouped_fused(probs, 0, 1, vp(8 * A), 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_fused(probs, 2, 1, vp(8 * A + 16), 1 << 30, None) == E["I2S_E_MISALIGNED"]
+    assert L.i2s_mul_mat_grouped_fused(probs, 2, 1, vp(8 * A), ws1 - 1, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    assert L.i2s_mul_mat_grouped_fused_init(None, 4096, None) == E["I2S_E_NULL_PTR"]
+    assert L.i2s_mul_mat_grouped_fused_init(vp(8 * A + 16), 4096, None) == E["I2S_E_MISALIGNED"]
+    assert L.i2s_mul_mat_grouped_fused_init(vp(8 * A), 1024, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    # nine distinct K values are more than one launch's operand maps hold
+    nine = (i2s.i2s_problem * 9)()
+    for i in range(9):
+        nine[i] = i2s.i2s_problem(A, 64, 128 * (i + 1), 2 * A + 65536 * i, 3 * A)
+    assert L.i2s_mul_mat_grouped_fused_workspace(nine, 8, 4) > 0
+    assert L.i2s_mul_mat_grouped_fused_workspace(nine, 9, 4) == 0
+    assert L.i2s_mul_mat_grouped_fused(nine, 9, 4, vp(8 * A), 1 << 30, None) == E["I2S_E_BAD_ARG"]
