@@ -555,8 +555,28 @@ int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, vo
         A.cost0 = cost;
         A.K = (int)p.K;
         A.kclass = c;
-        A.pad_ = 0;
+        A.dot_lo = A.dot_n = A.tk_lo = A.tk_n = 0;
         cost += M * p.K;
+    }
+    // split-K areas laid out activation by activation, so the prologue zeroes
+    // one contiguous range per activation
+    std::vector<int> dot_off(count, 0), ticket_off(count, 0);
+    {
+        int dot_elems = 0, ticket_elems = 0;
+        for (int a = 0; a < pl.n_act; ++a) {
+            GvAct& A = fa.acts[a];
+            A.dot_lo = dot_elems;
+            A.tk_lo = ticket_elems;
+            for (int i = 0; i < count; ++i) {
+                if (pl.act_of[i] != a || probs[i].K <= kGemvChunkPositions) continue;
+                dot_off[i] = dot_elems;
+                ticket_off[i] = ticket_elems;
+                dot_elems += (int)(M * probs[i].N);
+                ticket_elems += (int)((probs[i].N + kTcTileW - 1) / kTcTileW);
+            }
+            A.dot_n = dot_elems - A.dot_lo;
+            A.tk_n = ticket_elems - A.tk_lo;
+        }
     }
     fa.cost_total = cost;
     fa.wmaps = wmaps;
@@ -568,7 +588,7 @@ int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, vo
     fa.count = count;
     fa.M = (int)M;
     fa.BN = Mp;
-    int units = 0, dot_elems = 0, ticket_elems = 0;
+    int units = 0;
     for (int i = 0; i < count; ++i) {
         const i2s_problem& q = probs[i];
         const int act = pl.act_of[i];
@@ -585,12 +605,8 @@ int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, vo
         P.tile0 = units;
         P.n_act_tiles = 1;
         P.chunks = chunks;
-        P.dot_off = dot_elems;
-        P.ticket_off = ticket_elems;
-        if (chunks > 1) {
-            dot_elems += (int)(M * q.N);
-            ticket_elems += row_tiles;
-        }
+        P.dot_off = dot_off[i];
+        P.ticket_off = ticket_off[i];
         units += row_tiles * chunks;
     }
     fa.total_tiles = units;

@@ -233,88 +233,169 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* p, uint32_t want, vola
     return true;
 }
 
-__device__ __forceinline__ void team_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }   // epilogue warps 4-7
+// The prologue's quantizer team: every warp but the weight producer (352
+// threads), synchronised by named barrier 1.
+constexpr int kTeamThreads = kThreadsGv - 32;
+__device__ __forceinline__ void team_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTeamThreads) : "memory"); }
 
-constexpr int kTeamCache = 2;   // 16-value units per thread kept in registers while the amax is reduced
+constexpr int kTeamRows = 64;      // rows of one batch (shared-memory slots)
+constexpr int kTeamUnits = 2;      // 16-value units per thread kept in registers in the one-pass case
 
-// The prologue's share of the row quantization, done by the 128 threads of
-// the epilogue warps (team thread t). The rows of all activations are laid
-// end to end, each costing K positions; this CTA takes the rows whose first
-// position falls in its equal share [lo, hi) of the total. A row is written
-// as the activation's e2m1 digit operand rows plus its scale and int8 sum,
-// exactly as the quantization kernel writes them, then counted in the
-// activation's ready counter (a release). The CTA that owns row 0 of an
-// activation first zeroes the split-K partial dots and chunk counters of the
-// problems that read it, so every add to them comes after the zeroing.
+// Shared state of the prologue's quantizer: one batch of up to kTeamRows rows.
+struct TeamRows {
+    uint32_t amax_bits[kTeamRows];   // max |x| of each row, as float bits (non-negative, so integer max works)
+    float inv[kTeamRows];
+    int sum[kTeamRows];
+    int act[kTeamRows], m[kTeamRows];
+    int u0[kTeamRows + 1];           // first 16-value unit of each row in the batch's flattened order
+};
+
+// Row of flattened unit j of a batch of n rows (binary search over u0).
+__device__ __forceinline__ int team_row_of(const TeamRows& R, int n, int j) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (R.u0[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void team_load(const GvFusedArgs& a, const TeamRows& R, int r, int j, float4 (&v)[4]) {
+    const GvAct& A = a.acts[R.act[r]];
+    load_unit(reinterpret_cast<const float4*>(A.x + (size_t)R.m[r] * A.K), j - R.u0[r], v);
+}
+
+__device__ __forceinline__ int team_emit(const GvFusedArgs& a, const TeamRows& R, int r, int j, const float4 (&v)[4],
+                                         int Mp, const uint32_t* code) {
+    const GvAct& A = a.acts[R.act[r]];
+    return emit_unit(v, R.inv[r], j - R.u0[r], A.op, (size_t)A.K / 2, Mp, R.m[r], code);
+}
+
+// The prologue's share of the row quantization, done by the team (thread t).
+// The rows of all activations are laid end to end, each costing K positions;
+// this CTA takes the rows whose first position falls in its equal share
+// [lo, hi) of the total. Rows are handled in batches, every row of a batch at
+// once: each thread loads its 16-value units, folds each row's max |x| into
+// shared memory, and after a barrier quantizes with the row's 127/amax,
+// writes the e2m1 digit rows and folds the int8 sums. A batch whose units fit
+// in registers (kTeamUnits per thread) is read once; a longer row is read
+// twice (the second pass from L2). Each row is then published with its scale
+// and sum through its activation's ready counter (a release). The CTA that
+// owns row 0 of an activation first zeroes the split-K partial dots and
+// chunk counters of the problems that read it, so every add to them comes
+// after the zeroing.
 template <int Mp>
-__device__ void fused_quantize(const GvFusedArgs& a, int t, const uint32_t* code, float* s_red, int* s_sum) {
-    const int lane = t & 31, w = t >> 5;
+__device__ void fused_quantize(const GvFusedArgs& a, int t, const uint32_t* code, TeamRows& R) {
     const long long C = a.cost_total, G = gridDim.x, b = blockIdx.x;
     const long long lo = (b * C + G - 1) / G, hi = ((b + 1) * C + G - 1) / G;
-    for (int ai = 0; ai < a.n_acts; ++ai) {
+    if (lo >= hi) return;
+    constexpr int kCap = kTeamUnits * kTeamThreads;
+    // the last activation starting at or before lo (activations are laid out
+    // in order of cost0), and its first row starting at or after lo
+    int ai = 0;
+    {
+        int last = a.n_acts - 1;
+        while (ai < last) {
+            const int mid = (ai + last + 1) >> 1;
+            if (a.acts[mid].cost0 <= lo) ai = mid; else last = mid - 1;
+        }
+    }
+    int m = 0;
+    {
         const GvAct& A = a.acts[ai];
-        const long long K = A.K;
-        const long long s0 = A.cost0;
-        if (s0 + (long long)a.M * K <= lo || s0 >= hi) continue;
-        const int m_lo = lo <= s0 ? 0 : (int)((lo - s0 + K - 1) / K);
-        const int m_hi = (int)min((long long)a.M, (hi - s0 + K - 1) / K);
-        for (int m = m_lo; m < m_hi; ++m) {
-            if (m == 0) {
-                for (int i = 0; i < a.count; ++i) {
-                    const TcProb& P = a.p[i];
-                    if (P.map != ai || P.chunks <= 1) continue;
-                    int32_t* part = a.dot_base + P.dot_off;
-                    for (int e = t; e < a.M * P.N; e += 128) part[e] = 0;
-                    uint32_t* tk = a.ticket_base + P.ticket_off;
-                    for (int e = t; e < (P.N + kTileRows - 1) / kTileRows; e += 128) tk[e] = 0u;
-                }
+        if (lo > A.cost0) m = (int)((lo - A.cost0 + A.K - 1) / A.K);
+    }
+    while (true) {
+        // gather the next batch (the same walk in every team thread): rows
+        // starting in [lo, hi), while they fit the registers (a longer row
+        // goes alone)
+        int n = 0, units = 0;
+        while (n < kTeamRows && ai < a.n_acts) {
+            const GvAct& A = a.acts[ai];
+            if (m >= a.M) { ++ai; m = 0; continue; }
+            if (A.cost0 + (long long)m * A.K >= hi) break;
+            const int u = A.K / 16;
+            if (n > 0 && units + u > kCap) break;
+            if (t == 0) {
+                R.act[n] = ai;
+                R.m[n] = m;
+                R.u0[n] = units;
+                R.amax_bits[n] = 0u;
+                R.sum[n] = 0;
             }
-            const int Ki = A.K, U = Ki / 16;
-            const float4* x4 = reinterpret_cast<const float4*>(A.x + (size_t)m * Ki);
-            float4 cache[kTeamCache][4];
-            float amax = 0.0f;
+            units += u;
+            ++n;
+            ++m;
+        }
+        if (n == 0) break;
+        if (t == 0) R.u0[n] = units;
+        team_sync();
+        // zero the split-K areas of activations whose row 0 is in the batch
+        for (int i = 0; i < n; ++i) {
+            if (R.m[i] != 0) continue;
+            const GvAct& A = a.acts[R.act[i]];
+            for (int e = t; e < A.dot_n; e += kTeamThreads) a.dot_base[A.dot_lo + e] = 0;
+            for (int e = t; e < A.tk_n; e += kTeamThreads) a.ticket_base[A.tk_lo + e] = 0u;
+        }
+        if (units <= kCap) {
+            // one pass: every load in flight at once, the units kept in registers
+            float4 v[kTeamUnits][4];
+            int rr[kTeamUnits];
 #pragma unroll
-            for (int c = 0; c < kTeamCache; ++c) {
-                const int u = t + c * 128;
-                if (u < U) {
-                    load_unit(x4, u, cache[c]);
-                    amax = fmaxf(amax, unit_amax(cache[c]));
-                }
+            for (int c = 0; c < kTeamUnits; ++c) {
+                const int j = t + c * kTeamThreads;
+                rr[c] = j < units ? team_row_of(R, n, j) : -1;
+                if (rr[c] >= 0) team_load(a, R, rr[c], j, v[c]);
             }
-            for (int u = t + kTeamCache * 128; u < U; u += 128) {
-                float4 v[4];
-                load_unit(x4, u, v);
-                amax = fmaxf(amax, unit_amax(v));
-            }
-            amax = warp_max(amax);
-            if (lane == 0) s_red[w] = amax;
+#pragma unroll
+            for (int c = 0; c < kTeamUnits; ++c)
+                if (rr[c] >= 0) atomicMax(&R.amax_bits[rr[c]], __float_as_uint(unit_amax(v[c])));
             team_sync();
-            amax = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-            float scale, inv;
-            quant_params(amax, scale, inv);
-            int sum = 0;
+            for (int i = t; i < n; i += kTeamThreads) {
+                float scale, inv;
+                quant_params(__uint_as_float(R.amax_bits[i]), scale, inv);
+                R.inv[i] = inv;
+            }
+            team_sync();
 #pragma unroll
-            for (int c = 0; c < kTeamCache; ++c) {
-                const int u = t + c * 128;
-                if (u < U) sum += emit_unit(cache[c], inv, u, A.op, (size_t)Ki / 2, Mp, m, code);
-            }
-            for (int u = t + kTeamCache * 128; u < U; u += 128) {
+            for (int c = 0; c < kTeamUnits; ++c)
+                if (rr[c] >= 0) atomicAdd(&R.sum[rr[c]], team_emit(a, R, rr[c], t + c * kTeamThreads, v[c], Mp, code));
+        } else {
+            // one row longer than the registers hold: two passes
+            for (int j = t; j < units; j += kTeamThreads) {
                 float4 v[4];
-                load_unit(x4, u, v);
-                sum += emit_unit(v, inv, u, A.op, (size_t)Ki / 2, Mp, m, code);
+                team_load(a, R, 0, j, v);
+                atomicMax(&R.amax_bits[0], __float_as_uint(unit_amax(v)));
             }
-            sum = warp_sum(sum);
-            if (lane == 0) s_sum[w] = sum;
-            // the digit rows are read by other CTAs' TMA loads (the async proxy)
-            asm volatile("fence.proxy.async.global;" ::: "memory");
             team_sync();
             if (t == 0) {
-                A.scale[m] = scale;
-                A.sum[m] = s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
-                __threadfence();
-                atomicAdd(&a.flags[a.count + ai], 1u);
+                float scale, inv;
+                quant_params(__uint_as_float(R.amax_bits[0]), scale, inv);
+                R.inv[0] = inv;
+            }
+            team_sync();
+            for (int j = t; j < units; j += kTeamThreads) {
+                float4 v[4];
+                team_load(a, R, 0, j, v);
+                atomicAdd(&R.sum[0], team_emit(a, R, 0, j, v, Mp, code));
             }
         }
+        // the digit rows are read by other CTAs' TMA loads (the async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        team_sync();
+        // a fence of the counting thread after the barrier orders every team
+        // thread's stores (digit rows, zeroed areas) and its own scale and sum
+        // before the count
+        for (int i = t; i < n; i += kTeamThreads) {
+            const GvAct& A = a.acts[R.act[i]];
+            float scale, inv;
+            quant_params(__uint_as_float(R.amax_bits[i]), scale, inv);
+            A.scale[R.m[i]] = scale;
+            A.sum[R.m[i]] = R.sum[i];
+            __threadfence();
+            atomicAdd(&a.flags[a.count + R.act[i]], 1u);
+        }
+        team_sync();   // the batch's shared slots are reused by the next batch
     }
 }
 
@@ -383,16 +464,13 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                       p_first + i, row0, P.map};
     }
     uint32_t* s_code = nullptr;
-    float* s_red = nullptr;
-    int* s_sum = nullptr;
-    if constexpr (kFused) {   // the digit table of the prologue's quantizer
+    TeamRows* s_rows = nullptr;
+    if constexpr (kFused) {   // the digit table and row slots of the prologue's quantizer
         __shared__ uint32_t s_code_tab[255];
-        __shared__ float s_red_team[4];
-        __shared__ int s_sum_team[4];
+        __shared__ TeamRows s_rows_team;
         if (tid < 255) s_code_tab[tid] = digit_code(tid - 127);
         s_code = s_code_tab;
-        s_red = s_red_team;
-        s_sum = s_sum_team;
+        s_rows = &s_rows_team;
     }
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
@@ -451,20 +529,21 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
     pdl_wait();
     if constexpr (kFused) {
         // Prologue of the fused launch: the activation producer's lanes write
-        // the weight maps (map i by CTA i mod grid) and flag each; the
-        // epilogue warps quantize this CTA's share of the activation rows.
-        // The other roles start at once: the weight producer waits only for
-        // the flag of the map it needs, the activation producer and the
-        // epilogue for the ready counter of their activation.
+        // the weight maps (map i by CTA i mod grid) and flag each; every warp
+        // but the weight producer then quantizes this CTA's share of the
+        // activation rows. The weight producer starts streaming at once,
+        // waiting only for the flag of the map it needs; the activation
+        // producer and the epilogue wait for the ready counter of their
+        // activation.
         if (warp == kBProdWarp) {
             for (int i = (int)blockIdx.x + (int)gridDim.x * lane; i < a.count; i += (int)gridDim.x * 32) {
                 const TcProb& P = a.p[i];
                 write_weight_map(a.wtmpl, a.wmaps + i, P.w, P.N, P.K);
                 st_release_u32(a.flags + i, 1u);
             }
-        } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-            fused_quantize<Mp>(a, tid - kEpiWarp0 * 32, s_code, s_red, s_sum);
         }
+        if (warp != kWProdWarp)   // the team: thread index without the weight producer's warp
+            fused_quantize<Mp>(a, warp < kWProdWarp ? tid : tid - 32, s_code, *s_rows);
     }
 
     int ucur = u_begin;   // each role advances its own copy of the unit cursor

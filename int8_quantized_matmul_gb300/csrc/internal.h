@@ -120,7 +120,8 @@ struct GvAct {
     int K;
     int kclass;          // index into kmaps
     int row0;            // first operand row in its class's stacked buffer
-    int pad_;
+    int dot_lo, dot_n;   // split-K partial dots of the problems that read it (one contiguous range)
+    int tk_lo, tk_n;     // their chunk counters (one contiguous range)
 };
 struct GvFusedArgs {
     CUtensorMap kmaps[kGvMaxKClasses];
