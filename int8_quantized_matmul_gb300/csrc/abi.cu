@@ -745,8 +745,36 @@ static int i8s_plan_pairs(I8sTcArgs& a) {
 }
 
 // the tile height of a launch over these matmuls (the resident pairs decide)
+// The tile height of a launch. The busiest CTA pair's work bounds the
+// kernel, and a unit moves 256 weight rows and tm activation rows of operands
+// through shared memory per K position. For each height the pair ranges are
+// planned as the launch plans them (whole tiles where it can), and the height
+// whose busiest pair moves fewer operand rows wins, 160 on a tie. (Counting
+// units as if they were split evenly would favour 160 for the encoder's FC2,
+// whose whole tiles then run on 48 pairs of 8 x 416 rows, against 64 pairs of
+// 8 x 384 rows with 128-row tiles.)
 static int i8s_pick_tile(int64_t M, const int64_t* N, const int64_t* K, int count) {
-    return i8s_tile_m(M, N, K, count, i8s_gemm_tc_max_pairs());
+    static thread_local I8sTcArgs t;
+    int best = kI8sTileM;
+    int64_t best_cost = -1;
+    for (int tm : {kI8sTileM, kI8sTileMSmall}) {
+        t.count = count;
+        t.n_at = (int)((M + tm - 1) / tm);
+        int64_t units = 0;
+        for (int i = 0; i < count; ++i) {
+            t.p[i].n_wt = (int)((N[i] + 2 * kI8sTileN - 1) / (2 * kI8sTileN));
+            t.p[i].chunks = (int)i8s_chunks(K[i]);
+            units += (int64_t)t.p[i].n_wt * t.n_at * t.p[i].chunks;
+        }
+        if (units >= ((int64_t)1 << 30)) return i8s_tile_m(M, N, K, count, i8s_gemm_tc_max_pairs());
+        t.total_units = (int)units;
+        const int pairs = i8s_plan_pairs(t);
+        int64_t busiest = 0;
+        for (int q = 0; q < pairs; ++q) busiest = std::max<int64_t>(busiest, t.bounds[q + 1] - t.bounds[q]);
+        const int64_t cost = busiest * (2 * kI8sTileN + tm);
+        if (best_cost < 0 || cost < best_cost) best_cost = cost, best = tm;
+    }
+    return best;
 }
 
 // K is the operand row length i8s_kpad(K) wherever f16 rows are sized.

@@ -168,8 +168,9 @@ constexpr int kI8sMaxK = 64 * kI8sChunkK;   // at most 64 chunks (the slot mask 
 // a zero product adds nothing, so any K gives the exact integer dot.
 inline int64_t i8s_kpad(int64_t K) { return (K + 63) / 64 * 64; }
 
-// The tile height of a launch whose matmuls have M rows, N[i] features and
-// K[i] positions, run by `pairs` CTA pairs. The busiest pair takes
+// A first estimate of the tile height of a launch whose matmuls have M rows,
+// N[i] features and K[i] positions, run by `pairs` CTA pairs, counting units
+// as if split evenly (the host refines it with the actual pair plan). The busiest pair takes
 // ceil(units / pairs) work units (a 256-feature x tm-row tile over one K
 // chunk) and each unit moves 256 weight rows and tm activation rows of
 // operands through shared memory, the kernel's bound. The height with the
