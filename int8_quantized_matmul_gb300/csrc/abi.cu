@@ -64,8 +64,7 @@ struct ActSlot {
 };
 
 size_t act_slot_bytes(int64_t M, int64_t K) {
-    const int64_t Kp = round_up(K, 256);
-    size_t op = (size_t)M * (size_t)Kp * 2;                      // GEMM f16 rows
+    size_t op = 3 * (size_t)gemm_tc_rows_pad(M) * (size_t)(K / 2);   // GEMM: three digit planes
     if (M <= 16) {
         const size_t tc = (size_t)gemv_tc_op_rows(gemv_tc_mp(M)) * (size_t)(K / 2);   // GEMV tensor-core operand
         if (tc > op) op = tc;
@@ -248,7 +247,7 @@ static int group_acts(const i2s_problem* probs, int count, std::vector<int>& act
 }
 
 // Tensor-core GEMM path (M > 16): phase 1 quantizes every distinct activation
-// into the f16 operand layout, phase 2 runs one persistent GEMM launch over
+// into the e2m1 digit planes, phase 2 runs one persistent GEMM launch over
 // all problems. Arguments are validated by the callers.
 static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
                        i2s_stream_t stream, int phases) {
@@ -272,8 +271,8 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         qa.zero_16 = 0;
         qa.count = n_act;
         qa.M = (int)M;
-        qa.rows = (int)M;
-        qa.layout = kQuantF16Perm;
+        qa.rows = (int)gemm_tc_rows_pad(M);
+        qa.layout = kQuantE2M1Tc;
         for (int a = 0; a < n_act; ++a) {
             const i2s_problem& p = probs[first[a]];
             qa.j[a] = QuantJob{p.x, base + slots[a].op_off, reinterpret_cast<float*>(base + slots[a].scale_off),
@@ -284,15 +283,20 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     }
     if (phases & 2) {
         static thread_local TcArgs ta;
-        const int BN = M >= 256 ? 256 : (int)round_up(M, 32);
+        const int BN = gemm_tc_bn(M);
+        const int rows_pad = (int)gemm_tc_rows_pad(M);
         ta.n_maps = n_act;
         ta.count = count;
         ta.M = (int)M;
         ta.BN = BN;
+        ta.n_act_rows = rows_pad;
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        // the three digit planes of each activation; each CTA of a pair loads
+        // half of a tile's activation rows of a plane
         for (int a = 0; a < n_act; ++a)
-            if (!make_f16_operand_map(&ta.maps[a], base + slots[a].op_off, (int)M, (int)probs[first[a]].K, BN / 2))
-                return I2S_E_CUDA;   // each CTA of a pair loads half of a tile's activation rows
+            if (!make_u8_operand_map(&ta.maps[a], base + slots[a].op_off, 3 * rows_pad, (int)(probs[first[a]].K / 2),
+                                     BN / 2))
+                return I2S_E_CUDA;
         const int n_act_tiles = (int)((M + BN - 1) / BN);
         int tiles = 0;
         for (int i = 0; i < count; ++i) {

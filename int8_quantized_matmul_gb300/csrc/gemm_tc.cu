@@ -4,44 +4,55 @@
 // "ggml: additive INT8/ternary types ...", "Arithmetic is exact where it can
 // be").
 //
-// sm_103a has no integer tcgen05 MMA, so the exact int32 dot sum_k code*q is
-// formed with kind::f16 and f32 accumulation, exactly:
-//   * a code c in {0,1,2} placed in the low bits of an f16 is the subnormal
-//     c*2^-24, so a shift and a mask turn two packed codes into an f16 pair;
-//   * q in [-127,127] is an exact f16 integer (the quantizer writes it so);
-//   * every product and partial sum is an integer multiple of 2^-24 of
-//     magnitude <= 254*K*2^-24 < 1 for K <= 66052, which binary32 holds
-//     exactly, so dot = D * 2^24 exactly.
+// sm_103a has no integer tcgen05 MMA. The exact int32 dot sum_k code*q is
+// formed with tcgen05.mma kind::mxf4 (packed e2m1 operands, ue8m0 block
+// scales, f32 accumulation), exactly:
+//   * A: a code c in {0,1,2} read as an e2m1 nibble is c/2, so
+//     packed & 0x33333333 and (packed >> 2) & 0x33333333 turn a 32-bit word
+//     of packed codes into sixteen operands (as in the decode GEMV);
+//   * B: each quantized activation q is three balanced base-8 digits
+//     q = d0 + 8*d1 + 64*d2 (d0, d1 in [-4,3], d2 in [-2,2]), each exact in
+//     e2m1, stored as three digit planes (the GEMV's operand layout, one plane
+//     per digit). The MMAs of plane j use the block scale 2^(3j) (ue8m0 127,
+//     130, 133), so the three MMAs of a 64-position step, which share the A
+//     descriptor, add (c/2)*q into ONE accumulator;
+//   * every product is a multiple of 1/2 and every partial sum stays below
+//     2^23: the completed steps contribute at most 127 per position, and the
+//     step each of the two issue streams has in flight at most
+//     (4 + 8*4 + 64*2) * 64, so 127*65536 + 2*164*64 < 2^23 and binary32
+//     holds every partial sum exactly. dot = 2*D.
+// Each 256-position stage moves 16 KB of A (converted) and 3 * BN/2 * 128
+// bytes of B per CTA, half the bytes per multiply-add of f16 operands, and the
+// tensor time of a step is that of three fp4 MMAs.
 //
 // Roles (one CTA per SM, persistent over a static tile schedule):
 //   warps 0-3  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
 //              (w_scale * act_scale), coalesced F32 stores (warp w reads
 //              TMEM lanes 32w..32w+31 = weight rows of the tile);
 //   warps 4-11 converters: two threads per weight row of the 128-row tile,
-//              each loading 8 of the row's 16 packed bytes per K block (64
-//              positions) and expanding them to 32 f16 in the 128B-swizzled
-//              K-major layout, then fencing the writes into the async proxy;
-//   warp 12    TMA producer of the activation tile (f16, 128B swizzle);
+//              each loading the row's 32 packed bytes of one 128-position
+//              group per stage and writing its 64 bytes of e2m1 operands into
+//              the 128B-swizzled K-major layout, then fencing the writes into
+//              the async proxy;
+//   warp 12    TMA producer of the three digit planes of the activation tile;
 //   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM).
 // CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
-// cta_group::2 MMAs. A tile is 256 weight rows (the "swapped" A operand; 128
-// converted in each CTA's shared memory, 128 accumulator rows in each CTA's
-// TMEM) x up to 256 activation rows (the B operand; half of them TMA'd into
-// each CTA's shared memory). The leader (rank 0) issues M = 256 x N x K = 16
-// MMAs, 4 per K block; both CTAs' converters and TMA loads report to the
-// leader's stage barriers, its commits multicast to both CTAs, and each CTA's
-// epilogue releases the leader's accumulator barrier by a remote arrive. Two
-// TMEM accumulators of 256 columns let the epilogue of one tile overlap the
-// MMAs of the next. One thread needs well over 100 SM cycles to issue a
-// tcgen05.mma, so two warps issue, taking the K blocks of the stream in turn,
-// both into the tile's accumulator: every MMA accumulates, the epilogue zeroes
-// an accumulator after reading it, and since every partial sum is exact the
-// order in which the two streams land does not matter.
+// cta_group::2 MMAs. A tile is 256 weight rows (128 converted in each CTA's
+// shared memory, 128 accumulator rows in each CTA's TMEM) x BN <= 128
+// activation rows (half of each plane TMA'd into each CTA's shared memory).
+// The leader (rank 0) issues M = 256 x N = BN x K = 64 MMAs, 12 per stage;
+// both CTAs' converters and TMA loads report to the leader's stage barriers,
+// its commits multicast to both CTAs, and each CTA's epilogue releases the
+// leader's accumulator barrier by a remote arrive. Two TMEM accumulators of
+// 128 columns let the epilogue of one tile overlap the MMAs of the next; the
+// block scales live in TMEM beside them. Two warps issue, taking the stages in
+// turn, both into the tile's accumulator.
 //
-// K order: the converters emit a K block's 64 positions in the order in which
-// the packed bytes yield them (per 32-bit word: for each bit-pair slice, bytes
-// (0,2) then (1,3)); the quantizer writes the activation operand in the same
-// order (quant.cu, perm_index_of), and a dot product does not depend on the
+// K order: within a 128-position group, element 16w + 8t + 2i + h of the A
+// and B rows holds position 32s + 4w + i, where (t, h) = (0,0), (0,1), (1,0),
+// (1,1) for bit-pair slices s = 3, 1, 2, 0: the order in which the masks
+// yield the packed codes. The quantizer writes the digit planes in the same
+// order (quant.cu, kQuantE2M1Tc), and a dot product does not depend on the
 // order of its terms.
 //
 // Every wait is bounded: after ~1 s without progress the kernel records a
@@ -60,28 +71,31 @@ namespace i2s {
 namespace {
 
 constexpr int kEpiWarps = 4;
-constexpr int kCvtWarps = 8;               // two threads per weight row, 8 packed bytes each
+constexpr int kCvtWarps = 8;               // two threads per weight row, one 128-position group each
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;                // warps 13-14
 constexpr int kIssuersTc = 2;
 constexpr int kThreadsTc = 480;
-constexpr int kStagesTc = 6;
-constexpr int kCvtPrefetch = 8;             // K blocks of packed codes each converter keeps in flight
-constexpr int kBlockK = 64;                 // K positions per stage (one 128-byte f16 row)
-constexpr int kTileW = 128;                 // weight rows per tile (MMA M)
-constexpr int kATileBytes = kTileW * 128;   // 16 KB
-constexpr int kBTileBytesMax = 128 * 128;   // 16 KB: this CTA's half of up to 256 activation rows
+constexpr int kStagesTc = 4;
+constexpr int kCvtPrefetch = 4;             // stages of packed codes each converter keeps in flight
+constexpr int kBlockK = 256;                // K positions per stage (one 128-byte row of e2m1)
+constexpr int kTileW = 128;                 // weight rows per CTA (half of the pair's MMA M)
+constexpr int kATileBytes = kTileW * 128;   // 16 KB of e2m1
+constexpr int kBPlaneMax = 64 * 128;        // one digit plane of this CTA's half of up to 128 activation rows
+constexpr int kBStageMax = 3 * kBPlaneMax;  // 24 KB
 constexpr int kTmemCols = 512;
+constexpr uint32_t kAccCols = 128;          // two accumulators of BN <= 128 columns
+constexpr uint32_t kSfaCol = 256;           // block scales: A (all 1), then B for digits 0, 1, 2 (1, 8, 64)
+constexpr uint32_t kSfbCol0 = 272;
+constexpr uint32_t kSfCols = 16;
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
-// Issuer i takes the K blocks s with s % kIssuersTc == i; each stage slot must
-// always be served by the same issuer (a parity wait cannot tell the phase it
-// wants from the one two phases later).
 static_assert(kStagesTc % kIssuersTc == 0, "ring slots per issuer");
-static_assert(kCvtPrefetch % 2 == 0, "converters take K blocks in pairs");
+static_assert(kCvtPrefetch % 2 == 0, "converters take stages in pairs");
+static_assert(kSfbCol0 + 3 * kSfCols <= (uint32_t)kTmemCols, "TMEM budget");
 
 struct SmemTc {
-    float sc_col[2][256];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
-    float rs_col[2][256];   // epilogue: row_sum[m] per tile column (exact as a float), by accumulator
+    float sc_col[2][128];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
+    float rs_col[2][128];   // epilogue: row_sum[m] per tile column (exact as a float), by accumulator
     uint64_t full_a[kStagesTc];
     uint64_t full_b[kStagesTc];
     uint64_t empty[kStagesTc];
@@ -94,7 +108,7 @@ struct SmemTc {
     int abort;
 };
 
-constexpr size_t kSmemTcBytes = 1024 + (size_t)kStagesTc * (kATileBytes + kBTileBytesMax) + sizeof(SmemTc);
+constexpr size_t kSmemTcBytes = 1024 + (size_t)kStagesTc * (kATileBytes + kBStageMax) + sizeof(SmemTc);
 
 __device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
     int lo = 0, hi = a.count - 1;
@@ -105,14 +119,12 @@ __device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
     return lo;
 }
 
-// Expands one 32-bit word of packed codes into 8 f16 pairs (two 16-byte
-// chunks): for slices s = 6, 4, 2, 0: (byte0, byte2) then (byte1, byte3).
-__device__ __forceinline__ void expand_word_f16(uint32_t w, uint4& c0, uint4& c1) {
-    constexpr uint32_t m = 0x00030003u;
-    c0.x = (w >> 6) & m;  c0.y = (w >> 14) & m;
-    c0.z = (w >> 4) & m;  c0.w = (w >> 12) & m;
-    c1.x = (w >> 2) & m;  c1.y = (w >> 10) & m;
-    c1.z = w & m;         c1.w = (w >> 8) & m;
+// Two 32-bit words of packed codes -> one 16-byte chunk of e2m1 operands:
+// for each word, the codes at shifts 0 and 4 (slices 3 and 1), then those at
+// shifts 2 and 6 (slices 2 and 0), one nibble each (c/2 in e2m1).
+__device__ __forceinline__ uint4 expand_words_e2m1(uint32_t w0, uint32_t w1) {
+    constexpr uint32_t m = 0x33333333u;
+    return make_uint4(w0 & m, (w0 >> 2) & m, w1 & m, (w1 >> 2) & m);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_constant__ TcArgs a) {
@@ -120,13 +132,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + (size_t)kStagesTc * kATileBytes;
-    SmemTc& S = *reinterpret_cast<SmemTc*>(sB + (size_t)kStagesTc * kBTileBytesMax);
+    SmemTc& S = *reinterpret_cast<SmemTc*>(sB + (size_t)kStagesTc * kBStageMax);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int BN = a.BN;
-    const int BH = BN / 2;                                  // activation rows of a tile in each CTA
-    const uint32_t b_half_bytes = (uint32_t)BH * 128u;
+    const int BN = a.BN;                                    // activation rows per tile (<= 128)
+    const int BH = BN / 2;                                  // of them in each CTA
+    const uint32_t plane_bytes = (uint32_t)BH * 128u;       // one digit plane of this CTA's half
+    const int rows_pad = a.n_act_rows;                      // rows of one digit plane of the operand
     const uint32_t rank = tc::cluster_rank();               // 0: the leader, which issues the MMAs
     const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
@@ -159,13 +172,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
     const uint32_t tmem_base = S.tmem_base;
     volatile int* abort_flag = &S.abort;
     if (warp < kEpiWarps) {
-        // both accumulators start at zero (every MMA accumulates)
-        for (uint32_t col = 0; col < (uint32_t)kTmemCols; col += 32)
-            tc::tmem_st_zero_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16) + col);
+        // both accumulators start at zero (every MMA accumulates); the block
+        // scales: 1.0 for A, 2^(3j) for digit plane j, in every lane and byte
+        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        for (uint32_t col = 0; col < 2 * kAccCols; col += 32) tc::tmem_st_zero_32x32b_x32(lane_base + col);
+        uint32_t sf[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sf[i] = 0x7F7F7F7Fu;
+        tc::tmem_st_32x32b_x16(lane_base + kSfaCol, sf);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const uint32_t e = 127u + 3u * (uint32_t)j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sf[i] = e * 0x01010101u;
+            tc::tmem_st_32x32b_x16(lane_base + kSfbCol0 + kSfCols * (uint32_t)j, sf);
+        }
         tc::tmem_st_wait();
     }
-    // both CTAs' barriers initialised and accumulators zeroed before any
-    // remote arrive, multicast commit or MMA
+    // both CTAs' barriers initialised, accumulators zeroed and scales written
+    // before any remote arrive, multicast commit or MMA
     tc::tc_fence_before();
     tc::cluster_sync();
     tc::tc_fence_after();
@@ -177,6 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
+        // per stage: this CTA's half of the tile's rows in each digit plane
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -186,13 +212,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
                 const TcProb& P = a.p[find_problem(a, tile)];
                 const int at = (tile - P.tile0) % P.n_act_tiles;
-                const int KB = P.K / kBlockK;
+                const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
+                const int row = at * BN + (int)rank * BH;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit)) { fail(1); ok = false; break; }
-                    // the leader expects both CTAs' halves; a peer's bytes may land first
-                    if (rank == 0) tc::mbar_arrive_expect_tx(&S.full_b[stage], 2 * b_half_bytes);
-                    tc::pair_tma_load_2d(sB + (size_t)stage * kBTileBytesMax, &a.maps[P.map], kb * kBlockK,
-                                         at * BN + (int)rank * BH, tc::smem_in_rank(&S.full_b[stage], 0));
+                    // the leader expects both CTAs' planes; a peer's bytes may land first
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&S.full_b[stage], 6 * plane_bytes);
+                    uint8_t* dst = sB + (size_t)stage * kBStageMax;
+                    const uint32_t bar = tc::smem_in_rank(&S.full_b[stage], 0);
+#pragma unroll
+                    for (int j = 0; j < 3; ++j)
+                        tc::pair_tma_load_2d(dst + (size_t)j * plane_bytes, &a.maps[P.map], kb * (kBlockK / 2),
+                                             j * rows_pad + row, bar);
                     pending[stage] = true;
                     pending_phase[stage] = phase;
                     if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
@@ -207,10 +238,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
         // ---------------------------------------------------------- converters
-        // two threads per weight row: thread half hf expands the row's packed
-        // bytes 8hf..8hf+7 of each K block (32 positions) into 4 f16 chunks
+        // two threads per weight row: thread half hf turns the row's packed
+        // bytes of 128-position group hf of each stage (32 bytes) into the 64
+        // bytes of e2m1 operands at byte offset 64*hf of the stage row
         const int ct = tid - kEpiWarps * 32;
-        const int r = ct & (kTileW - 1);   // weight row within the tile
+        const int r = ct & (kTileW - 1);   // weight row within the CTA's half of the tile
         const int hf = ct >> 7;
         int stage = 0;
         uint32_t phase = 0;
@@ -219,20 +251,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             const TcProb& P = a.p[find_problem(a, tile)];
             const int wt = (tile - P.tile0) / P.n_act_tiles;
             const int n = wt * (2 * kTileW) + (int)rank * kTileW + r;   // this CTA's half of the 256 rows
-            const int KB = P.K / kBlockK;
+            const int groups = P.K / 128;
+            const int KB = (groups + 1) / 2;
             const bool valid = n < P.N;
-            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4) + 8 * hf;
-            auto load = [&](int kb) {
-                return (valid && kb < KB) ? __ldg(reinterpret_cast<const uint2*>(src + (size_t)kb * 16))
-                                          : make_uint2(0u, 0u);
+            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4) + 32 * hf;
+            auto load = [&](int kb, uint4& lo, uint4& hi) {
+                if (valid && kb < KB && 2 * kb + hf < groups) {
+                    const uint4* p = reinterpret_cast<const uint4*>(src + (size_t)kb * 64);
+                    lo = __ldg(p);
+                    hi = __ldg(p + 1);
+                } else {
+                    lo = make_uint4(0u, 0u, 0u, 0u);
+                    hi = lo;
+                }
             };
-            // the row's packed bytes, kCvtPrefetch K blocks ahead
-            uint2 buf[kCvtPrefetch];
+            // the row's packed bytes, kCvtPrefetch stages ahead
+            uint4 blo[kCvtPrefetch], bhi[kCvtPrefetch];
 #pragma unroll
-            for (int j = 0; j < kCvtPrefetch; ++j) buf[j] = load(j);
+            for (int j = 0; j < kCvtPrefetch; ++j) load(j, blo[j], bhi[j]);
             for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
-                // two K blocks (stage slots) per pass: one proxy fence and one
-                // warp sync for both halve the per-stage latency of the loop
+                // two stages per pass: one proxy fence and one warp sync for both
 #pragma unroll
                 for (int j = 0; j < kCvtPrefetch; j += 2) {
                     const int kb = kb0 + j;
@@ -248,16 +286,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                     for (int h = 0; h < 2; ++h) {
                         if (h == 1 && !two) break;
                         uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
-                        const uint32_t words[2] = {buf[j + h].x, buf[j + h].y};
-                        buf[j + h] = load(kb + h + kCvtPrefetch);
-#pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            const int word = 2 * hf + w;   // 32-bit word of the row's 16 bytes
-                            uint4 c0, c1;
-                            expand_word_f16(words[w], c0, c1);
-                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word)) = c0;
-                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * word + 1)) = c1;
-                        }
+                        const uint4 lo = blo[j + h], hi = bhi[j + h];
+                        load(kb + h + kCvtPrefetch, blo[j + h], bhi[j + h]);
+                        // words 0..7 of the group: chunk 4*hf + p holds words 2p and 2p + 1
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 0)) = expand_words_e2m1(lo.x, lo.y);
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 1)) = expand_words_e2m1(lo.z, lo.w);
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 2)) = expand_words_e2m1(hi.x, hi.y);
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 3)) = expand_words_e2m1(hi.z, hi.w);
                     }
                     tc::fence_proxy_async_smem();
                     __syncwarp();
@@ -280,10 +315,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc && rank == 0) {
         // ---------------------------------------------------------- MMA issue
-        // issuer `me` takes the K blocks whose position in this CTA's stream
-        // is me modulo kIssuersTc; the ring index advances over all of them
+        // issuer `me` takes the stages whose position in this CTA's stream is
+        // me modulo kIssuersTc; the ring index advances over all of them. Per
+        // 64-position step the three digit MMAs are issued back to back (the
+        // exactness bound above relies on it).
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16_f32(2 * kTileW, BN);   // 256 x BN over the pair
+            const uint32_t idesc = tc::idesc_mxf4_f32(2 * kTileW, BN);   // 256 x BN over the pair
+            const uint32_t sfa = tmem_base + kSfaCol;
             const int me = warp - kMmaWarp;
             int stage = 0;
             uint32_t phase = 0;
@@ -293,20 +331,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             bool ok = true;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
                 const TcProb& P = a.p[find_problem(a, tile)];
-                const int KB = P.K / kBlockK;
+                const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
                 if (!tc::mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimit)) { fail(4); break; }
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+                const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
                 for (int kb = 0; kb < KB; ++kb, ++seq) {
                     if (seq % kIssuersTc == me) {
                         if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit) ||
                             !tc::mbar_wait(&S.full_b[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
                         tc::tc_fence_after();
                         const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kATileBytes));
-                        const uint64_t bd = tc::sdesc_sw128_kmajor(tc::smem_u32(sB + (size_t)stage * kBTileBytesMax));
+                        const uint32_t b0 = tc::smem_u32(sB + (size_t)stage * kBStageMax);
+                        const uint64_t bd0 = tc::sdesc_sw128_kmajor(b0);
+                        const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + plane_bytes);
+                        const uint64_t bd2 = tc::sdesc_sw128_kmajor(b0 + 2 * plane_bytes);
+                        // a stage past K/128 groups holds zero codes in its second half
+                        const int steps = (kb * kBlockK + kBlockK <= P.K) ? 4 : 2;
 #pragma unroll
-                        for (int k = 0; k < kBlockK / 16; ++k)   // +32 bytes per 16-element K step
-                            tc::pair_umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
+                        for (int k = 0; k < 4; ++k) {   // +32 bytes (64 e2m1) per step
+                            if (k >= steps) break;
+                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd0 + 2 * k, idesc, sfa, tmem_base + kSfbCol0, 1u);
+                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd1 + 2 * k, idesc, sfa,
+                                               tmem_base + kSfbCol0 + kSfCols, 1u);
+                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd2 + 2 * k, idesc, sfa,
+                                               tmem_base + kSfbCol0 + 2 * kSfCols, 1u);
+                        }
                         tc::pair_commit(&S.empty[stage], 0x3);   // both CTAs' stage slots are free
                     }
                     if (++stage == kStagesTc) { stage = 0; phase ^= 1; }
@@ -330,7 +379,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-                const int KB = a.p[find_problem(a, tile)].K / kBlockK;
+                const TcProb& P = a.p[find_problem(a, tile)];
+                const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
                     tc::dsmem_copy_signal(tc::smem_in_rank(S.signal, 0), S.signal, 16,
@@ -381,13 +431,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             // TMEM -> registers 32 columns at a time, the load of the next slice
             // overlapping the stores of this one; the accumulator is released as
             // soon as its last slice is in registers
-            const uint32_t d_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * 256);
+            const uint32_t d_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)acc * kAccCols;
             const int C = (BN + 31) / 32;
             auto store_slice = [&](int c, uint32_t (&v)[32]) {
                 if (n >= N) return;
                 // 16 outputs at a time, computed in place with no per-element
                 // branch so that the conversions overlap, then stored (static
-                // indices keep v[] in registers; jj < C * 32 <= 256 stays
+                // indices keep v[] in registers; jj < C * 32 <= 128 stays
                 // inside the per-column tables)
                 const int rows = min(BN - c * 32, M - (m_base + c * 32));
                 float* yp = y_col + (size_t)(m_base + c * 32) * N;
@@ -396,10 +446,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
 #pragma unroll
                     for (int j = 16 * hh; j < 16 * hh + 16; ++j) {
                         const int jj = c * 32 + j;
-                        // D * 2^24 is the integer dot, exact; so is dot - row_sum
+                        // 2 * D is the integer dot, exact; so is dot - row_sum
                         // (|.| < 2^24): the float of (dot - row_sum) without any
                         // conversion instruction
-                        const float dr = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.0f), rs_col[jj]);
+                        const float dr = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 2.0f), rs_col[jj]);
                         v[j] = __float_as_uint(__fmul_rn(dr, sc_col[jj]));
                     }
                     if (rows >= 32) {
@@ -486,7 +536,7 @@ bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, i
     std::memset(map, 0, sizeof(*map));
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};   // 64 f16 = one 128-byte swizzle row
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -17,8 +17,7 @@ constexpr int kMaxGroup = 256;   // same value as I2S_MAX_GROUP
 // ---------------------------------------------------------------------------
 enum QuantLayout : int {
     kQuantI8Rows = 0,    // plain int8, row-major M x K (the public sidecar)
-    kQuantF16Perm = 2,   // tensor-core GEMM operand: f16, K permuted per 128-group
-    kQuantE2M1Tc = 3,    // tensor-core GEMV operand: e2m1 digit rows (gemv_tc.cu), gemv_tc_op_rows(M') x K/2 bytes
+    kQuantE2M1Tc = 3,    // tensor-core GEMV and GEMM operand: e2m1 digit rows, digit j of row m at row j*rows + m, K/2 bytes each
 };
 
 struct QuantJob {
@@ -85,8 +84,9 @@ struct TcArgs {
     int n_maps;
     int count;
     int M;
-    int BN;                   // GEMM: activation rows per tile (MMA N, multiple of 32, <= 256);
+    int BN;                   // GEMM: activation rows per tile (MMA N, multiple of 32, <= 128);
                               // GEMV: M' (8 or 16), MMA N = gemv_tc_op_rows(M')
+    int n_act_rows;           // GEMM: rows of one digit plane of the activation operands (M rounded up to BN)
 
     int total_tiles;          // GEMM: tiles; GEMV: work units
     int share_first;          // GEMV: relative unit shares of the first and second half of the
@@ -99,6 +99,11 @@ constexpr int kGemvChunkPositions = 1536;   // K positions per GEMV work unit
 // GEMV grid is full (two CTAs per SM): the first is issued ahead of the second,
 // and this split was measured to let both finish together.
 constexpr int kGemvShareFirst = 23, kGemvShareSecond = 17;
+
+// Tensor-core GEMM (M > 16): activation rows per tile and the rows of one digit
+// plane of its operand.
+__host__ __device__ constexpr int gemm_tc_bn(int64_t M) { return M >= 128 ? 128 : (int)((M + 31) / 32 * 32); }
+__host__ __device__ constexpr int64_t gemm_tc_rows_pad(int64_t M) { return (M + gemm_tc_bn(M) - 1) / gemm_tc_bn(M) * gemm_tc_bn(M); }
 
 // Tensor-core GEMV activation operand: M' = 8 (M <= 8) or 16 activation rows,
 // each split into three base-8 digit rows (digit j of row m at row j*M' + m),

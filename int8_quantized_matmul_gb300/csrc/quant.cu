@@ -5,13 +5,10 @@
 //
 // One CTA per row: the row is read once into registers, a block reduction
 // finds its absmax, and the quantized values and their int8 sum (reduced the
-// same way) are written out. Besides the plain int8 layout of the public sidecar, the kernel can
-// write the operand layouts of the two matmul kernels directly, so no separate
-// repacking pass is needed:
-//   kQuantF16Perm   the tensor-core GEMM's activation operand: q as f16 in the
-//                   K order in which the GEMM expands the packed codes;
-//   kQuantE2M1Tc    the tensor-core GEMV's operand: each q as three base-8
-//                   digits in e2m1, one operand row per digit (k_quant_rows_tc4).
+// same way) are written out: as plain int8 rows (the public sidecar,
+// k_quant_rows), or straight into the operand layout of the two tensor-core
+// matmuls, so no separate repacking pass is needed (kQuantE2M1Tc: each q as
+// three base-8 digits in e2m1, one operand row per digit, k_quant_rows_tc4).
 
 #include "common.cuh"
 #include "internal.h"
@@ -19,35 +16,12 @@
 
 namespace i2s {
 
-// K position of the f16 element at index e of a 128-group in the tensor-core
-// operand order. The GEMM expands one 32-bit word of packed codes (bytes
-// gp..gp+3 of a group, gp = 4w) into 8 f16 pairs: for each bit-pair slice s
-// (shift 6, 4, 2, 0) the pair (byte 0, byte 2) then (byte 1, byte 3). So
-// index e = 16w + 4s + j holds byte offset {0, 2, 1, 3}[j] of that slice.
-__device__ __forceinline__ int perm_index_of(int pos) {   // pos: group-relative 0..127
-    const int s = pos >> 5;
-    const int gp = pos & 31;
-    const int w = gp >> 2;
-    const int c = gp & 3;
-    const int j = (c == 0) ? 0 : (c == 2) ? 1 : (c == 1) ? 2 : 3;
-    return 16 * w + 4 * s + j;
-}
-
-// Writes the four quantized values of positions 4c..4c+3 of row m in the
-// requested operand layout.
-__device__ __forceinline__ void emit4(const QuantArgs& a, const QuantJob& J, int m, int c, const int (&q)[4]) {
-    const int K = J.K;
-    if (a.layout == kQuantI8Rows) {
-        uint32_t* q4 = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(J.out) + (size_t)m * K);
-        q4[c] = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
-                ((uint32_t)(q[3] & 0xff) << 24);
-    } else {   // kQuantF16Perm
-        __half* out = static_cast<__half*>(J.out) + (size_t)m * K;
-        const int pos0 = 4 * c;
-        const int group_base = pos0 & ~127;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) out[group_base + perm_index_of((pos0 + e) & 127)] = __int2half_rn(q[e]);
-    }
+// Writes the four quantized values of positions 4c..4c+3 of row m as plain
+// int8 (the public sidecar layout).
+__device__ __forceinline__ void emit4(const QuantJob& J, int m, int c, const int (&q)[4]) {
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(static_cast<int8_t*>(J.out) + (size_t)m * J.K);
+    q4[c] = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
+            ((uint32_t)(q[3] & 0xff) << 24);
 }
 
 constexpr int kQThreads = 256;
@@ -99,14 +73,14 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
             const int q[4] = {quantize_one(cache[i].x, inv), quantize_one(cache[i].y, inv),
                               quantize_one(cache[i].z, inv), quantize_one(cache[i].w, inv)};
             sum += q[0] + q[1] + q[2] + q[3];
-            emit4(a, J, m, c, q);
+            emit4(J, m, c, q);
         }
     }
     for (int c = tid + kQCache * kQThreads; c < K4; c += kQThreads) {
         const float4 v = x4[c];
         const int q[4] = {quantize_one(v.x, inv), quantize_one(v.y, inv), quantize_one(v.z, inv), quantize_one(v.w, inv)};
         sum += q[0] + q[1] + q[2] + q[3];
-        emit4(a, J, m, c, q);
+        emit4(J, m, c, q);
     }
     sum = warp_sum(sum);
     if (lane == 0) s_sum[warp] = sum;

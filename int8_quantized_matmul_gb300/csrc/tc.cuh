@@ -199,6 +199,20 @@ __device__ __forceinline__ void pair_umma_f16(uint32_t d_tmem, uint64_t a_desc, 
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Leader only: D (+)= A * B^T over the pair, kind::mxf4 with block scaling,
+// both operands in shared memory (packed e2m1, two per byte, K = 64 per
+// instruction), ue8m0 scale factors (one per 32 K elements) read from TMEM.
+__device__ __forceinline__ void pair_umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
 // Leader only: arrive on the barrier at this offset in every CTA of `mask` once
 // the leader's earlier tcgen05 operations are done.
 __device__ __forceinline__ void pair_commit(uint64_t* bar, uint16_t mask) {

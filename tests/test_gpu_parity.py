@@ -380,6 +380,27 @@ def test_i2s_gemm_headroom_k8960_m64(i2s, o):
     assert (y.view(np.uint32) == small[0, 0].view(np.uint32)).all()
 
 
+@pytest.mark.parametrize("M", [20, 300])
+def test_i2s_gemm_headroom_k65536(i2s, o, M):
+    # the largest K the library takes, every code 2, every q = 127: the
+    # accumulator reaches sum (c/2) q = 127 K = 8,323,072, just below 2^23,
+    # where binary32 still resolves the halves the digit MMAs add
+    K, N = 65536, 256
+    packed = o.i2s_pack(np.full((N, K), 2, np.uint8), 0.05)
+    x = np.ones((M, K), np.float32)
+    y = host(i2s.i2s_mul_mat(dev(packed), N, K, dev(x), path=2))
+    small = o.i2s_mul_mat(o.i2s_pack(np.full((4, K), 2, np.uint8), 0.05), 4, K, x[:2])
+    assert (small == small[0, 0]).all()
+    assert (y.view(np.uint32) == small[0, 0].view(np.uint32)).all()
+
+
+def test_i2s_gemm_large_k_random(i2s, o):
+    # K = 40960 with random codes and 1% outliers, ragged N and M
+    K, N, M = 40960, 300, 37
+    got, want = run_i2s(i2s, o, N, K, M, seed=123)
+    same_bits(got, want)
+
+
 def test_i2s_gemm_degenerate(i2s, o):
     K, N, M = 1024, 70, 40
     x = synth.normal_f32((M, K), seed=13)
