@@ -26,14 +26,14 @@
 // tensor time of a step is that of three fp4 MMAs.
 //
 // Roles (one CTA per SM, persistent over a static tile schedule):
-//   warps 0-3  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
+//   warps 0-7  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
 //              (w_scale * act_scale), coalesced F32 stores (warp w reads
-//              TMEM lanes 32w..32w+31 = weight rows of the tile);
-//   warps 4-11 converters: two threads per weight row of the 128-row tile,
-//              each loading the row's 32 packed bytes of one 128-position
-//              group per stage and writing its 64 bytes of e2m1 operands into
-//              the 128B-swizzled K-major layout, then fencing the writes into
-//              the async proxy;
+//              TMEM lanes 32(w%4)..+31 = weight rows of the tile, columns
+//              (w/4)*BN/2..+BN/2-1 = activation rows);
+//   warps 8-11 converters: one thread per weight row of the 128-row tile,
+//              loading the row's 64 packed bytes per stage and writing its
+//              128 bytes of e2m1 operands into the 128B-swizzled K-major
+//              layout, then fencing the writes into the async proxy;
 //   warp 12    TMA producer of the three digit planes of the activation tile;
 //   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM).
 // CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
@@ -70,14 +70,14 @@ namespace i2s {
 
 namespace {
 
-constexpr int kEpiWarps = 4;
-constexpr int kCvtWarps = 8;               // two threads per weight row, one 128-position group each
+constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, each half of the columns
+constexpr int kCvtWarps = 4;               // one thread per weight row
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;                // warps 13-14
 constexpr int kIssuersTc = 2;
 constexpr int kThreadsTc = 480;
 constexpr int kStagesTc = 4;
-constexpr int kCvtPrefetch = 4;             // stages of packed codes each converter keeps in flight
+constexpr int kCvtPrefetch = 2;             // stages of packed codes each converter keeps in flight
 constexpr int kBlockK = 256;                // K positions per stage (one 128-byte row of e2m1)
 constexpr int kTileW = 128;                 // weight rows per CTA (half of the pair's MMA M)
 constexpr int kATileBytes = kTileW * 128;   // 16 KB of e2m1
@@ -171,10 +171,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
     tc::tc_fence_after();
     const uint32_t tmem_base = S.tmem_base;
     volatile int* abort_flag = &S.abort;
-    if (warp < kEpiWarps) {
+    if (warp < 4) {
         // both accumulators start at zero (every MMA accumulates); the block
         // scales: 1.0 for A, 2^(3j) for digit plane j, in every lane and byte
-        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        // (warps 0-3 cover the four lane quarters)
+        const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
         for (uint32_t col = 0; col < 2 * kAccCols; col += 32) tc::tmem_st_zero_32x32b_x32(lane_base + col);
         uint32_t sf[16];
 #pragma unroll
@@ -238,12 +239,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
         // ---------------------------------------------------------- converters
-        // two threads per weight row: thread half hf turns the row's packed
-        // bytes of 128-position group hf of each stage (32 bytes) into the 64
-        // bytes of e2m1 operands at byte offset 64*hf of the stage row
-        const int ct = tid - kEpiWarps * 32;
-        const int r = ct & (kTileW - 1);   // weight row within the CTA's half of the tile
-        const int hf = ct >> 7;
+        // one thread per weight row: per stage the row's 64 packed bytes (two
+        // 128-position groups) become the 128 bytes of e2m1 operands of the
+        // stage row
+        const int r = tid - kEpiWarps * 32;   // weight row within the CTA's half of the tile
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -254,21 +253,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             const int groups = P.K / 128;
             const int KB = (groups + 1) / 2;
             const bool valid = n < P.N;
-            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4) + 32 * hf;
-            auto load = [&](int kb, uint4& lo, uint4& hi) {
-                if (valid && kb < KB && 2 * kb + hf < groups) {
-                    const uint4* p = reinterpret_cast<const uint4*>(src + (size_t)kb * 64);
-                    lo = __ldg(p);
-                    hi = __ldg(p + 1);
-                } else {
-                    lo = make_uint4(0u, 0u, 0u, 0u);
-                    hi = lo;
+            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4);
+            auto load = [&](int kb, uint4 (&v)[4]) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    if (valid && kb < KB && 2 * kb + g < groups) {
+                        const uint4* p = reinterpret_cast<const uint4*>(src + (size_t)kb * 64 + 32 * g);
+                        v[2 * g] = __ldg(p);
+                        v[2 * g + 1] = __ldg(p + 1);
+                    } else {
+                        v[2 * g] = make_uint4(0u, 0u, 0u, 0u);
+                        v[2 * g + 1] = v[2 * g];
+                    }
                 }
             };
             // the row's packed bytes, kCvtPrefetch stages ahead
-            uint4 blo[kCvtPrefetch], bhi[kCvtPrefetch];
+            uint4 buf[kCvtPrefetch][4];
 #pragma unroll
-            for (int j = 0; j < kCvtPrefetch; ++j) load(j, blo[j], bhi[j]);
+            for (int j = 0; j < kCvtPrefetch; ++j) load(j, buf[j]);
             for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
                 // two stages per pass: one proxy fence and one warp sync for both
 #pragma unroll
@@ -286,13 +288,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                     for (int h = 0; h < 2; ++h) {
                         if (h == 1 && !two) break;
                         uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
-                        const uint4 lo = blo[j + h], hi = bhi[j + h];
-                        load(kb + h + kCvtPrefetch, blo[j + h], bhi[j + h]);
-                        // words 0..7 of the group: chunk 4*hf + p holds words 2p and 2p + 1
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 0)) = expand_words_e2m1(lo.x, lo.y);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 1)) = expand_words_e2m1(lo.z, lo.w);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 2)) = expand_words_e2m1(hi.x, hi.y);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 4 * hf + 3)) = expand_words_e2m1(hi.z, hi.w);
+                        uint4 v[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] = buf[j + h][i];
+                        load(kb + h + kCvtPrefetch, buf[j + h]);
+                        // group g, words 2p and 2p + 1 -> chunk 4g + p of the 128-byte row
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i)) = expand_words_e2m1(v[i].x, v[i].y);
+                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i + 1)) = expand_words_e2m1(v[i].z, v[i].w);
+                        }
                     }
                     tc::fence_proxy_async_smem();
                     __syncwarp();
@@ -391,7 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        const int r = warp * 32 + lane;   // TMEM lane = weight row within the tile
+        const int q = warp & 3;                // TMEM lane quarter
+        const int r = q * 32 + lane;           // TMEM lane = weight row within the tile
+        const int half = warp >> 2;            // which half of the accumulator's columns
         int acc = 0;
         uint32_t acc_phase = 0, stage_phase = 0;
         for (int tile = pair; tile < a.total_tiles; tile += n_pairs) {
@@ -406,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
                 float* sc_col = S.sc_col[acc];
                 float* rs_col = S.rs_col[acc];
-                for (int j = r; j < BN; j += kEpiWarps * 32) {
+                for (int j = tid; j < BN; j += kEpiWarps * 32) {
                     const int m = m_base + j;
                     sc_col[j] = m < a.M ? __fmul_rn(w_scale, P.act_scale[m]) : 0.0f;
                     rs_col[j] = m < a.M ? (float)P.row_sum[m] : 0.0f;   // |row_sum| <= 127 K < 2^24
@@ -428,64 +435,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             const float* rs_col = S.rs_col[acc];
             const int N = P.N, M = a.M;
             float* y_col = P.y + n;   // this thread's output column
-            // TMEM -> registers 32 columns at a time, the load of the next slice
-            // overlapping the stores of this one; the accumulator is released as
-            // soon as its last slice is in registers
-            const uint32_t d_addr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)acc * kAccCols;
-            const int C = (BN + 31) / 32;
-            auto store_slice = [&](int c, uint32_t (&v)[32]) {
+            // this warp's BN/2 columns, 16 at a time: the load of the next
+            // slice overlaps the stores of this one; the accumulator is released
+            // as soon as its last slice is in registers
+            const int c_base = half * (BN / 2);
+            const uint32_t d_addr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols + (uint32_t)c_base;
+            const int H = BN / 32;   // 16-column slices per warp
+            auto store_slice = [&](int h, const uint32_t (&v)[16]) {
                 if (n >= N) return;
-                // 16 outputs at a time, computed in place with no per-element
-                // branch so that the conversions overlap, then stored (static
-                // indices keep v[] in registers; jj < C * 32 <= 128 stays
-                // inside the per-column tables)
-                const int rows = min(BN - c * 32, M - (m_base + c * 32));
-                float* yp = y_col + (size_t)(m_base + c * 32) * N;
+                const int m0 = c_base + 16 * h;   // first tile column of the slice
+                const int rows = min(16, M - (m_base + m0));
+                float* yp = y_col + (size_t)(m_base + m0) * N;
+                float o[16];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                for (int j = 0; j < 16; ++j) {
+                    // 2 * D is the integer dot, exact; so is dot - row_sum
+                    // (|.| < 2^24): the float of (dot - row_sum) without any
+                    // conversion instruction
+                    const float dr = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 2.0f), rs_col[m0 + j]);
+                    o[j] = __fmul_rn(dr, sc_col[m0 + j]);
+                }
+                if (rows >= 16) {
 #pragma unroll
-                    for (int j = 16 * hh; j < 16 * hh + 16; ++j) {
-                        const int jj = c * 32 + j;
-                        // 2 * D is the integer dot, exact; so is dot - row_sum
-                        // (|.| < 2^24): the float of (dot - row_sum) without any
-                        // conversion instruction
-                        const float dr = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 2.0f), rs_col[jj]);
-                        v[j] = __float_as_uint(__fmul_rn(dr, sc_col[jj]));
-                    }
-                    if (rows >= 32) {
+                    for (int j = 0; j < 16; ++j) yp[(size_t)j * N] = o[j];
+                } else {
 #pragma unroll
-                        for (int j = 16 * hh; j < 16 * hh + 16; ++j) yp[(size_t)j * N] = __uint_as_float(v[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 16 * hh; j < 16 * hh + 16; ++j)
-                            if (j < rows) yp[(size_t)j * N] = __uint_as_float(v[j]);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        if (j < rows) yp[(size_t)j * N] = o[j];
                 }
             };
             auto release = [&]() {
-                // every slice is in registers: zero the accumulator for the
-                // tile after next, then hand it back
-                for (int c2 = 0; c2 < C; ++c2) tc::tmem_st_zero_32x32b_x32(d_addr + 32u * c2);
+                // every slice is in registers: zero this warp's columns of the
+                // accumulator for the tile after next, then hand them back
+                for (int h2 = 0; h2 < H; ++h2) tc::tmem_st_zero_32x32b_x16(d_addr + 16u * h2);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive_cluster(tc::smem_in_rank(&S.tmem_empty[acc], 0));   // the leader's barrier
             };
-            uint32_t va[32], vb[32];
-            tc::tmem_ld_32x32b_x32(d_addr, va);
+            uint32_t va[16], vb[16];
+            tc::tmem_ld_32x32b_x16(d_addr, va);
             tc::tmem_ld_wait();
-            if (C == 1) release();
-            for (int c = 0; c < C; c += 2) {
-                if (c + 1 < C) tc::tmem_ld_32x32b_x32(d_addr + 32u * (c + 1), vb);
-                store_slice(c, va);
-                if (c + 1 < C) {
+            if (H == 1) release();
+            for (int h = 0; h < H; h += 2) {
+                if (h + 1 < H) tc::tmem_ld_32x32b_x16(d_addr + 16u * (h + 1), vb);
+                store_slice(h, va);
+                if (h + 1 < H) {
                     tc::tmem_ld_wait();
-                    if (c + 2 == C) release();
-                    if (c + 2 < C) tc::tmem_ld_32x32b_x32(d_addr + 32u * (c + 2), va);
-                    store_slice(c + 1, vb);
-                    if (c + 2 < C) {
+                    if (h + 2 == H) release();
+                    if (h + 2 < H) tc::tmem_ld_32x32b_x16(d_addr + 16u * (h + 2), va);
+                    store_slice(h + 1, vb);
+                    if (h + 2 < H) {
                         tc::tmem_ld_wait();
-                        if (c + 3 == C) release();
+                        if (h + 3 == H) release();
                     }
                 }
             }
