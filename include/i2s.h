@@ -162,6 +162,12 @@ typedef struct i2s_config {
     int grid_ctas;   /* persistent CTA count: GEMV at most 2 per SM; GEMM runs CTA pairs
                         (rounded down to an even count, at least 2, at most the pairs that
                         fit at once) */
+    int64_t test_stall_cycles;   /* tests only, GEMV path: > 0 makes the GEMV's epilogue
+                        wait this many SM cycles on a barrier nothing signals, then give
+                        up, so that the launch leaves through its device-timeout path
+                        (copies and MMAs in flight drained, TMEM freed) and
+                        i2s_read_status reports I2S_E_DEVICE_TIMEOUT. The output is then
+                        incomplete. 0 for normal use; negative is BAD_ARG. */
 } i2s_config;
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,

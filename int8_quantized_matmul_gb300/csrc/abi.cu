@@ -107,7 +107,7 @@ extern "C" {
 static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
                        i2s_stream_t stream, int phases);
 static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
-                       i2s_stream_t stream, int phases);
+                       i2s_stream_t stream, int phases, long long test_stall_cycles = 0);
 
 const char* i2s_status_string(int status) {
     switch (status) {
@@ -223,7 +223,9 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     if (path == 3 && M > 16) return I2S_E_BAD_ARG;
     i2s_problem p{w_i2s, N, K, x, y};
     if (path == 2 || (path == 0 && M > 16)) return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
-    return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
+    if (config && config->test_stall_cycles < 0) return I2S_E_BAD_ARG;
+    return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3,
+                       config ? (long long)config->test_stall_cycles : 0);
 }
 
 int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y, void* ws,
@@ -290,6 +292,7 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         ta.M = (int)M;
         ta.BN = BN;
         ta.n_act_rows = rows_pad;
+        ta.test_stall_cycles = 0;
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         // the three digit planes of each activation; each CTA of a pair loads
         // half of a tile's activation rows of a plane
@@ -332,7 +335,7 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
 // problems (two CTAs per SM). Arguments are validated by the callers.
 
 static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws, int grid_ctas,
-                       i2s_stream_t stream, int phases) {
+                       i2s_stream_t stream, int phases, long long test_stall_cycles) {
     std::vector<int> act_of, first;
     const int n_act = group_acts(probs, count, act_of, first);
     if (n_act > kTcMaxMaps) return I2S_E_BAD_ARG;
@@ -427,6 +430,7 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         // larger share measured to make both finish together.
         ta.share_first = grid == cap ? kGemvShareFirst : 1;
         ta.share_second = grid == cap ? kGemvShareSecond : 1;
+        ta.test_stall_cycles = test_stall_cycles;
         r = cuda_status(launch_gemv_tc(ta, grid, stream));
         if (r) return r;
     }

@@ -234,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 // let the copies in flight land before the CTA exits (they are
                 // counted on the leader's barriers)
                 for (int s = 0; s < kStagesTc; ++s)
-                    if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimit / 8);
+                    if (pending[s]) tc::mbar_wait_drain(&S.full_b[s], pending_phase[s], kWaitLimit / 8);
             }
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
@@ -372,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             }
             // every MMA this thread issued has completed before TMEM is freed
             tc::pair_commit(&S.mma_done[me], 0x1);
-            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit / 8);
+            tc::mbar_wait_drain(&S.mma_done[me], 0, kWaitLimit / 8);
         }
     } else if (warp == kMmaWarp && rank == 1) {
         // ---------------------------------------------------------- forwarder

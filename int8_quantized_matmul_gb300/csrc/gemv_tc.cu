@@ -94,6 +94,7 @@ struct SmemGv {
     uint64_t mma_done[kIssuersGv];
     uint64_t epi_sync;                  // the 4 epilogue warps finished their partial-dot atomics
     uint64_t epi_bcast;                 // the split-K finalize decision is published
+    uint64_t never;                     // test only: a barrier nothing arrives on
     uint32_t tmem_base;
     int abort;
     int final_flag;
@@ -492,6 +493,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         for (int i = 0; i < kIssuersGv; ++i) tc::mbar_init(&S.mma_done[i], 1);
         tc::mbar_init(&S.epi_sync, 4 * 32);
         tc::mbar_init(&S.epi_bcast, 1);
+        tc::mbar_init(&S.never, 1);
         S.abort = 0;
         S.final_flag = 0;
         tc::fence_mbar_init();
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             }
             if (!ok)
                 for (int s2 = 0; s2 < kWStages; ++s2)
-                    if (pending[s2]) tc::mbar_wait(&S.full_w[s2], pending_phase[s2], abort_flag, kWaitLimitGv / 8);
+                    if (pending[s2]) tc::mbar_wait_drain(&S.full_w[s2], pending_phase[s2], kWaitLimitGv / 8);
         }
     } else if (warp < kCvtWarpsGv) {
         // ---------------------------------------------------------- converters
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             }
             if (!ok)
                 for (int s = 0; s < kBStages; ++s)
-                    if (pending[s]) tc::mbar_wait(&S.full_b[s], pending_phase[s], abort_flag, kWaitLimitGv / 8);
+                    if (pending[s]) tc::mbar_wait_drain(&S.full_b[s], pending_phase[s], kWaitLimitGv / 8);
         }
     } else if (warp == kMmaWarpGv || warp == kMmaWarpGv2) {
         // ---------------------------------------------------------- MMA issue
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
             tc::umma_commit(&S.mma_done[me]);
-            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimitGv / 8);
+            tc::mbar_wait_drain(&S.mma_done[me], 0, kWaitLimitGv / 8);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue
@@ -763,6 +765,16 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 if (g.act != cur_act) {
                     if (!wait_flag(a.flags + a.count + g.act, (uint32_t)a.M, abort_flag, kWaitLimitGv)) { fail(8192); break; }
                     cur_act = g.act;
+                }
+            }
+            if constexpr (!kFused) {
+                if (a.test_stall_cycles > 0) {
+                    // test only: a bounded wait that nothing ends, so the
+                    // launch takes its give-up path with its MMAs and copies in
+                    // flight (the status word records the timeout)
+                    tc::mbar_wait(&S.never, 0, abort_flag, a.test_stall_cycles);
+                    fail(512);
+                    break;
                 }
             }
             if (!tc::mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kWaitLimitGv)) { fail(512); break; }

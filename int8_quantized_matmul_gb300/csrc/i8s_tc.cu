@@ -273,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
             // within the bounded waits of the final cluster barrier's wait)
             if (!ok && rank == 0)
                 for (int s = 0; s < kStages8; ++s)
-                    if (pending[s]) tc::mbar_wait(&S.full[s], pending_phase[s], abort_flag, kWaitLimit8 / 8);
+                    if (pending[s]) tc::mbar_wait_drain(&S.full[s], pending_phase[s], kWaitLimit8 / 8);
         }
     } else if (warp >= kMmaWarp8 && warp < kMmaWarp8 + kIssuers8 && rank == 0) {
         // ---------------------------------------------------------- MMA issue
@@ -318,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                 }
             }
             tc::pair_commit(&S.mma_done[me], 0x1);
-            tc::mbar_wait(&S.mma_done[me], 0, abort_flag, kWaitLimit8 / 8);
+            tc::mbar_wait_drain(&S.mma_done[me], 0, kWaitLimit8 / 8);
         }
     } else if (warp < kEpiWarps8) {
         // ------------------------------------------------- drain and epilogue

@@ -91,6 +91,7 @@ struct TcArgs {
     int total_tiles;          // GEMM: tiles; GEMV: work units
     int share_first;          // GEMV: relative unit shares of the first and second half of the
     int share_second;         //   grid (the first and second CTA placed on each SM)
+    long long test_stall_cycles;   // GEMV, test only: > 0 makes the epilogue give up a wait nothing ends
     TcProb p[kMaxGroup];
 };
 

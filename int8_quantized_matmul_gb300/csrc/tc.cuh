@@ -115,6 +115,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Bounded wait for asynchronous work this CTA already started (copies in
+// flight, issued MMAs) to complete before the CTA gives up shared memory or
+// TMEM. Unlike the waits above it does not stop when the abort flag is set:
+// on a give-up path the flag is set, and leaving before the hardware is done
+// writing would hand the memory to the next CTA with writes still landing.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copy global -> shared, completion counted on an mbarrier)
 // ---------------------------------------------------------------------------

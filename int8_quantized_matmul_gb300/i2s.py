@@ -36,7 +36,7 @@ STATUS = {0: "I2S_OK", -1: "I2S_E_BAD_SHAPE", -2: "I2S_E_NULL_PTR", -3: "I2S_E_M
 
 
 class i2s_config(ctypes.Structure):
-    _fields_ = [("path", _int), ("grid_ctas", _int)]
+    _fields_ = [("path", _int), ("grid_ctas", _int), ("test_stall_cycles", _i64)]
 
 
 class i2s_problem(ctypes.Structure):
