@@ -147,17 +147,23 @@ class DecodePass:
         self.x = self.x_host.to(device)
         self.y = torch.empty(out_elems, dtype=torch.float32, device=device)
         self.y_host = torch.empty(out_elems, dtype=torch.float32).pin_memory()
-        problems, xo, yo = [], 0, 0
+        problems, host_problems, xo, yo = [], [], 0, 0
         for layer in range(LAYERS):
-            xs = []
+            xs, xhs = [], []
             for K in ACT_K:
                 xs.append(self.x[xo:xo + M * K].view(M, K))
+                xhs.append(self.x_host[xo:xo + M * K].view(M, K))
                 xo += M * K
             for i, (name, N, K) in enumerate(PROJ):
                 y = self.y[yo:yo + M * N].view(M, N)
+                yh = self.y_host[yo:yo + M * N].view(M, N)
                 yo += M * N
                 problems.append((weights[layer][i], N, K, xs[ACT_OF[name]], y))
+                host_problems.append((weights[layer][i], N, K, xhs[ACT_OF[name]], yh))
         self.group = i2s.Group(problems, M)
+        # the same projections on the host buffers, one C-ABI call per pass
+        # (i2s_mul_mat_grouped_host: copy up, quantize + GEMV, copy back)
+        self.host_group = i2s.HostGroup(host_problems, M, device=device)
         self.h2d_bytes = self.x.numel() * 4
         self.d2h_bytes = self.y.numel() * 4
         # algorithmic bytes of one GEMV launch: the 2-bit codes and their scale
@@ -176,29 +182,44 @@ GEMV_SOURCES = ["gemv_tc.cu", "tc.cuh", "common.cuh", "internal.h"]
 
 
 def gemv_source_hash():
+    return source_hash(GEMV_SOURCES)
+
+
+def source_hash(sources):
     import hashlib
     h = hashlib.sha256()
-    for name in GEMV_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "int8_quantized_matmul_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def recorded_gemv_traffic():
+def recorded_traffic(profile, sources, key):
+    """DRAM bytes recorded under `key` in a committed ncu summary, or None once
+    the kernel's sources no longer hash to the value recorded with them."""
     try:
-        with open(GEMV_PROFILE) as f:
+        with open(profile) as f:
             text = f.read()
     except OSError:
         return None
     rec = {}
     for line in text.splitlines():
         line = line.strip().strip("`")
-        for key in ("source_sha256", "dram_bytes_per_launch"):
-            if line.startswith(key + ":"):
-                rec[key] = line.split(":", 1)[1].strip()
-    if rec.get("source_sha256") != gemv_source_hash() or "dram_bytes_per_launch" not in rec:
+        for k in ("source_sha256", key):
+            if line.startswith(k + ":"):
+                rec[k] = line.split(":", 1)[1].strip()
+    if rec.get("source_sha256") != source_hash(sources) or key not in rec:
         return None
-    return float(rec["dram_bytes_per_launch"])
+    return float(rec[key])
+
+
+def recorded_gemv_traffic():
+    return recorded_traffic(GEMV_PROFILE, GEMV_SOURCES, "dram_bytes_per_launch")
+
+
+# the I8_S tensor-core GEMM (encoder FC pair and W8A8 layer)
+I8S_PROFILE = os.path.join(ROOT, "profiles", "k_i8s_gemm_tc_encoder_fc.md")
+I8S_SOURCES = ["i8s_tc.cu", "tc.cuh", "common.cuh", "internal.h"]
 
 
 def run_prefill(torch, i2s, weights, device, peaks, steps=5):
@@ -326,8 +347,10 @@ def run_encoder_fc(torch, i2s, device, peaks, steps=10):
             "packed_weights": {"ms_per_pair": ms_p, "value": tops_p, "unit": "TOPS",
                                "frac": tops_p / peaks["bf16_tflops"],
                                "note": "weights packed once into f16 operand rows (i8s_pack_weights)"},
-            "roofline": {"bound": "tensor", "achieved": tops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tops / peaks["bf16_tflops"]}}
+            "roofline": {"bound": "tensor", "kernel": "k_i8s_gemm_tc", "achieved": tops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tops / peaks["bf16_tflops"],
+                         "traffic": recorded_traffic(I8S_PROFILE, I8S_SOURCES, "dram_bytes_per_fc_pair"),
+                         "traffic_note": "DRAM bytes of the pair's two GEMM launches (ncu, L2 flushed before each)"}}
 
 
 def run_decode_fused(torch, i2s, passes, stream, steps):
@@ -475,8 +498,10 @@ def run_w8a8_prefill(torch, i2s, device, peaks, steps=10):
                       "packed once)",
             "ms_per_layer": ms, "ms_per_layer_one_call_per_projection": ms_single,
             "value": tops, "unit": "TOPS",
-            "roofline": {"bound": "tensor", "achieved": tops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tops / peaks["bf16_tflops"]}}
+            "roofline": {"bound": "tensor", "kernel": "k_i8s_gemm_tc", "achieved": tops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tops / peaks["bf16_tflops"],
+                         "traffic": recorded_traffic(I8S_PROFILE, I8S_SOURCES, "dram_bytes_per_w8a8_layer"),
+                         "traffic_note": "DRAM bytes of the layer's grouped GEMM launch (ncu, L2 flushed before it)"}}
 
 
 def cpu_baseline_decode(seconds_target=12.0):
@@ -668,13 +693,12 @@ def run_ours(args, rank, world, torch, dist):
     gemv_avg_bytes = sum(gemv_bytes_all) / len(gemv_bytes_all)
     achieved = gemv_avg_bytes / (gemv_avg_ms * 1e-3) / 1e9
 
-    # end to end through the public API: activations host->device, the pass,
-    # outputs device->host, every step (pinned buffers). The two passes are
-    # independent batches, so each one's copies run on a second stream beside
-    # the other's kernels: the M = 8 inputs go up first, the M = 1 inputs go up
-    # while the M = 8 pass computes, the M = 8 outputs come back while the M = 1
-    # pass computes. Steps do not overlap: a step's first copy waits for the
-    # previous step's last.
+    # end to end through the C ABI on host buffers: each pass is one
+    # i2s_mul_mat_grouped_host call (pinned activations copied up, the
+    # quantization and GEMV launches, the outputs copied back). The two passes
+    # are independent batches on two streams, so one pass's copies overlap the
+    # other's kernels. Steps do not overlap: a step starts after both passes of
+    # the previous step are done.
     side = torch.cuda.Stream(device=device)
     p_big, p_small = sorted(passes, key=lambda q: -q.M)
 
@@ -682,23 +706,12 @@ def run_ours(args, rank, world, torch, dist):
         done_prev = torch.cuda.Event()
         done_prev.record(stream)
         side.wait_event(done_prev)
-        p_big.x.copy_(p_big.x_host, non_blocking=True)
+        p_big.host_group()
         with torch.cuda.stream(side):
-            p_small.x.copy_(p_small.x_host, non_blocking=True)
-            small_in = torch.cuda.Event()
-            small_in.record(side)
-        p_big.group()
-        big_done = torch.cuda.Event()
-        big_done.record(stream)
-        stream.wait_event(small_in)
-        p_small.group()
-        with torch.cuda.stream(side):
-            side.wait_event(big_done)
-            p_big.y_host.copy_(p_big.y, non_blocking=True)
-            big_out = torch.cuda.Event()
-            big_out.record(side)
-        p_small.y_host.copy_(p_small.y, non_blocking=True)
-        stream.wait_event(big_out)
+            p_small.host_group()
+            small_done = torch.cuda.Event()
+            small_done.record(side)
+        stream.wait_event(small_done)
 
     for _ in range(2):
         e2e_step()
@@ -717,7 +730,9 @@ def run_ours(args, rank, world, torch, dist):
     e2e = {"value": world * args.steps * bytes_per_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes for p in passes),
            "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes),
-           "note": "each pass's pinned copies overlap the other pass's kernels on a second stream; steps are serial"}
+           "api": "i2s_mul_mat_grouped_host (C ABI, pinned host activations and outputs), one call per pass",
+           "note": "the two passes run on two streams, so one pass's copies overlap the other's kernels; "
+                   "steps are serial"}
 
     fused = run_decode_fused(torch, i2s, passes, stream, args.steps)
     prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None
@@ -751,6 +766,23 @@ def run_ours(args, rank, world, torch, dist):
     return line
 
 
+def run_leg(args, torch):
+    """One side leg alone on cuda:0, so that an ncu capture sees only its kernels."""
+    from int8_quantized_matmul_gb300 import build as libbuild
+    libbuild.build()
+    from int8_quantized_matmul_gb300 import i2s
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    if args.leg == "prefill":
+        return run_prefill(torch, i2s, make_weights(torch, device), device, peaks, steps=args.steps)
+    if args.leg == "encoder":
+        return run_encoder_fc(torch, i2s, device, peaks, steps=args.steps)
+    if args.leg == "eltwise":
+        return run_encoder_eltwise(torch, i2s, device, peaks, steps=args.steps)
+    return run_w8a8_prefill(torch, i2s, device, peaks, steps=args.steps)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -759,6 +791,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, encoder and W8A8 legs")
+    ap.add_argument("--leg", choices=["prefill", "encoder", "eltwise", "w8a8"],
+                    help="run only this side leg on cuda:0 (--steps timed calls) and print its object")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -772,6 +806,9 @@ def main():
         return
 
     import torch
+    if args.leg:
+        print(json.dumps(run_leg(args, torch)), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist_mod

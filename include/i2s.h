@@ -255,6 +255,35 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
                             size_t ws_bytes, i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The grouped I2_S matmul on HOST activations and outputs: one call enqueues
+ * the activations' copy to the device, the grouped matmul (same kernels and
+ * results as i2s_mul_mat_grouped) and the outputs' copy back, all on
+ * `stream`. This is the whole mul_mat of [P2] Kernels for a caller whose
+ * src1 rows and results live in CPU memory; the weights stay on the device.
+ *
+ * probs  host array of `count` problems as for i2s_mul_mat_grouped, except
+ *        that x (M x K F32) and y (M x N F32) are HOST pointers, 16-byte
+ *        aligned. With page-locked memory (cudaHostAlloc, cudaHostRegister)
+ *        the copies are asynchronous; with pageable memory the runtime
+ *        stages them and the call may return only after they are done.
+ * ws     device workspace of at least i2s_mul_mat_grouped_host_workspace()
+ *        bytes, 256-byte aligned: the grouped workspace (so i2s_read_status
+ *        reads the same status word), then device copies of the activations
+ *        and outputs.
+ * Copies: host ranges of the activations that touch or overlap are merged,
+ * and each merged range moves up with one cudaMemcpyAsync; the outputs come
+ * back the same way. Activations and outputs that are slices of one buffer
+ * each take one copy each way. y holds the results once the stream's work is
+ * done; x and y must stay valid until then.
+ * Errors: as i2s_mul_mat_grouped, plus BAD_ARG if two outputs overlap or an
+ * output overlaps an activation. The workspace query returns 0 for a list the
+ * call would reject.
+ * ------------------------------------------------------------------------- */
+size_t i2s_mul_mat_grouped_host_workspace(const i2s_problem* probs, int count, int64_t M);
+int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                             i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Fused decode step: the grouped I2_S matmul for M <= 16 as ONE launch whose
  * prologue quantizes the activations, as the pages' mul_mat quantizes its
  * src1 rows before the dot products in the same op ([P2] Kernels, threading

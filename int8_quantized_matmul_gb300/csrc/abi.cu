@@ -684,6 +684,115 @@ int i2s_mul_mat_grouped_run(const i2s_problem* probs, int count, int64_t M, void
     return grouped_impl(probs, count, M, ws, ws_bytes, stream, 2);
 }
 
+// ---------------------------------------------------------------------------
+// Grouped call on host activations and outputs. Workspace: [grouped
+// workspace][device copies of the merged activation ranges][device copies of
+// the merged output ranges], each copy 256-byte aligned.
+// ---------------------------------------------------------------------------
+struct HostSpan {
+    uintptr_t lo, hi;   // host byte range
+    size_t off;         // its device copy's offset in the workspace
+};
+
+// Merges the host byte ranges that touch or overlap into spans sorted by
+// address and lays their device copies out from `base`. Returns the end offset.
+static size_t host_spans(std::vector<std::pair<uintptr_t, uintptr_t>> r, size_t base, std::vector<HostSpan>& out) {
+    std::sort(r.begin(), r.end());
+    out.clear();
+    for (const auto& e : r) {
+        if (!out.empty() && e.first <= out.back().hi) {
+            out.back().hi = std::max(out.back().hi, e.second);
+        } else {
+            out.push_back({e.first, e.second, 0});
+        }
+    }
+    for (HostSpan& s : out) {
+        s.off = base;
+        base += align_up((size_t)(s.hi - s.lo));
+    }
+    return base;
+}
+
+// The span holding host address p (spans sorted, p inside one of them).
+static const HostSpan& span_of(const std::vector<HostSpan>& spans, uintptr_t p) {
+    size_t lo = 0, hi = spans.size();
+    while (hi - lo > 1) {
+        const size_t mid = (lo + hi) / 2;
+        if (spans[mid].lo <= p) lo = mid; else hi = mid;
+    }
+    return spans[lo];
+}
+
+struct HostPlan {
+    std::vector<HostSpan> xs, ys;
+    size_t grouped = 0, total = 0;
+};
+
+// Validates the host problem list and lays out the workspace. Returns a status.
+static int host_plan(const i2s_problem* probs, int count, int64_t M, HostPlan& pl) {
+    if (!probs) return I2S_E_NULL_PTR;
+    if (count < 1 || count > I2S_MAX_GROUP) return I2S_E_BAD_ARG;
+    std::vector<std::pair<uintptr_t, uintptr_t>> xr, yr;
+    for (int i = 0; i < count; ++i) {
+        const i2s_problem& p = probs[i];
+        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
+        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
+        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+        const uintptr_t x = (uintptr_t)p.x, y = (uintptr_t)p.y;
+        xr.push_back({x, x + (uintptr_t)(M * p.K) * 4});
+        yr.push_back({y, y + (uintptr_t)(M * p.N) * 4});
+    }
+    // outputs may overlap neither one another nor any activation
+    std::vector<std::pair<uintptr_t, uintptr_t>> ys = yr;
+    std::sort(ys.begin(), ys.end());
+    for (size_t i = 1; i < ys.size(); ++i)
+        if (ys[i].first < ys[i - 1].second) return I2S_E_BAD_ARG;
+    for (const auto& y : ys)
+        for (const auto& x : xr)
+            if (y.first < x.second && x.first < y.second) return I2S_E_BAD_ARG;
+    pl.grouped = i2s_mul_mat_grouped_workspace(probs, count, M);
+    if (pl.grouped == 0) return I2S_E_BAD_SHAPE;
+    const size_t after_x = host_spans(xr, pl.grouped, pl.xs);
+    pl.total = host_spans(yr, after_x, pl.ys);
+    return I2S_OK;
+}
+
+size_t i2s_mul_mat_grouped_host_workspace(const i2s_problem* probs, int count, int64_t M) {
+    HostPlan pl;
+    return host_plan(probs, count, M, pl) == I2S_OK ? pl.total : 0;
+}
+
+int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                             i2s_stream_t stream) {
+    HostPlan pl;
+    int r = host_plan(probs, count, M, pl);
+    if (r) return r;
+    if (!ws) return I2S_E_NULL_PTR;
+    if (!aligned256(ws)) return I2S_E_MISALIGNED;
+    if (ws_bytes < pl.total) return I2S_E_WORKSPACE_TOO_SMALL;
+    r = check_device();
+    if (r) return r;
+    char* base = (char*)ws;
+    std::vector<i2s_problem> dev(probs, probs + count);
+    for (i2s_problem& p : dev) {
+        const HostSpan& sx = span_of(pl.xs, (uintptr_t)p.x);
+        const HostSpan& sy = span_of(pl.ys, (uintptr_t)p.y);
+        p.x = (const float*)(base + sx.off + ((uintptr_t)p.x - sx.lo));
+        p.y = (float*)(base + sy.off + ((uintptr_t)p.y - sy.lo));
+    }
+    for (const HostSpan& s : pl.xs) {
+        r = cuda_status(cudaMemcpyAsync(base + s.off, (const void*)s.lo, s.hi - s.lo, cudaMemcpyHostToDevice, stream));
+        if (r) return r;
+    }
+    r = grouped_impl(dev.data(), count, M, ws, pl.grouped, stream, 3);
+    if (r) return r;
+    for (const HostSpan& s : pl.ys) {
+        r = cuda_status(cudaMemcpyAsync((void*)s.lo, base + s.off, s.hi - s.lo, cudaMemcpyDeviceToHost, stream));
+        if (r) return r;
+    }
+    return I2S_OK;
+}
+
 size_t i8s_ws_f32_offset(void) { return kHeader; }
 
 static bool overlaps(const void* a, size_t na, const void* b, size_t nb);

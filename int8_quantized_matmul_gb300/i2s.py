@@ -66,6 +66,8 @@ _SIGS = {
     "i2s_mul_mat_grouped": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_quantize": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_run": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i2s_mul_mat_grouped_host_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
+    "i2s_mul_mat_grouped_host": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_fused_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
     "i2s_mul_mat_grouped_fused_init": (_int, [_p, _sz, _p]),
     "i2s_mul_mat_grouped_fused": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
@@ -295,6 +297,50 @@ class Group:
         _check("i2s_mul_mat_grouped",
                _L.i2s_mul_mat_grouped(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
                                       _stream()))
+
+
+def _hptr(t) -> int:
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _host_problems(problems: Sequence):
+    arr = (i2s_problem * len(problems))()
+    for i, (w, N, K, x, y) in enumerate(problems):
+        arr[i] = i2s_problem(_dptr(w), N, K, _hptr(x), _hptr(y))
+    return arr
+
+
+class HostGroup:
+    """A fixed list of projections [(w, N, K, x, y), ...] whose activations x
+    and outputs y are host (CPU, ideally pinned) tensors and whose weights w
+    are on the device; each call copies x up, runs the grouped matmul and
+    copies y back, on torch's current stream (i2s_mul_mat_grouped_host)."""
+
+    def __init__(self, problems: Sequence, M: int, device=None, ws=None):
+        self.problems = list(problems)
+        self.M = int(M)
+        self.arr = _host_problems(self.problems)
+        need = int(_L.i2s_mul_mat_grouped_host_workspace(self.arr, len(self.problems), self.M))
+        if need == 0:
+            raise I2SError("i2s_mul_mat_grouped_host_workspace", -1)
+        self.ws = ws if ws is not None else _ws(need, device if device is not None else self.problems[0][0].device)
+
+    def __call__(self):
+        _check("i2s_mul_mat_grouped_host",
+               _L.i2s_mul_mat_grouped_host(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
+                                           _stream()))
+
+
+def i2s_mul_mat_grouped_host(problems: Sequence, M: int, ws=None):
+    """One call of HostGroup; returns the workspace (the outputs are valid
+    once torch's current stream has finished)."""
+    g = HostGroup(problems, M, ws=ws)
+    g()
+    return g.ws
 
 
 class FusedGroup:

@@ -206,3 +206,54 @@ def test_fused_decode_validation_needs_no_device(i2s):
     assert L.i2s_mul_mat_grouped_fused_workspace(nine, 8, 4) > 0
     assert L.i2s_mul_mat_grouped_fused_workspace(nine, 9, 4) == 0
     assert L.i2s_mul_mat_grouped_fused(nine, 9, 4, vp(8 * A), 1 << 30, None) == E["I2S_E_BAD_ARG"]
+
+
+def test_host_buffer_call_validation_and_copy_plan(i2s):
+    # i2s_mul_mat_grouped_host: activations and outputs on the host. The
+    # workspace is the grouped one followed by one device copy per merged host
+    # range, so slices of one buffer cost one range each way.
+    L = i2s.lib
+    A = 1 << 20
+    vp = ctypes.c_void_p
+    E = {v: k for k, v in i2s.STATUS.items()}
+    M, K = 4, 1536
+    xb, yb = 64 * A, 96 * A                     # host addresses (never dereferenced)
+
+    def problems(xs, ys, Ns):
+        arr = (i2s.i2s_problem * len(xs))()
+        for i, (x, y, N) in enumerate(zip(xs, ys, Ns)):
+            arr[i] = i2s.i2s_problem(A, N, K, x, y)
+        return arr
+
+    def up(v):
+        return (v + 255) // 256 * 256
+    Ns = [64, 320, 256]
+    # x: one activation shared by the first two, the third right after it;
+    # y: three outputs back to back
+    xs = [xb, xb, xb + M * K * 4]
+    ys = [yb, yb + M * 64 * 4, yb + M * (64 + 320) * 4]
+    merged = problems(xs, ys, Ns)
+    grouped = L.i2s_mul_mat_grouped_workspace(merged, 3, M)
+    assert grouped > 0
+    assert L.i2s_mul_mat_grouped_host_workspace(merged, 3, M) == grouped + up(2 * M * K * 4) + up(M * 640 * 4)
+    # the same problems with gaps between the host buffers: one range each
+    apart = problems([xb, xb, xb + 2 * A], [yb, yb + A, yb + 2 * A], Ns)
+    assert L.i2s_mul_mat_grouped_host_workspace(apart, 3, M) == (
+        grouped + 2 * up(M * K * 4) + sum(up(M * n * 4) for n in Ns))
+    need = L.i2s_mul_mat_grouped_host_workspace(merged, 3, M)
+    ws = vp(8 * A)
+    assert L.i2s_mul_mat_grouped_host(merged, 3, M, ws, need - 1, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    assert L.i2s_mul_mat_grouped_host(merged, 3, M, vp(8 * A + 16), need, None) == E["I2S_E_MISALIGNED"]
+    assert L.i2s_mul_mat_grouped_host(merged, 3, M, None, need, None) == E["I2S_E_NULL_PTR"]
+    assert L.i2s_mul_mat_grouped_host(merged, 0, M, ws, need, None) == E["I2S_E_BAD_ARG"]
+    # overlapping outputs, and an output over an activation, are rejected
+    clash = problems(xs, [yb, yb + 16, yb + A], Ns)
+    assert L.i2s_mul_mat_grouped_host_workspace(clash, 3, M) == 0
+    assert L.i2s_mul_mat_grouped_host(clash, 3, M, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    onto = problems(xs, [yb, yb + A, xb + 64], Ns)
+    assert L.i2s_mul_mat_grouped_host(onto, 3, M, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    odd = problems([xb + 8, xb, xb], ys, Ns)
+    assert L.i2s_mul_mat_grouped_host(odd, 3, M, ws, 1 << 30, None) == E["I2S_E_MISALIGNED"]
+    bad_k = problems(xs, ys, Ns)
+    bad_k[1].K = 100
+    assert L.i2s_mul_mat_grouped_host(bad_k, 3, M, ws, 1 << 30, None) == E["I2S_E_BAD_SHAPE"]
