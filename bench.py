@@ -273,13 +273,14 @@ def run_prefill(torch, i2s, weights, device, peaks, steps=5):
     tops = ops / (g_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": "qwen2-1.5b projection set x28 layers + lm_head 1536->151936, M=512 (pp512 shape)",
-            "metric": "prefill int8 TOPS (exact integer dot on tcgen05 kind::f16)", "int_ops": ops,
+            "metric": "prefill int8 TOPS (exact integer dot on tcgen05 kind::mxf4)", "int_ops": ops,
             "gemm_ms": g_ms, "quant_ms": q_ms, "value": tops, "unit": "TOPS",
             "e2e_device_tops": ops / ((g_ms + q_ms) * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "kernel": "k_i2s_gemm_tc", "achieved": tops, "peak": peak,
                          "unit": "TFLOP/s", "frac": tops / peak,
                          "peak_source": ("measured bf16 dense (MEASURED_PEAKS.json bf16_tflops); the kernel runs "
-                                         "kind::f16, whose dense rate equals bf16's" if peaks["source"] == "measured"
+                                         "kind::mxf4 with three fp4 MMAs per integer multiply-add, so its own "
+                                         "ceiling is twice this (fp4 dense = 6x bf16)" if peaks["source"] == "measured"
                                          else "fallback 1900 TFLOP/s bf16")},
             "status": status}
 
