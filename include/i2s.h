@@ -247,7 +247,9 @@ int i2s_mul_mat_grouped(const i2s_problem* probs, int count, int64_t M, void* ws
  * activation's quantized rows, scale and row sum into ws; _run computes all
  * the projections from ws. A _run call must use the same problem list, M and
  * workspace as the _quantize call before it on the stream. Splitting lets a
- * caller quantize once and run the projections later or in several launches.
+ * caller quantize once and run the projections later or several times: a
+ * completed _run leaves the workspace's split-K sums and counters at zero, as
+ * _quantize leaves them.
  * Errors: as i2s_mul_mat_grouped. */
 int i2s_mul_mat_grouped_quantize(const i2s_problem* probs, int count, int64_t M, void* ws,
                                  size_t ws_bytes, i2s_stream_t stream);

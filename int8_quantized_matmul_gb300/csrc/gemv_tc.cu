@@ -753,7 +753,10 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         // A segment that covers all K chunks of its tile writes y directly.
         // Otherwise its exact int32 partial dots are added to the workspace;
         // the segment whose chunks complete the tile's count applies the
-        // epilogue to the summed dots (integer addition is order-independent).
+        // epilogue to the summed dots (integer addition is order-independent)
+        // and returns the tile's partial dots and ticket to zero, so a launch
+        // leaves the split-K state as it found it (a run may be repeated
+        // without a new quantization).
         const int q = warp - kEpiWarp0;   // TMEM lane quarter
         const int r = q * 32 + lane;
         int acc = 0;
@@ -813,8 +816,13 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 if (!tc::mbar_wait_idle(&S.epi_sync, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
                 if (r == 0) {
                     __threadfence();
-                    const unsigned prev = atomicAdd(&a.ticket_base[g.ticket_off + g.tile], (unsigned)g.units);
-                    S.final_flag = prev + (unsigned)g.units == (unsigned)g.chunks;
+                    unsigned* ticket = &a.ticket_base[g.ticket_off + g.tile];
+                    const unsigned prev = atomicAdd(ticket, (unsigned)g.units);
+                    const bool last = prev + (unsigned)g.units == (unsigned)g.chunks;
+                    // every other segment of the tile has counted itself: the
+                    // ticket starts the next launch on this workspace at zero
+                    if (last) *ticket = 0u;
+                    S.final_flag = last;
                     tc::mbar_arrive(&S.epi_bcast);
                 }
                 if (!tc::mbar_wait_idle(&S.epi_bcast, sync_phase, abort_flag, kWaitLimitGv)) { fail(2048); break; }
@@ -822,10 +830,13 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 write = S.final_flag != 0;
                 if (write) {
                     __threadfence();
-                    if (n < g.N) {
+                    if (n < g.N) {   // read the summed dots and leave zeros for the next launch
 #pragma unroll
                         for (int m = 0; m < Mp; ++m)
-                            if (m < a.M) dot[m] = __ldcg(&part[(size_t)m * g.N + n]);
+                            if (m < a.M) {
+                                dot[m] = __ldcg(&part[(size_t)m * g.N + n]);
+                                part[(size_t)m * g.N + n] = 0;
+                            }
                     }
                 }
             }

@@ -753,6 +753,8 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_weights(const float* __res
 // row holds K rounded up to 64 positions, the tail zero) and its scale, a
 // block with m >= M writes a zero row. The same launch clears the
 // status word, the amax word and the GEMM's split-tile counters.
+constexpr int kW8Cache = 8;   // float4 per thread kept in registers (rows up to 8192 values)
+
 __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_constant__ W8a8RowJobs J) {
     __shared__ float s_max[kEltThreads / 32];
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -768,14 +770,29 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_cons
     const int64_t K = J.K[j];
     const int64_t Kp = (K + 63) / 64 * 64;   // operand row length, the tail zero
     __half* out = J.xf[j] + m * Kp;
-    if (m >= J.M) {
-        for (int64_t k = threadIdx.x; k < Kp; k += blockDim.x) out[k] = __float2half_rn(0.0f);
+    if (m >= J.M) {   // Kp halves are Kp / 8 16-byte words
+        for (int64_t k = threadIdx.x; k < Kp / 8; k += blockDim.x) reinterpret_cast<uint4*>(out)[k] = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
     for (int64_t k = K + threadIdx.x; k < Kp; k += blockDim.x) out[k] = __float2half_rn(0.0f);
     const float* xr = J.x[j] + m * K;
+    // rows whose length is a multiple of 4 start 16-byte aligned: read as
+    // float4, kept in registers, written four halves at a time
+    const int K4 = (int)(K / 4);
+    const bool vec = (K % 4) == 0 && K4 <= kW8Cache * kEltThreads;
+    float4 c[kW8Cache];
     float mx = 0.0f;
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
+    if (vec) {
+        const float4* x4 = reinterpret_cast<const float4*>(xr);
+#pragma unroll
+        for (int i = 0; i < kW8Cache; ++i) {
+            const int k4 = (int)threadIdx.x + i * kEltThreads;
+            c[i] = k4 < K4 ? x4[k4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(c[i].x), fabsf(c[i].y)), fmaxf(fabsf(c[i].z), fabsf(c[i].w))));
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(xr[k]));
+    }
     mx = warp_max(mx);
     if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
     __syncthreads();
@@ -784,7 +801,22 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_cons
     mx = fmaxf(mx, 1e-9f);
     const float inv = __fdiv_rn(127.0f, mx);
     if (threadIdx.x == 0) J.ascale[j][m] = __fdiv_rn(mx, 127.0f);
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_one(xr[k], inv));
+    if (vec) {
+        uint2* o2 = reinterpret_cast<uint2*>(out);
+#pragma unroll
+        for (int i = 0; i < kW8Cache; ++i) {
+            const int k4 = (int)threadIdx.x + i * kEltThreads;
+            if (k4 < K4) {
+                const __half2 lo = __halves2half2(__int2half_rn(quantize_one(c[i].x, inv)),
+                                                  __int2half_rn(quantize_one(c[i].y, inv)));
+                const __half2 hi = __halves2half2(__int2half_rn(quantize_one(c[i].z, inv)),
+                                                  __int2half_rn(quantize_one(c[i].w, inv)));
+                o2[k4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            }
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_one(xr[k], inv));
+    }
 }
 
 // int8 -> f16 (exact), 16 values per thread and step.

@@ -176,3 +176,18 @@ def test_w8a8_epilogue_association_golden(i2s, o):
     want = np.array([int(v, 16) for v in c["d"]], dtype=np.uint32)
     d, _ = i2s.w8a8_mul_mat(dev(wq), dev(bs), dev(x))
     assert np.array_equal(host(d)[0].view(np.uint32), want)
+
+
+@pytest.mark.parametrize("K", [4, 8188, 8192, 8196, 8960])
+def test_w8a8_packed_row_lengths(i2s, o, K):
+    # the packed and grouped calls quantize each activation row straight into
+    # f16 operand rows: rows of up to 8192 values whose length is a multiple
+    # of 4 are read as float4 and kept in registers, other rows take the
+    # plain loop; both sides of that boundary against the oracle
+    M, N = 5, 70
+    wq, bs, x = w8a8_inputs(o, M, N, K, seed=K)
+    want = o.w8a8_mul_mat(wq, bs, x, nth=4)
+    packed = i2s.w8a8_pack_weights(dev(wq))
+    d, ws = i2s.w8a8_mul_mat_packed(packed, dev(bs), N, K, dev(x))
+    assert i2s.read_status(ws) == 0
+    same_bits(host(d), want)

@@ -297,6 +297,26 @@ def test_i2s_grouped_back_to_back_on_one_workspace(i2s, o):
             same_bits(host(y), o.i2s_mul_mat(packed, N, K, acts[act], nth=4))
 
 
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_i2s_grouped_run_repeated_after_one_quantize(i2s, o, M):
+    # A completed run leaves the split-K sums and tile counters at zero, so a
+    # run may be repeated after one quantization: three runs, the outputs
+    # cleared between them, each compared with the oracle (the down
+    # projection, K = 8960, is split over six K chunks per tile)
+    probs, acts = layer_problems(o, M=M, seed=40 + M)
+    dacts = {k: dev(v) for k, v in acts.items()}
+    dys = [torch.zeros((M, N), dtype=torch.float32, device="cuda") for _, N, _, _, _, _ in probs]
+    group = i2s.Group([(dev(p[3]), p[1], p[2], dacts[p[5]], y) for p, y in zip(probs, dys)], M)
+    group.quantize()
+    for _ in range(3):
+        for y in dys:
+            y.zero_()
+        group.run()
+        assert i2s.read_status(group.ws) == 0
+        for (name, N, K, packed, x, _), y in zip(probs, dys):
+            same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=4))
+
+
 def _row_slice(packed, N, K, n0, n1):
     """I2_S bytes of weight rows n0..n1 (rows are contiguous, K/4 bytes each)."""
     rb = K // 4
