@@ -174,8 +174,8 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
                    void* ws, size_t ws_bytes, const i2s_config* config, i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Decode I2_S matmul without a workspace. The pages have no counterpart of
- * this call. It exists for callers that cannot provide device scratch memory: a plain C or
+ * Decode I2_S matmul without a workspace. It exists for callers that cannot
+ * provide device scratch memory: a plain C or
  * ctypes host with no device allocator of its own, or a serving loop that
  * must not allocate once it runs, because cudaMalloc and cudaFree can
  * synchronize the device and a fixed memory budget leaves no room for

@@ -47,12 +47,17 @@ struct QuantArgs {
     int M;
     int rows;           // rows written per job: M, or M' (8 or 16) for kQuantE2M1Tc
     int layout;
+    int n_short;        // kQuantE2M1Tc: jobs j < n_short have K <= kQuantWarpRowK (one warp per row),
+    int short_ctas;     //   each over short_ctas CTAs; set by launch_quant, which orders the jobs
     int n_wmaps;
     WMapJob wj[kMaxGroup];
     QuantJob j[kMaxGroup];
 };
 
-cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s);
+// Rows of at most this many positions are quantized one per warp (kQuantE2M1Tc).
+constexpr int kQuantWarpRowK = 1536;
+// Orders a.j (short rows first), sets n_short and short_ctas, and launches.
+cudaError_t launch_quant(QuantArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Prefill GEMM (M > 16) on tcgen05 (gemm_tc.cu).

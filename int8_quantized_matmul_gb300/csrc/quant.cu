@@ -10,6 +10,8 @@
 // matmuls, so no separate repacking pass is needed (kQuantE2M1Tc: each q as
 // three base-8 digits in e2m1, one operand row per digit, k_quant_rows_tc4).
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "quant_tc.cuh"
@@ -94,15 +96,19 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows(const __grid_constant_
     }
 }
 
+// The e2m1 digit operand (kQuantE2M1Tc). Rows of at most kQuantWarpRowK
+// positions (the first n_short jobs) are quantized one per warp, eight rows
+// per CTA, with warp-level reductions only; longer rows take a whole CTA.
 __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_constant__ QuantArgs a) {
     __shared__ float s_red[kQThreads / 32];
     __shared__ int s_sum[kQThreads / 32];
     __shared__ uint32_t s_code[255];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 255) s_code[tid] = digit_code(tid - 127);
+    __syncthreads();
     // launched as a programmatic dependent of the kernel before it: wait for
     // that kernel (which may use the same workspace, or produce x) before
     // reading or writing global memory
-    if (tid < 255) s_code[tid] = digit_code(tid - 127);
     pdl_wait();
     if (a.status && blockIdx.x == 0 && tid == 0) *a.status = 0u;
     // map i is written by thread i / gridDim.x of CTA i % gridDim.x: one or two
@@ -113,9 +119,43 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
     for (unsigned long long i = blockIdx.x * (unsigned long long)kQThreads + tid; i < a.zero_16;
          i += (unsigned long long)gridDim.x * kQThreads)
         a.zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    const QuantJob& J = a.j[blockIdx.x / a.M];   // one CTA per present activation row
-    const int m = blockIdx.x % a.M;
     const int Mp = a.rows;
+    const int short_blocks = a.n_short * a.short_ctas;
+    if ((int)blockIdx.x < short_blocks) {   // one warp per row
+        const QuantJob& J = a.j[blockIdx.x / a.short_ctas];
+        const int m = (blockIdx.x % a.short_ctas) * (kQThreads / 32) + warp;
+        if (m >= a.M) return;
+        const int K = J.K, U = K / 16;   // U <= 32 * kQ4Cache
+        const float4* x4 = reinterpret_cast<const float4*>(J.x + (size_t)m * K);
+        float4 cache[kQ4Cache][4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kQ4Cache; ++c) {
+            const int u = lane + 32 * c;
+            if (u < U) {
+                load_unit(x4, u, cache[c]);
+                amax = fmaxf(amax, unit_amax(cache[c]));
+            }
+        }
+        amax = warp_max(amax);
+        float scale, inv;
+        quant_params(amax, scale, inv);
+        int sum = 0;
+#pragma unroll
+        for (int c = 0; c < kQ4Cache; ++c) {
+            const int u = lane + 32 * c;
+            if (u < U) sum += emit_unit(cache[c], inv, u, static_cast<uint8_t*>(J.out), (size_t)K / 2, Mp, m, s_code);
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+            J.scale[m] = scale;
+            J.sum[m] = sum;
+        }
+        return;
+    }
+    const int b = (int)blockIdx.x - short_blocks;   // one CTA per row
+    const QuantJob& J = a.j[a.n_short + b / a.M];
+    const int m = b % a.M;
     const int K = J.K, U = K / 16;
     const size_t row_bytes = (size_t)K / 2;
     uint8_t* op = static_cast<uint8_t*>(J.out);
@@ -168,11 +208,18 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
     }
 }
 
-cudaError_t launch_quant(const QuantArgs& a, cudaStream_t s) {
+static_assert(kQuantWarpRowK / 16 <= 32 * kQ4Cache, "a short row fits one warp's registers");
+
+cudaError_t launch_quant(QuantArgs& a, cudaStream_t s) {
     if (a.layout == kQuantE2M1Tc) {
+        // short rows first (stable), eight rows per CTA; then one CTA per long row
+        std::stable_partition(a.j, a.j + a.count, [](const QuantJob& q) { return q.K <= kQuantWarpRowK; });
+        a.n_short = 0;
+        while (a.n_short < a.count && a.j[a.n_short].K <= kQuantWarpRowK) ++a.n_short;
+        a.short_ctas = (a.M + kQThreads / 32 - 1) / (kQThreads / 32);
         // the decode path: a programmatic dependent of the kernel before it
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(a.count * a.M), 1, 1);
+        cfg.gridDim = dim3((unsigned)(a.n_short * a.short_ctas + (a.count - a.n_short) * a.M), 1, 1);
         cfg.blockDim = dim3(kQThreads, 1, 1);
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
