@@ -592,6 +592,22 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def max_over_ranks(torch, dist, ms, device):
+    """The slowest rank's time (every rank gets it): the job is done when its
+    last replica is."""
+    if dist is None:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, steps, bytes_per_step, max_ms):
+    """Whole-job GB/s: every replica moves bytes_per_step per step (weak
+    scaling), over the slowest replica's time."""
+    return world * steps * bytes_per_step / (max_ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, torch, dist):
     from int8_quantized_matmul_gb300 import build as libbuild
     libbuild.build()
@@ -690,11 +706,7 @@ def run_ours(args, rank, world, torch, dist):
         b2b_ev.append(evs)
     barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, t_start.elapsed_time(t_end), device)
 
     per_m = {}
     gemv_ms_all, gemv_bytes_all = [], []
@@ -709,7 +721,7 @@ def run_ours(args, rank, world, torch, dist):
             "gemv_only_weight_gbs": WEIGHT_BYTES_PER_PASS / statistics.median(g_ms) / 1e6,
         }
     bytes_per_step = WEIGHT_BYTES_PER_PASS * len(passes)
-    value = world * args.steps * bytes_per_step / (total_ms * 1e-3) / 1e9
+    value = job_rate(world, args.steps, bytes_per_step, total_ms)
     gemv_avg_ms = sum(gemv_ms_all) / len(gemv_ms_all)
     gemv_avg_bytes = sum(gemv_bytes_all) / len(gemv_bytes_all)
     iso_achieved = gemv_avg_bytes / (gemv_avg_ms * 1e-3) / 1e9
@@ -751,12 +763,8 @@ def run_ours(args, rank, world, torch, dist):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * args.steps * bytes_per_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), device)
+    e2e = {"value": job_rate(world, args.steps, bytes_per_step, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes for p in passes),
            "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes),
            "api": "i2s_mul_mat_grouped_host (C ABI, pinned host activations and outputs), one call per pass",
