@@ -263,11 +263,16 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         slots[a] = act_slot_at(off, M);
         off += act_slot_bytes(M, probs[first[a]].K);
     }
+    // one TMA map per weight matrix (its packed codes), written by the
+    // quantization launch
+    CUtensorMap* wmaps = reinterpret_cast<CUtensorMap*>(base + off);
     int r;
     if (phases & 1) {
         static thread_local QuantArgs qa;
-        qa.wmaps = nullptr;
-        qa.n_wmaps = 0;
+        if (!make_code_map_template(&qa.wtmpl, probs[0].w_i2s)) return I2S_E_CUDA;
+        qa.wmaps = wmaps;
+        qa.n_wmaps = count;
+        for (int i = 0; i < count; ++i) qa.wj[i] = WMapJob{probs[i].w_i2s, (int)probs[i].N, (int)probs[i].K};
         qa.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
         qa.zero = nullptr;
         qa.zero_16 = 0;
@@ -294,6 +299,7 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
         ta.n_act_rows = rows_pad;
         ta.test_stall_cycles = 0;
         ta.status = reinterpret_cast<uint32_t*>(base + kStatusOff);
+        ta.wmaps = wmaps;
         // the three digit planes of each activation; each CTA of a pair loads
         // half of a tile's activation rows of a plane
         for (int a = 0; a < n_act; ++a)
@@ -633,6 +639,11 @@ size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_
     for (int a : first) {
         if (!i2s_shape_ok(probs[a].N, probs[a].K, M)) return 0;
         total += act_slot_bytes(M, probs[a].K);
+    }
+    if (M > 16) {   // the GEMM's per-problem maps of the packed codes
+        for (int i = 0; i < count; ++i)
+            if (!i2s_shape_ok(probs[i].N, probs[i].K, M)) return 0;
+        total += wmap_area(count);
     }
     if (M <= 16) {   // split-K partials of the tensor-core GEMV
         size_t dots = 0, tickets = 0;

@@ -31,11 +31,15 @@
 //              TMEM lanes 32(w%4)..+31 = weight rows of the tile, columns
 //              (w/4)*BN/2..+BN/2-1 = activation rows);
 //   warps 8-11 converters: one thread per weight row of the 128-row tile,
-//              loading the row's 64 packed bytes per stage and writing its
-//              128 bytes of e2m1 operands into the 128B-swizzled K-major
-//              layout, then fencing the writes into the async proxy;
+//              reading the row's 64 packed bytes of a stage from the code
+//              ring and writing its 128 bytes of e2m1 operands into the
+//              128B-swizzled K-major layout, then fencing the writes into
+//              the async proxy;
 //   warp 12    TMA producer of the three digit planes of the activation tile;
-//   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM).
+//   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM);
+//   warp 15    TMA producer of the packed codes: a six-stage ring of 128 rows
+//              x 64 bytes (64-byte swizzle) that runs ahead of the operand
+//              ring, so the converters never wait on global loads.
 // CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
 // cta_group::2 MMAs. A tile is 256 weight rows (128 converted in each CTA's
 // shared memory, 128 accumulator rows in each CTA's TMEM) x BN <= 128
@@ -74,10 +78,12 @@ constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, each ha
 constexpr int kCvtWarps = 4;               // one thread per weight row
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;                // warps 13-14
+constexpr int kCodeWarp = 15;               // TMA producer of the packed codes
 constexpr int kIssuersTc = 2;
-constexpr int kThreadsTc = 480;
+constexpr int kThreadsTc = 512;
 constexpr int kStagesTc = 4;
-constexpr int kCvtPrefetch = 2;             // stages of packed codes each converter keeps in flight
+constexpr int kCodeStages = 6;              // ring of packed-code stages, ahead of the operand ring
+constexpr int kCodeStageBytes = 128 * 64;   // 128 weight rows x 64 packed bytes (256 positions)
 constexpr int kBlockK = 256;                // K positions per stage (one 128-byte row of e2m1)
 constexpr int kTileW = 128;                 // weight rows per CTA (half of the pair's MMA M)
 constexpr int kATileBytes = kTileW * 128;   // 16 KB of e2m1
@@ -90,7 +96,7 @@ constexpr uint32_t kSfbCol0 = 272;
 constexpr uint32_t kSfCols = 16;
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
 static_assert(kStagesTc % kIssuersTc == 0, "ring slots per issuer");
-static_assert(kCvtPrefetch % 2 == 0, "converters take stages in pairs");
+static_assert(kCodeStages % 2 == 0, "converters take stages in pairs");
 static_assert(kSfbCol0 + 3 * kSfCols <= (uint32_t)kTmemCols, "TMEM budget");
 
 struct SmemTc {
@@ -102,13 +108,16 @@ struct SmemTc {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done[kIssuersTc];
+    uint64_t code_full[kCodeStages];    // a stage of packed codes has landed
+    uint64_t code_empty[kCodeStages];   // every converter warp has read it
     uint64_t stage_bar;     // the epilogue threads have staged a tile's column factors
     alignas(16) uint8_t signal[16];   // source (peer) and destination (leader) of the stage-ready copies
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemTcBytes = 1024 + (size_t)kStagesTc * (kATileBytes + kBStageMax) + sizeof(SmemTc);
+constexpr size_t kSmemTcBytes =
+    1024 + (size_t)kStagesTc * (kATileBytes + kBStageMax) + (size_t)kCodeStages * kCodeStageBytes + sizeof(SmemTc);
 
 __device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
     int lo = 0, hi = a.count - 1;
@@ -132,7 +141,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + (size_t)kStagesTc * kATileBytes;
-    SmemTc& S = *reinterpret_cast<SmemTc*>(sB + (size_t)kStagesTc * kBStageMax);
+    uint8_t* sC = sB + (size_t)kStagesTc * kBStageMax;   // packed codes (1024-aligned)
+    SmemTc& S = *reinterpret_cast<SmemTc*>(sC + (size_t)kCodeStages * kCodeStageBytes);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -156,6 +166,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             tc::mbar_init(&S.tmem_empty[b], 2 * kEpiWarps);   // one arrive per epilogue warp of both CTAs
         }
         for (int i = 0; i < kIssuersTc; ++i) tc::mbar_init(&S.mma_done[i], 1);
+        for (int s = 0; s < kCodeStages; ++s) {
+            tc::mbar_init(&S.code_full[s], 1);
+            tc::mbar_init(&S.code_empty[s], kCvtWarps);
+        }
         tc::mbar_init(&S.stage_bar, kEpiWarps * 32);
         S.abort = 0;
         tc::fence_mbar_init();
@@ -237,85 +251,114 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                     if (pending[s]) tc::mbar_wait_drain(&S.full_b[s], pending_phase[s], kWaitLimit / 8);
             }
         }
+    } else if (warp == kCodeWarp) {
+        // ------------------------------------------------------- code producer
+        // per stage: this CTA's 128 weight rows x 64 packed bytes of the tile
+        // (rows past N and bytes past K/4 are zero-filled), from the problem's
+        // map (written by the quantization launch), into a ring that runs
+        // ahead of the operand stages
+        if (lane == 0) {
+            int cs = 0;
+            uint32_t cphase = 0;
+            bool pending[kCodeStages] = {};
+            uint32_t pending_phase[kCodeStages] = {};
+            bool ok = true;
+            int cur_p = -1;
+            for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
+                const int pi = find_problem(a, tile);
+                const TcProb& P = a.p[pi];
+                const CUtensorMap* map = a.wmaps + pi;
+                if (pi != cur_p) {   // first use of this map: order it after the writer's release
+                    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                    cur_p = pi;
+                }
+                const int wt = (tile - P.tile0) / P.n_act_tiles;
+                const int n0 = wt * (2 * kTileW) + (int)rank * kTileW;
+                const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&S.code_empty[cs], cphase ^ 1, abort_flag, kWaitLimit)) { fail(32); ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&S.code_full[cs], kCodeStageBytes);
+                    tc::tma_load_2d(sC + (size_t)cs * kCodeStageBytes, map, kb * 64, n0, &S.code_full[cs]);
+                    pending[cs] = true;
+                    pending_phase[cs] = cphase;
+                    if (++cs == kCodeStages) { cs = 0; cphase ^= 1; }
+                }
+            }
+            if (!ok)
+                for (int s2 = 0; s2 < kCodeStages; ++s2)
+                    if (pending[s2]) tc::mbar_wait_drain(&S.code_full[s2], pending_phase[s2], kWaitLimit / 8);
+        }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
         // ---------------------------------------------------------- converters
         // one thread per weight row: per stage the row's 64 packed bytes (two
-        // 128-position groups) become the 128 bytes of e2m1 operands of the
-        // stage row
+        // 128-position groups), read from the code ring (64-byte swizzle),
+        // become the 128 bytes of e2m1 operands of the stage row
         const int r = tid - kEpiWarps * 32;   // weight row within the CTA's half of the tile
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, cs = 0;
+        uint32_t phase = 0, cphase = 0;
         bool ok = true;
         for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
             const TcProb& P = a.p[find_problem(a, tile)];
-            const int wt = (tile - P.tile0) / P.n_act_tiles;
-            const int n = wt * (2 * kTileW) + (int)rank * kTileW + r;   // this CTA's half of the 256 rows
-            const int groups = P.K / 128;
-            const int KB = (groups + 1) / 2;
-            const bool valid = n < P.N;
-            const uint8_t* src = P.w + (size_t)(valid ? n : 0) * (P.K / 4);
-            auto load = [&](int kb, uint4 (&v)[4]) {
+            const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
+            for (int kb = 0; ok && kb < KB; kb += 2) {
+                // two stages per pass: one proxy fence and one warp sync for both
+                const bool two = kb + 1 < KB;
+                const int stage1 = stage + 1 == kStagesTc ? 0 : stage + 1;
+                const uint32_t phase1 = stage + 1 == kStagesTc ? phase ^ 1 : phase;
+                const int cs1 = cs + 1 == kCodeStages ? 0 : cs + 1;
+                const uint32_t cphase1 = cs + 1 == kCodeStages ? cphase ^ 1 : cphase;
+                // the codes first (their slots free as soon as they are in
+                // registers), then the operand slots; warp-uniform outcomes
+                bool got = tc::mbar_wait(&S.code_full[cs], cphase, abort_flag, kWaitLimit);
+                if (got && two) got = tc::mbar_wait(&S.code_full[cs1], cphase1, abort_flag, kWaitLimit);
+                if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
+                uint4 v[2][4];
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    if (valid && kb < KB && 2 * kb + g < groups) {
-                        const uint4* p = reinterpret_cast<const uint4*>(src + (size_t)kb * 64 + 32 * g);
-                        v[2 * g] = __ldg(p);
-                        v[2 * g + 1] = __ldg(p + 1);
-                    } else {
-                        v[2 * g] = make_uint4(0u, 0u, 0u, 0u);
-                        v[2 * g + 1] = v[2 * g];
+                for (int h = 0; h < 2; ++h) {
+                    const uint8_t* src = sC + (size_t)(h ? cs1 : cs) * kCodeStageBytes + (size_t)r * 64;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[h][c] = (h == 1 && !two) ? make_uint4(0u, 0u, 0u, 0u)
+                                                   : *reinterpret_cast<const uint4*>(src + ((c ^ ((r >> 1) & 3)) << 4));
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&S.code_empty[cs]);
+                    if (two) tc::mbar_arrive(&S.code_empty[cs1]);
+                }
+                got = tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit);
+                if (got && two) got = tc::mbar_wait(&S.empty[stage1], phase1 ^ 1, abort_flag, kWaitLimit);
+                if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
+                    // group g, words 2p and 2p + 1 -> chunk 4g + p of the 128-byte row
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i)) = expand_words_e2m1(v[h][i].x, v[h][i].y);
+                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i + 1)) = expand_words_e2m1(v[h][i].z, v[h][i].w);
                     }
                 }
-            };
-            // the row's packed bytes, kCvtPrefetch stages ahead
-            uint4 buf[kCvtPrefetch][4];
-#pragma unroll
-            for (int j = 0; j < kCvtPrefetch; ++j) load(j, buf[j]);
-            for (int kb0 = 0; ok && kb0 < KB; kb0 += kCvtPrefetch) {
-                // two stages per pass: one proxy fence and one warp sync for both
-#pragma unroll
-                for (int j = 0; j < kCvtPrefetch; j += 2) {
-                    const int kb = kb0 + j;
-                    if (kb >= KB) break;
-                    const bool two = kb + 1 < KB;
-                    const int stage1 = stage + 1 == kStagesTc ? 0 : stage + 1;
-                    const uint32_t phase1 = stage + 1 == kStagesTc ? phase ^ 1 : phase;
-                    // warp-uniform outcome: the warp arrives as one
-                    bool got = tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit);
-                    if (got && two) got = tc::mbar_wait(&S.empty[stage1], phase1 ^ 1, abort_flag, kWaitLimit);
-                    if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                // CTA-scope arrives: a cluster-scope release here would
+                // also wait for this thread's earlier memory operations
+                if (lane == 0) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h == 1 && !two) break;
-                        uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
-                        uint4 v[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) v[i] = buf[j + h][i];
-                        load(kb + h + kCvtPrefetch, buf[j + h]);
-                        // group g, words 2p and 2p + 1 -> chunk 4g + p of the 128-byte row
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i)) = expand_words_e2m1(v[i].x, v[i].y);
-                            *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i + 1)) = expand_words_e2m1(v[i].z, v[i].w);
-                        }
+                        uint64_t* bar = &S.full_a[h ? stage1 : stage];
+                        if (rank == 0 && warp == kEpiWarps) tc::mbar_arrive_expect_tx(bar, 16);
+                        else tc::mbar_arrive(bar);
                     }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    // CTA-scope arrives: a cluster-scope release here would
-                    // also wait for this thread's prefetched loads to land
-                    if (lane == 0) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            if (h == 1 && !two) break;
-                            uint64_t* bar = &S.full_a[h ? stage1 : stage];
-                            if (rank == 0 && warp == kEpiWarps) tc::mbar_arrive_expect_tx(bar, 16);
-                            else tc::mbar_arrive(bar);
-                        }
-                    }
-                    stage = stage1;
-                    phase = phase1;
-                    if (two && ++stage == kStagesTc) { stage = 0; phase ^= 1; }
                 }
+                stage = stage1;
+                phase = phase1;
+                if (two && ++stage == kStagesTc) { stage = 0; phase ^= 1; }
+                cs = cs1;
+                cphase = cphase1;
+                if (two && ++cs == kCodeStages) { cs = 0; cphase ^= 1; }
             }
         }
     } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc && rank == 0) {
@@ -558,6 +601,22 @@ bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_b
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Template of the per-problem maps of the packed codes (written into the
+// workspace by the quantization launch, which replaces address, extents and
+// stride): uint8 2-D, box 64 bytes x 128 rows, 64-byte swizzle.
+bool make_code_map_template(CUtensorMap* map, const void* base) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    std::memset(map, 0, sizeof(*map));
+    cuuint64_t dims[2] = {64u, 128u};
+    cuuint64_t strides[1] = {64u};
+    cuuint32_t box[2] = {64u, 128u};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

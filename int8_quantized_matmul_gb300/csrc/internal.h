@@ -82,7 +82,7 @@ struct TcProb {
 
 struct TcArgs {
     CUtensorMap maps[kTcMaxMaps];
-    const CUtensorMap* wmaps; // GEMV: per-problem weight maps in the workspace (written by the quantize launch)
+    const CUtensorMap* wmaps; // per-problem weight maps in the workspace (written by the quantize launch)
     uint32_t* status;         // workspace status word (timeouts)
     int32_t* dot_base;        // GEMV split-K partial dots (zeroed by the quantize launch)
     uint32_t* ticket_base;    // GEMV split-K chunk counters (zeroed by the quantize launch)
@@ -157,6 +157,7 @@ static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel paramete
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 // rows x row_bytes uint8 matrix, box {128 bytes, box_rows}, 128-byte swizzle
 bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes, int box_rows);
+bool make_code_map_template(CUtensorMap* map, const void* base);   // GEMM: packed codes, box 64 B x 128 rows
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
 int gemm_tc_max_pairs();   // CTA pairs of the GEMM that fit on the device at once
 cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);
