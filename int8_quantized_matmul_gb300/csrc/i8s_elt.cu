@@ -452,6 +452,44 @@ __global__ void __launch_bounds__(kEltThreads) k_im2col_win(const uint8_t* __res
     const int Tn = min(T, OL - t0);
     const int nloc = Tn * C * KW;
     uint8_t* out = dst + (int64_t)t0 * C * KW;
+    if ((KW & 3) == 0 && (nloc & 15) == 0 && ((uintptr_t)out & 15) == 0) {
+        // four output words per thread and step, stored as one 16-byte word:
+        // word w = (tl*C + c)*wpg + j, each from two aligned window words and
+        // a funnel shift; (tl, c, j) advance with carries (no division)
+        const int wpg = KW >> 2;   // words per (t, c) group
+        constexpr int kStep = 4 * kEltThreads;   // words per block step
+        const int dg = kStep / wpg, dj = kStep - dg * wpg;
+        const int dtl = dg / C, dc = dg - dtl * C;
+        int j, c, tl;
+        {
+            const int w0 = 4 * (int)threadIdx.x;
+            const int g0 = w0 / wpg;
+            j = w0 - g0 * wpg;
+            tl = g0 / C;
+            c = g0 - tl * C;
+        }
+        for (int q = threadIdx.x; 16 * q < nloc; q += kEltThreads) {
+            uint32_t v[4];
+            int jj = j, cc = c, tt = tl;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int off = cc * 4 * Wc + shs[cc] + tt * stride + 4 * jj;   // byte offset in the staged words
+                v[e] = __funnelshift_r(wsm[off >> 2], wsm[(off >> 2) + 1], 8 * (off & 3));
+                if (++jj == wpg) {
+                    jj = 0;
+                    if (++cc == C) { cc = 0; ++tt; }
+                }
+            }
+            *reinterpret_cast<uint4*>(out + 16 * q) = make_uint4(v[0], v[1], v[2], v[3]);
+            j += dj;
+            if (j >= wpg) { j -= wpg; ++c; }
+            c += dc;
+            if (c >= C) { c -= C; ++tl; }
+            tl += dtl;
+        }
+        if (blockIdx.x == 0) write_trailer(dst, (int64_t)OL * C * KW, i8s_scale_of(src, (int64_t)C * L));
+        return;
+    }
     if ((KW & 3) == 0) {
         // every output word lies inside one (t, c) group: two aligned window
         // words and a funnel shift (the window buffer has 4 spare bytes)

@@ -170,6 +170,27 @@ def test_im2col_asym(i2s, o, C, L, KW, stride, pad_l, pad_r):
     same_bytes(host(got), ref)
 
 
+# kernels a multiple of 4 wide: output rows go out as 16-byte words where a
+# block's bytes are a multiple of 16 (C*KW*T), word by word otherwise; ragged
+# last blocks, 1..3 words per (t, c) group, both paddings
+GEOMS_WIDE = [
+    (4, 1001, 4, 1, 3, 0),
+    (3, 777, 8, 2, 6, 0),
+    (5, 3000, 12, 3, 9, 0),
+    (16, 4099, 8, 2, 0, 6),
+    (32, 9001, 4, 2, 2, 0),
+]
+
+
+@pytest.mark.parametrize("C,L,KW,stride,pad_l,pad_r", GEOMS_WIDE)
+def test_im2col_asym_wide_kernels(i2s, o, C, L, KW, stride, pad_l, pad_r):
+    _, x = i8s_tensor(o, (C, L), seed=C + L + KW)
+    got, OL = i2s.i8s_im2col_asym(dev(x), C, L, KW, stride, pad_l, pad_r)
+    ref, OL_ref = o.i8s_im2col_asym(x, C, L, KW, stride, pad_l, pad_r)
+    assert OL == OL_ref
+    same_bytes(host(got), ref)
+
+
 def test_im2col_encoder_size(i2s, o):
     # the stage-1 downsampling conv: kernel 4 = 2*stride, causal left pad 2
     C, L, KW, stride = ENC_C, ENC_L, 4, 2
