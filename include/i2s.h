@@ -138,9 +138,9 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
  * ws     device workspace of at least i2s_mul_mat_workspace(M,N,K) bytes,
  *        256-byte aligned; holds the quantized rows, per-row scale and sum
  *        (the counterpart of the sidecar ggml keeps in params->wdata), the
- *        integer partial sums of a K-split launch and a status word. Not
- *        preserved between calls; calls sharing one ws must be ordered on one
- *        stream.
+ *        TMA descriptors of the weight matrix, the integer partial sums of a
+ *        K-split launch and a status word. Not preserved between calls; calls
+ *        sharing one ws must be ordered on one stream.
  * Requirements: K % 128 == 0, M >= 1, N >= 1, M*K < 2^31, N*K/4 < 2^31.
  * M <= 16 runs the decode GEMV (weight-bandwidth bound); larger M runs the
  * GEMM. Both run on the tcgen05 tensor cores and give identical bits.
