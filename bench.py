@@ -161,9 +161,12 @@ class DecodePass:
                 problems.append((weights[layer][i], N, K, xs[ACT_OF[name]], y))
                 host_problems.append((weights[layer][i], N, K, xhs[ACT_OF[name]], yh))
         self.group = i2s.Group(problems, M)
-        # the same projections on the host buffers, one C-ABI call per pass
-        # (i2s_mul_mat_grouped_host: copy up, quantize + GEMV, copy back)
+        # the same projections on the host buffers, one C-ABI call per pass:
+        # staged (i2s_mul_mat_grouped_host: copy up, quantize + GEMV, copy
+        # back) and mapped (the kernels read x and write y in the pinned
+        # host buffers directly)
         self.host_group = i2s.HostGroup(host_problems, M, device=device)
+        self.host_group_mapped = i2s.HostGroup(host_problems, M, device=device, mapped=True)
         self.h2d_bytes = self.x.numel() * 4
         self.d2h_bytes = self.y.numel() * 4
         # algorithmic bytes of one GEMV launch: the 2-bit codes and their scale
@@ -756,33 +759,38 @@ def run_ours(args, rank, world, torch, dist):
     side = torch.cuda.Stream(device=device)
     p_big, p_small = sorted(passes, key=lambda q: -q.M)
 
-    def e2e_step():
+    def e2e_step(mapped):
         done_prev = torch.cuda.Event()
         done_prev.record(stream)
         side.wait_event(done_prev)
-        p_big.host_group()
+        (p_big.host_group_mapped if mapped else p_big.host_group)()
         with torch.cuda.stream(side):
-            p_small.host_group()
+            (p_small.host_group_mapped if mapped else p_small.host_group)()
             small_done = torch.cuda.Event()
             small_done.record(side)
         stream.wait_event(small_done)
 
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), device)
+    def time_e2e(mapped):
+        for _ in range(2):
+            e2e_step(mapped)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step(mapped)
+        e1.record(stream)
+        barrier()
+        return max_over_ranks(torch, dist, e0.elapsed_time(e1), device)
+    e2e_staged_ms = time_e2e(False)
+    e2e_ms = time_e2e(True)
     e2e = {"value": job_rate(world, args.steps, bytes_per_step, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": sum(p.h2d_bytes for p in passes),
            "d2h_bytes_per_step": sum(p.d2h_bytes for p in passes),
-           "api": "i2s_mul_mat_grouped_host (C ABI, pinned host activations and outputs), one call per pass",
-           "note": "the two passes run on two streams, so one pass's copies overlap the other's kernels; "
-                   "steps are serial"}
+           "api": "i2s_mul_mat_grouped_host_ex with I2S_HOST_MAPPED (C ABI, pinned host activations and outputs "
+                  "read and written by the kernels over the host link), one call per pass",
+           "staged": {"value": job_rate(world, args.steps, bytes_per_step, e2e_staged_ms), "unit": "GB/s",
+                      "api": "i2s_mul_mat_grouped_host (the same call with copies to and from a staging area)"},
+           "note": "the two passes run on two streams; steps are serial"}
 
     fused = run_decode_fused(torch, i2s, passes, stream, args.steps)
     prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None

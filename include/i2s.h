@@ -285,6 +285,25 @@ size_t i2s_mul_mat_grouped_host_workspace(const i2s_problem* probs, int count, i
 int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
                              i2s_stream_t stream);
 
+/* As i2s_mul_mat_grouped_host, with flags:
+ *   0                 the staged copies above;
+ *   I2S_HOST_MAPPED   every x and y lies in page-locked host memory that the
+ *                     device reaches at the same address (cudaHostAlloc or
+ *                     cudaMallocHost memory, or memory registered with
+ *                     cudaHostRegisterMapped, under unified addressing): the
+ *                     quantization kernel reads x and the matmul's epilogue
+ *                     writes y over the host link directly, with no staging
+ *                     copies and no staging area (a workspace of
+ *                     i2s_mul_mat_grouped_workspace() bytes is enough). Every
+ *                     byte of every x and y must be so mapped; the call checks
+ *                     the ends of each merged range (cudaPointerGetAttributes)
+ *                     and returns BAD_ARG, with nothing enqueued, if one is not.
+ * Same results, bit for bit, either way. Errors: as i2s_mul_mat_grouped_host,
+ * plus BAD_ARG for unknown flag bits. */
+#define I2S_HOST_MAPPED 1u
+int i2s_mul_mat_grouped_host_ex(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                                unsigned flags, i2s_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Fused decode step: the grouped I2_S matmul for M <= 16 as ONE launch whose
  * prologue quantizes the activations, as the pages' mul_mat quantizes its

@@ -773,16 +773,38 @@ size_t i2s_mul_mat_grouped_host_workspace(const i2s_problem* probs, int count, i
     return host_plan(probs, count, M, pl) == I2S_OK ? pl.total : 0;
 }
 
-int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
-                             i2s_stream_t stream) {
+// True if host address p lies in page-locked memory that the current device
+// reaches at the same address (cudaHostAlloc / cudaMallocHost memory, or
+// memory registered as mapped, under unified addressing).
+static bool mapped_host(uintptr_t p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, (const void*)p) != cudaSuccess) {
+        cudaGetLastError();   // clear the error this query may leave
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost && at.devicePointer == (void*)p;
+}
+
+int i2s_mul_mat_grouped_host_ex(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                                unsigned flags, i2s_stream_t stream) {
+    if (flags & ~(unsigned)I2S_HOST_MAPPED) return I2S_E_BAD_ARG;
     HostPlan pl;
     int r = host_plan(probs, count, M, pl);
     if (r) return r;
     if (!ws) return I2S_E_NULL_PTR;
     if (!aligned256(ws)) return I2S_E_MISALIGNED;
-    if (ws_bytes < pl.total) return I2S_E_WORKSPACE_TOO_SMALL;
+    // mapped: the kernels read x and write y where they are, so only the
+    // grouped workspace is needed
+    if (ws_bytes < ((flags & I2S_HOST_MAPPED) ? pl.grouped : pl.total)) return I2S_E_WORKSPACE_TOO_SMALL;
     r = check_device();
     if (r) return r;
+    if (flags & I2S_HOST_MAPPED) {
+        for (const HostSpan& sp : pl.xs)
+            if (!mapped_host(sp.lo) || !mapped_host(sp.hi - 1)) return I2S_E_BAD_ARG;
+        for (const HostSpan& sp : pl.ys)
+            if (!mapped_host(sp.lo) || !mapped_host(sp.hi - 1)) return I2S_E_BAD_ARG;
+        return grouped_impl(probs, count, M, ws, pl.grouped, stream, 3);
+    }
     char* base = (char*)ws;
     std::vector<i2s_problem> dev(probs, probs + count);
     for (i2s_problem& p : dev) {
@@ -802,6 +824,11 @@ int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, voi
         if (r) return r;
     }
     return I2S_OK;
+}
+
+int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
+                             i2s_stream_t stream) {
+    return i2s_mul_mat_grouped_host_ex(probs, count, M, ws, ws_bytes, 0u, stream);
 }
 
 size_t i8s_ws_f32_offset(void) { return kHeader; }

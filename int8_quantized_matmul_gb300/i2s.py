@@ -68,6 +68,7 @@ _SIGS = {
     "i2s_mul_mat_grouped_run": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_host_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
     "i2s_mul_mat_grouped_host": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
+    "i2s_mul_mat_grouped_host_ex": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, ctypes.c_uint, _p]),
     "i2s_mul_mat_grouped_fused_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
     "i2s_mul_mat_grouped_fused_init": (_int, [_p, _sz, _p]),
     "i2s_mul_mat_grouped_fused": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
@@ -314,15 +315,22 @@ def _host_problems(problems: Sequence):
     return arr
 
 
+HOST_MAPPED = 1   # I2S_HOST_MAPPED
+
+
 class HostGroup:
     """A fixed list of projections [(w, N, K, x, y), ...] whose activations x
     and outputs y are host (CPU, ideally pinned) tensors and whose weights w
-    are on the device; each call copies x up, runs the grouped matmul and
-    copies y back, on torch's current stream (i2s_mul_mat_grouped_host)."""
+    are on the device; each call runs the grouped matmul on torch's current
+    stream. By default x is copied up and y back around it
+    (i2s_mul_mat_grouped_host); with mapped=True (every x and y in pinned,
+    device-mapped memory, as torch's pin_memory() gives) the kernels read x
+    and write y over the host link directly (I2S_HOST_MAPPED)."""
 
-    def __init__(self, problems: Sequence, M: int, device=None, ws=None):
+    def __init__(self, problems: Sequence, M: int, device=None, ws=None, mapped: bool = False):
         self.problems = list(problems)
         self.M = int(M)
+        self.flags = HOST_MAPPED if mapped else 0
         self.arr = _host_problems(self.problems)
         need = int(_L.i2s_mul_mat_grouped_host_workspace(self.arr, len(self.problems), self.M))
         if need == 0:
@@ -330,9 +338,9 @@ class HostGroup:
         self.ws = ws if ws is not None else _ws(need, device if device is not None else self.problems[0][0].device)
 
     def __call__(self):
-        _check("i2s_mul_mat_grouped_host",
-               _L.i2s_mul_mat_grouped_host(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
-                                           _stream()))
+        _check("i2s_mul_mat_grouped_host_ex",
+               _L.i2s_mul_mat_grouped_host_ex(self.arr, len(self.problems), self.M, _dptr(self.ws), self.ws.numel(),
+                                              self.flags, _stream()))
 
 
 def i2s_mul_mat_grouped_host(problems: Sequence, M: int, ws=None):

@@ -89,3 +89,32 @@ def test_host_call_repeated_with_new_inputs(i2s, o):
         for packed, N, K, x, y in keep:
             same_bits(y.numpy(), o.i2s_mul_mat(packed, N, K, x.numpy(), nth=8))
     assert i2s.read_status(g.ws) == 0
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_host_call_mapped_decoder_layer(i2s, o, M):
+    # I2S_HOST_MAPPED: pinned (device-mapped) host buffers read and written by
+    # the kernels directly, no staging copies; same bits as the oracle
+    probs, keep = layer(o, M, seed=M + 50, pinned=True)
+    g = i2s.HostGroup(probs, M, mapped=True)
+    for _ in range(2):
+        for _, _, _, _, y in keep:
+            y.fill_(float("nan"))
+        g()
+        torch.cuda.synchronize()
+        assert i2s.read_status(g.ws) == 0
+        for packed, N, K, x, y in keep:
+            same_bits(y.numpy(), o.i2s_mul_mat(packed, N, K, x.numpy(), nth=8))
+
+
+def test_host_call_mapped_rejects_pageable_buffers(i2s, o):
+    # the mapped mode checks its ranges before anything is enqueued: pageable
+    # buffers are refused, and the outputs stay untouched
+    probs, keep = layer(o, 8, seed=77, pinned=False)
+    g = i2s.HostGroup(probs, 8, mapped=True)
+    with pytest.raises(i2s.I2SError) as e:
+        g()
+    assert e.value.status == -8   # I2S_E_BAD_ARG
+    torch.cuda.synchronize()
+    for _, _, _, _, y in keep:
+        assert torch.isnan(y).all()
