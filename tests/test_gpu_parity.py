@@ -368,6 +368,18 @@ def test_i2s_gemm(i2s, o, M, N, K):
     same_bits(got, want)
 
 
+@pytest.mark.parametrize("K", [128, 384, 1152])
+@pytest.mark.parametrize("N", [1, 2, 100, 129])
+@pytest.mark.parametrize("M", [17, 100])
+def test_i2s_gemm_page_grid(i2s, o, K, N, M):
+    # the page's small K x N grid on the tensor-core GEMM: fewer weight rows
+    # than one tile (the code ring's rows past N arrive as zeros), K of one,
+    # three and nine 128-position groups (an odd count leaves half of the last
+    # 256-position stage past K)
+    got, want = run_i2s(i2s, o, N, K, M, seed=K * 17 + N * 3 + M)
+    same_bits(got, want)
+
+
 @pytest.mark.parametrize("M", [1, 5, 16])
 def test_i2s_gemm_small_m(i2s, o, M):
     got, want = run_i2s(i2s, o, 300, 1152, M, seed=M + 11, path=2)
