@@ -100,6 +100,32 @@ __device__ __forceinline__ int stage_window(const uint8_t* row, int64_t L, int64
     return sh;
 }
 
+// As stage_window, with 16-byte loads: word i of win (16-byte aligned) holds
+// the row bytes from pos0 - sh + 4i, where sh = the misalignment of row + pos0
+// modulo 16. Every thread has its loads in flight before any store. Returns sh.
+__device__ __forceinline__ int stage_window16(const uint8_t* row, int64_t L, int64_t pos0, int nbytes, uint32_t* win,
+                                              int tid, int nthreads) {
+    const int sh = (int)(((uintptr_t)row + (uintptr_t)pos0) & 15u);
+    const int nq = (sh + nbytes + 15) >> 4;
+    auto quad = [&](int i) {
+        const int64_t g = pos0 - sh + 16 * (int64_t)i;   // row position of the quad's first byte
+        if (g >= 0 && g + 16 <= L) return *reinterpret_cast<const uint4*>(row + g);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        for (int e = 0; e < 16; ++e)
+            if (g + e >= 0 && g + e < L) w[e >> 2] |= (uint32_t)row[g + e] << (8 * (e & 3));
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    };
+    for (int i0 = tid; i0 < nq; i0 += 4 * nthreads) {
+        uint4 v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = i0 + e * nthreads < nq ? quad(i0 + e * nthreads) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (i0 + e * nthreads < nq) reinterpret_cast<uint4*>(win)[i0 + e * nthreads] = v[e];
+    }
+    return sh;
+}
+
 // ---------------------------------------------------------------- add_scaled
 
 __device__ __forceinline__ float add_one(int8_t qa, int8_t qb, float sa, float sb) {
@@ -658,12 +684,14 @@ template <bool kQuant>
 __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned int* amax_bits,
                                                        uint8_t* __restrict__ dst) {
     constexpr int kWinBytes = kDw1T + 16;   // the block's outputs plus up to 8 taps, rounded
-    __shared__ uint32_t win32[(kWinBytes + 3) / 4 + 2];
+    __shared__ __align__(16) uint32_t win32[(kWinBytes + 15 + 15) / 16 * 4 + 4];
     const int c = blockIdx.y;
     const int t0 = blockIdx.x * kDw1T;
     const int p0 = t0 - d.pad_l;
     const uint8_t* row = d.x + (int64_t)c * d.L;
-    const int sh = stage_window(row, d.L, p0, kWinBytes, win32, threadIdx.x, kEltThreads);
+    // window byte b sits at byte b + sh16 of the staged words
+    const int sh16 = stage_window16(row, d.L, p0, kWinBytes, win32, threadIdx.x, kEltThreads);
+    const int sh = sh16 & 3, qsh = sh16 >> 2;
     const int8_t* wt = reinterpret_cast<const int8_t*>(d.w) + (int64_t)c * d.KW;
     uint32_t tw[2] = {0u, 0u};
     for (int k = 0; k < d.KW; ++k) tw[k >> 2] |= (uint32_t)(uint8_t)wt[k] << (8 * (k & 3));
@@ -692,7 +720,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     for (int chunk = 0; chunk < kDw1Chunks; ++chunk) {
         const int tl0 = kDw1Out * (threadIdx.x + chunk * kEltThreads);
         // window bytes tl0 .. tl0+15: five staged words shifted by sh
-        const int q0 = tl0 >> 2;
+        const int q0 = (tl0 >> 2) + qsh;
         uint32_t xw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) xw[i] = __funnelshift_r(win32[q0 + i], win32[q0 + i + 1], 8 * sh);
