@@ -292,18 +292,18 @@ __device__ __forceinline__ void load_row16(const uint8_t* p, uint32_t (&w)[4 * V
     }
 }
 
+// The row's sum of squares (one 4-way int8 dot product per word, exact) and
+// its largest |q|.
 template <int V>
 __device__ __forceinline__ float row_factor16(const uint32_t (&w)[4 * V], float s, float eps, int& qmax) {
     int ssq = 0;
     qmax = 0;
 #pragma unroll
-    for (int i = 0; i < 4 * V; ++i)
+    for (int i = 0; i < 4 * V; ++i) {
+        ssq = __dp4a((int)w[i], (int)w[i], ssq);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int b = byte_of(w[i], e);
-            ssq += b * b;
-            qmax = max(qmax, abs(b));
-        }
+        for (int e = 0; e < 4; ++e) qmax = max(qmax, abs((int)byte_of(w[i], e)));
+    }
     return rms_factor(ssq, 16 * V, s, eps);
 }
 
