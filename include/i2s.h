@@ -206,14 +206,21 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
  * clears what must start at zero (the status word, the split-K partial sums
  * and their counters) in its first launch, so callers never clear it.
  * Device waits that run out are recorded in the array's status word, which
- * this call cannot return; the return value reports validation and launch
- * errors only.
+ * this call cannot return (its return value reports validation and launch
+ * errors only); i2s_noalloc_read_status below reads it.
  * Errors: BAD_SHAPE, NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL,
  * UNSUPPORTED_DEVICE, CUDA.
  * ------------------------------------------------------------------------- */
 #define I2S_NOALLOC_SCRATCH_BYTES 4194304
 int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,
                         i2s_stream_t stream);
+
+/* The no-alloc counterpart of i2s_read_status, for the current device:
+ * synchronizes `stream`, reads the status word of the library's scratch array,
+ * clears it, and returns I2S_OK or I2S_E_DEVICE_TIMEOUT. It sets the device up
+ * as a first i2s_mul_mat_noalloc call would (so it may run before any).
+ * Errors: UNSUPPORTED_DEVICE, CUDA. */
+int i2s_noalloc_read_status(i2s_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Grouped I2_S matmul: several independent projections with the same number of

@@ -162,5 +162,17 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     return I2S_OK;
 }
 
+int i2s_noalloc_read_status(i2s_stream_t stream) {
+    NoAllocDev* d = nullptr;
+    int r = noalloc_setup(d);
+    if (r) return r;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return I2S_E_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->scratch, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return I2S_E_CUDA;
+    if (word == 0) return I2S_OK;
+    if (cudaMemset(d->scratch, 0, 4) != cudaSuccess) return I2S_E_CUDA;
+    return I2S_E_DEVICE_TIMEOUT;
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

@@ -62,6 +62,7 @@ _SIGS = {
     "i2s_mul_mat": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "i2s_mul_mat_ex": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, ctypes.POINTER(i2s_config), _p]),
     "i2s_mul_mat_noalloc": (_int, [_p, _i64, _i64, _p, _i64, _p, _p]),
+    "i2s_noalloc_read_status": (_int, [_p]),
     "i2s_mul_mat_grouped_workspace": (_sz, [ctypes.POINTER(i2s_problem), _int, _i64]),
     "i2s_mul_mat_grouped": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
     "i2s_mul_mat_grouped_quantize": (_int, [ctypes.POINTER(i2s_problem), _int, _i64, _p, _sz, _p]),
@@ -588,6 +589,10 @@ class W8A8Group:
 
 def read_status(ws) -> int:
     return int(_L.i2s_read_status(_dptr(ws), _stream()))
+
+
+def noalloc_read_status() -> int:
+    return int(_L.i2s_noalloc_read_status(_stream()))
 
 
 def device_supported() -> int:

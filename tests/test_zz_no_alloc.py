@@ -60,6 +60,8 @@ def bits(t):
 def noalloc(i2s, w, N, K, x):
     y = torch.full((x.shape[0], N), float("nan"), dtype=torch.float32, device="cuda")
     i2s.i2s_mul_mat_noalloc(w, N, K, x, y)
+    # no bounded device wait of the call ran out
+    assert i2s.noalloc_read_status() == 0
     return y
 
 
