@@ -34,7 +34,10 @@ __global__ void __launch_bounds__(256) k_absmax(const float* __restrict__ y, int
 }
 
 // y (F32, n) -> I8_S bytes at dst: int8 payload, zero padding to 32 bytes, the
-// F32 scale and 28 zero bytes.
+// F32 scale and 28 zero bytes. Each thread keeps U float4 loads in flight (a
+// warp's loads cover 512 contiguous bytes per step); the host picks U so that
+// one wave of resident CTAs covers the tensor.
+template <int U>
 __global__ void __launch_bounds__(256) k_requant(const float* __restrict__ y, int64_t n,
                                                  const unsigned int* __restrict__ amax_bits, uint8_t* dst) {
     pdl_wait();   // y and the folded amax come from the launch before
@@ -44,16 +47,15 @@ __global__ void __launch_bounds__(256) k_requant(const float* __restrict__ y, in
     const int64_t n4 = n / 4;
     const float4* y4 = reinterpret_cast<const float4*>(y);
     uint32_t* d4 = reinterpret_cast<uint32_t*>(dst);
-    // four float4 loads in flight per thread
-    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < n4; i0 += 4 * stride) {
-        float4 v[4];
+    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < n4; i0 += U * stride) {
+        float4 v[U];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < U; ++e) {
             const int64_t i = i0 + e * stride;
             v[e] = i < n4 ? y4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < U; ++e) {
             const int64_t i = i0 + e * stride;
             if (i < n4)
                 d4[i] = (uint32_t)(quantize_one(v[e].x, inv) & 0xff) | ((uint32_t)(quantize_one(v[e].y, inv) & 0xff) << 8) |
@@ -87,8 +89,20 @@ cudaError_t launch_absmax(const float* y, int64_t n, unsigned int* amax_bits, cu
 }
 
 cudaError_t launch_requant(const float* y, int64_t n, const unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
-    // four float4 per thread and step; a programmatic dependent of the launch before
-    return launch_pdl(k_requant, dim3(grid_for(n / 16)), dim3(256), 0, s, y, n, amax_bits, dst);
+    // the fewest float4 loads in flight per thread (at most 8) that let one
+    // wave of CTAs (eight of 256 threads per SM) cover the tensor; a
+    // programmatic dependent of the launch before
+    const int64_t n4 = n / 4, wave = (int64_t)device_sm_count() * 8 * 256;
+    int u = 1;
+    while (u < 8 && n4 > wave * u) u *= 2;
+    const int64_t g = (n4 + 256 * u - 1) / (256 * u), cap = wave / 256;
+    const dim3 grid((unsigned)(g < 1 ? 1 : (g > cap ? cap : g)));
+    switch (u) {
+        case 1: return launch_pdl(k_requant<1>, grid, dim3(256), 0, s, y, n, amax_bits, dst);
+        case 2: return launch_pdl(k_requant<2>, grid, dim3(256), 0, s, y, n, amax_bits, dst);
+        case 4: return launch_pdl(k_requant<4>, grid, dim3(256), 0, s, y, n, amax_bits, dst);
+        default: return launch_pdl(k_requant<8>, grid, dim3(256), 0, s, y, n, amax_bits, dst);
+    }
 }
 
 }  // namespace i2s

@@ -481,42 +481,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
 }
 
 // int8 -> f16 rows of the weights (N x K) and activations (M x K, zero rows up
-// to rows_pad), four 16-value loads in flight per thread; also clears the
-// status and amax words and the split-tile tickets and masks.
-__device__ __forceinline__ void i8x16_to_f16(const uint4 v, uint4& o0, uint4& o1) {
-    i8x4_to_f16x4(v.x, o0.x, o0.y);
-    i8x4_to_f16x4(v.y, o0.z, o0.w);
-    i8x4_to_f16x4(v.z, o1.x, o1.y);
-    i8x4_to_f16x4(v.w, o1.z, o1.w);
+// to rows_pad); also clears the status and amax words and the split-tile
+// tickets and masks. One unit is 8 values: 8 bytes in, 16 bytes out, so a
+// warp's loads cover 256 contiguous bytes and its stores 512. Units [0, nw)
+// are the weights, [nw, nw + nx_pad) the activations, those past nw + nx the
+// zero rows (a zero byte converts to +0). Each thread keeps U units' loads in
+// flight; the host picks U so that one wave of resident CTAs covers the call.
+__device__ __forceinline__ void i8x8_to_f16(const uint2 v, uint4& o) {
+    i8x4_to_f16x4(v.x, o.x, o.y);
+    i8x4_to_f16x4(v.y, o.z, o.w);
 }
 
-// dst[0 .. n_pad) (in units of 16 values) from src[0 .. n): values past n are zeros
-__device__ __forceinline__ void convert_rows(const uint4* __restrict__ src, unsigned long long n,
-                                             unsigned long long n_pad, uint4* __restrict__ dst, unsigned long long t0,
-                                             unsigned long long stride) {
-    for (unsigned long long i0 = t0; i0 < n_pad; i0 += 4 * stride) {
-        uint4 v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const unsigned long long i = i0 + e * stride;
-            v[e] = i < n ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const unsigned long long i = i0 + e * stride;
-            if (i >= n_pad) break;
-            uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-            if (i < n) i8x16_to_f16(v[e], o0, o1);
-            dst[2 * i] = o0;
-            dst[2 * i + 1] = o1;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w, unsigned long long w16,
-                                                    __half* __restrict__ wf, const int8_t* __restrict__ x,
-                                                    unsigned long long x16, unsigned long long x16_pad,
-                                                    __half* __restrict__ xf, uint4* zero, unsigned long long zero_16,
+template <int U>
+__global__ void __launch_bounds__(256) k_i8s_to_f16(const uint2* __restrict__ w, unsigned long long nw,
+                                                    uint4* __restrict__ wf, const uint2* __restrict__ x,
+                                                    unsigned long long nx, unsigned long long nx_pad,
+                                                    uint4* __restrict__ xf, uint4* zero, unsigned long long zero_16,
                                                     uint32_t* status, unsigned int* amax_bits) {
     const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
     const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
@@ -526,8 +506,26 @@ __global__ void __launch_bounds__(256) k_i8s_to_f16(const int8_t* __restrict__ w
         *amax_bits = 0u;
     }
     for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    convert_rows(reinterpret_cast<const uint4*>(w), w16, w16, reinterpret_cast<uint4*>(wf), t0, stride);
-    convert_rows(reinterpret_cast<const uint4*>(x), x16, x16_pad, reinterpret_cast<uint4*>(xf), t0, stride);
+    const unsigned long long total = nw + nx_pad;
+    for (unsigned long long i0 = t0; i0 < total; i0 += U * stride) {
+        uint2 v[U];
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+            const unsigned long long i = i0 + e * stride;
+            v[e] = make_uint2(0u, 0u);
+            if (i < nw) v[e] = __ldg(w + i);
+            else if (i - nw < nx) v[e] = __ldg(x + (i - nw));
+        }
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+            const unsigned long long i = i0 + e * stride;
+            if (i >= total) break;
+            uint4 o;
+            i8x8_to_f16(v[e], o);
+            if (i < nw) wf[i] = o;
+            else xf[i - nw] = o;
+        }
+    }
 }
 
 // K that is not a multiple of 64: src rows of K int8 (not 16-byte aligned)
@@ -583,6 +581,18 @@ int prepass_grid(unsigned long long n16) {
     return (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
 }
 
+// Units in flight per thread for `units` conversion units: the fewest that let
+// one wave of CTAs (eight of 256 threads per SM) cover the call, at most 16.
+int prepass_units(unsigned long long units, int& grid) {
+    const unsigned long long wave = (unsigned long long)device_sm_count() * 8 * 256;
+    int u = 1;
+    while (u < 16 && units > wave * (unsigned long long)u) u *= 2;
+    unsigned long long g = (units + 256ull * u - 1) / (256ull * u);
+    const unsigned long long cap = wave / 256;
+    grid = (int)(g < 1 ? 1 : (g > cap ? cap : g));
+    return u;
+}
+
 }  // namespace
 
 cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
@@ -595,11 +605,23 @@ cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* 
                           xf, K, Kp, static_cast<uint4*>(zero), (unsigned long long)(zero_bytes / 16), status,
                           amax_bits);
     }
-    const unsigned long long w16 = (unsigned long long)N * K / 16;
-    const unsigned long long x16 = (unsigned long long)M * K / 16, x16p = (unsigned long long)rows_pad * K / 16;
-    const unsigned long long n = w16 > x16p ? w16 : x16p;
-    return launch_pdl(k_i8s_to_f16, dim3(prepass_grid(n)), dim3(256), 0, s, w, w16, wf, x, x16, x16p, xf,
-                      static_cast<uint4*>(zero), (unsigned long long)(zero_bytes / 16), status, amax_bits);
+    const unsigned long long nw = w ? (unsigned long long)N * K / 8 : 0ull;
+    const unsigned long long nx = (unsigned long long)M * K / 8, nxp = (unsigned long long)rows_pad * K / 8;
+    int grid = 1;
+    const int u = prepass_units(nw + nxp, grid);
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint2*>(w), nw,
+                          reinterpret_cast<uint4*>(wf), reinterpret_cast<const uint2*>(x), nx, nxp,
+                          reinterpret_cast<uint4*>(xf), static_cast<uint4*>(zero),
+                          (unsigned long long)(zero_bytes / 16), status, amax_bits);
+    };
+    switch (u) {
+        case 1: return go(k_i8s_to_f16<1>);
+        case 2: return go(k_i8s_to_f16<2>);
+        case 4: return go(k_i8s_to_f16<4>);
+        case 8: return go(k_i8s_to_f16<8>);
+        default: return go(k_i8s_to_f16<16>);
+    }
 }
 
 cudaError_t launch_i8_to_f16_rows(const int8_t* src, int64_t rows, int64_t K, __half* dst, cudaStream_t s) {
