@@ -13,7 +13,7 @@
 // Every chunk gets a fresh accumulator, which the epilogue warps drain into an
 // int32 running sum kept in tensor memory.
 //
-// Operands: a pre-pass (k_i8s_to_f16) converts the int8 weights and
+// Operands: a pre-pass (k_i8s_to_f16, i8s.cu) converts the int8 weights and
 // activations to f16 rows once per call. The kernel runs on CTA pairs (clusters
 // of two CTAs on two SMs) driving cta_group::2 MMAs: a tile is 256 output
 // features (the A operand; 128 rows in each CTA's shared memory and TMEM) x 160
@@ -136,20 +136,6 @@ __device__ __forceinline__ Seg8 seg8_at(const I8sTcArgs& a, int u, int u_hi) {
     g.wt = g.tile / a.n_at;
     g.at = g.tile - g.wt * a.n_at;
     return g;
-}
-
-// Four int8 (one 32-bit word) -> two f16x2 words, exactly: byte b becomes the
-// f16 bit pattern 0x6400 | (b ^ 0x80) = 1152 + x (f16 integers are exact up to
-// 2048), and one f16 subtraction of 1152 leaves x.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t t0 = __byte_perm(w, 0x64u, 0x4140) ^ 0x00800080u;   // bytes 0, 1
-    const uint32_t t1 = __byte_perm(w, 0x64u, 0x4342) ^ 0x00800080u;   // bytes 2, 3
-    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480),
-                                        __ushort_as_half((unsigned short)0x6480));   // 1152
-    const __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&t0), bias);
-    const __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&t1), bias);
-    lo = *reinterpret_cast<const uint32_t*>(&h0);
-    hi = *reinterpret_cast<const uint32_t*>(&h1);
 }
 
 template <int BM>
@@ -480,156 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
     }
 }
 
-// int8 -> f16 rows of the weights (N x K) and activations (M x K, zero rows up
-// to rows_pad); also clears the status and amax words and the split-tile
-// tickets and masks. One unit is 8 values: 8 bytes in, 16 bytes out, so a
-// warp's loads cover 256 contiguous bytes and its stores 512. Units [0, nw)
-// are the weights, [nw, nw + nx_pad) the activations, those past nw + nx the
-// zero rows (a zero byte converts to +0). Each thread keeps U units' loads in
-// flight; the host picks U so that one wave of resident CTAs covers the call.
-__device__ __forceinline__ void i8x8_to_f16(const uint2 v, uint4& o) {
-    i8x4_to_f16x4(v.x, o.x, o.y);
-    i8x4_to_f16x4(v.y, o.z, o.w);
-}
-
-template <int U>
-__global__ void __launch_bounds__(256) k_i8s_to_f16(const uint2* __restrict__ w, unsigned long long nw,
-                                                    uint4* __restrict__ wf, const uint2* __restrict__ x,
-                                                    unsigned long long nx, unsigned long long nx_pad,
-                                                    uint4* __restrict__ xf, uint4* zero, unsigned long long zero_16,
-                                                    uint32_t* status, unsigned int* amax_bits) {
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-    const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
-    pdl_wait();   // the launch before may still use this workspace (or produce x)
-    if (t0 == 0) {
-        *status = 0u;
-        *amax_bits = 0u;
-    }
-    for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    const unsigned long long total = nw + nx_pad;
-    for (unsigned long long i0 = t0; i0 < total; i0 += U * stride) {
-        uint2 v[U];
-#pragma unroll
-        for (int e = 0; e < U; ++e) {
-            const unsigned long long i = i0 + e * stride;
-            v[e] = make_uint2(0u, 0u);
-            if (i < nw) v[e] = __ldg(w + i);
-            else if (i - nw < nx) v[e] = __ldg(x + (i - nw));
-        }
-#pragma unroll
-        for (int e = 0; e < U; ++e) {
-            const unsigned long long i = i0 + e * stride;
-            if (i >= total) break;
-            uint4 o;
-            i8x8_to_f16(v[e], o);
-            if (i < nw) wf[i] = o;
-            else xf[i - nw] = o;
-        }
-    }
-}
-
-// K that is not a multiple of 64: src rows of K int8 (not 16-byte aligned)
-// -> dst rows of Kp f16, positions K..Kp-1 and rows rows_in..rows_out-1 zero.
-// Zero products add nothing, so the padded contraction is the same integer
-// sum. One 16-byte output word (8 values) per thread and step, byte loads.
-__device__ __forceinline__ void convert_rows_ragged(const int8_t* __restrict__ src, int rows_in, int rows_out, int K,
-                                                    int Kp, uint4* __restrict__ dst, unsigned long long t0,
-                                                    unsigned long long stride) {
-    const unsigned long long words_per_row = (unsigned long long)(Kp / 8);
-    const unsigned long long n = (unsigned long long)rows_out * words_per_row;
-    for (unsigned long long i = t0; i < n; i += stride) {
-        const int r = (int)(i / words_per_row);
-        const int k0 = (int)(i - (unsigned long long)r * words_per_row) * 8;
-        __align__(16) __half h[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int k = k0 + j;
-            const int v = (r < rows_in && k < K) ? (int)src[(size_t)r * K + k] : 0;
-            h[j] = __int2half_rn(v);
-        }
-        dst[i] = *reinterpret_cast<const uint4*>(h);
-    }
-}
-
-__global__ void __launch_bounds__(256) k_i8s_to_f16_ragged(const int8_t* __restrict__ w, int N, __half* __restrict__ wf,
-                                                           const int8_t* __restrict__ x, int M, int rows_pad,
-                                                           __half* __restrict__ xf, int K, int Kp, uint4* zero,
-                                                           unsigned long long zero_16, uint32_t* status,
-                                                           unsigned int* amax_bits) {
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-    const unsigned long long t0 = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
-    pdl_wait();   // the launch before may still use this workspace (or produce x)
-    if (t0 == 0) {
-        *status = 0u;
-        *amax_bits = 0u;
-    }
-    for (unsigned long long i = t0; i < zero_16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (w) convert_rows_ragged(w, N, N, K, Kp, reinterpret_cast<uint4*>(wf), t0, stride);
-    convert_rows_ragged(x, M, rows_pad, K, Kp, reinterpret_cast<uint4*>(xf), t0, stride);
-}
-
-__global__ void __launch_bounds__(256) k_i8_to_f16_rows(const int8_t* __restrict__ src, int rows, int K, int Kp,
-                                                        __half* __restrict__ dst) {
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-    convert_rows_ragged(src, rows, rows, K, Kp, reinterpret_cast<uint4*>(dst),
-                        blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x, stride);
-}
-
-int prepass_grid(unsigned long long n16) {
-    const unsigned long long want = (n16 + 1023) / 1024;
-    const int cap = device_sm_count() * 8;
-    return (int)(want < (unsigned long long)cap ? (want < 1 ? 1 : want) : cap);
-}
-
-// Units in flight per thread for `units` conversion units: the fewest that let
-// one wave of CTAs (eight of 256 threads per SM) cover the call, at most 16.
-int prepass_units(unsigned long long units, int& grid) {
-    const unsigned long long wave = (unsigned long long)device_sm_count() * 8 * 256;
-    int u = 1;
-    while (u < 16 && units > wave * (unsigned long long)u) u *= 2;
-    unsigned long long g = (units + 256ull * u - 1) / (256ull * u);
-    const unsigned long long cap = wave / 256;
-    grid = (int)(g < 1 ? 1 : (g > cap ? cap : g));
-    return u;
-}
-
 }  // namespace
-
-cudaError_t launch_i8s_to_f16(const int8_t* w, int N, __half* wf, const int8_t* x, int M, int rows_pad, int K,
-                              __half* xf, void* zero, size_t zero_bytes, uint32_t* status, unsigned int* amax_bits,
-                              cudaStream_t s) {
-    const int Kp = (int)i8s_kpad(K);
-    if (Kp != K) {
-        const unsigned long long n8 = (unsigned long long)(N > rows_pad ? N : rows_pad) * (unsigned long long)(Kp / 8);
-        return launch_pdl(k_i8s_to_f16_ragged, dim3(prepass_grid(n8 / 4)), dim3(256), 0, s, w, N, wf, x, M, rows_pad,
-                          xf, K, Kp, static_cast<uint4*>(zero), (unsigned long long)(zero_bytes / 16), status,
-                          amax_bits);
-    }
-    const unsigned long long nw = w ? (unsigned long long)N * K / 8 : 0ull;
-    const unsigned long long nx = (unsigned long long)M * K / 8, nxp = (unsigned long long)rows_pad * K / 8;
-    int grid = 1;
-    const int u = prepass_units(nw + nxp, grid);
-    auto go = [&](auto kern) {
-        return launch_pdl(kern, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint2*>(w), nw,
-                          reinterpret_cast<uint4*>(wf), reinterpret_cast<const uint2*>(x), nx, nxp,
-                          reinterpret_cast<uint4*>(xf), static_cast<uint4*>(zero),
-                          (unsigned long long)(zero_bytes / 16), status, amax_bits);
-    };
-    switch (u) {
-        case 1: return go(k_i8s_to_f16<1>);
-        case 2: return go(k_i8s_to_f16<2>);
-        case 4: return go(k_i8s_to_f16<4>);
-        case 8: return go(k_i8s_to_f16<8>);
-        default: return go(k_i8s_to_f16<16>);
-    }
-}
-
-cudaError_t launch_i8_to_f16_rows(const int8_t* src, int64_t rows, int64_t K, __half* dst, cudaStream_t s) {
-    const int Kp = (int)i8s_kpad(K);
-    k_i8_to_f16_rows<<<prepass_grid((unsigned long long)rows * (Kp / 8) / 4), 256, 0, s>>>(src, (int)rows, (int)K, Kp,
-                                                                                          dst);
-    return cudaGetLastError();
-}
 
 // Per device: 1 + the number of CTA pairs that can be resident at once (0:
 // not yet configured). Clusters must fit inside a GPC, so on a part whose
