@@ -398,6 +398,34 @@ def run_decode_fused(torch, i2s, passes, stream, steps):
             "gpu_launches_per_step": len(passes), "status": status}
 
 
+def run_decode_per_projection(torch, i2s, passes, weights, device, steps=10):
+    """Each projection of the first layer as a call of its own with L2 flushed
+    before it (cold L2): the quantization and GEMV launches together, and the
+    GEMV launch alone after a separate quantization, at M = 1 and M = 8.
+    Small projections are launch-bound; the headline streams all 196 at once."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for p in passes:
+        per = {}
+        for i, (name, N, K) in enumerate(PROJ):
+            prob = p.group.problems[i]
+            g = i2s.Group([prob], p.M)
+            both = _timed_median(torch, g, steps, flush)
+            g.quantize()
+            gemv = _timed_median(torch, g.run, steps, flush)
+            wbytes = N * K // 4
+            per[name] = {"N": N, "K": K, "ms": both, "gemv_ms": gemv,
+                         "weight_gbs": wbytes / (both * 1e-3) / 1e9, "gemv_weight_gbs": wbytes / (gemv * 1e-3) / 1e9}
+        out[str(p.M)] = per
+    del flush
+    return {"workload": "each projection of one decoder layer alone, L2 flushed before every call",
+            "timing": f"median of {steps} calls, CUDA events around each (the flush, a 256 MB write, "
+                      "leaves L2 dirty)",
+            "note": "one projection per call is bound by latency (launch, cold map and operand fetches, "
+                    "one tile row per CTA), not by its bytes; the decode pass groups all 196",
+            "per_m": out}
+
+
 def _timed_median(torch, fn, steps, flush):
     """Median CUDA-event time (ms) of fn() over `steps` calls, each after an L2
     flush (a write larger than L2) outside the timed region."""
@@ -793,6 +821,7 @@ def run_ours(args, rank, world, torch, dist):
            "note": "the two passes run on two streams; steps are serial"}
 
     fused = run_decode_fused(torch, i2s, passes, stream, args.steps)
+    per_projection = run_decode_per_projection(torch, i2s, passes, weights, device)
     prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None
     encoder = run_encoder_fc(torch, i2s, device, peaks) if not args.no_prefill else None
     eltwise = run_encoder_eltwise(torch, i2s, device, peaks) if not args.no_prefill else None
@@ -811,6 +840,7 @@ def run_ours(args, rank, world, torch, dist):
         "gpu_launches": 2 * len(passes) * args.steps,
         "roofline": {"bound": "hbm", "kernel": "k_i2s_gemv_tc", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_gemv_traffic(),
+                     "frac_of_8tbs_spec": achieved / 8000.0,
                      "algorithmic_bytes_per_launch": b2b_avg_bytes,
                      "launch_ms": b2b_avg_ms,
                      "timing": f"median over {args.steps} runs of {B2B} GEMV launches in a row per M (each a "
@@ -822,6 +852,7 @@ def run_ours(args, rank, world, torch, dist):
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6800 GB/s"},
         "per_m": per_m,
+        "decode_per_projection_cold": per_projection,
     }
     if prefill is not None:
         line["prefill"] = prefill
