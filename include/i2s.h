@@ -305,9 +305,17 @@ int i2s_mul_mat_grouped_host(const i2s_problem* probs, int count, int64_t M, voi
  *                     byte of every x and y must be so mapped; the call checks
  *                     the ends of each merged range (cudaPointerGetAttributes)
  *                     and returns BAD_ARG, with nothing enqueued, if one is not.
- * Same results, bit for bit, either way. Errors: as i2s_mul_mat_grouped_host,
- * plus BAD_ARG for unknown flag bits. */
+ *   I2S_HOST_MAPPED_Y only the outputs are so mapped and written in place by
+ *                     the epilogue; the activations are staged (one copy up
+ *                     per merged range, as with flags 0), so their transfer
+ *                     runs on a copy engine and can overlap kernels of other
+ *                     streams. The workspace is the staged call's. Every byte
+ *                     of every y must be mapped (checked as above).
+ * I2S_HOST_MAPPED with I2S_HOST_MAPPED_Y is I2S_HOST_MAPPED. Same results, bit
+ * for bit, in every mode. Errors: as i2s_mul_mat_grouped_host, plus BAD_ARG
+ * for unknown flag bits. */
 #define I2S_HOST_MAPPED 1u
+#define I2S_HOST_MAPPED_Y 2u
 int i2s_mul_mat_grouped_host_ex(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
                                 unsigned flags, i2s_stream_t stream);
 

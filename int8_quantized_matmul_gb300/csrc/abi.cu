@@ -787,7 +787,8 @@ static bool mapped_host(uintptr_t p) {
 
 int i2s_mul_mat_grouped_host_ex(const i2s_problem* probs, int count, int64_t M, void* ws, size_t ws_bytes,
                                 unsigned flags, i2s_stream_t stream) {
-    if (flags & ~(unsigned)I2S_HOST_MAPPED) return I2S_E_BAD_ARG;
+    if (flags & ~(unsigned)(I2S_HOST_MAPPED | I2S_HOST_MAPPED_Y)) return I2S_E_BAD_ARG;
+    const bool map_y = (flags & I2S_HOST_MAPPED_Y) != 0u;
     HostPlan pl;
     int r = host_plan(probs, count, M, pl);
     if (r) return r;
@@ -805,20 +806,25 @@ int i2s_mul_mat_grouped_host_ex(const i2s_problem* probs, int count, int64_t M, 
             if (!mapped_host(sp.lo) || !mapped_host(sp.hi - 1)) return I2S_E_BAD_ARG;
         return grouped_impl(probs, count, M, ws, pl.grouped, stream, 3);
     }
+    if (map_y)
+        for (const HostSpan& sp : pl.ys)
+            if (!mapped_host(sp.lo) || !mapped_host(sp.hi - 1)) return I2S_E_BAD_ARG;
     char* base = (char*)ws;
     std::vector<i2s_problem> dev(probs, probs + count);
     for (i2s_problem& p : dev) {
         const HostSpan& sx = span_of(pl.xs, (uintptr_t)p.x);
-        const HostSpan& sy = span_of(pl.ys, (uintptr_t)p.y);
         p.x = (const float*)(base + sx.off + ((uintptr_t)p.x - sx.lo));
-        p.y = (float*)(base + sy.off + ((uintptr_t)p.y - sy.lo));
+        if (!map_y) {
+            const HostSpan& sy = span_of(pl.ys, (uintptr_t)p.y);
+            p.y = (float*)(base + sy.off + ((uintptr_t)p.y - sy.lo));
+        }
     }
     for (const HostSpan& s : pl.xs) {
         r = cuda_status(cudaMemcpyAsync(base + s.off, (const void*)s.lo, s.hi - s.lo, cudaMemcpyHostToDevice, stream));
         if (r) return r;
     }
     r = grouped_impl(dev.data(), count, M, ws, pl.grouped, stream, 3);
-    if (r) return r;
+    if (r || map_y) return r;
     for (const HostSpan& s : pl.ys) {
         r = cuda_status(cudaMemcpyAsync((void*)s.lo, base + s.off, s.hi - s.lo, cudaMemcpyDeviceToHost, stream));
         if (r) return r;

@@ -316,7 +316,8 @@ def _host_problems(problems: Sequence):
     return arr
 
 
-HOST_MAPPED = 1   # I2S_HOST_MAPPED
+HOST_MAPPED = 1     # I2S_HOST_MAPPED
+HOST_MAPPED_Y = 2   # I2S_HOST_MAPPED_Y
 
 
 class HostGroup:
@@ -326,12 +327,16 @@ class HostGroup:
     stream. By default x is copied up and y back around it
     (i2s_mul_mat_grouped_host); with mapped=True (every x and y in pinned,
     device-mapped memory, as torch's pin_memory() gives) the kernels read x
-    and write y over the host link directly (I2S_HOST_MAPPED)."""
+    and write y over the host link directly (I2S_HOST_MAPPED); with
+    mapped="y" x is copied up and the epilogue writes y in place
+    (I2S_HOST_MAPPED_Y)."""
 
-    def __init__(self, problems: Sequence, M: int, device=None, ws=None, mapped: bool = False):
+    def __init__(self, problems: Sequence, M: int, device=None, ws=None, mapped=False):
         self.problems = list(problems)
         self.M = int(M)
-        self.flags = HOST_MAPPED if mapped else 0
+        if mapped not in (False, True, "y"):
+            raise ValueError("mapped is False, True or 'y'")
+        self.flags = HOST_MAPPED_Y if mapped == "y" else (HOST_MAPPED if mapped else 0)
         self.arr = _host_problems(self.problems)
         need = int(_L.i2s_mul_mat_grouped_host_workspace(self.arr, len(self.problems), self.M))
         if need == 0:

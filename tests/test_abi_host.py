@@ -257,6 +257,13 @@ def test_host_buffer_call_validation_and_copy_plan(i2s):
     bad_k = problems(xs, ys, Ns)
     bad_k[1].K = 100
     assert L.i2s_mul_mat_grouped_host(bad_k, 3, M, ws, 1 << 30, None) == E["I2S_E_BAD_SHAPE"]
-    # flags: only I2S_HOST_MAPPED (1) is defined
-    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, need, 2, None) == E["I2S_E_BAD_ARG"]
+    # flags: I2S_HOST_MAPPED (1) and I2S_HOST_MAPPED_Y (2) are defined
+    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, need, 4, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, need, 8, None) == E["I2S_E_BAD_ARG"]
     assert L.i2s_mul_mat_grouped_host_ex(clash, 3, M, ws, 1 << 30, 1, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_host_ex(clash, 3, M, ws, 1 << 30, 2, None) == E["I2S_E_BAD_ARG"]
+    # outputs-only mapping stages the activations: the staged call's workspace
+    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, need - 1, 2, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    # both mapped needs only the grouped workspace
+    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, grouped - 1, 1, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+    assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, grouped - 1, 3, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]

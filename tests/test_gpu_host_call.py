@@ -91,12 +91,14 @@ def test_host_call_repeated_with_new_inputs(i2s, o):
     assert i2s.read_status(g.ws) == 0
 
 
+@pytest.mark.parametrize("mode", [True, "y"])
 @pytest.mark.parametrize("M", [1, 8, 64])
-def test_host_call_mapped_decoder_layer(i2s, o, M):
+def test_host_call_mapped_decoder_layer(i2s, o, M, mode):
     # I2S_HOST_MAPPED: pinned (device-mapped) host buffers read and written by
-    # the kernels directly, no staging copies; same bits as the oracle
+    # the kernels directly, no staging copies; I2S_HOST_MAPPED_Y: x copied up,
+    # y written in place by the epilogue. Same bits as the oracle either way.
     probs, keep = layer(o, M, seed=M + 50, pinned=True)
-    g = i2s.HostGroup(probs, M, mapped=True)
+    g = i2s.HostGroup(probs, M, mapped=mode)
     for _ in range(2):
         for _, _, _, _, y in keep:
             y.fill_(float("nan"))
@@ -107,11 +109,12 @@ def test_host_call_mapped_decoder_layer(i2s, o, M):
             same_bits(y.numpy(), o.i2s_mul_mat(packed, N, K, x.numpy(), nth=8))
 
 
-def test_host_call_mapped_rejects_pageable_buffers(i2s, o):
-    # the mapped mode checks its ranges before anything is enqueued: pageable
-    # buffers are refused, and the outputs stay untouched
+@pytest.mark.parametrize("mode", [True, "y"])
+def test_host_call_mapped_rejects_pageable_buffers(i2s, o, mode):
+    # the mapped modes check their ranges before anything is enqueued:
+    # pageable buffers are refused, and the outputs stay untouched
     probs, keep = layer(o, 8, seed=77, pinned=False)
-    g = i2s.HostGroup(probs, 8, mapped=True)
+    g = i2s.HostGroup(probs, 8, mapped=mode)
     with pytest.raises(i2s.I2SError) as e:
         g()
     assert e.value.status == -8   # I2S_E_BAD_ARG
