@@ -81,12 +81,11 @@ constexpr int kMmaWarp = 13;                // warps 13-14
 constexpr int kCodeWarp = 15;               // TMA producer of the packed codes
 constexpr int kIssuersTc = 2;
 constexpr int kThreadsTc = 512;
-constexpr int kStagesTc = 4;
+constexpr int kStagesTc = 6;
 constexpr int kCodeStages = 6;              // ring of packed-code stages, ahead of the operand ring
 constexpr int kCodeStageBytes = 128 * 64;   // 128 weight rows x 64 packed bytes (256 positions)
 constexpr int kBlockK = 256;                // K positions per stage (one 128-byte row of e2m1)
 constexpr int kTileW = 128;                 // weight rows per CTA (half of the pair's MMA M)
-constexpr int kATileBytes = kTileW * 128;   // 16 KB of e2m1
 constexpr int kBPlaneMax = 64 * 128;        // one digit plane of this CTA's half of up to 128 activation rows
 constexpr int kBStageMax = 3 * kBPlaneMax;  // 24 KB
 constexpr int kTmemCols = 512;
@@ -94,10 +93,13 @@ constexpr uint32_t kAccCols = 128;          // two accumulators of BN <= 128 col
 constexpr uint32_t kSfaCol = 256;           // block scales: A (all 1), then B for digits 0, 1, 2 (1, 8, 64)
 constexpr uint32_t kSfbCol0 = 272;
 constexpr uint32_t kSfCols = 16;
+constexpr uint32_t kACol0 = 320;            // the A ring in TMEM: one stage of 256 e2m1 per lane
+constexpr uint32_t kAStageCols = 32;        //   (eight per 32-bit column) per kAStageCols columns
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
 static_assert(kStagesTc % kIssuersTc == 0, "ring slots per issuer");
 static_assert(kCodeStages % 2 == 0, "converters take stages in pairs");
-static_assert(kSfbCol0 + 3 * kSfCols <= (uint32_t)kTmemCols, "TMEM budget");
+static_assert(kSfbCol0 + 3 * kSfCols <= kACol0, "TMEM budget: scales below the A ring");
+static_assert(kACol0 + kStagesTc * kAStageCols <= (uint32_t)kTmemCols, "TMEM budget: the A ring");
 
 struct SmemTc {
     float sc_col[2][128];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
@@ -117,7 +119,7 @@ struct SmemTc {
 };
 
 constexpr size_t kSmemTcBytes =
-    1024 + (size_t)kStagesTc * (kATileBytes + kBStageMax) + (size_t)kCodeStages * kCodeStageBytes + sizeof(SmemTc);
+    1024 + (size_t)kStagesTc * kBStageMax + (size_t)kCodeStages * kCodeStageBytes + sizeof(SmemTc);
 
 __device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
     int lo = 0, hi = a.count - 1;
@@ -136,11 +138,26 @@ __device__ __forceinline__ uint4 expand_words_e2m1(uint32_t w0, uint32_t w1) {
     return make_uint4(w0 & m, (w0 >> 2) & m, w1 & m, (w1 >> 2) & m);
 }
 
+// Leader only: D (+)= A * B^T over the pair, kind::mxf4 with block scaling, A
+// read from both CTAs' TMEM (each CTA's 128 lanes, eight e2m1 per 32-bit
+// column, element 8c + i in bits 4i..4i+3 of column c), B in shared memory.
+__device__ __forceinline__ void pair_umma_mxf4_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s_gemm_tc(const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + (size_t)kStagesTc * kATileBytes;
+    uint8_t* sB = smem;
     uint8_t* sC = sB + (size_t)kStagesTc * kBStageMax;   // packed codes (1024-aligned)
     SmemTc& S = *reinterpret_cast<SmemTc*>(sC + (size_t)kCodeStages * kCodeStageBytes);
 
@@ -294,6 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         // 128-position groups), read from the code ring (64-byte swizzle),
         // become the 128 bytes of e2m1 operands of the stage row
         const int r = tid - kEpiWarps * 32;   // weight row within the CTA's half of the tile
+        // = TMEM lane: converter warp w reaches lane quarter w % 4
+        const uint32_t lane_a = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kACol0;
         int stage = 0, cs = 0;
         uint32_t phase = 0, cphase = 0;
         bool ok = true;
@@ -329,18 +348,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 got = tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit);
                 if (got && two) got = tc::mbar_wait(&S.empty[stage1], phase1 ^ 1, abort_flag, kWaitLimit);
                 if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
+                // the MMAs that read these A stages have completed (their
+                // commit released the empty barriers): TMEM stores after them
+                tc::tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (h == 1 && !two) break;
-                    uint8_t* dst = sA + (size_t)(h ? stage1 : stage) * kATileBytes;
-                    // group g, words 2p and 2p + 1 -> chunk 4g + p of the 128-byte row
+                    // code word j -> e2m1 columns 2j and 2j + 1 of the lane's stage
+                    uint32_t e[32];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i)) = expand_words_e2m1(v[h][i].x, v[h][i].y);
-                        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * i + 1)) = expand_words_e2m1(v[h][i].z, v[h][i].w);
+                        const uint4 c4 = expand_words_e2m1(v[h][i].x, v[h][i].y);
+                        const uint4 d4 = expand_words_e2m1(v[h][i].z, v[h][i].w);
+                        e[8 * i] = c4.x, e[8 * i + 1] = c4.y, e[8 * i + 2] = c4.z, e[8 * i + 3] = c4.w;
+                        e[8 * i + 4] = d4.x, e[8 * i + 5] = d4.y, e[8 * i + 6] = d4.z, e[8 * i + 7] = d4.w;
                     }
+                    tc::tmem_st_32x32b_x32(lane_a + (uint32_t)(h ? stage1 : stage) * kAStageCols, e);
                 }
-                tc::fence_proxy_async_smem();
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
                 __syncwarp();
                 // CTA-scope arrives: a cluster-scope release here would
                 // also wait for this thread's earlier memory operations
@@ -388,7 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                         if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit) ||
                             !tc::mbar_wait(&S.full_b[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
                         tc::tc_fence_after();
-                        const uint64_t ad = tc::sdesc_sw128_kmajor(tc::smem_u32(sA + (size_t)stage * kATileBytes));
+                        const uint32_t a_tm = tmem_base + kACol0 + (uint32_t)stage * kAStageCols;
                         const uint32_t b0 = tc::smem_u32(sB + (size_t)stage * kBStageMax);
                         const uint64_t bd0 = tc::sdesc_sw128_kmajor(b0);
                         const uint64_t bd1 = tc::sdesc_sw128_kmajor(b0 + plane_bytes);
@@ -398,11 +424,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {   // +32 bytes (64 e2m1) per step
                             if (k >= steps) break;
-                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd0 + 2 * k, idesc, sfa, tmem_base + kSfbCol0, 1u);
-                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd1 + 2 * k, idesc, sfa,
-                                               tmem_base + kSfbCol0 + kSfCols, 1u);
-                            tc::pair_umma_mxf4(d_tmem, ad + 2 * k, bd2 + 2 * k, idesc, sfa,
-                                               tmem_base + kSfbCol0 + 2 * kSfCols, 1u);
+                            const uint32_t ak = a_tm + 8u * (uint32_t)k;   // 64 e2m1 per step
+                            pair_umma_mxf4_tmem_a(d_tmem, ak, bd0 + 2 * k, idesc, sfa, tmem_base + kSfbCol0, 1u);
+                            pair_umma_mxf4_tmem_a(d_tmem, ak, bd1 + 2 * k, idesc, sfa,
+                                                  tmem_base + kSfbCol0 + kSfCols, 1u);
+                            pair_umma_mxf4_tmem_a(d_tmem, ak, bd2 + 2 * k, idesc, sfa,
+                                                  tmem_base + kSfbCol0 + 2 * kSfCols, 1u);
                         }
                         tc::pair_commit(&S.empty[stage], 0x3);   // both CTAs' stage slots are free
                     }
