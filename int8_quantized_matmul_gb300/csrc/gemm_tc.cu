@@ -102,6 +102,7 @@ static_assert(kSfbCol0 + 3 * kSfCols <= kACol0, "TMEM budget: scales below the A
 static_assert(kACol0 + kStagesTc * kAStageCols <= (uint32_t)kTmemCols, "TMEM budget: the A ring");
 
 struct SmemTc {
+    TcProb prob[kMaxGroup];   // the launch's problem table, copied from the parameters
     float sc_col[2][128];   // epilogue: w_scale * act_scale[m] per tile column, by accumulator
     float rs_col[2][128];   // epilogue: row_sum[m] per tile column (exact as a float), by accumulator
     uint64_t full_a[kStagesTc];
@@ -121,13 +122,12 @@ struct SmemTc {
 constexpr size_t kSmemTcBytes =
     1024 + (size_t)kStagesTc * kBStageMax + (size_t)kCodeStages * kCodeStageBytes + sizeof(SmemTc);
 
-__device__ __forceinline__ int find_problem(const TcArgs& a, int tile) {
-    int lo = 0, hi = a.count - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.p[mid].tile0 <= tile) lo = mid; else hi = mid - 1;
-    }
-    return lo;
+// The problem holding `tile`, from the problem before: each role visits its
+// tiles in increasing order, and the problems' tile ranges are in order, so
+// the search only moves forward (over the shared-memory copy of the table).
+__device__ __forceinline__ int next_problem(const TcProb* sp, int count, int pi, int tile) {
+    while (pi + 1 < count && sp[pi + 1].tile0 <= tile) ++pi;
+    return pi;
 }
 
 // Two 32-bit words of packed codes -> one 16-byte chunk of e2m1 operands:
@@ -197,6 +197,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
     }
     if (warp == kTmaWarp && lane == 0)
         for (int i = 0; i < a.n_maps; ++i) tc::tma_prefetch_desc(&a.maps[i]);
+    static_assert(sizeof(TcProb) % 16 == 0, "problem entries copy as 16-byte words");
+    for (int i = tid; i < a.count * (int)(sizeof(TcProb) / 16); i += kThreadsTc)
+        reinterpret_cast<uint4*>(S.prob)[i] = reinterpret_cast<const uint4*>(a.p)[i];
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -241,8 +244,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             bool pending[kStagesTc] = {};
             uint32_t pending_phase[kStagesTc] = {};
             bool ok = true;
+            int pi = 0;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-                const TcProb& P = a.p[find_problem(a, tile)];
+                pi = next_problem(S.prob, a.count, pi, tile);
+                const TcProb& P = S.prob[pi];
                 const int at = (tile - P.tile0) % P.n_act_tiles;
                 const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
                 const int row = at * BN + (int)rank * BH;
@@ -280,10 +285,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             bool pending[kCodeStages] = {};
             uint32_t pending_phase[kCodeStages] = {};
             bool ok = true;
-            int cur_p = -1;
+            int cur_p = -1, pi = 0;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-                const int pi = find_problem(a, tile);
-                const TcProb& P = a.p[pi];
+                pi = next_problem(S.prob, a.count, pi, tile);
+                const TcProb& P = S.prob[pi];
                 const CUtensorMap* map = a.wmaps + pi;
                 if (pi != cur_p) {   // first use of this map: order it after the writer's release
                     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
@@ -316,8 +321,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         int stage = 0, cs = 0;
         uint32_t phase = 0, cphase = 0;
         bool ok = true;
+        int pi = 0;
         for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-            const TcProb& P = a.p[find_problem(a, tile)];
+            pi = next_problem(S.prob, a.count, pi, tile);
+            const TcProb& P = S.prob[pi];
             const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
             for (int kb = 0; ok && kb < KB; kb += 2) {
                 // two stages per pass: one proxy fence and one warp sync for both
@@ -403,8 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             uint32_t acc_phase = 0;
             int seq = 0;
             bool ok = true;
+            int pi = 0;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-                const TcProb& P = a.p[find_problem(a, tile)];
+                pi = next_problem(S.prob, a.count, pi, tile);
+                const TcProb& P = S.prob[pi];
                 const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
                 if (!tc::mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimit)) { fail(4); break; }
                 tc::tc_fence_after();
@@ -453,8 +462,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            int pi = 0;
             for (int tile = pair; ok && tile < a.total_tiles; tile += n_pairs) {
-                const TcProb& P = a.p[find_problem(a, tile)];
+                pi = next_problem(S.prob, a.count, pi, tile);
+                const TcProb& P = S.prob[pi];
                 const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!tc::mbar_wait(&S.full_a[stage], phase, abort_flag, kWaitLimit)) { fail(8); ok = false; break; }
@@ -471,8 +482,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         const int half = warp >> 2;            // which half of the accumulator's columns
         int acc = 0;
         uint32_t acc_phase = 0, stage_phase = 0;
+        int pi = 0;
         for (int tile = pair; tile < a.total_tiles; tile += n_pairs) {
-            const TcProb& P = a.p[find_problem(a, tile)];
+            pi = next_problem(S.prob, a.count, pi, tile);
+            const TcProb& P = S.prob[pi];
             const int local = tile - P.tile0;
             const int wt = local / P.n_act_tiles, at = local % P.n_act_tiles;
             const int n = wt * (2 * kTileW) + (int)rank * kTileW + r;
