@@ -138,6 +138,15 @@ __device__ __forceinline__ uint4 expand_words_e2m1(uint32_t w0, uint32_t w1) {
     return make_uint4(w0 & m, (w0 >> 2) & m, w1 & m, (w1 >> 2) & m);
 }
 
+// Arrive on a barrier of the cluster without release semantics. The epilogue
+// releases an accumulator with it: what the MMAs must not overtake are its
+// TMEM loads and zeroing stores, complete at tcgen05.wait::ld / ::st before
+// it, not its global stores of y, which a release arrive would wait for (over
+// a thousand cycles per warp and tile).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Leader only: D (+)= A * B^T over the pair, kind::mxf4 with block scaling, A
 // read from both CTAs' TMEM (each CTA's 128 lanes, eight e2m1 per 32-bit
 // column, element 8c + i in bits 4i..4i+3 of column c), B in shared memory.
@@ -554,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive_cluster(tc::smem_in_rank(&S.tmem_empty[acc], 0));   // the leader's barrier
+                if (lane == 0) mbar_arrive_cluster_relaxed(tc::smem_in_rank(&S.tmem_empty[acc], 0));   // the leader's barrier
             };
             uint32_t va[16], vb[16];
             tc::tmem_ld_32x32b_x16(d_addr, va);

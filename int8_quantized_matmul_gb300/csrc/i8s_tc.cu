@@ -138,6 +138,15 @@ __device__ __forceinline__ Seg8 seg8_at(const I8sTcArgs& a, int u, int u_hi) {
     return g;
 }
 
+// Arrive on a barrier of the cluster without release semantics. The drain
+// releases an accumulator with it: what the MMAs must not overtake are its
+// TMEM loads and stores, complete at tcgen05.wait::ld / ::st before it, not
+// the global stores of an earlier tile's epilogue, which a release arrive
+// would wait for.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 template <int BM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_gemm_tc(const __grid_constant__ I8sTcArgs a) {
     using T = Tile8<BM>;
@@ -347,7 +356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1) k_i8s_
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
-                tc::mbar_arrive_cluster(tc::smem_in_rank(&S.tmem_empty[buf], 0));   // the leader's barrier
+                mbar_arrive_cluster_relaxed(tc::smem_in_rank(&S.tmem_empty[buf], 0));   // the leader's barrier
                 if (++buf == 2) { buf = 0; buf_phase ^= 1; }
             }
             if (!ok) break;
