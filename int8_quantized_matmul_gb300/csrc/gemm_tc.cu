@@ -77,10 +77,10 @@ namespace {
 constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, each half of the columns
 constexpr int kCvtWarps = 4;               // one thread per weight row
 constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;                // warps 13-14
-constexpr int kCodeWarp = 15;               // TMA producer of the packed codes
-constexpr int kIssuersTc = 2;
-constexpr int kThreadsTc = 512;
+constexpr int kMmaWarp = 13;                // warps 13-15
+constexpr int kCodeWarp = 16;               // TMA producer of the packed codes
+constexpr int kIssuersTc = 3;
+constexpr int kThreadsTc = 544;
 constexpr int kStagesTc = 6;
 constexpr int kCodeStages = 6;              // ring of packed-code stages, ahead of the operand ring
 constexpr int kCodeStageBytes = 128 * 64;   // 128 weight rows x 64 packed bytes (256 positions)
