@@ -18,39 +18,41 @@
 //     descriptor, add (c/2)*q into ONE accumulator;
 //   * every product is a multiple of 1/2 and every partial sum stays below
 //     2^23: the completed steps contribute at most 127 per position, and the
-//     step each of the two issue streams has in flight at most
-//     (4 + 8*4 + 64*2) * 64, so 127*65536 + 2*164*64 < 2^23 and binary32
+//     step each of the three issue streams has in flight at most
+//     (4 + 8*4 + 64*2) * 64, so 127*65536 + 3*164*64 < 2^23 and binary32
 //     holds every partial sum exactly. dot = 2*D.
-// Each 256-position stage moves 16 KB of A (converted) and 3 * BN/2 * 128
-// bytes of B per CTA, half the bytes per multiply-add of f16 operands, and the
-// tensor time of a step is that of three fp4 MMAs.
+// Each 256-position stage holds 16 KB of A (converted, in TMEM) and
+// 3 * BN/2 * 128 bytes of B (shared memory) per CTA, and the tensor time of a
+// step is that of three fp4 MMAs.
 //
 // Roles (one CTA per SM, persistent over a static tile schedule):
 //   warps 0-7  epilogue: TMEM -> registers, y = (float)(dot - row_sum) *
 //              (w_scale * act_scale), coalesced F32 stores (warp w reads
 //              TMEM lanes 32(w%4)..+31 = weight rows of the tile, columns
 //              (w/4)*BN/2..+BN/2-1 = activation rows);
-//   warps 8-11 converters: one thread per weight row of the 128-row tile,
-//              reading the row's 64 packed bytes of a stage from the code
-//              ring and writing its 128 bytes of e2m1 operands into the
-//              128B-swizzled K-major layout, then fencing the writes into
-//              the async proxy;
+//   warps 8-11 converters: one thread per weight row of the 128-row tile =
+//              TMEM lane, reading the row's 64 packed bytes of a stage from
+//              the code ring and storing its 128 bytes of e2m1 operands
+//              (32 columns) into the stage's slot of a six-stage A ring in
+//              TMEM (tcgen05.st), which the MMAs read as their A operand;
 //   warp 12    TMA producer of the three digit planes of the activation tile;
-//   warps 13-14 MMA issue (one lane each; warp 13 also allocates TMEM);
-//   warp 15    TMA producer of the packed codes: a six-stage ring of 128 rows
+//   warps 13-15 MMA issue (one lane each; warp 13 also allocates TMEM): one
+//              thread needs about a hundred cycles to issue an MMA, more than
+//              the MMA's tensor time, so three take the stages in turn;
+//   warp 16    TMA producer of the packed codes: a six-stage ring of 128 rows
 //              x 64 bytes (64-byte swizzle) that runs ahead of the operand
 //              ring, so the converters never wait on global loads.
 // CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
-// cta_group::2 MMAs. A tile is 256 weight rows (128 converted in each CTA's
-// shared memory, 128 accumulator rows in each CTA's TMEM) x BN <= 128
-// activation rows (half of each plane TMA'd into each CTA's shared memory).
+// cta_group::2 MMAs. A tile is 256 weight rows (128 converted into each CTA's
+// TMEM, 128 accumulator rows in each CTA's TMEM) x BN <= 128 activation rows
+// (half of each plane TMA'd into each CTA's shared memory).
 // The leader (rank 0) issues M = 256 x N = BN x K = 64 MMAs, 12 per stage;
 // both CTAs' converters and TMA loads report to the leader's stage barriers,
 // its commits multicast to both CTAs, and each CTA's epilogue releases the
-// leader's accumulator barrier by a remote arrive. Two TMEM accumulators of
-// 128 columns let the epilogue of one tile overlap the MMAs of the next; the
-// block scales live in TMEM beside them. Two warps issue, taking the stages in
-// turn, both into the tile's accumulator.
+// leader's accumulator barrier by a remote arrive. TMEM per CTA: two
+// accumulators of 128 columns (the epilogue of one tile overlaps the MMAs of
+// the next), the block scales (64 columns) and the A ring (6 x 32 columns).
+// The issuers all accumulate into the tile's accumulator.
 //
 // K order: within a 128-position group, element 16w + 8t + 2i + h of the A
 // and B rows holds position 32s + 4w + i, where (t, h) = (0,0), (0,1), (1,0),
