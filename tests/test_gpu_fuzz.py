@@ -70,6 +70,31 @@ def test_fuzz_i2s_grouped(i2s, o, case):
         same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=8))
 
 
+@pytest.mark.parametrize("M", [4, 40])
+def test_grouped_many_problems(i2s, o, M):
+    # up to the group limit of small projections in one launch (M = 4: the
+    # GEMV, M = 40: the GEMM), every output against the oracle: the kernels'
+    # problem tables and their per-tile problem lookup cross every boundary
+    rng = np.random.default_rng(77 + M)
+    n_act = 7
+    Ks = [128 * int(rng.integers(1, 4)) for _ in range(n_act)]
+    xs = [synth.normal_f32((M, K), seed=500 + a, outlier_p=0.02) for a, K in enumerate(Ks)]
+    dxs = [dev(x) for x in xs]
+    count = 256 if M <= 16 else 200
+    group, keep = [], []
+    for i in range(count):
+        a = int(rng.integers(0, n_act))
+        K, N = Ks[a], int(rng.integers(1, 300))
+        packed = o.i2s_pack(synth.codes(N, K, seed=9000 + i), float(rng.uniform(0.005, 0.2)))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        group.append((dev(packed), N, K, dxs[a], y))
+        keep.append((packed, N, K, xs[a], y))
+    ws = i2s.i2s_mul_mat_grouped(group, M)
+    assert i2s.read_status(ws) == 0
+    for packed, N, K, x, y in keep:
+        same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=8))
+
+
 @pytest.mark.parametrize("case", range(24))
 def test_fuzz_i8s_mul_mat_add(i2s, o, case):
     rng = np.random.default_rng(2000 + case)
