@@ -566,12 +566,25 @@ def cpu_baseline_decode(seconds_target=12.0):
                 o.i2s_mul_mat(packed[i], N, K, xs[ACT_OF[name]], nth=nth)
             elapsed += time.perf_counter() - t0
             done_bytes += sum(N * K // 4 for _, N, K in PROJ)
+        if layer == 0:
+            first = packed
         layers += 1
         if elapsed >= seconds_target:
             break
+    # the same oracle on one thread, over the first layer at M = 1 and M = 8
+    t1_bytes, t1 = 0, 0.0
+    for M in (1, 8):
+        xs = [synth.normal_f32((M, K), seed=j) for j, K in enumerate(ACT_K)]
+        t0 = time.perf_counter()
+        for i, (name, N, K) in enumerate(PROJ):
+            o.i2s_mul_mat(first[i], N, K, xs[ACT_OF[name]], nth=1)
+        t1 += time.perf_counter() - t0
+        t1_bytes += sum(N * K // 4 for _, N, K in PROJ)
     return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
             "sample": f"first {layers} of 28 layers, all 7 projections, M=1 and M=8 "
-                      f"({done_bytes / 1e6:.1f} MB of codes, {elapsed:.1f} s)"}
+                      f"({done_bytes / 1e6:.1f} MB of codes, {elapsed:.1f} s)",
+            "single_thread": {"value": t1_bytes / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"layer 0, all 7 projections, M=1 and M=8 ({t1:.1f} s)"}}
 
 
 # ---------------------------------------------------------------------------
