@@ -361,6 +361,8 @@ def run_encoder_fc(torch, i2s, device, peaks, steps=10):
                                "note": "weights packed once into f16 operand rows (i8s_pack_weights)"},
             "roofline": {"bound": "tensor", "kernel": "k_i8s_gemm_tc", "achieved": tops, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tops / peaks["bf16_tflops"],
+                         "achieved_scope": "whole calls: the activation and weight pre-pass, the GEMM and the "
+                                           "requantization, each call's three launches between the events",
                          "traffic": recorded_traffic(I8S_PROFILE, I8S_SOURCES, "dram_bytes_per_fc_pair"),
                          "traffic_note": "DRAM bytes of the pair's two GEMM launches (ncu, L2 flushed before each)"}}
 
@@ -540,6 +542,8 @@ def run_w8a8_prefill(torch, i2s, device, peaks, steps=10):
             "value": tops, "unit": "TOPS",
             "roofline": {"bound": "tensor", "kernel": "k_i8s_gemm_tc", "achieved": tops, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tops / peaks["bf16_tflops"],
+                         "achieved_scope": "whole grouped calls: the activation row quantization into f16 operand "
+                                           "rows and the GEMM",
                          "traffic": recorded_traffic(I8S_PROFILE, I8S_SOURCES, "dram_bytes_per_w8a8_layer"),
                          "traffic_note": "DRAM bytes of the layer's grouped GEMM launch (ncu, L2 flushed before it)"}}
 
