@@ -126,6 +126,21 @@ __device__ __forceinline__ int stage_window16(const uint8_t* row, int64_t L, int
     return sh;
 }
 
+// quantize_one without its clamp, for a value bounded by the amax its scale came
+// from. Every caller in this file quantizes values whose largest magnitude is
+// that amax (or lies below its floor): the second passes recompute exactly the
+// values their first pass folded, and the W8A8 rows quantize the row they took
+// the maximum of. With |x| <= amax and inv = fl(127 / amax) <=
+// (127 / amax)(1 + 2^-24), fl(x * inv) is at most 127 + 2^-17 in magnitude,
+// below 127.5, so the clamp of quantize_one never acts and both give the same
+// integer.
+__device__ __forceinline__ int quantize_bounded(float x, float inv) {
+    const float v = __fmul_rn(x, inv);
+    const float a = __fadd_rn(fabsf(v), 0x1.fffffep-2f);
+    const int m = (int)(__float_as_uint(__fadd_rz(a, 12582912.0f)) - 0x4B400000u);
+    return v < 0.0f ? -m : m;
+}
+
 // ---------------------------------------------------------------- add_scaled
 
 __device__ __forceinline__ float add_one(int8_t qa, int8_t qb, float sa, float sb) {
@@ -169,14 +184,14 @@ __global__ void __launch_bounds__(kEltThreads) k_add_quant(const uint8_t* __rest
         for (int w = 0; w < 4; ++w) {
             int q[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) q[e] = quantize_one(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb), inv);
+            for (int e = 0; e < 4; ++e) q[e] = quantize_bounded(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb), inv);
             o[w] = pack4(q[0], q[1], q[2], q[3]);
         }
         *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (blockIdx.x == 0) {
         for (int64_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x)
-            dst[i] = (uint8_t)(quantize_one(add_one((int8_t)a[i], (int8_t)b[i], sa, sb), inv) & 0xff);
+            dst[i] = (uint8_t)(quantize_bounded(add_one((int8_t)a[i], (int8_t)b[i], sa, sb), inv) & 0xff);
         write_trailer(dst, n, scale);
     }
 }
@@ -266,12 +281,12 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant(const uint8_t* __rest
                 const uint32_t v = src[w];
                 int o[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[e] = quantize_one(rms_one(byte_of(v, e), s, r, gamma, 4 * w + e), inv);
+                for (int e = 0; e < 4; ++e) o[e] = quantize_bounded(rms_one(byte_of(v, e), s, r, gamma, 4 * w + e), inv);
                 out[w] = pack4(o[0], o[1], o[2], o[3]);
             }
         } else {
             for (int64_t i = lane; i < ne0; i += 32)
-                dst[row * ne0 + i] = (uint8_t)(quantize_one(rms_one(q[row * ne0 + i], s, r, gamma, i), inv) & 0xff);
+                dst[row * ne0 + i] = (uint8_t)(quantize_bounded(rms_one(q[row * ne0 + i], s, r, gamma, i), inv) & 0xff);
         }
     }
     if (blockIdx.x == 0) write_trailer(dst, n, scale);
@@ -352,10 +367,10 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_quant_t(const uint8_t* __re
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int wi = 4 * v + i;
-                o[i] = pack4(quantize_one(rms_one(byte_of(w[wi], 0), s, r, gamma, 4 * wi), inv),
-                             quantize_one(rms_one(byte_of(w[wi], 1), s, r, gamma, 4 * wi + 1), inv),
-                             quantize_one(rms_one(byte_of(w[wi], 2), s, r, gamma, 4 * wi + 2), inv),
-                             quantize_one(rms_one(byte_of(w[wi], 3), s, r, gamma, 4 * wi + 3), inv));
+                o[i] = pack4(quantize_bounded(rms_one(byte_of(w[wi], 0), s, r, gamma, 4 * wi), inv),
+                             quantize_bounded(rms_one(byte_of(w[wi], 1), s, r, gamma, 4 * wi + 1), inv),
+                             quantize_bounded(rms_one(byte_of(w[wi], 2), s, r, gamma, 4 * wi + 2), inv),
+                             quantize_bounded(rms_one(byte_of(w[wi], 3), s, r, gamma, 4 * wi + 3), inv));
             }
             *reinterpret_cast<uint4*>(dst + row * 16 * V + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
         }
@@ -610,10 +625,10 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_quant(const DwArgs d, const 
     const int n = d.C * d.OL, n4 = n / 4, step = gridDim.x * blockDim.x;
     for (int i4 = blockIdx.x * blockDim.x + threadIdx.x; i4 < n4; i4 += step)
         *reinterpret_cast<uint32_t*>(dst + 4 * i4) =
-            pack4(quantize_one(dw_one(d, sc, 4 * i4), inv), quantize_one(dw_one(d, sc, 4 * i4 + 1), inv),
-                  quantize_one(dw_one(d, sc, 4 * i4 + 2), inv), quantize_one(dw_one(d, sc, 4 * i4 + 3), inv));
+            pack4(quantize_bounded(dw_one(d, sc, 4 * i4), inv), quantize_bounded(dw_one(d, sc, 4 * i4 + 1), inv),
+                  quantize_bounded(dw_one(d, sc, 4 * i4 + 2), inv), quantize_bounded(dw_one(d, sc, 4 * i4 + 3), inv));
     if (blockIdx.x == 0) {
-        for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(quantize_one(dw_one(d, sc, i), inv) & 0xff);
+        for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) dst[i] = (uint8_t)(quantize_bounded(dw_one(d, sc, i), inv) & 0xff);
         write_trailer(dst, n, scale);
     }
 }
@@ -661,7 +676,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_win(const DwArgs d, int W, u
             float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
             if (d.bias) v = __fadd_rn(v, bc);
             if (d.relu) v = v > 0.0f ? v : 0.0f;
-            if (kQuant) out[tl0 + e] = (uint8_t)(quantize_one(v, inv) & 0xff);
+            if (kQuant) out[tl0 + e] = (uint8_t)(quantize_bounded(v, inv) & 0xff);
             else mx = fmaxf(mx, fabsf(v));
         }
     }
@@ -747,7 +762,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
         uint32_t packed[2] = {0u, 0u};
 #pragma unroll
         for (int e = 0; e < kDw1Out; ++e)
-            packed[e >> 2] |= (uint32_t)(quantize_one(y_of(acc[e]), inv) & 0xff) << (8 * (e & 3));
+            packed[e >> 2] |= (uint32_t)(quantize_bounded(y_of(acc[e]), inv) & 0xff) << (8 * (e & 3));
         {
             uint8_t* out = dst + (int64_t)c * d.OL + t0 + tl0;
             if (aligned && t0 + tl0 + kDw1Out <= d.OL) {
@@ -787,7 +802,7 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows(const float* __restri
     mx = fmaxf(mx, 1e-9f);
     const float inv = __fdiv_rn(127.0f, mx);
     if (threadIdx.x == 0) ascale[m] = __fdiv_rn(mx, 127.0f);
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) q[m * K + k] = (int8_t)quantize_one(xr[k], inv);
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) q[m * K + k] = (int8_t)quantize_bounded(xr[k], inv);
 }
 
 // W8A8 per-channel weights, one CTA per output channel: amax floored at 1e-9,
@@ -873,15 +888,15 @@ __global__ void __launch_bounds__(kEltThreads) k_w8a8_rows_f16(const __grid_cons
         for (int i = 0; i < kW8Cache; ++i) {
             const int k4 = (int)threadIdx.x + i * kEltThreads;
             if (k4 < K4) {
-                const __half2 lo = __halves2half2(__int2half_rn(quantize_one(c[i].x, inv)),
-                                                  __int2half_rn(quantize_one(c[i].y, inv)));
-                const __half2 hi = __halves2half2(__int2half_rn(quantize_one(c[i].z, inv)),
-                                                  __int2half_rn(quantize_one(c[i].w, inv)));
+                const __half2 lo = __halves2half2(__int2half_rn(quantize_bounded(c[i].x, inv)),
+                                                  __int2half_rn(quantize_bounded(c[i].y, inv)));
+                const __half2 hi = __halves2half2(__int2half_rn(quantize_bounded(c[i].z, inv)),
+                                                  __int2half_rn(quantize_bounded(c[i].w, inv)));
                 o2[k4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
             }
         }
     } else {
-        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_one(xr[k], inv));
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) out[k] = __int2half_rn(quantize_bounded(xr[k], inv));
     }
 }
 
