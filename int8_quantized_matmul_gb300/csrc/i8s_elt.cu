@@ -447,6 +447,53 @@ __global__ void __launch_bounds__(kEltThreads) k_transpose(const uint8_t* __rest
 
 // ---------------------------------------------------------------- im2col_asym
 
+// KW = 4, stride 2, C a multiple of 32, L a multiple of 16 and a 16-byte
+// aligned source (the encoder's stage-1 conv input): no staging. A warp takes
+// 32 output positions t0 .. t0+31 of 32 channels, one channel per lane. Output
+// row t holds, for channel c, the 4 bytes at positions 2t - pad_l .. +3 of the
+// channel's row; the 32 windows of a lane span 66 bytes starting at
+// s = 2 t0 - pad_l, which sits R bytes into a 16-byte chunk for every t0 (t0 is
+// a multiple of 32), so the lane loads five 16-byte chunks (a chunk lies wholly
+// inside [0, L) or wholly outside, where it reads as the zero padding) and
+// forms each window as one funnel shift of two of their words, at offsets known
+// at compile time. The warp's 32 lanes write word c of row t: 128 contiguous
+// bytes per store.
+template <int R>
+__global__ void __launch_bounds__(kEltThreads) k_im2col_k4s2(const uint8_t* __restrict__ src, int C, int64_t L,
+                                                             int pad_l, int64_t OL, uint8_t* __restrict__ dst) {
+    const int64_t warp = (blockIdx.x * (int64_t)kEltThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int groups = C >> 5;
+    const int64_t runs = (OL + 31) >> 5;
+    if (warp < groups * runs) {
+        const int64_t run = warp / groups;
+        const int c = (int)(warp - run * groups) * 32 + lane;
+        const int64_t t0 = run * 32;
+        const int64_t base = 2 * t0 - pad_l - R;   // 16-byte aligned
+        const uint8_t* row = src + (int64_t)c * L;
+        uint32_t w[20];
+#pragma unroll
+        for (int ch = 0; ch < 5; ++ch) {
+            const int64_t off = base + 16 * ch;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (off >= 0 && off < L) v = *reinterpret_cast<const uint4*>(row + off);
+            w[4 * ch] = v.x, w[4 * ch + 1] = v.y, w[4 * ch + 2] = v.z, w[4 * ch + 3] = v.w;
+        }
+        const int64_t row_bytes = 4 * (int64_t)C;
+        uint32_t* out = reinterpret_cast<uint32_t*>(dst + t0 * row_bytes) + c;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int o = R + 2 * i;   // window i's first byte within the loaded chunks
+            const int q = o >> 2, sh = (o & 3) * 8;
+            const uint32_t win = sh ? __funnelshift_r(w[q], w[q + 1], sh) : w[q];
+            if (t0 + i < OL) out[(int64_t)i * C] = win;
+        }
+    }
+    if (blockIdx.x == 0) write_trailer(dst, OL * C * 4, i8s_scale_of(src, (int64_t)C * L));
+}
+
+
+
 // Output and input sizes below 2^31 (checked by the host): 32-bit index math.
 __global__ void __launch_bounds__(kEltThreads) k_im2col(const uint8_t* __restrict__ src, int C, int L, int KW,
                                                         int stride, int pad_l, int OL, uint8_t* __restrict__ dst) {
@@ -979,6 +1026,22 @@ cudaError_t launch_im2col_asym(const uint8_t* src, int64_t C, int64_t L, int KW,
     // 256) whose C windows fit in 48 KB of shared memory
     // per channel 4*Wc bytes of staged words (W window bytes, up to 3 bytes of
     // alignment shift, one spare word) and one shift word
+    if (KW == 4 && stride == 2 && C % 32 == 0 && L % 16 == 0 && (pad_l & 1) == 0 &&
+        ((uintptr_t)src & 15u) == 0 && ((uintptr_t)dst & 15u) == 0) {
+        const int64_t warps = (C / 32) * ((OL + 31) / 32);
+        const unsigned blocks = (unsigned)((warps * 32 + kEltThreads - 1) / kEltThreads);
+        switch (((16 - pad_l % 16) % 16) / 2) {   // the window start's offset in its 16-byte chunk, halved
+            case 0: k_im2col_k4s2<0><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 1: k_im2col_k4s2<2><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 2: k_im2col_k4s2<4><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 3: k_im2col_k4s2<6><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 4: k_im2col_k4s2<8><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 5: k_im2col_k4s2<10><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            case 6: k_im2col_k4s2<12><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+            default: k_im2col_k4s2<14><<<blocks, kEltThreads, 0, s>>>(src, (int)C, L, pad_l, OL, dst); break;
+        }
+        return cudaGetLastError();
+    }
     constexpr int64_t kWinBytes = 48 * 1024;
     auto smem_for = [&](int64_t T_) {
         const int64_t W_ = (T_ - 1) * stride + KW;

@@ -191,6 +191,29 @@ def test_im2col_asym_wide_kernels(i2s, o, C, L, KW, stride, pad_l, pad_r):
     same_bytes(host(got), ref)
 
 
+# kernel 4, stride 2, channels a multiple of 32, rows a multiple of 16 bytes:
+# the path with one channel per lane and no staging, at every even left pad
+# modulo 16 (each is its own instantiation), with right pads, ragged output
+# lengths (not a multiple of 32) and inputs shorter than one run
+GEOMS_K4S2 = [(32, 4096, p, 0) for p in (0, 2, 4, 6, 8, 10, 12, 14)] + [
+    (32, 4096, 18, 5),
+    (64, 1008, 2, 3),
+    (96, 160, 2, 0),
+    (32, 16, 2, 0),
+    (32, 48, 30, 7),
+    (64, 80, 16, 16),
+]
+
+
+@pytest.mark.parametrize("C,L,pad_l,pad_r", GEOMS_K4S2)
+def test_im2col_k4_s2(i2s, o, C, L, pad_l, pad_r):
+    _, x = i8s_tensor(o, (C, L), seed=C + L + pad_l)
+    got, OL = i2s.i8s_im2col_asym(dev(x), C, L, 4, 2, pad_l, pad_r)
+    ref, OL_ref = o.i8s_im2col_asym(x, C, L, 4, 2, pad_l, pad_r)
+    assert OL == OL_ref
+    same_bytes(host(got), ref)
+
+
 def test_im2col_encoder_size(i2s, o):
     # the stage-1 downsampling conv: kernel 4 = 2*stride, causal left pad 2
     C, L, KW, stride = ENC_C, ENC_L, 4, 2
