@@ -1005,14 +1005,20 @@ cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, 
 }
 
 cudaError_t launch_i8s_transpose(const uint8_t* src, int64_t a, int64_t b, uint8_t* dst, cudaStream_t s) {
-    // 8 KB tiles (eight 4-byte loads per thread in flight) where the rows are
-    // wide or narrow enough to fill them, 4 KB tiles in between
-    if (b >= 256) {
+    // 16 KB tiles (sixteen 4-byte loads per thread in flight) where the rows
+    // are wide or narrow enough to fill them, then 8 KB, 4 KB in between
+    if (b >= 512) {
+        const int64_t ta = (a + 31) / 32, tb = (b + 511) / 512;
+        k_transpose<32, 512><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    } else if (b >= 256) {
         const int64_t ta = (a + 31) / 32, tb = (b + 255) / 256;
         k_transpose<32, 256><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
     } else if (b >= 128) {
         const int64_t ta = (a + 31) / 32, tb = (b + 127) / 128;
         k_transpose<32, 128><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
+    } else if (a >= 512) {
+        const int64_t ta = (a + 511) / 512, tb = (b + 31) / 32;
+        k_transpose<512, 32><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
     } else {
         const int64_t ta = (a + 255) / 256, tb = (b + 31) / 32;
         k_transpose<256, 32><<<(unsigned)(ta * tb), kEltThreads, 0, s>>>(src, a, b, dst, tb);
