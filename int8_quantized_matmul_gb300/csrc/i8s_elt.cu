@@ -147,6 +147,18 @@ __device__ __forceinline__ float add_one(int8_t qa, int8_t qb, float sa, float s
     return __fadd_rn(__fmul_rn(i8_to_float(qa), sa), __fmul_rn(i8_to_float(qb), sb));
 }
 
+// Byte e of a word whose bytes were XORed with 0x80 (each int8 as q + 128),
+// read as a float exactly: the byte placed in the low mantissa bits of 2^23 by
+// one byte permute, minus 2^23 + 128 (the same value and rounding as
+// i8_to_float, with the XOR done once per word).
+__device__ __forceinline__ float i8x_to_float(uint32_t wx, int e) {
+    return __fsub_rn(__uint_as_float(__byte_perm(wx, 0x4Bu, 0x4550u + (uint32_t)e)), 8388736.0f);
+}
+
+__device__ __forceinline__ float add_one_x(uint32_t wax, uint32_t wbx, int e, float sa, float sb) {
+    return __fadd_rn(__fmul_rn(i8x_to_float(wax, e), sa), __fmul_rn(i8x_to_float(wbx, e), sb));
+}
+
 // Pass 1: max |y| over the tensor. 16 bytes of each input per thread and step.
 __global__ void __launch_bounds__(kEltThreads) k_add_amax(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b,
                                                           int64_t n, unsigned int* amax_bits) {
@@ -159,7 +171,8 @@ __global__ void __launch_bounds__(kEltThreads) k_add_amax(const uint8_t* __restr
 #pragma unroll
         for (int w = 0; w < 4; ++w)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb)));
+            for (int e = 0; e < 4; ++e)
+                mx = fmaxf(mx, fabsf(add_one_x(wa[w] ^ 0x80808080u, wb[w] ^ 0x80808080u, e, sa, sb)));
     }
     if (blockIdx.x == 0)
         for (int64_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x)
@@ -184,7 +197,8 @@ __global__ void __launch_bounds__(kEltThreads) k_add_quant(const uint8_t* __rest
         for (int w = 0; w < 4; ++w) {
             int q[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) q[e] = quantize_bounded(add_one(byte_of(wa[w], e), byte_of(wb[w], e), sa, sb), inv);
+            for (int e = 0; e < 4; ++e)
+                q[e] = quantize_bounded(add_one_x(wa[w] ^ 0x80808080u, wb[w] ^ 0x80808080u, e, sa, sb), inv);
             o[w] = pack4(q[0], q[1], q[2], q[3]);
         }
         *reinterpret_cast<uint4*>(dst + 16 * i) = make_uint4(o[0], o[1], o[2], o[3]);
