@@ -756,7 +756,7 @@ constexpr int kDw1Out = 8;
 constexpr int kDw1Chunks = 4;                               // chunks of 2048 outputs per block
 constexpr int kDw1T = kDw1Out * kEltThreads * kDw1Chunks;   // outputs per block
 
-template <bool kQuant>
+template <bool kQuant, bool kBias, bool kRelu>
 __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned int* amax_bits,
                                                        uint8_t* __restrict__ dst) {
     constexpr int kWinBytes = kDw1T + 16;   // the block's outputs plus up to 8 taps, rounded
@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     for (int k = 0; k < d.KW; ++k) tw[k >> 2] |= (uint32_t)(uint8_t)wt[k] << (8 * (k & 3));
     __syncthreads();
     const float sc = __fmul_rn(i8s_scale_of(d.w, (int64_t)d.C * d.KW), i8s_scale_of(d.x, (int64_t)d.C * d.L));
-    const float bc = d.bias ? d.bias[c] : 0.0f;
+    const float bc = kBias ? d.bias[c] : 0.0f;
     float scale = 0.0f, inv = 0.0f;
     if (kQuant) {
         pdl_wait();   // the first pass's amax
@@ -782,8 +782,8 @@ __global__ void __launch_bounds__(kEltThreads) k_dw_s1(const DwArgs d, unsigned 
     // y of one accumulator, the same arithmetic in both passes
     auto y_of = [&](int acc) {
         float v = __fmul_rn(small_int_to_float(acc), sc);   // |acc| <= 64 * 128^2 < 2^22
-        if (d.bias) v = __fadd_rn(v, bc);
-        if (d.relu) v = v > 0.0f ? v : 0.0f;
+        if (kBias) v = __fadd_rn(v, bc);
+        if (kRelu) v = v > 0.0f ? v : 0.0f;
         return v;
     };
     // Pass 1 keeps the extremes of the live accumulators only. y_of is monotone in acc (an exact
@@ -1087,10 +1087,17 @@ cudaError_t launch_depthwise(const uint8_t* w, const uint8_t* x, const float* bi
     const DwArgs d{w, x, bias, (int)C, (int)L, (int)OL, KW, stride, pad_l, relu};
     if (stride == 1 && KW <= 8 && C <= 65535) {   // the 7-tap causal blocks: dp4a
         const dim3 g((unsigned)((OL + kDw1T - 1) / kDw1T), (unsigned)C);
-        k_dw_s1<false><<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_pdl(k_dw_s1<true>, g, dim3(kEltThreads), 0, s, d, amax_bits, dst);
+        // bias and ReLU as template parameters: no per-output test of either
+        auto run = [&](auto pass1, auto pass2) {
+            pass1<<<g, kEltThreads, 0, s>>>(d, amax_bits, dst);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            return launch_pdl(pass2, g, dim3(kEltThreads), 0, s, d, amax_bits, dst);
+        };
+        if (d.bias && d.relu) return run(k_dw_s1<false, true, true>, k_dw_s1<true, true, true>);
+        if (d.bias) return run(k_dw_s1<false, true, false>, k_dw_s1<true, true, false>);
+        if (d.relu) return run(k_dw_s1<false, false, true>, k_dw_s1<true, false, true>);
+        return run(k_dw_s1<false, false, false>, k_dw_s1<true, false, false>);
     }
     const int64_t W = (int64_t)(kDwT - 1) * stride + KW;
     if (C <= 65535 && KW <= 64 && W + KW <= 48 * 1024) {   // windowed kernel
