@@ -235,6 +235,19 @@ def test_depthwise(i2s, o, C, L, KW, stride, pad_l, pad_r, relu):
     same_bytes(host(got), ref)
 
 
+@pytest.mark.parametrize("with_bias,relu", [(False, False), (False, True), (True, False), (True, True)])
+def test_depthwise_stride1_bias_relu_combinations(i2s, o, with_bias, relu):
+    # the stride-1 kernel is built for each combination of bias and ReLU
+    C, L, KW = 40, 5000, 7
+    _, w = i8s_tensor(o, (C, KW), seed=17, scale=0.01)
+    _, x = i8s_tensor(o, (C, L), seed=18)
+    bias = synth.normal_f32(C, seed=19, std=0.1) if with_bias else None
+    got, OL = i2s.i8s_depthwise_mul_mat_add(dev(w), KW, dev(x), C, L, 1, KW - 1, 0,
+                                            bias=dev(bias) if with_bias else None, relu=relu)
+    ref, _ = o.i8s_depthwise_mul_mat_add(w, KW, x, C, L, 1, KW - 1, 0, bias=bias, relu=relu)
+    same_bytes(host(got), ref)
+
+
 def test_depthwise_no_bias_and_headroom(i2s, o):
     # every tap and input at +127 (acc = 7 * 127^2), no bias
     C, L, KW = 16, 300, 7
