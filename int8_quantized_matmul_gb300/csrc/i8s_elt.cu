@@ -336,10 +336,11 @@ __device__ __forceinline__ float row_factor16(const uint32_t (&w)[4 * V], float 
     return rms_factor(ssq, 16 * V, s, eps);
 }
 
-template <int V>
+template <int V, bool kGamma>
 __global__ void __launch_bounds__(kEltThreads) k_rms_rows_t(const uint8_t* __restrict__ x, int64_t rows, float eps,
-                                                            const float* __restrict__ gamma,
+                                                            const float* __restrict__ gamma_arg,
                                                             unsigned int* amax_bits) {
+    const float* gamma = kGamma ? gamma_arg : nullptr;   // known at compile time
     const float s = i8s_scale_of(x, rows * 16 * V);
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     float mx = 0.0f;
@@ -360,11 +361,12 @@ __global__ void __launch_bounds__(kEltThreads) k_rms_rows_t(const uint8_t* __res
     fold_max(mx, amax_bits);
 }
 
-template <int V>
+template <int V, bool kGamma>
 __global__ void __launch_bounds__(kEltThreads) k_rms_quant_t(const uint8_t* __restrict__ x, int64_t rows, float eps,
-                                                             const float* __restrict__ gamma,
+                                                             const float* __restrict__ gamma_arg,
                                                              const unsigned int* __restrict__ amax_bits,
                                                              uint8_t* __restrict__ dst) {
+    const float* gamma = kGamma ? gamma_arg : nullptr;   // known at compile time
     pdl_wait();   // the first pass's amax
     const float s = i8s_scale_of(x, rows * 16 * V);
     float scale, inv;
@@ -994,20 +996,31 @@ cudaError_t launch_add_scaled(const uint8_t* a, const uint8_t* b, int64_t n, uns
     return launch_pdl(k_add_quant, dim3(grid), dim3(kEltThreads), 0, s, a, b, n, (const unsigned int*)amax_bits, dst);
 }
 
+// the two passes of the short-row rms_norm (the second a programmatic dependent)
+template <int V, bool kGamma>
+cudaError_t run_rms_t(int grid, const uint8_t* x, int64_t rows, float eps, const float* gamma, unsigned int* amax_bits,
+                      uint8_t* dst, cudaStream_t s) {
+    k_rms_rows_t<V, kGamma><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_rms_quant_t<V, kGamma>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma,
+                      (const unsigned int*)amax_bits, dst);
+}
+
 cudaError_t launch_rms_norm_scaled(const uint8_t* x, int64_t rows, int64_t ne0, float eps, const float* gamma,
                                    float* rfac, unsigned int* amax_bits, uint8_t* dst, cudaStream_t s) {
     if (ne0 % 16 == 0 && ne0 <= 64) {   // short rows: one thread per row
         const int grid = elt_grid(rows);
         cudaError_t e = cudaSuccess;
         switch (ne0 / 16) {
-            case 1: k_rms_rows_t<1><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    e = launch_pdl(k_rms_quant_t<1>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
-            case 2: k_rms_rows_t<2><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    e = launch_pdl(k_rms_quant_t<2>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
-            case 3: k_rms_rows_t<3><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                    e = launch_pdl(k_rms_quant_t<3>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
-            default: k_rms_rows_t<4><<<grid, kEltThreads, 0, s>>>(x, rows, eps, gamma, amax_bits);
-                     e = launch_pdl(k_rms_quant_t<4>, dim3(grid), dim3(kEltThreads), 0, s, x, rows, eps, gamma, (const unsigned int*)amax_bits, dst); break;
+            case 1: e = gamma ? run_rms_t<1, true>(grid, x, rows, eps, gamma, amax_bits, dst, s)
+                              : run_rms_t<1, false>(grid, x, rows, eps, gamma, amax_bits, dst, s); break;
+            case 2: e = gamma ? run_rms_t<2, true>(grid, x, rows, eps, gamma, amax_bits, dst, s)
+                              : run_rms_t<2, false>(grid, x, rows, eps, gamma, amax_bits, dst, s); break;
+            case 3: e = gamma ? run_rms_t<3, true>(grid, x, rows, eps, gamma, amax_bits, dst, s)
+                              : run_rms_t<3, false>(grid, x, rows, eps, gamma, amax_bits, dst, s); break;
+            default: e = gamma ? run_rms_t<4, true>(grid, x, rows, eps, gamma, amax_bits, dst, s)
+                               : run_rms_t<4, false>(grid, x, rows, eps, gamma, amax_bits, dst, s); break;
         }
         return e != cudaSuccess ? e : cudaGetLastError();
     }
