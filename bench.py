@@ -129,6 +129,12 @@ def make_weights(torch, device, seed_base=0):
     return ws
 
 
+def tile_weights(i2s, weights):
+    """The same weights in the tiled layout (i2s_tile_weights): written once,
+    before any timing, as a model loader would lay them out."""
+    return [[i2s.tile_weights(w, N, K) for w, (_, N, K) in zip(layer, PROJ)] for layer in weights]
+
+
 ACT_OF = {"q": 0, "k": 0, "v": 0, "o": 1, "gate": 2, "up": 2, "down": 3}   # shared layer inputs
 ACT_K = (1536, 1536, 1536, 8960)
 
@@ -229,15 +235,20 @@ I8S_PROFILE = os.path.join(ROOT, "profiles", "k_i8s_gemm_tc_encoder_fc.md")
 I8S_SOURCES = ["i8s_tc.cu", "tc.cuh", "common.cuh", "internal.h"]
 
 
-def run_prefill(torch, i2s, weights, device, peaks, steps=5):
+def run_prefill(torch, i2s, weights, device, peaks, steps=5, tiled=False):
     """Prefill shape: the 28-layer set plus the lm_head at M = 512 activation
     rows (F32 ~N(0,1), 1% outliers x20), one grouped quantize launch and one
-    grouped tensor-core GEMM launch; int-ops = 2*M*N*K summed over projections."""
+    grouped tensor-core GEMM launch; int-ops = 2*M*N*K summed over projections.
+    `weights` are I2_S bytes; with tiled=True the GEMM reads their tiled layout
+    (written once, before timing)."""
     M = 512
     name, N_lm, K_lm = synth.QWEN2_1P5B_LM_HEAD
     lm = torch.cat([synth.packed_code_bytes_device(N_lm * K_lm // 4, 777, device),
                     torch.tensor(list(np.frombuffer(np.float32(0.02).tobytes(), np.uint8)) + [0] * 28,
                                  dtype=torch.uint8, device=device)])
+    if tiled:
+        weights = tile_weights(i2s, weights)
+        lm = i2s.tile_weights(lm, N_lm, K_lm)
     problems, outs = [], []
     ops = 0
     for layer in range(LAYERS):
@@ -286,6 +297,7 @@ def run_prefill(torch, i2s, weights, device, peaks, steps=5):
     peak = 2.0 * bf16
     return {"workload": "qwen2-1.5b projection set x28 layers + lm_head 1536->151936, M=512 (pp512 shape)",
             "metric": "prefill int8 TOPS (exact integer dot on tcgen05 kind::mxf4)", "int_ops": ops,
+            "weights": "tiled layout (i2s_tile_weights, written once before timing)" if tiled else "I2_S bytes",
             "gemm_ms": g_ms, "quant_ms": q_ms, "value": tops, "unit": "TOPS",
             "e2e_device_tops": ops / ((g_ms + q_ms) * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "kernel": "k_i2s_gemm_tc", "achieved": tops, "peak": peak,
@@ -662,29 +674,13 @@ def job_rate(world, steps, bytes_per_step, max_ms):
     return world * steps * bytes_per_step / (max_ms * 1e-3) / 1e9
 
 
-def run_ours(args, rank, world, torch, dist):
-    from int8_quantized_matmul_gb300 import build as libbuild
-    libbuild.build()
-    from int8_quantized_matmul_gb300 import i2s
-
-    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(device)
-    peaks = load_peaks()
-    weights = make_weights(torch, device)
-    passes = [DecodePass(torch, i2s, weights, M, device, seed=100 + M) for M in (1, 8)]
-    stream = torch.cuda.current_stream()
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    # A step is captured once as one CUDA graph: the M = 1 and M = 8 passes
-    # are independent batches with their own workspaces, so they are two
-    # branches of the graph (quantize, then run, each; 4 kernel launches, no
-    # host-side marshalling), and one pass's first kernels can take the SMs
-    # that the other's last CTAs leave. Each phase is also captured on its
-    # own, for the per-launch timings below.
+def capture_step(torch, passes, device):
+    """A decode step captured once as one CUDA graph: the M = 1 and M = 8
+    passes are independent batches with their own workspaces, so they are two
+    branches of the graph (quantize, then run, each; 4 kernel launches, no
+    host-side marshalling), and one pass's first kernels can take the SMs that
+    the other's last CTAs leave. Each phase is also captured on its own, for
+    the per-launch timings. Returns (step graph, [(quantize, run) per pass])."""
     for p in passes:
         p.group()
     torch.cuda.synchronize()
@@ -714,6 +710,75 @@ def run_ours(args, rank, world, torch, dist):
                 join.record(branch)
             cap.wait_event(join)
     torch.cuda.synchronize()
+    return step_graph, graphs
+
+
+def gemv_in_stream_ms(torch, passes, stream, steps):
+    """Each pass's GEMV launch duration: after one quantization, the pass's run
+    launched B2B times in a row on the stream, each launch a programmatic
+    dependent of the one before (as the GEMV follows the quantizer in the step
+    graph), CUDA events around them; the median over `steps` runs. A run leaves
+    the split-K state at zero, so every launch computes the full pass."""
+    out = []
+    for p in passes:
+        p.group.quantize()
+        evs = []
+        for _ in range(steps):
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(B2B):
+                p.group.run()
+            eb.record(stream)
+            evs.append((ea, eb))
+        out.append(evs)
+    torch.cuda.synchronize()
+    return [statistics.median(ea.elapsed_time(eb) / B2B for ea, eb in evs) for evs in out]
+
+
+def run_decode_i2s_layout(torch, i2s, weights, device, stream, peaks, steps):
+    """The headline step on the I2_S bytes as they are (the GEMV loads each
+    stage as a TMA tile of 128 row pieces): same graph, same timing."""
+    passes = [DecodePass(torch, i2s, weights, M, device, seed=100 + M) for M in (1, 8)]
+    step_graph, _ = capture_step(torch, passes, device)
+    for _ in range(20):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step_graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    gemv = gemv_in_stream_ms(torch, passes, stream, steps)
+    achieved = sum(p.gemv_bytes for p in passes) / sum(gemv) / 1e6
+    return {"value": steps * WEIGHT_BYTES_PER_PASS * len(passes) / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": ms / steps,
+            "gemv_ms_in_stream": {str(p.M): g for p, g in zip(passes, gemv)},
+            "gemv_achieved_gbs": achieved, "gemv_frac": achieved / peaks["hbm_gbs"],
+            "status": [i2s.read_status(p.group.ws) for p in passes],
+            "note": "the same step on the I2_S bytes, not tiled: each weight stage a TMA tile of 128 row pieces"}
+
+
+def run_ours(args, rank, world, torch, dist):
+    from int8_quantized_matmul_gb300 import build as libbuild
+    libbuild.build()
+    from int8_quantized_matmul_gb300 import i2s
+
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    weights = make_weights(torch, device)
+    tiled = tile_weights(i2s, weights)   # the weights every timed decode call reads
+    passes = [DecodePass(torch, i2s, tiled, M, device, seed=100 + M) for M in (1, 8)]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    step_graph, graphs = capture_step(torch, passes, device)
 
     def one_step():
         step_graph.replay()
@@ -753,24 +818,8 @@ def run_ours(args, rank, world, torch, dist):
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in passes] for _ in range(args.steps)]
     for s in range(args.steps):
         one_step_phases(events[s])
-    # the GEMV's own launch duration: after one quantization, each pass's run
-    # launched B2B times in a row on the stream, each launch a programmatic
-    # dependent of the one before (as the GEMV follows the quantizer in the
-    # step graph), CUDA events around the B2B launches. A run leaves the
-    # split-K state at zero, so every launch computes the full pass. The
-    # per-phase graphs above add each replayed graph's launch to the time.
-    b2b_ev = []
-    for p in passes:
-        p.group.quantize()
-        evs = []
-        for s in range(args.steps):
-            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ea.record(stream)
-            for _ in range(B2B):
-                p.group.run()
-            eb.record(stream)
-            evs.append((ea, eb))
-        b2b_ev.append(evs)
+    # the GEMV's own launch duration, launched back to back in the stream
+    b2b_ms = gemv_in_stream_ms(torch, passes, stream, args.steps)
     barrier()
     clk = clocks.stop()
     total_ms = max_over_ranks(torch, dist, t_start.elapsed_time(t_end), device)
@@ -792,11 +841,8 @@ def run_ours(args, rank, world, torch, dist):
     gemv_avg_ms = sum(gemv_ms_all) / len(gemv_ms_all)
     gemv_avg_bytes = sum(gemv_bytes_all) / len(gemv_bytes_all)
     iso_achieved = gemv_avg_bytes / (gemv_avg_ms * 1e-3) / 1e9
-    b2b_ms = []
-    for k, p in enumerate(passes):
-        per = statistics.median(ea.elapsed_time(eb) / B2B for ea, eb in b2b_ev[k])
+    for p, per in zip(passes, b2b_ms):
         per_m[str(p.M)]["gemv_ms_in_stream"] = per
-        b2b_ms.append(per)
     b2b_avg_ms = sum(b2b_ms) / len(b2b_ms)
     b2b_avg_bytes = sum(p.gemv_bytes for p in passes) / len(passes)
     achieved = b2b_avg_bytes / (b2b_avg_ms * 1e-3) / 1e9
@@ -856,8 +902,13 @@ def run_ours(args, rank, world, torch, dist):
            "note": "the two passes run on two streams; steps are serial"}
 
     fused = run_decode_fused(torch, i2s, passes, stream, args.steps)
+    i2s_layout = run_decode_i2s_layout(torch, i2s, weights, device, stream, peaks, args.steps)
     per_projection = run_decode_per_projection(torch, i2s, passes, weights, device)
-    prefill = run_prefill(torch, i2s, weights, device, peaks) if not args.no_prefill else None
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(torch, i2s, weights, device, peaks)
+        on_tiled = run_prefill(torch, i2s, weights, device, peaks, tiled=True)
+        prefill["tiled_layout"] = {k: on_tiled[k] for k in ("value", "unit", "gemm_ms", "weights", "status")}
     encoder = run_encoder_fc(torch, i2s, device, peaks) if not args.no_prefill else None
     eltwise = run_encoder_eltwise(torch, i2s, device, peaks) if not args.no_prefill else None
     w8a8 = run_w8a8_prefill(torch, i2s, device, peaks) if not args.no_prefill else None
@@ -868,10 +919,13 @@ def run_ours(args, rank, world, torch, dist):
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "layers": LAYERS, "M": [1, 8], "launch": "one CUDA graph per step (4 kernels; the M=1 and M=8 passes as two branches)",
                    "weight_bytes_per_pass": WEIGHT_BYTES_PER_PASS, "parallelism": f"replicas x{world}",
+                   "weights": "tiled layout (i2s_tile_weights: the I2_S bytes in contiguous 16 KB blocks, written "
+                              "once before timing); the I2_S layout's step is decode_i2s_layout",
                    "l2": "inputs larger than L2: 327.5 MB of codes per pass vs 129 MB L2, streamed once per pass"},
         "clocks": clk,
         "e2e": e2e,
         "decode_fused": fused,
+        "decode_i2s_layout": i2s_layout,
         "gpu_launches": 2 * len(passes) * args.steps,
         "roofline": {"bound": "hbm", "kernel": "k_i2s_gemv_tc", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_gemv_traffic(),

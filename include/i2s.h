@@ -112,6 +112,33 @@ int i2s_pack_host(const uint8_t* codes, int64_t N, int64_t K, float w_scale, voi
 int i8s_pack_host(const int8_t* q, int64_t n, float scale, void* dst);
 
 /* ---------------------------------------------------------------------------
+ * Tiled I2_S weights: the bytes of an I2_S tensor rearranged once, at load
+ * time, into contiguous 16 KB blocks. The GEMV and GEMM kernels read each
+ * block with one bulk copy instead of a strided tile of 128 row pieces, and
+ * give the same results, bit for bit, as on the I2_S bytes.
+ *
+ * Layout: the rows are split into Tn = 2*ceil(N/256) blocks of 128 rows, each
+ * row's K/4 bytes into Tk = ceil(K/512) blocks of 128 bytes. Block (i, j)
+ * holds bytes 128j..128j+127 of rows 128i..128i+127 and starts at byte
+ * (i*Tk + j)*16384. Row rr of a block starts at byte rr*128 of it, and the
+ * row's 16-byte piece c (its bytes 16c..16c+15 of the block) is stored as
+ * piece c ^ (rr % 8). Bytes of rows past N or past K/4 are zero. The I2_S
+ * tensor's 32-byte trailer (the F32 weight scale first) follows at
+ * Tn*Tk*16384.
+ * ------------------------------------------------------------------------- */
+#define I2S_LAYOUT_I2S 0u     /* i2s_problem::w_layout: w_i2s holds I2_S bytes */
+#define I2S_LAYOUT_TILED 1u   /* w_i2s holds the tiled layout (i2s_tile_weights) */
+size_t i2s_tiled_nbytes(int64_t N, int64_t K);        /* Tn*Tk*16384 + 32 */
+size_t i2s_tiled_scale_offset(int64_t N, int64_t K);  /* Tn*Tk*16384 */
+
+/* Writes the tiled layout of the I2_S weights w_i2s (device,
+ * i2s_nbytes(N, K) bytes) into tiled (device, i2s_tiled_nbytes(N, K) bytes),
+ * enqueued on stream. N and K as for i2s_mul_mat. Errors: BAD_SHAPE,
+ * NULL_PTR, MISALIGNED (a pointer not 16-byte aligned), BAD_ARG (the buffers
+ * overlap), CUDA. */
+int i2s_tile_weights(const void* w_i2s, int64_t N, int64_t K, void* tiled, i2s_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Activation quantization, per row ([P2] Arithmetic and the threading
  * paragraph of Kernels; [P3] Encoder for the 1e-5 floor; [P4] Implementation
  * for scale = amax/127, inv = 127/amax, round, clamp +-127).
@@ -232,16 +259,19 @@ int i2s_noalloc_read_status(i2s_stream_t stream);
  * count  1 .. I2S_MAX_GROUP.
  * ws     device workspace of at least i2s_mul_mat_grouped_workspace() bytes.
  * Requirements per problem as for i2s_mul_mat.
- * Errors: as i2s_mul_mat, plus BAD_ARG for count out of range.
+ * Errors: as i2s_mul_mat, plus BAD_ARG for count out of range or a w_layout
+ * other than I2S_LAYOUT_I2S and I2S_LAYOUT_TILED.
  * ------------------------------------------------------------------------- */
 #define I2S_MAX_GROUP 256
 
 typedef struct i2s_problem {
-    const void* w_i2s; /* device, I2_S N x K */
+    const void* w_i2s; /* device, I2_S N x K (or its tiled layout, below) */
     int64_t N;
     int64_t K;
     const float* x;    /* device, M x K F32 */
     float* y;          /* device, M x N F32 */
+    unsigned w_layout; /* I2S_LAYOUT_I2S (0) or I2S_LAYOUT_TILED; other values BAD_ARG.
+                          A group may mix the two. */
 } i2s_problem;
 
 size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M);

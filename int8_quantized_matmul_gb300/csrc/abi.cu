@@ -124,7 +124,7 @@ const char* i2s_status_string(int status) {
     }
 }
 
-int i2s_version(void) { return 100; }
+int i2s_version(void) { return 200; }
 
 int i2s_device_supported(void) {
     const int r = check_device();
@@ -141,6 +141,32 @@ size_t i2s_scale_offset(int64_t N, int64_t K) {
     if (N < 1 || K < 128 || K % 128) return 0;
     return (size_t)N * (size_t)K / 4;
 }
+size_t i2s_tiled_scale_offset(int64_t N, int64_t K) {
+    if (N < 1 || K < 128 || K % 128) return 0;
+    return tiled_scale_offset(N, K);
+}
+size_t i2s_tiled_nbytes(int64_t N, int64_t K) {
+    const size_t off = i2s_tiled_scale_offset(N, K);
+    return off ? off + 32 : 0;
+}
+
+int i2s_tile_weights(const void* w_i2s, int64_t N, int64_t K, void* tiled, i2s_stream_t stream) {
+    if (!w_i2s || !tiled) return I2S_E_NULL_PTR;
+    if (!i2s_shape_ok(N, K, 1)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(w_i2s) || !aligned16(tiled)) return I2S_E_MISALIGNED;
+    const uintptr_t a0 = (uintptr_t)w_i2s, a1 = a0 + i2s_nbytes(N, K);
+    const uintptr_t b0 = (uintptr_t)tiled, b1 = b0 + i2s_tiled_nbytes(N, K);
+    if (a0 < b1 && b0 < a1) return I2S_E_BAD_ARG;   // the buffers overlap
+    int r = check_device();
+    if (r) return r;
+    const uint8_t* w = static_cast<const uint8_t*>(w_i2s);
+    uint8_t* t = static_cast<uint8_t*>(tiled);
+    r = cuda_status(launch_i2s_tile(w, N, K, t, stream));
+    if (r) return r;
+    return cuda_status(cudaMemcpyAsync(t + tiled_scale_offset(N, K), w + i2s_scale_offset(N, K), 32,
+                                       cudaMemcpyDeviceToDevice, stream));
+}
+
 size_t i8s_nbytes(int64_t n) { return n < 1 ? 0 : (size_t)round_up(n, 32) + 32; }
 size_t i8s_scale_offset(int64_t n) { return n < 1 ? 0 : (size_t)round_up(n, 32); }
 
@@ -221,7 +247,7 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     const int path = config ? config->path : 0;
     if (path != 0 && path != 2 && path != 3) return I2S_E_BAD_ARG;
     if (path == 3 && M > 16) return I2S_E_BAD_ARG;
-    i2s_problem p{w_i2s, N, K, x, y};
+    i2s_problem p{w_i2s, N, K, x, y, I2S_LAYOUT_I2S};
     if (path == 2 || (path == 0 && M > 16)) return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
     if (config && config->test_stall_cycles < 0) return I2S_E_BAD_ARG;
     return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3,
@@ -234,6 +260,22 @@ int i2s_mul_mat(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t
 }
 
 // Distinct activations of a group, in first-use order.
+// The checks every grouped entry point makes on each problem, in this order.
+static int check_problem(const i2s_problem& p, int64_t M) {
+    if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
+    if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
+    if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+    if (p.w_layout != I2S_LAYOUT_I2S && p.w_layout != I2S_LAYOUT_TILED) return I2S_E_BAD_ARG;
+    return I2S_OK;
+}
+
+// Bit i set: problem i's weights are in the tiled layout.
+static void fill_tiled_mask(uint32_t* mask, const i2s_problem* probs, int count) {
+    for (int w = 0; w < kTiledMaskWords; ++w) mask[w] = 0;
+    for (int i = 0; i < count; ++i)
+        if (probs[i].w_layout == I2S_LAYOUT_TILED) mask[i >> 5] |= 1u << (i & 31);
+}
+
 static int group_acts(const i2s_problem* probs, int count, std::vector<int>& act_of,
                       std::vector<int>& first) {
     act_of.assign(count, -1);
@@ -269,7 +311,7 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
     int r;
     if (phases & 1) {
         static thread_local QuantArgs qa;
-        if (!make_code_map_template(&qa.wtmpl, probs[0].w_i2s)) return I2S_E_CUDA;
+        if (!make_u8_operand_map(&qa.wtmpl, wmaps, kTcTileW, 128, kTcTileW)) return I2S_E_CUDA;
         qa.wmaps = wmaps;
         qa.n_wmaps = count;
         for (int i = 0; i < count; ++i) qa.wj[i] = WMapJob{probs[i].w_i2s, (int)probs[i].N, (int)probs[i].K};
@@ -324,6 +366,7 @@ static int run_gemm_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
             tiles += (int)((q.N + 2 * kTcTileW - 1) / (2 * kTcTileW)) * n_act_tiles;   // 256-row tiles, one CTA pair each
         }
         ta.total_tiles = tiles;
+        fill_tiled_mask(ta.tiled, probs, count);
         const int sms = device_sm_count();
         int pairs = (grid_ctas > 0 ? grid_ctas : sms) / 2;   // clusters of two CTAs
         const int resident = gemm_tc_max_pairs();   // a persistent grid: no second wave
@@ -427,6 +470,7 @@ static int run_gemv_tc(const i2s_problem* probs, int count, int64_t M, void* ws,
             units += row_tiles * chunks;
         }
         ta.total_tiles = units;
+        fill_tiled_mask(ta.tiled, probs, count);
         const int tiles = units;
         const int cap = 2 * device_sm_count();
         int grid = grid_ctas > 0 ? grid_ctas : cap;
@@ -511,9 +555,7 @@ static int fused_check(const i2s_problem* probs, int count, int64_t M) {
     if (M < 1 || M > 16) return I2S_E_BAD_SHAPE;
     for (int i = 0; i < count; ++i) {
         const i2s_problem& p = probs[i];
-        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
-        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
-        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+        if (const int r = check_problem(p, M)) return r;
     }
     return I2S_OK;
 }
@@ -600,6 +642,7 @@ int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, vo
     fa.ticket_base = reinterpret_cast<uint32_t*>(base + pl.ticket_off);
     fa.n_acts = pl.n_act;
     fa.count = count;
+    fill_tiled_mask(fa.tiled, probs, count);
     fa.M = (int)M;
     fa.BN = Mp;
     int units = 0;
@@ -633,6 +676,8 @@ int i2s_mul_mat_grouped_fused(const i2s_problem* probs, int count, int64_t M, vo
 
 size_t i2s_mul_mat_grouped_workspace(const i2s_problem* probs, int count, int64_t M) {
     if (!probs || count < 1 || count > I2S_MAX_GROUP) return 0;
+    for (int i = 0; i < count; ++i)
+        if (probs[i].w_layout != I2S_LAYOUT_I2S && probs[i].w_layout != I2S_LAYOUT_TILED) return 0;
     std::vector<int> act_of, first;
     group_acts(probs, count, act_of, first);
     size_t total = kHeader;
@@ -668,9 +713,7 @@ static int grouped_impl(const i2s_problem* probs, int count, int64_t M, void* ws
     if (count < 1 || count > I2S_MAX_GROUP) return I2S_E_BAD_ARG;
     for (int i = 0; i < count; ++i) {
         const i2s_problem& p = probs[i];
-        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
-        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
-        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+        if (const int r = check_problem(p, M)) return r;
     }
     if (!aligned256(ws)) return I2S_E_MISALIGNED;
     if (ws_bytes < i2s_mul_mat_grouped_workspace(probs, count, M)) return I2S_E_WORKSPACE_TOO_SMALL;
@@ -746,9 +789,7 @@ static int host_plan(const i2s_problem* probs, int count, int64_t M, HostPlan& p
     std::vector<std::pair<uintptr_t, uintptr_t>> xr, yr;
     for (int i = 0; i < count; ++i) {
         const i2s_problem& p = probs[i];
-        if (!p.w_i2s || !p.x || !p.y) return I2S_E_NULL_PTR;
-        if (!i2s_shape_ok(p.N, p.K, M)) return I2S_E_BAD_SHAPE;
-        if (!aligned16(p.w_i2s) || !aligned16(p.x) || !aligned16(p.y)) return I2S_E_MISALIGNED;
+        if (const int r = check_problem(p, M)) return r;
         const uintptr_t x = (uintptr_t)p.x, y = (uintptr_t)p.y;
         xr.push_back({x, x + (uintptr_t)(M * p.K) * 4});
         yr.push_back({y, y + (uintptr_t)(M * p.N) * 4});

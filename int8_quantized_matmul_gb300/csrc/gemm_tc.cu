@@ -39,9 +39,11 @@
 //   warps 13-15 MMA issue (one lane each; warp 13 also allocates TMEM): one
 //              thread needs about a hundred cycles to issue an MMA, more than
 //              the MMA's tensor time, so three take the stages in turn;
-//   warp 16    TMA producer of the packed codes: a six-stage ring of 128 rows
-//              x 64 bytes (64-byte swizzle) that runs ahead of the operand
-//              ring, so the converters never wait on global loads.
+//   warp 16    producer of the packed codes: a three-stage ring of 128 rows
+//              x 128 bytes (two operand stages, 128-byte swizzle) that runs
+//              ahead of the operand ring, so the converters never wait on
+//              global loads; one TMA tile per stage, or on tiled weights one
+//              bulk copy of a block that is already in the ring's layout.
 // CTA pairs: the kernel runs on clusters of two CTAs on two SMs driving
 // cta_group::2 MMAs. A tile is 256 weight rows (128 converted into each CTA's
 // TMEM, 128 accumulator rows in each CTA's TMEM) x BN <= 128 activation rows
@@ -84,8 +86,9 @@ constexpr int kCodeWarp = 16;               // TMA producer of the packed codes
 constexpr int kIssuersTc = 3;
 constexpr int kThreadsTc = 544;
 constexpr int kStagesTc = 6;
-constexpr int kCodeStages = 6;              // ring of packed-code stages, ahead of the operand ring
-constexpr int kCodeStageBytes = 128 * 64;   // 128 weight rows x 64 packed bytes (256 positions)
+constexpr int kCodeStages = 3;              // ring of packed-code stages, ahead of the operand ring
+constexpr int kCodeStageBytes = 128 * 128;  // 128 weight rows x 128 packed bytes (512 positions: two operand stages)
+static_assert(kCodeStageBytes == kTiledBlockBytes, "a code stage is one block of tiled weights");
 constexpr int kBlockK = 256;                // K positions per stage (one 128-byte row of e2m1)
 constexpr int kTileW = 128;                 // weight rows per CTA (half of the pair's MMA M)
 constexpr int kBPlaneMax = 64 * 128;        // one digit plane of this CTA's half of up to 128 activation rows
@@ -99,7 +102,6 @@ constexpr uint32_t kACol0 = 320;            // the A ring in TMEM: one stage of 
 constexpr uint32_t kAStageCols = 32;        //   (eight per 32-bit column) per kAStageCols columns
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks
 static_assert(kStagesTc % kIssuersTc == 0, "ring slots per issuer");
-static_assert(kCodeStages % 2 == 0, "converters take stages in pairs");
 static_assert(kSfbCol0 + 3 * kSfCols <= kACol0, "TMEM budget: scales below the A ring");
 static_assert(kACol0 + kStagesTc * kAStageCols <= (uint32_t)kTmemCols, "TMEM budget: the A ring");
 
@@ -286,10 +288,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp == kCodeWarp) {
         // ------------------------------------------------------- code producer
-        // per stage: this CTA's 128 weight rows x 64 packed bytes of the tile
-        // (rows past N and bytes past K/4 are zero-filled), from the problem's
-        // map (written by the quantization launch), into a ring that runs
-        // ahead of the operand stages
+        // per stage: this CTA's 128 weight rows x 128 packed bytes of the
+        // tile (rows past N and bytes past K/4 are zero-filled), from the
+        // problem's map (written by the quantization launch), into a ring that
+        // runs ahead of the operand stages; on tiled weights the stage is one
+        // 16 KB block, already in the ring's layout: one bulk copy
         if (lane == 0) {
             int cs = 0;
             uint32_t cphase = 0;
@@ -308,10 +311,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 const int wt = (tile - P.tile0) / P.n_act_tiles;
                 const int n0 = wt * (2 * kTileW) + (int)rank * kTileW;
                 const int KB = P.K / kBlockK + (P.K % kBlockK ? 1 : 0);
-                for (int kb = 0; kb < KB; ++kb) {
+                const bool tiled = (a.tiled[pi >> 5] >> (pi & 31)) & 1u;
+                // tiled: this CTA's row block; its column blocks follow one another
+                const uint8_t* blk = P.w + (size_t)(n0 / kTiledRows) * tiled_col_blocks(P.K) * kTiledBlockBytes;
+                for (int kb = 0; kb < KB; kb += 2) {   // one code stage per two operand stages
                     if (!tc::mbar_wait(&S.code_empty[cs], cphase ^ 1, abort_flag, kWaitLimit)) { fail(32); ok = false; break; }
                     tc::mbar_arrive_expect_tx(&S.code_full[cs], kCodeStageBytes);
-                    tc::tma_load_2d(sC + (size_t)cs * kCodeStageBytes, map, kb * 64, n0, &S.code_full[cs]);
+                    if (tiled)
+                        tc::bulk_load(sC + (size_t)cs * kCodeStageBytes, blk + (size_t)(kb / 2) * kTiledBlockBytes,
+                                      kCodeStageBytes, &S.code_full[cs]);
+                    else
+                        tc::tma_load_2d(sC + (size_t)cs * kCodeStageBytes, map, kb * 64, n0, &S.code_full[cs]);
                     pending[cs] = true;
                     pending_phase[cs] = cphase;
                     if (++cs == kCodeStages) { cs = 0; cphase ^= 1; }
@@ -323,9 +333,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kCvtWarps) {
         // ---------------------------------------------------------- converters
-        // one thread per weight row: per stage the row's 64 packed bytes (two
-        // 128-position groups), read from the code ring (64-byte swizzle),
-        // become the 128 bytes of e2m1 operands of the stage row
+        // one thread per weight row: per operand stage the row's 64 packed
+        // bytes (two 128-position groups), read from a code stage (128-byte
+        // swizzle; one code stage holds two operand stages), become the 128
+        // bytes of e2m1 operands of the stage row
         const int r = tid - kEpiWarps * 32;   // weight row within the CTA's half of the tile
         // = TMEM lane: converter warp w reaches lane quarter w % 4
         const uint32_t lane_a = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kACol0;
@@ -342,27 +353,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 const bool two = kb + 1 < KB;
                 const int stage1 = stage + 1 == kStagesTc ? 0 : stage + 1;
                 const uint32_t phase1 = stage + 1 == kStagesTc ? phase ^ 1 : phase;
-                const int cs1 = cs + 1 == kCodeStages ? 0 : cs + 1;
-                const uint32_t cphase1 = cs + 1 == kCodeStages ? cphase ^ 1 : cphase;
                 // the codes first (their slots free as soon as they are in
                 // registers), then the operand slots; warp-uniform outcomes
                 bool got = tc::mbar_wait(&S.code_full[cs], cphase, abort_flag, kWaitLimit);
-                if (got && two) got = tc::mbar_wait(&S.code_full[cs1], cphase1, abort_flag, kWaitLimit);
                 if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
                 uint4 v[2][4];
+                {
+                    const uint8_t* src = sC + (size_t)cs * kCodeStageBytes;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint8_t* src = sC + (size_t)(h ? cs1 : cs) * kCodeStageBytes + (size_t)r * 64;
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[h][c] = (h == 1 && !two) ? make_uint4(0u, 0u, 0u, 0u)
-                                                   : *reinterpret_cast<const uint4*>(src + ((c ^ ((r >> 1) & 3)) << 4));
+                        for (int c = 0; c < 4; ++c)   // operand stage h: 16-byte pieces 4h..4h+3 of the row
+                            v[h][c] = (h == 1 && !two) ? make_uint4(0u, 0u, 0u, 0u)
+                                                       : *reinterpret_cast<const uint4*>(src + tc::sw128_offset(r, 4 * h + c));
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(&S.code_empty[cs]);
-                    if (two) tc::mbar_arrive(&S.code_empty[cs1]);
-                }
+                if (lane == 0) tc::mbar_arrive(&S.code_empty[cs]);
                 got = tc::mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, kWaitLimit);
                 if (got && two) got = tc::mbar_wait(&S.empty[stage1], phase1 ^ 1, abort_flag, kWaitLimit);
                 if (!__all_sync(0xffffffffu, got)) { fail(2); ok = false; break; }
@@ -400,9 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
                 stage = stage1;
                 phase = phase1;
                 if (two && ++stage == kStagesTc) { stage = 0; phase ^= 1; }
-                cs = cs1;
-                cphase = cphase1;
-                if (two && ++cs == kCodeStages) { cs = 0; cphase ^= 1; }
+                if (++cs == kCodeStages) { cs = 0; cphase ^= 1; }
             }
         }
     } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuersTc && rank == 0) {
@@ -504,7 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) k_i2s
             // row_sum[m]) in shared memory while the accumulator fills
             const int m_base = at * BN;
             {
-                const float w_scale = *reinterpret_cast<const float*>(P.w + (size_t)P.N * (P.K / 4));
+                const bool tiled = (a.tiled[pi >> 5] >> (pi & 31)) & 1u;
+                const float w_scale = *reinterpret_cast<const float*>(
+                    P.w + (tiled ? tiled_scale_offset(P.N, P.K) : (size_t)P.N * (P.K / 4)));
                 float* sc_col = S.sc_col[acc];
                 float* rs_col = S.rs_col[acc];
                 for (int j = tid; j < BN; j += kEpiWarps * 32) {
@@ -652,22 +658,6 @@ bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_b
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Template of the per-problem maps of the packed codes (written into the
-// workspace by the quantization launch, which replaces address, extents and
-// stride): uint8 2-D, box 64 bytes x 128 rows, 64-byte swizzle.
-bool make_code_map_template(CUtensorMap* map, const void* base) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    std::memset(map, 0, sizeof(*map));
-    cuuint64_t dims[2] = {64u, 128u};
-    cuuint64_t strides[1] = {64u};
-    cuuint32_t box[2] = {64u, 128u};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

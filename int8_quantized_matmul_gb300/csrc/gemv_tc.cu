@@ -74,6 +74,7 @@ constexpr int kBRingBytes = 36 * 1024; // activation ring: 4 stages of 8 KB (M' 
 constexpr int kBStagesMax = 8;
 constexpr int kTileRows = 128;
 constexpr int kWStageBytes = kTileRows * kStageBytes;
+static_assert(kWStageBytes == kTiledBlockBytes && kStageBytes == kTiledRowBytes, "a weight stage is one block of tiled weights");
 constexpr uint32_t kTmemColsGv = 256;
 // TMEM columns: A stages 0..127, accumulator 0 at 128 (up to 48 columns),
 // block scales 176..191, accumulator 1 at 192.
@@ -100,7 +101,7 @@ struct SmemGv {
     int final_flag;
 };
 
-constexpr size_t kSProbBytes = 72;      // shared copy of one problem-table entry (SProb)
+constexpr size_t kSProbBytes = 80;      // shared copy of one problem-table entry (SProb)
 constexpr size_t kSmemGvUsed = 1024 + (size_t)kBRingBytes + (size_t)kWStages * kWStageBytes + sizeof(SmemGv) + 16 +
                                (size_t)kMaxGroup * kSProbBytes;
 // At least 80 KB so that at most two CTAs share an SM: each holds 256 of the
@@ -118,6 +119,7 @@ struct SProb {
     int N, K, map, unit0, chunks, dot_off, ticket_off, pidx;
     int row0;   // first row of the activation operand in its map (fused launch: stacked operands)
     int act;    // activation index (fused launch: its ready counter)
+    int tiled;  // the weights are in the tiled layout (i2s_tile_weights)
 };
 
 constexpr int kChunkStages = kGemvChunkPositions / kKB;   // 3 stages per work unit
@@ -130,7 +132,7 @@ struct Seg {
     const float* act_scale;
     const int32_t* row_sum;
     float* y;
-    int N, K, map, pidx, sidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units, row0, act;
+    int N, K, map, pidx, sidx, n0, tile, st_lo, st_hi, c_lo, c_hi, chunks, dot_off, ticket_off, units, row0, act, tiled;
     bool live;
 };
 
@@ -159,6 +161,7 @@ __device__ __forceinline__ Seg seg_at(const SProb* sp, int n_sp, int u, int u_hi
     g.pidx = P.pidx;
     g.row0 = P.row0;
     g.act = P.act;
+    g.tiled = P.tiled;
     g.chunks = P.chunks;
     g.dot_off = P.dot_off;
     g.ticket_off = P.ticket_off;
@@ -198,6 +201,7 @@ __device__ __forceinline__ Seg seg_next(const SProb* sp, const Seg& g, int u, in
     n.pidx = P.pidx;
     n.row0 = P.row0;
     n.act = P.act;
+    n.tiled = P.tiled;
     n.chunks = P.chunks;
     n.dot_off = P.dot_off;
     n.ticket_off = P.ticket_off;
@@ -461,8 +465,9 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
             map = a.acts[P.map].kclass;
             row0 = a.acts[P.map].row0;
         }
+        const int pi = p_first + i;
         sp[i] = SProb{P.w, P.act_scale, P.row_sum, P.y, P.N, P.K, map, P.tile0, P.chunks, P.dot_off, P.ticket_off,
-                      p_first + i, row0, P.map};
+                      pi, row0, P.map, (int)((a.tiled[pi >> 5] >> (pi & 31)) & 1u)};
     }
     uint32_t* s_code = nullptr;
     TeamRows* s_rows = nullptr;
@@ -555,7 +560,9 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
         // --------------------------------------------------- weight producer
         // One TMA box per stage: 128 rows x 128 packed bytes of the tile, from
         // the problem's weight map (written by the quantization launch; rows
-        // past N and bytes past K/4 are zero-filled), into a 3-stage ring.
+        // past N and bytes past K/4 are zero-filled), into a 3-stage ring. On
+        // tiled weights the stage is one 16 KB block, already in the ring's
+        // layout: one bulk copy.
         if (lane == 0) {
             int ws = 0;
             uint32_t wphase = 0;
@@ -577,7 +584,13 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 for (int off = g.st_lo * kStageBytes; off < end; off += kStageBytes) {
                     if (!tc::mbar_wait_idle(&S.empty_w[ws], wphase ^ 1, abort_flag, kWaitLimitGv)) { fail(1024); ok = false; break; }
                     tc::mbar_arrive_expect_tx(&S.full_w[ws], kWStageBytes);
-                    tc::tma_load_2d(sW + (size_t)ws * kWStageBytes, map, off, g.n0, &S.full_w[ws]);
+                    if (g.tiled) {   // block (tile, stage) of the tiled weights
+                        const size_t blk = (size_t)(g.n0 / kTiledRows) * tiled_col_blocks(g.K) + off / kTiledRowBytes;
+                        tc::bulk_load(sW + (size_t)ws * kWStageBytes, g.w + blk * kTiledBlockBytes, kWStageBytes,
+                                      &S.full_w[ws]);
+                    } else {
+                        tc::tma_load_2d(sW + (size_t)ws * kWStageBytes, map, off, g.n0, &S.full_w[ws]);
+                    }
                     pending[ws] = true;
                     pending_phase[ws] = wphase;
                     if (++ws == kWStages) { ws = 0; wphase ^= 1; }
@@ -841,7 +854,8 @@ __global__ void __launch_bounds__(kThreadsGv, 2) k_i2s_gemv_tc(const __grid_cons
                 }
             }
             if (write && n < g.N) {
-                const float w_scale = *reinterpret_cast<const float*>(g.w + (size_t)g.N * (g.K / 4));
+                const float w_scale = *reinterpret_cast<const float*>(
+                    g.w + (g.tiled ? tiled_scale_offset(g.N, g.K) : (size_t)g.N * (g.K / 4)));
 #pragma unroll
                 for (int m = 0; m < Mp; ++m) {
                     if (m < a.M) {

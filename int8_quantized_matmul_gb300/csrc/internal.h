@@ -12,6 +12,21 @@ namespace i2s {
 
 constexpr int kMaxGroup = 256;   // same value as I2S_MAX_GROUP
 
+// Tiled I2_S weights (i2s_tile_weights): blocks of 128 rows x 128 bytes (512
+// positions), each the shared-memory image of one 128-byte-swizzled TMA tile
+// of the weights, row blocks padded to an even count (a CTA pair's 256 rows),
+// the I2_S trailer after the blocks.
+constexpr int kTiledRows = 128;
+constexpr int kTiledRowBytes = 128;
+constexpr int kTiledBlockBytes = kTiledRows * kTiledRowBytes;   // 16384
+__host__ __device__ __forceinline__ long long tiled_row_blocks(long long N) { return 2 * ((N + 255) / 256); }
+__host__ __device__ __forceinline__ long long tiled_col_blocks(long long K) { return (K + 511) / 512; }
+__host__ __device__ __forceinline__ size_t tiled_scale_offset(long long N, long long K) {
+    return (size_t)(tiled_row_blocks(N) * tiled_col_blocks(K)) * kTiledBlockBytes;
+}
+// Bit i of a launch's tiled mask: problem i's weights are in the tiled layout.
+constexpr int kTiledMaskWords = kMaxGroup / 32;
+
 // ---------------------------------------------------------------------------
 // Row quantizer. One warp quantizes one row of one activation matrix.
 // ---------------------------------------------------------------------------
@@ -58,6 +73,9 @@ struct QuantArgs {
 constexpr int kQuantWarpRowK = 1536;
 // Orders a.j (short rows first), sets n_short and short_ctas, and launches.
 cudaError_t launch_quant(QuantArgs& a, cudaStream_t s);
+// Writes the tiled layout of an I2_S payload (N x row_bytes, row_bytes a
+// multiple of 16) into tiled (tiled_scale_offset(N, K) bytes); no trailer.
+cudaError_t launch_i2s_tile(const uint8_t* w, int64_t N, int64_t K, uint8_t* tiled, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Prefill GEMM (M > 16) on tcgen05 (gemm_tc.cu).
@@ -97,6 +115,7 @@ struct TcArgs {
     int share_first;          // GEMV: relative unit shares of the first and second half of the
     int share_second;         //   grid (the first and second CTA placed on each SM)
     long long test_stall_cycles;   // GEMV, test only: > 0 makes the epilogue give up a wait nothing ends
+    uint32_t tiled[kTiledMaskWords];   // problems whose weights are in the tiled layout
     TcProb p[kMaxGroup];
 };
 
@@ -145,6 +164,7 @@ struct GvFusedArgs {
     uint32_t* ticket_base;      // split-K chunk counters, zeroed by the prologue
     long long cost_total;       // sum over activations of M * K
     int n_acts, count, M, BN, total_tiles, share_first, share_second;
+    uint32_t tiled[kTiledMaskWords];   // problems whose weights are in the tiled layout
     TcProb p[kMaxGroup];        // TcProb::map = activation index (its class and row0 in acts[])
 };
 cudaError_t launch_gemv_fused(const GvFusedArgs& a, int grid, cudaStream_t s);
@@ -157,7 +177,6 @@ static_assert(sizeof(QuantArgs) <= 32764, "QuantArgs exceeds the kernel paramete
 bool make_f16_operand_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows);
 // rows x row_bytes uint8 matrix, box {128 bytes, box_rows}, 128-byte swizzle
 bool make_u8_operand_map(CUtensorMap* map, const void* base, int rows, int row_bytes, int box_rows);
-bool make_code_map_template(CUtensorMap* map, const void* base);   // GEMM: packed codes, box 64 B x 128 rows
 cudaError_t launch_gemm_tc(const TcArgs& a, int grid, cudaStream_t s);
 int gemm_tc_max_pairs();   // CTA pairs of the GEMM that fit on the device at once
 cudaError_t launch_gemv_tc(const TcArgs& a, int grid, cudaStream_t s);

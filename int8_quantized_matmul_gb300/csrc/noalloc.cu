@@ -136,6 +136,7 @@ int i2s_mul_mat_noalloc(const void* w_i2s, int64_t N, int64_t K, const float* x,
     if (!make_u8_operand_map(&ta.maps[0], base + op_off, op_rows, (int)(K / 2), op_rows)) return I2S_E_CUDA;
     ta.wmaps = wmap;
     ta.test_stall_cycles = 0;
+    for (int w = 0; w < kTiledMaskWords; ++w) ta.tiled[w] = 0;   // I2_S bytes
     ta.dot_base = reinterpret_cast<int32_t*>(base + dot_off);
     ta.ticket_base = reinterpret_cast<uint32_t*>(base + ticket_off);
     const int chunks = (int)((K + kGemvChunkPositions - 1) / kGemvChunkPositions);

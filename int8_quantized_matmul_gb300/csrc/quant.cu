@@ -210,6 +210,40 @@ __global__ void __launch_bounds__(kQThreads) k_quant_rows_tc4(const __grid_const
 
 static_assert(kQuantWarpRowK / 16 <= 32 * kQ4Cache, "a short row fits one warp's registers");
 
+// Tiled I2_S weights: one thread per 16-byte piece of the output. Piece p of
+// row rr in block (bi, bj) holds bytes 128 bj + 16 (p ^ (rr % 8)) .. +15 of
+// payload row 128 bi + rr (the 128-byte swizzle of a TMA tile of 128 rows x
+// 128 bytes), or zeros past N or past the row's bytes.
+__global__ void __launch_bounds__(256) k_i2s_tile(const uint8_t* __restrict__ w, int64_t N, int row_bytes, int tk,
+                                                  int64_t pieces, uint4* __restrict__ out) {
+    constexpr int kPiecesPerRow = kTiledRowBytes / 16;
+    constexpr int kPiecesPerBlock = kTiledBlockBytes / 16;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < pieces; t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t blk = t / kPiecesPerBlock;
+        const int in = (int)(t - blk * kPiecesPerBlock);
+        const int rr = in / kPiecesPerRow, p = in % kPiecesPerRow;
+        const int64_t bi = blk / tk;
+        const int bj = (int)(blk - bi * tk);
+        const int64_t row = bi * kTiledRows + rr;
+        const int byte = bj * kTiledRowBytes + ((p ^ (rr & 7)) << 4);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < N && byte < row_bytes) v = __ldg(reinterpret_cast<const uint4*>(w + row * row_bytes + byte));
+        out[t] = v;
+    }
+}
+
+cudaError_t launch_i2s_tile(const uint8_t* w, int64_t N, int64_t K, uint8_t* tiled, cudaStream_t s) {
+    const int64_t pieces = (int64_t)(tiled_scale_offset(N, K) / 16);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (pieces + 255) / 256;
+    const int grid = (int)(want < 8LL * sms ? want : 8LL * sms);
+    k_i2s_tile<<<grid, 256, 0, s>>>(w, N, (int)(K / 4), (int)tiled_col_blocks(K), pieces, reinterpret_cast<uint4*>(tiled));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant(QuantArgs& a, cudaStream_t s) {
     if (a.layout == kQuantE2M1Tc) {
         // short rows first (stable), eight rows per CTA; then one CTA per long row

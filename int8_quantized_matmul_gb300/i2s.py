@@ -40,7 +40,7 @@ class i2s_config(ctypes.Structure):
 
 
 class i2s_problem(ctypes.Structure):
-    _fields_ = [("w_i2s", _p), ("N", _i64), ("K", _i64), ("x", _p), ("y", _p)]
+    _fields_ = [("w_i2s", _p), ("N", _i64), ("K", _i64), ("x", _p), ("y", _p), ("w_layout", ctypes.c_uint)]
 
 
 class w8a8_problem(ctypes.Structure):
@@ -53,6 +53,9 @@ _SIGS = {
     "i2s_device_supported": (_int, []),
     "i2s_nbytes": (_sz, [_i64, _i64]),
     "i2s_scale_offset": (_sz, [_i64, _i64]),
+    "i2s_tiled_nbytes": (_sz, [_i64, _i64]),
+    "i2s_tiled_scale_offset": (_sz, [_i64, _i64]),
+    "i2s_tile_weights": (_int, [_p, _i64, _i64, _p, _p]),
     "i8s_nbytes": (_sz, [_i64]),
     "i8s_scale_offset": (_sz, [_i64]),
     "i2s_pack_host": (_int, [_p, _i64, _i64, _f32, _p]),
@@ -227,10 +230,51 @@ def i2s_mul_mat_noalloc(w, N: int, K: int, x, y):
     return y
 
 
+LAYOUT_I2S = 0     # I2S_LAYOUT_I2S
+LAYOUT_TILED = 1   # I2S_LAYOUT_TILED
+
+
+class Tiled:
+    """I2_S weights in the tiled layout written by i2s_tile_weights: `data` is
+    a uint8 device tensor of i2s_tiled_nbytes(N, K) bytes. Give it as the
+    weight of a grouped problem, in place of the I2_S bytes."""
+
+    def __init__(self, data, N: int, K: int):
+        self.data, self.N, self.K = data, N, K
+
+    @property
+    def device(self):
+        return self.data.device
+
+
+def i2s_tiled_nbytes(N: int, K: int) -> int:
+    return int(_L.i2s_tiled_nbytes(N, K))
+
+
+def i2s_tiled_scale_offset(N: int, K: int) -> int:
+    return int(_L.i2s_tiled_scale_offset(N, K))
+
+
+def tile_weights(w, N: int, K: int, out=None) -> Tiled:
+    """The tiled layout of I2_S weights w (device), written once."""
+    if out is None:
+        out = _torch().empty(i2s_tiled_nbytes(N, K), dtype=_torch().uint8, device=w.device)
+    _check("i2s_tile_weights", _L.i2s_tile_weights(_dptr(w), N, K, _dptr(out), _stream()))
+    return Tiled(out, N, K)
+
+
+def _weight(w):
+    """(device pointer, I2S_LAYOUT_*) of a problem's weights."""
+    if isinstance(w, Tiled):
+        return _dptr(w.data), LAYOUT_TILED
+    return _dptr(w), LAYOUT_I2S
+
+
 def _problems(problems: Sequence):
     arr = (i2s_problem * len(problems))()
     for i, (w, N, K, x, y) in enumerate(problems):
-        arr[i] = i2s_problem(_dptr(w), N, K, _dptr(x), _dptr(y))
+        wp, layout = _weight(w)
+        arr[i] = i2s_problem(wp, N, K, _dptr(x), _dptr(y), layout)
     return arr
 
 
@@ -312,7 +356,8 @@ def _hptr(t) -> int:
 def _host_problems(problems: Sequence):
     arr = (i2s_problem * len(problems))()
     for i, (w, N, K, x, y) in enumerate(problems):
-        arr[i] = i2s_problem(_dptr(w), N, K, _hptr(x), _hptr(y))
+        wp, layout = _weight(w)
+        arr[i] = i2s_problem(wp, N, K, _hptr(x), _hptr(y), layout)
     return arr
 
 

@@ -267,3 +267,56 @@ def test_host_buffer_call_validation_and_copy_plan(i2s):
     # both mapped needs only the grouped workspace
     assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, grouped - 1, 1, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
     assert L.i2s_mul_mat_grouped_host_ex(merged, 3, M, ws, grouped - 1, 3, None) == E["I2S_E_WORKSPACE_TOO_SMALL"]
+
+
+def test_tiled_layout_sizes_and_validation(i2s):
+    # sizes against the header's formula; validation before any CUDA call
+    from tests import tiled_layout
+    L = i2s.lib
+    A = 1 << 20
+    vp = ctypes.c_void_p
+    E = {v: k for k, v in i2s.STATUS.items()}
+    for N, K in ((1, 128), (300, 1152), (256, 1536), (257, 1536), (1536, 8960), (151936, 1536)):
+        tn, tk = tiled_layout.blocks(N, K)
+        assert i2s.i2s_tiled_scale_offset(N, K) == tn * tk * 16384
+        assert i2s.i2s_tiled_nbytes(N, K) == tiled_layout.nbytes(N, K) >= i2s.i2s_nbytes(N, K)
+    for N, K in ((0, 128), (4, 100), (4, 0)):
+        assert i2s.i2s_tiled_nbytes(N, K) == 0 and i2s.i2s_tiled_scale_offset(N, K) == 0
+    assert L.i2s_tile_weights(None, 4, 128, vp(8 * A), None) == E["I2S_E_NULL_PTR"]
+    assert L.i2s_tile_weights(vp(A), 4, 100, vp(8 * A), None) == E["I2S_E_BAD_SHAPE"]
+    assert L.i2s_tile_weights(vp(A + 8), 4, 128, vp(8 * A), None) == E["I2S_E_MISALIGNED"]
+    assert L.i2s_tile_weights(vp(A), 4, 128, vp(8 * A + 8), None) == E["I2S_E_MISALIGNED"]
+    assert L.i2s_tile_weights(vp(A), 300, 1152, vp(A + 4096), None) == E["I2S_E_BAD_ARG"]   # overlap
+    # a w_layout other than I2S_LAYOUT_I2S / I2S_LAYOUT_TILED, in every grouped form
+    probs = (i2s.i2s_problem * 2)()
+    probs[0] = i2s.i2s_problem(A, 64, 1536, 2 * A, 3 * A, i2s.LAYOUT_TILED)
+    probs[1] = i2s.i2s_problem(A, 300, 1536, 2 * A, 4 * A, 2)
+    ws = vp(8 * A)
+    assert L.i2s_mul_mat_grouped(probs, 2, 4, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped(probs, 2, 64, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_fused(probs, 2, 4, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_host(probs, 2, 4, ws, 1 << 30, None) == E["I2S_E_BAD_ARG"]
+    assert L.i2s_mul_mat_grouped_workspace(probs, 2, 4) == 0
+    probs[1].w_layout = i2s.LAYOUT_TILED
+    assert L.i2s_mul_mat_grouped_workspace(probs, 2, 4) > 0
+
+
+def test_tiled_layout_restatement_by_enumeration():
+    # the numpy restatement against the header's sentence, byte by byte, on
+    # small shapes with ragged rows and row bytes
+    from tests import tiled_layout
+    for N, K in ((3, 128), (130, 640), (257, 1152)):
+        rb = K // 4
+        packed = np.random.default_rng(N + K).integers(0, 256, N * rb + 32, dtype=np.uint8)
+        t = tiled_layout.tile(packed, N, K)
+        tn, tk = tiled_layout.blocks(N, K)
+        assert t.size == tn * tk * 16384 + 32
+        want = np.zeros(tn * tk * 16384, np.uint8)
+        for n in range(N):
+            for b in range(rb):
+                i, rr = divmod(n, 128)
+                j, cb = divmod(b, 128)
+                c, off = divmod(cb, 16)
+                want[(i * tk + j) * 16384 + rr * 128 + (c ^ (rr % 8)) * 16 + off] = packed[n * rb + b]
+        np.testing.assert_array_equal(t[:-32], want)
+        np.testing.assert_array_equal(t[-32:], packed[N * rb:])
