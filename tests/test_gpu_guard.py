@@ -252,3 +252,26 @@ def test_guard_host_call(i2s, o, mapped):
     ws.check("workspace")
     assert i2s.read_status(ws.buf) == 0
     same_bits(yh.f32(M, N).numpy(), o.i2s_mul_mat(packed, N, K, xh.f32(M, K).numpy(), nth=8))
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (300, 1152), (257, 1920), (1536, 8960)])
+def test_guard_tile_weights_and_tiled_group(i2s, o, N, K):
+    # the tiling kernel and its trailer copy write exactly i2s_tiled_nbytes;
+    # the grouped GEMV and GEMM on the tiled copy write only their outputs
+    from tests import tiled_layout
+    packed = o.i2s_pack(synth.codes(N, K, seed=N + K), 0.04)
+    gt = Guarded(i2s.i2s_tiled_nbytes(N, K))
+    wt = i2s.tile_weights(dev(packed), N, K, out=gt.buf)
+    gt.check("i2s_tile_weights")
+    np.testing.assert_array_equal(gt.buf.cpu().numpy(), tiled_layout.tile(packed, N, K))
+    for M in (3, 40):
+        x = synth.normal_f32((M, K), seed=M + N)
+        gy = Guarded(M * N * 4)
+        y = gy.f32(M, N)
+        xd = dev(x)
+        gw = Guarded(i2s.i2s_mul_mat_grouped_workspace([(wt, N, K, xd, y)], M))
+        i2s.i2s_mul_mat_grouped([(wt, N, K, xd, y)], M, ws=gw.buf)
+        assert i2s.read_status(gw.buf) == 0
+        gy.check(f"tiled group y, M={M}")
+        gw.check(f"tiled group workspace, M={M}")
+        np.testing.assert_array_equal(y.cpu().numpy().view(np.uint32), o.i2s_mul_mat(packed, N, K, x, nth=8).view(np.uint32))
