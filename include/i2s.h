@@ -164,7 +164,8 @@ int i2s_quantize_act(const float* x, int64_t M, int64_t K, int8_t* q, float* act
  * y      device, M x N F32 output, 16-byte aligned.
  * ws     device workspace of at least i2s_mul_mat_workspace(M,N,K) bytes,
  *        256-byte aligned; holds the quantized rows, per-row scale and sum
- *        (the counterpart of the sidecar ggml keeps in params->wdata), the
+ *        (the counterpart of the sidecar the CPU mul_mat keeps in its work
+ *        buffer, [P2] Kernels, threading paragraph), the
  *        TMA descriptors of the weight matrix, the integer partial sums of a
  *        K-split launch and a status word. Not preserved between calls; calls
  *        sharing one ws must be ordered on one stream.
