@@ -4,7 +4,8 @@ The tiling kernel's bytes against the layout's numpy restatement, and the
 grouped matmul on tiled weights against the same call on the I2_S bytes and
 against the CPU oracle, bit for bit: the decode GEMV (M <= 16, split-K and
 ragged tiles), the prefill GEMM, groups that mix the two layouts, the fused
-decode launch, the host-buffer call, and the accumulator headroom case.
+decode launch, the host-buffer call (staged and mapped), the quantize and run
+phases with repeated runs, and the accumulator headroom case.
 """
 
 import numpy as np
@@ -146,3 +147,50 @@ def test_tiled_headroom_k8960(i2s, o, M):
     ws = i2s.i2s_mul_mat_grouped([(w, N, K, dev(x), y)], M)
     assert i2s.read_status(ws) == 0
     same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=8))
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_tiled_group_phases_repeated(i2s, o, M):
+    # the bench's form: one quantization, then the run phase several times,
+    # each leaving the split-K state at zero for the next
+    specs = GROUP
+    xs, packs, problems = {}, [], []
+    for i, (N, K, act) in enumerate(specs):
+        if act not in xs:
+            xs[act] = synth.normal_f32((M, K), seed=70 + act + M, outlier_p=0.01)
+        packed = weights(o, N, K, seed=90 + i)
+        packs.append(packed)
+        problems.append((i2s.tile_weights(dev(packed), N, K), N, K, act))
+    xd = {a: dev(x) for a, x in xs.items()}
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for N, _, _ in specs]
+    g = i2s.Group([(w, N, K, xd[act], y) for (w, N, K, act), y in zip(problems, ys)], M)
+    g.quantize()
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.run()
+        assert i2s.read_status(g.ws) == 0
+        for (N, K, act), y, packed in zip(specs, ys, packs):
+            same_bits(host(y), o.i2s_mul_mat(packed, N, K, xs[act], nth=8))
+
+
+@pytest.mark.parametrize("mapped", [True, "y"])
+def test_tiled_host_call_mapped(i2s, o, mapped):
+    # pinned host activations and outputs read and written in place by the kernels
+    M = 8
+    specs = GROUP[:4]
+    xs, packs, problems, ys = {}, [], [], []
+    for i, (N, K, act) in enumerate(specs):
+        if act not in xs:
+            xs[act] = torch.from_numpy(synth.normal_f32((M, K), seed=40 + act, outlier_p=0.01)).pin_memory()
+        packed = weights(o, N, K, seed=60 + i)
+        packs.append(packed)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+        ys.append(y)
+        problems.append((i2s.tile_weights(dev(packed), N, K), N, K, xs[act], y))
+    h = i2s.HostGroup(problems, M, mapped=mapped)
+    h()
+    torch.cuda.synchronize()
+    assert i2s.read_status(h.ws) == 0
+    for (N, K, act), y, packed in zip(specs, ys, packs):
+        same_bits(y.numpy(), o.i2s_mul_mat(packed, N, K, xs[act].numpy(), nth=8))
