@@ -196,6 +196,8 @@ typedef struct i2s_config {
                         (copies and MMAs in flight drained, TMEM freed) and
                         i2s_read_status reports I2S_E_DEVICE_TIMEOUT. The output is then
                         incomplete. 0 for normal use; negative is BAD_ARG. */
+    unsigned w_layout;   /* I2S_LAYOUT_I2S (0) or I2S_LAYOUT_TILED (w_i2s then holds the
+                        output of i2s_tile_weights); other values are BAD_ARG */
 } i2s_config;
 
 int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int64_t M, float* y,

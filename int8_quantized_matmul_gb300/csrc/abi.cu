@@ -241,15 +241,18 @@ int i2s_mul_mat_ex(const void* w_i2s, int64_t N, int64_t K, const float* x, int6
     if (!i2s_shape_ok(N, K, M)) return I2S_E_BAD_SHAPE;
     if (!aligned16(w_i2s) || !aligned16(x) || !aligned16(y) || !aligned256(ws)) return I2S_E_MISALIGNED;
     if (ws_bytes < i2s_mul_mat_workspace(M, N, K)) return I2S_E_WORKSPACE_TOO_SMALL;
-    int r = check_device();
-    if (r) return r;
-
+    // the configuration, checked on the host before any CUDA call
     const int path = config ? config->path : 0;
     if (path != 0 && path != 2 && path != 3) return I2S_E_BAD_ARG;
     if (path == 3 && M > 16) return I2S_E_BAD_ARG;
-    i2s_problem p{w_i2s, N, K, x, y, I2S_LAYOUT_I2S};
-    if (path == 2 || (path == 0 && M > 16)) return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
+    const unsigned layout = config ? config->w_layout : I2S_LAYOUT_I2S;
+    if (layout != I2S_LAYOUT_I2S && layout != I2S_LAYOUT_TILED) return I2S_E_BAD_ARG;
     if (config && config->test_stall_cycles < 0) return I2S_E_BAD_ARG;
+    int r = check_device();
+    if (r) return r;
+
+    i2s_problem p{w_i2s, N, K, x, y, layout};
+    if (path == 2 || (path == 0 && M > 16)) return run_gemm_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3);
     return run_gemv_tc(&p, 1, M, ws, config ? config->grid_ctas : 0, stream, 3,
                        config ? (long long)config->test_stall_cycles : 0);
 }

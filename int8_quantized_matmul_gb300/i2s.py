@@ -36,7 +36,7 @@ STATUS = {0: "I2S_OK", -1: "I2S_E_BAD_SHAPE", -2: "I2S_E_NULL_PTR", -3: "I2S_E_M
 
 
 class i2s_config(ctypes.Structure):
-    _fields_ = [("path", _int), ("grid_ctas", _int), ("test_stall_cycles", _i64)]
+    _fields_ = [("path", _int), ("grid_ctas", _int), ("test_stall_cycles", _i64), ("w_layout", ctypes.c_uint)]
 
 
 class i2s_problem(ctypes.Structure):
@@ -200,20 +200,21 @@ def i2s_mul_mat_workspace(M: int, N: int, K: int) -> int:
 
 
 def i2s_mul_mat(w, N: int, K: int, x, y=None, ws=None, path: int = 0, grid_ctas: int = 0):
-    """y (M x N F32) = I2_S weights w (N x K, device bytes) times x (M x K F32).
-    path / grid_ctas: the i2s_config overrides (0 = automatic)."""
+    """y (M x N F32) = I2_S weights w (N x K, device bytes, or their Tiled
+    layout) times x (M x K F32). path / grid_ctas: the i2s_config overrides
+    (0 = automatic)."""
     torch = _torch()
+    wp, layout = _weight(w)
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     if ws is None:
         ws = _ws(i2s_mul_mat_workspace(M, N, K), x.device)
-    if path or grid_ctas:
-        cfg = i2s_config(path, grid_ctas)
-        rc = _L.i2s_mul_mat_ex(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), ctypes.byref(cfg),
-                               _stream())
+    if path or grid_ctas or layout:
+        cfg = i2s_config(path, grid_ctas, 0, layout)
+        rc = _L.i2s_mul_mat_ex(wp, N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), ctypes.byref(cfg), _stream())
     else:
-        rc = _L.i2s_mul_mat(_dptr(w), N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), _stream())
+        rc = _L.i2s_mul_mat(wp, N, K, _dptr(x), M, _dptr(y), _dptr(ws), ws.numel(), _stream())
     _check("i2s_mul_mat", rc)
     return y
 

@@ -320,3 +320,20 @@ def test_tiled_layout_restatement_by_enumeration():
                 want[(i * tk + j) * 16384 + rr * 128 + (c ^ (rr % 8)) * 16 + off] = packed[n * rb + b]
         np.testing.assert_array_equal(t[:-32], want)
         np.testing.assert_array_equal(t[-32:], packed[N * rb:])
+
+
+def test_single_call_config_validation_needs_no_device(i2s):
+    # i2s_mul_mat_ex checks its configuration (path, weight layout, stall) on
+    # the host before any CUDA call
+    L = i2s.lib
+    A = 1 << 20
+    E = {v: k for k, v in i2s.STATUS.items()}
+    ws_need = i2s.i2s_mul_mat_workspace(4, 64, 128)
+
+    def call(cfg, M=4):
+        return L.i2s_mul_mat_ex(A, 64, 128, A, M, A, A, i2s.i2s_mul_mat_workspace(M, 64, 128), ctypes.byref(cfg), None)
+    assert call(i2s.i2s_config(1, 0)) == E["I2S_E_BAD_ARG"]                     # no such path
+    assert call(i2s.i2s_config(3, 0), M=17) == E["I2S_E_BAD_ARG"]               # the GEMV takes M <= 16
+    assert call(i2s.i2s_config(0, 0, -1)) == E["I2S_E_BAD_ARG"]                 # negative stall
+    assert call(i2s.i2s_config(0, 0, 0, 2)) == E["I2S_E_BAD_ARG"]               # no such weight layout
+    assert ws_need > 0

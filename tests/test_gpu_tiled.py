@@ -5,7 +5,8 @@ grouped matmul on tiled weights against the same call on the I2_S bytes and
 against the CPU oracle, bit for bit: the decode GEMV (M <= 16, split-K and
 ragged tiles), the prefill GEMM, groups that mix the two layouts, the fused
 decode launch, the host-buffer call (staged and mapped), the quantize and run
-phases with repeated runs, and the accumulator headroom case.
+phases with repeated runs, the single-matrix call, and the accumulator
+headroom case.
 """
 
 import numpy as np
@@ -194,3 +195,17 @@ def test_tiled_host_call_mapped(i2s, o, mapped):
     assert i2s.read_status(h.ws) == 0
     for (N, K, act), y, packed in zip(specs, ys, packs):
         same_bits(y.numpy(), o.i2s_mul_mat(packed, N, K, xs[act].numpy(), nth=8))
+
+
+@pytest.mark.parametrize("path,grid", [(0, 0), (3, 0), (2, 0), (3, 40)])
+@pytest.mark.parametrize("M", [1, 9, 16, 64])
+def test_tiled_single_call(i2s, o, path, grid, M):
+    # i2s_mul_mat_ex with I2S_LAYOUT_TILED in its config: automatic, GEMV and
+    # GEMM paths, and a GEMV grid smaller than the SMs
+    if path == 3 and M > 16:
+        pytest.skip("the GEMV takes M <= 16")
+    N, K = 900, 4608
+    packed = weights(o, N, K, seed=M + path)
+    x = synth.normal_f32((M, K), seed=M * 3 + path, outlier_p=0.01)
+    y = i2s.i2s_mul_mat(i2s.tile_weights(dev(packed), N, K), N, K, dev(x), path=path, grid_ctas=grid)
+    same_bits(host(y), o.i2s_mul_mat(packed, N, K, x, nth=8))
